@@ -1,0 +1,501 @@
+"""Float64 CPU oracle for the MoE layer's token dispatch and expert compute.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import or run
+anything in this package.  It shares no code with the CUDA library and never
+imports it; the GPU path never imports this.
+
+Sources.  Three MaxText pull-request pages describe the method:
+
+* "Support moe_dropless_fallback=layer on the ragged all-to-all MoE path"
+  (MaxText pull request 5920), sections "Why", "How", "Shortcomings", "Tests".
+  Cited below as [PR5920 <section>].
+* "Moe dynamic redundancy" (MaxText pull request 4760), review comments on
+  ``ra2a_dedup_and_route`` and the Zipf data generator.  Cited as
+  [PR4760 review <topic>].
+* "MoE ring-of-experts: TC Pallas ring all-gather for the combine backward +
+  x_sorted remat save" (MaxText pull request 4969), section "What".  Cited
+  as [PR4969 What].
+
+Where the pages leave a step open, the reading taken is stated at the step
+(marked READING) and listed in the design doc.  Every function is plain: Python
+loops where the order of things is the semantics, ``numpy.matmul`` for the
+dense products of the expert FFN, float64 throughout.
+
+Notation: T tokens, H hidden, E experts, k experts per token, F expert FFN
+width, S logical expert-parallel shards of E/S consecutive experts each.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Callable, Optional
+
+import numpy as np
+
+INT = np.int64
+
+
+# ---------------------------------------------------------------------------
+# Step 1: router top-k and combine weights.
+# [PR5920 How]: the overflow check is computed "from the router's top-k";
+# route() is the function that produces it.  The pages never say how the
+# combine weights are formed from the router scores.
+# READING: weights are the softmax over all E logits, read at the chosen
+# experts (not renormalised); with renorm=True they are the softmax over the
+# k chosen logits.  Ties in the top-k go to the lower expert index.  A logit
+# that is NaN or +-inf ranks as -inf and contributes exp(-inf) = 0.
+# ---------------------------------------------------------------------------
+def clean_logit(v: float) -> float:
+    """Non-finite logits rank as -inf (READING)."""
+    return v if math.isfinite(v) else -math.inf
+
+
+def topk_one_token(row, k: int):
+    """Top-k of one token's logits.
+
+    Descending logit; equal logits are ordered by ascending expert index, so
+    the order is total and the selected set is unique.
+    """
+    E = len(row)
+    keyed = [(-clean_logit(float(row[e])), e) for e in range(E)]
+    keyed.sort()
+    return [e for _, e in keyed[:k]]
+
+
+def softmax_f64(values):
+    """exp(v - max) / sum, float64, over finite entries; all -inf -> zeros."""
+    vals = [clean_logit(float(v)) for v in values]
+    finite = [v for v in vals if v != -math.inf]
+    if not finite:
+        return [0.0] * len(vals)
+    m = max(finite)
+    ex = [math.exp(v - m) if v != -math.inf else 0.0 for v in vals]
+    s = sum(ex)
+    return [v / s for v in ex]
+
+
+def route(logits: np.ndarray, k: int, renorm: bool = False):
+    """Router top-k: returns (topk_idx [T,k] int, topk_w [T,k] f64, nonfinite).
+
+    ``nonfinite`` is True when any logit was NaN or infinite (the GPU path
+    reports that as a status code; the ranking rule is the same).
+    """
+    logits = np.asarray(logits)
+    T, E = logits.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    idx = np.zeros((T, k), dtype=INT)
+    w = np.zeros((T, k), dtype=np.float64)
+    nonfinite = bool(not np.all(np.isfinite(logits)))
+    for t in range(T):
+        row = logits[t]
+        chosen = topk_one_token(row, k)
+        idx[t] = chosen
+        if renorm:
+            p = softmax_f64([row[e] for e in chosen])
+            w[t] = p
+        else:
+            p = softmax_f64(row)
+            w[t] = [p[e] for e in chosen]
+    return idx, w, nonfinite
+
+
+# ---------------------------------------------------------------------------
+# Step 2: counts.  Per-expert row counts are the grouped-GEMM group sizes
+# ([PR4760 review on get_gmm_for_local_experts]: group_sizes per expert);
+# per-shard receive counts sum them over each shard's expert range
+# (experts_per_rank consecutive experts per shard, [PR4760 review on
+# plan_expert_duplication]).
+# ---------------------------------------------------------------------------
+def expert_counts(topk_idx: np.ndarray, E: int) -> np.ndarray:
+    c = np.zeros(E, dtype=INT)
+    for e in np.asarray(topk_idx).reshape(-1):
+        c[int(e)] += 1
+    return c
+
+
+def exclusive_scan(v) -> np.ndarray:
+    out = np.zeros(len(v) + 1, dtype=INT)
+    run = 0
+    for i, x in enumerate(v):
+        out[i] = run
+        run += int(x)
+    out[len(v)] = run
+    return out
+
+
+def shard_counts(counts: np.ndarray, S: int) -> np.ndarray:
+    E = len(counts)
+    if E % S:
+        raise ValueError("E must be a multiple of S")
+    Es = E // S
+    r = np.zeros(S, dtype=INT)
+    for s in range(S):
+        for e in range(s * Es, (s + 1) * Es):
+            r[s] += int(counts[e])
+    return r
+
+
+# ---------------------------------------------------------------------------
+# Step 3: capacity and the overflow check.
+# [PR5920 Why]: with ragged_buffer_factor > 0 each shard's receive buffer is
+# capped at factor x balanced and rows past it are dropped; with -1 there is
+# no cap.  [PR5920 How]: the check asks whether any shard would receive more
+# than its buffer.  READING: the unit is routed rows (token, slot) because the
+# check works from the top-k; balanced B = T*k/S; C = floor(factor*T*k/S)
+# computed in double from the float32 factor, capped at T*k (no shard can
+# hold more rows than exist); factor <= 0 means uncapped.  The comparison is
+# strict: a shard overflows when r_s > C.
+# ---------------------------------------------------------------------------
+def capacity(T: int, k: int, S: int, factor: float) -> Optional[int]:
+    f = float(np.float32(factor))
+    if f <= 0.0:
+        return None
+    c = math.floor(f * T * k / S)
+    return min(c, T * k)
+
+
+def overflow_flag(r: np.ndarray, C: Optional[int]) -> bool:
+    if C is None:
+        return False
+    return any(int(x) > C for x in r)
+
+
+def required_factor(r: np.ndarray, T: int, k: int) -> float:
+    """max_s r_s / balanced: the factor that would have avoided overflow
+    (the quantity log_required_ragged_buffer_factor reports, [PR5920
+    Shortcomings])."""
+    S = len(r)
+    if T * k == 0:
+        return 0.0
+    return max(int(x) for x in r) * S / (T * k)
+
+
+# ---------------------------------------------------------------------------
+# Step 4: expert-sorted permute with capped drop and per-shard dedup.
+# The routed rows are sorted by expert for the grouped GEMM ([PR4969 What]:
+# x_sorted is the expert-sorted MoE input).  READING: the order is stable by
+# (expert, token).  Capped drop [PR5920 Why] "silently dropped": READING: the
+# rows of one shard keep their (expert, token) order and a row is dropped iff
+# its rank inside its shard is >= C.  Dedup [PR4760 review on
+# ra2a_dedup_and_route]: each token is sent once per shard and expanded to its
+# per-expert rows by expand_indices; the review requires that nothing be
+# truncated.  READING: U_s is the ascending set of tokens with at least one
+# KEPT row in shard s.
+# ---------------------------------------------------------------------------
+@dataclass
+class Permutation:
+    sorted_token: np.ndarray      # [R_kept] token of each kept sorted row
+    sorted_slot: np.ndarray       # [R_kept] slot j of each kept sorted row
+    row_of: np.ndarray            # [T,k] sorted row of (t, j), -1 if dropped
+    group_offsets: np.ndarray     # [E+1] kept rows per expert, scanned
+    uniq_offsets: np.ndarray      # [S+1] scanned |U_s|
+    uniq_tokens: np.ndarray       # [sum |U_s|] U_0 ++ U_1 ++ ...
+    expand_idx: np.ndarray        # [R_kept] row -> position in uniq_tokens
+    n_dropped: int
+    dropless_offsets: np.ndarray  # [E+1] scan of all counts (before drops)
+
+
+def permute_indices(topk_idx: np.ndarray, E: int, S: int,
+                    C: Optional[int]) -> Permutation:
+    topk_idx = np.asarray(topk_idx)
+    T, k = topk_idx.shape
+    Es = E // S
+    # every routed row with its sort key (expert, token); a token never picks
+    # one expert twice, so the key is unique
+    rows = []
+    for t in range(T):
+        for j in range(k):
+            rows.append((int(topk_idx[t, j]), t, j))
+    rows.sort()
+    counts = expert_counts(topk_idx, E)
+    dropless_offsets = exclusive_scan(counts)
+
+    kept = []
+    rank_in_shard = [0] * S
+    for (e, t, j) in rows:
+        s = e // Es
+        if C is None or rank_in_shard[s] < C:
+            kept.append((e, t, j))
+        rank_in_shard[s] += 1
+    n_dropped = len(rows) - len(kept)
+
+    kept_counts = np.zeros(E, dtype=INT)
+    row_of = -np.ones((T, k), dtype=INT)
+    sorted_token = np.zeros(len(kept), dtype=INT)
+    sorted_slot = np.zeros(len(kept), dtype=INT)
+    for r, (e, t, j) in enumerate(kept):
+        kept_counts[e] += 1
+        row_of[t, j] = r
+        sorted_token[r] = t
+        sorted_slot[r] = j
+    group_offsets = exclusive_scan(kept_counts)
+
+    uniq_sets = [set() for _ in range(S)]
+    for (e, t, j) in kept:
+        uniq_sets[e // Es].add(t)
+    uniq_lists = [sorted(u) for u in uniq_sets]
+    uniq_offsets = exclusive_scan([len(u) for u in uniq_lists])
+    uniq_tokens = np.array([t for u in uniq_lists for t in u], dtype=INT)
+    pos_in_shard = [{t: i for i, t in enumerate(u)} for u in uniq_lists]
+    expand_idx = np.zeros(len(kept), dtype=INT)
+    for r, (e, t, j) in enumerate(kept):
+        s = e // Es
+        expand_idx[r] = uniq_offsets[s] + pos_in_shard[s][t]
+    return Permutation(sorted_token, sorted_slot, row_of, group_offsets,
+                       uniq_offsets, uniq_tokens, expand_idx, n_dropped,
+                       dropless_offsets)
+
+
+def gather_rows(x: np.ndarray, sorted_token: np.ndarray) -> np.ndarray:
+    """x_sorted[r] = x[sorted_token[r]]."""
+    out = np.zeros((len(sorted_token), x.shape[1]), dtype=np.float64)
+    for r, t in enumerate(sorted_token):
+        out[r] = x[int(t)]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Step 5: expert FFN.  The pages name the expert weights (w0 of shape
+# [E, H, H_ffn], [PR4760 review on the dynamic weight manager]) and a grouped
+# matmul over experts with ragged group sizes (megablox / gmm); the SwiGLU
+# form is the one the workloads fix: h = silu(x Wg) * (x Wu), y = h Wd with
+# silu(z) = z / (1 + exp(-z)).  Layout READING: Wg, Wu are [E, H, F]; Wd is
+# [E, F, H].  Float64, no intermediate rounding.
+# ---------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+ExpertWeights = Callable[[int], tuple]
+
+
+def dense_weights(w_gate, w_up, w_down) -> ExpertWeights:
+    """Accessor over in-memory [E,H,F]/[E,H,F]/[E,F,H] arrays."""
+    def get(e):
+        return (np.asarray(w_gate[e], dtype=np.float64),
+                np.asarray(w_up[e], dtype=np.float64),
+                np.asarray(w_down[e], dtype=np.float64))
+    return get
+
+
+def expert_ffn(x_rows: np.ndarray, wg, wu, wd):
+    """SwiGLU FFN of one expert over a block of rows.
+    Returns (h [rows,F], y [rows,H])."""
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    g = np.matmul(x_rows, wg)
+    u = np.matmul(x_rows, wu)
+    h = silu(g) * u
+    return h, np.matmul(h, wd)
+
+
+def grouped_ffn(x_sorted: np.ndarray, group_offsets: np.ndarray,
+                weights: ExpertWeights):
+    """Grouped GEMM over experts: rows [off[e], off[e+1]) use expert e.
+    Returns (h [R,F], y_sorted [R,H])."""
+    E = len(group_offsets) - 1
+    R = int(group_offsets[E])
+    h_all = None
+    y_all = np.zeros((R, x_sorted.shape[1]), dtype=np.float64)
+    for e in range(E):
+        a, b = int(group_offsets[e]), int(group_offsets[e + 1])
+        if a == b:
+            continue
+        wg, wu, wd = weights(e)
+        h, y = expert_ffn(x_sorted[a:b], wg, wu, wd)
+        if h_all is None:
+            h_all = np.zeros((R, h.shape[1]), dtype=np.float64)
+        h_all[a:b] = h
+        y_all[a:b] = y
+    return h_all, y_all
+
+
+# ---------------------------------------------------------------------------
+# Step 6: weighted combine (unpermute).  Each token's output is the sum over
+# its k slots of weight x expert output ([PR4969 What]: the combine is a
+# reduce over expert outputs, a psum_scatter in the ring variant).  A dropped
+# row contributes nothing.  Summed in slot order j = 0..k-1.
+# ---------------------------------------------------------------------------
+def combine(y_sorted: np.ndarray, row_of: np.ndarray, topk_w: np.ndarray,
+            H: int) -> np.ndarray:
+    T, k = row_of.shape
+    y = np.zeros((T, H), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            r = int(row_of[t, j])
+            if r >= 0:
+                y[t] += float(topk_w[t, j]) * y_sorted[r]
+    return y
+
+
+# ---------------------------------------------------------------------------
+# Step 7: the chunked dropless fallback.
+# [PR5920 How]: on overflow, the layer runs over n sequence chunks, each with
+# the worst-case (force_dropless) buffer, and n is chosen so that this buffer
+# is no larger than the capped one.  [PR5920 Shortcomings]: about n x slower,
+# 8x for EP16 at factor 2.  READING: one source on one GPU can put at most
+# min(k, E/S) rows per token into one shard, so a chunk of c tokens has a
+# worst case of c*min(k, E/S) rows; the chunk is the largest c with
+# c*min(k, E/S) <= C (at least 1 token) and n = ceil(T / c).  An explicit
+# n_chunks gives chunks of ceil(T/n) tokens.  Chunks are contiguous token
+# ranges; the last may be shorter.
+# ---------------------------------------------------------------------------
+def chunk_plan(T: int, k: int, E: int, S: int, C: Optional[int],
+               n_chunks: int = 0):
+    """Returns the list of (t0, t1) token ranges of the chunked fallback."""
+    if T == 0:
+        return []
+    if n_chunks > 0:
+        c = -(-T // n_chunks)
+    elif C is None:
+        c = T
+    else:
+        worst_per_token = min(k, E // S)
+        c = max(1, C // worst_per_token)
+    return [(t0, min(T, t0 + c)) for t0 in range(0, T, c)]
+
+
+# ---------------------------------------------------------------------------
+# The layer.
+# ---------------------------------------------------------------------------
+@dataclass
+class MoEConfig:
+    T: int
+    H: int
+    E: int
+    k: int
+    F: int
+    S: int
+    ragged_buffer_factor: float = 2.0
+    n_chunks: int = 0
+    renorm: bool = False
+
+
+@dataclass
+class LayerResult:
+    y: np.ndarray
+    topk_idx: np.ndarray
+    topk_w: np.ndarray
+    counts: np.ndarray
+    shard: np.ndarray
+    C: Optional[int]
+    overflow: bool
+    required_factor: float
+    perm: Optional[Permutation] = None
+    x_sorted: Optional[np.ndarray] = None
+    h: Optional[np.ndarray] = None
+    y_sorted: Optional[np.ndarray] = None
+    chunks: list = field(default_factory=list)
+
+
+def layer_pass(cfg: MoEConfig, x, logits, weights: ExpertWeights,
+               C: Optional[int], topk=None) -> LayerResult:
+    """One pass: route -> counts -> permute (cap C) -> FFN -> combine."""
+    x = np.asarray(x, dtype=np.float64)
+    if topk is None:
+        idx, w, _ = route(logits, cfg.k, cfg.renorm)
+    else:
+        idx, w = topk
+    counts = expert_counts(idx, cfg.E)
+    shard = shard_counts(counts, cfg.S)
+    T = x.shape[0]
+    perm = permute_indices(idx, cfg.E, cfg.S, C)
+    xs = gather_rows(x, perm.sorted_token)
+    h, ys = grouped_ffn(xs, perm.group_offsets, weights)
+    y = combine(ys, perm.row_of, w, cfg.H)
+    return LayerResult(y, idx, w, counts, shard, C, overflow_flag(shard, C),
+                       required_factor(shard, T, cfg.k), perm, xs, h, ys)
+
+
+def layer_capped(cfg, x, logits, weights) -> LayerResult:
+    """The capped ragged path alone (no fallback): rows past C are dropped."""
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    return layer_pass(cfg, x, logits, weights, C)
+
+
+def layer_dropless(cfg, x, logits, weights) -> LayerResult:
+    """The uncapped (force_dropless) path."""
+    return layer_pass(cfg, x, logits, weights, None)
+
+
+def layer_dropless_chunked(cfg, x, logits, weights,
+                           n_chunks: Optional[int] = None) -> LayerResult:
+    """The chunked dropless fallback: every chunk runs uncapped."""
+    x = np.asarray(x, dtype=np.float64)
+    logits = np.asarray(logits)
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    plan = chunk_plan(cfg.T, cfg.k, cfg.E, cfg.S, C,
+                      cfg.n_chunks if n_chunks is None else n_chunks)
+    y = np.zeros((cfg.T, cfg.H), dtype=np.float64)
+    idx = np.zeros((cfg.T, cfg.k), dtype=INT)
+    w = np.zeros((cfg.T, cfg.k), dtype=np.float64)
+    parts = []
+    for (t0, t1) in plan:
+        sub = MoEConfig(t1 - t0, cfg.H, cfg.E, cfg.k, cfg.F, cfg.S,
+                        -1.0, 0, cfg.renorm)
+        res = layer_pass(sub, x[t0:t1], logits[t0:t1], weights, None)
+        y[t0:t1] = res.y
+        idx[t0:t1] = res.topk_idx
+        w[t0:t1] = res.topk_w
+        parts.append(res)
+    counts = expert_counts(idx, cfg.E)
+    shard = shard_counts(counts, cfg.S)
+    return LayerResult(y, idx, w, counts, shard, C, overflow_flag(shard, C),
+                       required_factor(shard, cfg.T, cfg.k), chunks=parts)
+
+
+def layer(cfg, x, logits, weights) -> LayerResult:
+    """moe_dropless_fallback=layer [PR5920 How]: check, then the capped path
+    when no shard overflows, else the chunked dropless fallback.  The flag is
+    global: one overflowing shard sends the whole layer to the fallback
+    [PR5920 Tests]."""
+    idx, w, _ = route(logits, cfg.k, cfg.renorm)
+    counts = expert_counts(idx, cfg.E)
+    shard = shard_counts(counts, cfg.S)
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    if overflow_flag(shard, C):
+        res = layer_dropless_chunked(cfg, x, logits, weights)
+        res.overflow = True
+        return res
+    return layer_pass(cfg, x, logits, weights, C, topk=(idx, w))
+
+
+# ---------------------------------------------------------------------------
+# Per-token output for large layers: one token's output depends only on its
+# own row, its routing and the weights of its k experts, so sampled tokens of
+# a full-size layer can be checked one by one (dropless semantics).
+# ---------------------------------------------------------------------------
+def token_outputs(x_rows: np.ndarray, idx_rows: np.ndarray,
+                  w_rows: np.ndarray, weights: ExpertWeights,
+                  keep: Optional[np.ndarray] = None) -> np.ndarray:
+    """y for a few tokens: sum_j w_j FFN_{e_j}(x).  ``keep[t, j]`` False
+    skips a dropped slot.  Experts are visited in ascending order so each
+    expert's weights are fetched once."""
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    n, k = idx_rows.shape
+    out = np.zeros_like(x_rows)
+    by_expert = {}
+    for i in range(n):
+        for j in range(k):
+            if keep is None or keep[i, j]:
+                by_expert.setdefault(int(idx_rows[i, j]), []).append((i, j))
+    for e in sorted(by_expert):
+        wg, wu, wd = weights(e)
+        for (i, j) in by_expert[e]:
+            _, y = expert_ffn(x_rows[i:i + 1], wg, wu, wd)
+            out[i] += float(w_rows[i, j]) * y[0]
+    return out
+
+
+def normwise_error(got: np.ndarray, ref: np.ndarray) -> float:
+    """max_i |g_i - r_i| / max_i |r_i| (the tolerance measure used by the
+    parity tests; 0 when both are all zero)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den

@@ -1,0 +1,457 @@
+"""Pins for the float64 oracle: checks against what the MaxText pages and the
+mathematics fix, never against a retyped copy of the oracle's own formulas.
+
+Each ``pin_*`` function raises AssertionError on a mismatch.  They are run
+directly by test_oracle_pins.py, and again by test_oracle_mutations.py against
+oracles with a planted mistake, to show that each plausible mistake is caught.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+
+from oracle import moe_ref as ref
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _tie_heavy_logits(rng, T, E, levels=3):
+    """Logits drawn from a handful of values so that ties are common."""
+    return rng.integers(0, levels, size=(T, E)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# top-k: the selected set is the unique k-subset that dominates its
+# complement under (larger logit, then lower index); found by enumeration.
+# --------------------------------------------------------------------------
+def _dominates(l, i, j):
+    return l[i] > l[j] or (l[i] == l[j] and i < j)
+
+
+def pin_topk_bruteforce():
+    rng = _rng(1)
+    for E in (3, 5, 6):
+        L = _tie_heavy_logits(rng, 12, E)
+        for k in range(1, E + 1):
+            idx, _, _ = ref.route(L, k)
+            for t in range(L.shape[0]):
+                l = [float(v) for v in L[t]]
+                valid = []
+                for sub in itertools.combinations(range(E), k):
+                    rest = [j for j in range(E) if j not in sub]
+                    if all(_dominates(l, i, j) for i in sub for j in rest):
+                        valid.append(set(sub))
+                assert len(valid) == 1
+                assert set(int(v) for v in idx[t]) == valid[0]
+                # rank order: each pick dominates the next
+                for a, b in zip(idx[t][:-1], idx[t][1:]):
+                    assert _dominates(l, int(a), int(b))
+
+
+def pin_topk_hand_ties():
+    # all equal -> the k lowest indices, in order
+    idx, _, _ = ref.route(np.zeros((1, 6), np.float32), 3)
+    assert idx[0].tolist() == [0, 1, 2]
+    # equal maxima at 4 and 1 -> 1 before 4, then the 0.5 at index 5
+    L = np.array([[0.0, 2.0, -1.0, 0.0, 2.0, 0.5]], np.float32)
+    idx, _, _ = ref.route(L, 3)
+    assert idx[0].tolist() == [1, 4, 5]
+    # NaN and +inf rank as -inf, after every finite logit
+    L = np.array([[np.nan, 1.0, np.inf, -5.0]], np.float32)
+    idx, w, nf = ref.route(L, 3)
+    assert nf
+    assert idx[0].tolist() == [1, 3, 0]
+    # the softmax ignores the non-finite entries: two finite logits 1, -5
+    p1 = 1.0 / (1.0 + math.exp(-6.0))
+    assert abs(w[0, 0] - p1) < 1e-15 and abs(w[0, 1] - (1 - p1)) < 1e-15
+    assert w[0, 2] == 0.0
+    # no finite logit at all -> lowest indices, zero weights
+    idx, w, _ = ref.route(np.full((1, 4), np.nan, np.float32), 2)
+    assert idx[0].tolist() == [0, 1] and np.all(w == 0)
+
+
+def pin_softmax_weights():
+    rng = _rng(2)
+    # equal logits -> 1/E; with renorm -> 1/k
+    _, w, _ = ref.route(np.full((2, 8), 0.7, np.float32), 3)
+    assert np.allclose(w, 1.0 / 8, rtol=0, atol=1e-15)
+    _, w, _ = ref.route(np.full((2, 8), 0.7, np.float32), 3, renorm=True)
+    assert np.allclose(w, 1.0 / 3, rtol=0, atol=1e-15)
+    # two experts: the larger gets the logistic of the gap
+    for d in (0.0, 0.3, 2.0, 9.0):
+        L = np.array([[0.25, 0.25 + d]], np.float32)
+        _, w, _ = ref.route(L, 1)
+        gap = float(np.float32(0.25 + d)) - 0.25
+        assert abs(w[0, 0] - 1.0 / (1.0 + math.exp(-gap))) < 1e-14
+    # against scipy's softmax on random rows
+    L = rng.standard_normal((20, 16)).astype(np.float32) * 3
+    idx, w, _ = ref.route(L, 4)
+    p = scipy.special.softmax(L.astype(np.float64), axis=1)
+    assert np.allclose(w, np.take_along_axis(p, idx, 1), rtol=1e-13, atol=0)
+    idx, w, _ = ref.route(L, 4, renorm=True)
+    sel = np.take_along_axis(L.astype(np.float64), idx, 1)
+    assert np.allclose(w, scipy.special.softmax(sel, axis=1), rtol=1e-13)
+    assert np.allclose(w.sum(1), 1.0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# counts
+# --------------------------------------------------------------------------
+def pin_counts():
+    rng = _rng(3)
+    for (T, E, k, S) in ((64, 8, 2, 2), (100, 16, 3, 4), (7, 4, 4, 4)):
+        L = rng.standard_normal((T, E)).astype(np.float32)
+        idx, _, _ = ref.route(L, k)
+        c = ref.expert_counts(idx, E)
+        assert int(c.sum()) == T * k
+        assert np.array_equal(c, np.bincount(idx.ravel(), minlength=E))
+        r = ref.shard_counts(c, S)
+        assert int(r.sum()) == T * k
+        assert np.array_equal(r, c.reshape(S, E // S).sum(1))
+        off = ref.exclusive_scan(c)
+        assert np.array_equal(off, np.concatenate([[0], np.cumsum(c)]))
+
+
+# --------------------------------------------------------------------------
+# capacity and the overflow flag
+# --------------------------------------------------------------------------
+def pin_capacity_closed_forms():
+    # factor x balanced, balanced = T*k/S rows
+    assert ref.capacity(4096, 2, 4, 2.0) == 4096
+    assert ref.capacity(8192, 8, 8, 2.0) == 16384
+    assert ref.capacity(8192, 1, 16, 2.0) == 1024
+    # capped at T*k: a shard cannot receive more rows than exist
+    assert ref.capacity(256, 2, 2, 2.0) == 512
+    # float32 factor 0.1 is slightly above 0.1: 25.6000003 -> 25
+    assert ref.capacity(256, 2, 2, 0.1) == 25
+    assert ref.capacity(10, 3, 4, 1.0) == 7          # floor(7.5)
+    assert ref.capacity(8, 1, 8, 1.0) == 1
+    # no cap for factor <= 0 ("-1" in the pages)
+    assert ref.capacity(256, 2, 2, -1.0) is None
+    assert ref.capacity(256, 2, 2, 0.0) is None
+
+
+def _idx_with_shard_loads(loads, k, E, S):
+    """A routing whose shard receive counts are exactly ``loads``: tokens
+    take k distinct experts inside one shard (needs k <= E/S)."""
+    Es = E // S
+    rows = []
+    for s, n in enumerate(loads):
+        assert n % k == 0
+        for _ in range(n // k):
+            rows.append([s * Es + j for j in range(k)])
+    return np.array(rows, dtype=np.int64)
+
+
+def pin_overflow_flag():
+    E, S, k = 8, 4, 2
+    # shard loads (rows) chosen by hand; T = sum/k
+    for loads in ([4, 4, 4, 4], [10, 2, 2, 2], [2, 2, 2, 10], [0, 0, 0, 16],
+                  [6, 6, 2, 2]):
+        idx = _idx_with_shard_loads(loads, k, E, S)
+        T = idx.shape[0]
+        r = ref.shard_counts(ref.expert_counts(idx, E), S)
+        assert r.tolist() == loads
+        for factor in (0.1, 0.5, 1.0, 1.5, 2.0, 4.0, -1.0):
+            C = ref.capacity(T, k, S, factor)
+            expect = C is not None and max(loads) > C
+            assert ref.overflow_flag(r, C) == expect
+    # strictness: a shard holding exactly C rows does not overflow
+    idx = _idx_with_shard_loads([8, 4, 2, 2], k, E, S)       # T=8, B=4
+    r = ref.shard_counts(ref.expert_counts(idx, E), S)
+    assert ref.capacity(8, k, S, 2.0) == 8
+    assert not ref.overflow_flag(r, 8)
+    assert ref.overflow_flag(r, 7)
+    # one asymmetric hot shard (the last) sets the global flag
+    idx = _idx_with_shard_loads([2, 2, 2, 10], k, E, S)
+    r = ref.shard_counts(ref.expert_counts(idx, E), S)
+    assert ref.overflow_flag(r, ref.capacity(8, k, S, 2.0))
+    # required factor: balanced -> 1, all in one shard -> S
+    idx = _idx_with_shard_loads([4, 4, 4, 4], k, E, S)
+    r = ref.shard_counts(ref.expert_counts(idx, E), S)
+    assert ref.required_factor(r, 8, k) == 1.0
+    idx = _idx_with_shard_loads([0, 16, 0, 0], k, E, S)
+    r = ref.shard_counts(ref.expert_counts(idx, E), S)
+    assert ref.required_factor(r, 8, k) == 4.0
+
+
+def pin_worst_case_buffer():
+    with open(os.path.join(GOLDEN, "worst_case_buffer.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        T, k, E, S = c["T"], c["k"], c["E"], c["S"]
+        Es = E // S
+        # adversarial routing: every token's picks inside shard 0
+        idx = np.array([[j for j in range(min(k, Es))]] * T, dtype=np.int64)
+        if k > Es:
+            return
+        r = ref.shard_counts(ref.expert_counts(idx, E), S)
+        assert int(r[0]) == c["worst_rows"]
+        assert T * k // S == c["balanced_rows"]
+        assert ref.required_factor(r, T, k) == c["ratio"]
+
+
+# --------------------------------------------------------------------------
+# the permutation
+# --------------------------------------------------------------------------
+def pin_permutation_dropless():
+    rng = _rng(4)
+    for (T, E, k, S) in ((50, 8, 2, 2), (33, 16, 4, 4), (5, 4, 4, 2)):
+        L = _tie_heavy_logits(rng, T, E, levels=5)
+        idx, _, _ = ref.route(L, k)
+        p = ref.permute_indices(idx, E, S, None)
+        R = T * k
+        assert p.n_dropped == 0 and len(p.sorted_token) == R
+        # bijection onto all (t, j)
+        pairs = sorted(zip(p.sorted_token.tolist(), p.sorted_slot.tolist()))
+        assert pairs == [(t, j) for t in range(T) for j in range(k)]
+        # row_of is the inverse
+        for r in range(R):
+            assert p.row_of[p.sorted_token[r], p.sorted_slot[r]] == r
+        # order: numpy's stable lexsort by (expert, token)
+        flat_e = idx.ravel()
+        flat_t = np.repeat(np.arange(T), k)
+        order = np.lexsort((flat_t, flat_e))
+        assert np.array_equal(p.sorted_token, flat_t[order])
+        assert np.array_equal(idx[p.sorted_token, p.sorted_slot],
+                              flat_e[order])
+        assert np.array_equal(p.group_offsets, p.dropless_offsets)
+        assert np.array_equal(
+            np.diff(p.group_offsets), np.bincount(flat_e, minlength=E))
+
+
+def pin_permutation_capped():
+    rng = _rng(5)
+    for (T, E, k, S, factor) in ((64, 8, 2, 2, 0.6), (40, 16, 3, 4, 0.5),
+                                 (64, 8, 2, 4, 1.0), (30, 8, 1, 2, 0.1)):
+        L = rng.standard_normal((T, E)).astype(np.float32)
+        L[:, : E // S] += 1.5            # make shard 0 hot
+        idx, _, _ = ref.route(L, k)
+        C = ref.capacity(T, k, S, factor)
+        p = ref.permute_indices(idx, E, S, C)
+        full = ref.permute_indices(idx, E, S, None)
+        r = ref.shard_counts(ref.expert_counts(idx, E), S)
+        assert p.n_dropped == int(sum(max(0, int(x) - C) for x in r))
+        Es = E // S
+        kept_rows = set(zip(p.sorted_token.tolist(), p.sorted_slot.tolist()))
+        for s in range(S):
+            # dropless rows of shard s, in order; the kept ones are its
+            # first C, and they keep their relative order
+            seg = [(int(full.sorted_token[q]), int(full.sorted_slot[q]))
+                   for q in range(full.group_offsets[s * Es],
+                                  full.group_offsets[(s + 1) * Es])]
+            want = seg[:C]
+            got = [(int(p.sorted_token[q]), int(p.sorted_slot[q]))
+                   for q in range(p.group_offsets[s * Es],
+                                  p.group_offsets[(s + 1) * Es])]
+            assert got == want
+            for pair in seg[C:]:
+                assert pair not in kept_rows
+                assert p.row_of[pair] == -1
+        assert int((p.row_of >= 0).sum()) == T * k - p.n_dropped
+
+
+def pin_dedup():
+    rng = _rng(6)
+    for (T, E, k, S, factor) in ((60, 8, 3, 2, -1.0), (48, 16, 4, 4, 0.5),
+                                 (20, 8, 1, 4, -1.0)):
+        L = rng.standard_normal((T, E)).astype(np.float32)
+        L[:, :2] += 1.0
+        idx, _, _ = ref.route(L, k)
+        C = ref.capacity(T, k, S, factor)
+        p = ref.permute_indices(idx, E, S, C)
+        Es = E // S
+        for s in range(S):
+            want = set()
+            for q in range(p.group_offsets[s * Es],
+                           p.group_offsets[(s + 1) * Es]):
+                want.add(int(p.sorted_token[q]))
+            seg = p.uniq_tokens[p.uniq_offsets[s]:p.uniq_offsets[s + 1]]
+            assert sorted(want) == seg.tolist()   # ascending, no truncation
+        x = rng.standard_normal((T, 5))
+        xs = ref.gather_rows(x, p.sorted_token)
+        assert np.array_equal(xs, x[p.uniq_tokens[p.expand_idx]])
+        if k == 1:
+            assert len(p.uniq_tokens) == len(p.sorted_token)
+    # adversarial: every pick in shard 0 -> each token sent exactly once
+    T, E, k, S = 16, 8, 3, 2
+    idx = np.array([[0, 1, 2]] * T)
+    p = ref.permute_indices(idx, E, S, None)
+    assert len(p.uniq_tokens) == T
+    assert p.uniq_offsets.tolist() == [0, T, T]
+
+
+# --------------------------------------------------------------------------
+# the FFN and the combine
+# --------------------------------------------------------------------------
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def pin_ffn_closed_form():
+    # H=4, F=2 by hand: x.Wg = (1, 2), x.Wu = (2, 1),
+    # h = (2 silu(1), silu(2)); Wd puts h0 on output 0 and h1 on output 3
+    x = np.array([[1.0, 2.0, 0.0, -1.0]])
+    wg = np.array([[1, 0], [0, 1], [0, 0], [0, 0]], np.float64)
+    wu = np.array([[0, 1], [1, 0], [7, 7], [0, 0]], np.float64)
+    wd = np.array([[1, 0, 0, 0], [0, 0, 0, 1]], np.float64)
+    h, y = ref.expert_ffn(x, wg, wu, wd)
+    s1 = 1.0 / (1.0 + math.exp(-1.0))
+    s2 = 2.0 / (1.0 + math.exp(-2.0))
+    assert abs(h[0, 0] - 2 * s1) < 1e-15 and abs(h[0, 1] - s2) < 1e-15
+    assert abs(y[0, 0] - 2 * s1) < 1e-15 and abs(y[0, 3] - s2) < 1e-15
+    assert y[0, 1] == 0 and y[0, 2] == 0
+    # silu at a few points: 0, odd part, large |z|
+    for z in (0.0, -3.0, 3.0, 30.0, -30.0):
+        assert abs(ref.silu(np.array([z]))[0] - _silu(z)) < 1e-15
+    assert abs(ref.silu(np.array([3.0]))[0] - ref.silu(np.array([-3.0]))[0]
+               - 3.0) < 1e-14
+
+
+def pin_dense_mlp_reduction():
+    # E=1, k=1, renorm: the layer is a dense SwiGLU MLP (torch, float64)
+    rng = _rng(7)
+    T, H, F = 9, 6, 10
+    x = rng.standard_normal((T, H))
+    wg, wu = rng.standard_normal((1, H, F)), rng.standard_normal((1, H, F))
+    wd = rng.standard_normal((1, F, H))
+    cfg = ref.MoEConfig(T, H, 1, 1, F, 1, -1.0, 0, True)
+    res = ref.layer_dropless(cfg, x, np.zeros((T, 1), np.float32),
+                             ref.dense_weights(wg, wu, wd))
+    xt = torch.from_numpy(x)
+    want = (torch.nn.functional.silu(xt @ torch.from_numpy(wg[0]))
+            * (xt @ torch.from_numpy(wu[0]))) @ torch.from_numpy(wd[0])
+    assert np.allclose(res.y, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_combine():
+    rng = _rng(8)
+    T, H, E, k, F, S = 24, 5, 8, 3, 7, 2
+    x = rng.standard_normal((T, H))
+    one = (rng.standard_normal((H, F)), rng.standard_normal((H, F)),
+           rng.standard_normal((F, H)))
+    same = ref.dense_weights(*[np.stack([w] * E) for w in one])
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    _, ffn = ref.expert_ffn(x, *one)
+    # identical experts + renorm: y = FFN(x)
+    cfg = ref.MoEConfig(T, H, E, k, F, S, -1.0, 0, True)
+    res = ref.layer_dropless(cfg, x, L, same)
+    assert np.allclose(res.y, ffn, rtol=1e-12, atol=1e-12)
+    # without renorm: y = (sum of the chosen softmax probabilities) FFN(x)
+    cfg = ref.MoEConfig(T, H, E, k, F, S, -1.0, 0, False)
+    res = ref.layer_dropless(cfg, x, L, same)
+    p = scipy.special.softmax(L.astype(np.float64), axis=1)
+    mass = np.sort(p, axis=1)[:, -k:].sum(1)
+    assert np.allclose(res.y, mass[:, None] * ffn, rtol=1e-12, atol=1e-12)
+    # all rows of a token dropped -> its output is exactly zero
+    L = np.zeros((T, E), np.float32)
+    L[:, 0] = 5.0                      # every token's top-1 is expert 0
+    cfg = ref.MoEConfig(T, H, E, 1, F, S, 0.25, 0, True)   # C = 3
+    res = ref.layer_capped(cfg, x, L, same)
+    C = ref.capacity(T, 1, S, 0.25)
+    assert C == 3
+    assert np.allclose(res.y[:C], ffn[:C], rtol=1e-12, atol=1e-12)
+    assert np.all(res.y[C:] == 0)
+
+
+# --------------------------------------------------------------------------
+# the chunked dropless fallback
+# --------------------------------------------------------------------------
+def pin_chunk_count_golden():
+    with open(os.path.join(GOLDEN, "fallback_chunks.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        C = ref.capacity(c["T"], c["k"], c["S"], c["factor"])
+        plan = ref.chunk_plan(c["T"], c["k"], c["E"], c["S"], C)
+        assert len(plan) == c["n_chunks"]
+    # DeepSeek-V3 shape: 2048-token chunks of 8 picks fill C = 16384 exactly
+    assert len(ref.chunk_plan(8192, 8, 256, 8, 16384)) == 4
+
+
+def pin_chunk_plan_bounds():
+    rng = _rng(9)
+    for _ in range(300):
+        S = int(rng.choice([1, 2, 4, 8]))
+        E = S * int(rng.integers(1, 6))
+        k = int(rng.integers(1, E + 1))
+        T = int(rng.integers(1, 200))
+        factor = float(rng.choice([0.1, 0.5, 1.0, 2.0, 3.0]))
+        C = ref.capacity(T, k, S, factor)
+        plan = ref.chunk_plan(T, k, E, S, C)
+        m = min(k, E // S)
+        # contiguous cover of [0, T)
+        assert plan[0][0] == 0 and plan[-1][1] == T
+        assert all(a[1] == b[0] for a, b in zip(plan[:-1], plan[1:]))
+        sizes = [b - a for a, b in plan]
+        c = sizes[0]
+        assert all(sz == c for sz in sizes[:-1]) and 0 < sizes[-1] <= c
+        # the chunk's worst case fits C, one more token would not
+        if C >= m:
+            assert c * m <= C < (c + 1) * m or c == T
+        else:
+            assert c == 1
+    # explicit count
+    assert [b - a for a, b in ref.chunk_plan(10, 2, 4, 2, 4, n_chunks=3)] \
+        == [4, 4, 2]
+
+
+def pin_fallback_equivalences():
+    rng = _rng(10)
+    T, H, E, k, F, S = 48, 6, 8, 2, 5, 2
+    x = rng.standard_normal((T, H))
+    ws = ref.dense_weights(rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, F, H)))
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    L[:, :3] += 1.0                                  # hot shard 0
+    cfg = ref.MoEConfig(T, H, E, k, F, S, 0.1)
+    drop = ref.layer_dropless(cfg, x, L, ws)
+    chunked = ref.layer_dropless_chunked(cfg, x, L, ws)
+    assert len(chunked.chunks) > 1
+    assert np.array_equal(chunked.y, drop.y) or \
+        np.allclose(chunked.y, drop.y, rtol=1e-13, atol=1e-13)
+    # factor 0.1 forces overflow; the capped path diverges from dropless
+    capped = ref.layer_capped(cfg, x, L, ws)
+    assert capped.overflow and capped.perm.n_dropped > 0
+    assert not np.allclose(capped.y, drop.y)
+    # the layer with fallback=layer matches dropless in both branches
+    for factor in (0.1, 2.0, 8.0):
+        c2 = ref.MoEConfig(T, H, E, k, F, S, factor)
+        out = ref.layer(c2, x, L, ws)
+        assert np.allclose(out.y, drop.y, rtol=1e-13, atol=1e-13)
+    # uncapped (factor <= 0) is dropless
+    for factor in (-1.0, 0.0):
+        c3 = ref.MoEConfig(T, H, E, k, F, S, factor)
+        assert np.array_equal(ref.layer_capped(c3, x, L, ws).y, drop.y)
+
+
+def pin_asymmetric_single_shard():
+    # only the last shard is hot; the layer still takes the fallback
+    rng = _rng(11)
+    T, H, E, k, F, S = 40, 4, 8, 2, 3, 4
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    L[:, 6:8] += 4.0
+    idx, _, _ = ref.route(L, k)
+    r = ref.shard_counts(ref.expert_counts(idx, E), S)
+    C = ref.capacity(T, k, S, 2.0)
+    assert int(np.argmax(r)) == 3 and r[3] > C
+    assert sum(int(v) > C for v in r) == 1
+    x = rng.standard_normal((T, H))
+    ws = ref.dense_weights(rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, F, H)))
+    out = ref.layer(ref.MoEConfig(T, H, E, k, F, S, 2.0), x, L, ws)
+    assert out.overflow and len(out.chunks) > 1
+
+
+ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -1,0 +1,101 @@
+"""Planted mistakes in the oracle must fail at least one pin (CPU only).
+
+Each mutant is the oracle's source with one plausible slip (a wrong tie
+break, a floor turned ceil, a swapped operand, a dropped weight ...).  The
+mutant is loaded as a separate module and the pins are run against it; the
+test passes only if some pin rejects it.  The real oracle is not modified.
+"""
+import importlib.util
+import os
+import sys
+import types
+
+import pytest
+
+from tests import oracle_pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(
+    os.path.abspath(__file__))), "oracle", "moe_ref.py")
+
+MUTANTS = {
+    "tie_to_higher_index": (
+        "keyed = [(-clean_logit(float(row[e])), e) for e in range(E)]",
+        "keyed = [(-clean_logit(float(row[e])), -e) for e in range(E)]"),
+    "nan_not_cleaned": (
+        "return v if math.isfinite(v) else -math.inf",
+        "return v"),
+    "always_renormalise": (
+        "            p = softmax_f64(row)\n            w[t] = [p[e] for e in chosen]",
+        "            w[t] = softmax_f64([row[e] for e in chosen])"),
+    "capacity_ceil": (
+        "c = math.floor(f * T * k / S)", "c = math.ceil(f * T * k / S)"),
+    "flag_not_strict": (
+        "return any(int(x) > C for x in r)",
+        "return any(int(x) >= C for x in r)"),
+    "strided_shards": (
+        "for e in range(s * Es, (s + 1) * Es):",
+        "for e in range(s, E, S):"),
+    "inclusive_scan": (
+        "        out[i] = run\n        run += int(x)\n",
+        "        run += int(x)\n        out[i] = run\n"),
+    "token_major_order": (
+        "    rows.sort()\n", "    rows.sort(key=lambda q: (q[1], q[0]))\n"),
+    "keep_one_extra_row": (
+        "if C is None or rank_in_shard[s] < C:",
+        "if C is None or rank_in_shard[s] <= C:"),
+    "dedup_over_all_rows": (
+        "    for (e, t, j) in kept:\n        uniq_sets[e // Es].add(t)",
+        "    for (e, t, j) in rows:\n        uniq_sets[e // Es].add(t)"),
+    "silu_sign": (
+        "return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
+    "gate_up_swapped": ("h = silu(g) * u", "h = silu(u) * g"),
+    "combine_ignores_weight": (
+        "y[t] += float(topk_w[t, j]) * y_sorted[r]", "y[t] += y_sorted[r]"),
+    "combine_skips_row_zero": ("            if r >= 0:\n",
+                               "            if r > 0:\n"),
+    "chunk_ignores_shard_bound": (
+        "c = max(1, C // worst_per_token)", "c = max(1, C // k)"),
+    "chunk_one_too_big": (
+        "c = max(1, C // worst_per_token)",
+        "c = max(1, C // worst_per_token + 1)"),
+}
+
+
+def _load_mutant(name, old, new):
+    with open(ORACLE_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    src = src.replace(old, new)
+    modname = f"_oracle_mutant_{name}"
+    mod = types.ModuleType(modname)
+    mod.__file__ = ORACLE_SRC
+    sys.modules[modname] = mod
+    try:
+        exec(compile(src, f"<mutant {name}>", "exec"), mod.__dict__)
+    except Exception:
+        del sys.modules[modname]
+        raise
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    old, new = MUTANTS[name]
+    mod = _load_mutant(name, old, new)
+    try:
+        monkeypatch.setattr(oracle_pins, "ref", mod)
+        caught = None
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin()
+            except Exception as exc:      # AssertionError or a crash
+                caught = (pin.__name__, type(exc).__name__)
+                break
+        assert caught is not None, f"no pin catches mutant {name}"
+    finally:
+        sys.modules.pop(mod.__name__, None)
+
+
+def test_real_oracle_passes_all_pins():
+    for pin in oracle_pins.ALL_PINS:
+        pin()
