@@ -1,0 +1,277 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE token-dispatch + expert-compute
+ * library (libmoe_gb300.so).
+ *
+ * The layer this library computes is the expert-parallel MoE layer of the
+ * MaxText pages:
+ *   router top-k -> per-expert / per-shard counts and the ragged
+ *   receive-buffer overflow check -> expert-sorted permute with per-shard
+ *   token dedup -> grouped-GEMM SwiGLU expert FFN -> weighted combine,
+ *   with the chunked dropless fallback when a shard would overflow.
+ * Sources:
+ *   [PR5920] "Support moe_dropless_fallback=layer on the ragged all-to-all
+ *            MoE path" (MaxText pull request 5920), sections Why, How,
+ *            Shortcomings, Tests.
+ *   [PR4760] "Moe dynamic redundancy" (MaxText pull request 4760), review
+ *            comments on ra2a_dedup_and_route and get_gmm_for_local_experts.
+ *   [PR4969] "MoE ring-of-experts: TC Pallas ring all-gather for the combine
+ *            backward + x_sorted remat save" (MaxText pull request 4969),
+ *            section What.
+ * On one GPU the expert-parallel shards are logical ranges of E/S
+ * consecutive experts; nothing is exchanged between GPUs.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Ownership: the caller owns every buffer.  The library never allocates
+ *   device memory; scratch space is passed in as `workspace`, sized by
+ *   moe_workspace_bytes().  Device pointers are plain CUDA device pointers.
+ * Execution: every call only enqueues work on `stream` (a cudaStream_t; NULL
+ *   is the legacy default stream) and returns before it runs, except
+ *   moe_layer() in MOE_MODE_FALLBACK_LAYER, which reads the 4-byte overflow
+ *   flag back to the host (one stream synchronisation) to choose its branch.
+ * Errors: arguments are validated on the host before anything is launched;
+ *   a bad argument returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a
+ *   valid shape the kernels do not cover) and nothing is enqueued.  A failed
+ *   launch returns MOE_ERR_CUDA.  Conditions found while the kernels run are
+ *   OR-ed into an optional device status word (int32, see MOE_DEV_*), which
+ *   the caller zeroes and reads when it wants; a NULL status word is allowed.
+ * Layouts (row-major, C order):
+ *   x        [T, H]    dtype         token activations
+ *   logits   [T, E]    float32       router logits
+ *   topk_idx [T, k]    int32         chosen experts, best first
+ *   topk_w   [T, k]    float32       combine weights
+ *   w_gate   [E, H, F] dtype         gate projection of each expert
+ *   w_up     [E, H, F] dtype         up projection of each expert
+ *   w_down   [E, F, H] dtype         down projection of each expert
+ *   x_sorted [T*k, H]  dtype         routed rows, grouped by expert
+ *   h        [T*k, F]  dtype         SwiGLU activations of the routed rows
+ *   y_sorted [T*k, H]  dtype         expert outputs of the routed rows
+ *   y        [T, H]    dtype         layer output
+ * The dtype matrices (x, w_*, x_sorted, h, y_sorted, y) must be 16-byte
+ * aligned and H and F must make their rows a multiple of 16 bytes; the
+ * int32/float arrays need only their natural 4-byte alignment.  A pointer
+ * that breaks this is rejected.  Buffers indexed by routed row are sized for the
+ * worst case of T*k rows; a capped pass fills only the first
+ * group_offsets[E] of them.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad shape, pointer, alignment or option      */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels cover    */
+  MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required   */
+  MOE_ERR_CUDA = 4         /* a CUDA runtime call or launch failed         */
+} moe_status_t;
+
+/* Bits OR-ed into the device status word by the kernels. */
+#define MOE_DEV_NONFINITE 1 /* a NaN/inf logit was seen; it ranked as -inf */
+#define MOE_DEV_TIMEOUT 2   /* a bounded wait in the GEMM gave up          */
+#define MOE_DEV_BAD_INDEX 4 /* an expert index outside [0, E) was skipped  */
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+typedef struct {
+  int32_t T; /* tokens (>= 0)                                             */
+  int32_t H; /* hidden size                                               */
+  int32_t E; /* experts, 1..1024                                          */
+  int32_t k; /* experts per token, 1..min(E, 32)                          */
+  int32_t F; /* expert FFN width                                          */
+  int32_t S; /* logical EP shards, divides E, 1..64                       */
+  /* Receive-buffer cap per shard [PR5920 Why]: > 0 gives the capacity
+   * C = floor(factor * T * k / S) rows (computed in double from this float,
+   * at most T*k); <= 0 means uncapped (the pages' -1).                    */
+  float ragged_buffer_factor;
+  /* Chunks of the dropless fallback [PR5920 How]; 0 derives the count:
+   * chunks of floor(C / min(k, E/S)) tokens (at least 1), so that a
+   * chunk's worst-case receive fits C.  n > 0 gives chunks of ceil(T/n). */
+  int32_t n_chunks;
+  moe_dtype_t dtype; /* type of x, the expert weights, h, y_sorted and y   */
+  /* Combine weights: 0 = softmax over all E logits read at the chosen
+   * experts; 1 = softmax over the k chosen logits.                        */
+  int32_t renorm;
+} moe_config_t;
+
+/* ----------------------------------------------------------------------
+ * moe_route -- router top-k and combine weights [PR5920 How: the check is
+ * computed from the router's top-k].  One warp per token.
+ *   logits   in  [T, E] float32 (device)
+ *   topk_idx out [T, k] int32: experts by descending logit; equal logits
+ *            go to the lower index.  NaN/inf logits rank as -inf and set
+ *            MOE_DEV_NONFINITE.
+ *   topk_w   out [T, k] float32: see moe_config_t.renorm; a token with no
+ *            finite logit gets zero weights.
+ *   status_word  in/out, device int32 or NULL.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_route(const moe_config_t *cfg, const float *logits,
+                       int32_t *topk_idx, float *topk_w,
+                       int32_t *status_word, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_check_overflow -- counts and the ragged overflow check [PR5920 Why,
+ * How; PR4760 review: group_sizes per expert, experts_per_rank].
+ *   topk_idx        in  [T, k] int32 (device)
+ *   expert_counts   out [E]   rows routed to each expert
+ *   expert_offsets  out [E+1] exclusive scan of expert_counts
+ *   shard_counts    out [S]   rows routed to each shard (r_s)
+ *   overflow_flag   out [1]   1 iff some r_s > C (strict); 0 when uncapped
+ *   required_factor out [1]   float max_s r_s * S / (T*k) (0 when T = 0)
+ *   capacity        out [1]   C, or -1 when uncapped
+ * All outputs are device pointers.  Indices outside [0, E) are skipped.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_check_overflow(const moe_config_t *cfg,
+                                const int32_t *topk_idx,
+                                int32_t *expert_counts,
+                                int32_t *expert_offsets,
+                                int32_t *shard_counts,
+                                int32_t *overflow_flag,
+                                float *required_factor, int32_t *capacity,
+                                moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_permute -- stable expert-sorted permute with the capped drop rule and
+ * per-shard token dedup [PR5920 Why: rows past the cap are dropped; PR4760
+ * review: ra2a_dedup_and_route / expand_indices must never truncate;
+ * PR4969 What: x_sorted].
+ *   Routed rows (t, j) are ordered by (expert, token).  With capped != 0 a
+ *   row whose rank inside its shard is >= C is dropped; kept rows are
+ *   compacted.  U_s is the ascending set of tokens with a kept row in shard
+ *   s; uniq_tokens = U_0 ++ U_1 ++ ...
+ *   x            in  [T, H] dtype
+ *   topk_idx     in  [T, k] int32
+ *   capped       in  nonzero: apply C from cfg; 0: uncapped
+ *   x_sorted     out [T*k, H]: row r = x[sorted_token[r]]
+ *   row_of       out [T, k] int32: sorted row of (t, j), -1 if dropped
+ *   sorted_token out [T*k] int32: token of each kept row
+ *   group_offsets out [E+1] int32: kept rows per expert, scanned
+ *   uniq_offsets out [S+1] int32: scanned |U_s|
+ *   uniq_tokens  out [T*min(k,S)] int32 (first uniq_offsets[S] written)
+ *   expand_idx   out [T*k] int32: row r -> its token's slot in uniq_tokens
+ *   n_dropped    out [1] int32
+ *   workspace    scratch of moe_workspace_bytes(cfg, MOE_WS_PERMUTE) bytes
+ * Entries past the valid prefix of sorted_token, expand_idx, x_sorted and
+ * uniq_tokens are left unwritten.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_permute(const moe_config_t *cfg, const void *x,
+                         const int32_t *topk_idx, int32_t capped,
+                         void *x_sorted, int32_t *row_of,
+                         int32_t *sorted_token, int32_t *group_offsets,
+                         int32_t *uniq_offsets, int32_t *uniq_tokens,
+                         int32_t *expand_idx, int32_t *n_dropped,
+                         void *workspace, size_t workspace_bytes,
+                         moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_gmm_swiglu -- grouped GEMM SwiGLU expert FFN over ragged expert groups
+ * [PR4760 review: grouped matmul with group_sizes per expert; expert weights
+ * w0 of shape [E, H, H_ffn]].  For the rows r of group e
+ * ([group_offsets[e], group_offsets[e+1])):
+ *     h[r] = silu(x_sorted[r] w_gate[e]) * (x_sorted[r] w_up[e])
+ *     y_sorted[r] = h[r] w_down[e],   silu(z) = z / (1 + exp(-z)).
+ *   bf16: tcgen05 tensor cores, fp32 accumulate, h and y_sorted rounded to
+ *   bf16 (needs H % 128 == 0 and F % 128 == 0, else MOE_ERR_UNSUPPORTED).
+ *   f32: CUDA-core FMA in fp32.
+ *   x_sorted, h, y_sorted have T*k rows allocated; group_offsets [E+1] is on
+ *   the device (nondecreasing, group_offsets[E] <= T*k).  Rows past
+ *   group_offsets[E] are not written.  status_word: MOE_DEV_TIMEOUT if a
+ *   pipeline wait gave up (the output is then incomplete).
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_gmm_swiglu(const moe_config_t *cfg, const void *x_sorted,
+                            const int32_t *group_offsets,
+                            const void *w_gate, const void *w_up,
+                            const void *w_down, void *h, void *y_sorted,
+                            int32_t *status_word, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_combine -- weighted unpermute [PR4969 What: the combine reduces the
+ * expert outputs back to tokens].  y[t] = sum_{j<k, row_of[t,j] >= 0}
+ * topk_w[t,j] * y_sorted[row_of[t,j]], accumulated in fp32 in slot order.
+ * A token whose rows were all dropped gets zeros.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_combine(const moe_config_t *cfg, const void *y_sorted,
+                         const int32_t *row_of, const float *topk_w, void *y,
+                         moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_layer_dropless_chunked -- the chunked dropless fallback [PR5920 How,
+ * Shortcomings]: the layer runs over contiguous token chunks (see
+ * moe_config_t.n_chunks), each uncapped (force_dropless), one after another
+ * on `stream`, each writing its own rows of y.  The result equals the
+ * uncapped layer.  workspace: moe_workspace_bytes(cfg, MOE_WS_CHUNKED).
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_layer_dropless_chunked(const moe_config_t *cfg,
+                                        const void *x, const float *logits,
+                                        const void *w_gate, const void *w_up,
+                                        const void *w_down, void *y,
+                                        int32_t *status_word, void *workspace,
+                                        size_t workspace_bytes,
+                                        moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * moe_layer -- the whole layer (an extension composing the calls above).
+ *   MOE_MODE_FALLBACK_LAYER: route, check, read the flag; no overflow -> the
+ *     capped path; overflow -> the chunked dropless fallback, reusing the
+ *     routing [PR5920 How, moe_dropless_fallback=layer].
+ *   MOE_MODE_CAPPED: the capped path only; rows past C are dropped.
+ *   MOE_MODE_DROPLESS: one uncapped pass (force_dropless).
+ * info (host, may be NULL) receives what the call learned; workspace:
+ * moe_workspace_bytes(cfg, MOE_WS_LAYER).
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  MOE_MODE_FALLBACK_LAYER = 0,
+  MOE_MODE_CAPPED = 1,
+  MOE_MODE_DROPLESS = 2
+} moe_mode_t;
+
+typedef struct {
+  int32_t overflow; /* flag read back (FALLBACK_LAYER); -1 if not read   */
+  int32_t n_chunks; /* passes run: 1, or the fallback's chunk count       */
+  int64_t capacity; /* C, or -1 when uncapped                             */
+} moe_layer_info_t;
+
+moe_status_t moe_layer(const moe_config_t *cfg, const void *x,
+                       const float *logits, const void *w_gate,
+                       const void *w_up, const void *w_down, void *y,
+                       moe_mode_t mode, moe_layer_info_t *info,
+                       int32_t *status_word, void *workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * Host-side queries (no GPU work).
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  MOE_WS_PERMUTE = 0, /* moe_permute                                   */
+  MOE_WS_CHUNKED = 1, /* moe_layer_dropless_chunked                    */
+  MOE_WS_LAYER = 2    /* moe_layer                                     */
+} moe_ws_kind_t;
+
+/* Workspace bytes an entry point needs for cfg (0 for an invalid cfg). */
+size_t moe_workspace_bytes(const moe_config_t *cfg, moe_ws_kind_t which);
+
+/* Validates cfg alone: MOE_OK or the reason it is rejected. */
+moe_status_t moe_validate_config(const moe_config_t *cfg);
+
+/* C = floor(factor*T*k/S) capped at T*k, or -1 when uncapped [PR5920 Why]. */
+int64_t moe_capacity_rows(const moe_config_t *cfg);
+
+/* Token count of each fallback chunk and the number of chunks. */
+int32_t moe_chunk_tokens(const moe_config_t *cfg);
+int32_t moe_num_chunks(const moe_config_t *cfg);
+
+/* Static text for a status code. */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,271 @@
+"""Python binding of libmoe_gb300.so, the sm_103a MoE dispatch + expert
+library declared in include/moe.h.
+
+The functions here carry the C names and only marshal arguments: tensors
+become device pointers, the current torch stream becomes the CUDA stream,
+and a non-OK status raises MoeError.  All arithmetic runs in the CUDA
+kernels of the library; there is no other code path.  If the library has
+not been built (``mixture_experts_token_gb300.build.build()``), every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int, c_int32, c_int64, c_size_t, c_void_p
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, \
+    MOE_ERR_CUDA = range(5)
+MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 1, 2, 4
+MOE_F32, MOE_BF16 = 0, 1
+MOE_MODE_FALLBACK_LAYER, MOE_MODE_CAPPED, MOE_MODE_DROPLESS = 0, 1, 2
+MOE_WS_PERMUTE, MOE_WS_CHUNKED, MOE_WS_LAYER = 0, 1, 2
+
+
+class MoeConfig(ctypes.Structure):
+    """moe_config_t."""
+    _fields_ = [("T", c_int32), ("H", c_int32), ("E", c_int32),
+                ("k", c_int32), ("F", c_int32), ("S", c_int32),
+                ("ragged_buffer_factor", c_float), ("n_chunks", c_int32),
+                ("dtype", c_int), ("renorm", c_int32)]
+
+    def with_(self, **kw) -> "MoeConfig":
+        c = MoeConfig()
+        ctypes.pointer(c)[0] = self
+        for key, v in kw.items():
+            setattr(c, key, v)
+        return c
+
+    def __repr__(self):
+        return ("MoeConfig(" + ", ".join(f"{n}={getattr(self, n)}"
+                                         for n, _ in self._fields_) + ")")
+
+
+class MoeLayerInfo(ctypes.Structure):
+    """moe_layer_info_t."""
+    _fields_ = [("overflow", c_int32), ("n_chunks", c_int32),
+                ("capacity", c_int64)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {moe_status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (loads it on first use)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "mixture_experts_token_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        _declare(handle)
+        _lib = handle
+    return _lib
+
+
+def _declare(h):
+    P = c_void_p
+    cfg = ctypes.POINTER(MoeConfig)
+    sig = {
+        "moe_route": [cfg, P, P, P, P, P],
+        "moe_check_overflow": [cfg, P, P, P, P, P, P, P, P],
+        "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
+                        c_size_t, P],
+        "moe_gmm_swiglu": [cfg, P, P, P, P, P, P, P, P, P],
+        "moe_combine": [cfg, P, P, P, P, P],
+        "moe_layer_dropless_chunked": [cfg, P, P, P, P, P, P, P, P, c_size_t,
+                                       P],
+        "moe_layer": [cfg, P, P, P, P, P, P, c_int,
+                      ctypes.POINTER(MoeLayerInfo), P, P, c_size_t, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(h, name)
+        fn.argtypes = args
+        fn.restype = c_int
+    h.moe_workspace_bytes.argtypes = [cfg, c_int]
+    h.moe_workspace_bytes.restype = c_size_t
+    h.moe_validate_config.argtypes = [cfg]
+    h.moe_validate_config.restype = c_int
+    h.moe_capacity_rows.argtypes = [cfg]
+    h.moe_capacity_rows.restype = c_int64
+    h.moe_chunk_tokens.argtypes = [cfg]
+    h.moe_chunk_tokens.restype = c_int32
+    h.moe_num_chunks.argtypes = [cfg]
+    h.moe_num_chunks.restype = c_int32
+    h.moe_status_string.argtypes = [c_int]
+    h.moe_status_string.restype = ctypes.c_char_p
+
+
+# ------------------------------------------------------------ marshalling --
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return c_void_p(t)
+    return c_void_p(t.data_ptr())
+
+
+def _nbytes(t):
+    if t is None:
+        return 0
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        if torch.cuda.is_available():
+            return c_void_p(torch.cuda.current_stream().cuda_stream)
+        return None
+    if isinstance(stream, int):
+        return c_void_p(stream)
+    return c_void_p(stream.cuda_stream)
+
+
+def _check(status, where):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def make_config(T, H, E, k, F, S, factor=2.0, n_chunks=0, dtype="bf16",
+                renorm=False) -> MoeConfig:
+    return MoeConfig(T, H, E, k, F, S, float(factor), n_chunks,
+                     MOE_F32 if dtype in ("f32", "float32") else MOE_BF16,
+                     1 if renorm else 0)
+
+
+# --------------------------------------------------------- entry points ---
+def moe_status_string(status) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_validate_config(cfg) -> int:
+    return lib().moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_capacity_rows(cfg) -> int:
+    return lib().moe_capacity_rows(ctypes.byref(cfg))
+
+
+def moe_chunk_tokens(cfg) -> int:
+    return lib().moe_chunk_tokens(ctypes.byref(cfg))
+
+
+def moe_num_chunks(cfg) -> int:
+    return lib().moe_num_chunks(ctypes.byref(cfg))
+
+
+def moe_workspace_bytes(cfg, which) -> int:
+    return lib().moe_workspace_bytes(ctypes.byref(cfg), which)
+
+
+def moe_route(cfg, logits, topk_idx, topk_w, status_word=None, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx),
+                           _ptr(topk_w), _ptr(status_word), _stream(stream)),
+           "moe_route")
+
+
+def moe_check_overflow(cfg, topk_idx, expert_counts, expert_offsets,
+                       shard_counts, overflow_flag, required_factor, capacity,
+                       stream=None):
+    _check(lib().moe_check_overflow(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(expert_counts),
+        _ptr(expert_offsets), _ptr(shard_counts), _ptr(overflow_flag),
+        _ptr(required_factor), _ptr(capacity), _stream(stream)),
+        "moe_check_overflow")
+
+
+def moe_permute(cfg, x, topk_idx, capped, x_sorted, row_of, sorted_token,
+                group_offsets, uniq_offsets, uniq_tokens, expand_idx,
+                n_dropped, workspace, stream=None):
+    _check(lib().moe_permute(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), 1 if capped else 0,
+        _ptr(x_sorted), _ptr(row_of), _ptr(sorted_token),
+        _ptr(group_offsets), _ptr(uniq_offsets), _ptr(uniq_tokens),
+        _ptr(expand_idx), _ptr(n_dropped), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "moe_permute")
+
+
+def moe_gmm_swiglu(cfg, x_sorted, group_offsets, w_gate, w_up, w_down, h,
+                   y_sorted, status_word=None, stream=None):
+    _check(lib().moe_gmm_swiglu(
+        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets),
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(h), _ptr(y_sorted),
+        _ptr(status_word), _stream(stream)), "moe_gmm_swiglu")
+
+
+def moe_combine(cfg, y_sorted, row_of, topk_w, y, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_sorted), _ptr(row_of),
+                             _ptr(topk_w), _ptr(y), _stream(stream)),
+           "moe_combine")
+
+
+def moe_layer_dropless_chunked(cfg, x, logits, w_gate, w_up, w_down, y,
+                               workspace, status_word=None, stream=None):
+    _check(lib().moe_layer_dropless_chunked(
+        ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(y), _ptr(status_word), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "moe_layer_dropless_chunked")
+
+
+def moe_layer(cfg, x, logits, w_gate, w_up, w_down, y, mode, workspace,
+              status_word=None, stream=None) -> dict:
+    info = MoeLayerInfo()
+    _check(lib().moe_layer(
+        ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(y), mode, ctypes.byref(info), _ptr(status_word),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "moe_layer")
+    return {"overflow": info.overflow, "n_chunks": info.n_chunks,
+            "capacity": info.capacity}
+
+
+# ------------------------------------------------- buffer allocation ------
+def alloc_step_buffers(cfg, device="cuda"):
+    """Device buffers for calling the entry points one by one (torch owns
+    the memory; sizes follow include/moe.h)."""
+    import torch
+    T, H, E, k, F, S = cfg.T, cfg.H, cfg.E, cfg.k, cfg.F, cfg.S
+    dt = torch.float32 if cfg.dtype == MOE_F32 else torch.bfloat16
+    i32 = dict(dtype=torch.int32, device=device)
+    R = T * k
+    return {
+        "topk_idx": torch.empty((T, k), **i32),
+        "topk_w": torch.empty((T, k), dtype=torch.float32, device=device),
+        "status": torch.zeros(1, **i32),
+        "expert_counts": torch.empty(E, **i32),
+        "expert_offsets": torch.empty(E + 1, **i32),
+        "shard_counts": torch.empty(S, **i32),
+        "overflow_flag": torch.empty(1, **i32),
+        "required_factor": torch.empty(1, dtype=torch.float32, device=device),
+        "capacity": torch.empty(1, **i32),
+        "x_sorted": torch.empty((R, H), dtype=dt, device=device),
+        "row_of": torch.empty((T, k), **i32),
+        "sorted_token": torch.empty(max(R, 1), **i32),
+        "group_offsets": torch.empty(E + 1, **i32),
+        "uniq_offsets": torch.empty(S + 1, **i32),
+        "uniq_tokens": torch.empty(max(T * min(k, S), 1), **i32),
+        "expand_idx": torch.empty(max(R, 1), **i32),
+        "n_dropped": torch.empty(1, **i32),
+        "permute_ws": torch.empty(
+            max(moe_workspace_bytes(cfg, MOE_WS_PERMUTE), 256),
+            dtype=torch.uint8, device=device),
+        "h": torch.empty((R, max(F, 1)), dtype=dt, device=device),
+        "y_sorted": torch.empty((R, H), dtype=dt, device=device),
+        "y": torch.empty((T, H), dtype=dt, device=device),
+    }
+
+
+def layer_workspace(cfg, which=MOE_WS_LAYER, device="cuda"):
+    import torch
+    n = moe_workspace_bytes(cfg, which)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)

@@ -1,0 +1,444 @@
+// C ABI entry points (include/moe.h): argument validation, workspace layout,
+// and the layer drivers that chain the kernels on one stream.
+//
+// "Support moe_dropless_fallback=layer on the ragged all-to-all MoE path"
+// (MaxText pull request 5920), section How: the layer checks for overflow
+// from the router's top-k, takes the capped path when no shard overflows
+// and otherwise runs the layer over sequence chunks, each with the
+// worst-case (force_dropless) buffer, chosen so that this buffer is no
+// larger than the capped one.  Section Shortcomings: an overflowing layer
+// costs about n_chunks passes.
+#include <cmath>
+#include <cstdint>
+#include <limits>
+
+#include "internal.h"
+
+namespace moe {
+
+cudaError_t launch_gmm_f32(const moe_config_t& c, const void* x_sorted,
+                           const int32_t* group_offsets, const void* w_gate,
+                           const void* w_up, const void* w_down, void* h,
+                           void* y_sorted, cudaStream_t s);
+cudaError_t launch_gmm_bf16(const moe_config_t& c, const void* x_sorted,
+                            const int32_t* group_offsets, const void* w_gate,
+                            const void* w_up, const void* w_down, void* h,
+                            void* y_sorted, int32_t* status, cudaStream_t s);
+
+int64_t capacity_rows(const moe_config_t& c) {
+  const double f = static_cast<double>(c.ragged_buffer_factor);
+  if (!(f > 0.0)) return -1;  // <= 0 or NaN: uncapped
+  const double v = std::floor(f * static_cast<double>(c.T) *
+                              static_cast<double>(c.k) /
+                              static_cast<double>(c.S));
+  const int64_t rows = static_cast<int64_t>(c.T) * c.k;
+  if (v >= static_cast<double>(rows)) return rows;
+  return static_cast<int64_t>(v);
+}
+
+int32_t chunk_tokens(const moe_config_t& c) {
+  if (c.T <= 0) return 0;
+  int64_t tok;
+  if (c.n_chunks > 0) {
+    tok = (static_cast<int64_t>(c.T) + c.n_chunks - 1) / c.n_chunks;
+  } else {
+    const int64_t cap = capacity_rows(c);
+    if (cap < 0) {
+      tok = c.T;
+    } else {
+      const int64_t worst_per_token = std::min(c.k, c.E / c.S);
+      tok = std::max<int64_t>(1, cap / worst_per_token);
+    }
+  }
+  return static_cast<int32_t>(std::min<int64_t>(tok, c.T));
+}
+
+cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
+                       const int32_t* group_offsets, const void* w_gate,
+                       const void* w_up, const void* w_down, void* h,
+                       void* y_sorted, int32_t* status, cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_gmm_f32(c, x_sorted, group_offsets, w_gate, w_up, w_down, h,
+                          y_sorted, s);
+  return launch_gmm_bf16(c, x_sorted, group_offsets, w_gate, w_up, w_down, h,
+                         y_sorted, status, s);
+}
+
+namespace {
+
+moe_status_t validate(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->H < 1 || c->F < 0) return MOE_ERR_INVALID_ARG;
+  if (c->E < 1 || c->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > c->E || c->k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (c->S < 1 || c->S > kMaxShards || c->E % c->S != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
+  if (c->n_chunks < 0) return MOE_ERR_INVALID_ARG;
+  if (std::isnan(c->ragged_buffer_factor)) return MOE_ERR_INVALID_ARG;
+  const int eb = elem_bytes(c->dtype);
+  if ((static_cast<int64_t>(c->H) * eb) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(c->F) * eb) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(c->T) * c->k;
+  if (rows > std::numeric_limits<int32_t>::max()) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool ok_ptr(const void* p, bool need16) {
+  if (p == nullptr) return false;
+  const uintptr_t u = reinterpret_cast<uintptr_t>(p);
+  return need16 ? (u & 15u) == 0 : (u & 3u) == 0;
+}
+
+moe_status_t cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Buffers of one layer pass over up to `T` tokens, carved from a workspace.
+struct LayerBufs {
+  int32_t *topk_idx, *counts, *offsets, *shard, *flag, *cap;
+  float *topk_w, *req;
+  int32_t *row_of, *sorted_token, *group_offsets, *uniq_offsets,
+      *uniq_tokens, *expand_idx, *n_dropped;
+  PermuteScratch pws;
+  void *x_sorted, *h, *y_sorted;
+};
+
+LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
+                      size_t* bytes) {
+  Carve cv(base);
+  LayerBufs b;
+  const size_t tk = static_cast<size_t>(T) * c.k;
+  const size_t eb = elem_bytes(c.dtype);
+  b.topk_idx = cv.take<int32_t>(tk);
+  b.topk_w = cv.take<float>(tk);
+  b.counts = cv.take<int32_t>(c.E);
+  b.offsets = cv.take<int32_t>(c.E + 1);
+  b.shard = cv.take<int32_t>(c.S);
+  b.flag = cv.take<int32_t>(1);
+  b.req = cv.take<float>(1);
+  b.cap = cv.take<int32_t>(1);
+  b.row_of = cv.take<int32_t>(tk);
+  b.sorted_token = cv.take<int32_t>(tk);
+  b.group_offsets = cv.take<int32_t>(c.E + 1);
+  b.uniq_offsets = cv.take<int32_t>(c.S + 1);
+  b.uniq_tokens =
+      cv.take<int32_t>(static_cast<size_t>(T) * std::min(c.k, c.S));
+  b.expand_idx = cv.take<int32_t>(tk);
+  b.n_dropped = cv.take<int32_t>(1);
+  b.pws = carve_permute_scratch(cv, T, c.E, c.k, c.S);
+  b.x_sorted = cv.take<char>(tk * c.H * eb);
+  b.h = cv.take<char>(tk * static_cast<size_t>(c.F) * eb);
+  b.y_sorted = cv.take<char>(tk * c.H * eb);
+  if (bytes) *bytes = align_up(cv.off, 256);
+  return b;
+}
+
+size_t layer_bytes(const moe_config_t& c, int T) {
+  size_t n = 0;
+  carve_layer(nullptr, c, T, &n);
+  return n;
+}
+
+moe_config_t sub_config(const moe_config_t& c, int T) {
+  moe_config_t s = c;
+  s.T = T;
+  s.ragged_buffer_factor = -1.0f;
+  s.n_chunks = 0;
+  return s;
+}
+
+// One pass on tokens whose routing is already in `topk_idx/topk_w`:
+// permute (cap or uncapped) -> grouped FFN -> combine into y.
+cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
+                 const float* topk_w, int64_t cap, const void* wg,
+                 const void* wu, const void* wd, void* y, const LayerBufs& b,
+                 int32_t* status, cudaStream_t s) {
+  cudaError_t e = launch_permute(c, x, topk_idx, cap, b.x_sorted, b.row_of,
+                                 b.sorted_token, b.group_offsets,
+                                 b.uniq_offsets, b.uniq_tokens, b.expand_idx,
+                                 b.n_dropped, b.pws, status, s);
+  if (e != cudaSuccess) return e;
+  e = launch_gmm(c, b.x_sorted, b.group_offsets, wg, wu, wd, b.h, b.y_sorted,
+                 status, s);
+  if (e != cudaSuccess) return e;
+  return launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
+}
+
+// The chunked dropless fallback over precomputed routing.
+cudaError_t chunked_passes(const moe_config_t& c, const void* x,
+                           const int32_t* topk_idx, const float* topk_w,
+                           const void* wg, const void* wu, const void* wd,
+                           void* y, const LayerBufs& b, int32_t* status,
+                           cudaStream_t s, int32_t* n_run) {
+  const int ct = chunk_tokens(c);
+  const size_t row_bytes = static_cast<size_t>(c.H) * elem_bytes(c.dtype);
+  int n = 0;
+  for (int t0 = 0; t0 < c.T; t0 += ct, ++n) {
+    const int tc = std::min(ct, c.T - t0);
+    const moe_config_t sc = sub_config(c, tc);
+    const size_t o = static_cast<size_t>(t0);
+    cudaError_t e = pass(sc, static_cast<const char*>(x) + o * row_bytes,
+                         topk_idx + o * c.k, topk_w + o * c.k, -1, wg, wu, wd,
+                         static_cast<char*>(y) + o * row_bytes, b, status, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (n_run) *n_run = n;
+  return cudaSuccess;
+}
+
+bool gmm_shape_ok(const moe_config_t& c) {
+  if (c.F < 1) return false;
+  return c.dtype == MOE_F32 || gmm_tc_supported(c);
+}
+
+bool weights_ok(const void* wg, const void* wu, const void* wd) {
+  return ok_ptr(wg, true) && ok_ptr(wu, true) && ok_ptr(wd, true);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_validate_config(const moe_config_t* cfg) {
+  return validate(cfg);
+}
+
+int64_t moe_capacity_rows(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return -1;
+  return capacity_rows(*cfg);
+}
+
+int32_t moe_chunk_tokens(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  return chunk_tokens(*cfg);
+}
+
+int32_t moe_num_chunks(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  const int ct = chunk_tokens(*cfg);
+  return ct > 0 ? (cfg->T + ct - 1) / ct : 0;
+}
+
+size_t moe_workspace_bytes(const moe_config_t* cfg, moe_ws_kind_t which) {
+  if (validate(cfg) != MOE_OK) return 0;
+  switch (which) {
+    case MOE_WS_PERMUTE:
+      return permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
+    case MOE_WS_CHUNKED:
+      return layer_bytes(*cfg, chunk_tokens(*cfg));
+    case MOE_WS_LAYER:
+      return layer_bytes(*cfg, cfg->T);
+  }
+  return 0;
+}
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK:
+      return "ok";
+    case MOE_ERR_INVALID_ARG:
+      return "invalid argument";
+    case MOE_ERR_UNSUPPORTED:
+      return "shape not supported by the kernels";
+    case MOE_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case MOE_ERR_CUDA:
+      return "CUDA error";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const float* logits,
+                       int32_t* topk_idx, float* topk_w, int32_t* status_word,
+                       moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(logits, false) || !ok_ptr(topk_idx, false) ||
+      !ok_ptr(topk_w, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_route(*cfg, logits, topk_idx, topk_w, status_word, stream));
+}
+
+moe_status_t moe_check_overflow(const moe_config_t* cfg,
+                                const int32_t* topk_idx,
+                                int32_t* expert_counts,
+                                int32_t* expert_offsets,
+                                int32_t* shard_counts, int32_t* overflow_flag,
+                                float* required_factor, int32_t* capacity,
+                                moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((cfg->T > 0 && !ok_ptr(topk_idx, false)) ||
+      !ok_ptr(expert_counts, false) || !ok_ptr(expert_offsets, false) ||
+      !ok_ptr(shard_counts, false) || !ok_ptr(overflow_flag, false) ||
+      !ok_ptr(required_factor, false) || !ok_ptr(capacity, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_check(*cfg, topk_idx, expert_counts,
+                                  expert_offsets, shard_counts, overflow_flag,
+                                  required_factor, capacity, stream));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x,
+                         const int32_t* topk_idx, int32_t capped,
+                         void* x_sorted, int32_t* row_of,
+                         int32_t* sorted_token, int32_t* group_offsets,
+                         int32_t* uniq_offsets, int32_t* uniq_tokens,
+                         int32_t* expand_idx, int32_t* n_dropped,
+                         void* workspace, size_t workspace_bytes,
+                         moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(uniq_offsets, false) ||
+      !ok_ptr(n_dropped, false))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 &&
+      (!ok_ptr(x, true) || !ok_ptr(topk_idx, false) ||
+       !ok_ptr(x_sorted, true) || !ok_ptr(row_of, false) ||
+       !ok_ptr(sorted_token, false) || !ok_ptr(uniq_tokens, false) ||
+       !ok_ptr(expand_idx, false)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need =
+      permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
+  if (workspace == nullptr || workspace_bytes < need ||
+      !ok_ptr(workspace, true))
+    return MOE_ERR_WORKSPACE;
+  Carve cv(workspace);
+  const PermuteScratch ws =
+      carve_permute_scratch(cv, cfg->T, cfg->E, cfg->k, cfg->S);
+  const int64_t cap = capped ? capacity_rows(*cfg) : -1;
+  return cuda_status(launch_permute(*cfg, x, topk_idx, cap, x_sorted, row_of,
+                                    sorted_token, group_offsets, uniq_offsets,
+                                    uniq_tokens, expand_idx, n_dropped, ws,
+                                    nullptr, stream));
+}
+
+moe_status_t moe_gmm_swiglu(const moe_config_t* cfg, const void* x_sorted,
+                            const int32_t* group_offsets, const void* w_gate,
+                            const void* w_up, const void* w_down, void* h,
+                            void* y_sorted, int32_t* status_word,
+                            moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(h, true) ||
+      !ok_ptr(y_sorted, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gmm(*cfg, x_sorted, group_offsets, w_gate, w_up,
+                                w_down, h, y_sorted, status_word, stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_sorted,
+                         const int32_t* row_of, const float* topk_w, void* y,
+                         moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(y_sorted, true) || !ok_ptr(row_of, false) ||
+      !ok_ptr(topk_w, false) || !ok_ptr(y, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*cfg, y_sorted, row_of, topk_w, y, stream));
+}
+
+moe_status_t moe_layer_dropless_chunked(const moe_config_t* cfg,
+                                        const void* x, const float* logits,
+                                        const void* w_gate, const void* w_up,
+                                        const void* w_down, void* y,
+                                        int32_t* status_word, void* workspace,
+                                        size_t workspace_bytes,
+                                        moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x, true) || !ok_ptr(logits, false) ||
+      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(y, true))
+    return MOE_ERR_INVALID_ARG;
+  const int ct = chunk_tokens(*cfg);
+  if (workspace == nullptr || !ok_ptr(workspace, true) ||
+      workspace_bytes < layer_bytes(*cfg, ct))
+    return MOE_ERR_WORKSPACE;
+  const LayerBufs b = carve_layer(workspace, *cfg, ct, nullptr);
+  const size_t row_bytes = static_cast<size_t>(cfg->H) * elem_bytes(cfg->dtype);
+  for (int t0 = 0; t0 < cfg->T; t0 += ct) {
+    const int tc = std::min(ct, cfg->T - t0);
+    const moe_config_t sc = sub_config(*cfg, tc);
+    const size_t o = static_cast<size_t>(t0);
+    cudaError_t e = launch_route(sc, logits + o * cfg->E, b.topk_idx,
+                                 b.topk_w, status_word, stream);
+    if (e == cudaSuccess)
+      e = pass(sc, static_cast<const char*>(x) + o * row_bytes, b.topk_idx,
+               b.topk_w, -1, w_gate, w_up, w_down,
+               static_cast<char*>(y) + o * row_bytes, b, status_word, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_layer(const moe_config_t* cfg, const void* x,
+                       const float* logits, const void* w_gate,
+                       const void* w_up, const void* w_down, void* y,
+                       moe_mode_t mode, moe_layer_info_t* info,
+                       int32_t* status_word, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (mode != MOE_MODE_FALLBACK_LAYER && mode != MOE_MODE_CAPPED &&
+      mode != MOE_MODE_DROPLESS)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  const int64_t cap = capacity_rows(*cfg);
+  if (info) {
+    info->overflow = -1;
+    info->n_chunks = cfg->T > 0 ? 1 : 0;
+    info->capacity = mode == MOE_MODE_DROPLESS ? -1 : cap;
+  }
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x, true) || !ok_ptr(logits, false) ||
+      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(y, true))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !ok_ptr(workspace, true) ||
+      workspace_bytes < layer_bytes(*cfg, cfg->T))
+    return MOE_ERR_WORKSPACE;
+  const LayerBufs b = carve_layer(workspace, *cfg, cfg->T, nullptr);
+  cudaError_t e = launch_route(*cfg, logits, b.topk_idx, b.topk_w,
+                               status_word, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (mode == MOE_MODE_CAPPED)
+    return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, cap, w_gate, w_up,
+                            w_down, y, b, status_word, stream));
+  if (mode == MOE_MODE_DROPLESS)
+    return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, -1, w_gate, w_up,
+                            w_down, y, b, status_word, stream));
+  // moe_dropless_fallback=layer: check, read the flag, branch.
+  e = launch_check(*cfg, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
+                   b.req, b.cap, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t flag = 0;
+  e = cudaMemcpyAsync(&flag, b.flag, sizeof(flag), cudaMemcpyDeviceToHost,
+                      stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (info) info->overflow = flag;
+  if (!flag)
+    return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, cap, w_gate, w_up,
+                            w_down, y, b, status_word, stream));
+  int32_t n = 0;
+  e = chunked_passes(*cfg, x, b.topk_idx, b.topk_w, w_gate, w_up, w_down, y,
+                     b, status_word, stream, &n);
+  if (info) info->n_chunks = n;
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,646 @@
+// Grouped GEMM SwiGLU expert FFN on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory, operands staged by TMA).
+//
+// "Moe dynamic redundancy" (MaxText pull request 4760), review comments:
+// the expert FFN is a grouped matmul over experts with ragged group_sizes
+// (megablox / gmm), expert weights w0 of shape [E, H, H_ffn].  The SwiGLU
+// form is h = silu(x Wg) * (x Wu), y = h Wd.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0  TMA producer (one thread): A tile [128 rows x 64 k] of the
+//           expert-sorted rows, B tile [64 k x BN] of the expert's weights,
+//           into a STAGES-deep ring of 128-byte-swizzled shared buffers.
+//   warp 1  TMEM owner and MMA issuer (one thread): tcgen05.mma kind::f16,
+//           M=128 x N=BN x K=16, fp32 accumulators in tensor memory, two
+//           accumulators of 256 columns so the epilogue of one tile
+//           overlaps the main loop of the next.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//           row per thread), SwiGLU (GEMM1) or plain (GEMM2), bf16 stores.
+// Tiles are (expert e, n-tile, m-tile) with m innermost: the CTAs running at
+// one time work on the same weight tile of a hot expert, so it comes from
+// HBM once and from L2 after.  Rows past an expert's group end are computed
+// (on the next expert's rows or TMA zero fill) and masked at the store; each
+// output row depends only on its own input row, so that garbage never mixes
+// into a valid row and a row's value does not depend on its tile position.
+//
+// Operand layouts (no repacking of the [E, H, F] / [E, F, H] weights):
+//   A (rows, K-major): TMA box {64 k, 128 rows}, SWIZZLE_128B -> 8-row atoms
+//     of 1024 B; descriptor SBO = 1024, start advanced 32 B per K=16 step.
+//   B (weights, N-major = "MN-major"): TMA box {64 n, 64 k}, SWIZZLE_128B,
+//     one box per 64-column chunk; descriptor LBO = 8192 (next 64-column
+//     chunk), SBO = 1024 (next 8 k-rows), start advanced 2048 B per K=16.
+//   GEMM1 issues one N=256 MMA whose columns 0-127 are the gate projection
+//     and 128-255 the up projection of the same 128 output columns.
+//
+// Every wait is bounded (2 s of %globaltimer); on expiry the kernel raises
+// MOE_DEV_TIMEOUT in the status word, tells the other roles to stop, drains
+// its own TMA loads and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int BN>
+struct Tile {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BK * BN * 2;
+  static constexpr int kStage = kABytes + kBBytes;
+  static constexpr int kChunks = BN / 64;
+};
+
+struct Params {
+  const int32_t* group_offsets;  // [E+1]
+  int E;
+  int K;        // reduction length: H (GEMM1) or F (GEMM2)
+  int n_tiles;  // output column tiles per expert
+  __nv_bfloat16* out;
+  int out_ld;   // F (GEMM1) or H (GEMM2)
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------- PTX ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false when it gave up (or another role already did).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                       volatile int* abort_flag,
+                                       int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m,
+                                            uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t cols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(cols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(cols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 x bf16 -> fp32, one thread issues.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc,
+                                          uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 op this thread issued completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+// TMEM -> registers: 32 columns of one lane per thread, with the wait for
+// completion in the same statement so no use of the registers can be
+// scheduled before it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                            uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (all >> 4), descriptor version 1 at bit 46, and
+// the 128-byte swizzle mode (2) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo,
+                                              uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
+// B bf16 (bits 10-12), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// ------------------------------------------------------------ tiles ------
+// mt_prefix[e] = number of 128-row tiles of experts < e.  Tile index order
+// is (expert, n-tile, m-tile), m fastest.
+__device__ __forceinline__ void decode_tile(int tile, const int* mt_prefix,
+                                            int E, int n_tiles, int& e,
+                                            int& m, int& n) {
+  const int q = tile / n_tiles;
+  int lo = 0, hi = E - 1;  // largest e with mt_prefix[e] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mt_prefix[mid] <= q)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  e = lo;
+  const int mt = mt_prefix[e + 1] - mt_prefix[e];
+  const int local = tile - mt_prefix[e] * n_tiles;
+  n = local / mt;
+  m = local - n * mt;
+}
+
+// All threads: goff[0..E] <- group offsets, mt_prefix[0..E] <- exclusive
+// scan of each expert's 128-row tile count.
+__device__ void build_tile_table(const int32_t* __restrict__ off, int E,
+                                 int* goff, int* mt_prefix, int* wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int a = __ldg(off + e), b = __ldg(off + e + 1);
+    const int mt = b > a ? (b - a + BM - 1) / BM : 0;
+    goff[e] = a;
+    mt_prefix[e] = mt;
+    local += mt;
+  }
+  if (tid == 0) goff[E] = __ldg(off + E);
+  int inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) wsum[w] = inc;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      const int v = wsum[i];
+      wsum[i] = run;
+      run += v;
+    }
+    wsum[kThreads / 32] = run;
+  }
+  __syncthreads();
+  int run = wsum[w] + inc - local;
+  for (int e = e0; e < e1; ++e) {
+    const int v = mt_prefix[e];
+    mt_prefix[e] = run;
+    run += v;
+  }
+  if (tid == 0) mt_prefix[E] = wsum[kThreads / 32];
+  __syncthreads();
+}
+
+// ----------------------------------------------------------- kernel ------
+// MODE 0: out = h = silu(A Wg) * (A Wu), BN = 256 (128 gate + 128 up cols)
+// MODE 1: out = y_sorted = A Wd, BN = 256 or 128
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                  const __grid_constant__ CUtensorMap tmB0,
+                  const __grid_constant__ CUtensorMap tmB1, Params p) {
+  using L = Tile<BN>;
+  static_assert(MODE == 1 || BN == 256, "GEMM1 tile is 128 gate + 128 up");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * L::kStage);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [8]
+  int* goff = wsum + 8;                                // [E+1]
+  int* mt_prefix = goff + (p.E + 1);                   // [E+1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      mbar_init(smem_u32(tempty + a), kEpilogueThreads);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (MODE == 0) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  build_tile_table(p.group_offsets, p.E, goff, mt_prefix, wsum);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = mt_prefix[p.E] * p.n_tiles;
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer -----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles;
+           tile += gridDim.x) {
+        int e, m, n;
+        decode_tile(tile, mt_prefix, p.E, p.n_tiles, e, m, n);
+        const int a_row = goff[e] + m * BM;
+        const int b_row = e * p.K;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_expect_tx(fb, L::kStage);
+          const uint32_t sa = smem_base + stage * L::kStage;
+          const uint32_t sb = sa + L::kABytes;
+          tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
+          if (MODE == 0) {
+            tma_load_2d(sb, &tmB0, fb, n * 128, b_row + kb * BK);
+            tma_load_2d(sb + 8192, &tmB0, fb, n * 128 + 64, b_row + kb * BK);
+            tma_load_2d(sb + 16384, &tmB1, fb, n * 128, b_row + kb * BK);
+            tma_load_2d(sb + 24576, &tmB1, fb, n * 128 + 64, b_row + kb * BK);
+          } else {
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_2d(sb + c * 8192, &tmB0, fb, n * BN + c * 64,
+                          b_row + kb * BK);
+          }
+          ++fills;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every load this thread issued has landed before exit.
+      const long long first = fills > STAGES ? fills - STAGES : 0;
+      for (long long f = first; f < fills; ++f)
+        mbar_wait(smem_u32(full + (f % STAGES)),
+                  static_cast<uint32_t>((f / STAGES) & 1), abort_flag,
+                  p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer -------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles;
+           tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag,
+                       p.status))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * L::kStage;
+          const uint32_t sb = sa + L::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(empty + stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(tfull + acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Drain: all MMAs issued by this thread are complete.
+      umma_commit(smem_u32(done));
+      mbar_wait(smem_u32(done), 0, abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------ epilogue ---------
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int e, m, n;
+      decode_tile(tile, mt_prefix, p.E, p.n_tiles, e, m, n);
+      bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
+                          p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int grow = goff[e] + m * BM + row;
+      const bool valid = grow < goff[e + 1];
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      if (MODE == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<long long>(grow) * p.out_ld + n * 128);
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32x2(taddr + c, taddr + 128 + c, g, u);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]);
+            const float g1 = __uint_as_float(g[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) *
+                             __uint_as_float(u[2 * i]);
+            const float h1 = g1 / (1.0f + __expf(-g1)) *
+                             __uint_as_float(u[2 * i + 1]);
+            pk[i] = pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
+                                          pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<long long>(grow) * p.out_ld + n * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
+                                __uint_as_float(r[2 * i + 1]));
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
+                                          pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(tempty + acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- host ------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                 void*, const cuuint64_t*, const cuuint64_t*,
+                                 const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+size_t smem_bytes(int E) {
+  return 1024 + STAGES * Tile<BN>::kStage + 8 * (2 * STAGES + 5) + 16 +
+         4 * (8 + 2 * (E + 1)) + 64;
+}
+
+template <int MODE, int BN>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
+                       const CUtensorMap& b1, const Params& p,
+                       cudaStream_t s) {
+  const size_t smem = smem_bytes<BN>(p.E);
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(gmm_tc_kernel<MODE, BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  gmm_tc_kernel<MODE, BN><<<sms, kThreads, smem, s>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+bool gmm_tc_supported(const moe_config_t& c) {
+  return c.dtype == MOE_BF16 && c.H % 128 == 0 && c.F % 128 == 0 &&
+         c.H >= 128 && c.F >= 128;
+}
+
+cudaError_t launch_gmm_bf16(const moe_config_t& c, const void* x_sorted,
+                            const int32_t* group_offsets, const void* w_gate,
+                            const void* w_up, const void* w_down, void* h,
+                            void* y_sorted, int32_t* status, cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap a1, bg, bu, a2, bd;
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  if (!tc::make_map(&a1, x_sorted, c.H, rows, 64, tc::BM) ||
+      !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, 64) ||
+      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, 64) ||
+      !tc::make_map(&a2, h, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, 64))
+    return cudaErrorInvalidValue;
+  tc::Params p1{group_offsets, c.E, c.H, c.F / 128,
+                static_cast<__nv_bfloat16*>(h), c.F, status};
+  cudaError_t err = tc::launch_one<0, 256>(a1, bg, bu, p1, s);
+  if (err != cudaSuccess) return err;
+  if (c.H % 256 == 0) {
+    tc::Params p2{group_offsets, c.E, c.F, c.H / 256,
+                  static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
+    return tc::launch_one<1, 256>(a2, bd, bd, p2, s);
+  }
+  tc::Params p2{group_offsets, c.E, c.F, c.H / 128,
+                static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
+  return tc::launch_one<1, 128>(a2, bd, bd, p2, s);
+}
+
+}  // namespace moe

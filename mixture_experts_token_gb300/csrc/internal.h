@@ -1,0 +1,86 @@
+// Internal declarations shared by the CUDA translation units of
+// libmoe_gb300.so.  Nothing here is part of the C ABI (include/moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include <algorithm>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Token block of the counting-sort permute: one thread per token.
+constexpr int kPermuteTokensPerBlock = 128;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxShards = 64;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int elem_bytes(moe_dtype_t d) { return d == MOE_F32 ? 4 : 2; }
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Bump allocator over a caller-provided workspace (no device allocation).
+struct Carve {
+  char* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+// Permute scratch for `T` tokens (counting-sort block tables).
+struct PermuteScratch {
+  int32_t* block_base;  // [nb, E] per-block expert counts, then bases
+  int32_t* kept;        // [E] kept rows per expert
+  int32_t* goff;        // [E] kept group offsets
+  int32_t* block_ucnt;  // [nb, S] per-block unique counts, then bases
+  int32_t* urank;       // [T*k] rank of (t,j)'s token inside its block/shard
+  int32_t* scal;        // [4] scalars
+};
+size_t permute_scratch_bytes(int T, int E, int k, int S);
+PermuteScratch carve_permute_scratch(Carve& c, int T, int E, int k, int S);
+
+// Device work of each entry point, already validated.
+cudaError_t launch_route(const moe_config_t& c, const float* logits,
+                         int32_t* topk_idx, float* topk_w, int32_t* status,
+                         cudaStream_t s);
+cudaError_t launch_check(const moe_config_t& c, const int32_t* topk_idx,
+                         int32_t* counts, int32_t* offsets, int32_t* shard,
+                         int32_t* flag, float* req, int32_t* cap,
+                         cudaStream_t s);
+cudaError_t launch_permute(const moe_config_t& c, const void* x,
+                           const int32_t* topk_idx, int64_t cap,
+                           void* x_sorted, int32_t* row_of,
+                           int32_t* sorted_token, int32_t* group_offsets,
+                           int32_t* uniq_offsets, int32_t* uniq_tokens,
+                           int32_t* expand_idx, int32_t* n_dropped,
+                           const PermuteScratch& ws, int32_t* status,
+                           cudaStream_t s);
+cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
+                       const int32_t* group_offsets, const void* w_gate,
+                       const void* w_up, const void* w_down, void* h,
+                       void* y_sorted, int32_t* status, cudaStream_t s);
+cudaError_t launch_combine(const moe_config_t& c, const void* y_sorted,
+                           const int32_t* row_of, const float* topk_w,
+                           void* y, cudaStream_t s);
+
+// Shape support of the bf16 tensor-core GEMM.
+bool gmm_tc_supported(const moe_config_t& c);
+
+// Host-side formulas shared by validation and drivers.
+int64_t capacity_rows(const moe_config_t& c);
+int32_t chunk_tokens(const moe_config_t& c);
+
+}  // namespace moe

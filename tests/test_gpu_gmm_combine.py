@@ -1,0 +1,141 @@
+"""GPU parity: the grouped SwiGLU GEMM and the weighted combine.
+
+Inputs are synthetic (rows, ragged group sizes, weights); the oracle's
+float64 grouped FFN and combine are the reference.  Tolerance: normwise
+2e-2 for bf16, 1e-4 for fp32, per output tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_token_gb300 as moe
+from oracle import moe_ref as ref
+from tests.gpu_util import TOL, f64, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def make_gmm_case(sizes, H, F, k_rows, dtype, seed=0, std=0.05):
+    """x_sorted with len(sizes) ragged groups; rows beyond the groups (up to
+    the allocation of T*k rows) are filled with NaN to prove they never leak
+    into a valid row."""
+    E = len(sizes)
+    R = int(sum(sizes))
+    alloc = max(k_rows, R)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    xs = torch.full((alloc, H), float("nan"), device="cuda", dtype=dt)
+    xs[:R] = torch.randn(R, H, generator=g, device="cuda").to(dt)
+    wg = (torch.randn(E, H, F, generator=g, device="cuda") * std).to(dt)
+    wu = (torch.randn(E, H, F, generator=g, device="cuda") * std).to(dt)
+    wd = (torch.randn(E, F, H, generator=g, device="cuda") * std).to(dt)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    return xs, torch.from_numpy(off).cuda(), wg, wu, wd, off, alloc
+
+
+def run_gmm(sizes, H, F, dtype, T=None, k=1, seed=0):
+    E = len(sizes)
+    R = int(sum(sizes))
+    T = T if T is not None else R
+    xs, goff, wg, wu, wd, off, alloc = make_gmm_case(sizes, H, F, T * k,
+                                                     dtype, seed)
+    cfg = moe.make_config(T, H, E, k, F, 1, 2.0, 0, dtype)
+    dt = xs.dtype
+    h = torch.zeros((alloc, F), dtype=dt, device="cuda")
+    ys = torch.zeros((alloc, H), dtype=dt, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_gmm_swiglu(cfg, xs, goff, wg, wu, wd, h, ys, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return xs, off, (wg, wu, wd), h, ys, R
+
+
+GMM_CASES = [
+    # (group sizes, H, F): empty groups, single rows, tile edges, many tiles
+    ([0, 1, 127, 128, 129, 300], 256, 256),
+    ([5, 0, 0, 700, 3], 384, 128),          # H % 256 != 0: 128-wide GEMM2
+    ([128] * 4, 128, 128),
+    ([1000], 512, 384),
+    ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512),
+]
+
+
+@pytest.mark.parametrize("case", GMM_CASES, ids=lambda c: f"{len(c[0])}x{c[1]}x{c[2]}")
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gmm_parity(case, dtype):
+    sizes, H, F = case
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, dtype)
+    want_h, want_y = ref.grouped_ffn(f64(xs[:R]), off,
+                                     ref.dense_weights(f64(wg), f64(wu),
+                                                       f64(wd)))
+    tol = TOL[dtype]
+    assert ref.normwise_error(f64(h[:R]), want_h) <= tol
+    assert ref.normwise_error(f64(ys[:R]), want_y) <= tol
+    # no row outside the groups was written
+    assert torch.all(h[R:] == 0) and torch.all(ys[R:] == 0)
+    # each group on its own scale
+    for e in range(len(sizes)):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            assert ref.normwise_error(f64(ys[a:b]), want_y[a:b]) <= tol
+
+
+def test_gmm_small_layer_shape():
+    """Zipf-like group sizes at the small layer's dims (H=1024, F=2048)."""
+    sizes = [2900, 1600, 1100, 800, 560, 420, 300, 190, 120, 80, 50, 30, 20,
+             12, 5, 1]
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, 1024, 2048, "bf16",
+                                              T=4096, k=2)
+    want_h, want_y = ref.grouped_ffn(f64(xs[:R]), off,
+                                     ref.dense_weights(f64(wg), f64(wu),
+                                                       f64(wd)))
+    assert ref.normwise_error(f64(h[:R]), want_h) <= 2e-2
+    assert ref.normwise_error(f64(ys[:R]), want_y) <= 2e-2
+
+
+def test_gmm_row_result_independent_of_tile_position():
+    """The same row computed at a different offset inside its 128-row tile
+    gives the same bits (this makes chunked and dropless passes agree
+    exactly)."""
+    H, F = 256, 256
+    sizes = [200, 77, 300]
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=5)
+    shift = 37
+    xs2 = torch.cat([torch.randn(shift, H, device="cuda").to(xs.dtype),
+                     xs[:R]])
+    off2 = torch.from_numpy(np.concatenate(
+        [[0], np.cumsum([sizes[0] + shift] + sizes[1:])]).astype(np.int32)
+    ).cuda()
+    cfg = moe.make_config(R + shift, H, 3, 1, F, 1, 2.0, 0, "bf16")
+    h2 = torch.empty((R + shift, F), dtype=xs.dtype, device="cuda")
+    ys2 = torch.empty((R + shift, H), dtype=xs.dtype, device="cuda")
+    moe.moe_gmm_swiglu(cfg, xs2, off2, wg, wu, wd, h2, ys2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2[shift:], h[:R])
+    assert torch.equal(ys2[shift:], ys[:R])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("k", [1, 2, 8, 13])
+def test_combine_parity(dtype, k):
+    rng = np.random.default_rng(k)
+    T, E, S, H = 1500, 16, 4, 256 if dtype == "bf16" else 64
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    L[:, :3] += 1.0
+    oi, ow, _ = ref.route(L, k)
+    # cap at half the balanced load so rows are dropped (some tokens lose all)
+    C = ref.capacity(T, k, S, 0.5)
+    p = ref.permute_indices(oi, E, S, C)
+    R = int(p.group_offsets[-1])
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    ys = torch.randn(T * k, H, device="cuda").to(dt)
+    cfg = moe.make_config(T, H, E, k, 128, S, 0.5, 0, dtype)
+    row_of = torch.from_numpy(p.row_of.astype(np.int32)).cuda()
+    w = torch.from_numpy(ow.astype(np.float32)).cuda()
+    y = torch.empty((T, H), dtype=dt, device="cuda")
+    moe.moe_combine(cfg, ys, row_of, w, y)
+    torch.cuda.synchronize()
+    want = ref.combine(f64(ys[:R]), p.row_of, ow.astype(np.float32), H)
+    assert ref.normwise_error(f64(y), want) <= TOL[dtype]
+    gone = np.all(p.row_of < 0, axis=1)
+    assert gone.any() and torch.all(y[torch.from_numpy(gone).cuda()] == 0)
