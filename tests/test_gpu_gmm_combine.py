@@ -138,4 +138,6 @@ def test_combine_parity(dtype, k):
     want = ref.combine(f64(ys[:R]), p.row_of, ow.astype(np.float32), H)
     assert ref.normwise_error(f64(y), want) <= TOL[dtype]
     gone = np.all(p.row_of < 0, axis=1)
-    assert gone.any() and torch.all(y[torch.from_numpy(gone).cuda()] == 0)
+    if k <= 2:   # with few slots some tokens lose every row
+        assert gone.any()
+    assert torch.all(y[torch.from_numpy(gone).cuda()] == 0)
