@@ -1,0 +1,603 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer (token dispatch + expert compute) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dsv3|l4mav|small|tiny|profile]
+
+One step = one pass of the whole layer over one batch of T tokens whose
+inputs (x, router logits, expert weights) are already in HBM:
+route -> counts + overflow check -> flag read -> capped path, or the chunked
+dropless fallback when a shard overflows -> (per pass) permute + dedup ->
+GEMM1 + SwiGLU -> GEMM2 -> combine.  The default workload is the
+DeepSeek-V3-shaped layer (T=8192, H=7168, E=256, k=8, F=2048, 8 shards,
+Zipf s=1.2 routing, ragged_buffer_factor 2.0), on which the grouped GEMM
+target is stated.
+
+The timed loop calls the C ABI entry points in the order moe_layer runs them
+(the check that both give identical bits is part of the run), with CUDA
+events on the launch stream around every launch group, so the per-kernel
+durations of the roofline come from the same timed region.  L2 is flushed
+(a 256 MiB write) between steps, outside the events.  ``e2e`` is the same
+metric through moe_layer with pinned host buffers, the host->device copies
+of x and the logits and the device->host copy of y inside the timed region.
+``cpu_baseline`` is the float64 oracle timed on a bounded token sample of the
+same workload on the host cores.  With torchrun (N > 1) every rank runs an
+independent replica on its own tokens (weak scaling, no collective on the
+data path); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# BLAS threads for the oracle: every core this process may use.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") \
+    else (os.cpu_count() or 1)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from synth import WORKLOADS, make_logits, make_weights, make_x  # noqa: E402
+
+METRIC = "MoE layer tokens/sec at 1 GB300; permute GB/s and GMM TFLOP/s vs roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+# bench-only workload for profiling captures: the DeepSeek-V3 layer shape with
+# 32 experts and 1024 tokens (2.8 GB of weights: larger than L2, a few GB in
+# total on the device)
+PROFILE_WL = WORKLOADS["dsv3"].with_(name="profile_dsv3_e32", T=1024, E=32)
+
+# oracle sample sizes (tokens) for the CPU baseline and the reference arm
+CPU_SAMPLE = {"dsv3": 32, "l4mav": 32, "small": 1024, "tiny": 256,
+              "profile_dsv3_e32": 32}
+REF_SAMPLE = {"dsv3": 8, "l4mav": 8, "small": 256, "tiny": 256,
+              "profile_dsv3_e32": 8}
+
+
+def workload_by_name(name):
+    if name == "profile":
+        return PROFILE_WL
+    return WORKLOADS[name]
+
+
+# ------------------------------------------------------------------ peaks --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_token_gb300", "csrc",
+                       "gmm_tc.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+        want = None
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_launch:"):
+                parts = line.split()
+                if len(parts) >= 4 and parts[3] == digest:
+                    want = float(parts[1])
+        return want
+    except OSError:
+        return None
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.device = device
+
+    def _id(self):
+        try:
+            u = str(torch.cuda.get_device_properties(self.device).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.device)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self._id()}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ the layer ---
+class Layer:
+    """Inputs in HBM and every buffer of the stepwise calls."""
+
+    def __init__(self, wl, device, seed_offset=0):
+        import mixture_experts_token_gb300 as moe
+        self.moe = moe
+        self.wl = wl.with_(seed=wl.seed + seed_offset)
+        w = self.wl
+        self.cfg = moe.make_config(w.T, w.H, w.E, w.k, w.F, w.S, w.factor,
+                                   w.n_chunks, w.dtype, w.renorm)
+        self.x = make_x(w, device)
+        L = make_logits(w, self.x if w.routing == "router" else None)
+        self.logits_np = L
+        self.logits = torch.from_numpy(L).to(device)
+        self.W = make_weights(w, device)
+        self.b = moe.alloc_step_buffers(self.cfg, device)
+        self.b["y"].zero_()
+        self.ws = moe.layer_workspace(self.cfg, moe.MOE_WS_LAYER, device)
+        self.chunk = moe.moe_chunk_tokens(self.cfg)
+
+    def sub(self, t0, t1, capped):
+        """Pass over tokens [t0, t1): the config the library uses."""
+        if capped:
+            return self.cfg
+        return self.cfg.with_(T=t1 - t0, ragged_buffer_factor=-1.0,
+                              n_chunks=0)
+
+    def step(self, ev=None):
+        """One layer step through the entry points; ev(name) marks stages.
+        Returns the list of passes (t0, t1, capped)."""
+        moe, b, c, W = self.moe, self.b, self.cfg, self.W
+        mark = ev or (lambda name: None)
+        mark("route")
+        moe.moe_route(c, self.logits, b["topk_idx"], b["topk_w"], b["status"])
+        mark("check")
+        moe.moe_check_overflow(c, b["topk_idx"], b["expert_counts"],
+                               b["expert_offsets"], b["shard_counts"],
+                               b["overflow_flag"], b["required_factor"],
+                               b["capacity"])
+        mark("flag")
+        flag = int(b["overflow_flag"].item())
+        if not flag:
+            passes = [(0, c.T, True)]
+        else:
+            passes = [(t0, min(c.T, t0 + self.chunk), False)
+                      for t0 in range(0, c.T, self.chunk)]
+        for (t0, t1, capped) in passes:
+            sc = self.sub(t0, t1, capped)
+            mark("permute")
+            moe.moe_permute(sc, self.x[t0:t1], b["topk_idx"][t0:t1], capped,
+                            b["x_sorted"], b["row_of"], b["sorted_token"],
+                            b["group_offsets"], b["uniq_offsets"],
+                            b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
+                            b["permute_ws"])
+            mark("gmm_gate_up")
+            moe.moe_gmm_gate_up(sc, b["x_sorted"], b["group_offsets"], W[0],
+                                W[1], b["h"], b["status"])
+            mark("gmm_down")
+            moe.moe_gmm_down(sc, b["h"], b["group_offsets"], W[2],
+                             b["y_sorted"], b["status"])
+            mark("combine")
+            moe.moe_combine(sc, b["y_sorted"], b["row_of"],
+                            b["topk_w"][t0:t1], b["y"][t0:t1])
+        mark(None)
+        return passes
+
+    def api_layer(self, x, logits, y):
+        return self.moe.moe_layer(self.cfg, x, logits, *self.W, y,
+                                  self.moe.MOE_MODE_FALLBACK_LAYER, self.ws,
+                                  self.b["status"])
+
+
+class StageTimer:
+    """CUDA events on the current stream between consecutive stage marks."""
+
+    def __init__(self):
+        self.events = []
+        self.names = []
+
+    def __call__(self, name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.events.append(e)
+        self.names.append(name)
+
+    def durations(self):
+        out = []
+        for i in range(len(self.events) - 1):
+            if self.names[i] is None:
+                continue
+            out.append((self.names[i],
+                        self.events[i].elapsed_time(self.events[i + 1])))
+        return out
+
+
+def launches_per_step(passes, T):
+    """Kernel launches of one step: route 1 + check 1, then per pass
+    permute 5 (block counts, expert scan, assign, dedup scan, row scatter),
+    GEMM1 1, GEMM2 1, combine 1."""
+    return 2 + sum(8 for (t0, t1, _) in passes if t1 > t0)
+
+
+def pass_accounting(layer, passes):
+    """Rows and active experts of each pass (bench bookkeeping with torch,
+    outside any timed region)."""
+    w = layer.wl
+    idx = layer.b["topk_idx"].long()
+    C = layer.moe.moe_capacity_rows(layer.cfg)
+    out = []
+    for (t0, t1, capped) in passes:
+        sub = idx[t0:t1].reshape(-1)
+        counts = torch.bincount(sub, minlength=w.E).cpu().numpy()
+        if capped and C >= 0:
+            Es = w.E // w.S
+            kept = np.zeros_like(counts)
+            for s in range(w.S):
+                room = C
+                for e in range(s * Es, (s + 1) * Es):
+                    kept[e] = min(counts[e], max(room, 0))
+                    room -= counts[e]
+            counts = kept
+        out.append({"T": t1 - t0, "R": int(counts.sum()),
+                    "E_act": int((counts > 0).sum())})
+    return out
+
+
+def stage_work(w, acc):
+    """Algorithmic bytes and flops of each stage for one pass."""
+    b = 2 if w.dtype == "bf16" else 4
+    T, R, Ea = acc["T"], acc["R"], acc["E_act"]
+    H, F, k = w.H, w.F, w.k
+    return {
+        "permute": {"bytes": T * H * b + R * H * b + 16 * R, "flops": 0},
+        "gmm_gate_up": {"bytes": 2 * Ea * H * F * b + R * H * b + R * F * b,
+                        "flops": 4 * R * H * F},
+        "gmm_down": {"bytes": Ea * F * H * b + R * F * b + R * H * b,
+                     "flops": 2 * R * F * H},
+        "combine": {"bytes": R * H * b + T * H * b + T * k * 8, "flops": 0},
+    }
+
+
+# ------------------------------------------------------------ the oracle --
+def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0):
+    """Runs the oracle layer on tokens [t0, t0+n_tok) as a batch of its own
+    (same shape parameters and factor); returns (seconds, tokens)."""
+    from oracle import moe_ref as ref
+    n_tok = min(n_tok, wl.T - t0)
+    xs = x_dev[t0:t0 + n_tok].to("cpu", torch.float64).numpy()
+    Ls = L[t0:t0 + n_tok]
+    oi, _, _ = ref.route(Ls, wl.k, wl.renorm)
+    touched = sorted(set(int(e) for e in oi.reshape(-1)))
+    host = {e: (W[0][e].cpu(), W[1][e].cpu(), W[2][e].cpu()) for e in touched}
+
+    def weights(e):
+        g, u, d = host[e]
+        return (g.to(torch.float64).numpy(), u.to(torch.float64).numpy(),
+                d.to(torch.float64).numpy())
+    cfg = ref.MoEConfig(n_tok, wl.H, wl.E, wl.k, wl.F, wl.S, wl.factor,
+                        wl.n_chunks, wl.renorm)
+    t = time.perf_counter()
+    ref.layer(cfg, xs, Ls, weights)
+    return time.perf_counter() - t, n_tok
+
+
+# ------------------------------------------------------------ main -------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3",
+                    choices=["dsv3", "l4mav", "small", "tiny", "profile"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = workload_by_name(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, wl, device)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    layer = Layer(wl, device, seed_offset=rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    # identical bits: stepwise entry points vs the moe_layer call
+    y_api = torch.empty_like(layer.b["y"])
+    info = layer.api_layer(layer.x, layer.logits, y_api)
+    passes = layer.step()
+    torch.cuda.synchronize()
+    if not torch.equal(y_api, layer.b["y"]):
+        raise SystemExit("stepwise path and moe_layer disagree")
+    if int(layer.b["status"].item()) != 0:
+        raise SystemExit(f"device status {int(layer.b['status'].item())}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = ClockSampler(device)
+    timers = []
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        st = StageTimer()
+        passes = layer.step(st)
+        timers.append(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    clock_rec = clocks.stop()
+
+    step_ms = [sum(d for _, d in st.durations()) for st in timers]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([mean_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+
+    # per-stage durations
+    stage = {}
+    for st in timers:
+        for name, d in st.durations():
+            s = stage.setdefault(name, {"ms": 0.0, "n": 0})
+            s["ms"] += d
+            s["n"] += 1
+    acc = pass_accounting(layer, passes)
+    work = {}
+    for a in acc:
+        for name, wv in stage_work(layer.wl, a).items():
+            t = work.setdefault(name, {"bytes": 0, "flops": 0})
+            t["bytes"] += wv["bytes"]
+            t["flops"] += wv["flops"]
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for name, s in stage.items():
+        per_step = s["ms"] / args.steps
+        ent = {"ms_per_step": round(per_step, 4),
+               "launch_groups_per_step": s["n"] // args.steps,
+               "share": round(per_step / mean_ms, 4)}
+        if name in work:
+            wv = work[name]
+            sec = per_step / 1e3
+            ent["GBps"] = round(wv["bytes"] / sec / 1e9, 1)
+            if wv["flops"]:
+                ent["TFLOPs"] = round(wv["flops"] / sec / 1e12, 1)
+        kernels[name] = ent
+
+    dom = max((n for n in work), key=lambda n: stage[n]["ms"])
+    wv = work[dom]
+    n_launch = len(passes)
+    dur = stage[dom]["ms"] / args.steps / n_launch / 1e3     # per launch
+    bytes_l, flops_l = wv["bytes"] / n_launch, wv["flops"] / n_launch
+    t_mem = bytes_l / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops_l / (peaks["bf16_tflops_sustained"] * 1e12) if flops_l else 0
+    if t_mem >= t_flop:
+        achieved = bytes_l / dur / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = flops_l / dur / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = round(achieved / roof["peak"], 4)
+    roof["traffic"] = profiled_traffic(dom, layer.wl.name)
+    roof["kernel"] = dom
+    roof["algorithmic_bytes_per_launch"] = int(bytes_l)
+    roof["algorithmic_flops_per_launch"] = int(flops_l)
+    roof["launch_ms"] = round(dur * 1e3, 4)
+    roof["peak_source"] = f"{peak_src} MEASURED_PEAKS.json" \
+        if peak_src == "measured" else "fallback"
+
+    # e2e through moe_layer with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_run(layer, args, world, device)
+
+    out = {
+        "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": layer.wl.dtype,
+        "data": "synthetic (seeded; Zipf/uniform expert popularity via "
+                "Gumbel-max router logits; random N(0,0.02) expert weights)",
+        "config": {
+            "workload": layer.wl.name, "T": layer.wl.T, "H": layer.wl.H,
+            "E": layer.wl.E, "k": layer.wl.k, "F": layer.wl.F,
+            "S": layer.wl.S, "ragged_buffer_factor": layer.wl.factor,
+            "routing": layer.wl.routing + (f" s={layer.wl.zipf_s}"
+                                           if layer.wl.routing == "zipf"
+                                           else ""),
+            "mode": "moe_dropless_fallback=layer",
+            "overflow": info["overflow"], "passes": len(passes),
+            "capacity": info["capacity"],
+            "l2": "flushed between steps (256 MiB write, outside the events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "wall_s_timed_loop": round(wall, 3),
+        "gpu_launches": launches_per_step(passes, layer.wl.T) * args.steps,
+        "kernels": kernels,
+        "roofline": roof,
+    }
+    out["value"] = round(world * layer.wl.T / (mean_ms / 1e3), 1)
+    if clock_rec:
+        out["clocks"] = clock_rec
+    if e2e:
+        out["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(layer)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_run(layer, args, world, device):
+    x_h = layer.x.cpu().pin_memory()
+    L_h = layer.logits.cpu().pin_memory()
+    y_h = torch.empty(layer.b["y"].shape, dtype=layer.b["y"].dtype,
+                      pin_memory=True)
+    x_d = torch.empty_like(layer.x)
+    L_d = torch.empty_like(layer.logits)
+    y_d = torch.empty_like(layer.b["y"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def one():
+        x_d.copy_(x_h, non_blocking=True)
+        L_d.copy_(L_h, non_blocking=True)
+        layer.api_layer(x_d, L_d, y_d)
+        y_h.copy_(y_d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), \
+            torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    mean = sum(ms) / len(ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([mean], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean = float(t.item())
+    h2d = x_h.numel() * x_h.element_size() + L_h.numel() * L_h.element_size()
+    d2h = y_h.numel() * y_h.element_size()
+    return {"value": round(world * layer.wl.T / (mean / 1e3), 1),
+            "unit": UNIT, "ms_per_step": round(mean, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "moe_layer (C ABI), pinned host buffers"}
+
+
+def cpu_baseline(layer):
+    wl = layer.wl
+    n = CPU_SAMPLE.get(wl.name, 32)
+    sec, n = oracle_sample_run(wl, layer.x, layer.logits_np, layer.W, n)
+    return {"value": round(n / sec, 4), "unit": UNIT, "cores": _CORES,
+            "kind": "oracle",
+            "sample": f"first {n} tokens of the {wl.name} batch run as a "
+                      f"layer of their own (same H, E, k, F, S, factor; "
+                      f"float64 numpy oracle incl. routing, check, fallback, "
+                      f"FFN and combine); {sec:.1f} s"}
+
+
+def reference_arm(args, wl, device):
+    """The float64 oracle as the reference implementation, on host cores."""
+    x = make_x(wl, device)
+    L = make_logits(wl, x if wl.routing == "router" else None)
+    W = make_weights(wl, device)
+    n = REF_SAMPLE.get(wl.name, 8)
+    for i in range(args.warmup):
+        oracle_sample_run(wl, x, L, W, n, t0=(i * n) % max(1, wl.T - n))
+    secs = []
+    toks = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s, m = oracle_sample_run(wl, x, L, W, n,
+                                 t0=((args.warmup + i) * n) % max(1, wl.T - n))
+        secs.append(s)
+        toks += m
+    wall = time.perf_counter() - t0
+    value = toks / sum(secs)
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4),
+           "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E,
+                      "k": wl.k, "F": wl.F, "S": wl.S,
+                      "ragged_buffer_factor": wl.factor,
+                      "sample_tokens_per_step": n},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
+                            "cores": _CORES, "kind": "oracle",
+                            "sample": f"{n} tokens of the {wl.name} batch per "
+                                      f"step as a layer of their own"},
+           "e2e": {"value": round(value, 4), "unit": UNIT,
+                   "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "wall_s": round(wall, 2)}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -192,6 +192,18 @@ moe_status_t moe_gmm_swiglu(const moe_config_t *cfg, const void *x_sorted,
                             const void *w_down, void *h, void *y_sorted,
                             int32_t *status_word, moe_stream_t stream);
 
+/* The two halves of moe_gmm_swiglu, one kernel launch each (same rules):
+ * moe_gmm_gate_up writes h = silu(x_sorted w_gate[e]) * (x_sorted w_up[e]);
+ * moe_gmm_down writes y_sorted = h w_down[e].                             */
+moe_status_t moe_gmm_gate_up(const moe_config_t *cfg, const void *x_sorted,
+                             const int32_t *group_offsets,
+                             const void *w_gate, const void *w_up, void *h,
+                             int32_t *status_word, moe_stream_t stream);
+moe_status_t moe_gmm_down(const moe_config_t *cfg, const void *h,
+                          const int32_t *group_offsets, const void *w_down,
+                          void *y_sorted, int32_t *status_word,
+                          moe_stream_t stream);
+
 /* ----------------------------------------------------------------------
  * moe_combine -- weighted unpermute [PR4969 What: the combine reduces the
  * expert outputs back to tokens].  y[t] = sum_{j<k, row_of[t,j] >= 0}

@@ -82,6 +82,8 @@ def _declare(h):
         "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
                         c_size_t, P],
         "moe_gmm_swiglu": [cfg, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_gate_up": [cfg, P, P, P, P, P, P, P],
+        "moe_gmm_down": [cfg, P, P, P, P, P, P],
         "moe_combine": [cfg, P, P, P, P, P],
         "moe_layer_dropless_chunked": [cfg, P, P, P, P, P, P, P, P, c_size_t,
                                        P],
@@ -202,6 +204,21 @@ def moe_gmm_swiglu(cfg, x_sorted, group_offsets, w_gate, w_up, w_down, h,
         ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets),
         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(h), _ptr(y_sorted),
         _ptr(status_word), _stream(stream)), "moe_gmm_swiglu")
+
+
+def moe_gmm_gate_up(cfg, x_sorted, group_offsets, w_gate, w_up, h,
+                    status_word=None, stream=None):
+    _check(lib().moe_gmm_gate_up(
+        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
+        _ptr(w_up), _ptr(h), _ptr(status_word), _stream(stream)),
+        "moe_gmm_gate_up")
+
+
+def moe_gmm_down(cfg, h, group_offsets, w_down, y_sorted, status_word=None,
+                 stream=None):
+    _check(lib().moe_gmm_down(
+        ctypes.byref(cfg), _ptr(h), _ptr(group_offsets), _ptr(w_down),
+        _ptr(y_sorted), _ptr(status_word), _stream(stream)), "moe_gmm_down")
 
 
 def moe_combine(cfg, y_sorted, row_of, topk_w, y, stream=None):

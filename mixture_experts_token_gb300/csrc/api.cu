@@ -16,14 +16,19 @@
 
 namespace moe {
 
-cudaError_t launch_gmm_f32(const moe_config_t& c, const void* x_sorted,
-                           const int32_t* group_offsets, const void* w_gate,
-                           const void* w_up, const void* w_down, void* h,
-                           void* y_sorted, cudaStream_t s);
-cudaError_t launch_gmm_bf16(const moe_config_t& c, const void* x_sorted,
+cudaError_t launch_gmm1_f32(const moe_config_t& c, const void* x_sorted,
                             const int32_t* group_offsets, const void* w_gate,
-                            const void* w_up, const void* w_down, void* h,
-                            void* y_sorted, int32_t* status, cudaStream_t s);
+                            const void* w_up, void* h, cudaStream_t s);
+cudaError_t launch_gmm2_f32(const moe_config_t& c, const void* h,
+                            const int32_t* group_offsets, const void* w_down,
+                            void* y_sorted, cudaStream_t s);
+cudaError_t launch_gmm1_bf16(const moe_config_t& c, const void* x_sorted,
+                             const int32_t* group_offsets, const void* w_gate,
+                             const void* w_up, void* h, int32_t* status,
+                             cudaStream_t s);
+cudaError_t launch_gmm2_bf16(const moe_config_t& c, const void* h,
+                             const int32_t* group_offsets, const void* w_down,
+                             void* y_sorted, int32_t* status, cudaStream_t s);
 
 int64_t capacity_rows(const moe_config_t& c) {
   const double f = static_cast<double>(c.ragged_buffer_factor);
@@ -53,15 +58,32 @@ int32_t chunk_tokens(const moe_config_t& c) {
   return static_cast<int32_t>(std::min<int64_t>(tok, c.T));
 }
 
+cudaError_t launch_gmm1(const moe_config_t& c, const void* x_sorted,
+                        const int32_t* group_offsets, const void* w_gate,
+                        const void* w_up, void* h, int32_t* status,
+                        cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_gmm1_f32(c, x_sorted, group_offsets, w_gate, w_up, h, s);
+  return launch_gmm1_bf16(c, x_sorted, group_offsets, w_gate, w_up, h, status,
+                          s);
+}
+
+cudaError_t launch_gmm2(const moe_config_t& c, const void* h,
+                        const int32_t* group_offsets, const void* w_down,
+                        void* y_sorted, int32_t* status, cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_gmm2_f32(c, h, group_offsets, w_down, y_sorted, s);
+  return launch_gmm2_bf16(c, h, group_offsets, w_down, y_sorted, status, s);
+}
+
 cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
                        const int32_t* group_offsets, const void* w_gate,
                        const void* w_up, const void* w_down, void* h,
                        void* y_sorted, int32_t* status, cudaStream_t s) {
-  if (c.dtype == MOE_F32)
-    return launch_gmm_f32(c, x_sorted, group_offsets, w_gate, w_up, w_down, h,
-                          y_sorted, s);
-  return launch_gmm_bf16(c, x_sorted, group_offsets, w_gate, w_up, w_down, h,
-                         y_sorted, status, s);
+  cudaError_t e =
+      launch_gmm1(c, x_sorted, group_offsets, w_gate, w_up, h, status, s);
+  if (e != cudaSuccess) return e;
+  return launch_gmm2(c, h, group_offsets, w_down, y_sorted, status, s);
 }
 
 namespace {
@@ -335,6 +357,38 @@ moe_status_t moe_gmm_swiglu(const moe_config_t* cfg, const void* x_sorted,
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_gmm(*cfg, x_sorted, group_offsets, w_gate, w_up,
                                 w_down, h, y_sorted, status_word, stream));
+}
+
+moe_status_t moe_gmm_gate_up(const moe_config_t* cfg, const void* x_sorted,
+                             const int32_t* group_offsets, const void* w_gate,
+                             const void* w_up, void* h, int32_t* status_word,
+                             moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+      !ok_ptr(w_gate, true) || !ok_ptr(w_up, true) || !ok_ptr(h, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gmm1(*cfg, x_sorted, group_offsets, w_gate, w_up,
+                                 h, status_word, stream));
+}
+
+moe_status_t moe_gmm_down(const moe_config_t* cfg, const void* h,
+                          const int32_t* group_offsets, const void* w_down,
+                          void* y_sorted, int32_t* status_word,
+                          moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(h, true) || !ok_ptr(group_offsets, false) ||
+      !ok_ptr(w_down, true) || !ok_ptr(y_sorted, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gmm2(*cfg, h, group_offsets, w_down, y_sorted,
+                                 status_word, stream));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_sorted,

@@ -92,10 +92,9 @@ __global__ void __launch_bounds__(256) gmm_f32_kernel(
 
 }  // namespace
 
-cudaError_t launch_gmm_f32(const moe_config_t& c, const void* x_sorted,
-                           const int32_t* group_offsets, const void* w_gate,
-                           const void* w_up, const void* w_down, void* h,
-                           void* y_sorted, cudaStream_t s) {
+cudaError_t launch_gmm1_f32(const moe_config_t& c, const void* x_sorted,
+                            const int32_t* group_offsets, const void* w_gate,
+                            const void* w_up, void* h, cudaStream_t s) {
   const long long rows = static_cast<long long>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   const dim3 block(BN, 8);
@@ -106,6 +105,17 @@ cudaError_t launch_gmm_f32(const moe_config_t& c, const void* x_sorted,
       static_cast<const float*>(x_sorted), group_offsets, c.E, c.H, c.F,
       static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
       static_cast<float*>(h), static_cast<int>(rows));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gmm2_f32(const moe_config_t& c, const void* h,
+                            const int32_t* group_offsets, const void* w_down,
+                            void* y_sorted, cudaStream_t s) {
+  const long long rows = static_cast<long long>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  const dim3 block(BN, 8);
+  const unsigned gy = static_cast<unsigned>(
+      std::min<long long>((rows + BR - 1) / BR, 65535));
   const dim3 g2((c.H + BN - 1) / BN, gy);
   gmm_f32_kernel<1><<<g2, block, 0, s>>>(
       static_cast<const float*>(h), group_offsets, c.E, c.F, c.H,

@@ -615,24 +615,33 @@ bool gmm_tc_supported(const moe_config_t& c) {
          c.H >= 128 && c.F >= 128;
 }
 
-cudaError_t launch_gmm_bf16(const moe_config_t& c, const void* x_sorted,
-                            const int32_t* group_offsets, const void* w_gate,
-                            const void* w_up, const void* w_down, void* h,
-                            void* y_sorted, int32_t* status, cudaStream_t s) {
+cudaError_t launch_gmm1_bf16(const moe_config_t& c, const void* x_sorted,
+                             const int32_t* group_offsets, const void* w_gate,
+                             const void* w_up, void* h, int32_t* status,
+                             cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
-  CUtensorMap a1, bg, bu, a2, bd;
+  CUtensorMap a1, bg, bu;
   const uint64_t E = static_cast<uint64_t>(c.E);
   if (!tc::make_map(&a1, x_sorted, c.H, rows, 64, tc::BM) ||
       !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, 64) ||
-      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, 64) ||
-      !tc::make_map(&a2, h, c.F, rows, 64, tc::BM) ||
-      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, 64))
+      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, 64))
     return cudaErrorInvalidValue;
   tc::Params p1{group_offsets, c.E, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
-  cudaError_t err = tc::launch_one<0, 256>(a1, bg, bu, p1, s);
-  if (err != cudaSuccess) return err;
+  return tc::launch_one<0, 256>(a1, bg, bu, p1, s);
+}
+
+cudaError_t launch_gmm2_bf16(const moe_config_t& c, const void* h,
+                             const int32_t* group_offsets, const void* w_down,
+                             void* y_sorted, int32_t* status, cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap a2, bd;
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  if (!tc::make_map(&a2, h, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, 64))
+    return cudaErrorInvalidValue;
   if (c.H % 256 == 0) {
     tc::Params p2{group_offsets, c.E, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};

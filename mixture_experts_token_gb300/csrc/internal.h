@@ -68,6 +68,14 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
                            int32_t* expand_idx, int32_t* n_dropped,
                            const PermuteScratch& ws, int32_t* status,
                            cudaStream_t s);
+// GEMM1 + SwiGLU (h) and GEMM2 (y_sorted), each one kernel launch.
+cudaError_t launch_gmm1(const moe_config_t& c, const void* x_sorted,
+                        const int32_t* group_offsets, const void* w_gate,
+                        const void* w_up, void* h, int32_t* status,
+                        cudaStream_t s);
+cudaError_t launch_gmm2(const moe_config_t& c, const void* h,
+                        const int32_t* group_offsets, const void* w_down,
+                        void* y_sorted, int32_t* status, cudaStream_t s);
 cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
                        const int32_t* group_offsets, const void* w_gate,
                        const void* w_up, const void* w_down, void* h,
