@@ -172,6 +172,36 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x,
                          moe_stream_t stream);
 
 /* ----------------------------------------------------------------------
+ * moe_permute_noalloc -- moe_permute with no workspace argument.  The pages
+ * have no counterpart to this call; it exists for callers of this library
+ * that cannot allocate device memory themselves: code inside a host
+ * framework whose pool allocator owns all device memory and forbids other
+ * cudaMalloc calls, or latency-critical paths where cudaMalloc's implicit
+ * device-wide synchronisation is unacceptable.  Arguments and outputs are
+ * those of moe_permute; the caller still owns every input and output.
+ *   - The counting-sort tables live in one 8 MiB device array inside the
+ *     library, held by every GPU that loads it until the process exits.  A
+ *     call whose tables (moe_workspace_bytes(cfg, MOE_WS_PERMUTE)) exceed
+ *     8 MiB returns MOE_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device uses the same array, which keeps the previous
+ *     call's contents (nothing in it needs to start at zero: each call
+ *     writes every entry before reading it).  Calls whose work overlaps on
+ *     the GPU race on it; order them on one stream or with events.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x,
+                                 const int32_t *topk_idx, int32_t capped,
+                                 void *x_sorted, int32_t *row_of,
+                                 int32_t *sorted_token,
+                                 int32_t *group_offsets,
+                                 int32_t *uniq_offsets, int32_t *uniq_tokens,
+                                 int32_t *expand_idx, int32_t *n_dropped,
+                                 moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
  * moe_gmm_swiglu -- grouped GEMM SwiGLU expert FFN over ragged expert groups
  * [PR4760 review: grouped matmul with group_sizes per expert; expert weights
  * w0 of shape [E, H, H_ffn]].  For the rows r of group e

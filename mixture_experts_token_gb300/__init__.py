@@ -81,6 +81,8 @@ def _declare(h):
         "moe_check_overflow": [cfg, P, P, P, P, P, P, P, P],
         "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
                         c_size_t, P],
+        "moe_permute_noalloc": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P,
+                                P],
         "moe_gmm_swiglu": [cfg, P, P, P, P, P, P, P, P, P],
         "moe_gmm_gate_up": [cfg, P, P, P, P, P, P, P],
         "moe_gmm_down": [cfg, P, P, P, P, P, P],
@@ -196,6 +198,19 @@ def moe_permute(cfg, x, topk_idx, capped, x_sorted, row_of, sorted_token,
         _ptr(group_offsets), _ptr(uniq_offsets), _ptr(uniq_tokens),
         _ptr(expand_idx), _ptr(n_dropped), _ptr(workspace),
         _nbytes(workspace), _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, x, topk_idx, capped, x_sorted, row_of,
+                        sorted_token, group_offsets, uniq_offsets,
+                        uniq_tokens, expand_idx, n_dropped, stream=None):
+    """moe_permute with the scratch in the library's fixed device array, for
+    callers that cannot allocate device memory (see include/moe.h)."""
+    _check(lib().moe_permute_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), 1 if capped else 0,
+        _ptr(x_sorted), _ptr(row_of), _ptr(sorted_token),
+        _ptr(group_offsets), _ptr(uniq_offsets), _ptr(uniq_tokens),
+        _ptr(expand_idx), _ptr(n_dropped), _stream(stream)),
+        "moe_permute_noalloc")
 
 
 def moe_gmm_swiglu(cfg, x_sorted, group_offsets, w_gate, w_up, w_down, h,
