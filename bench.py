@@ -166,9 +166,10 @@ class ClockSampler:
 class Layer:
     """Inputs in HBM and every buffer of the stepwise calls."""
 
-    def __init__(self, wl, device, seed_offset=0):
+    def __init__(self, wl, device, seed_offset=0, mode="fallback"):
         import mixture_experts_token_gb300 as moe
         self.moe = moe
+        self.mode = mode
         self.wl = wl.with_(seed=wl.seed + seed_offset)
         w = self.wl
         self.cfg = moe.make_config(w.T, w.H, w.E, w.k, w.F, w.S, w.factor,
@@ -197,6 +198,9 @@ class Layer:
         mark = ev or (lambda name: None)
         mark("route")
         moe.moe_route(c, self.logits, b["topk_idx"], b["topk_w"], b["status"])
+        if self.mode != "fallback":
+            passes = [(0, c.T, self.mode == "capped")]
+            return self._passes(passes, mark)
         mark("check")
         moe.moe_check_overflow(c, b["topk_idx"], b["expert_counts"],
                                b["expert_offsets"], b["shard_counts"],
@@ -209,6 +213,10 @@ class Layer:
         else:
             passes = [(t0, min(c.T, t0 + self.chunk), False)
                       for t0 in range(0, c.T, self.chunk)]
+        return self._passes(passes, mark)
+
+    def _passes(self, passes, mark):
+        moe, b, W = self.moe, self.b, self.W
         for (t0, t1, capped) in passes:
             sc = self.sub(t0, t1, capped)
             mark("permute")
@@ -230,9 +238,11 @@ class Layer:
         return passes
 
     def api_layer(self, x, logits, y):
-        return self.moe.moe_layer(self.cfg, x, logits, *self.W, y,
-                                  self.moe.MOE_MODE_FALLBACK_LAYER, self.ws,
-                                  self.b["status"])
+        mode = {"fallback": self.moe.MOE_MODE_FALLBACK_LAYER,
+                "capped": self.moe.MOE_MODE_CAPPED,
+                "dropless": self.moe.MOE_MODE_DROPLESS}[self.mode]
+        return self.moe.moe_layer(self.cfg, x, logits, *self.W, y, mode,
+                                  self.ws, self.b["status"])
 
 
 class StageTimer:
@@ -258,11 +268,12 @@ class StageTimer:
         return out
 
 
-def launches_per_step(passes, T):
-    """Kernel launches of one step: route 1 + check 1, then per pass
-    permute 5 (block counts, expert scan, assign, dedup scan, row scatter),
-    GEMM1 1, GEMM2 1, combine 1."""
-    return 2 + sum(8 for (t0, t1, _) in passes if t1 > t0)
+def launches_per_step(passes, mode):
+    """Kernel launches of one step: route 1 (+ check 1 with the fallback),
+    then per pass permute 5 (block counts, expert scan, assign, dedup scan,
+    row scatter), GEMM1 1, GEMM2 1, combine 1."""
+    return (2 if mode == "fallback" else 1) + \
+        sum(8 for (t0, t1, _) in passes if t1 > t0)
 
 
 def pass_accounting(layer, passes):
@@ -305,7 +316,7 @@ def stage_work(w, acc):
 
 
 # ------------------------------------------------------------ the oracle --
-def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0):
+def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0, mode="fallback"):
     """Runs the oracle layer on tokens [t0, t0+n_tok) as a batch of its own
     (same shape parameters and factor); returns (seconds, tokens)."""
     from oracle import moe_ref as ref
@@ -322,8 +333,10 @@ def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0):
                 d.to(torch.float64).numpy())
     cfg = ref.MoEConfig(n_tok, wl.H, wl.E, wl.k, wl.F, wl.S, wl.factor,
                         wl.n_chunks, wl.renorm)
+    run = {"fallback": ref.layer, "capped": ref.layer_capped,
+           "dropless": ref.layer_dropless}[mode]
     t = time.perf_counter()
-    ref.layer(cfg, xs, Ls, weights)
+    run(cfg, xs, Ls, weights)
     return time.perf_counter() - t, n_tok
 
 
@@ -336,6 +349,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3",
                     choices=["dsv3", "l4mav", "small", "tiny", "profile"])
+    ap.add_argument("--mode", default="fallback",
+                    choices=["fallback", "capped", "dropless"],
+                    help="fallback: moe_dropless_fallback=layer (default); "
+                         "capped: capped path only; dropless: one uncapped "
+                         "pass")
+    ap.add_argument("--routing", default=None,
+                    choices=["zipf", "uniform", "adversarial"],
+                    help="override the workload's routing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -350,6 +371,9 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wl = workload_by_name(args.workload)
+    if args.routing:
+        wl = wl.with_(routing=args.routing, zipf_s=wl.zipf_s or 1.2,
+                      name=f"{wl.name}_{args.routing}")
 
     if args.impl == "reference":
         if rank == 0:
@@ -361,7 +385,7 @@ def main():
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
-    layer = Layer(wl, device, seed_offset=rank)
+    layer = Layer(wl, device, seed_offset=rank, mode=args.mode)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
     # identical bits: stepwise entry points vs the moe_layer call
@@ -480,14 +504,16 @@ def main():
             "routing": layer.wl.routing + (f" s={layer.wl.zipf_s}"
                                            if layer.wl.routing == "zipf"
                                            else ""),
-            "mode": "moe_dropless_fallback=layer",
+            "mode": {"fallback": "moe_dropless_fallback=layer",
+                     "capped": "capped path only",
+                     "dropless": "one uncapped pass"}[args.mode],
             "overflow": info["overflow"], "passes": len(passes),
             "capacity": info["capacity"],
             "l2": "flushed between steps (256 MiB write, outside the events)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "wall_s_timed_loop": round(wall, 3),
-        "gpu_launches": launches_per_step(passes, layer.wl.T) * args.steps,
+        "gpu_launches": launches_per_step(passes, args.mode) * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }
@@ -552,7 +578,8 @@ def e2e_run(layer, args, world, device):
 def cpu_baseline(layer):
     wl = layer.wl
     n = CPU_SAMPLE.get(wl.name, 32)
-    sec, n = oracle_sample_run(wl, layer.x, layer.logits_np, layer.W, n)
+    sec, n = oracle_sample_run(wl, layer.x, layer.logits_np, layer.W, n,
+                               mode=layer.mode)
     return {"value": round(n / sec, 4), "unit": UNIT, "cores": _CORES,
             "kind": "oracle",
             "sample": f"first {n} tokens of the {wl.name} batch run as a "
