@@ -66,9 +66,12 @@ REF_SAMPLE = {"dsv3": 8, "l4mav": 8, "small": 256, "tiny": 256,
               "profile_dsv3_e32": 8}
 
 
-def workload_by_name(name):
+def workload_by_name(name, sweep_T=65536, routing=None):
     if name == "profile":
         return PROFILE_WL
+    if name == "sweep":
+        from synth import sweep_workload
+        return sweep_workload(sweep_T, routing or "zipf")
     return WORKLOADS[name]
 
 
@@ -162,6 +165,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------ ranks ------
+def max_over_ranks(value: float, device) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank's time);
+    the value itself with one process."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or \
+            dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_workload(wl, rank: int):
+    """Each rank runs an independent replica on its own tokens and weights:
+    the same shapes, a seed shifted by the rank (weak scaling)."""
+    return wl.with_(seed=wl.seed + rank)
+
+
+def whole_job_tokens_per_s(world: int, T: int, ms_per_step: float) -> float:
+    return world * T / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------ the layer ---
 class Layer:
     """Inputs in HBM and every buffer of the stepwise calls."""
@@ -170,7 +196,7 @@ class Layer:
         import mixture_experts_token_gb300 as moe
         self.moe = moe
         self.mode = mode
-        self.wl = wl.with_(seed=wl.seed + seed_offset)
+        self.wl = replica_workload(wl, seed_offset)
         w = self.wl
         self.cfg = moe.make_config(w.T, w.H, w.E, w.k, w.F, w.S, w.factor,
                                    w.n_chunks, w.dtype, w.renorm)
@@ -178,7 +204,8 @@ class Layer:
         L = make_logits(w, self.x if w.routing == "router" else None)
         self.logits_np = L
         self.logits = torch.from_numpy(L).to(device)
-        self.W = make_weights(w, device)
+        self.dispatch_only = w.F == 0   # the routing/permute sweep
+        self.W = make_weights(w, device) if not self.dispatch_only else None
         self.b = moe.alloc_step_buffers(self.cfg, device)
         self.b["y"].zero_()
         self.ws = moe.layer_workspace(self.cfg, moe.MOE_WS_LAYER, device)
@@ -225,6 +252,12 @@ class Layer:
                             b["group_offsets"], b["uniq_offsets"],
                             b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
                             b["permute_ws"])
+            if self.dispatch_only:
+                # no expert FFN: the combine reads the permuted rows back
+                mark("combine")
+                moe.moe_combine(sc, b["x_sorted"], b["row_of"],
+                                b["topk_w"][t0:t1], b["y"][t0:t1])
+                continue
             mark("gmm_gate_up")
             moe.moe_gmm_gate_up(sc, b["x_sorted"], b["group_offsets"], W[0],
                                 W[1], b["h"], b["status"])
@@ -268,12 +301,13 @@ class StageTimer:
         return out
 
 
-def launches_per_step(passes, mode):
+def launches_per_step(passes, mode, dispatch_only=False):
     """Kernel launches of one step: route 1 (+ check 1 with the fallback),
     then per pass permute 5 (block counts, expert scan, assign, dedup scan,
-    row scatter), GEMM1 1, GEMM2 1, combine 1."""
+    row scatter), GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the sweep)."""
+    per = 6 if dispatch_only else 8
     return (2 if mode == "fallback" else 1) + \
-        sum(8 for (t0, t1, _) in passes if t1 > t0)
+        sum(per for (t0, t1, _) in passes if t1 > t0)
 
 
 def pass_accounting(layer, passes):
@@ -348,7 +382,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3",
-                    choices=["dsv3", "l4mav", "small", "tiny", "profile"])
+                    choices=["dsv3", "l4mav", "small", "tiny", "profile",
+                             "sweep"],
+                    help="sweep: routing/permute/dedup only (no expert FFN)")
+    ap.add_argument("--sweep-T", type=int, default=65536)
     ap.add_argument("--mode", default="fallback",
                     choices=["fallback", "capped", "dropless"],
                     help="fallback: moe_dropless_fallback=layer (default); "
@@ -370,8 +407,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    wl = workload_by_name(args.workload)
-    if args.routing:
+    wl = workload_by_name(args.workload, args.sweep_T, args.routing)
+    if args.routing and args.workload != "sweep":
         wl = wl.with_(routing=args.routing, zipf_s=wl.zipf_s or 1.2,
                       name=f"{wl.name}_{args.routing}")
 
@@ -389,12 +426,18 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
     # identical bits: stepwise entry points vs the moe_layer call
-    y_api = torch.empty_like(layer.b["y"])
-    info = layer.api_layer(layer.x, layer.logits, y_api)
     passes = layer.step()
     torch.cuda.synchronize()
-    if not torch.equal(y_api, layer.b["y"]):
-        raise SystemExit("stepwise path and moe_layer disagree")
+    if layer.dispatch_only:
+        info = {"overflow": int(layer.b["overflow_flag"].item())
+                if args.mode == "fallback" else -1,
+                "capacity": layer.moe.moe_capacity_rows(layer.cfg)}
+    else:
+        y_api = torch.empty_like(layer.b["y"])
+        info = layer.api_layer(layer.x, layer.logits, y_api)
+        torch.cuda.synchronize()
+        if not torch.equal(y_api, layer.b["y"]):
+            raise SystemExit("stepwise path and moe_layer disagree")
     if int(layer.b["status"].item()) != 0:
         raise SystemExit(f"device status {int(layer.b['status'].item())}")
 
@@ -425,12 +468,7 @@ def main():
     clock_rec = clocks.stop()
 
     step_ms = [sum(d for _, d in st.durations()) for st in timers]
-    mean_ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([mean_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
 
     # per-stage durations
     stage = {}
@@ -461,7 +499,7 @@ def main():
                 ent["TFLOPs"] = round(wv["flops"] / sec / 1e12, 1)
         kernels[name] = ent
 
-    dom = max((n for n in work), key=lambda n: stage[n]["ms"])
+    dom = max((n for n in work if n in stage), key=lambda n: stage[n]["ms"])
     wv = work[dom]
     n_launch = len(passes)
     dur = stage[dom]["ms"] / args.steps / n_launch / 1e3     # per launch
@@ -487,7 +525,7 @@ def main():
 
     # e2e through moe_layer with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not layer.dispatch_only:
         e2e = e2e_run(layer, args, world, device)
 
     out = {
@@ -513,16 +551,18 @@ def main():
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "wall_s_timed_loop": round(wall, 3),
-        "gpu_launches": launches_per_step(passes, args.mode) * args.steps,
+        "gpu_launches": launches_per_step(passes, args.mode,
+                                          layer.dispatch_only) * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }
-    out["value"] = round(world * layer.wl.T / (mean_ms / 1e3), 1)
+    out["value"] = round(whole_job_tokens_per_s(world, layer.wl.T, mean_ms), 1)
     if clock_rec:
         out["clocks"] = clock_rec
     if e2e:
         out["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and \
+            not layer.dispatch_only:
         out["cpu_baseline"] = cpu_baseline(layer)
     if rank == 0:
         print(json.dumps(out))
@@ -561,15 +601,10 @@ def e2e_run(layer, args, world, device):
         b.record()
         b.synchronize()
         ms.append(a.elapsed_time(b))
-    mean = sum(ms) / len(ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([mean], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean = float(t.item())
+    mean = max_over_ranks(sum(ms) / len(ms), device)
     h2d = x_h.numel() * x_h.element_size() + L_h.numel() * L_h.element_size()
     d2h = y_h.numel() * y_h.element_size()
-    return {"value": round(world * layer.wl.T / (mean / 1e3), 1),
+    return {"value": round(whole_job_tokens_per_s(world, layer.wl.T, mean), 1),
             "unit": UNIT, "ms_per_step": round(mean, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "api": "moe_layer (C ABI), pinned host buffers"}
