@@ -26,6 +26,13 @@ CASES = [
     WORKLOADS["small"].with_(name="e40_s8", T=777, H=64, E=40, k=6, S=8,
                              routing="uniform"),
     WORKLOADS["small"].with_(name="k_eq_e", T=300, H=64, E=8, k=8, S=4),
+    # large tables: many token blocks, E above 256
+    WORKLOADS["small"].with_(name="rows_32768", T=4096, H=64, E=256, k=8,
+                             S=8, zipf_s=1.2),
+    WORKLOADS["small"].with_(name="rows_32776", T=4097, H=64, E=256, k=8,
+                             S=8, zipf_s=1.2),
+    WORKLOADS["small"].with_(name="e300", T=900, H=64, E=300, k=3, S=4,
+                             routing="uniform"),
 ]
 
 
