@@ -386,6 +386,8 @@ def main():
                              "sweep"],
                     help="sweep: routing/permute/dedup only (no expert FFN)")
     ap.add_argument("--sweep-T", type=int, default=65536)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count T")
     ap.add_argument("--mode", default="fallback",
                     choices=["fallback", "capped", "dropless"],
                     help="fallback: moe_dropless_fallback=layer (default); "
@@ -408,6 +410,8 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wl = workload_by_name(args.workload, args.sweep_T, args.routing)
+    if args.tokens > 0:
+        wl = wl.with_(T=args.tokens, name=f"{wl.name}_T{args.tokens}")
     if args.routing and args.workload != "sweep":
         wl = wl.with_(routing=args.routing, zipf_s=wl.zipf_s or 1.2,
                       name=f"{wl.name}_{args.routing}")
@@ -523,10 +527,11 @@ def main():
     roof["peak_source"] = f"{peak_src} MEASURED_PEAKS.json" \
         if peak_src == "measured" else "fallback"
 
-    # e2e through moe_layer with host buffers
+    # the layer as one CUDA graph launch; e2e with host buffers
+    graph = None if layer.dispatch_only else graph_run(layer, args, device)
     e2e = None
     if not args.no_e2e and not layer.dispatch_only:
-        e2e = e2e_run(layer, args, world, device)
+        e2e = e2e_run(layer, args, world, device, graph)
 
     out = {
         "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world,
@@ -557,6 +562,13 @@ def main():
         "roofline": roof,
     }
     out["value"] = round(whole_job_tokens_per_s(world, layer.wl.T, mean_ms), 1)
+    if graph is not None:
+        out["graph_layer"] = {
+            "value": round(whole_job_tokens_per_s(world, layer.wl.T,
+                                                  graph["ms_per_step"]), 1),
+            "unit": UNIT, "ms_per_step": round(graph["ms_per_step"], 4),
+            "api": "moe_layer_graph_launch: route, check, conditional node "
+                   "(capped pass | chunked fallback), one launch"}
     if clock_rec:
         out["clocks"] = clock_rec
     if e2e:
@@ -571,20 +583,69 @@ def main():
         dist.destroy_process_group()
 
 
-def e2e_run(layer, args, world, device):
+def graph_run(layer, args, device):
+    """The same layer as one CUDA graph launch per step (moe_layer_graph):
+    device-resident throughput, and the bits checked against the stepwise
+    result."""
+    if layer.mode != "fallback":
+        return None
+    moe = layer.moe
+    x_d = layer.x.clone()
+    L_d = layer.logits.clone()
+    y_d = torch.empty_like(layer.b["y"])
+    ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
+    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws)
+    g.launch()
+    torch.cuda.synchronize()
+    if not torch.equal(y_d, layer.b["y"]):
+        raise SystemExit("graph path and stepwise path disagree")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        flush.zero_()
+        g.launch()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), \
+            torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.launch()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    mean = max_over_ranks(sum(ms) / len(ms), device)
+    return {"graph": g, "x": x_d, "logits": L_d, "y": y_d, "ws": ws,
+            "ms_per_step": mean}
+
+
+def e2e_run(layer, args, world, device, graph=None):
+    """Same metric end to end: pinned host x and logits copied in, the layer,
+    y copied out, every step.  Through moe_layer_graph when available (one
+    launch per layer), else moe_layer."""
     x_h = layer.x.cpu().pin_memory()
     L_h = layer.logits.cpu().pin_memory()
     y_h = torch.empty(layer.b["y"].shape, dtype=layer.b["y"].dtype,
                       pin_memory=True)
-    x_d = torch.empty_like(layer.x)
-    L_d = torch.empty_like(layer.logits)
-    y_d = torch.empty_like(layer.b["y"])
+    if graph is not None:
+        x_d, L_d, y_d = graph["x"], graph["logits"], graph["y"]
+        api = "moe_layer_graph_launch (C ABI), pinned host buffers"
+
+        def run_layer():
+            graph["graph"].launch()
+    else:
+        x_d = torch.empty_like(layer.x)
+        L_d = torch.empty_like(layer.logits)
+        y_d = torch.empty_like(layer.b["y"])
+        api = "moe_layer (C ABI), pinned host buffers"
+
+        def run_layer():
+            layer.api_layer(x_d, L_d, y_d)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
     def one():
         x_d.copy_(x_h, non_blocking=True)
         L_d.copy_(L_h, non_blocking=True)
-        layer.api_layer(x_d, L_d, y_d)
+        run_layer()
         y_h.copy_(y_d, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -607,7 +668,7 @@ def e2e_run(layer, args, world, device):
     return {"value": round(whole_job_tokens_per_s(world, layer.wl.T, mean), 1),
             "unit": UNIT, "ms_per_step": round(mean, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "moe_layer (C ABI), pinned host buffers"}
+            "api": api}
 
 
 def cpu_baseline(layer):

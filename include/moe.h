@@ -289,6 +289,35 @@ moe_status_t moe_layer(const moe_config_t *cfg, const void *x,
                        size_t workspace_bytes, moe_stream_t stream);
 
 /* ----------------------------------------------------------------------
+ * moe_layer_graph_* -- the MOE_MODE_FALLBACK_LAYER layer as one CUDA graph
+ * (an extension).  The branch of [PR5920 How] is a conditional IF node:
+ * the check kernel's flag selects, on the device, either the chunked
+ * dropless passes or the capped pass, so a launch never waits on the host.
+ *   create: validates like moe_layer (T >= 1), captures the graph on the
+ *     current device and instantiates it; the graph stays bound to x,
+ *     logits, the weights, y, status_word and workspace (refresh x and the
+ *     logits in place between launches).  Allocates no device memory; the
+ *     graph objects live on the host until moe_layer_graph_destroy.
+ *   launch: enqueues one layer on `stream` (not the legacy NULL stream
+ *     while another capture is open).
+ *   overflow_flag: device int32 written by each launch (1 = overflowed).
+ *   fallback_chunks: passes the overflow branch runs.
+ * ---------------------------------------------------------------------- */
+typedef struct moe_layer_graph moe_layer_graph_t;
+
+moe_status_t moe_layer_graph_create(const moe_config_t *cfg, const void *x,
+                                    const float *logits, const void *w_gate,
+                                    const void *w_up, const void *w_down,
+                                    void *y, int32_t *status_word,
+                                    void *workspace, size_t workspace_bytes,
+                                    moe_layer_graph_t **graph_out);
+moe_status_t moe_layer_graph_launch(moe_layer_graph_t *graph,
+                                    moe_stream_t stream);
+const int32_t *moe_layer_graph_overflow_flag(const moe_layer_graph_t *graph);
+int32_t moe_layer_graph_fallback_chunks(const moe_layer_graph_t *graph);
+void moe_layer_graph_destroy(moe_layer_graph_t *graph);
+
+/* ----------------------------------------------------------------------
  * Host-side queries (no GPU work).
  * ---------------------------------------------------------------------- */
 typedef enum {

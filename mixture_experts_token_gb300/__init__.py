@@ -96,6 +96,17 @@ def _declare(h):
         fn = getattr(h, name)
         fn.argtypes = args
         fn.restype = c_int
+    h.moe_layer_graph_create.argtypes = [cfg, P, P, P, P, P, P, P, P,
+                                         c_size_t, ctypes.POINTER(P)]
+    h.moe_layer_graph_create.restype = c_int
+    h.moe_layer_graph_launch.argtypes = [P, P]
+    h.moe_layer_graph_launch.restype = c_int
+    h.moe_layer_graph_overflow_flag.argtypes = [P]
+    h.moe_layer_graph_overflow_flag.restype = P
+    h.moe_layer_graph_fallback_chunks.argtypes = [P]
+    h.moe_layer_graph_fallback_chunks.restype = c_int32
+    h.moe_layer_graph_destroy.argtypes = [P]
+    h.moe_layer_graph_destroy.restype = None
     h.moe_workspace_bytes.argtypes = [cfg, c_int]
     h.moe_workspace_bytes.restype = c_size_t
     h.moe_validate_config.argtypes = [cfg]
@@ -259,6 +270,43 @@ def moe_layer(cfg, x, logits, w_gate, w_up, w_down, y, mode, workspace,
         _ptr(workspace), _nbytes(workspace), _stream(stream)), "moe_layer")
     return {"overflow": info.overflow, "n_chunks": info.n_chunks,
             "capacity": info.capacity}
+
+
+class MoeLayerGraph:
+    """moe_layer_graph_t: the fallback=layer layer as one CUDA graph, bound
+    to the tensors given here (they must outlive the graph)."""
+
+    def __init__(self, cfg, x, logits, w_gate, w_up, w_down, y, workspace,
+                 status_word=None):
+        self._h = c_void_p()
+        self._keep = (x, logits, w_gate, w_up, w_down, y, workspace,
+                      status_word)
+        _check(lib().moe_layer_graph_create(
+            ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate),
+            _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(status_word),
+            _ptr(workspace), _nbytes(workspace), ctypes.byref(self._h)),
+            "moe_layer_graph_create")
+
+    def launch(self, stream=None):
+        _check(lib().moe_layer_graph_launch(self._h, _stream(stream)),
+               "moe_layer_graph_launch")
+
+    def overflow_flag_ptr(self) -> int:
+        return lib().moe_layer_graph_overflow_flag(self._h)
+
+    def fallback_chunks(self) -> int:
+        return lib().moe_layer_graph_fallback_chunks(self._h)
+
+    def close(self):
+        if self._h:
+            lib().moe_layer_graph_destroy(self._h)
+            self._h = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ------------------------------------------------- buffer allocation ------

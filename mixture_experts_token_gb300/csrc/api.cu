@@ -86,8 +86,6 @@ cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
   return launch_gmm2(c, h, group_offsets, w_down, y_sorted, status, s);
 }
 
-namespace {
-
 moe_status_t validate(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->H < 1 || c->F < 0) return MOE_ERR_INVALID_ARG;
@@ -116,16 +114,6 @@ bool ok_ptr(const void* p, bool need16) {
 moe_status_t cuda_status(cudaError_t e) {
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
-
-// Buffers of one layer pass over up to `T` tokens, carved from a workspace.
-struct LayerBufs {
-  int32_t *topk_idx, *counts, *offsets, *shard, *flag, *cap;
-  float *topk_w, *req;
-  int32_t *row_of, *sorted_token, *group_offsets, *uniq_offsets,
-      *uniq_tokens, *expand_idx, *n_dropped;
-  PermuteScratch pws;
-  void *x_sorted, *h, *y_sorted;
-};
 
 LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
                       size_t* bytes) {
@@ -219,7 +207,6 @@ bool weights_ok(const void* wg, const void* wu, const void* wd) {
   return ok_ptr(wg, true) && ok_ptr(wu, true) && ok_ptr(wd, true);
 }
 
-}  // namespace
 }  // namespace moe
 
 using namespace moe;

@@ -84,6 +84,35 @@ cudaError_t launch_combine(const moe_config_t& c, const void* y_sorted,
                            const int32_t* row_of, const float* topk_w,
                            void* y, cudaStream_t s);
 
+// Buffers of one layer pass over up to `T` tokens, carved from a workspace.
+struct LayerBufs {
+  int32_t *topk_idx, *counts, *offsets, *shard, *flag, *cap;
+  float *topk_w, *req;
+  int32_t *row_of, *sorted_token, *group_offsets, *uniq_offsets,
+      *uniq_tokens, *expand_idx, *n_dropped;
+  PermuteScratch pws;
+  void *x_sorted, *h, *y_sorted;
+};
+LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
+                      size_t* bytes);
+size_t layer_bytes(const moe_config_t& c, int T);
+moe_config_t sub_config(const moe_config_t& c, int T);
+// permute (cap, or uncapped when cap < 0) -> GEMM1 -> GEMM2 -> combine
+cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
+                 const float* topk_w, int64_t cap, const void* wg,
+                 const void* wu, const void* wd, void* y, const LayerBufs& b,
+                 int32_t* status, cudaStream_t s);
+// the chunked dropless fallback over routing already in topk_idx/topk_w
+cudaError_t chunked_passes(const moe_config_t& c, const void* x,
+                           const int32_t* topk_idx, const float* topk_w,
+                           const void* wg, const void* wu, const void* wd,
+                           void* y, const LayerBufs& b, int32_t* status,
+                           cudaStream_t s, int32_t* n_run);
+moe_status_t validate(const moe_config_t* c);
+bool ok_ptr(const void* p, bool need16);
+bool gmm_shape_ok(const moe_config_t& c);
+bool weights_ok(const void* wg, const void* wu, const void* wd);
+
 // Shape support of the bf16 tensor-core GEMM.
 bool gmm_tc_supported(const moe_config_t& c);
 

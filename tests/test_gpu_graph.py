@@ -1,0 +1,88 @@
+"""GPU: the layer as one CUDA graph with a conditional node (moe_layer_graph_*)
+gives the same bits as moe_layer in both branches, launch after launch with
+inputs refreshed in place, and reports the same overflow flag."""
+import pytest
+import torch
+
+import mixture_experts_token_gb300 as moe
+from synth import WORKLOADS, make_logits, make_weights, make_x
+from tests.gpu_util import cfg_from
+
+pytestmark = pytest.mark.gpu
+
+
+def batch(wl, seed):
+    w = wl.with_(seed=seed)
+    x = make_x(w, "cuda")
+    L = torch.from_numpy(make_logits(w, x if w.routing == "router" else None))
+    return x, L.cuda()
+
+
+def device_flag(graph, ws):
+    """The graph's overflow flag lives in the workspace: read it there."""
+    off = graph.overflow_flag_ptr() - ws.data_ptr()
+    assert 0 <= off < ws.numel() and off % 4 == 0
+    return int(ws[off:off + 4].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("wl,factor", [
+    (WORKLOADS["tiny"], 0.1),
+    (WORKLOADS["tiny"], 2.0),
+    (WORKLOADS["small"], 2.0),
+    (WORKLOADS["small"], 50.0),
+    (WORKLOADS["l4mav"], 2.0),
+    (WORKLOADS["dsv3"], 2.0),
+], ids=["tiny-ovf", "tiny", "small-ovf", "small", "l4mav", "dsv3"])
+def test_graph_matches_moe_layer(wl, factor):
+    cfg = cfg_from(wl, factor=factor)
+    W = make_weights(wl, "cuda")
+    x, L = batch(wl, 0)
+    y = torch.zeros((wl.T, wl.H), dtype=x.dtype, device="cuda")
+    ws = moe.layer_workspace(cfg)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = moe.MoeLayerGraph(cfg, x, L, *W, y, ws, status)
+    ref_ws = moe.layer_workspace(cfg)
+    for seed in (0, 1, 2):
+        xs, Ls = batch(wl, seed)
+        x.copy_(xs)
+        L.copy_(Ls)
+        g.launch()
+        torch.cuda.synchronize()
+        y_ref = torch.empty_like(y)
+        info = moe.moe_layer(cfg, xs, Ls, *W, y_ref,
+                             moe.MOE_MODE_FALLBACK_LAYER, ref_ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref), seed
+        assert device_flag(g, ws) == info["overflow"]
+        if info["overflow"]:
+            assert g.fallback_chunks() == info["n_chunks"]
+    assert int(status.item()) == 0
+    g.close()
+
+
+def test_graph_both_branches_on_one_graph():
+    """One graph, two batches: one that overflows and one that does not."""
+    wl = WORKLOADS["small"].with_(T=1024, H=256, F=256, E=8, S=4, k=2)
+    cfg = cfg_from(wl, factor=2.0)
+    W = make_weights(wl, "cuda")
+    x, L = batch(wl, 0)
+    y = torch.zeros((wl.T, wl.H), dtype=x.dtype, device="cuda")
+    ws = moe.layer_workspace(cfg)
+    g = moe.MoeLayerGraph(cfg, x, L, *W, y, ws)
+    hot = L.clone()
+    hot[:, :2] += 50.0            # every pick in shard 0 -> overflow
+    flat = torch.randn_like(L) * 0.01   # near-uniform -> no overflow
+    flags = []
+    for logits in (hot, flat, hot):
+        L.copy_(logits)
+        g.launch()
+        y_ref = torch.empty_like(y)
+        info = moe.moe_layer(cfg, x, logits, *W, y_ref,
+                             moe.MOE_MODE_FALLBACK_LAYER,
+                             moe.layer_workspace(cfg))
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+        flags.append(device_flag(g, ws))
+        assert flags[-1] == info["overflow"]
+    assert flags == [1, 0, 1]
+    g.close()
