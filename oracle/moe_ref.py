@@ -499,3 +499,144 @@ def normwise_error(got: np.ndarray, ref: np.ndarray) -> float:
     if den == 0.0:
         return num
     return num / den
+
+
+# ---------------------------------------------------------------------------
+# Dynamic redundant experts.  "Moe dynamic redundancy" (MaxText pull request
+# 4760), review comments: plan_expert_duplication duplicates the hottest
+# not-yet-duplicated expert of the most loaded rank (r_max) into a spare slot
+# (num_slots_B per rank) on an underloaded rank and diverts a fraction of its
+# tokens there (reroute_fractions); the review requires that (1) tokens are
+# really diverted, so the slots get non-zero group sizes, and (2) the plan
+# stops when r_max has no un-duplicated expert left (has_candidate), so no
+# expert is duplicated twice.  On one GPU a slot uses the same weights as
+# its expert (nothing is gathered).
+# READINGS: each round takes r_max = the most loaded shard (ties: lower
+# index), its hottest un-duplicated expert with rows (ties: lower index),
+# and r_min = the least loaded other shard with a free slot (ties: lower
+# index); it stops when there is no candidate, no such shard, or no gap; it
+# moves n = min(c_e, (load[r_max] - load[r_min]) // 2) rows (integer halving
+# of the gap, so the fraction is n / c_e).  The duplicate takes the expert's
+# LAST n rows in token order.  At most S*B rounds.
+# Virtual layout: shard s owns virtual groups [s*(E_s+B), (s+1)*(E_s+B)):
+# its E_s experts, then its B slots.
+# ---------------------------------------------------------------------------
+@dataclass
+class DuplicationPlan:
+    divert: np.ndarray        # [E] rows of e moved to its duplicate
+    slot_of: np.ndarray       # [E] virtual group of e's duplicate, -1 if none
+    group_expert: np.ndarray  # [E'] expert behind each virtual group (-1 unused)
+    loads_after: np.ndarray   # [S] shard loads after the diversion
+    B: int
+
+
+def virtual_group_of_expert(e: int, E: int, S: int, B: int) -> int:
+    Es = E // S
+    return (e // Es) * (Es + B) + e % Es
+
+
+def virtual_group_of_slot(s: int, b: int, E: int, S: int, B: int) -> int:
+    Es = E // S
+    return s * (Es + B) + Es + b
+
+
+def plan_duplication(counts: np.ndarray, S: int, B: int) -> DuplicationPlan:
+    counts = [int(c) for c in counts]
+    E = len(counts)
+    Es = E // S
+    load = [sum(counts[s * Es:(s + 1) * Es]) for s in range(S)]
+    dup = [False] * E
+    free = [B] * S
+    divert = [0] * E
+    slot_of = [-1] * E
+    group_expert = [-1] * (S * (Es + B))
+    for e in range(E):
+        group_expert[virtual_group_of_expert(e, E, S, B)] = e
+    for _ in range(S * B):
+        r_max = 0
+        for s in range(1, S):
+            if load[s] > load[r_max]:
+                r_max = s
+        cands = [e for e in range(r_max * Es, (r_max + 1) * Es)
+                 if not dup[e] and counts[e] > 0]
+        has_candidate = len(cands) > 0
+        r_min = -1
+        for s in range(S):
+            if s != r_max and free[s] > 0:
+                if r_min < 0 or load[s] < load[r_min]:
+                    r_min = s
+        if not has_candidate or r_min < 0 or load[r_max] <= load[r_min]:
+            break
+        e_star = cands[0]
+        for e in cands[1:]:
+            if counts[e] > counts[e_star]:
+                e_star = e
+        n = min(counts[e_star], (load[r_max] - load[r_min]) // 2)
+        if n <= 0:
+            break
+        b = B - free[r_min]
+        free[r_min] -= 1
+        g = virtual_group_of_slot(r_min, b, E, S, B)
+        dup[e_star] = True
+        divert[e_star] = n
+        slot_of[e_star] = g
+        group_expert[g] = e_star
+        load[r_max] -= n
+        load[r_min] += n
+    return DuplicationPlan(np.array(divert, dtype=INT),
+                           np.array(slot_of, dtype=INT),
+                           np.array(group_expert, dtype=INT),
+                           np.array(load, dtype=INT), B)
+
+
+def reroute(topk_idx: np.ndarray, plan: DuplicationPlan, E: int,
+            S: int) -> np.ndarray:
+    """Virtual group of every routed row (t, j): its expert's group, or the
+    duplicate's slot for the expert's last divert[e] rows in token order."""
+    topk_idx = np.asarray(topk_idx)
+    T, k = topk_idx.shape
+    counts = expert_counts(topk_idx, E)
+    seen = [0] * E
+    out = np.zeros_like(topk_idx, dtype=INT)
+    for t in range(T):
+        for j in range(k):
+            e = int(topk_idx[t, j])
+            keep = int(counts[e]) - int(plan.divert[e])
+            if seen[e] >= keep and plan.slot_of[e] >= 0:
+                out[t, j] = plan.slot_of[e]
+            else:
+                out[t, j] = virtual_group_of_expert(e, E, S, plan.B)
+            seen[e] += 1
+    return out
+
+
+def mapped_weights(weights: ExpertWeights,
+                   group_expert: np.ndarray) -> ExpertWeights:
+    """Weights of virtual group g = weights of expert group_expert[g]."""
+    return lambda g: weights(int(group_expert[g]))
+
+
+def layer_redundant(cfg: MoEConfig, x, logits, weights: ExpertWeights,
+                    B: int) -> LayerResult:
+    """fallback=layer with dynamic redundant experts: route, plan, divert,
+    then the overflow check on the virtual shard loads; capped pass over the
+    virtual groups, or the chunked dropless fallback when still over."""
+    idx, w, _ = route(logits, cfg.k, cfg.renorm)
+    counts = expert_counts(idx, cfg.E)
+    plan = plan_duplication(counts, cfg.S, B)
+    vidx = reroute(idx, plan, cfg.E, cfg.S)
+    G = cfg.S * (cfg.E // cfg.S + B)
+    vshard = shard_counts(expert_counts(vidx, G), cfg.S)
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    if overflow_flag(vshard, C):
+        res = layer_dropless_chunked(cfg, x, logits, weights)
+        res.overflow = True
+        return res
+    x = np.asarray(x, dtype=np.float64)
+    perm = permute_indices(vidx, G, cfg.S, C)
+    xs = gather_rows(x, perm.sorted_token)
+    h, ys = grouped_ffn(xs, perm.group_offsets,
+                        mapped_weights(weights, plan.group_expert))
+    y = combine(ys, perm.row_of, w, cfg.H)
+    return LayerResult(y, idx, w, counts, vshard, C, False,
+                       required_factor(vshard, cfg.T, cfg.k), perm, xs, h, ys)

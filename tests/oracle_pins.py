@@ -454,4 +454,117 @@ def pin_asymmetric_single_shard():
     assert out.overflow and len(out.chunks) > 1
 
 
+# --------------------------------------------------------------------------
+# dynamic redundant experts
+# --------------------------------------------------------------------------
+def pin_duplication_hand_cases():
+    # one hot expert, two shards of 4 experts, one slot per shard: half the
+    # gap (8 - 0) // 2 = 4 rows go to the slot of shard 1 (virtual group 9)
+    p = ref.plan_duplication(np.array([8, 0, 0, 0, 0, 0, 0, 0]), 2, 1)
+    assert p.divert.tolist() == [4, 0, 0, 0, 0, 0, 0, 0]
+    assert p.slot_of.tolist() == [9, -1, -1, -1, -1, -1, -1, -1]
+    assert p.group_expert.tolist() == [0, 1, 2, 3, -1, 4, 5, 6, 7, 0]
+    assert p.loads_after.tolist() == [4, 4]
+    # the review's case: once r_max's only expert is duplicated there is no
+    # candidate left, so the plan stops instead of duplicating it again
+    p = ref.plan_duplication(np.array([100, 0]), 2, 4)
+    assert p.divert.tolist() == [50, 0]
+    assert int((p.group_expert == 0).sum()) == 2      # home group + 1 slot
+    assert p.loads_after.tolist() == [50, 50]
+    # three shards: the hottest expert of the hottest shard goes first, to
+    # the least loaded shard; ties go to the lower index
+    p = ref.plan_duplication(np.array([6, 9, 2, 0, 0, 0]), 3, 1)
+    # loads [15, 2, 0]: e=1 (9 rows) to shard 2, n = min(9, 15 // 2) = 7;
+    # loads [8, 2, 7]: e=0 (6 rows) to shard 1, n = min(6, (8-2)//2) = 3;
+    # loads [5, 5, 7]: r_max = 2 has no rows of its own -> stop
+    assert p.divert.tolist() == [3, 7, 0, 0, 0, 0]
+    assert p.loads_after.tolist() == [5, 5, 7]
+    assert p.slot_of.tolist() == [
+        ref.virtual_group_of_slot(1, 0, 6, 3, 1),
+        ref.virtual_group_of_slot(2, 0, 6, 3, 1), -1, -1, -1, -1]
+
+
+def pin_duplication_invariants():
+    rng = _rng(12)
+    for _ in range(200):
+        S = int(rng.choice([2, 4, 8]))
+        Es = int(rng.integers(1, 6))
+        E = S * Es
+        B = int(rng.integers(1, 4))
+        counts = rng.integers(0, 50, size=E) * (rng.random(E) < 0.7)
+        counts[: Es] *= int(rng.integers(1, 6))        # a hot shard
+        p = ref.plan_duplication(counts, S, B)
+        before = ref.shard_counts(counts, S)
+        assert int(p.loads_after.sum()) == int(counts.sum())
+        assert int(p.loads_after.max()) <= int(before.max())
+        assert np.all(p.divert >= 0) and np.all(p.divert <= counts)
+        G = S * (Es + B)
+        assert len(p.group_expert) == G
+        for e in range(E):
+            home = ref.virtual_group_of_expert(e, E, S, B)
+            assert p.group_expert[home] == e
+            if p.slot_of[e] >= 0:
+                assert p.divert[e] > 0
+                g = int(p.slot_of[e])
+                assert p.group_expert[g] == e
+                assert g // (Es + B) != e // Es      # never on its home shard
+                assert g % (Es + B) >= Es            # a slot, not an expert
+            else:
+                assert p.divert[e] == 0
+            # an expert is duplicated at most once
+            assert int((p.group_expert == e).sum()) <= 2
+        for s in range(S):
+            used = sum(1 for b in range(B)
+                       if p.group_expert[s * (Es + B) + Es + b] >= 0)
+            assert used <= B
+        # loads after = virtual shard loads of the rerouted rows
+        L = rng.standard_normal((40, E)).astype(np.float32)
+        idx, _, _ = ref.route(L, min(2, E))
+        c = ref.expert_counts(idx, E)
+        p = ref.plan_duplication(c, S, B)
+        v = ref.reroute(idx, p, E, S)
+        vc = ref.expert_counts(v, G)
+        assert np.array_equal(ref.shard_counts(vc, S), p.loads_after)
+        for e in range(E):
+            assert vc[ref.virtual_group_of_expert(e, E, S, B)] == \
+                c[e] - p.divert[e]
+            if p.slot_of[e] >= 0:
+                assert vc[p.slot_of[e]] == p.divert[e]
+
+
+def pin_reroute_takes_last_rows():
+    # expert 0 picked by tokens 0..5; shard loads 12 and 4, so half the gap
+    # (4 rows) moves and the duplicate gets the LAST 4 of expert 0's rows
+    idx = np.array([[0, 1]] * 6 + [[4, 5]] * 2)
+    p = ref.plan_duplication(ref.expert_counts(idx, 8), 2, 1)
+    v = ref.reroute(idx, p, 8, 2)
+    d = int(p.divert[0])
+    assert d == 4
+    home = ref.virtual_group_of_expert(0, 8, 2, 1)
+    assert [int(g) for g in v[:, 0][:6]] == [home] * (6 - d) + \
+        [int(p.slot_of[0])] * d
+
+
+def pin_redundancy_preserves_the_layer():
+    rng = _rng(13)
+    T, H, E, k, F, S = 64, 5, 8, 2, 6, 4
+    x = rng.standard_normal((T, H))
+    ws = ref.dense_weights(rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, H, F)),
+                           rng.standard_normal((E, F, H)))
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    L[:, :2] += 2.5                               # shard 0 hot
+    cfg = ref.MoEConfig(T, H, E, k, F, S, 2.0)
+    plain = ref.layer(cfg, x, L, ws)
+    assert plain.overflow                          # without slots: fallback
+    red = ref.layer_redundant(cfg, x, L, ws, B=2)
+    assert not red.overflow                        # with slots: capped path
+    assert red.perm.n_dropped == 0
+    assert np.allclose(red.y, plain.y, rtol=1e-12, atol=1e-12)
+    # every duplicate slot that got rows runs its expert's weights
+    G = S * (E // S + 2)
+    sizes = np.diff(red.perm.group_offsets)
+    assert sizes[[g for g in range(G) if g % (E // S + 2) >= E // S]].sum() > 0
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

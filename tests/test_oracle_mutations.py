@@ -55,6 +55,20 @@ MUTANTS = {
                                "            if r > 0:\n"),
     "chunk_ignores_shard_bound": (
         "c = max(1, C // worst_per_token)", "c = max(1, C // k)"),
+    "dup_without_has_candidate": (
+        "        cands = [e for e in range(r_max * Es, (r_max + 1) * Es)\n"
+        "                 if not dup[e] and counts[e] > 0]\n",
+        "        cands = [e for e in range(r_max * Es, (r_max + 1) * Es)\n"
+        "                 if counts[e] > 0]\n"),
+    "dup_moves_whole_gap": (
+        "n = min(counts[e_star], (load[r_max] - load[r_min]) // 2)",
+        "n = min(counts[e_star], load[r_max] - load[r_min])"),
+    "reroute_never_diverts": (
+        "            if seen[e] >= keep and plan.slot_of[e] >= 0:",
+        "            if False:"),
+    "reroute_first_rows": (
+        "            if seen[e] >= keep and plan.slot_of[e] >= 0:",
+        "            if seen[e] < int(plan.divert[e]) and plan.slot_of[e] >= 0:"),
     "chunk_one_too_big": (
         "c = max(1, C // worst_per_token)",
         "c = max(1, C // worst_per_token + 1)"),
