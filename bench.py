@@ -199,7 +199,8 @@ class Layer:
         self.wl = replica_workload(wl, seed_offset)
         w = self.wl
         self.cfg = moe.make_config(w.T, w.H, w.E, w.k, w.F, w.S, w.factor,
-                                   w.n_chunks, w.dtype, w.renorm)
+                                   w.n_chunks, w.dtype, w.renorm,
+                                   w.redundant_slots)
         self.x = make_x(w, device)
         L = make_logits(w, self.x if w.routing == "router" else None)
         self.logits_np = L
@@ -216,7 +217,7 @@ class Layer:
         if capped:
             return self.cfg
         return self.cfg.with_(T=t1 - t0, ragged_buffer_factor=-1.0,
-                              n_chunks=0)
+                              n_chunks=0, redundant_slots=0)
 
     def step(self, ev=None):
         """One layer step through the entry points; ev(name) marks stages.
@@ -233,8 +234,14 @@ class Layer:
                                b["expert_offsets"], b["shard_counts"],
                                b["overflow_flag"], b["required_factor"],
                                b["capacity"])
+        planned = c.redundant_slots > 0
+        if planned:
+            mark("plan")
+            moe.moe_plan_duplication(c, b["expert_counts"], b["divert"],
+                                     b["slot_of"], b["group_expert"],
+                                     b["shard_after"], b["flag_after"])
         mark("flag")
-        flag = int(b["overflow_flag"].item())
+        flag = int((b["flag_after"] if planned else b["overflow_flag"]).item())
         if not flag:
             passes = [(0, c.T, True)]
         else:
@@ -246,12 +253,25 @@ class Layer:
         moe, b, W = self.moe, self.b, self.W
         for (t0, t1, capped) in passes:
             sc = self.sub(t0, t1, capped)
+            planned = capped and sc.redundant_slots > 0
             mark("permute")
-            moe.moe_permute(sc, self.x[t0:t1], b["topk_idx"][t0:t1], capped,
-                            b["x_sorted"], b["row_of"], b["sorted_token"],
-                            b["group_offsets"], b["uniq_offsets"],
-                            b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
-                            b["permute_ws"])
+            if planned:
+                moe.moe_permute_planned(
+                    sc, self.x[t0:t1], b["topk_idx"][t0:t1], capped,
+                    b["divert"], b["slot_of"], b["x_sorted"], b["row_of"],
+                    b["sorted_token"], b["group_offsets"], b["uniq_offsets"],
+                    b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
+                    b["permute_ws"])
+                groups = dict(n_groups=sc.E + sc.S * sc.redundant_slots,
+                              group_expert=b["group_expert"])
+            else:
+                moe.moe_permute(sc, self.x[t0:t1], b["topk_idx"][t0:t1],
+                                capped, b["x_sorted"], b["row_of"],
+                                b["sorted_token"], b["group_offsets"],
+                                b["uniq_offsets"], b["uniq_tokens"],
+                                b["expand_idx"], b["n_dropped"],
+                                b["permute_ws"])
+                groups = {}
             if self.dispatch_only:
                 # no expert FFN: the combine reads the permuted rows back
                 mark("combine")
@@ -260,10 +280,10 @@ class Layer:
                 continue
             mark("gmm_gate_up")
             moe.moe_gmm_gate_up(sc, b["x_sorted"], b["group_offsets"], W[0],
-                                W[1], b["h"], b["status"])
+                                W[1], b["h"], b["status"], **groups)
             mark("gmm_down")
             moe.moe_gmm_down(sc, b["h"], b["group_offsets"], W[2],
-                             b["y_sorted"], b["status"])
+                             b["y_sorted"], b["status"], **groups)
             mark("combine")
             moe.moe_combine(sc, b["y_sorted"], b["row_of"],
                             b["topk_w"][t0:t1], b["y"][t0:t1])
@@ -301,12 +321,12 @@ class StageTimer:
         return out
 
 
-def launches_per_step(passes, mode, dispatch_only=False):
+def launches_per_step(passes, mode, dispatch_only=False, planned=0):
     """Kernel launches of one step: route 1 (+ check 1 with the fallback),
     then per pass permute 5 (block counts, expert scan, assign, dedup scan,
     row scatter), GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the sweep)."""
     per = 6 if dispatch_only else 8
-    return (2 if mode == "fallback" else 1) + \
+    return (2 if mode == "fallback" else 1) + planned + \
         sum(per for (t0, t1, _) in passes if t1 > t0)
 
 
@@ -318,6 +338,16 @@ def pass_accounting(layer, passes):
     C = layer.moe.moe_capacity_rows(layer.cfg)
     out = []
     for (t0, t1, capped) in passes:
+        if capped and layer.cfg.redundant_slots > 0:
+            # virtual groups of the plan: rows kept, distinct experts used
+            G = w.E + w.S * layer.cfg.redundant_slots
+            off = layer.b["group_offsets"][:G + 1].cpu().numpy()
+            gexp = layer.b["group_expert"][:G].cpu().numpy()
+            sizes = np.diff(off)
+            out.append({"T": t1 - t0, "R": int(off[G]),
+                        "E_act": len(set(int(gexp[g]) for g in range(G)
+                                         if sizes[g] > 0))})
+            continue
         sub = idx[t0:t1].reshape(-1)
         counts = torch.bincount(sub, minlength=w.E).cpu().numpy()
         if capped and C >= 0:
@@ -386,6 +416,9 @@ def main():
                              "sweep"],
                     help="sweep: routing/permute/dedup only (no expert FFN)")
     ap.add_argument("--sweep-T", type=int, default=65536)
+    ap.add_argument("--redundant-slots", type=int, default=0,
+                    help="duplicate-expert slots per shard (dynamic "
+                         "redundancy; 0 = off)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count T")
     ap.add_argument("--mode", default="fallback",
@@ -410,6 +443,9 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wl = workload_by_name(args.workload, args.sweep_T, args.routing)
+    if args.redundant_slots > 0:
+        wl = wl.with_(redundant_slots=args.redundant_slots,
+                      name=f"{wl.name}_B{args.redundant_slots}")
     if args.tokens > 0:
         wl = wl.with_(T=args.tokens, name=f"{wl.name}_T{args.tokens}")
     if args.routing and args.workload != "sweep":
@@ -547,6 +583,7 @@ def main():
             "routing": layer.wl.routing + (f" s={layer.wl.zipf_s}"
                                            if layer.wl.routing == "zipf"
                                            else ""),
+            "redundant_slots": layer.wl.redundant_slots,
             "mode": {"fallback": "moe_dropless_fallback=layer",
                      "capped": "capped path only",
                      "dropless": "one uncapped pass"}[args.mode],
@@ -556,8 +593,10 @@ def main():
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "wall_s_timed_loop": round(wall, 3),
-        "gpu_launches": launches_per_step(passes, args.mode,
-                                          layer.dispatch_only) * args.steps,
+        "gpu_launches": launches_per_step(
+            passes, args.mode, layer.dispatch_only,
+            int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"))
+        * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }

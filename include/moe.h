@@ -100,6 +100,11 @@ typedef struct {
   /* Combine weights: 0 = softmax over all E logits read at the chosen
    * experts; 1 = softmax over the k chosen logits.                        */
   int32_t renorm;
+  /* Dynamic redundant experts [PR4760]: spare duplicate slots per shard
+   * (num_slots_B); 0 = off.  With B > 0 the layer plans duplicates of the
+   * hottest experts (moe_plan_duplication) before its overflow check.
+   * Needs E + S*B <= 1024.                                                */
+  int32_t redundant_slots;
 } moe_config_t;
 
 /* ----------------------------------------------------------------------
@@ -224,12 +229,17 @@ moe_status_t moe_gmm_swiglu(const moe_config_t *cfg, const void *x_sorted,
 
 /* The two halves of moe_gmm_swiglu, one kernel launch each (same rules):
  * moe_gmm_gate_up writes h = silu(x_sorted w_gate[e]) * (x_sorted w_up[e]);
- * moe_gmm_down writes y_sorted = h w_down[e].                             */
-moe_status_t moe_gmm_gate_up(const moe_config_t *cfg, const void *x_sorted,
+ * moe_gmm_down writes y_sorted = h w_down[e].  n_groups = 0 and
+ * group_expert = NULL mean the E experts' own groups; otherwise the row
+ * groups and weight map of moe_gmm_swiglu_mapped.                         */
+moe_status_t moe_gmm_gate_up(const moe_config_t *cfg, int32_t n_groups,
+                             const int32_t *group_expert,
+                             const void *x_sorted,
                              const int32_t *group_offsets,
                              const void *w_gate, const void *w_up, void *h,
                              int32_t *status_word, moe_stream_t stream);
-moe_status_t moe_gmm_down(const moe_config_t *cfg, const void *h,
+moe_status_t moe_gmm_down(const moe_config_t *cfg, int32_t n_groups,
+                          const int32_t *group_expert, const void *h,
                           const int32_t *group_offsets, const void *w_down,
                           void *y_sorted, int32_t *status_word,
                           moe_stream_t stream);
@@ -260,11 +270,75 @@ moe_status_t moe_layer_dropless_chunked(const moe_config_t *cfg,
                                         moe_stream_t stream);
 
 /* ----------------------------------------------------------------------
+ * Dynamic redundant experts ("Moe dynamic redundancy", MaxText pull request
+ * 4760, review of plan_expert_duplication).  B = cfg->redundant_slots spare
+ * slots per shard; a slot holds a duplicate of one expert and computes with
+ * that expert's weights (on one GPU nothing is copied).
+ * Virtual groups: shard s owns groups [s*(E/S+B), (s+1)*(E/S+B)): its E/S
+ * experts, then its B slots; G = S*(E/S+B) groups in all.
+ *
+ * moe_plan_duplication -- one warp, at most S*B rounds.  Each round takes
+ * the most loaded shard (ties: lower index), its hottest expert that has
+ * rows and is not yet duplicated (has_candidate; ties: lower index), and
+ * the least loaded other shard with a free slot; it stops when either is
+ * missing or the gap is zero, else moves n = min(rows of e,
+ * (load_max - load_min) / 2) rows of e to the next free slot of that shard.
+ *   expert_counts       in  [E] rows per expert (moe_check_overflow)
+ *   divert              out [E] rows of e moved to its duplicate
+ *   slot_of             out [E] virtual group of e's duplicate, -1 if none
+ *   group_expert        out [G] expert behind each virtual group, -1 for an
+ *                           unused slot
+ *   shard_counts_after  out [S] shard loads after the diversion
+ *   overflow_flag_after out [1] 1 iff some load after > C (0 if uncapped)
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_plan_duplication(const moe_config_t *cfg,
+                                  const int32_t *expert_counts,
+                                  int32_t *divert, int32_t *slot_of,
+                                  int32_t *group_expert,
+                                  int32_t *shard_counts_after,
+                                  int32_t *overflow_flag_after,
+                                  moe_stream_t stream);
+
+/* moe_permute_planned -- moe_permute over the virtual groups of a plan: the
+ * last divert[e] rows of expert e (token order) go to group slot_of[e], the
+ * rest to e's own group; capacity and dedup apply per shard of the virtual
+ * layout.  group_offsets has G+1 entries; the other outputs and the
+ * workspace (moe_workspace_bytes(cfg, MOE_WS_PERMUTE)) are those of
+ * moe_permute. */
+moe_status_t moe_permute_planned(const moe_config_t *cfg, const void *x,
+                                 const int32_t *topk_idx, int32_t capped,
+                                 const int32_t *divert,
+                                 const int32_t *slot_of, void *x_sorted,
+                                 int32_t *row_of, int32_t *sorted_token,
+                                 int32_t *group_offsets,
+                                 int32_t *uniq_offsets, int32_t *uniq_tokens,
+                                 int32_t *expand_idx, int32_t *n_dropped,
+                                 void *workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
+
+/* moe_gmm_swiglu_mapped -- moe_gmm_swiglu over n_groups row groups where
+ * group g computes with the weights of expert group_expert[g] (device,
+ * [n_groups]; a group of an expert < 0 must be empty).  group_offsets has
+ * n_groups+1 entries, n_groups <= 1024. */
+moe_status_t moe_gmm_swiglu_mapped(const moe_config_t *cfg, int32_t n_groups,
+                                   const int32_t *group_expert,
+                                   const void *x_sorted,
+                                   const int32_t *group_offsets,
+                                   const void *w_gate, const void *w_up,
+                                   const void *w_down, void *h,
+                                   void *y_sorted, int32_t *status_word,
+                                   moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
  * moe_layer -- the whole layer (an extension composing the calls above).
  *   MOE_MODE_FALLBACK_LAYER: route, check, read the flag; no overflow -> the
  *     capped path; overflow -> the chunked dropless fallback, reusing the
- *     routing [PR5920 How, moe_dropless_fallback=layer].
- *   MOE_MODE_CAPPED: the capped path only; rows past C are dropped.
+ *     routing [PR5920 How, moe_dropless_fallback=layer].  With
+ *     cfg->redundant_slots > 0 the check is taken after
+ *     moe_plan_duplication, on the shard loads of the virtual groups, and
+ *     the capped path runs over those groups.
+ *   MOE_MODE_CAPPED: the capped path only; rows past C are dropped (over
+ *     the virtual groups of a plan when cfg->redundant_slots > 0).
  *   MOE_MODE_DROPLESS: one uncapped pass (force_dropless).
  * info (host, may be NULL) receives what the call learned; workspace:
  * moe_workspace_bytes(cfg, MOE_WS_LAYER).

@@ -30,7 +30,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", c_int32), ("H", c_int32), ("E", c_int32),
                 ("k", c_int32), ("F", c_int32), ("S", c_int32),
                 ("ragged_buffer_factor", c_float), ("n_chunks", c_int32),
-                ("dtype", c_int), ("renorm", c_int32)]
+                ("dtype", c_int), ("renorm", c_int32),
+                ("redundant_slots", c_int32)]
 
     def with_(self, **kw) -> "MoeConfig":
         c = MoeConfig()
@@ -84,8 +85,13 @@ def _declare(h):
         "moe_permute_noalloc": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P,
                                 P],
         "moe_gmm_swiglu": [cfg, P, P, P, P, P, P, P, P, P],
-        "moe_gmm_gate_up": [cfg, P, P, P, P, P, P, P],
-        "moe_gmm_down": [cfg, P, P, P, P, P, P],
+        "moe_plan_duplication": [cfg, P, P, P, P, P, P, P],
+        "moe_permute_planned": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P,
+                                P, P, P, c_size_t, P],
+        "moe_gmm_swiglu_mapped": [cfg, c_int32, P, P, P, P, P, P, P, P, P,
+                                  P],
+        "moe_gmm_gate_up": [cfg, c_int32, P, P, P, P, P, P, P, P],
+        "moe_gmm_down": [cfg, c_int32, P, P, P, P, P, P, P],
         "moe_combine": [cfg, P, P, P, P, P],
         "moe_layer_dropless_chunked": [cfg, P, P, P, P, P, P, P, P, c_size_t,
                                        P],
@@ -153,10 +159,10 @@ def _check(status, where):
 
 
 def make_config(T, H, E, k, F, S, factor=2.0, n_chunks=0, dtype="bf16",
-                renorm=False) -> MoeConfig:
+                renorm=False, redundant_slots=0) -> MoeConfig:
     return MoeConfig(T, H, E, k, F, S, float(factor), n_chunks,
                      MOE_F32 if dtype in ("f32", "float32") else MOE_BF16,
-                     1 if renorm else 0)
+                     1 if renorm else 0, redundant_slots)
 
 
 # --------------------------------------------------------- entry points ---
@@ -233,18 +239,52 @@ def moe_gmm_swiglu(cfg, x_sorted, group_offsets, w_gate, w_up, w_down, h,
 
 
 def moe_gmm_gate_up(cfg, x_sorted, group_offsets, w_gate, w_up, h,
-                    status_word=None, stream=None):
+                    status_word=None, stream=None, n_groups=0,
+                    group_expert=None):
     _check(lib().moe_gmm_gate_up(
-        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
-        _ptr(w_up), _ptr(h), _ptr(status_word), _stream(stream)),
-        "moe_gmm_gate_up")
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(x_sorted),
+        _ptr(group_offsets), _ptr(w_gate), _ptr(w_up), _ptr(h),
+        _ptr(status_word), _stream(stream)), "moe_gmm_gate_up")
 
 
 def moe_gmm_down(cfg, h, group_offsets, w_down, y_sorted, status_word=None,
-                 stream=None):
+                 stream=None, n_groups=0, group_expert=None):
     _check(lib().moe_gmm_down(
-        ctypes.byref(cfg), _ptr(h), _ptr(group_offsets), _ptr(w_down),
-        _ptr(y_sorted), _ptr(status_word), _stream(stream)), "moe_gmm_down")
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(h),
+        _ptr(group_offsets), _ptr(w_down), _ptr(y_sorted), _ptr(status_word),
+        _stream(stream)), "moe_gmm_down")
+
+
+def moe_plan_duplication(cfg, expert_counts, divert, slot_of, group_expert,
+                         shard_counts_after, overflow_flag_after,
+                         stream=None):
+    _check(lib().moe_plan_duplication(
+        ctypes.byref(cfg), _ptr(expert_counts), _ptr(divert), _ptr(slot_of),
+        _ptr(group_expert), _ptr(shard_counts_after),
+        _ptr(overflow_flag_after), _stream(stream)), "moe_plan_duplication")
+
+
+def moe_permute_planned(cfg, x, topk_idx, capped, divert, slot_of, x_sorted,
+                        row_of, sorted_token, group_offsets, uniq_offsets,
+                        uniq_tokens, expand_idx, n_dropped, workspace,
+                        stream=None):
+    _check(lib().moe_permute_planned(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), 1 if capped else 0,
+        _ptr(divert), _ptr(slot_of), _ptr(x_sorted), _ptr(row_of),
+        _ptr(sorted_token), _ptr(group_offsets), _ptr(uniq_offsets),
+        _ptr(uniq_tokens), _ptr(expand_idx), _ptr(n_dropped),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "moe_permute_planned")
+
+
+def moe_gmm_swiglu_mapped(cfg, n_groups, group_expert, x_sorted,
+                          group_offsets, w_gate, w_up, w_down, h, y_sorted,
+                          status_word=None, stream=None):
+    _check(lib().moe_gmm_swiglu_mapped(
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(x_sorted),
+        _ptr(group_offsets), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(h),
+        _ptr(y_sorted), _ptr(status_word), _stream(stream)),
+        "moe_gmm_swiglu_mapped")
 
 
 def moe_combine(cfg, y_sorted, row_of, topk_w, y, stream=None):
@@ -331,7 +371,12 @@ def alloc_step_buffers(cfg, device="cuda"):
         "x_sorted": torch.empty((R, H), dtype=dt, device=device),
         "row_of": torch.empty((T, k), **i32),
         "sorted_token": torch.empty(max(R, 1), **i32),
-        "group_offsets": torch.empty(E + 1, **i32),
+        "group_offsets": torch.empty(E + S * cfg.redundant_slots + 1, **i32),
+        "divert": torch.empty(E, **i32),
+        "slot_of": torch.empty(E, **i32),
+        "group_expert": torch.empty(E + S * cfg.redundant_slots, **i32),
+        "shard_after": torch.empty(S, **i32),
+        "flag_after": torch.empty(1, **i32),
         "uniq_offsets": torch.empty(S + 1, **i32),
         "uniq_tokens": torch.empty(max(T * min(k, S), 1), **i32),
         "expand_idx": torch.empty(max(R, 1), **i32),

@@ -16,19 +16,23 @@
 
 namespace moe {
 
-cudaError_t launch_gmm1_f32(const moe_config_t& c, const void* x_sorted,
+cudaError_t launch_gmm1_f32(const moe_config_t& c, const Groups& g,
+                            const void* x_sorted,
                             const int32_t* group_offsets, const void* w_gate,
                             const void* w_up, void* h, cudaStream_t s);
-cudaError_t launch_gmm2_f32(const moe_config_t& c, const void* h,
-                            const int32_t* group_offsets, const void* w_down,
-                            void* y_sorted, cudaStream_t s);
-cudaError_t launch_gmm1_bf16(const moe_config_t& c, const void* x_sorted,
+cudaError_t launch_gmm2_f32(const moe_config_t& c, const Groups& g,
+                            const void* h, const int32_t* group_offsets,
+                            const void* w_down, void* y_sorted,
+                            cudaStream_t s);
+cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
+                             const void* x_sorted,
                              const int32_t* group_offsets, const void* w_gate,
                              const void* w_up, void* h, int32_t* status,
                              cudaStream_t s);
-cudaError_t launch_gmm2_bf16(const moe_config_t& c, const void* h,
-                             const int32_t* group_offsets, const void* w_down,
-                             void* y_sorted, int32_t* status, cudaStream_t s);
+cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
+                             const void* h, const int32_t* group_offsets,
+                             const void* w_down, void* y_sorted,
+                             int32_t* status, cudaStream_t s);
 
 int64_t capacity_rows(const moe_config_t& c) {
   const double f = static_cast<double>(c.ragged_buffer_factor);
@@ -58,32 +62,34 @@ int32_t chunk_tokens(const moe_config_t& c) {
   return static_cast<int32_t>(std::min<int64_t>(tok, c.T));
 }
 
-cudaError_t launch_gmm1(const moe_config_t& c, const void* x_sorted,
-                        const int32_t* group_offsets, const void* w_gate,
-                        const void* w_up, void* h, int32_t* status,
-                        cudaStream_t s) {
+cudaError_t launch_gmm1(const moe_config_t& c, const Groups& g,
+                        const void* x_sorted, const int32_t* group_offsets,
+                        const void* w_gate, const void* w_up, void* h,
+                        int32_t* status, cudaStream_t s) {
   if (c.dtype == MOE_F32)
-    return launch_gmm1_f32(c, x_sorted, group_offsets, w_gate, w_up, h, s);
-  return launch_gmm1_bf16(c, x_sorted, group_offsets, w_gate, w_up, h, status,
-                          s);
+    return launch_gmm1_f32(c, g, x_sorted, group_offsets, w_gate, w_up, h, s);
+  return launch_gmm1_bf16(c, g, x_sorted, group_offsets, w_gate, w_up, h,
+                          status, s);
 }
 
-cudaError_t launch_gmm2(const moe_config_t& c, const void* h,
+cudaError_t launch_gmm2(const moe_config_t& c, const Groups& g, const void* h,
                         const int32_t* group_offsets, const void* w_down,
                         void* y_sorted, int32_t* status, cudaStream_t s) {
   if (c.dtype == MOE_F32)
-    return launch_gmm2_f32(c, h, group_offsets, w_down, y_sorted, s);
-  return launch_gmm2_bf16(c, h, group_offsets, w_down, y_sorted, status, s);
+    return launch_gmm2_f32(c, g, h, group_offsets, w_down, y_sorted, s);
+  return launch_gmm2_bf16(c, g, h, group_offsets, w_down, y_sorted, status,
+                          s);
 }
 
-cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
-                       const int32_t* group_offsets, const void* w_gate,
-                       const void* w_up, const void* w_down, void* h,
-                       void* y_sorted, int32_t* status, cudaStream_t s) {
+cudaError_t launch_gmm(const moe_config_t& c, const Groups& g,
+                       const void* x_sorted, const int32_t* group_offsets,
+                       const void* w_gate, const void* w_up,
+                       const void* w_down, void* h, void* y_sorted,
+                       int32_t* status, cudaStream_t s) {
   cudaError_t e =
-      launch_gmm1(c, x_sorted, group_offsets, w_gate, w_up, h, status, s);
+      launch_gmm1(c, g, x_sorted, group_offsets, w_gate, w_up, h, status, s);
   if (e != cudaSuccess) return e;
-  return launch_gmm2(c, h, group_offsets, w_down, y_sorted, status, s);
+  return launch_gmm2(c, g, h, group_offsets, w_down, y_sorted, status, s);
 }
 
 moe_status_t validate(const moe_config_t* c) {
@@ -97,6 +103,11 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
   if (c->n_chunks < 0) return MOE_ERR_INVALID_ARG;
   if (std::isnan(c->ragged_buffer_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->redundant_slots < 0 ||
+      static_cast<int64_t>(c->E) +
+              static_cast<int64_t>(c->S) * c->redundant_slots >
+          kMaxExperts)
+    return MOE_ERR_INVALID_ARG;
   const int eb = elem_bytes(c->dtype);
   if ((static_cast<int64_t>(c->H) * eb) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if ((static_cast<int64_t>(c->F) * eb) % 16 != 0) return MOE_ERR_INVALID_ARG;
@@ -131,12 +142,17 @@ LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
   b.cap = cv.take<int32_t>(1);
   b.row_of = cv.take<int32_t>(tk);
   b.sorted_token = cv.take<int32_t>(tk);
-  b.group_offsets = cv.take<int32_t>(c.E + 1);
+  b.group_offsets = cv.take<int32_t>(num_groups(c) + 1);
   b.uniq_offsets = cv.take<int32_t>(c.S + 1);
   b.uniq_tokens =
       cv.take<int32_t>(static_cast<size_t>(T) * std::min(c.k, c.S));
   b.expand_idx = cv.take<int32_t>(tk);
   b.n_dropped = cv.take<int32_t>(1);
+  b.divert = cv.take<int32_t>(c.E);
+  b.slot_of = cv.take<int32_t>(c.E);
+  b.group_expert = cv.take<int32_t>(num_groups(c));
+  b.shard_after = cv.take<int32_t>(c.S);
+  b.flag_after = cv.take<int32_t>(1);
   b.pws = carve_permute_scratch(cv, T, c.E, c.k, c.S);
   b.x_sorted = cv.take<char>(tk * c.H * eb);
   b.h = cv.take<char>(tk * static_cast<size_t>(c.F) * eb);
@@ -156,6 +172,7 @@ moe_config_t sub_config(const moe_config_t& c, int T) {
   s.T = T;
   s.ragged_buffer_factor = -1.0f;
   s.n_chunks = 0;
+  s.redundant_slots = 0;
   return s;
 }
 
@@ -164,14 +181,22 @@ moe_config_t sub_config(const moe_config_t& c, int T) {
 cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const float* topk_w, int64_t cap, const void* wg,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
-                 int32_t* status, cudaStream_t s) {
+                 int32_t* status, cudaStream_t s, bool planned) {
+  PermutePlan plan;
+  Groups groups = identity_groups(c);
+  if (planned && c.redundant_slots > 0) {
+    plan.divert = b.divert;
+    plan.slot_of = b.slot_of;
+    plan.B = c.redundant_slots;
+    groups = {num_groups(c), b.group_expert};
+  }
   cudaError_t e = launch_permute(c, x, topk_idx, cap, b.x_sorted, b.row_of,
                                  b.sorted_token, b.group_offsets,
                                  b.uniq_offsets, b.uniq_tokens, b.expand_idx,
-                                 b.n_dropped, b.pws, status, s);
+                                 b.n_dropped, b.pws, status, s, plan);
   if (e != cudaSuccess) return e;
-  e = launch_gmm(c, b.x_sorted, b.group_offsets, wg, wu, wd, b.h, b.y_sorted,
-                 status, s);
+  e = launch_gmm(c, groups, b.x_sorted, b.group_offsets, wg, wu, wd, b.h,
+                 b.y_sorted, status, s);
   if (e != cudaSuccess) return e;
   return launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
 }
@@ -342,40 +367,143 @@ moe_status_t moe_gmm_swiglu(const moe_config_t* cfg, const void* x_sorted,
       !weights_ok(w_gate, w_up, w_down) || !ok_ptr(h, true) ||
       !ok_ptr(y_sorted, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_gmm(*cfg, x_sorted, group_offsets, w_gate, w_up,
-                                w_down, h, y_sorted, status_word, stream));
+  return cuda_status(launch_gmm(*cfg, identity_groups(*cfg), x_sorted,
+                                group_offsets, w_gate, w_up, w_down, h,
+                                y_sorted, status_word, stream));
 }
 
-moe_status_t moe_gmm_gate_up(const moe_config_t* cfg, const void* x_sorted,
+namespace {
+// n_groups = 0 with a null map: the experts' own groups.
+bool groups_of(const moe_config_t& c, int32_t n, const int32_t* map,
+               Groups* g) {
+  if (n == 0 && map == nullptr) {
+    *g = identity_groups(c);
+    return true;
+  }
+  if (n < 1 || n > kMaxExperts || !ok_ptr(map, false)) return false;
+  *g = {n, map};
+  return true;
+}
+}  // namespace
+
+moe_status_t moe_gmm_gate_up(const moe_config_t* cfg, int32_t n_groups,
+                             const int32_t* group_expert,
+                             const void* x_sorted,
                              const int32_t* group_offsets, const void* w_gate,
                              const void* w_up, void* h, int32_t* status_word,
                              moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
-  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  Groups g;
+  if (cfg->F < 1 || !groups_of(*cfg, n_groups, group_expert, &g))
+    return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
   if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
       !ok_ptr(w_gate, true) || !ok_ptr(w_up, true) || !ok_ptr(h, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_gmm1(*cfg, x_sorted, group_offsets, w_gate, w_up,
-                                 h, status_word, stream));
+  return cuda_status(launch_gmm1(*cfg, g, x_sorted, group_offsets, w_gate,
+                                 w_up, h, status_word, stream));
 }
 
-moe_status_t moe_gmm_down(const moe_config_t* cfg, const void* h,
+moe_status_t moe_gmm_down(const moe_config_t* cfg, int32_t n_groups,
+                          const int32_t* group_expert, const void* h,
                           const int32_t* group_offsets, const void* w_down,
                           void* y_sorted, int32_t* status_word,
                           moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
-  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  Groups g;
+  if (cfg->F < 1 || !groups_of(*cfg, n_groups, group_expert, &g))
+    return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
   if (!ok_ptr(h, true) || !ok_ptr(group_offsets, false) ||
       !ok_ptr(w_down, true) || !ok_ptr(y_sorted, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_gmm2(*cfg, h, group_offsets, w_down, y_sorted,
+  return cuda_status(launch_gmm2(*cfg, g, h, group_offsets, w_down, y_sorted,
                                  status_word, stream));
+}
+
+moe_status_t moe_plan_duplication(const moe_config_t* cfg,
+                                  const int32_t* expert_counts,
+                                  int32_t* divert, int32_t* slot_of,
+                                  int32_t* group_expert,
+                                  int32_t* shard_counts_after,
+                                  int32_t* overflow_flag_after,
+                                  moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(expert_counts, false) || !ok_ptr(divert, false) ||
+      !ok_ptr(slot_of, false) || !ok_ptr(group_expert, false) ||
+      !ok_ptr(shard_counts_after, false) || !ok_ptr(overflow_flag_after, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_plan(*cfg, expert_counts, divert, slot_of,
+                                 group_expert, shard_counts_after,
+                                 overflow_flag_after, stream));
+}
+
+moe_status_t moe_permute_planned(const moe_config_t* cfg, const void* x,
+                                 const int32_t* topk_idx, int32_t capped,
+                                 const int32_t* divert,
+                                 const int32_t* slot_of, void* x_sorted,
+                                 int32_t* row_of, int32_t* sorted_token,
+                                 int32_t* group_offsets,
+                                 int32_t* uniq_offsets, int32_t* uniq_tokens,
+                                 int32_t* expand_idx, int32_t* n_dropped,
+                                 void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(uniq_offsets, false) ||
+      !ok_ptr(n_dropped, false) || !ok_ptr(divert, false) ||
+      !ok_ptr(slot_of, false))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 &&
+      (!ok_ptr(x, true) || !ok_ptr(topk_idx, false) ||
+       !ok_ptr(x_sorted, true) || !ok_ptr(row_of, false) ||
+       !ok_ptr(sorted_token, false) || !ok_ptr(uniq_tokens, false) ||
+       !ok_ptr(expand_idx, false)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
+  if (workspace == nullptr || workspace_bytes < need ||
+      !ok_ptr(workspace, true))
+    return MOE_ERR_WORKSPACE;
+  Carve cv(workspace);
+  const PermuteScratch ws =
+      carve_permute_scratch(cv, cfg->T, cfg->E, cfg->k, cfg->S);
+  PermutePlan plan;
+  plan.divert = divert;
+  plan.slot_of = slot_of;
+  plan.B = cfg->redundant_slots;
+  const int64_t cap = capped ? capacity_rows(*cfg) : -1;
+  return cuda_status(launch_permute(*cfg, x, topk_idx, cap, x_sorted, row_of,
+                                    sorted_token, group_offsets, uniq_offsets,
+                                    uniq_tokens, expand_idx, n_dropped, ws,
+                                    nullptr, stream, plan));
+}
+
+moe_status_t moe_gmm_swiglu_mapped(const moe_config_t* cfg, int32_t n_groups,
+                                   const int32_t* group_expert,
+                                   const void* x_sorted,
+                                   const int32_t* group_offsets,
+                                   const void* w_gate, const void* w_up,
+                                   const void* w_down, void* h,
+                                   void* y_sorted, int32_t* status_word,
+                                   moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1 || n_groups < 1 || n_groups > kMaxExperts)
+    return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+      !ok_ptr(group_expert, false) || !weights_ok(w_gate, w_up, w_down) ||
+      !ok_ptr(h, true) || !ok_ptr(y_sorted, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gmm(*cfg, {n_groups, group_expert}, x_sorted,
+                                group_offsets, w_gate, w_up, w_down, h,
+                                y_sorted, status_word, stream));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_sorted,
@@ -453,28 +581,37 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x,
       workspace_bytes < layer_bytes(*cfg, cfg->T))
     return MOE_ERR_WORKSPACE;
   const LayerBufs b = carve_layer(workspace, *cfg, cfg->T, nullptr);
+  const bool planned = cfg->redundant_slots > 0 && mode != MOE_MODE_DROPLESS;
   cudaError_t e = launch_route(*cfg, logits, b.topk_idx, b.topk_w,
                                status_word, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (mode == MOE_MODE_CAPPED)
-    return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, cap, w_gate, w_up,
-                            w_down, y, b, status_word, stream));
   if (mode == MOE_MODE_DROPLESS)
     return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, -1, w_gate, w_up,
                             w_down, y, b, status_word, stream));
-  // moe_dropless_fallback=layer: check, read the flag, branch.
-  e = launch_check(*cfg, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
-                   b.req, b.cap, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (planned || mode == MOE_MODE_FALLBACK_LAYER) {
+    e = launch_check(*cfg, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
+                     b.req, b.cap, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (planned) {
+    e = launch_plan(*cfg, b.counts, b.divert, b.slot_of, b.group_expert,
+                    b.shard_after, b.flag_after, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (mode == MOE_MODE_CAPPED)
+    return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, cap, w_gate, w_up,
+                            w_down, y, b, status_word, stream, planned));
+  // moe_dropless_fallback=layer: check (after the plan), read the flag,
+  // branch.
   int32_t flag = 0;
-  e = cudaMemcpyAsync(&flag, b.flag, sizeof(flag), cudaMemcpyDeviceToHost,
-                      stream);
+  e = cudaMemcpyAsync(&flag, planned ? b.flag_after : b.flag, sizeof(flag),
+                      cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (info) info->overflow = flag;
   if (!flag)
     return cuda_status(pass(*cfg, x, b.topk_idx, b.topk_w, cap, w_gate, w_up,
-                            w_down, y, b, status_word, stream));
+                            w_down, y, b, status_word, stream, planned));
   int32_t n = 0;
   e = chunked_passes(*cfg, x, b.topk_idx, b.topk_w, w_gate, w_up, w_down, y,
                      b, status_word, stream, &n);

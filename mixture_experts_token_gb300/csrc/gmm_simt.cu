@@ -39,7 +39,8 @@ __device__ __forceinline__ int expert_of_row(const int32_t* off, int E,
 template <int MODE>
 __global__ void __launch_bounds__(256) gmm_f32_kernel(
     const float* __restrict__ a, const int32_t* __restrict__ off, int E,
-    int K, int N, const float* __restrict__ w0, const float* __restrict__ w1,
+    const int32_t* __restrict__ group_expert, int K, int N,
+    const float* __restrict__ w0, const float* __restrict__ w1,
     float* __restrict__ out, int rows_alloc) {
   __shared__ float sa[BR][KS + 1];
   const int R = __ldg(off + E);
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(256) gmm_f32_kernel(
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       rr[q] = r0 + ty + 8 * q;
-      ee[q] = rr[q] < R ? expert_of_row(off, E, rr[q]) : 0;
+      const int g = rr[q] < R ? expert_of_row(off, E, rr[q]) : 0;
+      ee[q] = group_expert ? max(__ldg(group_expert + g), 0) : g;
     }
     for (int k0 = 0; k0 < K; k0 += KS) {
       __syncthreads();
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(256) gmm_f32_kernel(
 
 }  // namespace
 
-cudaError_t launch_gmm1_f32(const moe_config_t& c, const void* x_sorted,
+cudaError_t launch_gmm1_f32(const moe_config_t& c, const Groups& g,
+                            const void* x_sorted,
                             const int32_t* group_offsets, const void* w_gate,
                             const void* w_up, void* h, cudaStream_t s) {
   const long long rows = static_cast<long long>(c.T) * c.k;
@@ -102,15 +105,16 @@ cudaError_t launch_gmm1_f32(const moe_config_t& c, const void* x_sorted,
       std::min<long long>((rows + BR - 1) / BR, 65535));
   const dim3 g1((c.F + BN - 1) / BN, gy);
   gmm_f32_kernel<0><<<g1, block, 0, s>>>(
-      static_cast<const float*>(x_sorted), group_offsets, c.E, c.H, c.F,
-      static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
+      static_cast<const float*>(x_sorted), group_offsets, g.n, g.map, c.H,
+      c.F, static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
       static_cast<float*>(h), static_cast<int>(rows));
   return cudaGetLastError();
 }
 
-cudaError_t launch_gmm2_f32(const moe_config_t& c, const void* h,
-                            const int32_t* group_offsets, const void* w_down,
-                            void* y_sorted, cudaStream_t s) {
+cudaError_t launch_gmm2_f32(const moe_config_t& c, const Groups& g,
+                            const void* h, const int32_t* group_offsets,
+                            const void* w_down, void* y_sorted,
+                            cudaStream_t s) {
   const long long rows = static_cast<long long>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   const dim3 block(BN, 8);
@@ -118,7 +122,7 @@ cudaError_t launch_gmm2_f32(const moe_config_t& c, const void* h,
       std::min<long long>((rows + BR - 1) / BR, 65535));
   const dim3 g2((c.H + BN - 1) / BN, gy);
   gmm_f32_kernel<1><<<g2, block, 0, s>>>(
-      static_cast<const float*>(h), group_offsets, c.E, c.F, c.H,
+      static_cast<const float*>(h), group_offsets, g.n, g.map, c.F, c.H,
       static_cast<const float*>(w_down), nullptr,
       static_cast<float*>(y_sorted), static_cast<int>(rows));
   return cudaGetLastError();

@@ -64,7 +64,8 @@ struct Tile {
 
 struct Params {
   const int32_t* group_offsets;  // [E+1]
-  int E;
+  const int32_t* group_expert;   // [E] weights of each group; null: identity
+  int E;                         // row groups
   int K;        // reduction length: H (GEMM1) or F (GEMM2)
   int n_tiles;  // output column tiles per expert
   __nv_bfloat16* out;
@@ -389,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int e, m, n;
         decode_tile(tile, mt_prefix, p.E, p.n_tiles, e, m, n);
         const int a_row = goff[e] + m * BM;
-        const int b_row = e * p.K;
+        const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
+        const int b_row = we * p.K;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
                          p.status)) {
@@ -615,7 +617,8 @@ bool gmm_tc_supported(const moe_config_t& c) {
          c.H >= 128 && c.F >= 128;
 }
 
-cudaError_t launch_gmm1_bf16(const moe_config_t& c, const void* x_sorted,
+cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
+                             const void* x_sorted,
                              const int32_t* group_offsets, const void* w_gate,
                              const void* w_up, void* h, int32_t* status,
                              cudaStream_t s) {
@@ -627,14 +630,15 @@ cudaError_t launch_gmm1_bf16(const moe_config_t& c, const void* x_sorted,
       !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, 64) ||
       !tc::make_map(&bu, w_up, c.F, E * c.H, 64, 64))
     return cudaErrorInvalidValue;
-  tc::Params p1{group_offsets, c.E, c.H, c.F / 128,
+  tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
   return tc::launch_one<0, 256>(a1, bg, bu, p1, s);
 }
 
-cudaError_t launch_gmm2_bf16(const moe_config_t& c, const void* h,
-                             const int32_t* group_offsets, const void* w_down,
-                             void* y_sorted, int32_t* status, cudaStream_t s) {
+cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
+                             const void* h, const int32_t* group_offsets,
+                             const void* w_down, void* y_sorted,
+                             int32_t* status, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   CUtensorMap a2, bd;
@@ -643,11 +647,11 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const void* h,
       !tc::make_map(&bd, w_down, c.H, E * c.F, 64, 64))
     return cudaErrorInvalidValue;
   if (c.H % 256 == 0) {
-    tc::Params p2{group_offsets, c.E, c.F, c.H / 256,
+    tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
     return tc::launch_one<1, 256>(a2, bd, bd, p2, s);
   }
-  tc::Params p2{group_offsets, c.E, c.F, c.H / 128,
+  tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 128,
                 static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
   return tc::launch_one<1, 128>(a2, bd, bd, p2, s);
 }

@@ -43,12 +43,24 @@ struct Carve {
 // Permute scratch for `T` tokens (counting-sort block tables).
 struct PermuteScratch {
   int32_t* block_base;  // [nb, E] per-block expert counts, then bases
-  int32_t* kept;        // [E] kept rows per expert
-  int32_t* goff;        // [E] kept group offsets
+  int32_t* etab;        // [6, E] per expert: rows kept in its own group,
+                        // that group's kept offset, rows routed to its own
+                        // group, rows kept in its duplicate slot, the
+                        // slot's kept offset, the slot's shard
   int32_t* block_ucnt;  // [nb, S] per-block unique counts, then bases
-  int32_t* urank;       // [T*k] rank of (t,j)'s token inside its block/shard
+  int32_t* urank;       // [T*k] (rank of (t,j)'s token among the members of
+                        // its shard in its block) * 64 + shard, -1 dropped
   int32_t* scal;        // [4] scalars
 };
+// Redundancy plan of a permute (all null / 0: none).
+struct PermutePlan {
+  const int32_t* divert = nullptr;   // [E]
+  const int32_t* slot_of = nullptr;  // [E]
+  int B = 0;                         // slots per shard
+};
+inline int num_groups(const moe_config_t& c) {
+  return c.S * (c.E / c.S + c.redundant_slots);
+}
 size_t permute_scratch_bytes(int T, int E, int k, int S);
 PermuteScratch carve_permute_scratch(Carve& c, int T, int E, int k, int S);
 
@@ -67,19 +79,32 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
                            int32_t* uniq_offsets, int32_t* uniq_tokens,
                            int32_t* expand_idx, int32_t* n_dropped,
                            const PermuteScratch& ws, int32_t* status,
-                           cudaStream_t s);
+                           cudaStream_t s, const PermutePlan& plan = {});
+cudaError_t launch_plan(const moe_config_t& c, const int32_t* counts,
+                        int32_t* divert, int32_t* slot_of,
+                        int32_t* group_expert, int32_t* shard_after,
+                        int32_t* flag_after, cudaStream_t s);
+// Row groups of a grouped GEMM: n groups; group g uses the weights of
+// expert map[g] (identity when map is null).
+struct Groups {
+  int n;
+  const int32_t* map;
+};
+inline Groups identity_groups(const moe_config_t& c) { return {c.E, nullptr}; }
+
 // GEMM1 + SwiGLU (h) and GEMM2 (y_sorted), each one kernel launch.
-cudaError_t launch_gmm1(const moe_config_t& c, const void* x_sorted,
-                        const int32_t* group_offsets, const void* w_gate,
-                        const void* w_up, void* h, int32_t* status,
-                        cudaStream_t s);
-cudaError_t launch_gmm2(const moe_config_t& c, const void* h,
+cudaError_t launch_gmm1(const moe_config_t& c, const Groups& g,
+                        const void* x_sorted, const int32_t* group_offsets,
+                        const void* w_gate, const void* w_up, void* h,
+                        int32_t* status, cudaStream_t s);
+cudaError_t launch_gmm2(const moe_config_t& c, const Groups& g, const void* h,
                         const int32_t* group_offsets, const void* w_down,
                         void* y_sorted, int32_t* status, cudaStream_t s);
-cudaError_t launch_gmm(const moe_config_t& c, const void* x_sorted,
-                       const int32_t* group_offsets, const void* w_gate,
-                       const void* w_up, const void* w_down, void* h,
-                       void* y_sorted, int32_t* status, cudaStream_t s);
+cudaError_t launch_gmm(const moe_config_t& c, const Groups& g,
+                       const void* x_sorted, const int32_t* group_offsets,
+                       const void* w_gate, const void* w_up,
+                       const void* w_down, void* h, void* y_sorted,
+                       int32_t* status, cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t& c, const void* y_sorted,
                            const int32_t* row_of, const float* topk_w,
                            void* y, cudaStream_t s);
@@ -90,6 +115,8 @@ struct LayerBufs {
   float *topk_w, *req;
   int32_t *row_of, *sorted_token, *group_offsets, *uniq_offsets,
       *uniq_tokens, *expand_idx, *n_dropped;
+  // redundancy plan (sized for cfg.redundant_slots; unused when 0)
+  int32_t *divert, *slot_of, *group_expert, *shard_after, *flag_after;
   PermuteScratch pws;
   void *x_sorted, *h, *y_sorted;
 };
@@ -97,11 +124,12 @@ LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
                       size_t* bytes);
 size_t layer_bytes(const moe_config_t& c, int T);
 moe_config_t sub_config(const moe_config_t& c, int T);
-// permute (cap, or uncapped when cap < 0) -> GEMM1 -> GEMM2 -> combine
+// permute (cap, or uncapped when cap < 0) -> GEMM1 -> GEMM2 -> combine;
+// with planned = true, over the virtual groups of the plan in b.
 cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const float* topk_w, int64_t cap, const void* wg,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
-                 int32_t* status, cudaStream_t s);
+                 int32_t* status, cudaStream_t s, bool planned = false);
 // the chunked dropless fallback over routing already in topk_idx/topk_w
 cudaError_t chunked_passes(const moe_config_t& c, const void* x,
                            const int32_t* topk_idx, const float* topk_w,

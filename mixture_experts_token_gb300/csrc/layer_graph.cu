@@ -63,12 +63,18 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   e = cudaStreamBeginCaptureToGraph(main_s.s, out->graph, nullptr, nullptr, 0,
                                     cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
+  const bool planned = c.redundant_slots > 0;
   if ((e = launch_route(c, logits, b.topk_idx, b.topk_w, status,
                         main_s.s)) != cudaSuccess ||
       (e = launch_check(c, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
                         b.req, b.cap, main_s.s)) != cudaSuccess)
     return e;
-  set_branch_kernel<<<1, 1, 0, main_s.s>>>(handle, b.flag);
+  if (planned &&
+      (e = launch_plan(c, b.counts, b.divert, b.slot_of, b.group_expert,
+                       b.shard_after, b.flag_after, main_s.s)) != cudaSuccess)
+    return e;
+  set_branch_kernel<<<1, 1, 0, main_s.s>>>(handle,
+                                           planned ? b.flag_after : b.flag);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   cudaStreamCaptureStatus cst;
@@ -103,7 +109,7 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
                                     0, cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
   e = pass(c, x, b.topk_idx, b.topk_w, capacity_rows(c), wg, wu, wd, y, b,
-           status, body_s.s);
+           status, body_s.s, planned);
   if (e != cudaSuccess) return e;
   if ((e = cudaStreamEndCapture(body_s.s, &tmp)) != cudaSuccess) return e;
 
@@ -111,7 +117,7 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
                                           cudaStreamSetCaptureDependencies);
   if (e != cudaSuccess) return e;
   if ((e = cudaStreamEndCapture(main_s.s, &tmp)) != cudaSuccess) return e;
-  out->flag = b.flag;
+  out->flag = planned ? b.flag_after : b.flag;
   return cudaGraphInstantiate(&out->exec, out->graph, 0);
 }
 

@@ -24,6 +24,12 @@
 //   4 scan_uniq   : per shard, exclusive scan of block member counts; |U_s|
 //   5 scatter     : one CTA per token: dedup indices, then x[t] read once
 //                   with 16-byte loads and written to each kept row
+// With a duplication plan ("Moe dynamic redundancy" (MaxText pull request
+// 4760), review of plan_expert_duplication) the groups are virtual: shard s
+// owns its E/S experts and then its B duplicate slots, and the last
+// divert[e] rows of expert e (token order) go to e's slot.  Kernel 2 splits
+// each expert's rows between its two groups before the capacity rule, and
+// kernel 3 places a row in the group its rank falls in.
 // Algorithmic traffic: T*H*b read + R_kept*H*b written (+ small index
 // arrays).
 #include "internal.h"
@@ -85,71 +91,98 @@ __device__ int block_exclusive_scan_1024(int v, int* warp_tot, int* total) {
   return r;
 }
 
-// One CTA of 1024 threads, thread e owns expert e.
+// One CTA of 1024 threads.  Thread e owns expert e (its block scan and the
+// split of its rows), thread g owns virtual group g (the scans over groups
+// and the capacity rule).  G <= 1024.
 __global__ void __launch_bounds__(1024) scan_experts_kernel(
-    int32_t* __restrict__ block_base, int nb, int E, int S, int cap,
-    int32_t* __restrict__ kept_out, int32_t* __restrict__ goff_out,
-    int32_t* __restrict__ group_offsets, int32_t* __restrict__ n_dropped) {
+    int32_t* __restrict__ block_base, int nb, int E, int S, int B, int cap,
+    const int32_t* __restrict__ divert, const int32_t* __restrict__ slot_of,
+    int32_t* __restrict__ etab, int32_t* __restrict__ group_offsets,
+    int32_t* __restrict__ n_dropped) {
+  __shared__ int cv[kMaxExperts];       // rows per virtual group
   __shared__ int scan[kMaxExperts + 1];
+  __shared__ int keptv[kMaxExperts];
+  __shared__ int goffv[kMaxExperts];
   __shared__ int warp_tot[32];
   __shared__ int total, ktotal;
-  const int e = threadIdx.x;
-  int c = 0;
-  if (e < E) {
+  const int tid = threadIdx.x;
+  const int Es = E / S, Gs = Es + B, G = S * Gs;
+  if (tid < G) cv[tid] = 0;
+  __syncthreads();
+  int c = 0, d = 0, slot = -1;
+  if (tid < E) {
     int run = 0;
     for (int b = 0; b < nb; ++b) {
-      int32_t* p = block_base + static_cast<long long>(b) * E + e;
+      int32_t* p = block_base + static_cast<long long>(b) * E + tid;
       const int v = *p;
       *p = run;
       run += v;
     }
     c = run;
+    if (divert != nullptr && slot_of != nullptr) {
+      slot = slot_of[tid];
+      // a duplicate must sit in a slot position of some shard
+      if (slot < 0 || slot >= G || slot % Gs < Es) slot = -1;
+      d = slot >= 0 ? min(max(divert[tid], 0), c) : 0;
+      if (d == 0) slot = -1;
+    }
+    cv[(tid / Es) * Gs + tid % Es] = c - d;
+    if (slot >= 0) cv[slot] = d;
   }
-  const int ex = block_exclusive_scan_1024(c, warp_tot, &total);
-  if (e < E) scan[e] = ex;
-  if (e == 0) scan[E] = total;
   __syncthreads();
-  int kept = c;
-  if (e < E && cap >= 0) {
-    const int Es = E / S;
-    const int local = ex - scan[(e / Es) * Es];  // rows of the shard before e
-    kept = min(max(cap - local, 0), c);
+  const int cg = tid < G ? cv[tid] : 0;
+  const int ex = block_exclusive_scan_1024(cg, warp_tot, &total);
+  if (tid < G) scan[tid] = ex;
+  if (tid == 0) scan[G] = total;
+  __syncthreads();
+  int kept = cg;
+  if (tid < G && cap >= 0) {
+    const int local = ex - scan[(tid / Gs) * Gs];  // rows of the shard before g
+    kept = min(max(cap - local, 0), cg);
   }
-  const int kex = block_exclusive_scan_1024(e < E ? kept : 0, warp_tot,
+  const int kex = block_exclusive_scan_1024(tid < G ? kept : 0, warp_tot,
                                             &ktotal);
-  if (e < E) {
-    kept_out[e] = kept;
-    goff_out[e] = kex;
-    group_offsets[e] = kex;
+  if (tid < G) {
+    keptv[tid] = kept;
+    goffv[tid] = kex;
+    group_offsets[tid] = kex;
   }
-  if (e == 0) {
-    group_offsets[E] = ktotal;
+  if (tid == 0) {
+    group_offsets[G] = ktotal;
     *n_dropped = total - ktotal;
+  }
+  __syncthreads();
+  if (tid < E) {
+    const int home = (tid / Es) * Gs + tid % Es;
+    etab[0 * E + tid] = keptv[home];
+    etab[1 * E + tid] = goffv[home];
+    etab[2 * E + tid] = c - d;
+    etab[3 * E + tid] = slot >= 0 ? keptv[slot] : 0;
+    etab[4 * E + tid] = slot >= 0 ? goffv[slot] : 0;
+    etab[5 * E + tid] = slot >= 0 ? slot / Gs : tid / Es;
   }
 }
 
 __global__ void __launch_bounds__(TB) assign_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k, int S,
-    const int32_t* __restrict__ block_base, const int32_t* __restrict__ kept_g,
-    const int32_t* __restrict__ goff_g, int32_t* __restrict__ row_of,
-    int32_t* __restrict__ sorted_token, int32_t* __restrict__ block_ucnt,
-    int32_t* __restrict__ urank) {
+    const int32_t* __restrict__ block_base, const int32_t* __restrict__ etab_g,
+    int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token,
+    int32_t* __restrict__ block_ucnt, int32_t* __restrict__ urank) {
   extern __shared__ int sm[];
   uint32_t* mask = reinterpret_cast<uint32_t*>(sm);  // [kWarps][E]
   int* wpre = sm + kWarps * E;                       // [kWarps][E]
   int* base = wpre + kWarps * E;                     // [E]
-  int* kept = base + E;                              // [E]
-  int* goff = kept + E;                              // [E]
-  uint32_t* ballot = reinterpret_cast<uint32_t*>(goff + E);  // [kWarps][S]
-  int* upre = reinterpret_cast<int*>(ballot + kWarps * S);   // [kWarps][S]
+  int* etab = base + E;                              // [6][E]
+  uint32_t* ballot = reinterpret_cast<uint32_t*>(etab + 6 * E);  // [kWarps][S]
+  int* upre = reinterpret_cast<int*>(ballot + kWarps * S);       // [kWarps][S]
 
   const int b = blockIdx.x, tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const uint32_t lt = (1u << lane) - 1u;
   for (int e = tid; e < E; e += TB) {
     base[e] = block_base[static_cast<long long>(b) * E + e];
-    kept[e] = kept_g[e];
-    goff[e] = goff_g[e];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) etab[q * E + e] = etab_g[q * E + e];
 #pragma unroll
     for (int q = 0; q < kWarps; ++q) mask[q * E + e] = 0u;
   }
@@ -182,11 +215,17 @@ __global__ void __launch_bounds__(TB) assign_kernel(
       if (e >= 0 && e < E) {
         const int rank =
             base[e] + wpre[w * E + e] + __popc(mask[w * E + e] & lt);
-        if (rank < kept[e]) {
-          row = goff[e] + rank;
-          sorted_token[row] = t;
-          smask |= 1ull << (e / Es);
+        const int own = etab[2 * E + e];
+        if (rank < own) {            // the expert's own group
+          if (rank < etab[0 * E + e]) {
+            row = etab[1 * E + e] + rank;
+            smask |= 1ull << (e / Es);
+          }
+        } else if (rank - own < etab[3 * E + e]) {  // its duplicate slot
+          row = etab[4 * E + e] + (rank - own);
+          smask |= 1ull << etab[5 * E + e];
         }
+        if (row >= 0) sorted_token[row] = t;
       }
       row_of[tk + j] = row;
     }
@@ -210,8 +249,11 @@ __global__ void __launch_bounds__(TB) assign_kernel(
     for (int j = 0; j < k; ++j) {
       int ur = -1;
       if (row_of[tk + j] >= 0) {
-        const int s = __ldg(idx + tk + j) / Es;
-        ur = upre[w * S + s] + __popc(ballot[w * S + s] & lt);
+        const int e = __ldg(idx + tk + j);
+        const int rank =
+            base[e] + wpre[w * E + e] + __popc(mask[w * E + e] & lt);
+        const int s = rank < etab[2 * E + e] ? e / Es : etab[5 * E + e];
+        ur = ((upre[w * S + s] + __popc(ballot[w * S + s] & lt)) << 6) | s;
       }
       urank[tk + j] = ur;
     }
@@ -262,16 +304,15 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     const int row = row_of[tk + tid];
     rows[tid] = row;
     if (row >= 0) {
-      const int Es = E / S;
-      const int s = __ldg(idx + tk + tid) / Es;
+      const int code = urank[tk + tid];
+      const int s = code & 63;
       const int upos = uniq_offsets[s] +
                        block_ucnt[static_cast<long long>(t / TB) * S + s] +
-                       urank[tk + tid];
+                       (code >> 6);
       expand_idx[row] = upos;
       bool first = true;
       for (int q = 0; q < tid; ++q)
-        if (row_of[tk + q] >= 0 && __ldg(idx + tk + q) / Es == s)
-          first = false;
+        if (row_of[tk + q] >= 0 && (urank[tk + q] & 63) == s) first = false;
       if (first) uniq_tokens[upos] = t;
     }
   }
@@ -298,7 +339,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 }
 
 size_t assign_smem_bytes(int E, int S) {
-  return sizeof(int) * (2 * kWarps * E + 3 * E + 2 * kWarps * S);
+  return sizeof(int) * (2 * kWarps * E + 7 * E + 2 * kWarps * S);
 }
 
 }  // namespace
@@ -313,8 +354,7 @@ PermuteScratch carve_permute_scratch(Carve& c, int T, int E, int k, int S) {
   const size_t nb = static_cast<size_t>((T + TB - 1) / TB);
   PermuteScratch p;
   p.block_base = c.take<int32_t>(nb * E);
-  p.kept = c.take<int32_t>(E);
-  p.goff = c.take<int32_t>(E);
+  p.etab = c.take<int32_t>(6 * static_cast<size_t>(E));
   p.block_ucnt = c.take<int32_t>(nb * S);
   p.urank = c.take<int32_t>(static_cast<size_t>(T) * k);
   p.scal = c.take<int32_t>(4);
@@ -328,28 +368,26 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
                            int32_t* uniq_offsets, int32_t* uniq_tokens,
                            int32_t* expand_idx, int32_t* n_dropped,
                            const PermuteScratch& ws, int32_t* status,
-                           cudaStream_t s) {
+                           cudaStream_t s, const PermutePlan& plan) {
   const int nb = (c.T + TB - 1) / TB;
   if (nb > 0) {
     block_count_kernel<<<nb, TB, c.E * sizeof(int), s>>>(
         topk_idx, c.T, c.E, c.k, ws.block_base, status);
   }
-  scan_experts_kernel<<<1, 1024, 0, s>>>(ws.block_base, nb, c.E, c.S,
-                                         static_cast<int>(cap), ws.kept,
-                                         ws.goff, group_offsets, n_dropped);
+  scan_experts_kernel<<<1, 1024, 0, s>>>(
+      ws.block_base, nb, c.E, c.S, plan.B, static_cast<int>(cap),
+      plan.divert, plan.slot_of, ws.etab, group_offsets, n_dropped);
   if (nb > 0) {
     const size_t smem = assign_smem_bytes(c.E, c.S);
-    static bool attr_set = false;
-    if (smem > 48 * 1024 && !attr_set) {
-      cudaFuncSetAttribute(assign_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-      attr_set = true;
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
     }
     assign_kernel<<<nb, TB, smem, s>>>(topk_idx, c.T, c.E, c.k, c.S,
-                                       ws.block_base, ws.kept, ws.goff,
-                                       row_of, sorted_token, ws.block_ucnt,
-                                       ws.urank);
+                                       ws.block_base, ws.etab, row_of,
+                                       sorted_token, ws.block_ucnt, ws.urank);
   }
   scan_uniq_kernel<<<1, 64, 0, s>>>(ws.block_ucnt, nb, c.S, uniq_offsets);
   if (c.T > 0) {

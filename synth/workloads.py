@@ -51,6 +51,7 @@ class Workload:
     seed: int = 0
     x_scale: float = 1.0  # std of x
     w_std: float = 0.02   # std of the expert weights
+    redundant_slots: int = 0  # duplicate-expert slots per shard (0: off)
 
     @property
     def torch_dtype(self):

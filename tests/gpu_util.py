@@ -18,11 +18,11 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 def cfg_from(wl, **over):
     kw = dict(T=wl.T, H=wl.H, E=wl.E, k=wl.k, F=wl.F, S=wl.S,
               factor=wl.factor, n_chunks=wl.n_chunks, dtype=wl.dtype,
-              renorm=wl.renorm)
+              renorm=wl.renorm, redundant_slots=wl.redundant_slots)
     kw.update(over)
     return moe.make_config(kw["T"], kw["H"], kw["E"], kw["k"], kw["F"],
                            kw["S"], kw["factor"], kw["n_chunks"], kw["dtype"],
-                           kw["renorm"])
+                           kw["renorm"], kw["redundant_slots"])
 
 
 def np_(t):
