@@ -254,68 +254,109 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------ tiles ------
-// mt_prefix[e] = number of 128-row tiles of experts < e.  Tile index order
-// is (expert, n-tile, m-tile), m fastest.
-__device__ __forceinline__ void decode_tile(int tile, const int* mt_prefix,
-                                            int E, int n_tiles, int& e,
-                                            int& m, int& n) {
-  const int q = tile / n_tiles;
-  int lo = 0, hi = E - 1;  // largest e with mt_prefix[e] <= q
+// A tile is (group g, n-tile, m-tile of 128 rows).  Groups with at least two
+// m-tiles ("heavy": their weight tile feeds several m-tiles, so they lean on
+// the tensor cores) and groups with one ("light": pure weight streaming)
+// form two streams, each in (group, n-tile, m-tile) order with m fastest so
+// the m-tiles of a weight tile run together and share it through L2.  The
+// two streams are interleaved evenly (position i of the launch is heavy iff
+// floor((i+1)*Nh/N) > floor(i*Nh/N)), so every wave of CTAs mixes
+// compute-bound and HBM-bound tiles instead of running the hot experts
+// first and the cold ones last.
+struct TileTable {
+  const int* goff;   // [G+1] row offsets of the groups
+  const int* hpre;   // [G+1] m-tiles of heavy groups before g
+  const int* lpre;   // [G+1] m-tiles of light groups before g
+  int G, n_tiles;
+  long long heavy, total;  // tiles
+};
+
+// Largest g with pre[g] <= q (the group holding stream m-tile q).
+__device__ __forceinline__ int group_of(const int* pre, int G, int q) {
+  int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (mt_prefix[mid] <= q)
+    if (pre[mid] <= q)
       lo = mid;
     else
       hi = mid - 1;
   }
-  e = lo;
-  const int mt = mt_prefix[e + 1] - mt_prefix[e];
-  const int local = tile - mt_prefix[e] * n_tiles;
+  return lo;
+}
+
+__device__ __forceinline__ void decode_tile(const TileTable& tt, int tile,
+                                            int& e, int& m, int& n) {
+  const long long i = tile;
+  const long long hb = i * tt.heavy / tt.total;           // heavy before i
+  const bool heavy = (i + 1) * tt.heavy / tt.total > hb;
+  const int* pre = heavy ? tt.hpre : tt.lpre;
+  const int q = static_cast<int>(heavy ? hb : i - hb);     // rank in stream
+  e = group_of(pre, tt.G, q / tt.n_tiles);
+  const int mt = pre[e + 1] - pre[e];
+  const int local = q - pre[e] * tt.n_tiles;
   n = local / mt;
   m = local - n * mt;
 }
 
-// All threads: goff[0..E] <- group offsets, mt_prefix[0..E] <- exclusive
-// scan of each expert's 128-row tile count.
-__device__ void build_tile_table(const int32_t* __restrict__ off, int E,
-                                 int* goff, int* mt_prefix, int* wsum) {
+// All threads: goff[0..G], hpre[0..G], lpre[0..G] for tiles of
+// rows_per_tile rows.
+__device__ void build_tile_table(const int32_t* __restrict__ off, int G,
+                                 int* goff, int* hpre, int* lpre, int* wsum,
+                                 int rows_per_tile) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (E + kThreads - 1) / kThreads;
-  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int local = 0;
-  for (int e = e0; e < e1; ++e) {
-    const int a = __ldg(off + e), b = __ldg(off + e + 1);
-    const int mt = b > a ? (b - a + BM - 1) / BM : 0;
-    goff[e] = a;
-    mt_prefix[e] = mt;
-    local += mt;
+  const int per = (G + kThreads - 1) / kThreads;
+  const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+  int lh = 0, ll = 0;
+  for (int g = g0; g < g1; ++g) {
+    const int a = __ldg(off + g), b = __ldg(off + g + 1);
+    const int mt = b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
+    goff[g] = a;
+    hpre[g] = mt >= 2 ? mt : 0;
+    lpre[g] = mt == 1 ? 1 : 0;
+    lh += hpre[g];
+    ll += lpre[g];
   }
-  if (tid == 0) goff[E] = __ldg(off + E);
-  int inc = local;
+  if (tid == 0) goff[G] = __ldg(off + G);
+  int ih = lh, il = ll;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
+    const int nh = __shfl_up_sync(0xffffffffu, ih, o);
+    const int nl = __shfl_up_sync(0xffffffffu, il, o);
+    if (lane >= o) {
+      ih += nh;
+      il += nl;
+    }
   }
-  if (lane == 31) wsum[w] = inc;
+  if (lane == 31) {
+    wsum[w] = ih;
+    wsum[8 + w] = il;
+  }
   __syncthreads();
   if (tid == 0) {
-    int run = 0;
+    int rh = 0, rl = 0;
     for (int i = 0; i < kThreads / 32; ++i) {
-      const int v = wsum[i];
-      wsum[i] = run;
-      run += v;
+      const int vh = wsum[i], vl = wsum[8 + i];
+      wsum[i] = rh;
+      wsum[8 + i] = rl;
+      rh += vh;
+      rl += vl;
     }
-    wsum[kThreads / 32] = run;
+    wsum[kThreads / 32] = rh;
+    wsum[8 + kThreads / 32] = rl;
   }
   __syncthreads();
-  int run = wsum[w] + inc - local;
-  for (int e = e0; e < e1; ++e) {
-    const int v = mt_prefix[e];
-    mt_prefix[e] = run;
-    run += v;
+  int rh = wsum[w] + ih - lh, rl = wsum[8 + w] + il - ll;
+  for (int g = g0; g < g1; ++g) {
+    const int vh = hpre[g], vl = lpre[g];
+    hpre[g] = rh;
+    lpre[g] = rl;
+    rh += vh;
+    rl += vl;
   }
-  if (tid == 0) mt_prefix[E] = wsum[kThreads / 32];
+  if (tid == 0) {
+    hpre[G] = wsum[kThreads / 32];
+    lpre[G] = wsum[8 + kThreads / 32];
+  }
   __syncthreads();
 }
 
@@ -340,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [8]
-  int* goff = wsum + 8;                                // [E+1]
-  int* mt_prefix = goff + (p.E + 1);                   // [E+1]
+  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
+  int* goff = wsum + 16;                               // [E+1]
+  int* hpre = goff + (p.E + 1);                        // [E+1]
+  int* lpre = hpre + (p.E + 1);                        // [E+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -370,12 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  build_tile_table(p.group_offsets, p.E, goff, mt_prefix, wsum);
+  build_tile_table(p.group_offsets, p.E, goff, hpre, lpre, wsum, BM);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = mt_prefix[p.E] * p.n_tiles;
+  TileTable tt;
+  tt.goff = goff;
+  tt.hpre = hpre;
+  tt.lpre = lpre;
+  tt.G = p.E;
+  tt.n_tiles = p.n_tiles;
+  tt.heavy = static_cast<long long>(hpre[p.E]) * p.n_tiles;
+  tt.total = tt.heavy + static_cast<long long>(lpre[p.E]) * p.n_tiles;
+  const int total_tiles = static_cast<int>(tt.total);
   const int kblocks = p.K / BK;
 
   if (warp == 0) {
@@ -388,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < total_tiles;
            tile += gridDim.x) {
         int e, m, n;
-        decode_tile(tile, mt_prefix, p.E, p.n_tiles, e, m, n);
+        decode_tile(tt, tile, e, m, n);
         const int a_row = goff[e] + m * BM;
         const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
         const int b_row = we * p.K;
@@ -480,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, m, n;
-      decode_tile(tile, mt_prefix, p.E, p.n_tiles, e, m, n);
+      decode_tile(tt, tile, e, m, n);
       bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
                           p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -589,7 +639,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 template <int BN>
 size_t smem_bytes(int E) {
   return 1024 + STAGES * Tile<BN>::kStage + 8 * (2 * STAGES + 5) + 16 +
-         4 * (8 + 2 * (E + 1)) + 64;
+         4 * (16 + 3 * (E + 1)) + 64;
 }
 
 template <int MODE, int BN>
