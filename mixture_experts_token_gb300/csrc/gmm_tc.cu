@@ -32,6 +32,15 @@
 //   GEMM1 issues one N=256 MMA whose columns 0-127 are the gate projection
 //     and 128-255 the up projection of the same 128 output columns.
 //
+// Two-SM form (gmm_tc2_kernel, used when the output tile is 256 wide): a
+// cluster of two CTAs on one TPC shares each M=256 x N=256 tile through
+// tcgen05.mma.cta_group::2.  Each CTA stages its own 128 rows of A and half
+// of B (for GEMM1: the leader the gate columns, the peer the up columns) in
+// 6 stages of 32 KB, so a stage of compute needs a third less shared memory
+// and more loads are in flight.  The leader issues the MMAs and multicasts
+// its commits to both CTAs; the peer's TMA loads complete on the leader's
+// barrier; both CTAs run an epilogue on their own 128 rows of TMEM.
+//
 // Every wait is bounded (2 s of %globaltimer); on expiry the kernel raises
 // MOE_DEV_TIMEOUT in the status word, tells the other roles to stop, drains
 // its own TMA loads and MMAs, frees its tensor memory and returns.
@@ -225,6 +234,102 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       "tcgen05.wait::ld.sync.aligned;\n"
       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
       : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// ------------------------------------------------------- CTA pair ------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// TMA load into this CTA's shared memory, completing on an mbarrier that
+// may sit in either CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
+                                                 const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile(
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+          bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
+                                                uint32_t cols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(cols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr,
+                                                  uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(cols)
+               : "memory");
+}
+
+// D (both CTAs' TMEM, 128 rows each) (+)= A (both CTAs' smem, 128 rows
+// each) * B (both CTAs' smem, N/2 columns each); one thread of the leader.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc,
+                                               uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at this shared-memory offset in both CTAs once the
+// leader's tcgen05 ops are complete.
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
       : "memory");
 }
 
@@ -598,6 +703,249 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------ pair kernel ------
+constexpr int STAGES2 = 6;
+constexpr int BMP = 2 * BM;                     // rows of a pair tile
+constexpr int kA2Bytes = BM * BK * 2;           // this CTA's 128 rows
+constexpr int kB2Bytes = BK * 128 * 2;          // this CTA's half of N=256
+constexpr int kStage2 = kA2Bytes + kB2Bytes;    // 32 KB
+constexpr uint32_t kTxPair = 2 * kStage2;       // bytes per stage, both CTAs
+constexpr int kPairArrivals = 2 * kEpilogueThreads;
+
+// MODE 0: h = silu(A Wg) * (A Wu): the leader stages the gate columns, the
+// peer the up columns of the same 128 outputs; TMEM columns 0-127 of either
+// CTA hold gate, 128-255 up, for its own 128 rows.
+// MODE 1: y_sorted = A Wd, 256 output columns: the leader stages the first
+// 128, the peer the last 128.
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gmm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * kStage2);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES2;
+  uint64_t* tfull = bars + 2 * STAGES2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
+  int* goff = wsum + 16;                               // [E+1]
+  int* hpre = goff + (p.E + 1);                        // [E+1]
+  int* lpre = hpre + (p.E + 1);                        // [E+1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: leader, 1: peer
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      mbar_init(smem_u32(tempty + a), kPairArrivals);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    if (MODE == 0) prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  build_tile_table(p.group_offsets, p.E, goff, hpre, lpre, wsum, BMP);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  TileTable tt;
+  tt.goff = goff;
+  tt.hpre = hpre;
+  tt.lpre = lpre;
+  tt.G = p.E;
+  tt.n_tiles = p.n_tiles;
+  tt.heavy = static_cast<long long>(hpre[p.E]) * p.n_tiles;
+  tt.total = tt.heavy + static_cast<long long>(lpre[p.E]) * p.n_tiles;
+  const int total_tiles = static_cast<int>(tt.total);
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ---------------------------------------- TMA producer (both CTAs) ---
+    if (lane == 0) {
+      const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        int e, m, n;
+        decode_tile(tt, tile, e, m, n);
+        const int a_row = goff[e] + m * BMP + static_cast<int>(rank) * BM;
+        const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
+        const int b_row = we * p.K;
+        const int b_col = MODE == 0 ? n * 128 : n * 256 + rank * 128;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = map_to_rank(smem_u32(full + stage), 0);
+          if (rank == 0) mbar_expect_tx(smem_u32(full + stage), kTxPair);
+          const uint32_t sa = smem_base + stage * kStage2;
+          const uint32_t sb = sa + kA2Bytes;
+          tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+          tma_load_2d_pair(sb, mb, fb, b_col, b_row + kb * BK);
+          tma_load_2d_pair(sb + 8192, mb, fb, b_col + 64, b_row + kb * BK);
+          ++fills;
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: the leader's full barriers count both CTAs' bytes.
+      if (rank == 0) {
+        const long long first = fills > STAGES2 ? fills - STAGES2 : 0;
+        for (long long f = first; f < fills; ++f)
+          mbar_wait(smem_u32(full + (f % STAGES2)),
+                    static_cast<uint32_t>((f / STAGES2) & 1), abort_flag,
+                    p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------- MMA issuer (leader) ------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc(BMP, 256);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag,
+                       p.status))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag,
+                         p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * kStage2;
+          const uint32_t sb = sa + kA2Bytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
+            umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_mc(smem_u32(empty + stage));
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(smem_u32(tfull + acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit_pair(smem_u32(done));
+      mbar_wait(smem_u32(done), 0, abort_flag, p.status);
+    }
+  } else {
+    // ---------------------------------------- epilogue (both CTAs) -----
+    const int q = warp & 3;
+    const int row = static_cast<int>(rank) * BM + q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < total_tiles; tile += npairs) {
+      int e, m, n;
+      decode_tile(tt, tile, e, m, n);
+      bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
+                          p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int grow = goff[e] + m * BMP + row;
+      const bool valid = grow < goff[e + 1];
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      if (MODE == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<long long>(grow) * p.out_ld + n * 128);
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32x2(taddr + c, taddr + 128 + c, g, u);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]);
+            const float g1 = __uint_as_float(g[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) *
+                             __uint_as_float(u[2 * i]);
+            const float h1 = g1 / (1.0f + __expf(-g1)) *
+                             __uint_as_float(u[2 * i + 1]);
+            pk[i] = pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
+                                          pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<long long>(grow) * p.out_ld + n * 256);
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
+                                __uint_as_float(r[2 * i + 1]));
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
+                                          pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(map_to_rank(smem_u32(tempty + acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still use it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------- host ------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                  void*, const cuuint64_t*, const cuuint64_t*,
@@ -642,6 +990,41 @@ size_t smem_bytes(int E) {
          4 * (16 + 3 * (E + 1)) + 64;
 }
 
+// The pair form pays off only when groups are large: a pair tile covers 256
+// rows, and for smaller groups the peer SM stages rows it then masks (more
+// L2 traffic and tensor work per weight tile, measured 15-25% slower on
+// weight-streaming layers).  With >= 1024 routed rows per group on average
+// it was measured 2% (GEMM1) and 9% (GEMM2) faster.
+constexpr long long kPairMinRowsPerGroup = 1024;
+
+bool use_pair(const moe_config_t& c, const Groups& g) {
+  return static_cast<long long>(c.T) * c.k >= kPairMinRowsPerGroup * g.n;
+}
+
+size_t smem_bytes_pair(int E) {
+  return 1024 + STAGES2 * kStage2 + 8 * (2 * STAGES2 + 5) + 16 +
+         4 * (16 + 3 * (E + 1)) + 64;
+}
+
+template <int MODE>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const Params& p,
+                        cudaStream_t s) {
+  const size_t smem = smem_bytes_pair(p.E);
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(gmm_tc2_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int grid = sms & ~1;  // whole CTA pairs
+  gmm_tc2_kernel<MODE><<<grid, kThreads, smem, s>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
 template <int MODE, int BN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
                        const CUtensorMap& b1, const Params& p,
@@ -682,6 +1065,7 @@ cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
     return cudaErrorInvalidValue;
   tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
+  if (tc::use_pair(c, g)) return tc::launch_pair<0>(a1, bg, bu, p1, s);
   return tc::launch_one<0, 256>(a1, bg, bu, p1, s);
 }
 
@@ -699,6 +1083,7 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
   if (c.H % 256 == 0) {
     tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
+    if (tc::use_pair(c, g)) return tc::launch_pair<1>(a2, bd, bd, p2, s);
     return tc::launch_one<1, 256>(a2, bd, bd, p2, s);
   }
   tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 128,

@@ -57,6 +57,9 @@ GMM_CASES = [
     ([128] * 4, 128, 128),
     ([1000], 512, 384),
     ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512),
+    # >= 1024 rows per group on average: the two-SM (CTA pair) kernel
+    ([2100, 900, 1300, 4, 1], 512, 256),
+    ([4096, 3000], 256, 384),
 ]
 
 
@@ -91,6 +94,53 @@ def test_gmm_small_layer_shape():
                                                        f64(wd)))
     assert ref.normwise_error(f64(h[:R]), want_h) <= 2e-2
     assert ref.normwise_error(f64(ys[:R]), want_y) <= 2e-2
+
+
+def test_gmm_pair_kernel_row_independence():
+    """Large groups take the CTA-pair kernel (256-row tiles): a row computed
+    at another offset inside its pair tile gives the same bits, and the
+    same bits as the one-CTA kernel computes for it in a small-group
+    launch."""
+    H, F = 256, 256
+    sizes = [1500, 700]                      # 1100 rows per group: pair
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=7)
+    # the same rows split into many small groups of the same experts would
+    # change the weights; instead shift every row by 77 positions
+    shift = 77
+    xs2 = torch.cat([torch.randn(shift, H, device="cuda").to(xs.dtype),
+                     xs[:R]])
+    off2 = torch.tensor([0, sizes[0] + shift, R + shift], dtype=torch.int32,
+                        device="cuda")
+    cfg = moe.make_config(R + shift, H, 2, 1, F, 1, 2.0, 0, "bf16")
+    h2 = torch.empty((R + shift, F), dtype=xs.dtype, device="cuda")
+    ys2 = torch.empty((R + shift, H), dtype=xs.dtype, device="cuda")
+    moe.moe_gmm_swiglu(cfg, xs2, off2, wg, wu, wd, h2, ys2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2[shift:], h[:R])
+    assert torch.equal(ys2[shift:], ys[:R])
+
+
+def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
+    """The same rows and weights through the CTA-pair kernel (2 groups of
+    ~1100 rows) and the one-CTA kernel (the same groups padded with empty
+    ones, so fewer rows per group): identical bits.  This keeps chunked and
+    dropless passes bit-identical when they pick different kernels."""
+    H, F = 512, 256
+    sizes = [1500, 700]
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=9)
+    n_groups = 8                                  # 275 rows per group
+    gexp = torch.tensor([0, 1] + [0] * (n_groups - 2), dtype=torch.int32,
+                        device="cuda")
+    off8 = torch.tensor([0, 1500] + [R] * (n_groups - 1), dtype=torch.int32,
+                        device="cuda")
+    cfg = moe.make_config(R, H, 2, 1, F, 1, 2.0, 0, "bf16")
+    h2 = torch.empty_like(h)
+    ys2 = torch.empty_like(ys)
+    moe.moe_gmm_swiglu_mapped(cfg, n_groups, gexp, xs, off8, wg, wu, wd, h2,
+                              ys2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2[:R], h[:R])
+    assert torch.equal(ys2[:R], ys[:R])
 
 
 def test_gmm_row_result_independent_of_tile_position():
