@@ -416,6 +416,14 @@ int32_t moe_num_chunks(const moe_config_t *cfg);
 /* Static text for a status code. */
 const char *moe_status_string(moe_status_t status);
 
+/* For tests of failure detection only: with fills >= 0 the bf16 GEMM's TMA
+ * producer stops after that many pipeline-stage fills, so the MMA warp's
+ * bounded wait runs out (about 2 s): the kernel then sets MOE_DEV_TIMEOUT in
+ * the status word, stops its other roles, drains its copies and MMAs, frees
+ * its tensor memory and returns, and the CUDA context stays usable.  -1
+ * restores normal operation.  Process-wide; not for production use. */
+void moe_test_stall_gemm_producer(int64_t fills);
+
 #ifdef __cplusplus
 }
 #endif

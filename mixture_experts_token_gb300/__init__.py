@@ -123,6 +123,8 @@ def _declare(h):
     h.moe_chunk_tokens.restype = c_int32
     h.moe_num_chunks.argtypes = [cfg]
     h.moe_num_chunks.restype = c_int32
+    h.moe_test_stall_gemm_producer.argtypes = [c_int64]
+    h.moe_test_stall_gemm_producer.restype = None
     h.moe_status_string.argtypes = [c_int]
     h.moe_status_string.restype = ctypes.c_char_p
 
@@ -184,6 +186,11 @@ def moe_chunk_tokens(cfg) -> int:
 
 def moe_num_chunks(cfg) -> int:
     return lib().moe_num_chunks(ctypes.byref(cfg))
+
+
+def moe_test_stall_gemm_producer(fills: int):
+    """Tests of failure detection only (see include/moe.h)."""
+    lib().moe_test_stall_gemm_producer(fills)
 
 
 def moe_workspace_bytes(cfg, which) -> int:

@@ -271,6 +271,10 @@ size_t moe_workspace_bytes(const moe_config_t* cfg, moe_ws_kind_t which) {
   return 0;
 }
 
+void moe_test_stall_gemm_producer(int64_t fills) {
+  set_gemm_stall_for_tests(fills);
+}
+
 const char* moe_status_string(moe_status_t st) {
   switch (st) {
     case MOE_OK:

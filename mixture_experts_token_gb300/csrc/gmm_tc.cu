@@ -47,6 +47,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -80,7 +81,12 @@ struct Params {
   __nv_bfloat16* out;
   int out_ld;   // F (GEMM1) or H (GEMM2)
   int32_t* status;
+  // Tests of the timeout path only: the producer stops after this many
+  // stage fills (-1: never), so the MMA warp's next wait runs out.
+  long long stall_after_fills = -1;
 };
+
+std::atomic<long long> g_stall_after_fills{-1};
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -124,6 +130,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait; false when it gave up (or another role already did).
+// A drain passes abort_flag = nullptr: it waits for its own copies or MMAs
+// even after another role gave up, bounded by the time limit alone.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                        volatile int* abort_flag,
                                        int32_t* status) {
@@ -133,9 +141,9 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0) {
-      if (*abort_flag) return false;
+      if (abort_flag && *abort_flag) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
+        if (abort_flag) *abort_flag = 1;
         if (status) atomicOr(status, MOE_DEV_TIMEOUT);
         return false;
       }
@@ -548,6 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
         const int b_row = we * p.K;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (p.stall_after_fills >= 0 && fills >= p.stall_after_fills) {
+            ok = false;  // test hook: leave the MMA warp waiting
+            break;
+          }
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
                          p.status)) {
             ok = false;
@@ -580,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long first = fills > STAGES ? fills - STAGES : 0;
       for (long long f = first; f < fills; ++f)
         mbar_wait(smem_u32(full + (f % STAGES)),
-                  static_cast<uint32_t>((f / STAGES) & 1), abort_flag,
+                  static_cast<uint32_t>((f / STAGES) & 1), nullptr,
                   p.status);
     }
   } else if (warp == 1) {
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Drain: all MMAs issued by this thread are complete.
       umma_commit(smem_u32(done));
-      mbar_wait(smem_u32(done), 0, abort_flag, p.status);
+      mbar_wait(smem_u32(done), 0, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------ epilogue ---------
@@ -823,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const long long first = fills > STAGES2 ? fills - STAGES2 : 0;
         for (long long f = first; f < fills; ++f)
           mbar_wait(smem_u32(full + (f % STAGES2)),
-                    static_cast<uint32_t>((f / STAGES2) & 1), abort_flag,
+                    static_cast<uint32_t>((f / STAGES2) & 1), nullptr,
                     p.status);
       }
     }
@@ -867,7 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       umma_commit_pair(smem_u32(done));
-      mbar_wait(smem_u32(done), 0, abort_flag, p.status);
+      mbar_wait(smem_u32(done), 0, nullptr, p.status);
     }
   } else {
     // ---------------------------------------- epilogue (both CTAs) -----
@@ -998,7 +1010,8 @@ size_t smem_bytes(int E) {
 constexpr long long kPairMinRowsPerGroup = 1024;
 
 bool use_pair(const moe_config_t& c, const Groups& g) {
-  return static_cast<long long>(c.T) * c.k >= kPairMinRowsPerGroup * g.n;
+  return g_stall_after_fills.load() < 0 &&
+         static_cast<long long>(c.T) * c.k >= kPairMinRowsPerGroup * g.n;
 }
 
 size_t smem_bytes_pair(int E) {
@@ -1027,8 +1040,8 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0,
 
 template <int MODE, int BN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
-                       const CUtensorMap& b1, const Params& p,
-                       cudaStream_t s) {
+                       const CUtensorMap& b1, Params p, cudaStream_t s) {
+  p.stall_after_fills = g_stall_after_fills.load();
   const size_t smem = smem_bytes<BN>(p.E);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -1044,6 +1057,10 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
 }
 
 }  // namespace tc
+
+void set_gemm_stall_for_tests(long long fills) {
+  tc::g_stall_after_fills.store(fills);
+}
 
 bool gmm_tc_supported(const moe_config_t& c) {
   return c.dtype == MOE_BF16 && c.H % 128 == 0 && c.F % 128 == 0 &&

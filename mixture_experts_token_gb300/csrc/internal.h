@@ -141,6 +141,10 @@ bool ok_ptr(const void* p, bool need16);
 bool gmm_shape_ok(const moe_config_t& c);
 bool weights_ok(const void* wg, const void* wu, const void* wd);
 
+// Tests of the GEMM's bounded waits: stop the TMA producer after `fills`
+// stage fills (-1: normal operation).
+void set_gemm_stall_for_tests(long long fills);
+
 // Shape support of the bf16 tensor-core GEMM.
 bool gmm_tc_supported(const moe_config_t& c);
 

@@ -1,0 +1,64 @@
+"""Failure detection on the GPU without a fault: the GEMM's bounded waits.
+
+A test hook stops the GEMM's TMA producer after a few stage fills, so the
+MMA warp waits on a barrier nothing will complete.  The wait gives up after
+its limit (about 2 s); the kernel must report MOE_DEV_TIMEOUT in the status
+word, return on its own (no trap, no hang), and leave the CUDA context
+usable: the next, normal launch gives correct results.  Nothing here faults
+or hangs the GPU.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_token_gb300 as moe
+from oracle import moe_ref as ref
+from tests.gpu_util import f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _case():
+    E, H, F = 3, 256, 256
+    sizes = [300, 0, 200]
+    R = sum(sizes)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    xs = torch.randn(R, H, generator=g, device="cuda").to(torch.bfloat16)
+    W = [(torch.randn(E, *shp, generator=g, device="cuda") * 0.05)
+         .to(torch.bfloat16) for shp in ((H, F), (H, F), (F, H))]
+    off = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]),
+                       dtype=torch.int32, device="cuda")
+    cfg = moe.make_config(R, H, E, 1, F, 1, 2.0, 0, "bf16")
+    return cfg, xs, off, W, R
+
+
+def _run(cfg, xs, off, W, R, status):
+    h = torch.zeros(R, cfg.F, dtype=torch.bfloat16, device="cuda")
+    ys = torch.zeros(R, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_gmm_swiglu(cfg, xs, off, *W, h, ys, status)
+    torch.cuda.synchronize()
+    return h, ys
+
+
+def test_gemm_wait_times_out_and_context_survives():
+    cfg, xs, off, W, R = _case()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        moe.moe_test_stall_gemm_producer(3)
+        t0 = time.time()
+        _run(cfg, xs, off, W, R, status)
+        took = time.time() - t0
+    finally:
+        moe.moe_test_stall_gemm_producer(-1)
+    assert int(status.item()) & moe.MOE_DEV_TIMEOUT
+    assert took < 30.0
+    # the context is intact: a normal launch is correct
+    status.zero_()
+    h, ys = _run(cfg, xs, off, W, R, status)
+    assert int(status.item()) == 0
+    want_h, want_y = ref.grouped_ffn(
+        f64(xs), off.cpu().numpy(),
+        ref.dense_weights(*(f64(w) for w in W)))
+    assert ref.normwise_error(f64(ys), want_y) <= 2e-2
