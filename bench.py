@@ -567,7 +567,12 @@ def main():
     graph = None if layer.dispatch_only else graph_run(layer, args, device)
     e2e = None
     if not args.no_e2e and not layer.dispatch_only:
-        e2e = e2e_run(layer, args, world, device, graph)
+        if graph is not None:
+            graph["graph"].close()
+            e2e = e2e_pipelined(layer, args, world, device)
+            e2e["serial"] = e2e_run(layer, args, world, device, None)
+        else:
+            e2e = e2e_run(layer, args, world, device, None)
 
     out = {
         "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world,
@@ -655,6 +660,81 @@ def graph_run(layer, args, device):
     mean = max_over_ranks(sum(ms) / len(ms), device)
     return {"graph": g, "x": x_d, "logits": L_d, "y": y_d, "ws": ws,
             "ms_per_step": mean}
+
+
+def e2e_pipelined(layer, args, world, device):
+    """Same metric end to end through moe_layer_graph with two buffer sets:
+    every step copies its x and logits from pinned host memory and its y
+    back, on a copy stream that overlaps the neighbouring steps' compute
+    (step i+1's inputs go in while step i runs; step i's output comes back
+    while step i+1 runs).  One workspace, one compute stream: the layers
+    themselves run one after another."""
+    moe = layer.moe
+    x_h = layer.x.cpu().pin_memory()
+    L_h = layer.logits.cpu().pin_memory()
+    y_h = [torch.empty(layer.b["y"].shape, dtype=layer.b["y"].dtype,
+                       pin_memory=True) for _ in range(2)]
+    ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
+    sets = []
+    for _ in range(2):
+        x_d = torch.empty_like(layer.x)
+        L_d = torch.empty_like(layer.logits)
+        y_d = torch.empty_like(layer.b["y"])
+        g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws)
+        sets.append((x_d, L_d, y_d, g))
+    comp = torch.cuda.current_stream()
+    up = torch.cuda.Stream(device=device)     # host -> device
+    down = torch.cuda.Stream(device=device)   # device -> host
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    free = [ev(), ev()]
+    for e in free:
+        e.record(down)
+
+    def steps(n):
+        for i in range(n):
+            b = i % 2
+            x_d, L_d, y_d, g = sets[b]
+            with torch.cuda.stream(up):
+                up.wait_event(free[b])       # buffer b's last output is out
+                x_d.copy_(x_h, non_blocking=True)
+                L_d.copy_(L_h, non_blocking=True)
+                h2d = ev()
+                h2d.record(up)
+            comp.wait_event(h2d)
+            g.launch(comp)
+            done = ev()
+            done.record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done)
+                y_h[b].copy_(y_d, non_blocking=True)
+                free[b].record(down)
+
+    steps(max(1, args.warmup))
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    up.wait_event(a)
+    down.wait_event(a)
+    steps(args.steps)
+    comp.wait_stream(up)
+    comp.wait_stream(down)
+    z.record(comp)
+    z.synchronize()
+    mean = max_over_ranks(a.elapsed_time(z) / args.steps, device)
+    # the last step's output reached the host and equals the device result
+    if not torch.equal(y_h[(args.steps - 1) % 2], layer.b["y"].cpu()):
+        raise SystemExit("pipelined end-to-end output differs")
+    for s_ in sets:
+        s_[3].close()
+    h2d = x_h.numel() * x_h.element_size() + L_h.numel() * L_h.element_size()
+    d2h = y_h[0].numel() * y_h[0].element_size()
+    return {"value": round(whole_job_tokens_per_s(world, layer.wl.T, mean), 1),
+            "unit": UNIT, "ms_per_step": round(mean, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "moe_layer_graph_launch (C ABI), pinned host buffers, "
+                   "copies on two copy streams overlapping neighbouring "
+                   "steps"}
 
 
 def e2e_run(layer, args, world, device, graph=None):
