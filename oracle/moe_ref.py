@@ -640,3 +640,157 @@ def layer_redundant(cfg: MoEConfig, x, logits, weights: ExpertWeights,
     y = combine(ys, perm.row_of, w, cfg.H)
     return LayerResult(y, idx, w, counts, vshard, C, False,
                        required_factor(vshard, cfg.T, cfg.k), perm, xs, h, ys)
+
+
+# ---------------------------------------------------------------------------
+# Backward pass.  "Support moe_dropless_fallback=layer on the ragged
+# all-to-all MoE path" (MaxText pull request 5920): section Tests requires
+# the fallback's outputs AND gradients to match the dropless model; section
+# How: the chunked fallback recomputes one chunk at a time in the backward
+# and accumulates the expert-weight gradients across chunks.  "MoE
+# ring-of-experts ... x_sorted remat save" (MaxText pull request 4969),
+# section What: the backward reuses the expert-sorted input and its routing
+# metadata instead of re-running the dispatch.
+# Gradients of the layer output y w.r.t. x, the router logits (through the
+# combine weights; the top-k choice itself is piecewise constant) and the
+# expert weights, given dy = dL/dy.  The chain, per routed row r = (t, j)
+# of expert e (dropped rows carry no gradient):
+#   dw[t,j] = <dy[t], y_sorted[r]>,   dy_sorted[r] = w[t,j] dy[t]
+#   dWd[e] += h_r^T dy_sorted[r],     dh_r = dy_sorted[r] Wd[e]^T
+#   dg_r = dh_r * u_r * silu'(g_r),   du_r = dh_r * silu(g_r)
+#   dWg[e] += x_r^T dg_r,  dWu[e] += x_r^T du_r
+#   dx_sorted[r] = dg_r Wg[e]^T + du_r Wu[e]^T,   dx[t] = sum_j dx_sorted[r]
+# with silu'(z) = s(z) (1 + z (1 - s(z))), s = logistic; and for the logits
+#   w = softmax(all logits) read at the chosen experts:
+#     dp[e] = sum_j [idx_j = e] dw_j,  dlogits = p * (dp - <p, dp>)
+#   renorm (softmax over the k chosen): dlogits[idx_j] = w_j (dw_j - sum w dw)
+# ---------------------------------------------------------------------------
+def silu_grad(z: np.ndarray) -> np.ndarray:
+    z = np.asarray(z, dtype=np.float64)
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+@dataclass
+class Gradients:
+    dx: np.ndarray
+    dlogits: np.ndarray
+    dwg: np.ndarray
+    dwu: np.ndarray
+    dwd: np.ndarray
+    dtopk_w: np.ndarray
+
+
+def route_backward(logits: np.ndarray, idx: np.ndarray, dw: np.ndarray,
+                   renorm: bool) -> np.ndarray:
+    logits = np.asarray(logits)
+    T, E = logits.shape
+    k = idx.shape[1]
+    dl = np.zeros((T, E), dtype=np.float64)
+    for t in range(T):
+        if renorm:
+            w = softmax_f64([logits[t, e] for e in idx[t]])
+            dot = sum(w[j] * dw[t, j] for j in range(k))
+            for j in range(k):
+                dl[t, idx[t, j]] += w[j] * (dw[t, j] - dot)
+        else:
+            p = softmax_f64(logits[t])
+            dp = [0.0] * E
+            for j in range(k):
+                dp[int(idx[t, j])] += float(dw[t, j])
+            dot = sum(p[e] * dp[e] for e in range(E))
+            for e in range(E):
+                dl[t, e] = p[e] * (dp[e] - dot)
+    return dl
+
+
+def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
+                        dy, C: Optional[int]) -> Gradients:
+    """Backward of one pass (capacity C, None = uncapped) over in-memory
+    float64 weights [E,H,F], [E,H,F], [E,F,H]."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    T, H = x.shape
+    idx, w, _ = route(logits, cfg.k, cfg.renorm)
+    perm = permute_indices(idx, cfg.E, cfg.S, C)
+    xs = gather_rows(x, perm.sorted_token)
+    R = len(perm.sorted_token)
+    F = w_gate.shape[2]
+    dwg = np.zeros_like(w_gate, dtype=np.float64)
+    dwu = np.zeros_like(w_up, dtype=np.float64)
+    dwd = np.zeros_like(w_down, dtype=np.float64)
+    ys = np.zeros((R, H))
+    hs = np.zeros((R, F))
+    gs = np.zeros((R, F))
+    us = np.zeros((R, F))
+    for e in range(cfg.E):
+        a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
+        if a == b:
+            continue
+        gs[a:b] = xs[a:b] @ w_gate[e]
+        us[a:b] = xs[a:b] @ w_up[e]
+        hs[a:b] = silu(gs[a:b]) * us[a:b]
+        ys[a:b] = hs[a:b] @ w_down[e]
+    dtw = np.zeros((T, cfg.k))
+    dys = np.zeros((R, H))
+    for t in range(T):
+        for j in range(cfg.k):
+            r = int(perm.row_of[t, j])
+            if r >= 0:
+                dtw[t, j] = float(dy[t] @ ys[r])
+                dys[r] = w[t, j] * dy[t]
+    dxs = np.zeros((R, H))
+    for e in range(cfg.E):
+        a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
+        if a == b:
+            continue
+        dwd[e] = hs[a:b].T @ dys[a:b]
+        dh = dys[a:b] @ w_down[e].T
+        dg = dh * us[a:b] * silu_grad(gs[a:b])
+        du = dh * silu(gs[a:b])
+        dwg[e] = xs[a:b].T @ dg
+        dwu[e] = xs[a:b].T @ du
+        dxs[a:b] = dg @ w_gate[e].T + du @ w_up[e].T
+    dx = np.zeros((T, H))
+    for t in range(T):
+        for j in range(cfg.k):
+            r = int(perm.row_of[t, j])
+            if r >= 0:
+                dx[t] += dxs[r]
+    dl = route_backward(logits, idx, dtw, cfg.renorm)
+    return Gradients(dx, dl, dwg, dwu, dwd, dtw)
+
+
+def layer_backward_dropless(cfg, x, logits, w_gate, w_up, w_down, dy):
+    return layer_pass_backward(cfg, x, logits, w_gate, w_up, w_down, dy, None)
+
+
+def layer_backward_capped(cfg, x, logits, w_gate, w_up, w_down, dy):
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    return layer_pass_backward(cfg, x, logits, w_gate, w_up, w_down, dy, C)
+
+
+def layer_backward_chunked(cfg, x, logits, w_gate, w_up, w_down, dy):
+    """The chunked fallback's backward: each chunk's pass is differentiated
+    on its own and the weight gradients are summed over chunks."""
+    x = np.asarray(x, dtype=np.float64)
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    plan = chunk_plan(cfg.T, cfg.k, cfg.E, cfg.S, C, cfg.n_chunks)
+    out = Gradients(np.zeros_like(x), np.zeros((cfg.T, cfg.E)),
+                    np.zeros_like(w_gate, dtype=np.float64),
+                    np.zeros_like(w_up, dtype=np.float64),
+                    np.zeros_like(w_down, dtype=np.float64),
+                    np.zeros((cfg.T, cfg.k)))
+    for (t0, t1) in plan:
+        sub = MoEConfig(t1 - t0, cfg.H, cfg.E, cfg.k, cfg.F, cfg.S, -1.0, 0,
+                        cfg.renorm)
+        g = layer_pass_backward(sub, x[t0:t1], np.asarray(logits)[t0:t1],
+                                w_gate, w_up, w_down, np.asarray(dy)[t0:t1],
+                                None)
+        out.dx[t0:t1] = g.dx
+        out.dlogits[t0:t1] = g.dlogits
+        out.dtopk_w[t0:t1] = g.dtopk_w
+        out.dwg += g.dwg
+        out.dwu += g.dwu
+        out.dwd += g.dwd
+    return out

@@ -567,4 +567,100 @@ def pin_redundancy_preserves_the_layer():
     assert sizes[[g for g in range(G) if g % (E // S + 2) >= E // S]].sum() > 0
 
 
+# --------------------------------------------------------------------------
+# backward pass: central finite differences of L = sum(y * dy) in float64
+# (independent of the analytic chain rule), chunked == dropless, and a
+# dense-MLP reduction through torch.autograd
+# --------------------------------------------------------------------------
+def _tiny_backward_case(seed, T=6, H=4, E=4, k=2, F=3, S=2):
+    rng = _rng(seed)
+    x = rng.standard_normal((T, H))
+    # distinct, well separated logits: the top-k choice is stable under eps
+    L = rng.permutation(T * E).reshape(T, E) * 0.37 - 3.0
+    w = (rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F)),
+         rng.standard_normal((E, F, H)))
+    dy = rng.standard_normal((T, H))
+    return x, L.astype(np.float64), w, dy
+
+
+def _fd_check(loss, arr, grad, eps=1e-6, tol=1e-6):
+    it = np.nditer(arr, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = arr[i]
+        arr[i] = old + eps
+        lp = loss()
+        arr[i] = old - eps
+        lm = loss()
+        arr[i] = old
+        fd = (lp - lm) / (2 * eps)
+        assert abs(fd - grad[i]) <= tol * max(1.0, abs(fd)), (i, fd, grad[i])
+
+
+def pin_backward_finite_differences():
+    for renorm in (False, True):
+        for factor in (-1.0, 0.6):          # dropless, and capped with drops
+            x, L, (wg, wu, wd), dy = _tiny_backward_case(14)
+            cfg = ref.MoEConfig(6, 4, 4, 2, 3, 2, factor, 0, renorm)
+            back = ref.layer_backward_capped if factor > 0 else \
+                ref.layer_backward_dropless
+            run = ref.layer_capped if factor > 0 else ref.layer_dropless
+            g = back(cfg, x, L, wg, wu, wd, dy)
+
+            def loss():
+                y = run(cfg, x, L, ref.dense_weights(wg, wu, wd)).y
+                return float((y * dy).sum())
+            _fd_check(loss, x, g.dx)
+            _fd_check(loss, L, g.dlogits)
+            _fd_check(loss, wg, g.dwg)
+            _fd_check(loss, wu, g.dwu)
+            _fd_check(loss, wd, g.dwd)
+            if factor > 0:   # the capped pass dropped rows: no gradient there
+                C = ref.capacity(6, 2, 2, factor)
+                idx, _, _ = ref.route(L, 2, renorm)
+                p = ref.permute_indices(idx, 4, 2, C)
+                assert p.n_dropped > 0
+                assert np.all(g.dtopk_w[p.row_of < 0] == 0)
+
+
+def pin_backward_chunked_equals_dropless():
+    rng = _rng(15)
+    T, H, E, k, F, S = 40, 5, 8, 2, 4, 2
+    x = rng.standard_normal((T, H))
+    L = rng.standard_normal((T, E))
+    L[:, :3] += 1.5
+    w = (rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F)),
+         rng.standard_normal((E, F, H)))
+    dy = rng.standard_normal((T, H))
+    cfg = ref.MoEConfig(T, H, E, k, F, S, 0.2)
+    drop = ref.layer_backward_dropless(cfg, x, L, *w, dy)
+    chunk = ref.layer_backward_chunked(cfg, x, L, *w, dy)
+    C = ref.capacity(T, k, S, 0.2)
+    assert len(ref.chunk_plan(T, k, E, S, C)) > 1
+    for a, b in ((drop.dx, chunk.dx), (drop.dlogits, chunk.dlogits),
+                 (drop.dwg, chunk.dwg), (drop.dwu, chunk.dwu),
+                 (drop.dwd, chunk.dwd)):
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def pin_backward_dense_reduction():
+    rng = _rng(16)
+    T, H, F = 7, 5, 6
+    x = rng.standard_normal((T, H))
+    w = (rng.standard_normal((1, H, F)), rng.standard_normal((1, H, F)),
+         rng.standard_normal((1, F, H)))
+    dy = rng.standard_normal((T, H))
+    cfg = ref.MoEConfig(T, H, 1, 1, F, 1, -1.0, 0, True)
+    g = ref.layer_backward_dropless(cfg, x, np.zeros((T, 1)), *w, dy)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = [torch.tensor(a[0], requires_grad=True) for a in w]
+    y = (torch.nn.functional.silu(xt @ wt[0]) * (xt @ wt[1])) @ wt[2]
+    (y * torch.from_numpy(dy)).sum().backward()
+    assert np.allclose(g.dx, xt.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(g.dwg[0], wt[0].grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(g.dwu[0], wt[1].grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(g.dwd[0], wt[2].grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.all(g.dlogits == 0)       # one expert, renorm: weight is 1
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -51,8 +51,11 @@ MUTANTS = {
     "gate_up_swapped": ("h = silu(g) * u", "h = silu(u) * g"),
     "combine_ignores_weight": (
         "y[t] += float(topk_w[t, j]) * y_sorted[r]", "y[t] += y_sorted[r]"),
-    "combine_skips_row_zero": ("            if r >= 0:\n",
-                               "            if r > 0:\n"),
+    "combine_skips_row_zero": (
+        "            if r >= 0:\n"
+        "                y[t] += float(topk_w[t, j]) * y_sorted[r]",
+        "            if r > 0:\n"
+        "                y[t] += float(topk_w[t, j]) * y_sorted[r]"),
     "chunk_ignores_shard_bound": (
         "c = max(1, C // worst_per_token)", "c = max(1, C // k)"),
     "dup_without_has_candidate": (
@@ -69,6 +72,24 @@ MUTANTS = {
     "reroute_first_rows": (
         "            if seen[e] >= keep and plan.slot_of[e] >= 0:",
         "            if seen[e] < int(plan.divert[e]) and plan.slot_of[e] >= 0:"),
+    "silu_grad_wrong": (
+        "    return s * (1.0 + z * (1.0 - s))",
+        "    return s * (1.0 + z * s)"),
+    "swiglu_backward_drops_u": (
+        "        dg = dh * us[a:b] * silu_grad(gs[a:b])",
+        "        dg = dh * silu_grad(gs[a:b])"),
+    "dy_sorted_unweighted": (
+        "                dys[r] = w[t, j] * dy[t]",
+        "                dys[r] = dy[t]"),
+    "softmax_jacobian_sign": (
+        "                dl[t, e] = p[e] * (dp[e] - dot)",
+        "                dl[t, e] = p[e] * (dp[e] + dot)"),
+    "dx_gate_only": (
+        "        dxs[a:b] = dg @ w_gate[e].T + du @ w_up[e].T",
+        "        dxs[a:b] = dg @ w_gate[e].T"),
+    "chunked_dw_not_summed": (
+        "        out.dwg += g.dwg",
+        "        out.dwg = g.dwg"),
     "chunk_one_too_big": (
         "c = max(1, C // worst_per_token)",
         "c = max(1, C // worst_per_token + 1)"),
