@@ -392,12 +392,86 @@ int32_t moe_layer_graph_fallback_chunks(const moe_layer_graph_t *graph);
 void moe_layer_graph_destroy(moe_layer_graph_t *graph);
 
 /* ----------------------------------------------------------------------
+ * Backward pass.  "Support moe_dropless_fallback=layer on the ragged
+ * all-to-all MoE path" [PR5920 Tests]: with the layer fallback, outputs
+ * AND gradients match the dropless model; [PR5920 How]: the fallback's
+ * backward recomputes one chunk at a time and accumulates the expert-weight
+ * gradients across chunks.  Per routed row r = (t, j) of expert e:
+ *   dw[t,j] = <dy[t], y_sorted[r]>,  dy_sorted[r] = w[t,j] dy[t]
+ *   dWd[e] += h^T dy_sorted,  dh = dy_sorted Wd[e]^T
+ *   dg = dh * u * silu'(g),  du = dh * silu(g)
+ *   dWg[e] += x^T dg,  dWu[e] += x^T du,  dx_sorted = dg Wg^T + du Wu^T
+ *   dx[t] = sum_j dx_sorted[r];  dlogits through the softmax weights.
+ * Weight gradients are float32 [E,H,F], [E,H,F], [E,F,H]; the rest uses the
+ * layer dtype (dy, dx, dy_sorted, dx_sorted, g, u) or float32 (dtopk_w,
+ * dlogits).  Dropped rows (row_of < 0) get no gradient.
+ * ---------------------------------------------------------------------- */
+
+/* dy_sorted [T*k,H] and dtopk_w [T,k] (float32) from dy [T,H]. */
+moe_status_t moe_combine_backward(const moe_config_t *cfg, const void *dy,
+                                  const void *y_sorted, const int32_t *row_of,
+                                  const float *topk_w, void *dy_sorted,
+                                  float *dtopk_w, moe_stream_t stream);
+
+/* dlogits [T,E] (float32) from dtopk_w through the combine weights. */
+moe_status_t moe_route_backward(const moe_config_t *cfg, const float *logits,
+                                const int32_t *topk_idx, const float *dtopk_w,
+                                float *dlogits, moe_stream_t stream);
+
+/* dx [T,H] = sum over a token's kept rows of dx_sorted. */
+moe_status_t moe_permute_backward(const moe_config_t *cfg,
+                                  const void *dx_sorted, const int32_t *row_of,
+                                  void *dx, moe_stream_t stream);
+
+/* Forward GEMMs that also keep g = x Wg and u = x Wu ([T*k, F] each) for
+ * the backward: h and y_sorted as moe_gmm_swiglu. */
+moe_status_t moe_gmm_swiglu_saved(const moe_config_t *cfg,
+                                  const void *x_sorted,
+                                  const int32_t *group_offsets,
+                                  const void *w_gate, const void *w_up,
+                                  const void *w_down, void *g, void *u,
+                                  void *h, void *y_sorted,
+                                  int32_t *status_word, moe_stream_t stream);
+
+/* Backward of the grouped SwiGLU FFN.  accumulate != 0 adds the weight
+ * gradients into dw_* (float32), 0 overwrites them (every expert, also
+ * those without rows).  workspace: moe_workspace_bytes(cfg,
+ * MOE_WS_GMM_BACKWARD) (dg and du). */
+moe_status_t moe_gmm_swiglu_backward(const moe_config_t *cfg,
+                                     const void *x_sorted,
+                                     const int32_t *group_offsets,
+                                     const void *w_gate, const void *w_up,
+                                     const void *w_down, const void *g,
+                                     const void *u, const void *h,
+                                     const void *dy_sorted, void *dx_sorted,
+                                     float *dw_gate, float *dw_up,
+                                     float *dw_down, int32_t accumulate,
+                                     int32_t *status_word, void *workspace,
+                                     size_t workspace_bytes,
+                                     moe_stream_t stream);
+
+/* The whole layer's backward (recomputing its forward, as the chunked
+ * fallback does), for the mode given (as moe_layer): dx [T,H], dlogits
+ * [T,E] float32, dw_* float32 (overwritten).  info as moe_layer.
+ * workspace: moe_workspace_bytes(cfg, MOE_WS_LAYER_BACKWARD). */
+moe_status_t moe_layer_backward(const moe_config_t *cfg, const void *x,
+                                const float *logits, const void *w_gate,
+                                const void *w_up, const void *w_down,
+                                const void *dy, void *dx, float *dlogits,
+                                float *dw_gate, float *dw_up, float *dw_down,
+                                moe_mode_t mode, moe_layer_info_t *info,
+                                int32_t *status_word, void *workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
  * Host-side queries (no GPU work).
  * ---------------------------------------------------------------------- */
 typedef enum {
-  MOE_WS_PERMUTE = 0, /* moe_permute                                   */
-  MOE_WS_CHUNKED = 1, /* moe_layer_dropless_chunked                    */
-  MOE_WS_LAYER = 2    /* moe_layer                                     */
+  MOE_WS_PERMUTE = 0,       /* moe_permute                              */
+  MOE_WS_CHUNKED = 1,       /* moe_layer_dropless_chunked               */
+  MOE_WS_LAYER = 2,         /* moe_layer                                */
+  MOE_WS_GMM_BACKWARD = 3,  /* moe_gmm_swiglu_backward                  */
+  MOE_WS_LAYER_BACKWARD = 4 /* moe_layer_backward                       */
 } moe_ws_kind_t;
 
 /* Workspace bytes an entry point needs for cfg (0 for an invalid cfg). */

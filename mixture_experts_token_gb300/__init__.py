@@ -23,6 +23,7 @@ MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 1, 2, 4
 MOE_F32, MOE_BF16 = 0, 1
 MOE_MODE_FALLBACK_LAYER, MOE_MODE_CAPPED, MOE_MODE_DROPLESS = 0, 1, 2
 MOE_WS_PERMUTE, MOE_WS_CHUNKED, MOE_WS_LAYER = 0, 1, 2
+MOE_WS_GMM_BACKWARD, MOE_WS_LAYER_BACKWARD = 3, 4
 
 
 class MoeConfig(ctypes.Structure):
@@ -97,6 +98,15 @@ def _declare(h):
                                        P],
         "moe_layer": [cfg, P, P, P, P, P, P, c_int,
                       ctypes.POINTER(MoeLayerInfo), P, P, c_size_t, P],
+        "moe_combine_backward": [cfg, P, P, P, P, P, P, P],
+        "moe_route_backward": [cfg, P, P, P, P, P],
+        "moe_permute_backward": [cfg, P, P, P, P],
+        "moe_gmm_swiglu_saved": [cfg, P, P, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_swiglu_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, P,
+                                    P, c_int32, P, P, c_size_t, P],
+        "moe_layer_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, c_int,
+                               ctypes.POINTER(MoeLayerInfo), P, P, c_size_t,
+                               P],
     }
     for name, args in sig.items():
         fn = getattr(h, name)
@@ -315,6 +325,61 @@ def moe_layer(cfg, x, logits, w_gate, w_up, w_down, y, mode, workspace,
         ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
         _ptr(w_down), _ptr(y), mode, ctypes.byref(info), _ptr(status_word),
         _ptr(workspace), _nbytes(workspace), _stream(stream)), "moe_layer")
+    return {"overflow": info.overflow, "n_chunks": info.n_chunks,
+            "capacity": info.capacity}
+
+
+# --------------------------------------------------------- backward ------
+def moe_combine_backward(cfg, dy, y_sorted, row_of, topk_w, dy_sorted,
+                         dtopk_w, stream=None):
+    _check(lib().moe_combine_backward(
+        ctypes.byref(cfg), _ptr(dy), _ptr(y_sorted), _ptr(row_of),
+        _ptr(topk_w), _ptr(dy_sorted), _ptr(dtopk_w), _stream(stream)),
+        "moe_combine_backward")
+
+
+def moe_route_backward(cfg, logits, topk_idx, dtopk_w, dlogits, stream=None):
+    _check(lib().moe_route_backward(
+        ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx), _ptr(dtopk_w),
+        _ptr(dlogits), _stream(stream)), "moe_route_backward")
+
+
+def moe_permute_backward(cfg, dx_sorted, row_of, dx, stream=None):
+    _check(lib().moe_permute_backward(
+        ctypes.byref(cfg), _ptr(dx_sorted), _ptr(row_of), _ptr(dx),
+        _stream(stream)), "moe_permute_backward")
+
+
+def moe_gmm_swiglu_saved(cfg, x_sorted, group_offsets, w_gate, w_up, w_down,
+                         g, u, h, y_sorted, status_word=None, stream=None):
+    _check(lib().moe_gmm_swiglu_saved(
+        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(g), _ptr(u), _ptr(h), _ptr(y_sorted),
+        _ptr(status_word), _stream(stream)), "moe_gmm_swiglu_saved")
+
+
+def moe_gmm_swiglu_backward(cfg, x_sorted, group_offsets, w_gate, w_up,
+                            w_down, g, u, h, dy_sorted, dx_sorted, dw_gate,
+                            dw_up, dw_down, accumulate, workspace,
+                            status_word=None, stream=None):
+    _check(lib().moe_gmm_swiglu_backward(
+        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(g), _ptr(u), _ptr(h), _ptr(dy_sorted),
+        _ptr(dx_sorted), _ptr(dw_gate), _ptr(dw_up), _ptr(dw_down),
+        int(accumulate), _ptr(status_word), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "moe_gmm_swiglu_backward")
+
+
+def moe_layer_backward(cfg, x, logits, w_gate, w_up, w_down, dy, dx,
+                       dlogits, dw_gate, dw_up, dw_down, mode, workspace,
+                       status_word=None, stream=None) -> dict:
+    info = MoeLayerInfo()
+    _check(lib().moe_layer_backward(
+        ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(dy), _ptr(dx), _ptr(dlogits), _ptr(dw_gate),
+        _ptr(dw_up), _ptr(dw_down), mode, ctypes.byref(info),
+        _ptr(status_word), _ptr(workspace), _nbytes(workspace),
+        _stream(stream)), "moe_layer_backward")
     return {"overflow": info.overflow, "n_chunks": info.n_chunks,
             "capacity": info.capacity}
 

@@ -267,6 +267,10 @@ size_t moe_workspace_bytes(const moe_config_t* cfg, moe_ws_kind_t which) {
       return layer_bytes(*cfg, chunk_tokens(*cfg));
     case MOE_WS_LAYER:
       return layer_bytes(*cfg, cfg->T);
+    case MOE_WS_GMM_BACKWARD:
+      return gmm_backward_bytes(*cfg);
+    case MOE_WS_LAYER_BACKWARD:
+      return layer_backward_bytes(*cfg);
   }
   return 0;
 }

@@ -11,6 +11,8 @@
 // compile-time bound so the loads overlap), accumulates in fp32 in slot
 // order j = 0..k-1 (deterministic: no atomics), and stores once.
 // Algorithmic traffic: R_kept*H*b read + T*H*b written.
+// With null weights every kept row counts once: the permute's transpose,
+// dx[t] = sum_j dx_sorted[row_of[t,j]], in the backward pass.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -74,7 +76,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   if (tid < KMAX) {
     const bool on = tid < k;
     rows[tid] = on ? row_of[static_cast<long long>(t) * k + tid] : -1;
-    wts[tid] = on ? topk_w[static_cast<long long>(t) * k + tid] : 0.0f;
+    wts[tid] = !on ? 0.0f
+                   : topk_w ? topk_w[static_cast<long long>(t) * k + tid]
+                            : 1.0f;
   }
   __syncthreads();
   for (int c0 = tid; c0 < n16; c0 += kThreads * kUnroll) {

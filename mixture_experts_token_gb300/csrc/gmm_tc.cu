@@ -81,6 +81,12 @@ struct Params {
   __nv_bfloat16* out;
   int out_ld;   // F (GEMM1) or H (GEMM2)
   int32_t* status;
+  // Backward and saving modes: second/third outputs and epilogue inputs.
+  __nv_bfloat16* out2 = nullptr;        // MODE 4: u;  MODE 2: du
+  __nv_bfloat16* out3 = nullptr;        // MODE 4: g
+  const __nv_bfloat16* aux_g = nullptr; // MODE 2: g
+  const __nv_bfloat16* aux_u = nullptr; // MODE 2: u
+  int k_split = 0;                      // MODE 3: k-blocks from the 1st pair
   // Tests of the timeout path only: the producer stops after this many
   // stage fills (-1: never), so the MMA warp's next wait runs out.
   long long stall_after_fills = -1;
@@ -355,8 +361,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo,
 // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
 // B bf16 (bits 10-12), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N,
+                                                  bool b_mn_major = true,
+                                                  bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) |
+         (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
          (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -476,13 +485,22 @@ __device__ void build_tile_table(const int32_t* __restrict__ off, int G,
 // ----------------------------------------------------------- kernel ------
 // MODE 0: out = h = silu(A Wg) * (A Wu), BN = 256 (128 gate + 128 up cols)
 // MODE 1: out = y_sorted = A Wd, BN = 256 or 128
+// MODE 4: MODE 0 that also stores g (out3) and u (out2) for the backward
+// MODE 2: dh = dy_sorted Wd^T with Wd read K-major (one 64 x 256 box); the
+//         epilogue turns dh into dg (out) and du (out2) with g, u (aux_*)
+// MODE 3: dx_sorted = [dg | du] [Wg^T ; Wu^T]: K = 2F, the first k_split
+//         k-blocks from (tmA, tmB0), the rest from (tmA1, tmB1), K-major B
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                   const __grid_constant__ CUtensorMap tmB0,
-                  const __grid_constant__ CUtensorMap tmB1, Params p) {
+                  const __grid_constant__ CUtensorMap tmB1,
+                  const __grid_constant__ CUtensorMap tmA1, Params p) {
   using L = Tile<BN>;
-  static_assert(MODE == 1 || BN == 256, "GEMM1 tile is 128 gate + 128 up");
+  static_assert(MODE == 1 || MODE == 2 || MODE == 3 || BN == 256,
+                "gate + up tiles are 128 + 128 columns");
+  constexpr bool kGateUp = MODE == 0 || MODE == 4;   // MN-major gate/up B
+  constexpr bool kBKMajor = MODE == 2 || MODE == 3;  // K-major B
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -519,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB0);
-    if (MODE == 0) prefetch_tmap(&tmB1);
+    if (kGateUp || MODE == 3) prefetch_tmap(&tmB1);
+    if (MODE == 3) prefetch_tmap(&tmA1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -569,17 +588,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(fb, L::kStage);
           const uint32_t sa = smem_base + stage * L::kStage;
           const uint32_t sb = sa + L::kABytes;
-          tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
-          if (MODE == 0) {
+          if (kGateUp) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
             tma_load_2d(sb, &tmB0, fb, n * 128, b_row + kb * BK);
             tma_load_2d(sb + 8192, &tmB0, fb, n * 128 + 64, b_row + kb * BK);
             tma_load_2d(sb + 16384, &tmB1, fb, n * 128, b_row + kb * BK);
             tma_load_2d(sb + 24576, &tmB1, fb, n * 128 + 64, b_row + kb * BK);
-          } else {
+          } else if (MODE == 1) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
               tma_load_2d(sb + c * 8192, &tmB0, fb, n * BN + c * 64,
                           b_row + kb * BK);
+          } else if (MODE == 2) {
+            // B rows = the BN output columns (f) of expert we, K-major:
+            // Wd[we] is [F, H] with H (the reduction) contiguous
+            tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
+            tma_load_2d(sb, &tmB0, fb, kb * BK, we * p.out_ld + n * BN);
+          } else {  // MODE 3: Wg[we], Wu[we] are [H, F], F contiguous
+            const bool second = kb >= p.k_split;
+            const int kk = (second ? kb - p.k_split : kb) * BK;
+            tma_load_2d(sa, second ? &tmA1 : &tmA, fb, kk, a_row);
+            tma_load_2d(sb, second ? &tmB1 : &tmB0, fb, kk,
+                        we * p.out_ld + n * BN);
           }
           ++fills;
           if (++stage == STAGES) {
@@ -598,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer -------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, BN);
+      constexpr uint32_t idesc = make_idesc(BM, BN, !kBKMajor);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -621,7 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
+            // K-major B: 256 rows of 128 B, advanced 32 B per K=16 step;
+            // N-major B: 64-column chunks 8 KB apart, 16 k-rows per step
+            const uint64_t bd = kBKMajor
+                                    ? smem_desc(sb + kk * 32, 16, 1024)
+                                    : smem_desc(sb + kk * 2048, 8192, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(smem_u32(empty + stage));
@@ -656,9 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = grow < goff[e + 1];
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      if (MODE == 0) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + static_cast<long long>(grow) * p.out_ld + n * 128);
+      if (kGateUp) {
+        const long long base = static_cast<long long>(grow) * p.out_ld + n * 128;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + base);
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t g[32], u[32];
@@ -679,6 +714,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v = 0; v < 4; ++v)
               dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
                                           pk[4 * v + 2], pk[4 * v + 3]);
+          }
+          if (MODE == 4 && valid) {  // keep g and u for the backward
+            uint4* dg_ = reinterpret_cast<uint4*>(p.out3 + base);
+            uint4* du_ = reinterpret_cast<uint4*>(p.out2 + base);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t a[4], b[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int i = 4 * v + q;
+                a[q] = pack_bf16x2(__uint_as_float(g[2 * i]),
+                                   __uint_as_float(g[2 * i + 1]));
+                b[q] = pack_bf16x2(__uint_as_float(u[2 * i]),
+                                   __uint_as_float(u[2 * i + 1]));
+              }
+              dg_[c / 8 + v] = make_uint4(a[0], a[1], a[2], a[3]);
+              du_[c / 8 + v] = make_uint4(b[0], b[1], b[2], b[3]);
+            }
+          }
+        }
+      } else if (MODE == 2) {
+        // dh (TMEM) -> dg = dh * u * silu'(g), du = dh * silu(g)
+        const long long base = static_cast<long long>(grow) * p.out_ld + n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          if (!valid) continue;
+          uint32_t gk[16], uk[16];
+          const uint4* gs = reinterpret_cast<const uint4*>(p.aux_g + base + c);
+          const uint4* us = reinterpret_cast<const uint4*>(p.aux_u + base + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 a = gs[v], b = us[v];
+            gk[4 * v] = a.x; gk[4 * v + 1] = a.y;
+            gk[4 * v + 2] = a.z; gk[4 * v + 3] = a.w;
+            uk[4 * v] = b.x; uk[4 * v + 1] = b.y;
+            uk[4 * v + 2] = b.z; uk[4 * v + 3] = b.w;
+          }
+          uint32_t pg[16], pu[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float dgv[2], duv[2];
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+              const float gv = __uint_as_float(
+                  hlf ? (gk[i] & 0xffff0000u) : (gk[i] << 16));
+              const float uv = __uint_as_float(
+                  hlf ? (uk[i] & 0xffff0000u) : (uk[i] << 16));
+              const float dh = __uint_as_float(r[2 * i + hlf]);
+              const float sg = 1.0f / (1.0f + __expf(-gv));
+              dgv[hlf] = dh * uv * sg * (1.0f + gv * (1.0f - sg));
+              duv[hlf] = dh * gv * sg;
+            }
+            pg[i] = pack_bf16x2(dgv[0], dgv[1]);
+            pu[i] = pack_bf16x2(duv[0], duv[1]);
+          }
+          uint4* dgo = reinterpret_cast<uint4*>(p.out + base + c);
+          uint4* duo = reinterpret_cast<uint4*>(p.out2 + base + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            dgo[v] = make_uint4(pg[4 * v], pg[4 * v + 1], pg[4 * v + 2],
+                                pg[4 * v + 3]);
+            duo[v] = make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2],
+                                pu[4 * v + 3]);
           }
         }
       } else {
@@ -958,6 +1058,379 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------- weight gradients ------
+// dW[e] (+)= P_e^T Q_e over the rows of expert e: P = x_sorted, Q = [dg | du]
+// (WMODE 0: dWg and dWu, tile = 128 rows of H x (128 gate + 128 up) cols
+// of F) or P = h, Q = dy_sorted (WMODE 1: dWd, 128 rows of F x BN of H).
+// The reduction runs over routed rows, so both operands are read
+// "MN-major" straight from the row-major activations: TMA box {64 cols,
+// 64 rows}, one 8 KB box per 64 columns, descriptors LBO = 8192, SBO =
+// 1024, start advanced 2048 B per K=16 step, and both major bits set.
+// K is ragged: a group's last k-block holds rows of the next group (or TMA
+// zero fill, or unwritten rows past the end), so the MMA warp clears those
+// rows of both operands in shared memory before it issues the block.
+// Segments: rows of one expert may sit in several independent row ranges
+// (one per chunk of the chunked fallback); a tile accumulates all of them
+// in tensor memory before its single write.  The epilogue moves each
+// 32 x 32 fp32 sub-tile through a 128-byte-swizzled staging buffer to a
+// TMA store (overwrite) or a TMA reduce-add (accumulate in L2).
+constexpr int WSTAGES = 3;
+constexpr int kWStage = BM * BK * 2 + BK * 256 * 2;  // 48 KB
+constexpr int kStageBuf = 32 * 32 * 4;               // 4 KB
+constexpr int kMaxSeg = 16;
+
+struct WParams {
+  const int32_t* seg_off[kMaxSeg];  // [G+1] group row offsets per segment
+  int seg_base[kMaxSeg];            // row of the segment's first row
+  int n_seg;
+  const int32_t* group_expert;      // [G] or null (identity)
+  int G;
+  int m_tiles;   // 128-row tiles of one expert's dW
+  int n_tiles;   // column tiles
+  int reduce;    // 1: TMA reduce-add, 0: TMA store
+  int32_t* status;
+};
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m,
+                                             uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m,
+                                                  uint32_t src, int c0,
+                                                  int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile."
+      "bulk_group [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// At most one bulk group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ int wgrad_rows(const WParams& p, int g) {
+  int n = 0;
+  for (int sg = 0; sg < p.n_seg; ++sg)
+    n += __ldg(p.seg_off[sg] + g + 1) - __ldg(p.seg_off[sg] + g);
+  return n;
+}
+
+// tpre[g] = tiles of groups before g (a group with rows has m*n tiles).
+__device__ void build_wgrad_table(const WParams& p, int* tpre, int* wsum) {
+  const int G = p.G, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (G + kThreads - 1) / kThreads;
+  const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+  const int tiles = p.m_tiles * p.n_tiles;
+  int loc = 0;
+  for (int g = g0; g < g1; ++g) {
+    tpre[g] = wgrad_rows(p, g) > 0 ? tiles : 0;
+    loc += tpre[g];
+  }
+  int inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) wsum[w] = inc;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      const int v = wsum[i];
+      wsum[i] = run;
+      run += v;
+    }
+    wsum[kThreads / 32] = run;
+  }
+  __syncthreads();
+  int run = wsum[w] + inc - loc;
+  for (int g = g0; g < g1; ++g) {
+    const int v = tpre[g];
+    tpre[g] = run;
+    run += v;
+  }
+  if (tid == 0) tpre[G] = wsum[kThreads / 32];
+  __syncthreads();
+}
+
+template <int WMODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmP,
+                    const __grid_constant__ CUtensorMap tmQ0,
+                    const __grid_constant__ CUtensorMap tmQ1,
+                    const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1, WParams p) {
+  static_assert(WMODE == 1 || BN == 256, "gate + up tiles are 128 + 128");
+  constexpr int kAChunks = BM / 64;       // 2
+  constexpr int kBChunks = BN / 64;       // 2 or 4
+  constexpr uint32_t kTx = (kAChunks + kBChunks) * 8192;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stagebuf = smem + WSTAGES * kWStage;  // [4 warps][2][4 KB]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stagebuf + 8 * kStageBuf);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + WSTAGES;
+  uint64_t* tfull = bars + 2 * WSTAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
+  int* tpre = wsum + 16;                               // [G+1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WSTAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      mbar_init(smem_u32(tempty + a), kEpilogueThreads);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmP);
+    prefetch_tmap(&tmQ0);
+    if (WMODE == 0) prefetch_tmap(&tmQ1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  build_wgrad_table(p, tpre, wsum);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tpre[p.G];
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer -----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles;
+           tile += gridDim.x) {
+        const int g = group_of(tpre, p.G, tile);
+        const int local = tile - tpre[g];
+        const int m = local % p.m_tiles, n = local / p.m_tiles;
+        for (int sg = 0; ok && sg < p.n_seg; ++sg) {
+          const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
+          for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
+               r += BK) {
+            if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
+                           p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(full + stage);
+            mbar_expect_tx(fb, kTx);
+            const uint32_t sa = smem_base + stage * kWStage;
+            const uint32_t sb = sa + kAChunks * 8192;
+#pragma unroll
+            for (int j = 0; j < kAChunks; ++j)
+              tma_load_2d(sa + j * 8192, &tmP, fb, m * BM + j * 64, r);
+            if (WMODE == 0) {
+              tma_load_2d(sb, &tmQ0, fb, n * 128, r);
+              tma_load_2d(sb + 8192, &tmQ0, fb, n * 128 + 64, r);
+              tma_load_2d(sb + 16384, &tmQ1, fb, n * 128, r);
+              tma_load_2d(sb + 24576, &tmQ1, fb, n * 128 + 64, r);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kBChunks; ++j)
+                tma_load_2d(sb + j * 8192, &tmQ0, fb, n * BN + j * 64, r);
+            }
+            ++fills;
+            if (++stage == WSTAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      const long long first = fills > WSTAGES ? fills - WSTAGES : 0;
+      for (long long f = first; f < fills; ++f)
+        mbar_wait(smem_u32(full + (f % WSTAGES)),
+                  static_cast<uint32_t>((f / WSTAGES) & 1), nullptr,
+                  p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------ tail clearing + MMA issuer ---
+    constexpr uint32_t idesc = make_idesc(BM, BN, true, true);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles;
+         tile += gridDim.x) {
+      const int g = group_of(tpre, p.G, tile);
+      bool w_ok = true;
+      if (lane == 0)
+        w_ok = mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag,
+                         p.status);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * kAccCols;
+      bool first = true;
+      for (int sg = 0; ok && sg < p.n_seg; ++sg) {
+        const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
+        for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
+             r += BK) {
+          const bool got = mbar_wait(smem_u32(full + stage), phase,
+                                     abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + stage * kWStage;
+          const int valid = min(BK, r1 - r);
+          if (valid < BK) {
+            // rows valid..63 of every 64-column box: one 8 KB box is 64
+            // rows of 128 B, so the cleared rows are contiguous (and the
+            // 128-byte swizzle only permutes 16-byte units inside a row)
+            const int per_box = (BK - valid) * 8;  // 16-byte units
+            uint4* base = reinterpret_cast<uint4*>(smem + stage * kWStage);
+            for (int i = lane; i < (kAChunks + kBChunks) * per_box;
+                 i += 32) {
+              const int box = i / per_box, u = i - box * per_box;
+              base[box * 512 + valid * 8 + u] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t sb = sa + kAChunks * 8192;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 2048, 8192, 1024);
+              const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
+              umma_bf16(d, ad, bd, idesc, (!first || kk != 0) ? 1u : 0u);
+            }
+            umma_commit(smem_u32(empty + stage));
+          }
+          __syncwarp();
+          first = false;
+          if (++stage == WSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(smem_u32(tfull + acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) {
+      umma_commit(smem_u32(done));
+      mbar_wait(smem_u32(done), 0, nullptr, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue ---------
+    const int q = warp & 3;
+    uint8_t* mybuf = stagebuf + q * 2 * kStageBuf;
+    int acc = 0, nsub = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const int g = group_of(tpre, p.G, tile);
+      const int local = tile - tpre[g];
+      const int m = local % p.m_tiles, n = local / p.m_tiles;
+      const int we = p.group_expert ? __ldg(p.group_expert + g) : g;
+      bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
+                          p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      const int orow = we * p.m_tiles * BM + m * BM + q * 32;
+#pragma unroll 1
+      for (int sub = 0; sub < BN / 32; ++sub, ++nsub) {
+        uint32_t r[32];
+        tmem_ld32(taddr + sub * 32, r);
+        uint8_t* buf = mybuf + (nsub & 1) * kStageBuf;
+        if (lane == 0) bulk_wait_read_1();
+        __syncwarp();
+        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          row[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1],
+                                           r[4 * j + 2], r[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const CUtensorMap* om = &tmO0;
+          int col = n * BN + sub * 32;
+          if (WMODE == 0) {
+            om = sub < 4 ? &tmO0 : &tmO1;
+            col = n * 128 + (sub & 3) * 32;
+          }
+          if (p.reduce)
+            tma_reduce_add_2d(om, smem_u32(buf), col, orow);
+          else
+            tma_store_2d(om, smem_u32(buf), col, orow);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(tempty + acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Zeroes dW[e] of every expert without rows in any segment (store mode:
+// no tile writes it).  Grid (G, blocks), 16-byte stores.
+__global__ void zero_empty_kernel(WParams p, float* a, float* b,
+                                  long long per_expert) {
+  const int g = blockIdx.x;
+  if (wgrad_rows(p, g) > 0) return;
+  const long long n4 = per_expert / 4;
+  float4* pa = reinterpret_cast<float4*>(a + g * per_expert);
+  float4* pb = b ? reinterpret_cast<float4*>(b + g * per_expert) : nullptr;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = blockIdx.y * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.y) * blockDim.x) {
+    pa[i] = z;
+    if (pb) pb[i] = z;
+  }
+}
+
 // ------------------------------------------------------------- host ------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                  void*, const cuuint64_t*, const cuuint64_t*,
@@ -981,18 +1454,22 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzle.
+// 2-D map over a row-major [outer, inner] matrix, 128-byte swizzle (bf16
+// operands, or fp32 for the weight-gradient output).
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, bool f32 = false) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * (f32 ? 4 : 2)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m,
+            f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1040,7 +1517,8 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0,
 
 template <int MODE, int BN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
-                       const CUtensorMap& b1, Params p, cudaStream_t s) {
+                       const CUtensorMap& b1, const CUtensorMap& a1, Params p,
+                       cudaStream_t s) {
   p.stall_after_fills = g_stall_after_fills.load();
   const size_t smem = smem_bytes<BN>(p.E);
   int dev = 0, sms = 0;
@@ -1052,7 +1530,32 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  gmm_tc_kernel<MODE, BN><<<sms, kThreads, smem, s>>>(a, b0, b1, p);
+  gmm_tc_kernel<MODE, BN><<<sms, kThreads, smem, s>>>(a, b0, b1, a1, p);
+  return cudaGetLastError();
+}
+
+size_t smem_bytes_wgrad(int G) {
+  return 1024 + WSTAGES * kWStage + 8 * kStageBuf + 8 * (2 * WSTAGES + 5) +
+         16 + 4 * (16 + G + 1) + 64;
+}
+
+template <int WMODE, int BN>
+cudaError_t launch_wgrad(const CUtensorMap& pm, const CUtensorMap& q0,
+                         const CUtensorMap& q1, const CUtensorMap& o0,
+                         const CUtensorMap& o1, const WParams& p,
+                         cudaStream_t s) {
+  const size_t smem = smem_bytes_wgrad(p.G);
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(wgrad_tc_kernel<WMODE, BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  wgrad_tc_kernel<WMODE, BN><<<sms, kThreads, smem, s>>>(pm, q0, q1, o0, o1,
+                                                          p);
   return cudaGetLastError();
 }
 
@@ -1083,7 +1586,7 @@ cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
   tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
   if (tc::use_pair(c, g)) return tc::launch_pair<0>(a1, bg, bu, p1, s);
-  return tc::launch_one<0, 256>(a1, bg, bu, p1, s);
+  return tc::launch_one<0, 256>(a1, bg, bu, a1, p1, s);
 }
 
 cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
@@ -1101,11 +1604,143 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
     tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
     if (tc::use_pair(c, g)) return tc::launch_pair<1>(a2, bd, bd, p2, s);
-    return tc::launch_one<1, 256>(a2, bd, bd, p2, s);
+    return tc::launch_one<1, 256>(a2, bd, bd, a2, p2, s);
   }
   tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 128,
                 static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
-  return tc::launch_one<1, 128>(a2, bd, bd, p2, s);
+  return tc::launch_one<1, 128>(a2, bd, bd, a2, p2, s);
+}
+
+// Forward GEMM1 that keeps g = x Wg and u = x Wu, then GEMM2.
+cudaError_t launch_gmm_saved_bf16(const moe_config_t& c, const Groups& g,
+                                  const void* x_sorted,
+                                  const int32_t* group_offsets,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, void* gbuf, void* ubuf,
+                                  void* h, void* y_sorted, int32_t* status,
+                                  cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap a1, bg, bu;
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  if (!tc::make_map(&a1, x_sorted, c.H, rows, 64, tc::BM) ||
+      !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, 64) ||
+      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, 64))
+    return cudaErrorInvalidValue;
+  tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
+                static_cast<__nv_bfloat16*>(h), c.F, status};
+  p1.out2 = static_cast<__nv_bfloat16*>(ubuf);
+  p1.out3 = static_cast<__nv_bfloat16*>(gbuf);
+  cudaError_t e = tc::launch_one<4, 256>(a1, bg, bu, a1, p1, s);
+  if (e != cudaSuccess) return e;
+  return launch_gmm2_bf16(c, g, h, group_offsets, w_down, y_sorted, status,
+                          s);
+}
+
+// Data gradients: dh = dy_sorted Wd^T with the SwiGLU backward in the
+// epilogue (dg, du), then dx_sorted = dg Wg^T + du Wu^T as one GEMM with
+// K = 2F.
+cudaError_t launch_gmm_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                  const int32_t* group_offsets,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, const void* gbuf,
+                                  const void* ubuf, const void* dy_sorted,
+                                  void* dg, void* du, void* dx_sorted,
+                                  int32_t* status, cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  const int bn2 = c.F % 256 == 0 ? 256 : 128;
+  const int bn3 = c.H % 256 == 0 ? 256 : 128;
+  CUtensorMap ad, bd, ag, au, bg, bu;
+  if (!tc::make_map(&ad, dy_sorted, c.H, rows, 64, tc::BM) ||
+      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, bn2) ||
+      !tc::make_map(&ag, dg, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&au, du, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, bn3) ||
+      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, bn3))
+    return cudaErrorInvalidValue;
+  tc::Params p2{group_offsets, g.map, g.n, c.H, c.F / bn2,
+                static_cast<__nv_bfloat16*>(dg), c.F, status};
+  p2.out2 = static_cast<__nv_bfloat16*>(du);
+  p2.aux_g = static_cast<const __nv_bfloat16*>(gbuf);
+  p2.aux_u = static_cast<const __nv_bfloat16*>(ubuf);
+  cudaError_t e = bn2 == 256
+                      ? tc::launch_one<2, 256>(ad, bd, bd, ad, p2, s)
+                      : tc::launch_one<2, 128>(ad, bd, bd, ad, p2, s);
+  if (e != cudaSuccess) return e;
+  tc::Params p3{group_offsets, g.map, g.n, 2 * c.F, c.H / bn3,
+                static_cast<__nv_bfloat16*>(dx_sorted), c.H, status};
+  p3.k_split = c.F / 64;
+  return bn3 == 256 ? tc::launch_one<3, 256>(ag, bg, bu, au, p3, s)
+                    : tc::launch_one<3, 128>(ag, bg, bu, au, p3, s);
+}
+
+// Weight gradients over row segments (each {group offsets, first row}),
+// all inside buffers of `rows_total` rows.  accumulate = 0 overwrites every
+// expert's dW (experts without rows get zeros); 1 adds into dW.
+cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
+                              const WgradSegment* seg, int n_seg,
+                              int64_t rows_total, const void* x_sorted,
+                              const void* dg, const void* du, const void* h,
+                              const void* dy_sorted, float* dw_gate,
+                              float* dw_up, float* dw_down, int accumulate,
+                              int32_t* status, cudaStream_t s) {
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  const uint64_t rows = static_cast<uint64_t>(std::max<int64_t>(rows_total, 1));
+  const long long per_expert = static_cast<long long>(c.H) * c.F;
+  const bool mapped = g.map != nullptr;
+  cudaError_t e = cudaSuccess;
+  if (!accumulate && mapped) {  // duplicates reduce into one expert
+    const size_t bytes = static_cast<size_t>(E) * per_expert * sizeof(float);
+    if ((e = cudaMemsetAsync(dw_gate, 0, bytes, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(dw_up, 0, bytes, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(dw_down, 0, bytes, s)) != cudaSuccess)
+      return e;
+  }
+  const int bnd = c.H % 256 == 0 ? 256 : 128;
+  CUtensorMap px, qg, qu, og, ou, ph, qd, od;
+  if (!tc::make_map(&px, x_sorted, c.H, rows, 64, 64) ||
+      !tc::make_map(&qg, dg, c.F, rows, 64, 64) ||
+      !tc::make_map(&qu, du, c.F, rows, 64, 64) ||
+      !tc::make_map(&og, dw_gate, c.F, E * c.H, 32, 32, true) ||
+      !tc::make_map(&ou, dw_up, c.F, E * c.H, 32, 32, true) ||
+      !tc::make_map(&ph, h, c.F, rows, 64, 64) ||
+      !tc::make_map(&qd, dy_sorted, c.H, rows, 64, 64) ||
+      !tc::make_map(&od, dw_down, c.H, E * c.F, 32, 32, true))
+    return cudaErrorInvalidValue;
+  for (int s0 = 0; s0 < std::max(n_seg, 1); s0 += tc::kMaxSeg) {
+    tc::WParams p{};
+    p.n_seg = std::min(tc::kMaxSeg, n_seg - s0);
+    for (int i = 0; i < p.n_seg; ++i) {
+      p.seg_off[i] = seg[s0 + i].group_offsets;
+      p.seg_base[i] = seg[s0 + i].first_row;
+    }
+    p.group_expert = g.map;
+    p.G = g.n;
+    p.reduce = (accumulate || mapped || s0 > 0) ? 1 : 0;
+    p.status = status;
+    if (!p.reduce) {
+      // experts without rows: no tile writes their dW
+      const dim3 grid(static_cast<unsigned>(g.n), 16);
+      tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_gate, dw_up,
+                                                 per_expert);
+      tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_down, nullptr,
+                                                 per_expert);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (p.n_seg == 0) break;
+    p.m_tiles = c.H / tc::BM;
+    p.n_tiles = c.F / 128;
+    e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
+    if (e != cudaSuccess) return e;
+    p.m_tiles = c.F / tc::BM;
+    p.n_tiles = c.H / bnd;
+    e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
+                   : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace moe

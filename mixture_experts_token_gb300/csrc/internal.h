@@ -141,6 +141,61 @@ bool ok_ptr(const void* p, bool need16);
 bool gmm_shape_ok(const moe_config_t& c);
 bool weights_ok(const void* wg, const void* wu, const void* wd);
 
+// ---------------------------------------------------------- backward ---
+// Rows of one weight-gradient segment: groups at group_offsets (relative),
+// shifted by first_row inside the activation buffers.
+struct WgradSegment {
+  const int32_t* group_offsets;  // [groups + 1]
+  int first_row;
+};
+cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy,
+                                    const void* y_sorted,
+                                    const int32_t* row_of,
+                                    const float* topk_w, void* dy_sorted,
+                                    float* dtopk_w, cudaStream_t s);
+cudaError_t launch_route_backward(const moe_config_t& c, const float* logits,
+                                  const int32_t* topk_idx,
+                                  const float* dtopk_w, float* dlogits,
+                                  cudaStream_t s);
+// fp32 (CUDA cores): GEMM1 keeping g, u, h; and the whole FFN backward
+cudaError_t launch_gmm_saved_f32(const moe_config_t& c, const Groups& g,
+                                 const void* xs, const int32_t* off,
+                                 const void* wg, const void* wu, void* gbuf,
+                                 void* ubuf, void* h, cudaStream_t s);
+cudaError_t launch_gmm_backward_f32(const moe_config_t& c, const Groups& g,
+                                    const void* xs, const int32_t* off,
+                                    const void* wg, const void* wu,
+                                    const void* wd, const void* gbuf,
+                                    const void* ubuf, const void* h,
+                                    const void* dys, void* dxs, float* dwg,
+                                    float* dwu, float* dwd, int accumulate,
+                                    void* dg, void* du, cudaStream_t s);
+// bf16 (tensor cores)
+cudaError_t launch_gmm_saved_bf16(const moe_config_t& c, const Groups& g,
+                                  const void* x_sorted,
+                                  const int32_t* group_offsets,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, void* gbuf, void* ubuf,
+                                  void* h, void* y_sorted, int32_t* status,
+                                  cudaStream_t s);
+cudaError_t launch_gmm_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                  const int32_t* group_offsets,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, const void* gbuf,
+                                  const void* ubuf, const void* dy_sorted,
+                                  void* dg, void* du, void* dx_sorted,
+                                  int32_t* status, cudaStream_t s);
+cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
+                              const WgradSegment* seg, int n_seg,
+                              int64_t rows_total, const void* x_sorted,
+                              const void* dg, const void* du, const void* h,
+                              const void* dy_sorted, float* dw_gate,
+                              float* dw_up, float* dw_down, int accumulate,
+                              int32_t* status, cudaStream_t s);
+
+size_t gmm_backward_bytes(const moe_config_t& c);
+size_t layer_backward_bytes(const moe_config_t& c);
+
 // Tests of the GEMM's bounded waits: stop the TMA producer after `fills`
 // stage fills (-1: normal operation).
 void set_gemm_stall_for_tests(long long fills);

@@ -1,0 +1,362 @@
+// C ABI entry points of the backward pass and the layer-level driver.
+//
+// "Support moe_dropless_fallback=layer on the ragged all-to-all MoE path"
+// (MaxText pull request 5920): section Tests asks that with the layer
+// fallback both the outputs and the gradients match the dropless model;
+// section How says the fallback's backward recomputes each chunk's forward
+// (the chunk loop is rematerialised) and accumulates the expert-weight
+// gradients across chunks.
+//
+// moe_layer_backward follows that plan pass by pass: route once, then for
+// each pass (one capped or uncapped pass, or the fallback's chunks)
+// permute -> forward GEMMs keeping g, u, h -> combine backward -> data
+// gradients -> permute backward.  The weight gradients of all passes are
+// summed in one launch at the end: each pass leaves its rows in a disjoint
+// row range of the activation buffers, and one tile of the weight-gradient
+// kernel accumulates an expert's rows from every range in tensor memory, so
+// dW is written once instead of read and rewritten per chunk.
+#include <algorithm>
+#include <vector>
+
+#include "internal.h"
+
+namespace moe {
+
+cudaError_t launch_gmm2_f32(const moe_config_t& c, const Groups& g,
+                            const void* h, const int32_t* group_offsets,
+                            const void* w_down, void* y_sorted,
+                            cudaStream_t s);
+
+namespace {
+
+struct BwdBufs {
+  LayerBufs f;           // routing, permute and forward buffers for T
+  void *g, *u, *dg, *du;  // [T*k, F]
+  void *dys, *dxs;        // [T*k, H]
+  float* dtw;             // [T, k]
+  int32_t* seg_off;       // [n_seg, E + 1] group offsets of every pass
+};
+
+int max_passes(const moe_config_t& c, moe_mode_t mode) {
+  if (mode != MOE_MODE_FALLBACK_LAYER || c.T == 0) return 1;
+  const int ct = chunk_tokens(c);
+  return std::max(1, (c.T + ct - 1) / ct);
+}
+
+BwdBufs carve_bwd(void* base, const moe_config_t& c, int n_seg,
+                  size_t* bytes) {
+  BwdBufs b;
+  size_t fb = 0;
+  b.f = carve_layer(base, c, c.T, &fb);
+  Carve cv(base ? static_cast<char*>(base) + fb : nullptr);
+  const size_t rows = static_cast<size_t>(c.T) * c.k;
+  const size_t eb = elem_bytes(c.dtype);
+  b.g = cv.take<char>(rows * c.F * eb);
+  b.u = cv.take<char>(rows * c.F * eb);
+  b.dg = cv.take<char>(rows * c.F * eb);
+  b.du = cv.take<char>(rows * c.F * eb);
+  b.dys = cv.take<char>(rows * c.H * eb);
+  b.dxs = cv.take<char>(rows * c.H * eb);
+  b.dtw = cv.take<float>(rows);
+  b.seg_off = cv.take<int32_t>(static_cast<size_t>(n_seg) * (c.E + 1));
+  if (bytes) *bytes = fb + align_up(cv.off, 256);
+  return b;
+}
+
+void* rows_at(const void* p, size_t row, size_t row_bytes) {
+  return const_cast<char*>(static_cast<const char*>(p)) + row * row_bytes;
+}
+
+// Backward of one pass over tokens [t0, t0 + tc) with capacity cap (-1:
+// uncapped).  Its rows occupy [t0*k, (t0+tc)*k) of the row buffers and its
+// group offsets row `seg` of the segment table.  fp32 layers also add their
+// weight gradients here (accumulate after the first pass).
+cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
+                     int seg, const void* x, const void* wg, const void* wu,
+                     const void* wd, const void* dy, void* dx, float* dwg,
+                     float* dwu, float* dwd, const BwdBufs& b,
+                     int32_t* status, cudaStream_t s) {
+  moe_config_t sc = c;
+  sc.T = tc;
+  const size_t eb = elem_bytes(c.dtype);
+  const size_t hb = c.H * eb, fb = c.F * eb;
+  const size_t base = static_cast<size_t>(t0) * c.k;
+  const Groups ids = identity_groups(sc);
+  const void* xc = rows_at(x, t0, hb);
+  const int32_t* idx = b.f.topk_idx + base;
+  const float* w = b.f.topk_w + base;
+  int32_t* row_of = b.f.row_of + base;
+  int32_t* goff = b.seg_off + static_cast<size_t>(seg) * (c.E + 1);
+  void* xs = rows_at(b.f.x_sorted, base, hb);
+  void* h = rows_at(b.f.h, base, fb);
+  void* ys = rows_at(b.f.y_sorted, base, hb);
+  void* gg = rows_at(b.g, base, fb);
+  void* uu = rows_at(b.u, base, fb);
+  void* dg = rows_at(b.dg, base, fb);
+  void* du = rows_at(b.du, base, fb);
+  void* dys = rows_at(b.dys, base, hb);
+  void* dxs = rows_at(b.dxs, base, hb);
+  cudaError_t e = launch_permute(
+      sc, xc, idx, cap, xs, row_of, b.f.sorted_token + base, goff,
+      b.f.uniq_offsets, b.f.uniq_tokens, b.f.expand_idx + base, b.f.n_dropped,
+      b.f.pws, status, s);
+  if (e != cudaSuccess) return e;
+  if (c.dtype == MOE_BF16) {
+    e = launch_gmm_saved_bf16(sc, ids, xs, goff, wg, wu, wd, gg, uu, h, ys,
+                              status, s);
+  } else {
+    e = launch_gmm_saved_f32(sc, ids, xs, goff, wg, wu, gg, uu, h, s);
+    if (e == cudaSuccess) e = launch_gmm2_f32(sc, ids, h, goff, wd, ys, s);
+  }
+  if (e != cudaSuccess) return e;
+  e = launch_combine_backward(sc, rows_at(dy, t0, hb), ys, row_of, w, dys,
+                              b.dtw + base, s);
+  if (e != cudaSuccess) return e;
+  if (c.dtype == MOE_BF16)
+    e = launch_gmm_dgrad_bf16(sc, ids, goff, wg, wu, wd, gg, uu, dys, dg, du,
+                              dxs, status, s);
+  else
+    e = launch_gmm_backward_f32(sc, ids, xs, goff, wg, wu, wd, gg, uu, h, dys,
+                                dxs, dwg, dwu, dwd, seg > 0 ? 1 : 0, dg, du,
+                                s);
+  if (e != cudaSuccess) return e;
+  return launch_combine(sc, dxs, row_of, nullptr, rows_at(dx, t0, hb), s);
+}
+
+}  // namespace
+
+size_t gmm_backward_bytes(const moe_config_t& c) {
+  Carve cv(nullptr);
+  const size_t rows = static_cast<size_t>(c.T) * c.k;
+  cv.take<char>(rows * c.F * elem_bytes(c.dtype));
+  cv.take<char>(rows * c.F * elem_bytes(c.dtype));
+  return align_up(cv.off, 256);
+}
+
+size_t layer_backward_bytes(const moe_config_t& c) {
+  size_t n = 0;
+  carve_bwd(nullptr, c, max_passes(c, MOE_MODE_FALLBACK_LAYER), &n);
+  return n;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+moe_status_t cuda_st(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  cudaGetLastError();
+  return MOE_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_combine_backward(const moe_config_t* cfg, const void* dy,
+                                  const void* y_sorted, const int32_t* row_of,
+                                  const float* topk_w, void* dy_sorted,
+                                  float* dtopk_w, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(dy, true) || !ok_ptr(y_sorted, true) || !ok_ptr(row_of, false) ||
+      !ok_ptr(topk_w, false) || !ok_ptr(dy_sorted, true) ||
+      !ok_ptr(dtopk_w, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_combine_backward(*cfg, dy, y_sorted, row_of, topk_w,
+                                         dy_sorted, dtopk_w, stream));
+}
+
+moe_status_t moe_route_backward(const moe_config_t* cfg, const float* logits,
+                                const int32_t* topk_idx, const float* dtopk_w,
+                                float* dlogits, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(logits, false) || !ok_ptr(topk_idx, false) ||
+      !ok_ptr(dtopk_w, false) || !ok_ptr(dlogits, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_route_backward(*cfg, logits, topk_idx, dtopk_w,
+                                       dlogits, stream));
+}
+
+moe_status_t moe_permute_backward(const moe_config_t* cfg,
+                                  const void* dx_sorted,
+                                  const int32_t* row_of, void* dx,
+                                  moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(dx_sorted, true) || !ok_ptr(row_of, false) || !ok_ptr(dx, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_combine(*cfg, dx_sorted, row_of, nullptr, dx, stream));
+}
+
+moe_status_t moe_gmm_swiglu_saved(const moe_config_t* cfg,
+                                  const void* x_sorted,
+                                  const int32_t* group_offsets,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, void* g, void* u,
+                                  void* h, void* y_sorted,
+                                  int32_t* status_word, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(g, true) ||
+      !ok_ptr(u, true) || !ok_ptr(h, true) || !ok_ptr(y_sorted, true))
+    return MOE_ERR_INVALID_ARG;
+  const Groups ids = identity_groups(*cfg);
+  if (cfg->dtype == MOE_BF16)
+    return cuda_st(launch_gmm_saved_bf16(*cfg, ids, x_sorted, group_offsets,
+                                         w_gate, w_up, w_down, g, u, h,
+                                         y_sorted, status_word, stream));
+  cudaError_t e = launch_gmm_saved_f32(*cfg, ids, x_sorted, group_offsets,
+                                       w_gate, w_up, g, u, h, stream);
+  if (e == cudaSuccess)
+    e = launch_gmm2_f32(*cfg, ids, h, group_offsets, w_down, y_sorted, stream);
+  return cuda_st(e);
+}
+
+moe_status_t moe_gmm_swiglu_backward(
+    const moe_config_t* cfg, const void* x_sorted,
+    const int32_t* group_offsets, const void* w_gate, const void* w_up,
+    const void* w_down, const void* g, const void* u, const void* h,
+    const void* dy_sorted, void* dx_sorted, float* dw_gate, float* dw_up,
+    float* dw_down, int32_t accumulate, int32_t* status_word, void* workspace,
+    size_t workspace_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1 || (accumulate != 0 && accumulate != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(dw_gate, true) ||
+      !ok_ptr(dw_up, true) || !ok_ptr(dw_down, true))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 &&
+      (!ok_ptr(x_sorted, true) || !weights_ok(w_gate, w_up, w_down) ||
+       !ok_ptr(g, true) || !ok_ptr(u, true) || !ok_ptr(h, true) ||
+       !ok_ptr(dy_sorted, true) || !ok_ptr(dx_sorted, true)))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !ok_ptr(workspace, true) ||
+      workspace_bytes < gmm_backward_bytes(*cfg))
+    return MOE_ERR_WORKSPACE;
+  Carve cv(workspace);
+  const size_t rows = static_cast<size_t>(cfg->T) * cfg->k;
+  void* dg = cv.take<char>(rows * cfg->F * elem_bytes(cfg->dtype));
+  void* du = cv.take<char>(rows * cfg->F * elem_bytes(cfg->dtype));
+  const Groups ids = identity_groups(*cfg);
+  if (cfg->dtype == MOE_F32)
+    return cuda_st(launch_gmm_backward_f32(
+        *cfg, ids, x_sorted, group_offsets, w_gate, w_up, w_down, g, u, h,
+        dy_sorted, dx_sorted, dw_gate, dw_up, dw_down, accumulate, dg, du,
+        stream));
+  cudaError_t e = launch_gmm_dgrad_bf16(*cfg, ids, group_offsets, w_gate,
+                                        w_up, w_down, g, u, dy_sorted, dg, du,
+                                        dx_sorted, status_word, stream);
+  if (e != cudaSuccess) return cuda_st(e);
+  const WgradSegment seg{group_offsets, 0};
+  return cuda_st(launch_wgrad_bf16(*cfg, ids, &seg, cfg->T > 0 ? 1 : 0,
+                                   static_cast<int64_t>(rows), x_sorted, dg,
+                                   du, h, dy_sorted, dw_gate, dw_up, dw_down,
+                                   accumulate, status_word, stream));
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
+                                const float* logits, const void* w_gate,
+                                const void* w_up, const void* w_down,
+                                const void* dy, void* dx, float* dlogits,
+                                float* dw_gate, float* dw_up, float* dw_down,
+                                moe_mode_t mode, moe_layer_info_t* info,
+                                int32_t* status_word, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (mode != MOE_MODE_FALLBACK_LAYER && mode != MOE_MODE_CAPPED &&
+      mode != MOE_MODE_DROPLESS)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->redundant_slots != 0) return MOE_ERR_UNSUPPORTED;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (!weights_ok(w_gate, w_up, w_down) || !ok_ptr(dw_gate, true) ||
+      !ok_ptr(dw_up, true) || !ok_ptr(dw_down, true))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(x, true) || !ok_ptr(logits, false) ||
+                     !ok_ptr(dy, true) || !ok_ptr(dx, true) ||
+                     !ok_ptr(dlogits, false)))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !ok_ptr(workspace, true) ||
+      workspace_bytes < layer_backward_bytes(*cfg))
+    return MOE_ERR_WORKSPACE;
+  const int64_t cap = capacity_rows(*cfg);
+  if (info) {
+    info->overflow = -1;
+    info->n_chunks = cfg->T > 0 ? 1 : 0;
+    info->capacity = mode == MOE_MODE_DROPLESS ? -1 : cap;
+  }
+  const size_t wbytes =
+      static_cast<size_t>(cfg->E) * cfg->H * cfg->F * sizeof(float);
+  if (cfg->T == 0) {  // no rows: every weight gradient is zero
+    cudaError_t e = cudaMemsetAsync(dw_gate, 0, wbytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw_up, 0, wbytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw_down, 0, wbytes, stream);
+    return cuda_st(e);
+  }
+  const BwdBufs b = carve_bwd(workspace, *cfg,
+                              max_passes(*cfg, MOE_MODE_FALLBACK_LAYER),
+                              nullptr);
+  cudaError_t e = launch_route(*cfg, logits, b.f.topk_idx, b.f.topk_w,
+                               status_word, stream);
+  if (e != cudaSuccess) return cuda_st(e);
+  // the passes: (t0, tokens, capacity)
+  struct Pass {
+    int t0, tc;
+    int64_t cap;
+  };
+  std::vector<Pass> passes;
+  if (mode == MOE_MODE_DROPLESS) {
+    passes.push_back({0, cfg->T, -1});
+  } else if (mode == MOE_MODE_CAPPED) {
+    passes.push_back({0, cfg->T, cap});
+  } else {
+    e = launch_check(*cfg, b.f.topk_idx, b.f.counts, b.f.offsets, b.f.shard,
+                     b.f.flag, b.f.req, b.f.cap, stream);
+    if (e != cudaSuccess) return cuda_st(e);
+    int32_t flag = 0;
+    e = cudaMemcpyAsync(&flag, b.f.flag, sizeof(flag), cudaMemcpyDeviceToHost,
+                        stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_st(e);
+    if (info) info->overflow = flag;
+    if (!flag) {
+      passes.push_back({0, cfg->T, cap});
+    } else {
+      const int ct = chunk_tokens(*cfg);
+      for (int t0 = 0; t0 < cfg->T; t0 += ct)
+        passes.push_back({t0, std::min(ct, cfg->T - t0), -1});
+      if (info) info->n_chunks = static_cast<int32_t>(passes.size());
+    }
+  }
+  std::vector<WgradSegment> segs;
+  for (size_t i = 0; i < passes.size(); ++i) {
+    const Pass& p = passes[i];
+    e = bwd_pass(*cfg, p.t0, p.tc, p.cap, static_cast<int>(i), x, w_gate,
+                 w_up, w_down, dy, dx, dw_gate, dw_up, dw_down, b,
+                 status_word, stream);
+    if (e != cudaSuccess) return cuda_st(e);
+    segs.push_back({b.seg_off + i * (cfg->E + 1), p.t0 * cfg->k});
+  }
+  e = launch_route_backward(*cfg, logits, b.f.topk_idx, b.dtw, dlogits,
+                            stream);
+  if (e != cudaSuccess) return cuda_st(e);
+  if (cfg->dtype == MOE_F32) return MOE_OK;  // added in the passes
+  return cuda_st(launch_wgrad_bf16(
+      *cfg, identity_groups(*cfg), segs.data(), static_cast<int>(segs.size()),
+      static_cast<int64_t>(cfg->T) * cfg->k, b.f.x_sorted, b.dg, b.du, b.f.h,
+      b.dys, dw_gate, dw_up, dw_down, 0, status_word, stream));
+}
+
+}  // extern "C"

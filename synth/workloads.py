@@ -90,7 +90,8 @@ def sweep_workload(T: int, routing: str) -> Workload:
 
 def seeds_for(seed: int, n: int = 8):
     """Independent child seeds (ints) for the tensors of one workload:
-    0 x, 1 router weight, 2 logit noise, 3 w_gate, 4 w_up, 5 w_down."""
+    0 x, 1 router weight, 2 logit noise, 3 w_gate, 4 w_up, 5 w_down,
+    6 the output gradient dy of the backward pass."""
     ss = np.random.SeedSequence(seed).spawn(n)
     return [int(s.generate_state(1, dtype=np.uint64)[0] & 0x7FFFFFFFFFFFFFFF)
             for s in ss]
@@ -155,3 +156,12 @@ def make_weights(wl: Workload, device="cpu"):
             w[e].copy_(blk.mul_(wl.w_std))
         out.append(w)
     return tuple(out)
+
+
+def make_dy(wl: Workload, device="cpu", T: Optional[int] = None) -> torch.Tensor:
+    """Gradient of the loss with respect to the layer output, dy [T, H]
+    ~ N(0, 1) in the workload dtype (the backward pass's input)."""
+    T = wl.T if T is None else T
+    g = _torch_gen(device, seeds_for(wl.seed)[6])
+    dy = torch.randn(T, wl.H, generator=g, device=device, dtype=torch.float32)
+    return dy.to(wl.torch_dtype)

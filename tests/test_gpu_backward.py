@@ -1,0 +1,265 @@
+"""GPU parity of the backward pass against the float64 oracle.
+
+The layer backward (moe_layer_backward) in every mode, and the backward
+entry points one by one (combine, route and permute transposes, the saved
+forward GEMMs and the FFN backward).  Gradient buffers are pre-filled with
+NaN so that a gradient the library forgot to write shows up.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_token_gb300 as moe
+from oracle import moe_ref as ref
+from synth import WORKLOADS, make_logits, make_weights, make_x
+from synth.workloads import make_dy
+from tests.gpu_util import TOL, cfg_from, f64, np_
+
+pytestmark = pytest.mark.gpu
+
+BWD = [
+    WORKLOADS["tiny"],
+    # ragged T, F % 256 != 0 (128-wide dgrad tiles), Zipf routing
+    WORKLOADS["small"].with_(name="bwd_a", T=1000, H=512, E=8, k=2, F=384,
+                             S=2, zipf_s=1.0),
+    # H % 256 != 0 (128-wide tiles of dx_sorted and dWd), k=4, renorm
+    WORKLOADS["small"].with_(name="bwd_b", T=777, H=384, E=16, k=4, F=256,
+                             S=4, renorm=True, routing="uniform"),
+]
+
+
+def oracle_cfg(wl, **over):
+    d = dict(T=wl.T, H=wl.H, E=wl.E, k=wl.k, F=wl.F, S=wl.S,
+             ragged_buffer_factor=wl.factor, n_chunks=wl.n_chunks,
+             renorm=wl.renorm)
+    d.update(over)
+    return ref.MoEConfig(**d)
+
+
+def oracle_backward(mc, mode, x, L, W, dy):
+    """The oracle's gradients of the mode moe_layer_backward runs."""
+    if mode == moe.MOE_MODE_DROPLESS:
+        return ref.layer_backward_dropless(mc, x, L, *W, dy), None
+    if mode == moe.MOE_MODE_CAPPED:
+        return ref.layer_backward_capped(mc, x, L, *W, dy), None
+    idx, _, _ = ref.route(L, mc.k, mc.renorm)
+    shard = ref.shard_counts(ref.expert_counts(idx, mc.E), mc.S)
+    C = ref.capacity(mc.T, mc.k, mc.S, mc.ragged_buffer_factor)
+    over = ref.overflow_flag(shard, C)
+    if over:
+        return ref.layer_backward_chunked(mc, x, L, *W, dy), True
+    return ref.layer_backward_capped(mc, x, L, *W, dy), False
+
+
+def setup(wl):
+    x = make_x(wl, "cuda")
+    L = make_logits(wl, x if wl.routing == "router" else None)
+    W = make_weights(wl, "cuda")
+    dy = make_dy(wl, "cuda")
+    return x, L, W, dy
+
+
+def gpu_layer_backward(cfg, x, L, W, dy, mode):
+    T, H, E, F = cfg.T, cfg.H, cfg.E, cfg.F
+    dev = "cuda"
+    nan = float("nan")
+    out = {
+        "dx": torch.full((T, H), nan, dtype=x.dtype, device=dev),
+        "dlogits": torch.full((T, E), nan, dtype=torch.float32, device=dev),
+        "dwg": torch.full((E, H, F), nan, dtype=torch.float32, device=dev),
+        "dwu": torch.full((E, H, F), nan, dtype=torch.float32, device=dev),
+        "dwd": torch.full((E, F, H), nan, dtype=torch.float32, device=dev),
+    }
+    ws = moe.layer_workspace(cfg, moe.MOE_WS_LAYER_BACKWARD)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    Ld = torch.from_numpy(np.ascontiguousarray(L)).to(dev)
+    info = moe.moe_layer_backward(cfg, x, Ld, *W, dy, out["dx"],
+                                  out["dlogits"], out["dwg"], out["dwu"],
+                                  out["dwd"], mode, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, info
+
+
+def compare(out, g, tol):
+    pairs = [("dx", g.dx), ("dlogits", g.dlogits), ("dwg", g.dwg),
+             ("dwu", g.dwu), ("dwd", g.dwd)]
+    for name, want in pairs:
+        got = f64(out[name])
+        assert np.isfinite(got).all(), f"{name}: unwritten or non-finite"
+        err = ref.normwise_error(got, want)
+        assert err <= tol, f"{name}: normwise error {err:.3g} > {tol}"
+
+
+MODES = [(moe.MOE_MODE_DROPLESS, 2.0), (moe.MOE_MODE_CAPPED, 1.0),
+         (moe.MOE_MODE_FALLBACK_LAYER, 1.0),
+         (moe.MOE_MODE_FALLBACK_LAYER, 50.0)]
+
+
+@pytest.mark.parametrize("mode,factor", MODES,
+                         ids=["dropless", "capped_f1", "fallback_f1",
+                              "fallback_f50"])
+@pytest.mark.parametrize("wl", BWD, ids=lambda w: w.name)
+def test_layer_backward_matches_oracle(wl, mode, factor):
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=factor)
+    out, info = gpu_layer_backward(cfg, x, L, W, dy, mode)
+    mc = oracle_cfg(wl, ragged_buffer_factor=factor)
+    g, over = oracle_backward(mc, mode, f64(x), L, [f64(w) for w in W],
+                              f64(dy))
+    if over is not None:
+        assert info["overflow"] == int(over)
+        if over:
+            assert info["n_chunks"] == moe.moe_num_chunks(cfg)
+    compare(out, g, TOL[wl.dtype])
+
+
+def test_fallback_backward_many_chunks():
+    """More chunks than one weight-gradient launch takes (segments are
+    handled 16 at a time, the later batches adding into dW)."""
+    wl = BWD[1].with_(name="bwd_chunks", T=700, n_chunks=20)
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=1.0)
+    out, info = gpu_layer_backward(cfg, x, L, W, dy,
+                                   moe.MOE_MODE_FALLBACK_LAYER)
+    assert info["overflow"] == 1 and info["n_chunks"] == 20
+    mc = oracle_cfg(wl, ragged_buffer_factor=1.0)
+    g = ref.layer_backward_dropless(mc, f64(x), L, *[f64(w) for w in W],
+                                    f64(dy))
+    compare(out, g, TOL["bf16"])
+
+
+def test_unused_expert_gets_zero_weight_gradient():
+    """An expert no token picks: its dW is exactly zero (written, not left
+    as it was)."""
+    wl = BWD[1].with_(name="bwd_unused", T=300)
+    x, L, W, dy = setup(wl)
+    L = L.copy()
+    L[:, 5] = -1.0e30
+    cfg = cfg_from(wl)
+    out, _ = gpu_layer_backward(cfg, x, L, W, dy, moe.MOE_MODE_DROPLESS)
+    for name in ("dwg", "dwu", "dwd"):
+        assert torch.count_nonzero(out[name][5]).item() == 0
+    g = ref.layer_backward_dropless(oracle_cfg(wl), f64(x), L,
+                                    *[f64(w) for w in W], f64(dy))
+    compare(out, g, TOL["bf16"])
+
+
+def test_zero_tokens_zero_weight_gradients():
+    wl = BWD[1].with_(name="bwd_t0", T=0)
+    cfg = cfg_from(wl)
+    E, H, F = wl.E, wl.H, wl.F
+    dw = [torch.full(s, float("nan"), device="cuda")
+          for s in ((E, H, F), (E, H, F), (E, F, H))]
+    W = make_weights(wl, "cuda")
+    ws = moe.layer_workspace(cfg, moe.MOE_WS_LAYER_BACKWARD)
+    moe.moe_layer_backward(cfg, None, None, *W, None, None, None, *dw,
+                           moe.MOE_MODE_FALLBACK_LAYER, ws)
+    torch.cuda.synchronize()
+    for t in dw:
+        assert torch.count_nonzero(t).item() == 0
+
+
+@pytest.mark.parametrize("wl", BWD, ids=lambda w: w.name)
+def test_backward_entry_points_stepwise(wl):
+    """route -> permute -> saved GEMMs -> combine backward -> FFN backward
+    -> permute backward -> route backward, each through its own entry
+    point; then the FFN backward again with accumulate = 1 doubles dW."""
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl)
+    T, H, E, k, F = wl.T, wl.H, wl.E, wl.k, wl.F
+    R = T * k
+    dt = x.dtype
+    b = moe.alloc_step_buffers(cfg)
+    Ld = torch.from_numpy(L).cuda()
+    moe.moe_route(cfg, Ld, b["topk_idx"], b["topk_w"], b["status"])
+    moe.moe_permute(cfg, x, b["topk_idx"], 0, b["x_sorted"], b["row_of"],
+                    b["sorted_token"], b["group_offsets"], b["uniq_offsets"],
+                    b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
+                    b["permute_ws"])
+    g = torch.empty((R, F), dtype=dt, device="cuda")
+    u = torch.empty_like(g)
+    moe.moe_gmm_swiglu_saved(cfg, b["x_sorted"], b["group_offsets"], *W, g,
+                             u, b["h"], b["y_sorted"], b["status"])
+    dys = torch.empty((R, H), dtype=dt, device="cuda")
+    dtw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_combine_backward(cfg, dy, b["y_sorted"], b["row_of"],
+                             b["topk_w"], dys, dtw)
+    dxs = torch.empty((R, H), dtype=dt, device="cuda")
+    dw = [torch.full(s, float("nan"), device="cuda")
+          for s in ((E, H, F), (E, H, F), (E, F, H))]
+    ws = moe.layer_workspace(cfg, moe.MOE_WS_GMM_BACKWARD)
+    moe.moe_gmm_swiglu_backward(cfg, b["x_sorted"], b["group_offsets"], *W,
+                                g, u, b["h"], dys, dxs, *dw, 0, ws,
+                                b["status"])
+    dx = torch.empty((T, H), dtype=dt, device="cuda")
+    moe.moe_permute_backward(cfg, dxs, b["row_of"], dx)
+    dl = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_route_backward(cfg, Ld, b["topk_idx"], dtw, dl)
+    torch.cuda.synchronize()
+    assert int(b["status"].item()) == 0
+    want = ref.layer_backward_dropless(oracle_cfg(wl), f64(x), L,
+                                       *[f64(w) for w in W], f64(dy))
+    tol = TOL[wl.dtype]
+    assert ref.normwise_error(f64(dtw), want.dtopk_w) <= tol
+    compare({"dx": dx, "dlogits": dl, "dwg": dw[0], "dwu": dw[1],
+             "dwd": dw[2]}, want, tol)
+    # saved g, u against the oracle's x_sorted W products (g = x Wg)
+    xs = f64(b["x_sorted"])
+    off = np_(b["group_offsets"]).astype(np.int64)
+    wg = f64(W[0])
+    gs = np.zeros((R, F))
+    for e in range(E):
+        gs[off[e]:off[e + 1]] = xs[off[e]:off[e + 1]] @ wg[e]
+    assert ref.normwise_error(f64(g), gs) <= tol
+    # accumulate: a second backward adds the same gradient again.  bf16
+    # adds the finished tile to dW (a + a: exact); fp32 continues its
+    # accumulation from the old value (rounding differs in the last bits).
+    first = [t.clone() for t in dw]
+    moe.moe_gmm_swiglu_backward(cfg, b["x_sorted"], b["group_offsets"], *W,
+                                g, u, b["h"], dys, dxs, *dw, 1, ws,
+                                b["status"])
+    torch.cuda.synchronize()
+    for a, b2 in zip(first, dw):
+        if wl.dtype == "bf16":
+            assert torch.equal(b2, a * 2)
+        else:
+            scale = a.abs().max().item()
+            assert torch.allclose(b2, a * 2, rtol=1e-5, atol=1e-6 * scale)
+
+
+def test_combine_backward_exact_small():
+    """dy_sorted rows are w * dy exactly rounded; dtopk_w is the fp32 dot
+    product within fp32 rounding; dropped rows get a zero weight gradient."""
+    wl = BWD[1].with_(name="cb", T=64)
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=0.5)
+    b = moe.alloc_step_buffers(cfg)
+    Ld = torch.from_numpy(L).cuda()
+    moe.moe_route(cfg, Ld, b["topk_idx"], b["topk_w"], b["status"])
+    moe.moe_permute(cfg, x, b["topk_idx"], 1, b["x_sorted"], b["row_of"],
+                    b["sorted_token"], b["group_offsets"], b["uniq_offsets"],
+                    b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
+                    b["permute_ws"])
+    R = wl.T * wl.k
+    ys = torch.randn((R, wl.H), device="cuda").to(x.dtype)
+    dys = torch.zeros((R, wl.H), dtype=x.dtype, device="cuda")
+    dtw = torch.full((wl.T, wl.k), float("nan"), device="cuda")
+    moe.moe_combine_backward(cfg, dy, ys, b["row_of"], b["topk_w"], dys, dtw)
+    torch.cuda.synchronize()
+    row_of = np_(b["row_of"]).astype(np.int64)
+    w = np_(b["topk_w"]).astype(np.float64)
+    dyh, ysh, dysh, dtwh = f64(dy), f64(ys), f64(dys), f64(dtw)
+    assert (row_of < 0).any()
+    for t in range(wl.T):
+        for j in range(wl.k):
+            r = row_of[t, j]
+            if r < 0:
+                assert dtwh[t, j] == 0.0
+                continue
+            want = (w[t, j] * dyh[t]).astype(np.float32)
+            want = torch.from_numpy(want).to(torch.bfloat16).double().numpy()
+            assert np.array_equal(dysh[r], want)
+            dot = float(dyh[t] @ ysh[r])
+            assert abs(dtwh[t, j] - dot) <= 1e-5 * (np.abs(dyh[t]) @
+                                                     np.abs(ysh[r]) + 1e-30)
