@@ -18,7 +18,7 @@ Sources.  Three MaxText pull-request pages describe the method:
   as [PR4969 What].
 
 Where the pages leave a step open, the reading taken is stated at the step
-(marked READING) and listed in the design doc.  Every function is plain: Python
+(marked READING).  Every function is plain: Python
 loops where the order of things is the semantics, ``numpy.matmul`` for the
 dense products of the expert FFN, float64 throughout.
 
@@ -704,10 +704,12 @@ def route_backward(logits: np.ndarray, idx: np.ndarray, dw: np.ndarray,
     return dl
 
 
-def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
-                        dy, C: Optional[int]) -> Gradients:
-    """Backward of one pass (capacity C, None = uncapped) over in-memory
-    float64 weights [E,H,F], [E,H,F], [E,F,H]."""
+def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
+                          dy, C: Optional[int]):
+    """Backward of one pass (capacity C, None = uncapped) with the weights
+    read one expert at a time through an accessor.  Returns (Gradients with
+    dwg = dwu = dwd = None, {e: (dWg[e], dWu[e], dWd[e])} for the experts
+    that received rows); every other expert's gradient is zero."""
     x = np.asarray(x, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
     T, H = x.shape
@@ -715,10 +717,8 @@ def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
     perm = permute_indices(idx, cfg.E, cfg.S, C)
     xs = gather_rows(x, perm.sorted_token)
     R = len(perm.sorted_token)
-    F = w_gate.shape[2]
-    dwg = np.zeros_like(w_gate, dtype=np.float64)
-    dwu = np.zeros_like(w_up, dtype=np.float64)
-    dwd = np.zeros_like(w_down, dtype=np.float64)
+    F = cfg.F
+    dW = {}
     ys = np.zeros((R, H))
     hs = np.zeros((R, F))
     gs = np.zeros((R, F))
@@ -727,10 +727,11 @@ def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
         a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
         if a == b:
             continue
-        gs[a:b] = xs[a:b] @ w_gate[e]
-        us[a:b] = xs[a:b] @ w_up[e]
+        wg, wu, wd = weights(e)
+        gs[a:b] = xs[a:b] @ wg
+        us[a:b] = xs[a:b] @ wu
         hs[a:b] = silu(gs[a:b]) * us[a:b]
-        ys[a:b] = hs[a:b] @ w_down[e]
+        ys[a:b] = hs[a:b] @ wd
     dtw = np.zeros((T, cfg.k))
     dys = np.zeros((R, H))
     for t in range(T):
@@ -744,13 +745,12 @@ def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
         a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
         if a == b:
             continue
-        dwd[e] = hs[a:b].T @ dys[a:b]
-        dh = dys[a:b] @ w_down[e].T
+        wg, wu, wd = weights(e)
+        dh = dys[a:b] @ wd.T
         dg = dh * us[a:b] * silu_grad(gs[a:b])
         du = dh * silu(gs[a:b])
-        dwg[e] = xs[a:b].T @ dg
-        dwu[e] = xs[a:b].T @ du
-        dxs[a:b] = dg @ w_gate[e].T + du @ w_up[e].T
+        dW[e] = (xs[a:b].T @ dg, xs[a:b].T @ du, hs[a:b].T @ dys[a:b])
+        dxs[a:b] = dg @ wg.T + du @ wu.T
     dx = np.zeros((T, H))
     for t in range(T):
         for j in range(cfg.k):
@@ -758,7 +758,21 @@ def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
             if r >= 0:
                 dx[t] += dxs[r]
     dl = route_backward(logits, idx, dtw, cfg.renorm)
-    return Gradients(dx, dl, dwg, dwu, dwd, dtw)
+    return Gradients(dx, dl, None, None, None, dtw), dW
+
+
+def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
+                        dy, C: Optional[int]) -> Gradients:
+    """Backward of one pass (capacity C, None = uncapped) over in-memory
+    float64 weights [E,H,F], [E,H,F], [E,F,H]; dense weight gradients."""
+    g, dW = pass_backward_touched(cfg, x, logits,
+                                  dense_weights(w_gate, w_up, w_down), dy, C)
+    g.dwg = np.zeros(np.shape(w_gate), dtype=np.float64)
+    g.dwu = np.zeros(np.shape(w_up), dtype=np.float64)
+    g.dwd = np.zeros(np.shape(w_down), dtype=np.float64)
+    for e, (a, b, c) in dW.items():
+        g.dwg[e], g.dwu[e], g.dwd[e] = a, b, c
+    return g
 
 
 def layer_backward_dropless(cfg, x, logits, w_gate, w_up, w_down, dy):

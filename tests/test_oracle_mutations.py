@@ -85,8 +85,11 @@ MUTANTS = {
         "                dl[t, e] = p[e] * (dp[e] - dot)",
         "                dl[t, e] = p[e] * (dp[e] + dot)"),
     "dx_gate_only": (
-        "        dxs[a:b] = dg @ w_gate[e].T + du @ w_up[e].T",
-        "        dxs[a:b] = dg @ w_gate[e].T"),
+        "        dxs[a:b] = dg @ wg.T + du @ wu.T",
+        "        dxs[a:b] = dg @ wg.T"),
+    "dwd_uses_x": (
+        "hs[a:b].T @ dys[a:b])",
+        "xs[a:b, :hs.shape[1]].T @ dys[a:b])"),
     "chunked_dw_not_summed": (
         "        out.dwg += g.dwg",
         "        out.dwg = g.dwg"),
