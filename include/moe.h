@@ -433,7 +433,69 @@ moe_status_t moe_gmm_swiglu_saved(const moe_config_t *cfg,
                                   void *h, void *y_sorted,
                                   int32_t *status_word, moe_stream_t stream);
 
-/* Backward of the grouped SwiGLU FFN.  accumulate != 0 adds the weight
+/* The steps of the FFN backward one kernel each (the compositions above
+ * and below chain them).  Rows of group e use the weights of expert e;
+ * only the group_offsets[E] rows are read and written.
+ *
+ * GEMM1 + SwiGLU of the forward that also keeps g = x Wg and u = x Wu
+ * ([T*k, F] each, layer dtype); h as moe_gmm_gate_up. */
+moe_status_t moe_gmm_gate_up_saved(const moe_config_t *cfg,
+                                   const void *x_sorted,
+                                   const int32_t *group_offsets,
+                                   const void *w_gate, const void *w_up,
+                                   void *g, void *u, void *h,
+                                   int32_t *status_word, moe_stream_t stream);
+
+/* dh = dy_sorted Wd^T, then dg = dh * u * silu'(g) and du = dh * silu(g)
+ * ([T*k, F] each), silu'(z) = s(z) (1 + z (1 - s(z))), s the logistic. */
+moe_status_t moe_gmm_down_dgrad(const moe_config_t *cfg,
+                                const int32_t *group_offsets,
+                                const void *w_down, const void *g,
+                                const void *u, const void *dy_sorted,
+                                void *dg, void *du, int32_t *status_word,
+                                moe_stream_t stream);
+
+/* dx_sorted = dg Wg^T + du Wu^T ([T*k, H]). */
+moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t *cfg,
+                                   const int32_t *group_offsets,
+                                   const void *w_gate, const void *w_up,
+                                   const void *dg, const void *du,
+                                   void *dx_sorted, int32_t *status_word,
+                                   moe_stream_t stream);
+
+/* One row range of the weight-gradient reduction: its groups' rows are
+ * first_row + group_offsets[e] .. first_row + group_offsets[e+1] of the
+ * row buffers (group_offsets: device, [E+1]). */
+typedef struct {
+  const int32_t *group_offsets;
+  int32_t first_row;
+} moe_row_segment_t;
+
+/* Weight gradients summed over n_segments row ranges (a host array; e.g.
+ * one per chunk of the fallback, so that an expert's gradient over all
+ * chunks is accumulated on chip and written once), over the rows of
+ * expert e:
+ *   gate_up: dWg[e] (+)= x^T dg,  dWu[e] (+)= x^T du   ([E,H,F] float32)
+ *   down:    dWd[e] (+)= h^T dy_sorted                 ([E,F,H] float32)
+ * The row buffers have rows_total rows.  accumulate = 0 overwrites every
+ * expert's gradient (zeros for experts without rows), 1 adds into it. */
+moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t *cfg,
+                                   const moe_row_segment_t *segments,
+                                   int32_t n_segments, int64_t rows_total,
+                                   const void *x_sorted, const void *dg,
+                                   const void *du, float *dw_gate,
+                                   float *dw_up, int32_t accumulate,
+                                   int32_t *status_word, moe_stream_t stream);
+moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg,
+                                const moe_row_segment_t *segments,
+                                int32_t n_segments, int64_t rows_total,
+                                const void *h, const void *dy_sorted,
+                                float *dw_down, int32_t accumulate,
+                                int32_t *status_word, moe_stream_t stream);
+
+/* Backward of the grouped SwiGLU FFN (down dgrad, gate/up dgrad, then
+ * both weight gradients over one row range).  accumulate != 0 adds the
+ * weight
  * gradients into dw_* (float32), 0 overwrites them (every expert, also
  * those without rows).  workspace: moe_workspace_bytes(cfg,
  * MOE_WS_GMM_BACKWARD) (dg and du). */

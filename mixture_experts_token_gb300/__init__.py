@@ -52,6 +52,11 @@ class MoeLayerInfo(ctypes.Structure):
                 ("capacity", c_int64)]
 
 
+class MoeRowSegment(ctypes.Structure):
+    """moe_row_segment_t."""
+    _fields_ = [("group_offsets", c_void_p), ("first_row", c_int32)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -104,6 +109,14 @@ def _declare(h):
         "moe_gmm_swiglu_saved": [cfg, P, P, P, P, P, P, P, P, P, P, P],
         "moe_gmm_swiglu_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, P,
                                     P, c_int32, P, P, c_size_t, P],
+        "moe_gmm_gate_up_saved": [cfg, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_down_dgrad": [cfg, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_gate_up_dgrad": [cfg, P, P, P, P, P, P, P, P],
+        "moe_gmm_gate_up_wgrad": [cfg, ctypes.POINTER(MoeRowSegment),
+                                  c_int32, c_int64, P, P, P, P, P, c_int32,
+                                  P, P],
+        "moe_gmm_down_wgrad": [cfg, ctypes.POINTER(MoeRowSegment), c_int32,
+                               c_int64, P, P, P, c_int32, P, P],
         "moe_layer_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, c_int,
                                ctypes.POINTER(MoeLayerInfo), P, P, c_size_t,
                                P],
@@ -368,6 +381,58 @@ def moe_gmm_swiglu_backward(cfg, x_sorted, group_offsets, w_gate, w_up,
         _ptr(dx_sorted), _ptr(dw_gate), _ptr(dw_up), _ptr(dw_down),
         int(accumulate), _ptr(status_word), _ptr(workspace),
         _nbytes(workspace), _stream(stream)), "moe_gmm_swiglu_backward")
+
+
+def moe_gmm_gate_up_saved(cfg, x_sorted, group_offsets, w_gate, w_up, g, u,
+                          h, status_word=None, stream=None):
+    _check(lib().moe_gmm_gate_up_saved(
+        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
+        _ptr(w_up), _ptr(g), _ptr(u), _ptr(h), _ptr(status_word),
+        _stream(stream)), "moe_gmm_gate_up_saved")
+
+
+def moe_gmm_down_dgrad(cfg, group_offsets, w_down, g, u, dy_sorted, dg, du,
+                       status_word=None, stream=None):
+    _check(lib().moe_gmm_down_dgrad(
+        ctypes.byref(cfg), _ptr(group_offsets), _ptr(w_down), _ptr(g),
+        _ptr(u), _ptr(dy_sorted), _ptr(dg), _ptr(du), _ptr(status_word),
+        _stream(stream)), "moe_gmm_down_dgrad")
+
+
+def moe_gmm_gate_up_dgrad(cfg, group_offsets, w_gate, w_up, dg, du,
+                          dx_sorted, status_word=None, stream=None):
+    _check(lib().moe_gmm_gate_up_dgrad(
+        ctypes.byref(cfg), _ptr(group_offsets), _ptr(w_gate), _ptr(w_up),
+        _ptr(dg), _ptr(du), _ptr(dx_sorted), _ptr(status_word),
+        _stream(stream)), "moe_gmm_gate_up_dgrad")
+
+
+def _segments(segments):
+    """(group_offsets tensor, first_row) pairs -> moe_row_segment_t[]."""
+    arr = (MoeRowSegment * max(len(segments), 1))()
+    for i, (off, first) in enumerate(segments):
+        arr[i].group_offsets = off if isinstance(off, int) else off.data_ptr()
+        arr[i].first_row = int(first)
+    return arr
+
+
+def moe_gmm_gate_up_wgrad(cfg, segments, rows_total, x_sorted, dg, du,
+                          dw_gate, dw_up, accumulate, status_word=None,
+                          stream=None):
+    _check(lib().moe_gmm_gate_up_wgrad(
+        ctypes.byref(cfg), _segments(segments), len(segments),
+        int(rows_total), _ptr(x_sorted), _ptr(dg), _ptr(du), _ptr(dw_gate),
+        _ptr(dw_up), int(accumulate), _ptr(status_word), _stream(stream)),
+        "moe_gmm_gate_up_wgrad")
+
+
+def moe_gmm_down_wgrad(cfg, segments, rows_total, h, dy_sorted, dw_down,
+                       accumulate, status_word=None, stream=None):
+    _check(lib().moe_gmm_down_wgrad(
+        ctypes.byref(cfg), _segments(segments), len(segments),
+        int(rows_total), _ptr(h), _ptr(dy_sorted), _ptr(dw_down),
+        int(accumulate), _ptr(status_word), _stream(stream)),
+        "moe_gmm_down_wgrad")
 
 
 def moe_layer_backward(cfg, x, logits, w_gate, w_up, w_down, dy, dx,

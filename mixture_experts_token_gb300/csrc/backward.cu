@@ -397,35 +397,74 @@ cudaError_t launch_gmm_saved_f32(const moe_config_t& c, const Groups& g,
   return cudaGetLastError();
 }
 
-cudaError_t launch_gmm_backward_f32(const moe_config_t& c, const Groups& g,
-                                    const void* xs, const int32_t* off,
-                                    const void* wg, const void* wu,
-                                    const void* wd, const void* gbuf,
-                                    const void* ubuf, const void* h,
-                                    const void* dys, void* dxs, float* dwg,
-                                    float* dwu, float* dwd, int accumulate,
-                                    void* dg, void* du, cudaStream_t s) {
+cudaError_t launch_down_dgrad_f32(const moe_config_t& c, const Groups& g,
+                                  const int32_t* off, const void* wd,
+                                  const void* gbuf, const void* ubuf,
+                                  const void* dys, void* dg, void* du,
+                                  cudaStream_t s) {
   const long long rows = static_cast<long long>(c.T) * c.k;
-  const float* X = static_cast<const float*>(xs);
-  float* DG = static_cast<float*>(dg);
-  float* DU = static_cast<float*>(du);
-  if (rows > 0) {
-    dgrad2_swiglu_f32<<<blocks_for(rows * c.F, 256), 256, 0, s>>>(
-        static_cast<const float*>(dys), off, g.n, g.map, c.H, c.F,
-        static_cast<const float*>(wd), static_cast<const float*>(gbuf),
-        static_cast<const float*>(ubuf), DG, DU);
-    dgrad1_f32<<<blocks_for(rows * c.H, 256), 256, 0, s>>>(
-        DG, DU, off, g.n, g.map, c.H, c.F, static_cast<const float*>(wg),
-        static_cast<const float*>(wu), static_cast<float*>(dxs));
-  }
+  if (rows == 0) return cudaSuccess;
+  dgrad2_swiglu_f32<<<blocks_for(rows * c.F, 256), 256, 0, s>>>(
+      static_cast<const float*>(dys), off, g.n, g.map, c.H, c.F,
+      static_cast<const float*>(wd), static_cast<const float*>(gbuf),
+      static_cast<const float*>(ubuf), static_cast<float*>(dg),
+      static_cast<float*>(du));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_up_dgrad_f32(const moe_config_t& c, const Groups& g,
+                                     const int32_t* off, const void* wg,
+                                     const void* wu, const void* dg,
+                                     const void* du, void* dxs,
+                                     cudaStream_t s) {
+  const long long rows = static_cast<long long>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  dgrad1_f32<<<blocks_for(rows * c.H, 256), 256, 0, s>>>(
+      static_cast<const float*>(dg), static_cast<const float*>(du), off, g.n,
+      g.map, c.H, c.F, static_cast<const float*>(wg),
+      static_cast<const float*>(wu), static_cast<float*>(dxs));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad_f32(const moe_config_t& c, const Groups& g,
+                             const WgradSegment* seg, int n_seg,
+                             const void* xs, const void* dg, const void* du,
+                             const void* h, const void* dys, float* dwg,
+                             float* dwu, float* dwd, int accumulate,
+                             int parts, cudaStream_t s) {
   const long long nw = static_cast<long long>(c.E) * c.H * c.F;
-  wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
-      static_cast<const float*>(h), c.F, static_cast<const float*>(dys), c.H,
-      off, g.n, g.map, c.E, accumulate, dwd);
-  wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(X, c.H, DG, c.F, off, g.n,
-                                                g.map, c.E, accumulate, dwg);
-  wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(X, c.H, DU, c.F, off, g.n,
-                                                g.map, c.E, accumulate, dwu);
+  const bool gu = (parts & kWgradGateUp) != 0;
+  const bool dn = (parts & kWgradDown) != 0;
+  if (n_seg == 0 && !accumulate) {
+    const size_t bytes = static_cast<size_t>(nw) * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    if (gu) e = cudaMemsetAsync(dwg, 0, bytes, s);
+    if (gu && e == cudaSuccess) e = cudaMemsetAsync(dwu, 0, bytes, s);
+    if (dn && e == cudaSuccess) e = cudaMemsetAsync(dwd, 0, bytes, s);
+    return e;
+  }
+  const float* X = static_cast<const float*>(xs);
+  const float* DG = static_cast<const float*>(dg);
+  const float* DU = static_cast<const float*>(du);
+  const float* Hs = static_cast<const float*>(h);
+  const float* DY = static_cast<const float*>(dys);
+  for (int i = 0; i < n_seg; ++i) {
+    const long long r0 = seg[i].first_row;
+    const int acc = (accumulate || i > 0) ? 1 : 0;
+    const int32_t* off = seg[i].group_offsets;
+    if (dn)
+      wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
+          Hs + r0 * c.F, c.F, DY + r0 * c.H, c.H, off, g.n, g.map, c.E, acc,
+          dwd);
+    if (gu) {
+      wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
+          X + r0 * c.H, c.H, DG + r0 * c.F, c.F, off, g.n, g.map, c.E, acc,
+          dwg);
+      wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
+          X + r0 * c.H, c.H, DU + r0 * c.F, c.F, off, g.n, g.map, c.E, acc,
+          dwu);
+    }
+  }
   return cudaGetLastError();
 }
 

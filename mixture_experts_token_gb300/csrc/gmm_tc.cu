@@ -1611,14 +1611,13 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
   return tc::launch_one<1, 128>(a2, bd, bd, a2, p2, s);
 }
 
-// Forward GEMM1 that keeps g = x Wg and u = x Wu, then GEMM2.
-cudaError_t launch_gmm_saved_bf16(const moe_config_t& c, const Groups& g,
-                                  const void* x_sorted,
-                                  const int32_t* group_offsets,
-                                  const void* w_gate, const void* w_up,
-                                  const void* w_down, void* gbuf, void* ubuf,
-                                  void* h, void* y_sorted, int32_t* status,
-                                  cudaStream_t s) {
+// Forward GEMM1 + SwiGLU that also keeps g = x Wg and u = x Wu.
+cudaError_t launch_gate_up_saved_bf16(const moe_config_t& c, const Groups& g,
+                                      const void* x_sorted,
+                                      const int32_t* group_offsets,
+                                      const void* w_gate, const void* w_up,
+                                      void* gbuf, void* ubuf, void* h,
+                                      int32_t* status, cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   CUtensorMap a1, bg, bu;
@@ -1631,49 +1630,55 @@ cudaError_t launch_gmm_saved_bf16(const moe_config_t& c, const Groups& g,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
   p1.out2 = static_cast<__nv_bfloat16*>(ubuf);
   p1.out3 = static_cast<__nv_bfloat16*>(gbuf);
-  cudaError_t e = tc::launch_one<4, 256>(a1, bg, bu, a1, p1, s);
-  if (e != cudaSuccess) return e;
-  return launch_gmm2_bf16(c, g, h, group_offsets, w_down, y_sorted, status,
-                          s);
+  return tc::launch_one<4, 256>(a1, bg, bu, a1, p1, s);
 }
 
-// Data gradients: dh = dy_sorted Wd^T with the SwiGLU backward in the
-// epilogue (dg, du), then dx_sorted = dg Wg^T + du Wu^T as one GEMM with
-// K = 2F.
-cudaError_t launch_gmm_dgrad_bf16(const moe_config_t& c, const Groups& g,
-                                  const int32_t* group_offsets,
-                                  const void* w_gate, const void* w_up,
-                                  const void* w_down, const void* gbuf,
-                                  const void* ubuf, const void* dy_sorted,
-                                  void* dg, void* du, void* dx_sorted,
-                                  int32_t* status, cudaStream_t s) {
+// dh = dy_sorted Wd^T with the SwiGLU backward in the epilogue: dg, du.
+cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                   const int32_t* group_offsets,
+                                   const void* w_down, const void* gbuf,
+                                   const void* ubuf, const void* dy_sorted,
+                                   void* dg, void* du, int32_t* status,
+                                   cudaStream_t s) {
   const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   const uint64_t E = static_cast<uint64_t>(c.E);
-  const int bn2 = c.F % 256 == 0 ? 256 : 128;
-  const int bn3 = c.H % 256 == 0 ? 256 : 128;
-  CUtensorMap ad, bd, ag, au, bg, bu;
+  const int bn = c.F % 256 == 0 ? 256 : 128;
+  CUtensorMap ad, bd;
   if (!tc::make_map(&ad, dy_sorted, c.H, rows, 64, tc::BM) ||
-      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, bn2) ||
-      !tc::make_map(&ag, dg, c.F, rows, 64, tc::BM) ||
-      !tc::make_map(&au, du, c.F, rows, 64, tc::BM) ||
-      !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, bn3) ||
-      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, bn3))
+      !tc::make_map(&bd, w_down, c.H, E * c.F, 64, bn))
     return cudaErrorInvalidValue;
-  tc::Params p2{group_offsets, g.map, g.n, c.H, c.F / bn2,
-                static_cast<__nv_bfloat16*>(dg), c.F, status};
-  p2.out2 = static_cast<__nv_bfloat16*>(du);
-  p2.aux_g = static_cast<const __nv_bfloat16*>(gbuf);
-  p2.aux_u = static_cast<const __nv_bfloat16*>(ubuf);
-  cudaError_t e = bn2 == 256
-                      ? tc::launch_one<2, 256>(ad, bd, bd, ad, p2, s)
-                      : tc::launch_one<2, 128>(ad, bd, bd, ad, p2, s);
-  if (e != cudaSuccess) return e;
-  tc::Params p3{group_offsets, g.map, g.n, 2 * c.F, c.H / bn3,
-                static_cast<__nv_bfloat16*>(dx_sorted), c.H, status};
-  p3.k_split = c.F / 64;
-  return bn3 == 256 ? tc::launch_one<3, 256>(ag, bg, bu, au, p3, s)
-                    : tc::launch_one<3, 128>(ag, bg, bu, au, p3, s);
+  tc::Params p{group_offsets, g.map, g.n, c.H, c.F / bn,
+               static_cast<__nv_bfloat16*>(dg), c.F, status};
+  p.out2 = static_cast<__nv_bfloat16*>(du);
+  p.aux_g = static_cast<const __nv_bfloat16*>(gbuf);
+  p.aux_u = static_cast<const __nv_bfloat16*>(ubuf);
+  return bn == 256 ? tc::launch_one<2, 256>(ad, bd, bd, ad, p, s)
+                   : tc::launch_one<2, 128>(ad, bd, bd, ad, p, s);
+}
+
+// dx_sorted = dg Wg^T + du Wu^T as one GEMM with K = 2F.
+cudaError_t launch_gate_up_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                      const int32_t* group_offsets,
+                                      const void* w_gate, const void* w_up,
+                                      const void* dg, const void* du,
+                                      void* dx_sorted, int32_t* status,
+                                      cudaStream_t s) {
+  const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
+  if (rows == 0) return cudaSuccess;
+  const uint64_t E = static_cast<uint64_t>(c.E);
+  const int bn = c.H % 256 == 0 ? 256 : 128;
+  CUtensorMap ag, au, bg, bu;
+  if (!tc::make_map(&ag, dg, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&au, du, c.F, rows, 64, tc::BM) ||
+      !tc::make_map(&bg, w_gate, c.F, E * c.H, 64, bn) ||
+      !tc::make_map(&bu, w_up, c.F, E * c.H, 64, bn))
+    return cudaErrorInvalidValue;
+  tc::Params p{group_offsets, g.map, g.n, 2 * c.F, c.H / bn,
+               static_cast<__nv_bfloat16*>(dx_sorted), c.H, status};
+  p.k_split = c.F / 64;
+  return bn == 256 ? tc::launch_one<3, 256>(ag, bg, bu, au, p, s)
+                   : tc::launch_one<3, 128>(ag, bg, bu, au, p, s);
 }
 
 // Weight gradients over row segments (each {group offsets, first row}),
@@ -1685,7 +1690,9 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
                               float* dw_up, float* dw_down, int accumulate,
-                              int32_t* status, cudaStream_t s) {
+                              int parts, int32_t* status, cudaStream_t s) {
+  const bool gu = (parts & kWgradGateUp) != 0;
+  const bool dn = (parts & kWgradDown) != 0;
   const uint64_t E = static_cast<uint64_t>(c.E);
   const uint64_t rows = static_cast<uint64_t>(std::max<int64_t>(rows_total, 1));
   const long long per_expert = static_cast<long long>(c.H) * c.F;
@@ -1693,21 +1700,22 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
   cudaError_t e = cudaSuccess;
   if (!accumulate && mapped) {  // duplicates reduce into one expert
     const size_t bytes = static_cast<size_t>(E) * per_expert * sizeof(float);
-    if ((e = cudaMemsetAsync(dw_gate, 0, bytes, s)) != cudaSuccess ||
-        (e = cudaMemsetAsync(dw_up, 0, bytes, s)) != cudaSuccess ||
-        (e = cudaMemsetAsync(dw_down, 0, bytes, s)) != cudaSuccess)
+    if ((gu && (e = cudaMemsetAsync(dw_gate, 0, bytes, s)) != cudaSuccess) ||
+        (gu && (e = cudaMemsetAsync(dw_up, 0, bytes, s)) != cudaSuccess) ||
+        (dn && (e = cudaMemsetAsync(dw_down, 0, bytes, s)) != cudaSuccess))
       return e;
   }
   const int bnd = c.H % 256 == 0 ? 256 : 128;
   CUtensorMap px, qg, qu, og, ou, ph, qd, od;
-  if (!tc::make_map(&px, x_sorted, c.H, rows, 64, 64) ||
-      !tc::make_map(&qg, dg, c.F, rows, 64, 64) ||
-      !tc::make_map(&qu, du, c.F, rows, 64, 64) ||
-      !tc::make_map(&og, dw_gate, c.F, E * c.H, 32, 32, true) ||
-      !tc::make_map(&ou, dw_up, c.F, E * c.H, 32, 32, true) ||
-      !tc::make_map(&ph, h, c.F, rows, 64, 64) ||
-      !tc::make_map(&qd, dy_sorted, c.H, rows, 64, 64) ||
-      !tc::make_map(&od, dw_down, c.H, E * c.F, 32, 32, true))
+  if (gu && (!tc::make_map(&px, x_sorted, c.H, rows, 64, 64) ||
+             !tc::make_map(&qg, dg, c.F, rows, 64, 64) ||
+             !tc::make_map(&qu, du, c.F, rows, 64, 64) ||
+             !tc::make_map(&og, dw_gate, c.F, E * c.H, 32, 32, true) ||
+             !tc::make_map(&ou, dw_up, c.F, E * c.H, 32, 32, true)))
+    return cudaErrorInvalidValue;
+  if (dn && (!tc::make_map(&ph, h, c.F, rows, 64, 64) ||
+             !tc::make_map(&qd, dy_sorted, c.H, rows, 64, 64) ||
+             !tc::make_map(&od, dw_down, c.H, E * c.F, 32, 32, true)))
     return cudaErrorInvalidValue;
   for (int s0 = 0; s0 < std::max(n_seg, 1); s0 += tc::kMaxSeg) {
     tc::WParams p{};
@@ -1723,22 +1731,28 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
     if (!p.reduce) {
       // experts without rows: no tile writes their dW
       const dim3 grid(static_cast<unsigned>(g.n), 16);
-      tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_gate, dw_up,
-                                                 per_expert);
-      tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_down, nullptr,
-                                                 per_expert);
+      if (gu)
+        tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_gate, dw_up,
+                                                   per_expert);
+      if (dn)
+        tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_down, nullptr,
+                                                   per_expert);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (p.n_seg == 0) break;
-    p.m_tiles = c.H / tc::BM;
-    p.n_tiles = c.F / 128;
-    e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
-    if (e != cudaSuccess) return e;
-    p.m_tiles = c.F / tc::BM;
-    p.n_tiles = c.H / bnd;
-    e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
-                   : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
-    if (e != cudaSuccess) return e;
+    if (gu) {
+      p.m_tiles = c.H / tc::BM;
+      p.n_tiles = c.F / 128;
+      e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (dn) {
+      p.m_tiles = c.F / tc::BM;
+      p.n_tiles = c.H / bnd;
+      e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
+                     : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }

@@ -144,10 +144,9 @@ bool weights_ok(const void* wg, const void* wu, const void* wd);
 // ---------------------------------------------------------- backward ---
 // Rows of one weight-gradient segment: groups at group_offsets (relative),
 // shifted by first_row inside the activation buffers.
-struct WgradSegment {
-  const int32_t* group_offsets;  // [groups + 1]
-  int first_row;
-};
+using WgradSegment = moe_row_segment_t;
+constexpr int kWgradGateUp = 1;  // dWg and dWu
+constexpr int kWgradDown = 2;    // dWd
 cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy,
                                     const void* y_sorted,
                                     const int32_t* row_of,
@@ -157,42 +156,75 @@ cudaError_t launch_route_backward(const moe_config_t& c, const float* logits,
                                   const int32_t* topk_idx,
                                   const float* dtopk_w, float* dlogits,
                                   cudaStream_t s);
-// fp32 (CUDA cores): GEMM1 keeping g, u, h; and the whole FFN backward
+// fp32 (CUDA cores)
 cudaError_t launch_gmm_saved_f32(const moe_config_t& c, const Groups& g,
                                  const void* xs, const int32_t* off,
                                  const void* wg, const void* wu, void* gbuf,
                                  void* ubuf, void* h, cudaStream_t s);
-cudaError_t launch_gmm_backward_f32(const moe_config_t& c, const Groups& g,
-                                    const void* xs, const int32_t* off,
-                                    const void* wg, const void* wu,
-                                    const void* wd, const void* gbuf,
-                                    const void* ubuf, const void* h,
-                                    const void* dys, void* dxs, float* dwg,
-                                    float* dwu, float* dwd, int accumulate,
-                                    void* dg, void* du, cudaStream_t s);
-// bf16 (tensor cores)
-cudaError_t launch_gmm_saved_bf16(const moe_config_t& c, const Groups& g,
-                                  const void* x_sorted,
-                                  const int32_t* group_offsets,
-                                  const void* w_gate, const void* w_up,
-                                  const void* w_down, void* gbuf, void* ubuf,
-                                  void* h, void* y_sorted, int32_t* status,
+cudaError_t launch_down_dgrad_f32(const moe_config_t& c, const Groups& g,
+                                  const int32_t* off, const void* wd,
+                                  const void* gbuf, const void* ubuf,
+                                  const void* dys, void* dg, void* du,
                                   cudaStream_t s);
-cudaError_t launch_gmm_dgrad_bf16(const moe_config_t& c, const Groups& g,
-                                  const int32_t* group_offsets,
-                                  const void* w_gate, const void* w_up,
-                                  const void* w_down, const void* gbuf,
-                                  const void* ubuf, const void* dy_sorted,
-                                  void* dg, void* du, void* dx_sorted,
-                                  int32_t* status, cudaStream_t s);
+cudaError_t launch_gate_up_dgrad_f32(const moe_config_t& c, const Groups& g,
+                                     const int32_t* off, const void* wg,
+                                     const void* wu, const void* dg,
+                                     const void* du, void* dxs,
+                                     cudaStream_t s);
+cudaError_t launch_wgrad_f32(const moe_config_t& c, const Groups& g,
+                             const WgradSegment* seg, int n_seg,
+                             const void* xs, const void* dg, const void* du,
+                             const void* h, const void* dys, float* dwg,
+                             float* dwu, float* dwd, int accumulate,
+                             int parts, cudaStream_t s);
+// bf16 (tensor cores)
+cudaError_t launch_gate_up_saved_bf16(const moe_config_t& c, const Groups& g,
+                                      const void* x_sorted,
+                                      const int32_t* group_offsets,
+                                      const void* w_gate, const void* w_up,
+                                      void* gbuf, void* ubuf, void* h,
+                                      int32_t* status, cudaStream_t s);
+cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                   const int32_t* group_offsets,
+                                   const void* w_down, const void* gbuf,
+                                   const void* ubuf, const void* dy_sorted,
+                                   void* dg, void* du, int32_t* status,
+                                   cudaStream_t s);
+cudaError_t launch_gate_up_dgrad_bf16(const moe_config_t& c, const Groups& g,
+                                      const int32_t* group_offsets,
+                                      const void* w_gate, const void* w_up,
+                                      const void* dg, const void* du,
+                                      void* dx_sorted, int32_t* status,
+                                      cudaStream_t s);
 cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               const WgradSegment* seg, int n_seg,
                               int64_t rows_total, const void* x_sorted,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
                               float* dw_up, float* dw_down, int accumulate,
+                              int parts, int32_t* status, cudaStream_t s);
+// Dispatch on the layer dtype (bf16: tensor cores, fp32: CUDA cores).
+cudaError_t launch_gate_up_saved(const moe_config_t& c, const Groups& g,
+                                 const void* xs, const int32_t* off,
+                                 const void* wg, const void* wu, void* gbuf,
+                                 void* ubuf, void* h, int32_t* status,
+                                 cudaStream_t s);
+cudaError_t launch_down_dgrad(const moe_config_t& c, const Groups& g,
+                              const int32_t* off, const void* wd,
+                              const void* gbuf, const void* ubuf,
+                              const void* dys, void* dg, void* du,
                               int32_t* status, cudaStream_t s);
-
+cudaError_t launch_gate_up_dgrad(const moe_config_t& c, const Groups& g,
+                                 const int32_t* off, const void* wg,
+                                 const void* wu, const void* dg,
+                                 const void* du, void* dxs, int32_t* status,
+                                 cudaStream_t s);
+cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
+                         const WgradSegment* seg, int n_seg,
+                         int64_t rows_total, const void* xs, const void* dg,
+                         const void* du, const void* h, const void* dys,
+                         float* dwg, float* dwu, float* dwd, int accumulate,
+                         int parts, int32_t* status, cudaStream_t s);
 size_t gmm_backward_bytes(const moe_config_t& c);
 size_t layer_backward_bytes(const moe_config_t& c);
 

@@ -16,16 +16,12 @@
 // kernel accumulates an expert's rows from every range in tensor memory, so
 // dW is written once instead of read and rewritten per chunk.
 #include <algorithm>
+#include <limits>
 #include <vector>
 
 #include "internal.h"
 
 namespace moe {
-
-cudaError_t launch_gmm2_f32(const moe_config_t& c, const Groups& g,
-                            const void* h, const int32_t* group_offsets,
-                            const void* w_down, void* y_sorted,
-                            cudaStream_t s);
 
 namespace {
 
@@ -68,14 +64,13 @@ void* rows_at(const void* p, size_t row, size_t row_bytes) {
 }
 
 // Backward of one pass over tokens [t0, t0 + tc) with capacity cap (-1:
-// uncapped).  Its rows occupy [t0*k, (t0+tc)*k) of the row buffers and its
-// group offsets row `seg` of the segment table.  fp32 layers also add their
-// weight gradients here (accumulate after the first pass).
+// uncapped), all but the weight gradients.  Its rows occupy
+// [t0*k, (t0+tc)*k) of the row buffers and its group offsets row `seg` of
+// the segment table.
 cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
                      int seg, const void* x, const void* wg, const void* wu,
-                     const void* wd, const void* dy, void* dx, float* dwg,
-                     float* dwu, float* dwd, const BwdBufs& b,
-                     int32_t* status, cudaStream_t s) {
+                     const void* wd, const void* dy, void* dx,
+                     const BwdBufs& b, int32_t* status, cudaStream_t s) {
   moe_config_t sc = c;
   sc.T = tc;
   const size_t eb = elem_bytes(c.dtype);
@@ -101,29 +96,66 @@ cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
       b.f.uniq_offsets, b.f.uniq_tokens, b.f.expand_idx + base, b.f.n_dropped,
       b.f.pws, status, s);
   if (e != cudaSuccess) return e;
-  if (c.dtype == MOE_BF16) {
-    e = launch_gmm_saved_bf16(sc, ids, xs, goff, wg, wu, wd, gg, uu, h, ys,
-                              status, s);
-  } else {
-    e = launch_gmm_saved_f32(sc, ids, xs, goff, wg, wu, gg, uu, h, s);
-    if (e == cudaSuccess) e = launch_gmm2_f32(sc, ids, h, goff, wd, ys, s);
-  }
-  if (e != cudaSuccess) return e;
-  e = launch_combine_backward(sc, rows_at(dy, t0, hb), ys, row_of, w, dys,
-                              b.dtw + base, s);
-  if (e != cudaSuccess) return e;
-  if (c.dtype == MOE_BF16)
-    e = launch_gmm_dgrad_bf16(sc, ids, goff, wg, wu, wd, gg, uu, dys, dg, du,
-                              dxs, status, s);
-  else
-    e = launch_gmm_backward_f32(sc, ids, xs, goff, wg, wu, wd, gg, uu, h, dys,
-                                dxs, dwg, dwu, dwd, seg > 0 ? 1 : 0, dg, du,
-                                s);
-  if (e != cudaSuccess) return e;
+  if ((e = launch_gate_up_saved(sc, ids, xs, goff, wg, wu, gg, uu, h, status,
+                                s)) != cudaSuccess ||
+      (e = launch_gmm2(sc, ids, h, goff, wd, ys, status, s)) != cudaSuccess ||
+      (e = launch_combine_backward(sc, rows_at(dy, t0, hb), ys, row_of, w,
+                                   dys, b.dtw + base, s)) != cudaSuccess ||
+      (e = launch_down_dgrad(sc, ids, goff, wd, gg, uu, dys, dg, du, status,
+                             s)) != cudaSuccess ||
+      (e = launch_gate_up_dgrad(sc, ids, goff, wg, wu, dg, du, dxs, status,
+                                s)) != cudaSuccess)
+    return e;
   return launch_combine(sc, dxs, row_of, nullptr, rows_at(dx, t0, hb), s);
 }
 
 }  // namespace
+
+cudaError_t launch_gate_up_saved(const moe_config_t& c, const Groups& g,
+                                 const void* xs, const int32_t* off,
+                                 const void* wg, const void* wu, void* gbuf,
+                                 void* ubuf, void* h, int32_t* status,
+                                 cudaStream_t s) {
+  if (c.dtype == MOE_BF16)
+    return launch_gate_up_saved_bf16(c, g, xs, off, wg, wu, gbuf, ubuf, h,
+                                     status, s);
+  return launch_gmm_saved_f32(c, g, xs, off, wg, wu, gbuf, ubuf, h, s);
+}
+
+cudaError_t launch_down_dgrad(const moe_config_t& c, const Groups& g,
+                              const int32_t* off, const void* wd,
+                              const void* gbuf, const void* ubuf,
+                              const void* dys, void* dg, void* du,
+                              int32_t* status, cudaStream_t s) {
+  if (c.dtype == MOE_BF16)
+    return launch_down_dgrad_bf16(c, g, off, wd, gbuf, ubuf, dys, dg, du,
+                                  status, s);
+  return launch_down_dgrad_f32(c, g, off, wd, gbuf, ubuf, dys, dg, du, s);
+}
+
+cudaError_t launch_gate_up_dgrad(const moe_config_t& c, const Groups& g,
+                                 const int32_t* off, const void* wg,
+                                 const void* wu, const void* dg,
+                                 const void* du, void* dxs, int32_t* status,
+                                 cudaStream_t s) {
+  if (c.dtype == MOE_BF16)
+    return launch_gate_up_dgrad_bf16(c, g, off, wg, wu, dg, du, dxs, status,
+                                     s);
+  return launch_gate_up_dgrad_f32(c, g, off, wg, wu, dg, du, dxs, s);
+}
+
+cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
+                         const WgradSegment* seg, int n_seg,
+                         int64_t rows_total, const void* xs, const void* dg,
+                         const void* du, const void* h, const void* dys,
+                         float* dwg, float* dwu, float* dwd, int accumulate,
+                         int parts, int32_t* status, cudaStream_t s) {
+  if (c.dtype == MOE_BF16)
+    return launch_wgrad_bf16(c, g, seg, n_seg, rows_total, xs, dg, du, h, dys,
+                             dwg, dwu, dwd, accumulate, parts, status, s);
+  return launch_wgrad_f32(c, g, seg, n_seg, xs, dg, du, h, dys, dwg, dwu, dwd,
+                          accumulate, parts, s);
+}
 
 size_t gmm_backward_bytes(const moe_config_t& c) {
   Carve cv(nullptr);
@@ -210,14 +242,12 @@ moe_status_t moe_gmm_swiglu_saved(const moe_config_t* cfg,
       !ok_ptr(u, true) || !ok_ptr(h, true) || !ok_ptr(y_sorted, true))
     return MOE_ERR_INVALID_ARG;
   const Groups ids = identity_groups(*cfg);
-  if (cfg->dtype == MOE_BF16)
-    return cuda_st(launch_gmm_saved_bf16(*cfg, ids, x_sorted, group_offsets,
-                                         w_gate, w_up, w_down, g, u, h,
-                                         y_sorted, status_word, stream));
-  cudaError_t e = launch_gmm_saved_f32(*cfg, ids, x_sorted, group_offsets,
-                                       w_gate, w_up, g, u, h, stream);
+  cudaError_t e = launch_gate_up_saved(*cfg, ids, x_sorted, group_offsets,
+                                       w_gate, w_up, g, u, h, status_word,
+                                       stream);
   if (e == cudaSuccess)
-    e = launch_gmm2_f32(*cfg, ids, h, group_offsets, w_down, y_sorted, stream);
+    e = launch_gmm2(*cfg, ids, h, group_offsets, w_down, y_sorted,
+                    status_word, stream);
   return cuda_st(e);
 }
 
@@ -249,20 +279,138 @@ moe_status_t moe_gmm_swiglu_backward(
   void* dg = cv.take<char>(rows * cfg->F * elem_bytes(cfg->dtype));
   void* du = cv.take<char>(rows * cfg->F * elem_bytes(cfg->dtype));
   const Groups ids = identity_groups(*cfg);
-  if (cfg->dtype == MOE_F32)
-    return cuda_st(launch_gmm_backward_f32(
-        *cfg, ids, x_sorted, group_offsets, w_gate, w_up, w_down, g, u, h,
-        dy_sorted, dx_sorted, dw_gate, dw_up, dw_down, accumulate, dg, du,
-        stream));
-  cudaError_t e = launch_gmm_dgrad_bf16(*cfg, ids, group_offsets, w_gate,
-                                        w_up, w_down, g, u, dy_sorted, dg, du,
-                                        dx_sorted, status_word, stream);
+  cudaError_t e = launch_down_dgrad(*cfg, ids, group_offsets, w_down, g, u,
+                                    dy_sorted, dg, du, status_word, stream);
+  if (e == cudaSuccess)
+    e = launch_gate_up_dgrad(*cfg, ids, group_offsets, w_gate, w_up, dg, du,
+                             dx_sorted, status_word, stream);
   if (e != cudaSuccess) return cuda_st(e);
   const WgradSegment seg{group_offsets, 0};
-  return cuda_st(launch_wgrad_bf16(*cfg, ids, &seg, cfg->T > 0 ? 1 : 0,
-                                   static_cast<int64_t>(rows), x_sorted, dg,
-                                   du, h, dy_sorted, dw_gate, dw_up, dw_down,
-                                   accumulate, status_word, stream));
+  return cuda_st(launch_wgrad(*cfg, ids, &seg, cfg->T > 0 ? 1 : 0,
+                              static_cast<int64_t>(rows), x_sorted, dg, du, h,
+                              dy_sorted, dw_gate, dw_up, dw_down, accumulate,
+                              kWgradGateUp | kWgradDown, status_word,
+                              stream));
+}
+
+moe_status_t moe_gmm_gate_up_saved(const moe_config_t* cfg,
+                                   const void* x_sorted,
+                                   const int32_t* group_offsets,
+                                   const void* w_gate, const void* w_up,
+                                   void* g, void* u, void* h,
+                                   int32_t* status_word, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+      !ok_ptr(w_gate, true) || !ok_ptr(w_up, true) || !ok_ptr(g, true) ||
+      !ok_ptr(u, true) || !ok_ptr(h, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_gate_up_saved(*cfg, identity_groups(*cfg), x_sorted,
+                                      group_offsets, w_gate, w_up, g, u, h,
+                                      status_word, stream));
+}
+
+moe_status_t moe_gmm_down_dgrad(const moe_config_t* cfg,
+                                const int32_t* group_offsets,
+                                const void* w_down, const void* g,
+                                const void* u, const void* dy_sorted,
+                                void* dg, void* du, int32_t* status_word,
+                                moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(w_down, true) ||
+      !ok_ptr(g, true) || !ok_ptr(u, true) || !ok_ptr(dy_sorted, true) ||
+      !ok_ptr(dg, true) || !ok_ptr(du, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_down_dgrad(*cfg, identity_groups(*cfg), group_offsets,
+                                   w_down, g, u, dy_sorted, dg, du,
+                                   status_word, stream));
+}
+
+moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t* cfg,
+                                   const int32_t* group_offsets,
+                                   const void* w_gate, const void* w_up,
+                                   const void* dg, const void* du,
+                                   void* dx_sorted, int32_t* status_word,
+                                   moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(w_gate, true) ||
+      !ok_ptr(w_up, true) || !ok_ptr(dg, true) || !ok_ptr(du, true) ||
+      !ok_ptr(dx_sorted, true))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_gate_up_dgrad(*cfg, identity_groups(*cfg),
+                                      group_offsets, w_gate, w_up, dg, du,
+                                      dx_sorted, status_word, stream));
+}
+
+namespace {
+moe_status_t check_segments(const moe_config_t* cfg,
+                            const moe_row_segment_t* segments,
+                            int32_t n_segments, int64_t rows_total,
+                            int32_t accumulate) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1 || n_segments < 0 || rows_total < 0 ||
+      rows_total > std::numeric_limits<int32_t>::max() ||
+      (accumulate != 0 && accumulate != 1) ||
+      (n_segments > 0 && segments == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  for (int32_t i = 0; i < n_segments; ++i)
+    if (!ok_ptr(segments[i].group_offsets, false) ||
+        segments[i].first_row < 0 || segments[i].first_row > rows_total)
+      return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t* cfg,
+                                   const moe_row_segment_t* segments,
+                                   int32_t n_segments, int64_t rows_total,
+                                   const void* x_sorted, const void* dg,
+                                   const void* du, float* dw_gate,
+                                   float* dw_up, int32_t accumulate,
+                                   int32_t* status_word, moe_stream_t stream) {
+  moe_status_t st =
+      check_segments(cfg, segments, n_segments, rows_total, accumulate);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(dw_gate, true) || !ok_ptr(dw_up, true) ||
+      (n_segments > 0 &&
+       (!ok_ptr(x_sorted, true) || !ok_ptr(dg, true) || !ok_ptr(du, true))))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), segments,
+                              n_segments, rows_total, x_sorted, dg, du,
+                              nullptr, nullptr, dw_gate, dw_up, nullptr,
+                              accumulate, kWgradGateUp, status_word, stream));
+}
+
+moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg,
+                                const moe_row_segment_t* segments,
+                                int32_t n_segments, int64_t rows_total,
+                                const void* h, const void* dy_sorted,
+                                float* dw_down, int32_t accumulate,
+                                int32_t* status_word, moe_stream_t stream) {
+  moe_status_t st =
+      check_segments(cfg, segments, n_segments, rows_total, accumulate);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(dw_down, true) ||
+      (n_segments > 0 && (!ok_ptr(h, true) || !ok_ptr(dy_sorted, true))))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), segments,
+                              n_segments, rows_total, nullptr, nullptr,
+                              nullptr, h, dy_sorted, nullptr, nullptr,
+                              dw_down, accumulate, kWgradDown, status_word,
+                              stream));
 }
 
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
@@ -344,19 +492,18 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
   for (size_t i = 0; i < passes.size(); ++i) {
     const Pass& p = passes[i];
     e = bwd_pass(*cfg, p.t0, p.tc, p.cap, static_cast<int>(i), x, w_gate,
-                 w_up, w_down, dy, dx, dw_gate, dw_up, dw_down, b,
-                 status_word, stream);
+                 w_up, w_down, dy, dx, b, status_word, stream);
     if (e != cudaSuccess) return cuda_st(e);
     segs.push_back({b.seg_off + i * (cfg->E + 1), p.t0 * cfg->k});
   }
   e = launch_route_backward(*cfg, logits, b.f.topk_idx, b.dtw, dlogits,
                             stream);
   if (e != cudaSuccess) return cuda_st(e);
-  if (cfg->dtype == MOE_F32) return MOE_OK;  // added in the passes
-  return cuda_st(launch_wgrad_bf16(
+  return cuda_st(launch_wgrad(
       *cfg, identity_groups(*cfg), segs.data(), static_cast<int>(segs.size()),
       static_cast<int64_t>(cfg->T) * cfg->k, b.f.x_sorted, b.dg, b.du, b.f.h,
-      b.dys, dw_gate, dw_up, dw_down, 0, status_word, stream));
+      b.dys, dw_gate, dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
+      status_word, stream));
 }
 
 }  // extern "C"
