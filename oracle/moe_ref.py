@@ -704,6 +704,21 @@ def route_backward(logits: np.ndarray, idx: np.ndarray, dw: np.ndarray,
     return dl
 
 
+def expert_ffn_backward(x_rows, dy_rows, wg, wu, wd):
+    """Backward of one expert's SwiGLU FFN over a block of rows, given the
+    gradient dy_rows of its outputs y = (silu(x Wg) * (x Wu)) Wd.
+    Returns (dx_rows, (dWg, dWu, dWd))."""
+    x = np.asarray(x_rows, dtype=np.float64)
+    dy = np.asarray(dy_rows, dtype=np.float64)
+    g = x @ wg
+    u = x @ wu
+    h = silu(g) * u
+    dh = dy @ wd.T
+    dg = dh * u * silu_grad(g)
+    du = dh * silu(g)
+    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, h.T @ dy)
+
+
 def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
                           dy, C: Optional[int]):
     """Backward of one pass (capacity C, None = uncapped) with the weights
@@ -745,12 +760,7 @@ def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
         a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
         if a == b:
             continue
-        wg, wu, wd = weights(e)
-        dh = dys[a:b] @ wd.T
-        dg = dh * us[a:b] * silu_grad(gs[a:b])
-        du = dh * silu(gs[a:b])
-        dW[e] = (xs[a:b].T @ dg, xs[a:b].T @ du, hs[a:b].T @ dys[a:b])
-        dxs[a:b] = dg @ wg.T + du @ wu.T
+        dxs[a:b], dW[e] = expert_ffn_backward(xs[a:b], dys[a:b], *weights(e))
     dx = np.zeros((T, H))
     for t in range(T):
         for j in range(cfg.k):

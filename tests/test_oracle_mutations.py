@@ -48,7 +48,11 @@ MUTANTS = {
         "    for (e, t, j) in rows:\n        uniq_sets[e // Es].add(t)"),
     "silu_sign": (
         "return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
-    "gate_up_swapped": ("h = silu(g) * u", "h = silu(u) * g"),
+    "gate_up_swapped": ("    h = silu(g) * u\n    return h, np.matmul(h, wd)",
+                        "    h = silu(u) * g\n    return h, np.matmul(h, wd)"),
+    "backward_gate_up_swapped": (
+        "    h = silu(g) * u\n    dh = dy @ wd.T",
+        "    h = silu(u) * g\n    dh = dy @ wd.T"),
     "combine_ignores_weight": (
         "y[t] += float(topk_w[t, j]) * y_sorted[r]", "y[t] += y_sorted[r]"),
     "combine_skips_row_zero": (
@@ -76,8 +80,8 @@ MUTANTS = {
         "    return s * (1.0 + z * (1.0 - s))",
         "    return s * (1.0 + z * s)"),
     "swiglu_backward_drops_u": (
-        "        dg = dh * us[a:b] * silu_grad(gs[a:b])",
-        "        dg = dh * silu_grad(gs[a:b])"),
+        "    dg = dh * u * silu_grad(g)",
+        "    dg = dh * silu_grad(g)"),
     "dy_sorted_unweighted": (
         "                dys[r] = w[t, j] * dy[t]",
         "                dys[r] = dy[t]"),
@@ -85,11 +89,15 @@ MUTANTS = {
         "                dl[t, e] = p[e] * (dp[e] - dot)",
         "                dl[t, e] = p[e] * (dp[e] + dot)"),
     "dx_gate_only": (
-        "        dxs[a:b] = dg @ wg.T + du @ wu.T",
-        "        dxs[a:b] = dg @ wg.T"),
+        "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, h.T @ dy)",
+        "    return dg @ wg.T, (x.T @ dg, x.T @ du, h.T @ dy)"),
     "dwd_uses_x": (
-        "hs[a:b].T @ dys[a:b])",
-        "xs[a:b, :hs.shape[1]].T @ dys[a:b])"),
+        "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, h.T @ dy)",
+        "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, "
+        "x[:, :h.shape[1]].T @ dy)"),
+    "dwu_uses_dg": (
+        "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, h.T @ dy)",
+        "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ dg, h.T @ dy)"),
     "chunked_dw_not_summed": (
         "        out.dwg += g.dwg",
         "        out.dwg = g.dwg"),
