@@ -21,7 +21,15 @@ durations of the roofline come from the same timed region.  L2 is flushed
 metric through moe_layer with pinned host buffers, the host->device copies
 of x and the logits and the device->host copy of y inside the timed region.
 ``cpu_baseline`` is the float64 oracle timed on a bounded token sample of the
-same workload on the host cores.  With torchrun (N > 1) every rank runs an
+same workload on the host cores.
+
+``--backward`` times the layer's backward pass instead (its own JSON line):
+route -> check -> per pass: permute, GEMM1 keeping g and u, GEMM2, combine
+backward, down-projection dgrad with the SwiGLU backward, gate/up dgrad,
+permute backward -> route backward -> the two weight-gradient GEMMs over
+the rows of every pass (one launch each).  Its ``e2e`` goes through
+moe_layer_backward with x, logits and dy copied in and dx and dlogits
+copied out every step; the weight gradients stay in HBM.  With torchrun (N > 1) every rank runs an
 independent replica on its own tokens (weak scaling, no collective on the
 data path); the reported time is the max over ranks.
 """
@@ -48,8 +56,10 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from synth import WORKLOADS, make_logits, make_weights, make_x  # noqa: E402
+from synth.workloads import make_dy  # noqa: E402
 
 METRIC = "MoE layer tokens/sec at 1 GB300; permute GB/s and GMM TFLOP/s vs roofline"
+METRIC_BWD = "MoE layer backward tokens/sec at 1 GB300 (forward recomputed per pass)"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
@@ -64,6 +74,8 @@ CPU_SAMPLE = {"dsv3": 32, "l4mav": 32, "small": 1024, "tiny": 256,
               "profile_dsv3_e32": 32}
 REF_SAMPLE = {"dsv3": 8, "l4mav": 8, "small": 256, "tiny": 256,
               "profile_dsv3_e32": 8}
+BWD_CPU_SAMPLE = {"dsv3": 8, "l4mav": 8, "small": 256, "tiny": 256,
+                  "profile_dsv3_e32": 8}
 
 
 def workload_by_name(name, sweep_T=65536, routing=None):
@@ -431,6 +443,8 @@ def main():
                     help="override the workload's routing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer's backward pass (own JSON line)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -463,6 +477,12 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     layer = Layer(wl, device, seed_offset=rank, mode=args.mode)
+    if args.backward:
+        backward_main(layer, args, world, rank, device)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
     # identical bits: stepwise entry points vs the moe_layer call
@@ -801,6 +821,376 @@ def cpu_baseline(layer):
                       f"layer of their own (same H, E, k, F, S, factor; "
                       f"float64 numpy oracle incl. routing, check, fallback, "
                       f"FFN and combine); {sec:.1f} s"}
+
+
+# ------------------------------------------------------------ backward ----
+class Backward:
+    """Buffers and the stepwise backward of one layer (inputs and forward
+    buffers shared with the Layer)."""
+
+    def __init__(self, layer):
+        moe, c, w = layer.moe, layer.cfg, layer.wl
+        dev = layer.x.device
+        T, H, E, k, F = w.T, w.H, w.E, w.k, w.F
+        R = T * k
+        dt = layer.x.dtype
+        self.layer = layer
+        self.dy = make_dy(w, dev)
+        self.g, self.u, self.dg, self.du = (
+            torch.empty((R, F), dtype=dt, device=dev) for _ in range(4))
+        self.dys = torch.empty((R, H), dtype=dt, device=dev)
+        self.dxs = torch.empty((R, H), dtype=dt, device=dev)
+        self.dtw = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.dx = torch.empty((T, H), dtype=dt, device=dev)
+        self.dl = torch.empty((T, E), dtype=torch.float32, device=dev)
+        self.dw = [torch.empty((E, H, F), dtype=torch.float32, device=dev),
+                   torch.empty((E, H, F), dtype=torch.float32, device=dev),
+                   torch.empty((E, F, H), dtype=torch.float32, device=dev)]
+        n_max = max(1, moe.moe_num_chunks(c))
+        self.goff = [torch.empty(E + 1, dtype=torch.int32, device=dev)
+                     for _ in range(n_max)]
+        self.ws = moe.layer_workspace(c, moe.MOE_WS_LAYER_BACKWARD, dev)
+
+    def step(self, ev=None):
+        L = self
+        lay = self.layer
+        moe, b, c, W = lay.moe, lay.b, lay.cfg, lay.W
+        k = c.k
+        mark = ev or (lambda name: None)
+        mark("route")
+        moe.moe_route(c, lay.logits, b["topk_idx"], b["topk_w"], b["status"])
+        if lay.mode != "fallback":
+            passes = [(0, c.T, lay.mode == "capped")]
+        else:
+            mark("check")
+            moe.moe_check_overflow(c, b["topk_idx"], b["expert_counts"],
+                                   b["expert_offsets"], b["shard_counts"],
+                                   b["overflow_flag"], b["required_factor"],
+                                   b["capacity"])
+            mark("flag")
+            if int(b["overflow_flag"].item()):
+                passes = [(t0, min(c.T, t0 + lay.chunk), False)
+                          for t0 in range(0, c.T, lay.chunk)]
+            else:
+                passes = [(0, c.T, True)]
+        xs, h, ys = b["x_sorted"], b["h"], b["y_sorted"]
+        for i, (t0, t1, capped) in enumerate(passes):
+            sc = lay.sub(t0, t1, capped)
+            r0 = t0 * k
+            go = L.goff[i]
+            mark("permute")
+            moe.moe_permute(sc, lay.x[t0:t1], b["topk_idx"][t0:t1], capped,
+                            xs[r0:], b["row_of"][t0:t1],
+                            b["sorted_token"][r0:], go, b["uniq_offsets"],
+                            b["uniq_tokens"], b["expand_idx"][r0:],
+                            b["n_dropped"], b["permute_ws"])
+            mark("gmm_gate_up_saved")
+            moe.moe_gmm_gate_up_saved(sc, xs[r0:], go, W[0], W[1], L.g[r0:],
+                                      L.u[r0:], h[r0:], b["status"])
+            mark("gmm_down")
+            moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"])
+            mark("combine_bwd")
+            moe.moe_combine_backward(sc, L.dy[t0:t1], ys[r0:],
+                                     b["row_of"][t0:t1], b["topk_w"][t0:t1],
+                                     L.dys[r0:], L.dtw[t0:t1])
+            mark("gmm_down_dgrad")
+            moe.moe_gmm_down_dgrad(sc, go, W[2], L.g[r0:], L.u[r0:],
+                                   L.dys[r0:], L.dg[r0:], L.du[r0:],
+                                   b["status"])
+            mark("gmm_gate_up_dgrad")
+            moe.moe_gmm_gate_up_dgrad(sc, go, W[0], W[1], L.dg[r0:],
+                                      L.du[r0:], L.dxs[r0:], b["status"])
+            mark("permute_bwd")
+            moe.moe_permute_backward(sc, L.dxs[r0:], b["row_of"][t0:t1],
+                                     L.dx[t0:t1])
+        mark("route_bwd")
+        moe.moe_route_backward(c, lay.logits, b["topk_idx"], L.dtw, L.dl)
+        segs = [(L.goff[i], t0 * k) for i, (t0, _, _) in enumerate(passes)]
+        mark("gmm_gate_up_wgrad")
+        moe.moe_gmm_gate_up_wgrad(c, segs, c.T * k, xs, L.dg, L.du,
+                                  L.dw[0], L.dw[1], 0, b["status"])
+        mark("gmm_down_wgrad")
+        moe.moe_gmm_down_wgrad(c, segs, c.T * k, h, L.dys, L.dw[2], 0,
+                               b["status"])
+        mark(None)
+        return passes
+
+    def api(self, x, logits, dy, dx, dl):
+        moe = self.layer.moe
+        mode = {"fallback": moe.MOE_MODE_FALLBACK_LAYER,
+                "capped": moe.MOE_MODE_CAPPED,
+                "dropless": moe.MOE_MODE_DROPLESS}[self.layer.mode]
+        return moe.moe_layer_backward(self.layer.cfg, x, logits,
+                                      *self.layer.W, dy, dx, dl, *self.dw_api,
+                                      mode, self.ws, self.layer.b["status"])
+
+
+def backward_launches(passes, mode):
+    """Kernel launches of one backward step: route (+ check), per pass
+    permute 5 + GEMM1-saved + GEMM2 + combine backward + two dgrad GEMMs +
+    permute backward, route backward, and per batch of 16 row segments the
+    two weight-gradient GEMMs (+ the two zero fills of experts without rows
+    in the first batch)."""
+    n = len(passes)
+    batches = (n + 15) // 16
+    return (2 if mode == "fallback" else 1) + 11 * n + 1 + 2 * batches + 2
+
+
+def backward_work(w, accs):
+    """Algorithmic bytes and flops of each backward stage over the step."""
+    b = 2 if w.dtype == "bf16" else 4
+    H, F, k, E = w.H, w.F, w.k, w.E
+    out = {}
+
+    def add(name, by, fl):
+        t = out.setdefault(name, {"bytes": 0, "flops": 0, "launches": 0})
+        t["bytes"] += by
+        t["flops"] += fl
+        t["launches"] += 1
+    R_tot = 0
+    T_tot = 0
+    for a in accs:
+        T, R, Ea = a["T"], a["R"], a["E_act"]
+        R_tot += R
+        T_tot += T
+        add("permute", T * H * b + R * H * b + 16 * R, 0)
+        add("gmm_gate_up_saved", 2 * Ea * H * F * b + R * H * b + 3 * R * F * b,
+            4 * R * H * F)
+        add("gmm_down", Ea * F * H * b + R * F * b + R * H * b, 2 * R * F * H)
+        add("combine_bwd", T * H * b + 2 * R * H * b + 12 * T * k, 0)
+        add("gmm_down_dgrad", Ea * F * H * b + R * H * b + 4 * R * F * b,
+            2 * R * H * F)
+        add("gmm_gate_up_dgrad", 2 * Ea * H * F * b + 2 * R * F * b + R * H * b,
+            4 * R * H * F)
+        add("permute_bwd", R * H * b + T * H * b + 4 * T * k, 0)
+    add("route_bwd", 8 * T_tot * E + 8 * T_tot * k, 0)
+    add("gmm_gate_up_wgrad", R_tot * H * b + 2 * R_tot * F * b + 2 * E * H * F * 4,
+        4 * R_tot * H * F)
+    add("gmm_down_wgrad", R_tot * F * b + R_tot * H * b + E * F * H * 4,
+        2 * R_tot * H * F)
+    return out
+
+
+def oracle_backward_sample(wl, x_dev, L, W, dy_dev, n_tok, mode):
+    """The oracle's backward of the mode on tokens [0, n_tok) as a layer of
+    their own: routing, check, the capped pass or the chunked passes, each
+    pass's full backward (weight gradients of the experts it touched)."""
+    from oracle import moe_ref as ref
+    n = min(n_tok, wl.T)
+    xs = x_dev[:n].to("cpu", torch.float64).numpy()
+    dys = dy_dev[:n].to("cpu", torch.float64).numpy()
+    Ls = L[:n]
+    idx, _, _ = ref.route(Ls, wl.k, wl.renorm)
+    touched = sorted(set(int(e) for e in idx.reshape(-1)))
+    host = {e: (W[0][e].cpu(), W[1][e].cpu(), W[2][e].cpu()) for e in touched}
+
+    def weights(e):
+        g, u, d = host[e]
+        return (g.to(torch.float64).numpy(), u.to(torch.float64).numpy(),
+                d.to(torch.float64).numpy())
+    t = time.perf_counter()
+    idx, _, _ = ref.route(Ls, wl.k, wl.renorm)
+    C = ref.capacity(n, wl.k, wl.S, wl.factor)
+    if mode == "dropless":
+        passes = [(0, n, None)]
+    elif mode == "capped":
+        passes = [(0, n, C)]
+    else:
+        shard = ref.shard_counts(ref.expert_counts(idx, wl.E), wl.S)
+        if ref.overflow_flag(shard, C):
+            passes = [(t0, t1, None) for (t0, t1) in
+                      ref.chunk_plan(n, wl.k, wl.E, wl.S, C, wl.n_chunks)]
+        else:
+            passes = [(0, n, C)]
+    for (t0, t1, Cp) in passes:
+        sub = ref.MoEConfig(t1 - t0, wl.H, wl.E, wl.k, wl.F, wl.S,
+                            wl.factor if Cp is not None else -1.0, 0,
+                            wl.renorm)
+        ref.pass_backward_touched(sub, xs[t0:t1], Ls[t0:t1], weights,
+                                  dys[t0:t1], Cp)
+    return time.perf_counter() - t, n
+
+
+def backward_main(layer, args, world, rank, device):
+    moe = layer.moe
+    bw = Backward(layer)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    # identical bits: stepwise entry points vs moe_layer_backward
+    passes = bw.step()
+    torch.cuda.synchronize()
+    dx_api = torch.empty_like(bw.dx)
+    dl_api = torch.empty_like(bw.dl)
+    bw.dw_api = [torch.empty_like(t) for t in bw.dw]
+    info = bw.api(layer.x, layer.logits, bw.dy, dx_api, dl_api)
+    torch.cuda.synchronize()
+    same = torch.equal(dx_api, bw.dx) and torch.equal(dl_api, bw.dl) and \
+        all(torch.equal(a, b) for a, b in zip(bw.dw_api, bw.dw))
+    if not same:
+        raise SystemExit("stepwise backward and moe_layer_backward disagree")
+    if int(layer.b["status"].item()) != 0:
+        raise SystemExit(f"device status {int(layer.b['status'].item())}")
+    del bw.dw_api
+    for _ in range(args.warmup):
+        flush.zero_()
+        bw.step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+    clocks = ClockSampler(device)
+    timers = []
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        st = StageTimer()
+        passes = bw.step(st)
+        timers.append(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    clock_rec = clocks.stop()
+    step_ms = [sum(d for _, d in st.durations()) for st in timers]
+    mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
+    stage = {}
+    for st in timers:
+        for name, d in st.durations():
+            s_ = stage.setdefault(name, {"ms": 0.0, "n": 0})
+            s_["ms"] += d
+            s_["n"] += 1
+    work = backward_work(layer.wl, pass_accounting(layer, passes))
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for name, s_ in stage.items():
+        per_step = s_["ms"] / args.steps
+        ent = {"ms_per_step": round(per_step, 4),
+               "launch_groups_per_step": s_["n"] // args.steps,
+               "share": round(per_step / mean_ms, 4)}
+        if name in work:
+            wv = work[name]
+            sec = per_step / 1e3
+            ent["GBps"] = round(wv["bytes"] / sec / 1e9, 1)
+            if wv["flops"]:
+                ent["TFLOPs"] = round(wv["flops"] / sec / 1e12, 1)
+        kernels[name] = ent
+    # dominant kernel: the single-kernel stage with the most time
+    single = [n for n in work if n in stage and n != "permute"]
+    dom = max(single, key=lambda n: stage[n]["ms"])
+    wv = work[dom]
+    n_launch = wv["launches"]
+    dur = stage[dom]["ms"] / args.steps / n_launch / 1e3
+    bytes_l, flops_l = wv["bytes"] / n_launch, wv["flops"] / n_launch
+    t_mem = bytes_l / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops_l / (peaks["bf16_tflops_sustained"] * 1e12) if flops_l else 0
+    if t_mem >= t_flop:
+        achieved = bytes_l / dur / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = flops_l / dur / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = round(achieved / roof["peak"], 4)
+    roof["traffic"] = profiled_traffic(dom, layer.wl.name)
+    roof["kernel"] = dom
+    roof["algorithmic_bytes_per_launch"] = int(bytes_l)
+    roof["algorithmic_flops_per_launch"] = int(flops_l)
+    roof["launch_ms"] = round(dur * 1e3, 4)
+    roof["peak_source"] = f"{peak_src} MEASURED_PEAKS.json" \
+        if peak_src == "measured" else "fallback"
+    w = layer.wl
+    out = {
+        "metric": METRIC_BWD, "value": None, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; router logits, x, dy N(0,1), expert "
+                "weights N(0,0.02))",
+        "config": {
+            "workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k,
+            "F": w.F, "S": w.S, "ragged_buffer_factor": w.factor,
+            "routing": w.routing + (f" s={w.zipf_s}" if w.routing == "zipf"
+                                    else ""),
+            "mode": layer.mode, "overflow": info["overflow"],
+            "passes": len(passes), "capacity": info["capacity"],
+            "pass": "backward: forward recomputed per pass, dW float32 "
+                    "written once over all passes",
+            "l2": "flushed between steps (256 MiB write, outside the events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "wall_s_timed_loop": round(wall, 3),
+        "gpu_launches": backward_launches(passes, layer.mode) * args.steps,
+        "kernels": kernels,
+        "roofline": roof,
+    }
+    out["value"] = round(whole_job_tokens_per_s(world, w.T, mean_ms), 1)
+    if clock_rec:
+        out["clocks"] = clock_rec
+    if not args.no_e2e:
+        out["e2e"] = backward_e2e(bw, args, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = BWD_CPU_SAMPLE.get(w.name, 8)
+        sec, n = oracle_backward_sample(w, layer.x, layer.logits_np, layer.W,
+                                        bw.dy, n, layer.mode)
+        out["cpu_baseline"] = {
+            "value": round(n / sec, 4), "unit": UNIT, "cores": _CORES,
+            "kind": "oracle",
+            "sample": f"backward of the first {n} tokens of the {w.name} "
+                      f"batch as a layer of their own (float64 oracle: "
+                      f"routing, check, passes, FFN backward, weight "
+                      f"gradients of the touched experts); {sec:.1f} s"}
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def backward_e2e(bw, args, world, device):
+    """moe_layer_backward with pinned host x, logits and dy copied in and
+    dx and dlogits copied out inside the timed region, every step."""
+    lay = bw.layer
+    x_h = lay.x.cpu().pin_memory()
+    L_h = lay.logits.cpu().pin_memory()
+    dy_h = bw.dy.cpu().pin_memory()
+    dx_h = torch.empty(bw.dx.shape, dtype=bw.dx.dtype, pin_memory=True)
+    dl_h = torch.empty(bw.dl.shape, dtype=bw.dl.dtype, pin_memory=True)
+    x_d, L_d, dy_d = (torch.empty_like(t) for t in (lay.x, lay.logits, bw.dy))
+    dx_d, dl_d = torch.empty_like(bw.dx), torch.empty_like(bw.dl)
+    bw.dw_api = bw.dw
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def one():
+        x_d.copy_(x_h, non_blocking=True)
+        L_d.copy_(L_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        bw.api(x_d, L_d, dy_d, dx_d, dl_d)
+        dx_h.copy_(dx_d, non_blocking=True)
+        dl_h.copy_(dl_d, non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), \
+            torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    mean = max_over_ranks(sum(ms) / len(ms), device)
+    if not torch.equal(dx_h, bw.dx.cpu()):
+        raise SystemExit("end-to-end backward output differs")
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, L_h, dy_h))
+    d2h = sum(t.numel() * t.element_size() for t in (dx_h, dl_h))
+    return {"value": round(whole_job_tokens_per_s(world, lay.wl.T, mean), 1),
+            "unit": UNIT, "ms_per_step": round(mean, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "moe_layer_backward (C ABI), pinned host buffers"}
 
 
 def reference_arm(args, wl, device):
