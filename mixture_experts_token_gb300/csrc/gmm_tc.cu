@@ -1067,8 +1067,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // 64 rows}, one 8 KB box per 64 columns, descriptors LBO = 8192, SBO =
 // 1024, start advanced 2048 B per K=16 step, and both major bits set.
 // K is ragged: a group's last k-block holds rows of the next group (or TMA
-// zero fill, or unwritten rows past the end), so the MMA warp clears those
-// rows of both operands in shared memory before it issues the block.
+// zero fill, or unwritten rows past the end).  The MMA warp issues only the
+// K=16 steps that reach valid rows and clears the invalid rows of those
+// steps in both operands (shared memory) before it issues them.
+// Tiles of one expert run with the column tile fastest, so the CTAs at work
+// at one time write whole rows of dW; dW goes out with an L2 evict-first
+// policy and the activation rows come in with evict-last, so the 100+ MB
+// gradient stream of an expert does not push its few MB of rows (read by
+// every tile) out of L2.
 // Segments: rows of one expert may sit in several independent row ranges
 // (one per chunk of the chunked fallback); a tile accumulates all of them
 // in tensor memory before its single write.  The epilogue moves each
@@ -1091,22 +1097,54 @@ struct WParams {
   int32_t* status;
 };
 
+// L2 policies: the weight gradients stream through L2 once (evict first);
+// the activation rows feed every tile of their expert (evict last).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;"
+               : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
+                                                 const CUtensorMap* m,
+                                                 uint32_t bar, int c0, int c1,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1),
+      "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m,
-                                             uint32_t src, int c0, int c1) {
+                                             uint32_t src, int c0, int c1,
+                                             uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group"
-      " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(c0), "r"(c1)
+      ".L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m,
                                                   uint32_t src, int c0,
-                                                  int c1) {
+                                                  int c1, uint64_t policy) {
   asm volatile(
       "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile."
-      "bulk_group [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(c0), "r"(c1)
+      "bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
@@ -1231,6 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer -----
     if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       long long fills = 0;
@@ -1239,7 +1278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
            tile += gridDim.x) {
         const int g = group_of(tpre, p.G, tile);
         const int local = tile - tpre[g];
-        const int m = local % p.m_tiles, n = local / p.m_tiles;
+        const int n = local % p.n_tiles, m = local / p.n_tiles;
         for (int sg = 0; ok && sg < p.n_seg; ++sg) {
           const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
           for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
@@ -1255,16 +1294,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sb = sa + kAChunks * 8192;
 #pragma unroll
             for (int j = 0; j < kAChunks; ++j)
-              tma_load_2d(sa + j * 8192, &tmP, fb, m * BM + j * 64, r);
+              tma_load_2d_hint(sa + j * 8192, &tmP, fb, m * BM + j * 64, r,
+                               keep);
             if (WMODE == 0) {
-              tma_load_2d(sb, &tmQ0, fb, n * 128, r);
-              tma_load_2d(sb + 8192, &tmQ0, fb, n * 128 + 64, r);
-              tma_load_2d(sb + 16384, &tmQ1, fb, n * 128, r);
-              tma_load_2d(sb + 24576, &tmQ1, fb, n * 128 + 64, r);
+              tma_load_2d_hint(sb, &tmQ0, fb, n * 128, r, keep);
+              tma_load_2d_hint(sb + 8192, &tmQ0, fb, n * 128 + 64, r, keep);
+              tma_load_2d_hint(sb + 16384, &tmQ1, fb, n * 128, r, keep);
+              tma_load_2d_hint(sb + 24576, &tmQ1, fb, n * 128 + 64, r, keep);
             } else {
 #pragma unroll
               for (int j = 0; j < kBChunks; ++j)
-                tma_load_2d(sb + j * 8192, &tmQ0, fb, n * BN + j * 64, r);
+                tma_load_2d_hint(sb + j * 8192, &tmQ0, fb, n * BN + j * 64, r,
+                                 keep);
             }
             ++fills;
             if (++stage == WSTAGES) {
@@ -1309,25 +1350,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sa = smem_base + stage * kWStage;
           const int valid = min(BK, r1 - r);
-          if (valid < BK) {
-            // rows valid..63 of every 64-column box: one 8 KB box is 64
-            // rows of 128 B, so the cleared rows are contiguous (and the
-            // 128-byte swizzle only permutes 16-byte units inside a row)
-            const int per_box = (BK - valid) * 8;  // 16-byte units
-            uint4* base = reinterpret_cast<uint4*>(smem + stage * kWStage);
-            for (int i = lane; i < (kAChunks + kBChunks) * per_box;
-                 i += 32) {
-              const int box = i / per_box, u = i - box * per_box;
-              base[box * 512 + valid * 8 + u] = make_uint4(0, 0, 0, 0);
-            }
+          // a short block issues only the K=16 steps that hold valid rows;
+          // rows valid .. steps*16 of every 64-column box are cleared (a box
+          // is 64 rows of 128 B, so they are contiguous, and the 128-byte
+          // swizzle only permutes 16-byte units inside a row)
+          const int steps = (valid + 15) >> 4;
+          const int nz = (steps * 16 - valid) * 8;  // 16-byte units per box
+          if (nz > 0) {
+            uint4* base = reinterpret_cast<uint4*>(smem + stage * kWStage) +
+                          valid * 8;
+#pragma unroll
+            for (int box = 0; box < kAChunks + kBChunks; ++box)
+              for (int u = lane; u < nz; u += 32)
+                base[box * 512 + u] = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
           __syncwarp();
           if (lane == 0) {
             tc_fence_after();
             const uint32_t sb = sa + kAChunks * 8192;
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
+            for (int kk = 0; kk < steps; ++kk) {
               const uint64_t ad = smem_desc(sa + kk * 2048, 8192, 1024);
               const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
               umma_bf16(d, ad, bd, idesc, (!first || kk != 0) ? 1u : 0u);
@@ -1356,12 +1398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue ---------
     const int q = warp & 3;
     uint8_t* mybuf = stagebuf + q * 2 * kStageBuf;
+    const uint64_t stream = policy_evict_first();
     int acc = 0, nsub = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const int g = group_of(tpre, p.G, tile);
       const int local = tile - tpre[g];
-      const int m = local % p.m_tiles, n = local / p.m_tiles;
+      const int n = local % p.n_tiles, m = local / p.n_tiles;
       const int we = p.group_expert ? __ldg(p.group_expert + g) : g;
       bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
                           p.status);
@@ -1392,9 +1435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             col = n * 128 + (sub & 3) * 32;
           }
           if (p.reduce)
-            tma_reduce_add_2d(om, smem_u32(buf), col, orow);
+            tma_reduce_add_2d(om, smem_u32(buf), col, orow, stream);
           else
-            tma_store_2d(om, smem_u32(buf), col, orow);
+            tma_store_2d(om, smem_u32(buf), col, orow, stream);
           bulk_commit();
         }
       }
