@@ -68,6 +68,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
 # 32 experts and 1024 tokens (2.8 GB of weights: larger than L2, a few GB in
 # total on the device)
 PROFILE_WL = WORKLOADS["dsv3"].with_(name="profile_dsv3_e32", T=1024, E=32)
+# the backward's kernel captures: DeepSeek-V3 layer shape with 8 experts,
+# 256 tokens (256 rows per expert, as at full size) in 4 fallback chunks, so
+# the weight gradients sum 4 row segments; ~2 GB on the device
+PROFILE_BWD_WL = WORKLOADS["dsv3"].with_(name="profile_bwd_dsv3_e8", T=256,
+                                         E=8, n_chunks=4)
 
 # oracle sample sizes (tokens) for the CPU baseline and the reference arm
 CPU_SAMPLE = {"dsv3": 32, "l4mav": 32, "small": 1024, "tiny": 256,
@@ -81,6 +86,8 @@ BWD_CPU_SAMPLE = {"dsv3": 8, "l4mav": 8, "small": 256, "tiny": 256,
 def workload_by_name(name, sweep_T=65536, routing=None):
     if name == "profile":
         return PROFILE_WL
+    if name == "profile_bwd":
+        return PROFILE_BWD_WL
     if name == "sweep":
         from synth import sweep_workload
         return sweep_workload(sweep_T, routing or "zipf")
@@ -98,14 +105,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_digest(kernel):
+    """First 16 hex digits of the sha256 of the sources a GEMM kernel is
+    built from (the shared tensor-core header + its own file)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "mixture_experts_token_gb300", "csrc")
+    own = "wgrad_tc.cu" if kernel.endswith("_wgrad") else "gmm_tc.cu"
+    h = hashlib.sha256()
+    for name in ("tc_common.cuh", own):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    import hashlib
-    src = os.path.join(ROOT, "mixture_experts_token_gb300", "csrc",
-                       "gmm_tc.cu")
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = kernel_source_digest(kernel)
         path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
         want = None
         for line in open(path):
@@ -425,7 +442,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3",
                     choices=["dsv3", "l4mav", "small", "tiny", "profile",
-                             "sweep"],
+                             "profile_bwd", "sweep"],
                     help="sweep: routing/permute/dedup only (no expert FFN)")
     ap.add_argument("--sweep-T", type=int, default=65536)
     ap.add_argument("--redundant-slots", type=int, default=0,
