@@ -866,6 +866,17 @@ class Backward:
         n_max = max(1, moe.moe_num_chunks(c))
         self.goff = [torch.empty(E + 1, dtype=torch.int32, device=dev)
                      for _ in range(n_max)]
+        # the passes' rows regrouped for the weight gradients (bf16, as
+        # moe_layer_backward does)
+        self.regroup = w.dtype == "bf16"
+        rr = R + 16 * E
+        self.rr = rr
+        if self.regroup:
+            self.xs2 = torch.empty((rr, H), dtype=dt, device=dev)
+            self.dys2 = torch.empty((rr, H), dtype=dt, device=dev)
+            self.dg2, self.du2, self.h2 = (
+                torch.empty((rr, F), dtype=dt, device=dev) for _ in range(3))
+            self.off2 = torch.empty(E + 1, dtype=torch.int32, device=dev)
         self.ws = moe.layer_workspace(c, moe.MOE_WS_LAYER_BACKWARD, dev)
 
     def step(self, ev=None):
@@ -923,11 +934,20 @@ class Backward:
         mark("route_bwd")
         moe.moe_route_backward(c, lay.logits, b["topk_idx"], L.dtw, L.dl)
         segs = [(L.goff[i], t0 * k) for i, (t0, _, _) in enumerate(passes)]
+        if L.regroup and len(passes) <= 64:
+            mark("regroup")
+            moe.moe_regroup_rows(c, segs, L.rr, xs, L.dg, L.du, h, L.dys,
+                                 L.xs2, L.dg2, L.du2, L.h2, L.dys2, L.off2)
+            segs, rows = [(L.off2, 0)], L.rr
+            wx, wdg, wdu, wh, wdy = L.xs2, L.dg2, L.du2, L.h2, L.dys2
+        else:
+            rows = c.T * k
+            wx, wdg, wdu, wh, wdy = xs, L.dg, L.du, h, L.dys
         mark("gmm_gate_up_wgrad")
-        moe.moe_gmm_gate_up_wgrad(c, segs, c.T * k, xs, L.dg, L.du,
+        moe.moe_gmm_gate_up_wgrad(c, segs, rows, wx, wdg, wdu,
                                   L.dw[0], L.dw[1], 0, b["status"])
         mark("gmm_down_wgrad")
-        moe.moe_gmm_down_wgrad(c, segs, c.T * k, h, L.dys, L.dw[2], 0,
+        moe.moe_gmm_down_wgrad(c, segs, rows, wh, wdy, L.dw[2], 0,
                                b["status"])
         mark(None)
         return passes
@@ -942,15 +962,17 @@ class Backward:
                                       mode, self.ws, self.layer.b["status"])
 
 
-def backward_launches(passes, mode):
+def backward_launches(passes, mode, regroup):
     """Kernel launches of one backward step: route (+ check), per pass
     permute 5 + GEMM1-saved + GEMM2 + combine backward + two dgrad GEMMs +
-    permute backward, route backward, and per batch of 16 row segments the
-    two weight-gradient GEMMs (+ the two zero fills of experts without rows
-    in the first batch)."""
+    permute backward, route backward, the regrouping of the rows (2) or the
+    row segments in batches of 16, and per batch the two weight-gradient
+    GEMMs (+ the two zero fills of experts without rows in the first
+    batch)."""
     n = len(passes)
-    batches = (n + 15) // 16
-    return (2 if mode == "fallback" else 1) + 11 * n + 1 + 2 * batches + 2
+    batches = 1 if regroup else (n + 15) // 16
+    return (2 if mode == "fallback" else 1) + 11 * n + 1 + \
+        (2 if regroup else 0) + 2 * batches + 2
 
 
 def backward_work(w, accs):
@@ -981,6 +1003,8 @@ def backward_work(w, accs):
             4 * R * H * F)
         add("permute_bwd", R * H * b + T * H * b + 4 * T * k, 0)
     add("route_bwd", 8 * T_tot * E + 8 * T_tot * k, 0)
+    # the five row buffers read once and written once (pad rows not counted)
+    add("regroup", 2 * R_tot * (2 * H + 3 * F) * b, 0)
     add("gmm_gate_up_wgrad", R_tot * H * b + 2 * R_tot * F * b + 2 * E * H * F * 4,
         4 * R_tot * H * F)
     add("gmm_down_wgrad", R_tot * F * b + R_tot * H * b + E * F * H * 4,
@@ -1140,7 +1164,9 @@ def backward_main(layer, args, world, rank, device):
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "wall_s_timed_loop": round(wall, 3),
-        "gpu_launches": backward_launches(passes, layer.mode) * args.steps,
+        "gpu_launches": backward_launches(
+            passes, layer.mode, bw.regroup and len(passes) <= 64)
+        * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }

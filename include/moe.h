@@ -493,6 +493,26 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg,
                                 float *dw_down, int32_t accumulate,
                                 int32_t *status_word, moe_stream_t stream);
 
+/* Regroups the rows of several row ranges (the passes of a layer backward)
+ * for the weight-gradient GEMMs: group e of the output holds, in range
+ * order, e's rows from every range, starts on a 16-row boundary, and its pad
+ * rows up to the next boundary are zero, so the GEMMs see one row range per
+ * expert and whole K=16 steps.  Copies x_sorted [.,H], dg, du, h [.,F] and
+ * dy_sorted [.,H] (layer dtype) into the *_out buffers of rows_out rows;
+ * out_offsets (device, [E+1]) receives the new group offsets.  rows_out
+ * must be at least T*k + 16*E (cfg->T: the tokens of all ranges together);
+ * 1 <= n_segments <= 64.  The source ranges must lie inside the source
+ * buffers; a row of the output that no range fills is zero. */
+moe_status_t moe_regroup_rows(const moe_config_t *cfg,
+                              const moe_row_segment_t *segments,
+                              int32_t n_segments, int64_t rows_out,
+                              const void *x_sorted, const void *dg,
+                              const void *du, const void *h,
+                              const void *dy_sorted, void *x_out,
+                              void *dg_out, void *du_out, void *h_out,
+                              void *dy_out, int32_t *out_offsets,
+                              moe_stream_t stream);
+
 /* Backward of the grouped SwiGLU FFN (down dgrad, gate/up dgrad, then
  * both weight gradients over one row range).  accumulate != 0 adds the
  * weight

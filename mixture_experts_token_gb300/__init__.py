@@ -117,6 +117,8 @@ def _declare(h):
                                   P, P],
         "moe_gmm_down_wgrad": [cfg, ctypes.POINTER(MoeRowSegment), c_int32,
                                c_int64, P, P, P, c_int32, P, P],
+        "moe_regroup_rows": [cfg, ctypes.POINTER(MoeRowSegment), c_int32,
+                             c_int64, P, P, P, P, P, P, P, P, P, P, P, P],
         "moe_layer_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, c_int,
                                ctypes.POINTER(MoeLayerInfo), P, P, c_size_t,
                                P],
@@ -433,6 +435,16 @@ def moe_gmm_down_wgrad(cfg, segments, rows_total, h, dy_sorted, dw_down,
         int(rows_total), _ptr(h), _ptr(dy_sorted), _ptr(dw_down),
         int(accumulate), _ptr(status_word), _stream(stream)),
         "moe_gmm_down_wgrad")
+
+
+def moe_regroup_rows(cfg, segments, rows_out, x_sorted, dg, du, h,
+                     dy_sorted, x_out, dg_out, du_out, h_out, dy_out,
+                     out_offsets, stream=None):
+    _check(lib().moe_regroup_rows(
+        ctypes.byref(cfg), _segments(segments), len(segments), int(rows_out),
+        _ptr(x_sorted), _ptr(dg), _ptr(du), _ptr(h), _ptr(dy_sorted),
+        _ptr(x_out), _ptr(dg_out), _ptr(du_out), _ptr(h_out), _ptr(dy_out),
+        _ptr(out_offsets), _stream(stream)), "moe_regroup_rows")
 
 
 def moe_layer_backward(cfg, x, logits, w_gate, w_up, w_down, dy, dx,

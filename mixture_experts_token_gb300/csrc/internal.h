@@ -225,6 +225,19 @@ cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
                          const void* du, const void* h, const void* dys,
                          float* dwg, float* dwu, float* dwd, int accumulate,
                          int parts, int32_t* status, cudaStream_t s);
+// Rows of up to kMaxRegroupSegments ranges copied into one expert-major
+// layout with 16-row-aligned groups and zero pad rows (see regroup.cu);
+// destination buffers of regroup_rows(c) rows.
+constexpr int kMaxRegroupSegments = 64;
+inline int64_t regroup_rows(const moe_config_t& c) {
+  return static_cast<int64_t>(c.T) * c.k + 16 * static_cast<int64_t>(c.E);
+}
+cudaError_t launch_regroup(const moe_config_t& c, const WgradSegment* seg,
+                           int n_seg, int64_t rows_out, const void* xs,
+                           const void* dg, const void* du, const void* h,
+                           const void* dys, void* xs2, void* dg2, void* du2,
+                           void* h2, void* dys2, int32_t* out_off,
+                           cudaStream_t s);
 size_t gmm_backward_bytes(const moe_config_t& c);
 size_t layer_backward_bytes(const moe_config_t& c);
 

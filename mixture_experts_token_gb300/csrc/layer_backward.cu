@@ -14,7 +14,9 @@
 // summed in one launch at the end: each pass leaves its rows in a disjoint
 // row range of the activation buffers, and one tile of the weight-gradient
 // kernel accumulates an expert's rows from every range in tensor memory, so
-// dW is written once instead of read and rewritten per chunk.
+// dW is written once instead of read and rewritten per chunk.  Before that
+// launch (bf16, up to 64 passes) the passes' rows are regrouped into one
+// 16-row-aligned range per expert (regroup.cu).
 #include <algorithm>
 #include <limits>
 #include <vector>
@@ -31,6 +33,9 @@ struct BwdBufs {
   void *dys, *dxs;        // [T*k, H]
   float* dtw;             // [T, k]
   int32_t* seg_off;       // [n_seg, E + 1] group offsets of every pass
+  // the passes' rows regrouped for the weight gradients (regroup.cu)
+  void *xs2, *dg2, *du2, *h2, *dys2;  // [T*k + 16*E, H or F]
+  int32_t* off2;                      // [E + 1]
 };
 
 int max_passes(const moe_config_t& c, moe_mode_t mode) {
@@ -55,6 +60,13 @@ BwdBufs carve_bwd(void* base, const moe_config_t& c, int n_seg,
   b.dxs = cv.take<char>(rows * c.H * eb);
   b.dtw = cv.take<float>(rows);
   b.seg_off = cv.take<int32_t>(static_cast<size_t>(n_seg) * (c.E + 1));
+  const size_t rr = static_cast<size_t>(regroup_rows(c));
+  b.xs2 = cv.take<char>(rr * c.H * eb);
+  b.dys2 = cv.take<char>(rr * c.H * eb);
+  b.dg2 = cv.take<char>(rr * c.F * eb);
+  b.du2 = cv.take<char>(rr * c.F * eb);
+  b.h2 = cv.take<char>(rr * c.F * eb);
+  b.off2 = cv.take<int32_t>(c.E + 1);
   if (bytes) *bytes = fb + align_up(cv.off, 256);
   return b;
 }
@@ -413,6 +425,35 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg,
                               stream));
 }
 
+moe_status_t moe_regroup_rows(const moe_config_t* cfg,
+                              const moe_row_segment_t* segments,
+                              int32_t n_segments, int64_t rows_out,
+                              const void* x_sorted, const void* dg,
+                              const void* du, const void* h,
+                              const void* dy_sorted, void* x_out,
+                              void* dg_out, void* du_out, void* h_out,
+                              void* dy_out, int32_t* out_offsets,
+                              moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1 || n_segments < 1 || n_segments > kMaxRegroupSegments ||
+      segments == nullptr || rows_out < regroup_rows(*cfg) ||
+      rows_out > std::numeric_limits<int32_t>::max())
+    return MOE_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_segments; ++i)
+    if (!ok_ptr(segments[i].group_offsets, false) ||
+        segments[i].first_row < 0)
+      return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(x_sorted, true) || !ok_ptr(dg, true) || !ok_ptr(du, true) ||
+      !ok_ptr(h, true) || !ok_ptr(dy_sorted, true) || !ok_ptr(x_out, true) ||
+      !ok_ptr(dg_out, true) || !ok_ptr(du_out, true) || !ok_ptr(h_out, true) ||
+      !ok_ptr(dy_out, true) || !ok_ptr(out_offsets, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_regroup(*cfg, segments, n_segments, rows_out,
+                                x_sorted, dg, du, h, dy_sorted, x_out, dg_out,
+                                du_out, h_out, dy_out, out_offsets, stream));
+}
+
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
                                 const float* logits, const void* w_gate,
                                 const void* w_up, const void* w_down,
@@ -499,6 +540,20 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
   e = launch_route_backward(*cfg, logits, b.f.topk_idx, b.dtw, dlogits,
                             stream);
   if (e != cudaSuccess) return cuda_st(e);
+  if (cfg->dtype == MOE_BF16 &&
+      segs.size() <= static_cast<size_t>(kMaxRegroupSegments)) {
+    // one 16-row-aligned row range per expert for the tensor-core GEMMs
+    const int64_t rr = regroup_rows(*cfg);
+    e = launch_regroup(*cfg, segs.data(), static_cast<int>(segs.size()), rr,
+                       b.f.x_sorted, b.dg, b.du, b.f.h, b.dys, b.xs2, b.dg2,
+                       b.du2, b.h2, b.dys2, b.off2, stream);
+    if (e != cudaSuccess) return cuda_st(e);
+    const WgradSegment one{b.off2, 0};
+    return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), &one, 1, rr,
+                                b.xs2, b.dg2, b.du2, b.h2, b.dys2, dw_gate,
+                                dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
+                                status_word, stream));
+  }
   return cuda_st(launch_wgrad(
       *cfg, identity_groups(*cfg), segs.data(), static_cast<int>(segs.size()),
       static_cast<int64_t>(cfg->T) * cfg->k, b.f.x_sorted, b.dg, b.du, b.f.h,

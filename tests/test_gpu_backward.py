@@ -263,3 +263,52 @@ def test_combine_backward_exact_small():
             dot = float(dyh[t] @ ysh[r])
             assert abs(dtwh[t, j] - dot) <= 1e-5 * (np.abs(dyh[t]) @
                                                      np.abs(ysh[r]) + 1e-30)
+
+
+def test_regroup_rows_layout():
+    """moe_regroup_rows: group e of the output holds e's rows of every range
+    in range order (byte copies), starts at the exclusive scan of the
+    16-rounded group sizes, and its pad rows are zero."""
+    E, H, F, k, T = 6, 256, 128, 2, 300
+    cfg = cfg_from(BWD[1], T=T, H=H, E=E, k=k, F=F, S=2)
+    rng = np.random.default_rng(3)
+    R = T * k
+    # three ranges: rows [base, base + sum(counts)) grouped by expert
+    counts = [rng.integers(0, 60, size=E) for _ in range(3)]
+    counts[1][2] = 0
+    counts[2][:] = 0
+    counts[2][E - 1] = 17
+    bases, offs, b0 = [], [], 0
+    for cnt in counts:
+        off = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        bases.append(b0)
+        offs.append(torch.from_numpy(off).cuda())
+        b0 += int(off[-1]) + 5          # a gap of foreign rows between ranges
+    assert b0 <= R
+    src = {n: torch.randn((R, w), device="cuda").to(torch.bfloat16)
+           for n, w in (("xs", H), ("dg", F), ("du", F), ("h", F),
+                        ("dys", H))}
+    rr = R + 16 * E
+    out = {n: torch.full((rr, t.shape[1]), float("nan"), device="cuda",
+                         dtype=torch.bfloat16) for n, t in src.items()}
+    off2 = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    segs = list(zip(offs, bases))
+    moe.moe_regroup_rows(cfg, segs, rr, src["xs"], src["dg"], src["du"],
+                         src["h"], src["dys"], out["xs"], out["dg"],
+                         out["du"], out["h"], out["dys"], off2)
+    torch.cuda.synchronize()
+    tot = sum(counts)
+    want_off = np.concatenate([[0], np.cumsum((tot + 15) // 16 * 16)])
+    assert np.array_equal(np_(off2), want_off)
+    for name in src:
+        s_, o_ = src[name].cpu(), out[name].cpu()
+        for e in range(E):
+            rows = []
+            for cnt, base, off in zip(counts, bases, offs):
+                a = base + int(np_(off)[e])
+                rows += list(range(a, a + int(cnt[e])))
+            g0 = int(want_off[e])
+            if rows:
+                assert torch.equal(o_[g0:g0 + len(rows)], s_[rows]), (name, e)
+            pad = o_[g0 + len(rows):int(want_off[e + 1])]
+            assert torch.count_nonzero(pad.float()).item() == 0, (name, e)
