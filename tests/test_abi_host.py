@@ -138,3 +138,60 @@ def test_workspace_sizes(m):
         R = w.T * w.k
         assert layer >= R * (2 * w.H + w.F) * 2
     assert m.moe_workspace_bytes(cfg_of(m, k=0), m.MOE_WS_LAYER) == 0
+
+
+def test_backward_workspace_sizes(m):
+    from synth import WORKLOADS
+    for name in ("small", "dsv3", "l4mav"):
+        w = WORKLOADS[name]
+        c = cfg_of(m, T=w.T, H=w.H, E=w.E, k=w.k, F=w.F, S=w.S,
+                   factor=w.factor)
+        R = w.T * w.k
+        gb = m.moe_workspace_bytes(c, m.MOE_WS_GMM_BACKWARD)
+        lb = m.moe_workspace_bytes(c, m.MOE_WS_LAYER_BACKWARD)
+        layer = m.moe_workspace_bytes(c, m.MOE_WS_LAYER)
+        # dg and du [T*k, F]
+        assert gb >= 2 * R * w.F * 2
+        # the forward layer buffers + g, u, dg, du, dy_sorted, dx_sorted,
+        # and the regrouped copies of five row buffers (T*k + 16*E rows)
+        assert lb >= layer + R * (4 * w.F + 2 * w.H) * 2 + \
+            (R + 16 * w.E) * (2 * w.H + 3 * w.F) * 2
+        # one group-offset row per possible pass
+        small = cfg_of(m, T=w.T, H=w.H, E=w.E, k=w.k, F=w.F, S=w.S,
+                       factor=w.factor, n_chunks=1)
+        assert m.moe_workspace_bytes(small, m.MOE_WS_LAYER_BACKWARD) <= lb
+
+
+def test_backward_arguments_are_rejected_before_any_launch(m):
+    c = cfg_of(m, H=128)   # a shape the tensor-core kernels cover
+    p = ctypes.c_void_p(0x1000)
+    seg = (m.MoeRowSegment * 1)()
+    seg[0].group_offsets = 0x1000
+    seg[0].first_row = 0
+    lib = m.lib()
+    # regrouping: no ranges, too many ranges, an output too small
+    args = (p, p, p, p, p, p, p, p, p, p, p)
+    rows = c.T * c.k + 16 * c.E
+    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 0, rows, *args,
+                                None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 65, rows, *args,
+                                None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 1, rows - 1, *args,
+                                None) == m.MOE_ERR_INVALID_ARG
+    # weight gradients: a negative range start, accumulate not 0/1
+    seg[0].first_row = -1
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), seg, 1, rows, p, p, p, 0,
+                                  None, None) == m.MOE_ERR_INVALID_ARG
+    seg[0].first_row = 0
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), seg, 1, rows, p, p, p, 2,
+                                  None, None) == m.MOE_ERR_INVALID_ARG
+    # layer backward: duplicate slots are not covered; no workspace
+    c2 = cfg_of(m, H=128)
+    c2.redundant_slots = 1
+    info = m.MoeLayerInfo()
+    assert lib.moe_layer_backward(ctypes.byref(c2), p, p, p, p, p, p, p, p, p,
+                                  p, p, 0, ctypes.byref(info), None, p, 1 << 40,
+                                  None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layer_backward(ctypes.byref(c), p, p, p, p, p, p, p, p, p,
+                                  p, p, 0, ctypes.byref(info), None, None, 0,
+                                  None) == m.MOE_ERR_WORKSPACE
