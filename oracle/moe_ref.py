@@ -720,16 +720,25 @@ def expert_ffn_backward(x_rows, dy_rows, wg, wu, wd):
 
 
 def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
-                          dy, C: Optional[int]):
+                          dy, C: Optional[int], groups=None):
     """Backward of one pass (capacity C, None = uncapped) with the weights
     read one expert at a time through an accessor.  Returns (Gradients with
     dwg = dwu = dwd = None, {e: (dWg[e], dWu[e], dWd[e])} for the experts
-    that received rows); every other expert's gradient is zero."""
+    that received rows); every other expert's gradient is zero.
+
+    groups = (vidx, G, group_expert): the rows are permuted over G virtual
+    groups by vidx instead of over the experts (dynamic redundancy); group g
+    computes with the weights of expert group_expert[g], and an expert's
+    weight gradient is the sum over its groups (in group order)."""
     x = np.asarray(x, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
     T, H = x.shape
     idx, w, _ = route(logits, cfg.k, cfg.renorm)
-    perm = permute_indices(idx, cfg.E, cfg.S, C)
+    if groups is None:
+        pidx, G, gexp = idx, cfg.E, None
+    else:
+        pidx, G, gexp = groups
+    perm = permute_indices(pidx, G, cfg.S, C)
     xs = gather_rows(x, perm.sorted_token)
     R = len(perm.sorted_token)
     F = cfg.F
@@ -738,11 +747,11 @@ def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
     hs = np.zeros((R, F))
     gs = np.zeros((R, F))
     us = np.zeros((R, F))
-    for e in range(cfg.E):
-        a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
+    for grp in range(G):
+        a, b = int(perm.group_offsets[grp]), int(perm.group_offsets[grp + 1])
         if a == b:
             continue
-        wg, wu, wd = weights(e)
+        wg, wu, wd = weights(grp if gexp is None else int(gexp[grp]))
         gs[a:b] = xs[a:b] @ wg
         us[a:b] = xs[a:b] @ wu
         hs[a:b] = silu(gs[a:b]) * us[a:b]
@@ -756,11 +765,14 @@ def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
                 dtw[t, j] = float(dy[t] @ ys[r])
                 dys[r] = w[t, j] * dy[t]
     dxs = np.zeros((R, H))
-    for e in range(cfg.E):
-        a, b = int(perm.group_offsets[e]), int(perm.group_offsets[e + 1])
+    for grp in range(G):
+        a, b = int(perm.group_offsets[grp]), int(perm.group_offsets[grp + 1])
         if a == b:
             continue
-        dxs[a:b], dW[e] = expert_ffn_backward(xs[a:b], dys[a:b], *weights(e))
+        e = grp if gexp is None else int(gexp[grp])
+        dxs[a:b], dWe = expert_ffn_backward(xs[a:b], dys[a:b], *weights(e))
+        dW[e] = dWe if e not in dW else tuple(
+            acc + v for acc, v in zip(dW[e], dWe))
     dx = np.zeros((T, H))
     for t in range(T):
         for j in range(cfg.k):
@@ -772,11 +784,13 @@ def pass_backward_touched(cfg: MoEConfig, x, logits, weights: ExpertWeights,
 
 
 def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
-                        dy, C: Optional[int]) -> Gradients:
+                        dy, C: Optional[int], groups=None) -> Gradients:
     """Backward of one pass (capacity C, None = uncapped) over in-memory
-    float64 weights [E,H,F], [E,H,F], [E,F,H]; dense weight gradients."""
+    float64 weights [E,H,F], [E,H,F], [E,F,H]; dense weight gradients.
+    groups: as pass_backward_touched."""
     g, dW = pass_backward_touched(cfg, x, logits,
-                                  dense_weights(w_gate, w_up, w_down), dy, C)
+                                  dense_weights(w_gate, w_up, w_down), dy, C,
+                                  groups)
     g.dwg = np.zeros(np.shape(w_gate), dtype=np.float64)
     g.dwu = np.zeros(np.shape(w_up), dtype=np.float64)
     g.dwd = np.zeros(np.shape(w_down), dtype=np.float64)
@@ -818,3 +832,25 @@ def layer_backward_chunked(cfg, x, logits, w_gate, w_up, w_down, dy):
         out.dwu += g.dwu
         out.dwd += g.dwd
     return out
+
+
+def layer_redundant_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
+                             dy, B: int) -> Gradients:
+    """Backward of layer_redundant ("Moe dynamic redundancy" (MaxText pull
+    request 4760), review comments: a duplicated expert's weight gradient is
+    the sum of its copies' gradients, a psum across devices there and a sum
+    over its virtual groups on one device).  Same plan, reroute and check as
+    the forward; the capped pass over the virtual groups, or the plain
+    chunked fallback when the diverted loads still overflow."""
+    idx, _, _ = route(logits, cfg.k, cfg.renorm)
+    counts = expert_counts(idx, cfg.E)
+    plan = plan_duplication(counts, cfg.S, B)
+    vidx = reroute(idx, plan, cfg.E, cfg.S)
+    G = cfg.S * (cfg.E // cfg.S + B)
+    vshard = shard_counts(expert_counts(vidx, G), cfg.S)
+    C = capacity(cfg.T, cfg.k, cfg.S, cfg.ragged_buffer_factor)
+    if overflow_flag(vshard, C):
+        return layer_backward_chunked(cfg, x, logits, w_gate, w_up, w_down,
+                                      dy)
+    return layer_pass_backward(cfg, x, logits, w_gate, w_up, w_down, dy, C,
+                               groups=(vidx, G, plan.group_expert))

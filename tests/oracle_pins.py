@@ -663,4 +663,42 @@ def pin_backward_dense_reduction():
     assert np.all(g.dlogits == 0)       # one expert, renorm: weight is 1
 
 
+def pin_redundant_backward_equals_dropless():
+    """fallback=layer with duplicate slots never drops a row (a shard over
+    capacity takes the dropless fallback), so its gradients equal the
+    dropless ones; the cases include plans that divert rows into slots (the
+    virtual-group path: slot groups with their expert's weights, an expert's
+    weight gradient summed over its groups)."""
+    rng = _rng(17)
+    diverted = 0
+    for _ in range(24):
+        S = int(rng.choice([2, 4]))
+        E = S * int(rng.choice([2, 3]))
+        k = int(rng.choice([1, 2]))
+        B = int(rng.choice([1, 2]))
+        T, H, F = int(rng.integers(12, 30)), 3, 4
+        factor = float(rng.choice([1.0, 1.5, 2.0]))
+        x = rng.standard_normal((T, H))
+        L = rng.standard_normal((T, E)) - 1.5 * np.log(np.arange(E) + 1.0)
+        w = (rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F)),
+             rng.standard_normal((E, F, H)))
+        dy = rng.standard_normal((T, H))
+        cfg = ref.MoEConfig(T, H, E, k, F, S, factor)
+        red = ref.layer_redundant_backward(cfg, x, L, *w, dy, B)
+        drop = ref.layer_backward_dropless(cfg, x, L, *w, dy)
+        for a, b in ((red.dx, drop.dx), (red.dlogits, drop.dlogits),
+                     (red.dwg, drop.dwg), (red.dwu, drop.dwu),
+                     (red.dwd, drop.dwd), (red.dtopk_w, drop.dtopk_w)):
+            assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+        idx, _, _ = ref.route(L, k)
+        plan = ref.plan_duplication(ref.expert_counts(idx, E), S, B)
+        vidx = ref.reroute(idx, plan, E, S)
+        G = S * (E // S + B)
+        C = ref.capacity(T, k, S, factor)
+        if plan.divert.sum() > 0 and not ref.overflow_flag(
+                ref.shard_counts(ref.expert_counts(vidx, G), S), C):
+            diverted += 1
+    assert diverted >= 4   # the virtual-group pass really ran
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -98,6 +98,12 @@ MUTANTS = {
     "dwu_uses_dg": (
         "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ du, h.T @ dy)",
         "    return dg @ wg.T + du @ wu.T, (x.T @ dg, x.T @ dg, h.T @ dy)"),
+    "duplicate_dw_not_summed": (
+        "        dW[e] = dWe if e not in dW else tuple(",
+        "        dW[e] = dWe if True else tuple("),
+    "slot_uses_group_weights": (
+        "        wg, wu, wd = weights(grp if gexp is None else int(gexp[grp]))",
+        "        wg, wu, wd = weights(grp % cfg.E)"),
     "chunked_dw_not_summed": (
         "        out.dwg += g.dwg",
         "        out.dwg = g.dwg"),
