@@ -864,19 +864,21 @@ class Backward:
                    torch.empty((E, H, F), dtype=torch.float32, device=dev),
                    torch.empty((E, F, H), dtype=torch.float32, device=dev)]
         n_max = max(1, moe.moe_num_chunks(c))
-        self.goff = [torch.empty(E + 1, dtype=torch.int32, device=dev)
+        G = E + w.S * w.redundant_slots     # groups with duplicate slots
+        self.G = G
+        self.goff = [torch.empty(G + 1, dtype=torch.int32, device=dev)
                      for _ in range(n_max)]
         # the passes' rows regrouped for the weight gradients (bf16, as
         # moe_layer_backward does)
         self.regroup = w.dtype == "bf16"
-        rr = R + 16 * E
+        rr = R + 16 * G
         self.rr = rr
         if self.regroup:
             self.xs2 = torch.empty((rr, H), dtype=dt, device=dev)
             self.dys2 = torch.empty((rr, H), dtype=dt, device=dev)
             self.dg2, self.du2, self.h2 = (
                 torch.empty((rr, F), dtype=dt, device=dev) for _ in range(3))
-            self.off2 = torch.empty(E + 1, dtype=torch.int32, device=dev)
+            self.off2 = torch.empty(G + 1, dtype=torch.int32, device=dev)
         self.ws = moe.layer_workspace(c, moe.MOE_WS_LAYER_BACKWARD, dev)
 
     def step(self, ev=None):
@@ -887,36 +889,58 @@ class Backward:
         mark = ev or (lambda name: None)
         mark("route")
         moe.moe_route(c, lay.logits, b["topk_idx"], b["topk_w"], b["status"])
-        if lay.mode != "fallback":
-            passes = [(0, c.T, lay.mode == "capped")]
-        else:
+        # duplicate-expert slots: check and plan first (as moe_layer_backward)
+        planned = c.redundant_slots > 0 and lay.mode != "dropless"
+        if planned or lay.mode == "fallback":
             mark("check")
             moe.moe_check_overflow(c, b["topk_idx"], b["expert_counts"],
                                    b["expert_offsets"], b["shard_counts"],
                                    b["overflow_flag"], b["required_factor"],
                                    b["capacity"])
+        if planned:
+            mark("plan")
+            moe.moe_plan_duplication(c, b["expert_counts"], b["divert"],
+                                     b["slot_of"], b["group_expert"],
+                                     b["shard_after"], b["flag_after"])
+        if lay.mode != "fallback":
+            passes = [(0, c.T, lay.mode == "capped")]
+        else:
             mark("flag")
-            if int(b["overflow_flag"].item()):
+            flag = b["flag_after"] if planned else b["overflow_flag"]
+            if int(flag.item()):
                 passes = [(t0, min(c.T, t0 + lay.chunk), False)
                           for t0 in range(0, c.T, lay.chunk)]
             else:
                 passes = [(0, c.T, True)]
+        # the plan's virtual groups for a capped pass, else the experts'
+        on_plan = planned and passes[0][2]
+        grp = dict(n_groups=L.G, group_expert=b["group_expert"]) \
+            if on_plan else {}
         xs, h, ys = b["x_sorted"], b["h"], b["y_sorted"]
         for i, (t0, t1, capped) in enumerate(passes):
             sc = lay.sub(t0, t1, capped)
             r0 = t0 * k
             go = L.goff[i]
             mark("permute")
-            moe.moe_permute(sc, lay.x[t0:t1], b["topk_idx"][t0:t1], capped,
-                            xs[r0:], b["row_of"][t0:t1],
-                            b["sorted_token"][r0:], go, b["uniq_offsets"],
-                            b["uniq_tokens"], b["expand_idx"][r0:],
-                            b["n_dropped"], b["permute_ws"])
+            if on_plan:
+                moe.moe_permute_planned(
+                    sc, lay.x[t0:t1], b["topk_idx"][t0:t1], capped,
+                    b["divert"], b["slot_of"], xs[r0:], b["row_of"][t0:t1],
+                    b["sorted_token"][r0:], go, b["uniq_offsets"],
+                    b["uniq_tokens"], b["expand_idx"][r0:], b["n_dropped"],
+                    b["permute_ws"])
+            else:
+                moe.moe_permute(sc, lay.x[t0:t1], b["topk_idx"][t0:t1],
+                                capped, xs[r0:], b["row_of"][t0:t1],
+                                b["sorted_token"][r0:], go, b["uniq_offsets"],
+                                b["uniq_tokens"], b["expand_idx"][r0:],
+                                b["n_dropped"], b["permute_ws"])
             mark("gmm_gate_up_saved")
             moe.moe_gmm_gate_up_saved(sc, xs[r0:], go, W[0], W[1], L.g[r0:],
-                                      L.u[r0:], h[r0:], b["status"])
+                                      L.u[r0:], h[r0:], b["status"], **grp)
             mark("gmm_down")
-            moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"])
+            moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"],
+                             **grp)
             mark("combine_bwd")
             moe.moe_combine_backward(sc, L.dy[t0:t1], ys[r0:],
                                      b["row_of"][t0:t1], b["topk_w"][t0:t1],
@@ -924,10 +948,11 @@ class Backward:
             mark("gmm_down_dgrad")
             moe.moe_gmm_down_dgrad(sc, go, W[2], L.g[r0:], L.u[r0:],
                                    L.dys[r0:], L.dg[r0:], L.du[r0:],
-                                   b["status"])
+                                   b["status"], **grp)
             mark("gmm_gate_up_dgrad")
             moe.moe_gmm_gate_up_dgrad(sc, go, W[0], W[1], L.dg[r0:],
-                                      L.du[r0:], L.dxs[r0:], b["status"])
+                                      L.du[r0:], L.dxs[r0:], b["status"],
+                                      **grp)
             mark("permute_bwd")
             moe.moe_permute_backward(sc, L.dxs[r0:], b["row_of"][t0:t1],
                                      L.dx[t0:t1])
@@ -937,7 +962,8 @@ class Backward:
         if L.regroup and len(passes) <= 64:
             mark("regroup")
             moe.moe_regroup_rows(c, segs, L.rr, xs, L.dg, L.du, h, L.dys,
-                                 L.xs2, L.dg2, L.du2, L.h2, L.dys2, L.off2)
+                                 L.xs2, L.dg2, L.du2, L.h2, L.dys2, L.off2,
+                                 n_groups=L.G if on_plan else 0)
             segs, rows = [(L.off2, 0)], L.rr
             wx, wdg, wdu, wh, wdy = L.xs2, L.dg2, L.du2, L.h2, L.dys2
         else:
@@ -945,10 +971,10 @@ class Backward:
             wx, wdg, wdu, wh, wdy = xs, L.dg, L.du, h, L.dys
         mark("gmm_gate_up_wgrad")
         moe.moe_gmm_gate_up_wgrad(c, segs, rows, wx, wdg, wdu,
-                                  L.dw[0], L.dw[1], 0, b["status"])
+                                  L.dw[0], L.dw[1], 0, b["status"], **grp)
         mark("gmm_down_wgrad")
         moe.moe_gmm_down_wgrad(c, segs, rows, wh, wdy, L.dw[2], 0,
-                               b["status"])
+                               b["status"], **grp)
         mark(None)
         return passes
 
@@ -962,17 +988,20 @@ class Backward:
                                       mode, self.ws, self.layer.b["status"])
 
 
-def backward_launches(passes, mode, regroup):
-    """Kernel launches of one backward step: route (+ check), per pass
-    permute 5 + GEMM1-saved + GEMM2 + combine backward + two dgrad GEMMs +
-    permute backward, route backward, the regrouping of the rows (2) or the
-    row segments in batches of 16, and per batch the two weight-gradient
-    GEMMs (+ the two zero fills of experts without rows in the first
-    batch)."""
+def backward_launches(passes, mode, regroup, planned=False, on_plan=False):
+    """Kernel launches of one backward step: route (+ check, + the plan with
+    duplicate slots), per pass permute 5 + GEMM1-saved + GEMM2 + combine
+    backward + two dgrad GEMMs + permute backward, route backward, the
+    regrouping of the rows (2) or the row segments in batches of 16, and per
+    batch the two weight-gradient GEMMs (+ the two zero fills of experts
+    without rows in the first batch; over the plan's groups a memset
+    replaces them)."""
     n = len(passes)
     batches = 1 if regroup else (n + 15) // 16
-    return (2 if mode == "fallback" else 1) + 11 * n + 1 + \
-        (2 if regroup else 0) + 2 * batches + 2
+    head = 1 + (1 if (mode == "fallback" or planned) else 0) + \
+        (1 if planned else 0)
+    return head + 11 * n + 1 + (2 if regroup else 0) + 2 * batches + \
+        (0 if on_plan else 2)
 
 
 def backward_work(w, accs):
@@ -1032,23 +1061,32 @@ def oracle_backward_sample(wl, x_dev, L, W, dy_dev, n_tok, mode):
     t = time.perf_counter()
     idx, _, _ = ref.route(Ls, wl.k, wl.renorm)
     C = ref.capacity(n, wl.k, wl.S, wl.factor)
+    counts = ref.expert_counts(idx, wl.E)
+    groups = None
+    load = ref.shard_counts(counts, wl.S)
+    if wl.redundant_slots > 0 and mode != "dropless":
+        B = wl.redundant_slots
+        plan = ref.plan_duplication(counts, wl.S, B)
+        vidx = ref.reroute(idx, plan, wl.E, wl.S)
+        G = wl.S * (wl.E // wl.S + B)
+        groups = (vidx, G, plan.group_expert)
+        load = ref.shard_counts(ref.expert_counts(vidx, G), wl.S)
     if mode == "dropless":
         passes = [(0, n, None)]
     elif mode == "capped":
         passes = [(0, n, C)]
+    elif ref.overflow_flag(load, C):
+        passes = [(t0, t1, None) for (t0, t1) in
+                  ref.chunk_plan(n, wl.k, wl.E, wl.S, C, wl.n_chunks)]
+        groups = None    # the fallback's chunks run plain
     else:
-        shard = ref.shard_counts(ref.expert_counts(idx, wl.E), wl.S)
-        if ref.overflow_flag(shard, C):
-            passes = [(t0, t1, None) for (t0, t1) in
-                      ref.chunk_plan(n, wl.k, wl.E, wl.S, C, wl.n_chunks)]
-        else:
-            passes = [(0, n, C)]
+        passes = [(0, n, C)]
     for (t0, t1, Cp) in passes:
         sub = ref.MoEConfig(t1 - t0, wl.H, wl.E, wl.k, wl.F, wl.S,
                             wl.factor if Cp is not None else -1.0, 0,
                             wl.renorm)
         ref.pass_backward_touched(sub, xs[t0:t1], Ls[t0:t1], weights,
-                                  dys[t0:t1], Cp)
+                                  dys[t0:t1], Cp, groups)
     return time.perf_counter() - t, n
 
 
@@ -1103,6 +1141,10 @@ def backward_main(layer, args, world, rank, device):
             s_ = stage.setdefault(name, {"ms": 0.0, "n": 0})
             s_["ms"] += d
             s_["n"] += 1
+    planned = layer.cfg.redundant_slots > 0 and layer.mode != "dropless"
+    on_plan = planned and passes[0][2]
+    if on_plan:   # the virtual groups' offsets, for the accounting only
+        layer.b["group_offsets"][:bw.G + 1].copy_(bw.goff[0])
     work = backward_work(layer.wl, pass_accounting(layer, passes))
     peaks, peak_src = load_peaks()
     kernels = {}
@@ -1158,6 +1200,7 @@ def backward_main(layer, args, world, rank, device):
                                     else ""),
             "mode": layer.mode, "overflow": info["overflow"],
             "passes": len(passes), "capacity": info["capacity"],
+            "redundant_slots": w.redundant_slots,
             "pass": "backward: forward recomputed per pass, dW float32 "
                     "written once over all passes",
             "l2": "flushed between steps (256 MiB write, outside the events)",
@@ -1165,8 +1208,8 @@ def backward_main(layer, args, world, rank, device):
         },
         "wall_s_timed_loop": round(wall, 3),
         "gpu_launches": backward_launches(
-            passes, layer.mode, bw.regroup and len(passes) <= 64)
-        * args.steps,
+            passes, layer.mode, bw.regroup and len(passes) <= 64, planned,
+            on_plan) * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }

@@ -435,11 +435,18 @@ moe_status_t moe_gmm_swiglu_saved(const moe_config_t *cfg,
 
 /* The steps of the FFN backward one kernel each (the compositions above
  * and below chain them).  Rows of group e use the weights of expert e;
- * only the group_offsets[E] rows are read and written.
+ * only the group_offsets[E] rows are read and written.  n_groups = 0 and
+ * group_expert = NULL mean the E experts' own groups; otherwise n_groups
+ * row groups (group_offsets [n_groups+1]) whose group g computes with the
+ * weights of expert group_expert[g] (device, [n_groups]): the virtual groups
+ * of moe_plan_duplication, a duplicate's weight gradient adding into its
+ * expert's.
  *
  * GEMM1 + SwiGLU of the forward that also keeps g = x Wg and u = x Wu
  * ([T*k, F] each, layer dtype); h as moe_gmm_gate_up. */
 moe_status_t moe_gmm_gate_up_saved(const moe_config_t *cfg,
+                                   int32_t n_groups,
+                                   const int32_t *group_expert,
                                    const void *x_sorted,
                                    const int32_t *group_offsets,
                                    const void *w_gate, const void *w_up,
@@ -448,7 +455,8 @@ moe_status_t moe_gmm_gate_up_saved(const moe_config_t *cfg,
 
 /* dh = dy_sorted Wd^T, then dg = dh * u * silu'(g) and du = dh * silu(g)
  * ([T*k, F] each), silu'(z) = s(z) (1 + z (1 - s(z))), s the logistic. */
-moe_status_t moe_gmm_down_dgrad(const moe_config_t *cfg,
+moe_status_t moe_gmm_down_dgrad(const moe_config_t *cfg, int32_t n_groups,
+                                const int32_t *group_expert,
                                 const int32_t *group_offsets,
                                 const void *w_down, const void *g,
                                 const void *u, const void *dy_sorted,
@@ -457,6 +465,8 @@ moe_status_t moe_gmm_down_dgrad(const moe_config_t *cfg,
 
 /* dx_sorted = dg Wg^T + du Wu^T ([T*k, H]). */
 moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t *cfg,
+                                   int32_t n_groups,
+                                   const int32_t *group_expert,
                                    const int32_t *group_offsets,
                                    const void *w_gate, const void *w_up,
                                    const void *dg, const void *du,
@@ -480,13 +490,16 @@ typedef struct {
  * The row buffers have rows_total rows.  accumulate = 0 overwrites every
  * expert's gradient (zeros for experts without rows), 1 adds into it. */
 moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t *cfg,
+                                   int32_t n_groups,
+                                   const int32_t *group_expert,
                                    const moe_row_segment_t *segments,
                                    int32_t n_segments, int64_t rows_total,
                                    const void *x_sorted, const void *dg,
                                    const void *du, float *dw_gate,
                                    float *dw_up, int32_t accumulate,
                                    int32_t *status_word, moe_stream_t stream);
-moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg,
+moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg, int32_t n_groups,
+                                const int32_t *group_expert,
                                 const moe_row_segment_t *segments,
                                 int32_t n_segments, int64_t rows_total,
                                 const void *h, const void *dy_sorted,
@@ -500,10 +513,13 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg,
  * expert and whole K=16 steps.  Copies x_sorted [.,H], dg, du, h [.,F] and
  * dy_sorted [.,H] (layer dtype) into the *_out buffers of rows_out rows;
  * out_offsets (device, [E+1]) receives the new group offsets.  rows_out
- * must be at least T*k + 16*E (cfg->T: the tokens of all ranges together);
+ * must be at least T*k + 16*(E + S*redundant_slots) (cfg->T: the tokens
+ * of all ranges together);
  * 1 <= n_segments <= 64.  The source ranges must lie inside the source
- * buffers; a row of the output that no range fills is zero. */
-moe_status_t moe_regroup_rows(const moe_config_t *cfg,
+ * buffers; a row of the output that no range fills is zero.  n_groups: the
+ * groups of the ranges' offsets (0: E; else the virtual groups of
+ * moe_plan_duplication, E + S*redundant_slots). */
+moe_status_t moe_regroup_rows(const moe_config_t *cfg, int32_t n_groups,
                               const moe_row_segment_t *segments,
                               int32_t n_segments, int64_t rows_out,
                               const void *x_sorted, const void *dg,

@@ -109,16 +109,19 @@ def _declare(h):
         "moe_gmm_swiglu_saved": [cfg, P, P, P, P, P, P, P, P, P, P, P],
         "moe_gmm_swiglu_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, P,
                                     P, c_int32, P, P, c_size_t, P],
-        "moe_gmm_gate_up_saved": [cfg, P, P, P, P, P, P, P, P, P],
-        "moe_gmm_down_dgrad": [cfg, P, P, P, P, P, P, P, P, P],
-        "moe_gmm_gate_up_dgrad": [cfg, P, P, P, P, P, P, P, P],
-        "moe_gmm_gate_up_wgrad": [cfg, ctypes.POINTER(MoeRowSegment),
-                                  c_int32, c_int64, P, P, P, P, P, c_int32,
-                                  P, P],
-        "moe_gmm_down_wgrad": [cfg, ctypes.POINTER(MoeRowSegment), c_int32,
+        "moe_gmm_gate_up_saved": [cfg, c_int32, P, P, P, P, P, P, P, P, P,
+                                  P],
+        "moe_gmm_down_dgrad": [cfg, c_int32, P, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_gate_up_dgrad": [cfg, c_int32, P, P, P, P, P, P, P, P, P],
+        "moe_gmm_gate_up_wgrad": [cfg, c_int32, P,
+                                  ctypes.POINTER(MoeRowSegment), c_int32,
+                                  c_int64, P, P, P, P, P, c_int32, P, P],
+        "moe_gmm_down_wgrad": [cfg, c_int32, P,
+                               ctypes.POINTER(MoeRowSegment), c_int32,
                                c_int64, P, P, P, c_int32, P, P],
-        "moe_regroup_rows": [cfg, ctypes.POINTER(MoeRowSegment), c_int32,
-                             c_int64, P, P, P, P, P, P, P, P, P, P, P, P],
+        "moe_regroup_rows": [cfg, c_int32, ctypes.POINTER(MoeRowSegment),
+                             c_int32, c_int64, P, P, P, P, P, P, P, P, P, P,
+                             P, P],
         "moe_layer_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, c_int,
                                ctypes.POINTER(MoeLayerInfo), P, P, c_size_t,
                                P],
@@ -386,25 +389,28 @@ def moe_gmm_swiglu_backward(cfg, x_sorted, group_offsets, w_gate, w_up,
 
 
 def moe_gmm_gate_up_saved(cfg, x_sorted, group_offsets, w_gate, w_up, g, u,
-                          h, status_word=None, stream=None):
+                          h, status_word=None, stream=None, n_groups=0,
+                          group_expert=None):
     _check(lib().moe_gmm_gate_up_saved(
-        ctypes.byref(cfg), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(x_sorted), _ptr(group_offsets), _ptr(w_gate),
         _ptr(w_up), _ptr(g), _ptr(u), _ptr(h), _ptr(status_word),
         _stream(stream)), "moe_gmm_gate_up_saved")
 
 
 def moe_gmm_down_dgrad(cfg, group_offsets, w_down, g, u, dy_sorted, dg, du,
-                       status_word=None, stream=None):
+                       status_word=None, stream=None, n_groups=0,
+                       group_expert=None):
     _check(lib().moe_gmm_down_dgrad(
-        ctypes.byref(cfg), _ptr(group_offsets), _ptr(w_down), _ptr(g),
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(group_offsets), _ptr(w_down), _ptr(g),
         _ptr(u), _ptr(dy_sorted), _ptr(dg), _ptr(du), _ptr(status_word),
         _stream(stream)), "moe_gmm_down_dgrad")
 
 
 def moe_gmm_gate_up_dgrad(cfg, group_offsets, w_gate, w_up, dg, du,
-                          dx_sorted, status_word=None, stream=None):
+                          dx_sorted, status_word=None, stream=None,
+                          n_groups=0, group_expert=None):
     _check(lib().moe_gmm_gate_up_dgrad(
-        ctypes.byref(cfg), _ptr(group_offsets), _ptr(w_gate), _ptr(w_up),
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(group_offsets), _ptr(w_gate), _ptr(w_up),
         _ptr(dg), _ptr(du), _ptr(dx_sorted), _ptr(status_word),
         _stream(stream)), "moe_gmm_gate_up_dgrad")
 
@@ -420,18 +426,19 @@ def _segments(segments):
 
 def moe_gmm_gate_up_wgrad(cfg, segments, rows_total, x_sorted, dg, du,
                           dw_gate, dw_up, accumulate, status_word=None,
-                          stream=None):
+                          stream=None, n_groups=0, group_expert=None):
     _check(lib().moe_gmm_gate_up_wgrad(
-        ctypes.byref(cfg), _segments(segments), len(segments),
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _segments(segments), len(segments),
         int(rows_total), _ptr(x_sorted), _ptr(dg), _ptr(du), _ptr(dw_gate),
         _ptr(dw_up), int(accumulate), _ptr(status_word), _stream(stream)),
         "moe_gmm_gate_up_wgrad")
 
 
 def moe_gmm_down_wgrad(cfg, segments, rows_total, h, dy_sorted, dw_down,
-                       accumulate, status_word=None, stream=None):
+                       accumulate, status_word=None, stream=None, n_groups=0,
+                       group_expert=None):
     _check(lib().moe_gmm_down_wgrad(
-        ctypes.byref(cfg), _segments(segments), len(segments),
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _segments(segments), len(segments),
         int(rows_total), _ptr(h), _ptr(dy_sorted), _ptr(dw_down),
         int(accumulate), _ptr(status_word), _stream(stream)),
         "moe_gmm_down_wgrad")
@@ -439,9 +446,9 @@ def moe_gmm_down_wgrad(cfg, segments, rows_total, h, dy_sorted, dw_down,
 
 def moe_regroup_rows(cfg, segments, rows_out, x_sorted, dg, du, h,
                      dy_sorted, x_out, dg_out, du_out, h_out, dy_out,
-                     out_offsets, stream=None):
+                     out_offsets, stream=None, n_groups=0):
     _check(lib().moe_regroup_rows(
-        ctypes.byref(cfg), _segments(segments), len(segments), int(rows_out),
+        ctypes.byref(cfg), n_groups, _segments(segments), len(segments), int(rows_out),
         _ptr(x_sorted), _ptr(dg), _ptr(du), _ptr(h), _ptr(dy_sorted),
         _ptr(x_out), _ptr(dg_out), _ptr(du_out), _ptr(h_out), _ptr(dy_out),
         _ptr(out_offsets), _stream(stream)), "moe_regroup_rows")

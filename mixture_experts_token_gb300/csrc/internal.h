@@ -230,9 +230,11 @@ cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
 // destination buffers of regroup_rows(c) rows.
 constexpr int kMaxRegroupSegments = 64;
 inline int64_t regroup_rows(const moe_config_t& c) {
-  return static_cast<int64_t>(c.T) * c.k + 16 * static_cast<int64_t>(c.E);
+  return static_cast<int64_t>(c.T) * c.k +
+         16 * static_cast<int64_t>(num_groups(c));
 }
-cudaError_t launch_regroup(const moe_config_t& c, const WgradSegment* seg,
+cudaError_t launch_regroup(const moe_config_t& c, int G,
+                           const WgradSegment* seg,
                            int n_seg, int64_t rows_out, const void* xs,
                            const void* dg, const void* du, const void* h,
                            const void* dys, void* xs2, void* dg2, void* du2,

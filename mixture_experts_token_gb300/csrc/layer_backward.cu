@@ -32,10 +32,10 @@ struct BwdBufs {
   void *g, *u, *dg, *du;  // [T*k, F]
   void *dys, *dxs;        // [T*k, H]
   float* dtw;             // [T, k]
-  int32_t* seg_off;       // [n_seg, E + 1] group offsets of every pass
+  int32_t* seg_off;       // [n_seg, G + 1] group offsets of every pass
   // the passes' rows regrouped for the weight gradients (regroup.cu)
   void *xs2, *dg2, *du2, *h2, *dys2;  // [T*k + 16*E, H or F]
-  int32_t* off2;                      // [E + 1]
+  int32_t* off2;                      // [G + 1]
 };
 
 int max_passes(const moe_config_t& c, moe_mode_t mode) {
@@ -59,14 +59,15 @@ BwdBufs carve_bwd(void* base, const moe_config_t& c, int n_seg,
   b.dys = cv.take<char>(rows * c.H * eb);
   b.dxs = cv.take<char>(rows * c.H * eb);
   b.dtw = cv.take<float>(rows);
-  b.seg_off = cv.take<int32_t>(static_cast<size_t>(n_seg) * (c.E + 1));
+  b.seg_off =
+      cv.take<int32_t>(static_cast<size_t>(n_seg) * (num_groups(c) + 1));
   const size_t rr = static_cast<size_t>(regroup_rows(c));
   b.xs2 = cv.take<char>(rr * c.H * eb);
   b.dys2 = cv.take<char>(rr * c.H * eb);
   b.dg2 = cv.take<char>(rr * c.F * eb);
   b.du2 = cv.take<char>(rr * c.F * eb);
   b.h2 = cv.take<char>(rr * c.F * eb);
-  b.off2 = cv.take<int32_t>(c.E + 1);
+  b.off2 = cv.take<int32_t>(num_groups(c) + 1);
   if (bytes) *bytes = fb + align_up(cv.off, 256);
   return b;
 }
@@ -78,22 +79,30 @@ void* rows_at(const void* p, size_t row, size_t row_bytes) {
 // Backward of one pass over tokens [t0, t0 + tc) with capacity cap (-1:
 // uncapped), all but the weight gradients.  Its rows occupy
 // [t0*k, (t0+tc)*k) of the row buffers and its group offsets row `seg` of
-// the segment table.
+// the segment table.  planned: over the virtual groups of the duplication
+// plan in b (each computing with its expert's weights).
 cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
-                     int seg, const void* x, const void* wg, const void* wu,
-                     const void* wd, const void* dy, void* dx,
+                     bool planned, int seg, const void* x, const void* wg,
+                     const void* wu, const void* wd, const void* dy, void* dx,
                      const BwdBufs& b, int32_t* status, cudaStream_t s) {
   moe_config_t sc = c;
   sc.T = tc;
   const size_t eb = elem_bytes(c.dtype);
   const size_t hb = c.H * eb, fb = c.F * eb;
   const size_t base = static_cast<size_t>(t0) * c.k;
-  const Groups ids = identity_groups(sc);
+  PermutePlan plan;
+  Groups ids = identity_groups(sc);
+  if (planned) {
+    plan.divert = b.f.divert;
+    plan.slot_of = b.f.slot_of;
+    plan.B = c.redundant_slots;
+    ids = {num_groups(c), b.f.group_expert};
+  }
   const void* xc = rows_at(x, t0, hb);
   const int32_t* idx = b.f.topk_idx + base;
   const float* w = b.f.topk_w + base;
   int32_t* row_of = b.f.row_of + base;
-  int32_t* goff = b.seg_off + static_cast<size_t>(seg) * (c.E + 1);
+  int32_t* goff = b.seg_off + static_cast<size_t>(seg) * (num_groups(c) + 1);
   void* xs = rows_at(b.f.x_sorted, base, hb);
   void* h = rows_at(b.f.h, base, fb);
   void* ys = rows_at(b.f.y_sorted, base, hb);
@@ -106,7 +115,7 @@ cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
   cudaError_t e = launch_permute(
       sc, xc, idx, cap, xs, row_of, b.f.sorted_token + base, goff,
       b.f.uniq_offsets, b.f.uniq_tokens, b.f.expand_idx + base, b.f.n_dropped,
-      b.f.pws, status, s);
+      b.f.pws, status, s, plan);
   if (e != cudaSuccess) return e;
   if ((e = launch_gate_up_saved(sc, ids, xs, goff, wg, wu, gg, uu, h, status,
                                 s)) != cudaSuccess ||
@@ -305,7 +314,22 @@ moe_status_t moe_gmm_swiglu_backward(
                               stream));
 }
 
-moe_status_t moe_gmm_gate_up_saved(const moe_config_t* cfg,
+namespace {
+// n_groups = 0 with a null map: the experts' own groups.
+bool bwd_groups(const moe_config_t& c, int32_t n, const int32_t* map,
+                Groups* g) {
+  if (n == 0 && map == nullptr) {
+    *g = identity_groups(c);
+    return true;
+  }
+  if (n < 1 || n > kMaxExperts || !ok_ptr(map, false)) return false;
+  *g = {n, map};
+  return true;
+}
+}  // namespace
+
+moe_status_t moe_gmm_gate_up_saved(const moe_config_t* cfg, int32_t n_groups,
+                                   const int32_t* group_expert,
                                    const void* x_sorted,
                                    const int32_t* group_offsets,
                                    const void* w_gate, const void* w_up,
@@ -316,16 +340,19 @@ moe_status_t moe_gmm_gate_up_saved(const moe_config_t* cfg,
   if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
-  if (!ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(x_sorted, true) || !ok_ptr(group_offsets, false) ||
       !ok_ptr(w_gate, true) || !ok_ptr(w_up, true) || !ok_ptr(g, true) ||
       !ok_ptr(u, true) || !ok_ptr(h, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_gate_up_saved(*cfg, identity_groups(*cfg), x_sorted,
+  return cuda_st(launch_gate_up_saved(*cfg, grp, x_sorted,
                                       group_offsets, w_gate, w_up, g, u, h,
                                       status_word, stream));
 }
 
-moe_status_t moe_gmm_down_dgrad(const moe_config_t* cfg,
+moe_status_t moe_gmm_down_dgrad(const moe_config_t* cfg, int32_t n_groups,
+                                const int32_t* group_expert,
                                 const int32_t* group_offsets,
                                 const void* w_down, const void* g,
                                 const void* u, const void* dy_sorted,
@@ -336,16 +363,19 @@ moe_status_t moe_gmm_down_dgrad(const moe_config_t* cfg,
   if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
-  if (!ok_ptr(group_offsets, false) || !ok_ptr(w_down, true) ||
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(group_offsets, false) || !ok_ptr(w_down, true) ||
       !ok_ptr(g, true) || !ok_ptr(u, true) || !ok_ptr(dy_sorted, true) ||
       !ok_ptr(dg, true) || !ok_ptr(du, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_down_dgrad(*cfg, identity_groups(*cfg), group_offsets,
+  return cuda_st(launch_down_dgrad(*cfg, grp, group_offsets,
                                    w_down, g, u, dy_sorted, dg, du,
                                    status_word, stream));
 }
 
-moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t* cfg,
+moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t* cfg, int32_t n_groups,
+                                   const int32_t* group_expert,
                                    const int32_t* group_offsets,
                                    const void* w_gate, const void* w_up,
                                    const void* dg, const void* du,
@@ -356,11 +386,13 @@ moe_status_t moe_gmm_gate_up_dgrad(const moe_config_t* cfg,
   if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
-  if (!ok_ptr(group_offsets, false) || !ok_ptr(w_gate, true) ||
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(group_offsets, false) || !ok_ptr(w_gate, true) ||
       !ok_ptr(w_up, true) || !ok_ptr(dg, true) || !ok_ptr(du, true) ||
       !ok_ptr(dx_sorted, true))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_gate_up_dgrad(*cfg, identity_groups(*cfg),
+  return cuda_st(launch_gate_up_dgrad(*cfg, grp,
                                       group_offsets, w_gate, w_up, dg, du,
                                       dx_sorted, status_word, stream));
 }
@@ -386,7 +418,8 @@ moe_status_t check_segments(const moe_config_t* cfg,
 }
 }  // namespace
 
-moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t* cfg,
+moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t* cfg, int32_t n_groups,
+                                   const int32_t* group_expert,
                                    const moe_row_segment_t* segments,
                                    int32_t n_segments, int64_t rows_total,
                                    const void* x_sorted, const void* dg,
@@ -396,17 +429,20 @@ moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t* cfg,
   moe_status_t st =
       check_segments(cfg, segments, n_segments, rows_total, accumulate);
   if (st != MOE_OK) return st;
-  if (!ok_ptr(dw_gate, true) || !ok_ptr(dw_up, true) ||
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(dw_gate, true) || !ok_ptr(dw_up, true) ||
       (n_segments > 0 &&
        (!ok_ptr(x_sorted, true) || !ok_ptr(dg, true) || !ok_ptr(du, true))))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), segments,
+  return cuda_st(launch_wgrad(*cfg, grp, segments,
                               n_segments, rows_total, x_sorted, dg, du,
                               nullptr, nullptr, dw_gate, dw_up, nullptr,
                               accumulate, kWgradGateUp, status_word, stream));
 }
 
-moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg,
+moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg, int32_t n_groups,
+                                const int32_t* group_expert,
                                 const moe_row_segment_t* segments,
                                 int32_t n_segments, int64_t rows_total,
                                 const void* h, const void* dy_sorted,
@@ -415,17 +451,19 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg,
   moe_status_t st =
       check_segments(cfg, segments, n_segments, rows_total, accumulate);
   if (st != MOE_OK) return st;
-  if (!ok_ptr(dw_down, true) ||
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(dw_down, true) ||
       (n_segments > 0 && (!ok_ptr(h, true) || !ok_ptr(dy_sorted, true))))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), segments,
+  return cuda_st(launch_wgrad(*cfg, grp, segments,
                               n_segments, rows_total, nullptr, nullptr,
                               nullptr, h, dy_sorted, nullptr, nullptr,
                               dw_down, accumulate, kWgradDown, status_word,
                               stream));
 }
 
-moe_status_t moe_regroup_rows(const moe_config_t* cfg,
+moe_status_t moe_regroup_rows(const moe_config_t* cfg, int32_t n_groups,
                               const moe_row_segment_t* segments,
                               int32_t n_segments, int64_t rows_out,
                               const void* x_sorted, const void* dg,
@@ -436,8 +474,10 @@ moe_status_t moe_regroup_rows(const moe_config_t* cfg,
                               moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
+  const int G = n_groups == 0 ? cfg->E : n_groups;
   if (cfg->F < 1 || n_segments < 1 || n_segments > kMaxRegroupSegments ||
-      segments == nullptr || rows_out < regroup_rows(*cfg) ||
+      n_groups < 0 || G > num_groups(*cfg) || segments == nullptr ||
+      rows_out < regroup_rows(*cfg) ||
       rows_out > std::numeric_limits<int32_t>::max())
     return MOE_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n_segments; ++i)
@@ -449,7 +489,7 @@ moe_status_t moe_regroup_rows(const moe_config_t* cfg,
       !ok_ptr(dg_out, true) || !ok_ptr(du_out, true) || !ok_ptr(h_out, true) ||
       !ok_ptr(dy_out, true) || !ok_ptr(out_offsets, false))
     return MOE_ERR_INVALID_ARG;
-  return cuda_st(launch_regroup(*cfg, segments, n_segments, rows_out,
+  return cuda_st(launch_regroup(*cfg, G, segments, n_segments, rows_out,
                                 x_sorted, dg, du, h, dy_sorted, x_out, dg_out,
                                 du_out, h_out, dy_out, out_offsets, stream));
 }
@@ -468,7 +508,6 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
       mode != MOE_MODE_DROPLESS)
     return MOE_ERR_INVALID_ARG;
   if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
-  if (cfg->redundant_slots != 0) return MOE_ERR_UNSUPPORTED;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (!weights_ok(w_gate, w_up, w_down) || !ok_ptr(dw_gate, true) ||
       !ok_ptr(dw_up, true) || !ok_ptr(dw_down, true))
@@ -500,43 +539,65 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
   cudaError_t e = launch_route(*cfg, logits, b.f.topk_idx, b.f.topk_w,
                                status_word, stream);
   if (e != cudaSuccess) return cuda_st(e);
-  // the passes: (t0, tokens, capacity)
+  // the passes: (t0, tokens, capacity, over the plan's virtual groups)
   struct Pass {
     int t0, tc;
     int64_t cap;
+    bool planned;
   };
-  std::vector<Pass> passes;
-  if (mode == MOE_MODE_DROPLESS) {
-    passes.push_back({0, cfg->T, -1});
-  } else if (mode == MOE_MODE_CAPPED) {
-    passes.push_back({0, cfg->T, cap});
-  } else {
+  // duplicate-expert slots: as moe_layer, the plan is made after the check
+  // and the capped pass runs over its virtual groups; the chunked fallback
+  // runs plain
+  const bool planned = cfg->redundant_slots > 0 && mode != MOE_MODE_DROPLESS;
+  if (planned) {
     e = launch_check(*cfg, b.f.topk_idx, b.f.counts, b.f.offsets, b.f.shard,
                      b.f.flag, b.f.req, b.f.cap, stream);
+    if (e == cudaSuccess)
+      e = launch_plan(*cfg, b.f.counts, b.f.divert, b.f.slot_of,
+                      b.f.group_expert, b.f.shard_after, b.f.flag_after,
+                      stream);
     if (e != cudaSuccess) return cuda_st(e);
+  }
+  std::vector<Pass> passes;
+  if (mode == MOE_MODE_DROPLESS) {
+    passes.push_back({0, cfg->T, -1, false});
+  } else if (mode == MOE_MODE_CAPPED) {
+    passes.push_back({0, cfg->T, cap, planned});
+  } else {
+    if (!planned) {
+      e = launch_check(*cfg, b.f.topk_idx, b.f.counts, b.f.offsets,
+                       b.f.shard, b.f.flag, b.f.req, b.f.cap, stream);
+      if (e != cudaSuccess) return cuda_st(e);
+    }
     int32_t flag = 0;
-    e = cudaMemcpyAsync(&flag, b.f.flag, sizeof(flag), cudaMemcpyDeviceToHost,
-                        stream);
+    e = cudaMemcpyAsync(&flag, planned ? b.f.flag_after : b.f.flag,
+                        sizeof(flag), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_st(e);
     if (info) info->overflow = flag;
     if (!flag) {
-      passes.push_back({0, cfg->T, cap});
+      passes.push_back({0, cfg->T, cap, planned});
     } else {
       const int ct = chunk_tokens(*cfg);
       for (int t0 = 0; t0 < cfg->T; t0 += ct)
-        passes.push_back({t0, std::min(ct, cfg->T - t0), -1});
+        passes.push_back({t0, std::min(ct, cfg->T - t0), -1, false});
       if (info) info->n_chunks = static_cast<int32_t>(passes.size());
     }
   }
   std::vector<WgradSegment> segs;
+  const size_t G1 = static_cast<size_t>(num_groups(*cfg)) + 1;
   for (size_t i = 0; i < passes.size(); ++i) {
     const Pass& p = passes[i];
-    e = bwd_pass(*cfg, p.t0, p.tc, p.cap, static_cast<int>(i), x, w_gate,
-                 w_up, w_down, dy, dx, b, status_word, stream);
+    e = bwd_pass(*cfg, p.t0, p.tc, p.cap, p.planned, static_cast<int>(i), x,
+                 w_gate, w_up, w_down, dy, dx, b, status_word, stream);
     if (e != cudaSuccess) return cuda_st(e);
-    segs.push_back({b.seg_off + i * (cfg->E + 1), p.t0 * cfg->k});
+    segs.push_back({b.seg_off + i * G1, p.t0 * cfg->k});
   }
+  // the weight gradients' groups: the plan's virtual groups (a duplicate's
+  // rows add into its expert's gradient) or the experts themselves
+  const Groups wgroups = passes[0].planned
+                             ? Groups{num_groups(*cfg), b.f.group_expert}
+                             : identity_groups(*cfg);
   e = launch_route_backward(*cfg, logits, b.f.topk_idx, b.dtw, dlogits,
                             stream);
   if (e != cudaSuccess) return cuda_st(e);
@@ -544,18 +605,19 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
       segs.size() <= static_cast<size_t>(kMaxRegroupSegments)) {
     // one 16-row-aligned row range per expert for the tensor-core GEMMs
     const int64_t rr = regroup_rows(*cfg);
-    e = launch_regroup(*cfg, segs.data(), static_cast<int>(segs.size()), rr,
-                       b.f.x_sorted, b.dg, b.du, b.f.h, b.dys, b.xs2, b.dg2,
-                       b.du2, b.h2, b.dys2, b.off2, stream);
+    e = launch_regroup(*cfg, wgroups.n, segs.data(),
+                       static_cast<int>(segs.size()), rr, b.f.x_sorted, b.dg,
+                       b.du, b.f.h, b.dys, b.xs2, b.dg2, b.du2, b.h2, b.dys2,
+                       b.off2, stream);
     if (e != cudaSuccess) return cuda_st(e);
     const WgradSegment one{b.off2, 0};
-    return cuda_st(launch_wgrad(*cfg, identity_groups(*cfg), &one, 1, rr,
+    return cuda_st(launch_wgrad(*cfg, wgroups, &one, 1, rr,
                                 b.xs2, b.dg2, b.du2, b.h2, b.dys2, dw_gate,
                                 dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
                                 status_word, stream));
   }
   return cuda_st(launch_wgrad(
-      *cfg, identity_groups(*cfg), segs.data(), static_cast<int>(segs.size()),
+      *cfg, wgroups, segs.data(), static_cast<int>(segs.size()),
       static_cast<int64_t>(cfg->T) * cfg->k, b.f.x_sorted, b.dg, b.du, b.f.h,
       b.dys, dw_gate, dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
       status_word, stream));

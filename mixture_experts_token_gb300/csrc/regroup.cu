@@ -3,7 +3,7 @@
 // The layer backward leaves every pass's rows in its own row range (one
 // range per chunk of the fallback).  The weight gradient of expert e sums
 // over its rows of every pass.  This copies x_sorted, dg, du, h and
-// dy_sorted into one expert-major layout: group g holds the rows of every
+// dy_sorted into one group-major layout: group g holds the rows of every
 // range in range order, starts on a 16-row boundary, and its pad rows up to
 // the next boundary are zero.  The weight-gradient GEMM then sees one row
 // range per expert, and every block of it is a whole number of K=16 steps
@@ -115,13 +115,15 @@ __global__ void __launch_bounds__(256) regroup_rows_kernel(
 
 }  // namespace
 
-cudaError_t launch_regroup(const moe_config_t& c, const WgradSegment* seg,
-                           int n_seg, int64_t rows_out, const void* xs,
+cudaError_t launch_regroup(const moe_config_t& c, int G,
+                           const WgradSegment* seg, int n_seg,
+                           int64_t rows_out, const void* xs,
                            const void* dg, const void* du, const void* h,
                            const void* dys, void* xs2, void* dg2, void* du2,
                            void* h2, void* dys2, int32_t* out_off,
                            cudaStream_t s) {
-  if (n_seg < 1 || n_seg > kMaxRegroupSegments || c.E > kRegroupThreads)
+  if (n_seg < 1 || n_seg > kMaxRegroupSegments || G < 1 ||
+      G > kRegroupThreads)
     return cudaErrorInvalidValue;
   RegroupParams p{};
   for (int i = 0; i < n_seg; ++i) {
@@ -129,7 +131,7 @@ cudaError_t launch_regroup(const moe_config_t& c, const WgradSegment* seg,
     p.base[i] = seg[i].first_row;
   }
   p.n_seg = n_seg;
-  p.G = c.E;
+  p.G = G;
   regroup_offsets_kernel<<<1, kRegroupThreads, 0, s>>>(p, out_off);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

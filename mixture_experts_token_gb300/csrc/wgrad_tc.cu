@@ -46,7 +46,10 @@ struct WParams {
   int G;
   int m_tiles;   // 128-row tiles of one expert's dW
   int n_tiles;   // column tiles
-  int reduce;    // 1: TMA reduce-add, 0: TMA store
+  int reduce;    // 1: TMA reduce-add everywhere; 0: TMA store, except
+                 // for experts with several groups (duplicates), whose
+                 // tiles add onto a slice zeroed beforehand
+  int E;         // experts (dW slices)
   int32_t* status;
 };
 
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
   int* tpre = wsum + 16;                               // [G+1]
+  int* ecnt = tpre + (p.G + 1);                        // [E] groups w/ rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -213,6 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   build_wgrad_table(p, tpre, wsum);
+  // groups with rows per expert: an expert with one writes its dW with
+  // plain stores, one with several (a duplicated expert) adds each group's
+  // tile onto its zeroed slice
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) ecnt[e] = 0;
+  __syncthreads();
+  if (p.group_expert != nullptr)
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x)
+      if (tpre[g + 1] > tpre[g]) atomicAdd(&ecnt[__ldg(p.group_expert + g)], 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -366,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       const int orow = we * p.m_tiles * BM + m * BM + q * 32;
+      const bool add = p.reduce || (p.group_expert != nullptr && ecnt[we] > 1);
 #pragma unroll 1
       for (int sub = 0; sub < BN / 32; ++sub, ++nsub) {
         uint32_t r[32];
@@ -387,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             om = sub < 4 ? &tmO0 : &tmO1;
             col = n * 128 + (sub & 3) * 32;
           }
-          if (p.reduce)
+          if (add)
             tma_reduce_add_2d(om, smem_u32(buf), col, orow, stream);
           else
             tma_store_2d(om, smem_u32(buf), col, orow, stream);
@@ -410,15 +423,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Zeroes dW[e] of every expert without rows in any segment (store mode:
-// no tile writes it).  Grid (G, blocks), 16-byte stores.
-__global__ void zero_empty_kernel(WParams p, float* a, float* b,
-                                  long long per_expert) {
-  const int g = blockIdx.x;
-  if (wgrad_rows(p, g) > 0) return;
+// Store mode: zeroes dW[e] of every expert that does not have exactly one
+// group with rows -- none (no tile writes it) or several (its tiles add onto
+// it).  Grid (E, blocks), 16-byte stores.
+__global__ void zero_experts_kernel(WParams p, float* a, float* b,
+                                    long long per_expert) {
+  const int e = blockIdx.x;
+  int n = 0;
+  if (p.group_expert == nullptr) {
+    n = wgrad_rows(p, e) > 0 ? 1 : 0;
+  } else {
+    for (int g = 0; g < p.G; ++g)
+      if (__ldg(p.group_expert + g) == e && wgrad_rows(p, g) > 0) ++n;
+  }
+  if (n == 1) return;
   const long long n4 = per_expert / 4;
-  float4* pa = reinterpret_cast<float4*>(a + g * per_expert);
-  float4* pb = b ? reinterpret_cast<float4*>(b + g * per_expert) : nullptr;
+  float4* pa = reinterpret_cast<float4*>(a + e * per_expert);
+  float4* pb = b ? reinterpret_cast<float4*>(b + e * per_expert) : nullptr;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long long i = blockIdx.y * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.y) * blockDim.x) {
@@ -427,9 +448,9 @@ __global__ void zero_empty_kernel(WParams p, float* a, float* b,
   }
 }
 
-size_t smem_bytes_wgrad(int G) {
+size_t smem_bytes_wgrad(int G, int E) {
   return 1024 + WSTAGES * kWStage + 8 * kStageBuf + 8 * (2 * WSTAGES + 5) +
-         16 + 4 * (16 + G + 1) + 64;
+         16 + 4 * (16 + G + 1 + E) + 64;
 }
 
 template <int WMODE, int BN>
@@ -437,7 +458,7 @@ cudaError_t launch_wgrad(const CUtensorMap& pm, const CUtensorMap& q0,
                          const CUtensorMap& q1, const CUtensorMap& o0,
                          const CUtensorMap& o1, const WParams& p,
                          cudaStream_t s) {
-  const size_t smem = smem_bytes_wgrad(p.G);
+  const size_t smem = smem_bytes_wgrad(p.G, p.E);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -469,15 +490,7 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
   const uint64_t E = static_cast<uint64_t>(c.E);
   const uint64_t rows = static_cast<uint64_t>(std::max<int64_t>(rows_total, 1));
   const long long per_expert = static_cast<long long>(c.H) * c.F;
-  const bool mapped = g.map != nullptr;
   cudaError_t e = cudaSuccess;
-  if (!accumulate && mapped) {  // duplicates reduce into one expert
-    const size_t bytes = static_cast<size_t>(E) * per_expert * sizeof(float);
-    if ((gu && (e = cudaMemsetAsync(dw_gate, 0, bytes, s)) != cudaSuccess) ||
-        (gu && (e = cudaMemsetAsync(dw_up, 0, bytes, s)) != cudaSuccess) ||
-        (dn && (e = cudaMemsetAsync(dw_down, 0, bytes, s)) != cudaSuccess))
-      return e;
-  }
   const int bnd = c.H % 256 == 0 ? 256 : 128;
   CUtensorMap px, qg, qu, og, ou, ph, qd, od;
   if (gu && (!tc::make_map(&px, x_sorted, c.H, rows, 64, 64) ||
@@ -499,17 +512,19 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
     }
     p.group_expert = g.map;
     p.G = g.n;
-    p.reduce = (accumulate || mapped || s0 > 0) ? 1 : 0;
+    p.E = c.E;
+    p.reduce = (accumulate || s0 > 0) ? 1 : 0;
     p.status = status;
     if (!p.reduce) {
-      // experts without rows: no tile writes their dW
-      const dim3 grid(static_cast<unsigned>(g.n), 16);
+      // experts without rows (no tile writes their dW) and duplicated
+      // experts (their groups' tiles add onto it) start from zeros
+      const dim3 grid(static_cast<unsigned>(c.E), 16);
       if (gu)
-        tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_gate, dw_up,
-                                                   per_expert);
+        tc::zero_experts_kernel<<<grid, 256, 0, s>>>(p, dw_gate, dw_up,
+                                                     per_expert);
       if (dn)
-        tc::zero_empty_kernel<<<grid, 256, 0, s>>>(p, dw_down, nullptr,
-                                                   per_expert);
+        tc::zero_experts_kernel<<<grid, 256, 0, s>>>(p, dw_down, nullptr,
+                                                     per_expert);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (p.n_seg == 0) break;

@@ -172,26 +172,27 @@ def test_backward_arguments_are_rejected_before_any_launch(m):
     # regrouping: no ranges, too many ranges, an output too small
     args = (p, p, p, p, p, p, p, p, p, p, p)
     rows = c.T * c.k + 16 * c.E
-    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 0, rows, *args,
+    assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 0, rows, *args,
                                 None) == m.MOE_ERR_INVALID_ARG
-    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 65, rows, *args,
+    assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 65, rows, *args,
                                 None) == m.MOE_ERR_INVALID_ARG
-    assert lib.moe_regroup_rows(ctypes.byref(c), seg, 1, rows - 1, *args,
+    assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 1, rows - 1, *args,
                                 None) == m.MOE_ERR_INVALID_ARG
+    # a group count beyond the configuration's groups
+    assert lib.moe_regroup_rows(ctypes.byref(c), c.E + 1, seg, 1, rows,
+                                *args, None) == m.MOE_ERR_INVALID_ARG
+    # a group map without its group count
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, p, seg, 1, rows, p, p,
+                                  p, 0, None, None) == m.MOE_ERR_INVALID_ARG
     # weight gradients: a negative range start, accumulate not 0/1
     seg[0].first_row = -1
-    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), seg, 1, rows, p, p, p, 0,
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 0,
                                   None, None) == m.MOE_ERR_INVALID_ARG
     seg[0].first_row = 0
-    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), seg, 1, rows, p, p, p, 2,
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 2,
                                   None, None) == m.MOE_ERR_INVALID_ARG
-    # layer backward: duplicate slots are not covered; no workspace
-    c2 = cfg_of(m, H=128)
-    c2.redundant_slots = 1
+    # layer backward: no workspace
     info = m.MoeLayerInfo()
-    assert lib.moe_layer_backward(ctypes.byref(c2), p, p, p, p, p, p, p, p, p,
-                                  p, p, 0, ctypes.byref(info), None, p, 1 << 40,
-                                  None) == m.MOE_ERR_UNSUPPORTED
     assert lib.moe_layer_backward(ctypes.byref(c), p, p, p, p, p, p, p, p, p,
                                   p, p, 0, ctypes.byref(info), None, None, 0,
                                   None) == m.MOE_ERR_WORKSPACE

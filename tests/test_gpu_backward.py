@@ -312,3 +312,58 @@ def test_regroup_rows_layout():
                 assert torch.equal(o_[g0:g0 + len(rows)], s_[rows]), (name, e)
             pad = o_[g0 + len(rows):int(want_off[e + 1])]
             assert torch.count_nonzero(pad.float()).item() == 0, (name, e)
+
+
+RED = [
+    # bf16, skewed toward shard 0 so the plan diverts rows into slots
+    WORKLOADS["small"].with_(name="red_a", T=1200, H=256, E=16, k=2, F=256,
+                             S=4, zipf_s=1.2),
+    # fp32 tiny layer (CUDA-core path), routed by x Wr
+    WORKLOADS["tiny"].with_(name="red_tiny"),
+]
+
+
+@pytest.mark.parametrize("B,factor", [(1, 2.0), (2, 2.0), (2, 0.6)],
+                         ids=["B1_f2", "B2_f2", "B2_f06"])
+@pytest.mark.parametrize("wl", RED, ids=lambda w: w.name)
+def test_layer_backward_redundant_fallback(wl, B, factor):
+    """fallback=layer with duplicate-expert slots: plan, reroute, check on
+    the diverted loads; the capped pass over the virtual groups (a slot's
+    rows add into its expert's weight gradient) or the plain chunks."""
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=factor, redundant_slots=B)
+    out, info = gpu_layer_backward(cfg, x, L, W, dy,
+                                   moe.MOE_MODE_FALLBACK_LAYER)
+    mc = oracle_cfg(wl, ragged_buffer_factor=factor)
+    idx, _, _ = ref.route(L, wl.k, wl.renorm)
+    plan = ref.plan_duplication(ref.expert_counts(idx, wl.E), wl.S, B)
+    vidx = ref.reroute(idx, plan, wl.E, wl.S)
+    G = wl.S * (wl.E // wl.S + B)
+    C = ref.capacity(wl.T, wl.k, wl.S, factor)
+    over = ref.overflow_flag(
+        ref.shard_counts(ref.expert_counts(vidx, G), wl.S), C)
+    assert info["overflow"] == int(over)
+    g = ref.layer_redundant_backward(mc, f64(x), L, *[f64(w) for w in W],
+                                     f64(dy), B)
+    compare(out, g, TOL[wl.dtype])
+
+
+@pytest.mark.parametrize("wl", RED, ids=lambda w: w.name)
+def test_layer_backward_redundant_capped(wl):
+    """Capped mode with slots: the capped pass over the plan's virtual
+    groups, drops included, against the oracle's pass over the same
+    groups."""
+    B, factor = 1, 0.7
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=factor, redundant_slots=B)
+    out, _ = gpu_layer_backward(cfg, x, L, W, dy, moe.MOE_MODE_CAPPED)
+    mc = oracle_cfg(wl, ragged_buffer_factor=factor)
+    idx, _, _ = ref.route(L, wl.k, wl.renorm)
+    plan = ref.plan_duplication(ref.expert_counts(idx, wl.E), wl.S, B)
+    vidx = ref.reroute(idx, plan, wl.E, wl.S)
+    G = wl.S * (wl.E // wl.S + B)
+    C = ref.capacity(wl.T, wl.k, wl.S, factor)
+    assert ref.permute_indices(vidx, G, wl.S, C).n_dropped > 0
+    g = ref.layer_pass_backward(mc, f64(x), L, *[f64(w) for w in W], f64(dy),
+                                C, groups=(vidx, G, plan.group_expert))
+    compare(out, g, TOL[wl.dtype])
