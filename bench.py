@@ -248,16 +248,19 @@ class Layer:
         return self.cfg.with_(T=t1 - t0, ragged_buffer_factor=-1.0,
                               n_chunks=0, redundant_slots=0)
 
-    def step(self, ev=None):
+    def step(self, ev=None, hold_cycles=0):
         """One layer step through the entry points; ev(name) marks stages.
-        Returns the list of passes (t0, t1, capped)."""
+        hold_cycles > 0 puts a GPU sleep of that many cycles (its own stage,
+        "hold") before the first pass, so that the host has queued the
+        pass's launches before the GPU reaches them.  Returns the list of
+        passes (t0, t1, capped)."""
         moe, b, c, W = self.moe, self.b, self.cfg, self.W
         mark = ev or (lambda name: None)
         mark("route")
         moe.moe_route(c, self.logits, b["topk_idx"], b["topk_w"], b["status"])
         if self.mode != "fallback":
             passes = [(0, c.T, self.mode == "capped")]
-            return self._passes(passes, mark)
+            return self._passes(passes, mark, hold_cycles)
         mark("check")
         moe.moe_check_overflow(c, b["topk_idx"], b["expert_counts"],
                                b["expert_offsets"], b["shard_counts"],
@@ -276,10 +279,13 @@ class Layer:
         else:
             passes = [(t0, min(c.T, t0 + self.chunk), False)
                       for t0 in range(0, c.T, self.chunk)]
-        return self._passes(passes, mark)
+        return self._passes(passes, mark, hold_cycles)
 
-    def _passes(self, passes, mark):
+    def _passes(self, passes, mark, hold_cycles=0):
         moe, b, W = self.moe, self.b, self.W
+        if hold_cycles:
+            mark("hold")
+            torch.cuda._sleep(hold_cycles)
         for (t0, t1, capped) in passes:
             sc = self.sub(t0, t1, capped)
             planned = capped and sc.redundant_slots > 0
@@ -350,11 +356,15 @@ class StageTimer:
         return out
 
 
+HOLD_CYCLES = 1_000_000   # about 0.5 ms at 2 GHz
+
+
 def launches_per_step(passes, mode, dispatch_only=False, planned=0):
     """Kernel launches of one step: route 1 (+ check 1 with the fallback),
-    then per pass permute 5 (block counts, expert scan, assign, dedup scan,
-    row scatter), GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the sweep)."""
-    per = 6 if dispatch_only else 8
+    then per pass permute 4 (block counts, expert scan, assign with the
+    dedup scan, row scatter), GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the
+    sweep)."""
+    per = 5 if dispatch_only else 7
     return (2 if mode == "fallback" else 1) + planned + \
         sum(per for (t0, t1, _) in passes if t1 > t0)
 
@@ -547,6 +557,18 @@ def main():
     step_ms = [sum(d for _, d in st.durations()) for st in timers]
     mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
 
+    # The same steps with the GPU held until the host has queued the first
+    # pass: the stage times of the kernels alone, without the host's launch
+    # latency after the overflow-flag read (outside the timed region).
+    held = {}
+    for _ in range(args.steps):
+        flush.zero_()
+        st = StageTimer()
+        layer.step(st, hold_cycles=HOLD_CYCLES)
+        torch.cuda.synchronize()
+        for name, d in st.durations():
+            held[name] = held.get(name, 0.0) + d
+
     # per-stage durations
     stage = {}
     for st in timers:
@@ -575,6 +597,18 @@ def main():
             if wv["flops"]:
                 ent["TFLOPs"] = round(wv["flops"] / sec / 1e12, 1)
         kernels[name] = ent
+
+    stages_held = {"note": "CUDA events per stage in separate steps whose "
+                           "GPU work waits (a sleep before the first pass) "
+                           "until the host has queued it; HBM fraction of "
+                           "the measured copy peak"}
+    for name in ("permute", "combine"):
+        if name in held and name in work:
+            per_step = held[name] / args.steps
+            gbps = work[name]["bytes"] / (per_step / 1e3) / 1e9
+            stages_held[name] = {"ms_per_step": round(per_step, 4),
+                                 "GBps": round(gbps, 1),
+                                 "frac": round(gbps / peaks["hbm_gbs"], 4)}
 
     dom = max((n for n in work if n in stage), key=lambda n: stage[n]["ms"])
     wv = work[dom]
@@ -640,6 +674,7 @@ def main():
             int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"))
         * args.steps,
         "kernels": kernels,
+        "stages_host_held": stages_held,
         "roofline": roof,
     }
     out["value"] = round(whole_job_tokens_per_s(world, layer.wl.T, mean_ms), 1)
@@ -990,7 +1025,7 @@ class Backward:
 
 def backward_launches(passes, mode, regroup, planned=False, on_plan=False):
     """Kernel launches of one backward step: route (+ check, + the plan with
-    duplicate slots), per pass permute 5 + GEMM1-saved + GEMM2 + combine
+    duplicate slots), per pass permute 4 + GEMM1-saved + GEMM2 + combine
     backward + two dgrad GEMMs + permute backward, route backward, the
     regrouping of the rows (2) or the row segments in batches of 16, and per
     batch the two weight-gradient GEMMs (+ the two zero fills of experts
@@ -1000,7 +1035,7 @@ def backward_launches(passes, mode, regroup, planned=False, on_plan=False):
     batches = 1 if regroup else (n + 15) // 16
     head = 1 + (1 if (mode == "fallback" or planned) else 0) + \
         (1 if planned else 0)
-    return head + 11 * n + 1 + (2 if regroup else 0) + 2 * batches + \
+    return head + 10 * n + 1 + (2 if regroup else 0) + 2 * batches + \
         (0 if on_plan else 2)
 
 

@@ -452,17 +452,16 @@ cudaError_t launch_wgrad_f32(const moe_config_t& c, const Groups& g,
     const long long r0 = seg[i].first_row;
     const int acc = (accumulate || i > 0) ? 1 : 0;
     const int32_t* off = seg[i].group_offsets;
-    if (dn)
+    if (dn)  // the buffers of a part left out may be null
       wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
           Hs + r0 * c.F, c.F, DY + r0 * c.H, c.H, off, g.n, g.map, c.E, acc,
           dwd);
     if (gu) {
+      const float* xr = X + r0 * c.H;
       wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
-          X + r0 * c.H, c.H, DG + r0 * c.F, c.F, off, g.n, g.map, c.E, acc,
-          dwg);
+          xr, c.H, DG + r0 * c.F, c.F, off, g.n, g.map, c.E, acc, dwg);
       wgrad_f32<<<blocks_for(nw, 256), 256, 0, s>>>(
-          X + r0 * c.H, c.H, DU + r0 * c.F, c.F, off, g.n, g.map, c.E, acc,
-          dwu);
+          xr, c.H, DU + r0 * c.F, c.F, off, g.n, g.map, c.E, acc, dwu);
     }
   }
   return cudaGetLastError();

@@ -22,8 +22,14 @@
 //                   expert); row_of, sorted_token; per-shard membership of
 //                   each token and its rank among the block's members
 //   4 scan_uniq   : per shard, exclusive scan of block member counts; |U_s|
+//                   (only for tables of more than 1024 block-shard counts:
+//                   below that, every scatter CTA sums the table itself)
 //   5 scatter     : one CTA per token: dedup indices, then x[t] read once
 //                   with 16-byte loads and written to each kept row
+// Kernels 2 to 5 are programmatic dependent launches: each may start once
+// its predecessor has started, does the work that needs none of its
+// predecessor's output (assign: the lane masks from the routing indices;
+// scatter: the read of x[t]), and then waits for its predecessor to finish.
 // With a duplication plan ("Moe dynamic redundancy" (MaxText pull request
 // 4760), review of plan_expert_duplication) the groups are virtual: shard s
 // owns its E/S experts and then its B duplicate slots, and the last
@@ -39,21 +45,44 @@ namespace {
 
 constexpr int TB = kPermuteTokensPerBlock;  // tokens per block, 4 warps
 constexpr int kWarps = TB / 32;
+constexpr int kBatch = 16;  // independent loads a thread issues together
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start once every CTA of its producer has called
+// allow_dependents() (or exited); wait_for_producer() returns when the
+// producer grid has finished and its writes are visible.  Without that
+// launch attribute the wait returns at once.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_producer() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(TB) block_count_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k,
     int32_t* __restrict__ block_base, int32_t* __restrict__ status) {
   extern __shared__ int cnt[];
+  allow_dependents();
   const int b = blockIdx.x, tid = threadIdx.x;
   for (int e = tid; e < E; e += TB) cnt[e] = 0;
   __syncthreads();
-  const int t = b * TB + tid;
+  // the block's entries (t, j) in memory order, kBatch loads in flight
+  const int32_t* src = idx + static_cast<long long>(b) * TB * k;
+  const int m = min(TB, T - b * TB) * k;
   bool bad = false;
-  if (t < T) {
-    for (int j = 0; j < k; ++j) {
-      const int e = __ldg(idx + static_cast<long long>(t) * k + j);
-      if (e >= 0 && e < E)
-        atomicAdd(&cnt[e], 1);
+  for (int i0 = tid; i0 < m; i0 += kBatch * TB) {
+    int v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * TB;
+      v[u] = i < m ? __ldg(src + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (i0 + u * TB >= m) break;
+      if (v[u] >= 0 && v[u] < E)
+        atomicAdd(&cnt[v[u]], 1);
       else
         bad = true;
     }
@@ -91,6 +120,28 @@ __device__ int block_exclusive_scan_1024(int v, int* warp_tot, int* total) {
   return r;
 }
 
+// In place, over one column of a row-major [n, stride] table: v[b] becomes
+// the sum of v[0..b); returns the total.  The loads of a batch are issued
+// before its stores, so the column costs about n/kBatch memory latencies
+// rather than n.
+__device__ __forceinline__ int exclusive_scan_column(int32_t* col, int n,
+                                                     int stride) {
+  int run = 0;
+  for (int b0 = 0; b0 < n; b0 += kBatch) {
+    int v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      v[i] = b0 + i < n ? __ldcg(col + static_cast<long long>(b0 + i) * stride)
+                        : 0;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (b0 + i < n) col[static_cast<long long>(b0 + i) * stride] = run;
+      run += v[i];
+    }
+  }
+  return run;
+}
+
 // One CTA of 1024 threads.  Thread e owns expert e (its block scan and the
 // split of its rows), thread g owns virtual group g (the scans over groups
 // and the capacity rule).  G <= 1024.
@@ -98,27 +149,22 @@ __global__ void __launch_bounds__(1024) scan_experts_kernel(
     int32_t* __restrict__ block_base, int nb, int E, int S, int B, int cap,
     const int32_t* __restrict__ divert, const int32_t* __restrict__ slot_of,
     int32_t* __restrict__ etab, int32_t* __restrict__ group_offsets,
-    int32_t* __restrict__ n_dropped) {
+    int32_t* __restrict__ n_dropped, int32_t* __restrict__ uniq_offsets) {
   __shared__ int cv[kMaxExperts];       // rows per virtual group
   __shared__ int scan[kMaxExperts + 1];
   __shared__ int keptv[kMaxExperts];
   __shared__ int goffv[kMaxExperts];
   __shared__ int warp_tot[32];
   __shared__ int total, ktotal;
+  allow_dependents();
   const int tid = threadIdx.x;
   const int Es = E / S, Gs = Es + B, G = S * Gs;
   if (tid < G) cv[tid] = 0;
   __syncthreads();
+  wait_for_producer();
   int c = 0, d = 0, slot = -1;
   if (tid < E) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      int32_t* p = block_base + static_cast<long long>(b) * E + tid;
-      const int v = *p;
-      *p = run;
-      run += v;
-    }
-    c = run;
+    c = exclusive_scan_column(block_base + tid, nb, E);
     if (divert != nullptr && slot_of != nullptr) {
       slot = slot_of[tid];
       // a duplicate must sit in a slot position of some shard
@@ -151,6 +197,7 @@ __global__ void __launch_bounds__(1024) scan_experts_kernel(
     group_offsets[G] = ktotal;
     *n_dropped = total - ktotal;
   }
+  if (nb == 0 && tid <= S) uniq_offsets[tid] = 0;  // no tokens: no assign
   __syncthreads();
   if (tid < E) {
     const int home = (tid / Es) * Gs + tid % Es;
@@ -176,13 +223,11 @@ __global__ void __launch_bounds__(TB) assign_kernel(
   uint32_t* ballot = reinterpret_cast<uint32_t*>(etab + 6 * E);  // [kWarps][S]
   int* upre = reinterpret_cast<int*>(ballot + kWarps * S);       // [kWarps][S]
 
+  allow_dependents();
   const int b = blockIdx.x, tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const uint32_t lt = (1u << lane) - 1u;
   for (int e = tid; e < E; e += TB) {
-    base[e] = block_base[static_cast<long long>(b) * E + e];
-#pragma unroll
-    for (int q = 0; q < 6; ++q) etab[q * E + e] = etab_g[q * E + e];
 #pragma unroll
     for (int q = 0; q < kWarps; ++q) mask[q * E + e] = 0u;
   }
@@ -190,10 +235,23 @@ __global__ void __launch_bounds__(TB) assign_kernel(
   const int t = b * TB + tid;
   const bool valid = t < T;
   const long long tk = static_cast<long long>(t) * k;
-  if (valid) {
-    for (int j = 0; j < k; ++j) {
-      const int e = __ldg(idx + tk + j);
-      if (e >= 0 && e < E) atomicOr(&mask[w * E + e], 1u << lane);
+  {
+    // entry i of the block is (token i / k, pick i % k)
+    const int32_t* src = idx + static_cast<long long>(b) * TB * k;
+    const int m = min(TB, T - b * TB) * k;
+    for (int i0 = tid; i0 < m; i0 += kBatch * TB) {
+      int v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * TB;
+        v[u] = i < m ? __ldg(src + i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int tl = (i0 + u * TB) / k;  // token within the block
+        if (v[u] >= 0 && v[u] < E)
+          atomicOr(&mask[(tl >> 5) * E + v[u]], 1u << (tl & 31));
+      }
     }
   }
   __syncthreads();
@@ -205,9 +263,18 @@ __global__ void __launch_bounds__(TB) assign_kernel(
       run += __popc(mask[q * E + e]);
     }
   }
+  // Everything above reads only the routing indices; the block bases and
+  // the expert tables come from the scan.
+  wait_for_producer();
+  for (int e = tid; e < E; e += TB) {
+    base[e] = block_base[static_cast<long long>(b) * E + e];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) etab[q * E + e] = etab_g[q * E + e];
+  }
   __syncthreads();
   const int Es = E / S;
   uint64_t smask = 0;
+  uint32_t kept = 0;  // bit j: (t, j) has a row
   if (valid) {
     for (int j = 0; j < k; ++j) {
       const int e = __ldg(idx + tk + j);
@@ -225,7 +292,10 @@ __global__ void __launch_bounds__(TB) assign_kernel(
           row = etab[4 * E + e] + (rank - own);
           smask |= 1ull << etab[5 * E + e];
         }
-        if (row >= 0) sorted_token[row] = t;
+        if (row >= 0) {
+          sorted_token[row] = t;
+          kept |= 1u << j;
+        }
       }
       row_of[tk + j] = row;
     }
@@ -248,7 +318,7 @@ __global__ void __launch_bounds__(TB) assign_kernel(
   if (valid) {
     for (int j = 0; j < k; ++j) {
       int ur = -1;
-      if (row_of[tk + j] >= 0) {
+      if ((kept >> j) & 1u) {
         const int e = __ldg(idx + tk + j);
         const int rank =
             base[e] + wpre[w * E + e] + __popc(mask[w * E + e] & lt);
@@ -265,17 +335,10 @@ __global__ void __launch_bounds__(64) scan_uniq_kernel(
     int32_t* __restrict__ block_ucnt, int nb, int S,
     int32_t* __restrict__ uniq_offsets) {
   __shared__ int tot[kMaxShards];
+  allow_dependents();
+  wait_for_producer();
   const int s = threadIdx.x;
-  if (s < S) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      int32_t* p = block_ucnt + static_cast<long long>(b) * S + s;
-      const int v = *p;
-      *p = run;
-      run += v;
-    }
-    tot[s] = run;
-  }
+  if (s < S) tot[s] = exclusive_scan_column(block_ucnt + s, nb, S);
   __syncthreads();
   if (s == 0) {
     int run = 0;
@@ -290,40 +353,95 @@ __global__ void __launch_bounds__(64) scan_uniq_kernel(
 constexpr int kScatterThreads = 128;
 constexpr int kScatterUnroll = 8;
 
-// One CTA per token.
+// Block-shard tables up to this many counts are summed by every scatter CTA
+// (no scan kernel between assign and the scatter).
+constexpr int kInlineUniqCounts = 1024;
+static_assert(kInlineUniqCounts % kScatterThreads == 0, "whole loads");
+
+// One CTA per token.  The first slice of x[t] (all of it up to 16 KB) is
+// read before the wait for the tables.  Dedup position of (t, j) in shard
+// s: the members of shards before s, plus those of s in the token blocks
+// before t's, plus t's rank among its block's members.  With inline_uniq
+// the first two come from the block_ucnt counts as assign left them, and
+// CTA 0 writes uniq_offsets; otherwise scan_uniq has scanned them.
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
-    const int4* __restrict__ x, int n16, const int32_t* __restrict__ idx,
-    int E, int k, int S, const int32_t* __restrict__ row_of,
+    const int4* __restrict__ x, int n16, int k, int S, int nb,
+    int inline_uniq, const int32_t* __restrict__ row_of,
     const int32_t* __restrict__ block_ucnt, const int32_t* __restrict__ urank,
-    const int32_t* __restrict__ uniq_offsets, int4* __restrict__ x_sorted,
+    int32_t* __restrict__ uniq_offsets, int4* __restrict__ x_sorted,
     int32_t* __restrict__ expand_idx, int32_t* __restrict__ uniq_tokens) {
   __shared__ int rows[kMaxTopK];
+  __shared__ int codes[kMaxTopK];
+  __shared__ int tot[kMaxShards];     // members of shard s, all blocks
+  __shared__ int before[kMaxShards];  // members of shard s, blocks before t's
   const int t = blockIdx.x, tid = threadIdx.x;
+  const int bt = t / TB;
   const long long tk = static_cast<long long>(t) * k;
+  const int4* src = x + static_cast<long long>(t) * n16;
+  int4 v[kScatterUnroll];
+#pragma unroll
+  for (int u = 0; u < kScatterUnroll; ++u) {
+    const int c = tid + u * kScatterThreads;
+    if (c < n16) v[u] = __ldg(src + c);
+  }
+  for (int q = tid; q < S; q += kScatterThreads) {
+    tot[q] = 0;
+    before[q] = 0;
+  }
+  wait_for_producer();
   if (tid < k) {
-    const int row = row_of[tk + tid];
-    rows[tid] = row;
-    if (row >= 0) {
-      const int code = urank[tk + tid];
-      const int s = code & 63;
-      const int upos = uniq_offsets[s] +
-                       block_ucnt[static_cast<long long>(t / TB) * S + s] +
-                       (code >> 6);
-      expand_idx[row] = upos;
-      bool first = true;
-      for (int q = 0; q < tid; ++q)
-        if (row_of[tk + q] >= 0 && (urank[tk + q] & 63) == s) first = false;
-      if (first) uniq_tokens[upos] = t;
+    rows[tid] = row_of[tk + tid];
+    codes[tid] = urank[tk + tid];
+  }
+  if (inline_uniq) {
+    constexpr int kPer = kInlineUniqCounts / kScatterThreads;
+    int c[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * kScatterThreads;
+      c[u] = i < nb * S ? __ldcg(block_ucnt + i) : 0;
+    }
+    __syncthreads();  // the zeroed sums
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = tid + u * kScatterThreads;
+      if (c[u] == 0) continue;
+      const int q = i % S;
+      atomicAdd(&tot[q], c[u]);
+      if (i / S < bt) atomicAdd(&before[q], c[u]);
     }
   }
   __syncthreads();
-  const int4* src = x + static_cast<long long>(t) * n16;
+  if (tid < k && rows[tid] >= 0) {
+    const int code = codes[tid];
+    const int q = code & 63;
+    int base;
+    if (inline_uniq) {
+      base = before[q];
+      for (int p = 0; p < q; ++p) base += tot[p];
+    } else {
+      base = uniq_offsets[q] + block_ucnt[static_cast<long long>(bt) * S + q];
+    }
+    const int upos = base + (code >> 6);
+    expand_idx[rows[tid]] = upos;
+    bool first = true;  // the token's first row bound for shard q
+    for (int p = 0; p < tid; ++p)
+      if (rows[p] >= 0 && (codes[p] & 63) == q) first = false;
+    if (first) uniq_tokens[upos] = t;
+  }
+  if (inline_uniq && t == 0 && tid <= S) {
+    int o = 0;
+    for (int p = 0; p < tid; ++p) o += tot[p];
+    uniq_offsets[tid] = o;
+  }
+  __syncthreads();
   for (int c0 = tid; c0 < n16; c0 += kScatterThreads * kScatterUnroll) {
-    int4 v[kScatterUnroll];
+    if (c0 != tid) {
 #pragma unroll
-    for (int u = 0; u < kScatterUnroll; ++u) {
-      const int c = c0 + u * kScatterThreads;
-      if (c < n16) v[u] = __ldg(src + c);
+      for (int u = 0; u < kScatterUnroll; ++u) {
+        const int c = c0 + u * kScatterThreads;
+        if (c < n16) v[u] = __ldg(src + c);
+      }
     }
     for (int j = 0; j < k; ++j) {
       const int r = rows[j];
@@ -340,6 +458,26 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 
 size_t assign_smem_bytes(int E, int S) {
   return sizeof(int) * (2 * kWarps * E + 7 * E + 2 * kWarps * S);
+}
+
+// A launch on stream s that may start before the previous kernel on s has
+// finished (that kernel calls allow_dependents(), this one
+// wait_for_producer() before reading its output).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid,
+                             unsigned block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(block);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<Params>(args)...);
 }
 
 }  // namespace
@@ -370,32 +508,44 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
                            const PermuteScratch& ws, int32_t* status,
                            cudaStream_t s, const PermutePlan& plan) {
   const int nb = (c.T + TB - 1) / TB;
+  cudaError_t e = cudaSuccess;
   if (nb > 0) {
     block_count_kernel<<<nb, TB, c.E * sizeof(int), s>>>(
         topk_idx, c.T, c.E, c.k, ws.block_base, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  scan_experts_kernel<<<1, 1024, 0, s>>>(
-      ws.block_base, nb, c.E, c.S, plan.B, static_cast<int>(cap),
-      plan.divert, plan.slot_of, ws.etab, group_offsets, n_dropped);
+  if ((e = launch_dependent(scan_experts_kernel, 1, 1024, 0, s, ws.block_base,
+                            nb, c.E, c.S, plan.B, static_cast<int>(cap),
+                            plan.divert, plan.slot_of, ws.etab, group_offsets,
+                            n_dropped, uniq_offsets)) != cudaSuccess)
+    return e;
   if (nb > 0) {
     const size_t smem = assign_smem_bytes(c.E, c.S);
-    if (smem > 48 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(
-          assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-          static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
-    assign_kernel<<<nb, TB, smem, s>>>(topk_idx, c.T, c.E, c.k, c.S,
-                                       ws.block_base, ws.etab, row_of,
-                                       sorted_token, ws.block_ucnt, ws.urank);
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(assign_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem))) != cudaSuccess)
+      return e;
+    if ((e = launch_dependent(assign_kernel, nb, TB, smem, s, topk_idx, c.T,
+                              c.E, c.k, c.S, ws.block_base, ws.etab, row_of,
+                              sorted_token, ws.block_ucnt, ws.urank)) !=
+        cudaSuccess)
+      return e;
   }
-  scan_uniq_kernel<<<1, 64, 0, s>>>(ws.block_ucnt, nb, c.S, uniq_offsets);
+  const int inline_uniq =
+      static_cast<long long>(nb) * c.S <= kInlineUniqCounts ? 1 : 0;
+  if (nb > 0 && !inline_uniq &&
+      (e = launch_dependent(scan_uniq_kernel, 1, 64, 0, s, ws.block_ucnt, nb,
+                            c.S, uniq_offsets)) != cudaSuccess)
+    return e;
   if (c.T > 0) {
     const int n16 = c.H * elem_bytes(c.dtype) / 16;
-    scatter_kernel<<<c.T, kScatterThreads, 0, s>>>(
-        static_cast<const int4*>(x), n16, topk_idx, c.E, c.k, c.S, row_of,
-        ws.block_ucnt, ws.urank, uniq_offsets, static_cast<int4*>(x_sorted),
-        expand_idx, uniq_tokens);
+    if ((e = launch_dependent(scatter_kernel, c.T, kScatterThreads, 0, s,
+                              static_cast<const int4*>(x), n16, c.k, c.S, nb,
+                              inline_uniq, row_of, ws.block_ucnt, ws.urank,
+                              uniq_offsets, static_cast<int4*>(x_sorted),
+                              expand_idx, uniq_tokens)) != cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }

@@ -33,6 +33,15 @@ CASES = [
                              S=8, zipf_s=1.2),
     WORKLOADS["small"].with_(name="e300", T=900, H=64, E=300, k=3, S=4,
                              routing="uniform"),
+    WORKLOADS["small"].with_(name="e640", T=1500, H=64, E=640, k=4, S=8,
+                             zipf_s=1.2),
+    # the most shards: 64 lanes of per-shard dedup; a block-shard table
+    # above 1024 counts (the dedup scan kernel runs)
+    WORKLOADS["small"].with_(name="s64", T=3000, H=64, E=512, k=8, S=64,
+                             routing="uniform"),
+    # 157 token blocks x 8 shards: the dedup scan kernel with 8 shards
+    WORKLOADS["small"].with_(name="t20000", T=20000, H=64, E=256, k=8, S=8,
+                             zipf_s=1.2),
 ]
 
 
