@@ -36,6 +36,7 @@ namespace tc {
 constexpr int WSTAGES = 3;
 constexpr int kWStage = BM * BK * 2 + BK * 256 * 2;  // 48 KB
 constexpr int kStageBuf = 32 * 32 * 4;               // 4 KB
+constexpr int kStageBufs = 4;  // staging buffers per epilogue warp
 constexpr int kMaxSeg = 16;
 
 struct WParams {
@@ -108,9 +109,11 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// At most one bulk group of this thread still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// At most kStageBufs - 1 bulk groups of this thread still reading shared
+// memory: the oldest staging buffer is free again.
+__device__ __forceinline__ void bulk_wait_read_free() {
+  static_assert(kStageBufs == 4, "the wait depth below is kStageBufs - 1");
+  asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() {
@@ -177,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stagebuf = smem + WSTAGES * kWStage;  // [4 warps][2][4 KB]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stagebuf + 8 * kStageBuf);
+  uint8_t* stagebuf = smem + WSTAGES * kWStage;  // [4 warps][kStageBufs][4 KB]
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(stagebuf + 4 * kStageBufs * kStageBuf);
   uint64_t* full = bars;
   uint64_t* empty = bars + WSTAGES;
   uint64_t* tfull = bars + 2 * WSTAGES;
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue ---------
     const int q = warp & 3;
-    uint8_t* mybuf = stagebuf + q * 2 * kStageBuf;
+    uint8_t* mybuf = stagebuf + q * kStageBufs * kStageBuf;
     const uint64_t stream = policy_evict_first();
     int acc = 0, nsub = 0;
     uint32_t acc_phase = 0;
@@ -383,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int sub = 0; sub < BN / 32; ++sub, ++nsub) {
         uint32_t r[32];
         tmem_ld32(taddr + sub * 32, r);
-        uint8_t* buf = mybuf + (nsub & 1) * kStageBuf;
-        if (lane == 0) bulk_wait_read_1();
+        uint8_t* buf = mybuf + (nsub % kStageBufs) * kStageBuf;
+        if (lane == 0) bulk_wait_read_free();
         __syncwarp();
         uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
 #pragma unroll
@@ -449,7 +453,8 @@ __global__ void zero_experts_kernel(WParams p, float* a, float* b,
 }
 
 size_t smem_bytes_wgrad(int G, int E) {
-  return 1024 + WSTAGES * kWStage + 8 * kStageBuf + 8 * (2 * WSTAGES + 5) +
+  return 1024 + WSTAGES * kWStage + 4 * kStageBufs * kStageBuf +
+         8 * (2 * WSTAGES + 5) +
          16 + 4 * (16 + G + 1 + E) + 64;
 }
 
