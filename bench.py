@@ -240,6 +240,15 @@ class Layer:
         self.b["y"].zero_()
         self.ws = moe.layer_workspace(self.cfg, moe.MOE_WS_LAYER, device)
         self.chunk = moe.moe_chunk_tokens(self.cfg)
+        # Two sets of a pass's permute tables: the tables of pass i+1 are
+        # computed on the side stream while pass i runs its expert FFN.
+        # Set 0 is the step buffers themselves.
+        keys = ("sorted_token", "group_offsets", "uniq_offsets",
+                "uniq_tokens", "expand_idx", "n_dropped", "permute_ws")
+        self.tabs = [{k: self.b[k] for k in keys},
+                     {k: torch.empty_like(self.b[k]) for k in keys}]
+        self.side = torch.cuda.Stream(device=device)
+        self.pass_events = []   # (tables ready, pass done) per pass, reused
 
     def sub(self, t0, t1, capped):
         """Pass over tokens [t0, t1): the config the library uses."""
@@ -282,46 +291,86 @@ class Layer:
         return self._passes(passes, mark, hold_cycles)
 
     def _passes(self, passes, mark, hold_cycles=0):
+        """The passes, each: permute tables -> row scatter -> GEMM1 ->
+        GEMM2 -> combine.  The first pass's tables run on the main stream;
+        those of pass i+1 are queued on the side stream after pass i's
+        work, so they run during pass i's FFN.  They reuse the table set of
+        pass i-1 and wait for that pass's combine."""
         moe, b, W = self.moe, self.b, self.W
         if hold_cycles:
             mark("hold")
             torch.cuda._sleep(hold_cycles)
-        for (t0, t1, capped) in passes:
+        main, side = torch.cuda.current_stream(), self.side
+        side.wait_stream(main)   # the routing (and the hold) first
+        while len(self.pass_events) < len(passes):
+            self.pass_events.append((torch.cuda.Event(), torch.cuda.Event()))
+        ready = [e[0] for e in self.pass_events]
+        done = [e[1] for e in self.pass_events]
+        side_times = getattr(mark, "side", None)
+
+        def tables(i, stream):
+            t0, t1, capped = passes[i]
             sc = self.sub(t0, t1, capped)
-            planned = capped and sc.redundant_slots > 0
-            mark("permute")
-            if planned:
-                moe.moe_permute_planned(
-                    sc, self.x[t0:t1], b["topk_idx"][t0:t1], capped,
-                    b["divert"], b["slot_of"], b["x_sorted"], b["row_of"],
-                    b["sorted_token"], b["group_offsets"], b["uniq_offsets"],
-                    b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
-                    b["permute_ws"])
+            tb = self.tabs[i % 2]
+            plan = {}
+            if capped and sc.redundant_slots > 0:
+                plan = dict(divert=b["divert"], slot_of=b["slot_of"])
+            timed = side_times is not None and stream is side
+            with torch.cuda.stream(stream):
+                if i >= 2:
+                    stream.wait_event(done[i - 2])
+                if timed:
+                    ev0 = torch.cuda.Event(enable_timing=True)
+                    ev0.record(stream)
+                moe.moe_permute_tables(
+                    sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
+                    tb["sorted_token"], tb["group_offsets"],
+                    tb["uniq_offsets"], tb["n_dropped"], tb["permute_ws"],
+                    stream=stream, **plan)
+                ready[i].record(stream)
+                if timed:
+                    ev1 = torch.cuda.Event(enable_timing=True)
+                    ev1.record(stream)
+                    side_times.append((ev0, ev1))
+
+        for i, (t0, t1, capped) in enumerate(passes):
+            sc = self.sub(t0, t1, capped)
+            tb = self.tabs[i % 2]
+            row_of = b["row_of"][t0:t1]
+            groups = {}
+            if capped and sc.redundant_slots > 0:
                 groups = dict(n_groups=sc.E + sc.S * sc.redundant_slots,
                               group_expert=b["group_expert"])
+            mark("permute")
+            if i == 0:
+                tables(0, main)
             else:
-                moe.moe_permute(sc, self.x[t0:t1], b["topk_idx"][t0:t1],
-                                capped, b["x_sorted"], b["row_of"],
-                                b["sorted_token"], b["group_offsets"],
-                                b["uniq_offsets"], b["uniq_tokens"],
-                                b["expand_idx"], b["n_dropped"],
-                                b["permute_ws"])
-                groups = {}
+                main.wait_event(ready[i])
+            moe.moe_permute_scatter(sc, self.x[t0:t1], row_of,
+                                    tb["uniq_offsets"], b["x_sorted"],
+                                    tb["uniq_tokens"], tb["expand_idx"],
+                                    tb["permute_ws"])
             if self.dispatch_only:
                 # no expert FFN: the combine reads the permuted rows back
                 mark("combine")
-                moe.moe_combine(sc, b["x_sorted"], b["row_of"],
+                moe.moe_combine(sc, b["x_sorted"], row_of,
                                 b["topk_w"][t0:t1], b["y"][t0:t1])
+                done[i].record(main)
+                if i + 1 < len(passes):
+                    tables(i + 1, side)
                 continue
             mark("gmm_gate_up")
-            moe.moe_gmm_gate_up(sc, b["x_sorted"], b["group_offsets"], W[0],
+            moe.moe_gmm_gate_up(sc, b["x_sorted"], tb["group_offsets"], W[0],
                                 W[1], b["h"], b["status"], **groups)
             mark("gmm_down")
-            moe.moe_gmm_down(sc, b["h"], b["group_offsets"], W[2],
+            moe.moe_gmm_down(sc, b["h"], tb["group_offsets"], W[2],
                              b["y_sorted"], b["status"], **groups)
             mark("combine")
-            moe.moe_combine(sc, b["y_sorted"], b["row_of"],
-                            b["topk_w"][t0:t1], b["y"][t0:t1])
+            moe.moe_combine(sc, b["y_sorted"], row_of, b["topk_w"][t0:t1],
+                            b["y"][t0:t1])
+            done[i].record(main)
+            if i + 1 < len(passes):
+                tables(i + 1, side)
         mark(None)
         return passes
 
@@ -334,11 +383,14 @@ class Layer:
 
 
 class StageTimer:
-    """CUDA events on the current stream between consecutive stage marks."""
+    """CUDA events on the current stream between consecutive stage marks;
+    `side` collects (start, end) events of the permute tables on the side
+    stream."""
 
     def __init__(self):
         self.events = []
         self.names = []
+        self.side = []
 
     def __call__(self, name):
         e = torch.cuda.Event(enable_timing=True)
@@ -561,6 +613,7 @@ def main():
     # pass: the stage times of the kernels alone, without the host's launch
     # latency after the overflow-flag read (outside the timed region).
     held = {}
+    side_ms = 0.0
     for _ in range(args.steps):
         flush.zero_()
         st = StageTimer()
@@ -568,6 +621,7 @@ def main():
         torch.cuda.synchronize()
         for name, d in st.durations():
             held[name] = held.get(name, 0.0) + d
+        side_ms += sum(a.elapsed_time(z) for a, z in st.side)
 
     # per-stage durations
     stage = {}
@@ -601,7 +655,14 @@ def main():
     stages_held = {"note": "CUDA events per stage in separate steps whose "
                            "GPU work waits (a sleep before the first pass) "
                            "until the host has queued it; HBM fraction of "
-                           "the measured copy peak"}
+                           "the measured copy peak. permute = the row "
+                           "scatter (plus the first pass's tables); "
+                           "permute_tables = the counting-sort kernels of "
+                           "passes 2.. on the side stream, each overlapping "
+                           "the previous pass's expert FFN",
+                   "permute_tables": {"ms_per_step":
+                                      round(side_ms / args.steps, 4),
+                                      "stream": "side"}}
     for name in ("permute", "combine"):
         if name in held and name in work:
             per_step = held[name] / args.steps

@@ -316,6 +316,44 @@ moe_status_t moe_permute_planned(const moe_config_t *cfg, const void *x,
                                  void *workspace, size_t workspace_bytes,
                                  moe_stream_t stream);
 
+/* ----------------------------------------------------------------------
+ * moe_permute_tables / moe_permute_scatter -- moe_permute (or, with divert
+ * and slot_of, moe_permute_planned) in two calls, same bits.  The pages
+ * have no such split; it lets a caller of the chunked fallback [PR5920
+ * How: the fallback runs the layer chunk by chunk] compute the next
+ * chunk's counting-sort tables on a second stream while the current
+ * chunk's expert FFN runs, so that only the row copy stays between two
+ * chunks' FFNs.
+ * moe_permute_tables: the counting sort.
+ *   topk_idx, capped         as moe_permute
+ *   divert, slot_of          both NULL (no plan) or both a plan's arrays
+ *                            (as moe_permute_planned)
+ *   row_of, sorted_token, group_offsets, n_dropped   out, as moe_permute
+ *   uniq_offsets             out [S+1]; complete only after the scatter
+ *   workspace                moe_workspace_bytes(cfg, MOE_WS_PERMUTE)
+ *                            bytes; holds the scatter's tables: pass the
+ *                            same workspace, unchanged, to the scatter
+ * moe_permute_scatter: x_sorted, uniq_tokens, expand_idx and the rest of
+ *   uniq_offsets, from row_of, uniq_offsets and the workspace that
+ *   moe_permute_tables wrote (same cfg).  Order the two on the device
+ *   (same stream, or an event) before the scatter runs.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_permute_tables(const moe_config_t *cfg,
+                                const int32_t *topk_idx, int32_t capped,
+                                const int32_t *divert,
+                                const int32_t *slot_of, int32_t *row_of,
+                                int32_t *sorted_token,
+                                int32_t *group_offsets,
+                                int32_t *uniq_offsets, int32_t *n_dropped,
+                                void *workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+moe_status_t moe_permute_scatter(const moe_config_t *cfg, const void *x,
+                                 const int32_t *row_of,
+                                 int32_t *uniq_offsets, void *x_sorted,
+                                 int32_t *uniq_tokens, int32_t *expand_idx,
+                                 const void *workspace,
+                                 size_t workspace_bytes, moe_stream_t stream);
+
 /* moe_gmm_swiglu_mapped -- moe_gmm_swiglu over n_groups row groups where
  * group g computes with the weights of expert group_expert[g] (device,
  * [n_groups]; a group of an expert < 0 must be empty).  group_offsets has

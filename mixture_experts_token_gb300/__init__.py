@@ -90,6 +90,9 @@ def _declare(h):
                         c_size_t, P],
         "moe_permute_noalloc": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P,
                                 P],
+        "moe_permute_tables": [cfg, P, c_int32, P, P, P, P, P, P, P, P,
+                               c_size_t, P],
+        "moe_permute_scatter": [cfg, P, P, P, P, P, P, P, c_size_t, P],
         "moe_gmm_swiglu": [cfg, P, P, P, P, P, P, P, P, P],
         "moe_plan_duplication": [cfg, P, P, P, P, P, P, P],
         "moe_permute_planned": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P,
@@ -250,6 +253,28 @@ def moe_permute(cfg, x, topk_idx, capped, x_sorted, row_of, sorted_token,
         _ptr(group_offsets), _ptr(uniq_offsets), _ptr(uniq_tokens),
         _ptr(expand_idx), _ptr(n_dropped), _ptr(workspace),
         _nbytes(workspace), _stream(stream)), "moe_permute")
+
+
+def moe_permute_tables(cfg, topk_idx, capped, row_of, sorted_token,
+                       group_offsets, uniq_offsets, n_dropped, workspace,
+                       divert=None, slot_of=None, stream=None):
+    """The counting-sort half of moe_permute (moe_permute_planned with
+    divert and slot_of); moe_permute_scatter completes it."""
+    _check(lib().moe_permute_tables(
+        ctypes.byref(cfg), _ptr(topk_idx), 1 if capped else 0, _ptr(divert),
+        _ptr(slot_of), _ptr(row_of), _ptr(sorted_token), _ptr(group_offsets),
+        _ptr(uniq_offsets), _ptr(n_dropped), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "moe_permute_tables")
+
+
+def moe_permute_scatter(cfg, x, row_of, uniq_offsets, x_sorted, uniq_tokens,
+                        expand_idx, workspace, stream=None):
+    """The row copy of moe_permute, from the tables moe_permute_tables left
+    in row_of, uniq_offsets and the workspace."""
+    _check(lib().moe_permute_scatter(
+        ctypes.byref(cfg), _ptr(x), _ptr(row_of), _ptr(uniq_offsets),
+        _ptr(x_sorted), _ptr(uniq_tokens), _ptr(expand_idx), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "moe_permute_scatter")
 
 
 def moe_permute_noalloc(cfg, x, topk_idx, capped, x_sorted, row_of,

@@ -157,6 +157,14 @@ LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
   b.x_sorted = cv.take<char>(tk * c.H * eb);
   b.h = cv.take<char>(tk * static_cast<size_t>(c.F) * eb);
   b.y_sorted = cv.take<char>(tk * c.H * eb);
+  b.alt.sorted_token = cv.take<int32_t>(tk);
+  b.alt.group_offsets = cv.take<int32_t>(num_groups(c) + 1);
+  b.alt.uniq_offsets = cv.take<int32_t>(c.S + 1);
+  b.alt.uniq_tokens =
+      cv.take<int32_t>(static_cast<size_t>(T) * std::min(c.k, c.S));
+  b.alt.expand_idx = cv.take<int32_t>(tk);
+  b.alt.n_dropped = cv.take<int32_t>(1);
+  b.alt.pws = carve_permute_scratch(cv, T, c.E, c.k, c.S);
   if (bytes) *bytes = align_up(cv.off, 256);
   return b;
 }
@@ -201,14 +209,77 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
   return launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
 }
 
+// The chunked fallback with each chunk's permute tables computed one chunk
+// ahead on pp.side, so that they overlap the previous chunk's expert FFN.
+// Chunk i uses table set i % 2 and its own rows of row_of; the tables of
+// chunk i+2 wait for chunk i's combine.  Chunk 0's tables run on s.
+cudaError_t pipelined_passes(const moe_config_t& c, const void* x,
+                             const int32_t* topk_idx, const float* topk_w,
+                             const void* wg, const void* wu, const void* wd,
+                             void* y, const LayerBufs& b, int32_t* status,
+                             cudaStream_t s, int n, const PassPipeline& pp) {
+  const int ct = chunk_tokens(c);
+  const size_t row_bytes = static_cast<size_t>(c.H) * elem_bytes(c.dtype);
+  cudaError_t e;
+  if ((e = cudaEventRecord(pp.fork, s)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(pp.side, pp.fork, 0)) != cudaSuccess)
+    return e;
+  auto tables = [&](int i, cudaStream_t st) -> cudaError_t {
+    const int t0 = i * ct, tc = std::min(ct, c.T - t0);
+    const PassTables tb = b.tables(i);
+    const size_t o = static_cast<size_t>(t0) * c.k;
+    cudaError_t r;
+    if (st == pp.side && i >= 2 &&
+        (r = cudaStreamWaitEvent(st, pp.done[i & 1], 0)) != cudaSuccess)
+      return r;
+    if ((r = launch_permute_tables(sub_config(c, tc), topk_idx + o, -1,
+                                   b.row_of + o, tb.sorted_token,
+                                   tb.group_offsets, tb.uniq_offsets,
+                                   tb.n_dropped, tb.pws, status, st)) !=
+        cudaSuccess)
+      return r;
+    return st == pp.side ? cudaEventRecord(pp.ready[i & 1], st) : cudaSuccess;
+  };
+  for (int i = 0; i < n; ++i) {
+    const int t0 = i * ct, tc = std::min(ct, c.T - t0);
+    const moe_config_t sc = sub_config(c, tc);
+    const PassTables tb = b.tables(i);
+    const size_t o = static_cast<size_t>(t0);
+    e = i == 0 ? tables(0, s) : cudaStreamWaitEvent(s, pp.ready[i & 1], 0);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_permute_scatter(
+             sc, static_cast<const char*>(x) + o * row_bytes,
+             b.row_of + o * c.k, tb.uniq_offsets, b.x_sorted, tb.uniq_tokens,
+             tb.expand_idx, tb.pws, s)) != cudaSuccess ||
+        (e = launch_gmm(sc, identity_groups(sc), b.x_sorted, tb.group_offsets,
+                        wg, wu, wd, b.h, b.y_sorted, status, s)) !=
+            cudaSuccess ||
+        (e = launch_combine(sc, b.y_sorted, b.row_of + o * c.k,
+                            topk_w + o * c.k,
+                            static_cast<char*>(y) + o * row_bytes, s)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(pp.done[i & 1], s)) != cudaSuccess)
+      return e;
+    if (i + 1 < n && (e = tables(i + 1, pp.side)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 // The chunked dropless fallback over precomputed routing.
 cudaError_t chunked_passes(const moe_config_t& c, const void* x,
                            const int32_t* topk_idx, const float* topk_w,
                            const void* wg, const void* wu, const void* wd,
                            void* y, const LayerBufs& b, int32_t* status,
-                           cudaStream_t s, int32_t* n_run) {
+                           cudaStream_t s, int32_t* n_run,
+                           const PassPipeline* pp) {
   const int ct = chunk_tokens(c);
   const size_t row_bytes = static_cast<size_t>(c.H) * elem_bytes(c.dtype);
+  const int n_all = ct > 0 ? (c.T + ct - 1) / ct : 0;
+  if (pp != nullptr && n_all >= 2) {
+    if (n_run) *n_run = n_all;
+    return pipelined_passes(c, x, topk_idx, topk_w, wg, wu, wd, y, b, status,
+                            s, n_all, *pp);
+  }
   int n = 0;
   for (int t0 = 0; t0 < c.T; t0 += ct, ++n) {
     const int tc = std::min(ct, c.T - t0);
@@ -489,6 +560,72 @@ moe_status_t moe_permute_planned(const moe_config_t* cfg, const void* x,
                                     sorted_token, group_offsets, uniq_offsets,
                                     uniq_tokens, expand_idx, n_dropped, ws,
                                     nullptr, stream, plan));
+}
+
+moe_status_t moe_permute_tables(const moe_config_t* cfg,
+                                const int32_t* topk_idx, int32_t capped,
+                                const int32_t* divert,
+                                const int32_t* slot_of, int32_t* row_of,
+                                int32_t* sorted_token,
+                                int32_t* group_offsets,
+                                int32_t* uniq_offsets, int32_t* n_dropped,
+                                void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((divert == nullptr) != (slot_of == nullptr)) return MOE_ERR_INVALID_ARG;
+  const bool planned = divert != nullptr;
+  if (!ok_ptr(group_offsets, false) || !ok_ptr(uniq_offsets, false) ||
+      !ok_ptr(n_dropped, false) ||
+      (planned && (!ok_ptr(divert, false) || !ok_ptr(slot_of, false))))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(topk_idx, false) || !ok_ptr(row_of, false) ||
+                     !ok_ptr(sorted_token, false)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
+  if (workspace == nullptr || workspace_bytes < need ||
+      !ok_ptr(workspace, true))
+    return MOE_ERR_WORKSPACE;
+  Carve cv(workspace);
+  const PermuteScratch ws =
+      carve_permute_scratch(cv, cfg->T, cfg->E, cfg->k, cfg->S);
+  PermutePlan plan;
+  if (planned) {
+    plan.divert = divert;
+    plan.slot_of = slot_of;
+    plan.B = cfg->redundant_slots;
+  }
+  const int64_t cap = capped ? capacity_rows(*cfg) : -1;
+  return cuda_status(launch_permute_tables(*cfg, topk_idx, cap, row_of,
+                                           sorted_token, group_offsets,
+                                           uniq_offsets, n_dropped, ws,
+                                           nullptr, stream, plan));
+}
+
+moe_status_t moe_permute_scatter(const moe_config_t* cfg, const void* x,
+                                 const int32_t* row_of,
+                                 int32_t* uniq_offsets, void* x_sorted,
+                                 int32_t* uniq_tokens, int32_t* expand_idx,
+                                 const void* workspace,
+                                 size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!ok_ptr(uniq_offsets, false)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(x, true) || !ok_ptr(row_of, false) ||
+                     !ok_ptr(x_sorted, true) || !ok_ptr(uniq_tokens, false) ||
+                     !ok_ptr(expand_idx, false)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
+  if (workspace == nullptr || workspace_bytes < need ||
+      !ok_ptr(workspace, true))
+    return MOE_ERR_WORKSPACE;
+  Carve cv(const_cast<void*>(workspace));
+  const PermuteScratch ws =
+      carve_permute_scratch(cv, cfg->T, cfg->E, cfg->k, cfg->S);
+  return cuda_status(launch_permute_scatter(*cfg, x, row_of, uniq_offsets,
+                                            x_sorted, uniq_tokens, expand_idx,
+                                            ws, stream));
 }
 
 moe_status_t moe_gmm_swiglu_mapped(const moe_config_t* cfg, int32_t n_groups,

@@ -80,6 +80,22 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
                            int32_t* expand_idx, int32_t* n_dropped,
                            const PermuteScratch& ws, int32_t* status,
                            cudaStream_t s, const PermutePlan& plan = {});
+// The two halves of launch_permute: the counting-sort tables (row_of,
+// sorted_token, group_offsets, n_dropped, and the scatter's tables in ws),
+// then the row copy with the dedup indices.  uniq_offsets is complete after
+// the scatter.  Between the two, ws must not be reused.
+cudaError_t launch_permute_tables(const moe_config_t& c,
+                                  const int32_t* topk_idx, int64_t cap,
+                                  int32_t* row_of, int32_t* sorted_token,
+                                  int32_t* group_offsets,
+                                  int32_t* uniq_offsets, int32_t* n_dropped,
+                                  const PermuteScratch& ws, int32_t* status,
+                                  cudaStream_t s, const PermutePlan& plan = {});
+cudaError_t launch_permute_scatter(const moe_config_t& c, const void* x,
+                                   const int32_t* row_of,
+                                   int32_t* uniq_offsets, void* x_sorted,
+                                   int32_t* uniq_tokens, int32_t* expand_idx,
+                                   const PermuteScratch& ws, cudaStream_t s);
 cudaError_t launch_plan(const moe_config_t& c, const int32_t* counts,
                         int32_t* divert, int32_t* slot_of,
                         int32_t* group_expert, int32_t* shard_after,
@@ -110,6 +126,12 @@ cudaError_t launch_combine(const moe_config_t& c, const void* y_sorted,
                            void* y, cudaStream_t s);
 
 // Buffers of one layer pass over up to `T` tokens, carved from a workspace.
+// A pass's permute tables (one set per pass in flight).
+struct PassTables {
+  int32_t *sorted_token, *group_offsets, *uniq_offsets, *uniq_tokens,
+      *expand_idx, *n_dropped;
+  PermuteScratch pws;
+};
 struct LayerBufs {
   int32_t *topk_idx, *counts, *offsets, *shard, *flag, *cap;
   float *topk_w, *req;
@@ -119,6 +141,18 @@ struct LayerBufs {
   int32_t *divert, *slot_of, *group_expert, *shard_after, *flag_after;
   PermuteScratch pws;
   void *x_sorted, *h, *y_sorted;
+  PassTables alt;  // a second table set, for pipelined chunked passes
+  PassTables tables(int i) const {  // set i % 2
+    if (i & 1) return alt;
+    return {sorted_token, group_offsets, uniq_offsets, uniq_tokens,
+            expand_idx, n_dropped, pws};
+  }
+};
+// Streams and events for chunked passes whose permute tables run one pass
+// ahead on a side stream (see chunked_passes).
+struct PassPipeline {
+  cudaStream_t side;
+  cudaEvent_t fork, ready[2], done[2];
 };
 LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
                       size_t* bytes);
@@ -130,12 +164,15 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const float* topk_w, int64_t cap, const void* wg,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
                  int32_t* status, cudaStream_t s, bool planned = false);
-// the chunked dropless fallback over routing already in topk_idx/topk_w
+// the chunked dropless fallback over routing already in topk_idx/topk_w.
+// With pp (b carved for all T tokens), the permute tables of chunk i+1 run
+// on pp->side during chunk i's expert FFN, in two table sets.
 cudaError_t chunked_passes(const moe_config_t& c, const void* x,
                            const int32_t* topk_idx, const float* topk_w,
                            const void* wg, const void* wu, const void* wd,
                            void* y, const LayerBufs& b, int32_t* status,
-                           cudaStream_t s, int32_t* n_run);
+                           cudaStream_t s, int32_t* n_run,
+                           const PassPipeline* pp = nullptr);
 moe_status_t validate(const moe_config_t* c);
 bool ok_ptr(const void* p, bool need16);
 bool gmm_shape_ok(const moe_config_t& c);

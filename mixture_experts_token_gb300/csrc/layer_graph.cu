@@ -43,6 +43,23 @@ struct CaptureGuard {  // ends a capture left open by an early return
   }
 };
 
+// Events of one capture, destroyed with it (the graph keeps the edges).
+struct PipelineEvents {
+  cudaEvent_t ev[5] = {};
+  cudaError_t create() {
+    for (auto& e : ev) {
+      const cudaError_t r =
+          cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }
+  ~PipelineEvents() {
+    for (auto e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+};
+
 cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
                   const void* wg, const void* wu, const void* wd, void* y,
                   int32_t* status, const LayerBufs& b, moe_layer_graph* out) {
@@ -94,13 +111,22 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   cudaGraph_t body_overflow = cp.conditional.phGraph_out[0];
   cudaGraph_t body_capped = cp.conditional.phGraph_out[1];
 
-  // body 0: the chunked dropless fallback on the routing already computed
+  // body 0: the chunked dropless fallback on the routing already computed,
+  // each chunk's permute tables a chunk ahead on a second captured stream
   cudaGraph_t tmp = nullptr;
+  CaptureGuard side_s;
+  PipelineEvents pe;
+  if ((e = cudaStreamCreateWithFlags(&side_s.s, cudaStreamNonBlocking)) !=
+          cudaSuccess ||
+      (e = pe.create()) != cudaSuccess)
+    return e;
+  PassPipeline pp{side_s.s, pe.ev[0], {pe.ev[1], pe.ev[2]},
+                  {pe.ev[3], pe.ev[4]}};
   e = cudaStreamBeginCaptureToGraph(body_s.s, body_overflow, nullptr, nullptr,
                                     0, cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
   e = chunked_passes(c, x, b.topk_idx, b.topk_w, wg, wu, wd, y, b, status,
-                     body_s.s, &out->n_chunks);
+                     body_s.s, &out->n_chunks, &pp);
   if (e != cudaSuccess) return e;
   if ((e = cudaStreamEndCapture(body_s.s, &tmp)) != cudaSuccess) return e;
 

@@ -357,6 +357,9 @@ constexpr int kScatterUnroll = 8;
 // (no scan kernel between assign and the scatter).
 constexpr int kInlineUniqCounts = 1024;
 static_assert(kInlineUniqCounts % kScatterThreads == 0, "whole loads");
+inline bool inline_uniq(int nb, int S) {
+  return static_cast<long long>(nb) * S <= kInlineUniqCounts;
+}
 
 // One CTA per token.  The first slice of x[t] (all of it up to 16 KB) is
 // read before the wait for the tables.  Dedup position of (t, j) in shard
@@ -499,14 +502,13 @@ PermuteScratch carve_permute_scratch(Carve& c, int T, int E, int k, int S) {
   return p;
 }
 
-cudaError_t launch_permute(const moe_config_t& c, const void* x,
-                           const int32_t* topk_idx, int64_t cap,
-                           void* x_sorted, int32_t* row_of,
-                           int32_t* sorted_token, int32_t* group_offsets,
-                           int32_t* uniq_offsets, int32_t* uniq_tokens,
-                           int32_t* expand_idx, int32_t* n_dropped,
-                           const PermuteScratch& ws, int32_t* status,
-                           cudaStream_t s, const PermutePlan& plan) {
+cudaError_t launch_permute_tables(const moe_config_t& c,
+                                  const int32_t* topk_idx, int64_t cap,
+                                  int32_t* row_of, int32_t* sorted_token,
+                                  int32_t* group_offsets,
+                                  int32_t* uniq_offsets, int32_t* n_dropped,
+                                  const PermuteScratch& ws, int32_t* status,
+                                  cudaStream_t s, const PermutePlan& plan) {
   const int nb = (c.T + TB - 1) / TB;
   cudaError_t e = cudaSuccess;
   if (nb > 0) {
@@ -532,22 +534,44 @@ cudaError_t launch_permute(const moe_config_t& c, const void* x,
         cudaSuccess)
       return e;
   }
-  const int inline_uniq =
-      static_cast<long long>(nb) * c.S <= kInlineUniqCounts ? 1 : 0;
-  if (nb > 0 && !inline_uniq &&
+  if (nb > 0 && !inline_uniq(nb, c.S) &&
       (e = launch_dependent(scan_uniq_kernel, 1, 64, 0, s, ws.block_ucnt, nb,
                             c.S, uniq_offsets)) != cudaSuccess)
     return e;
-  if (c.T > 0) {
-    const int n16 = c.H * elem_bytes(c.dtype) / 16;
-    if ((e = launch_dependent(scatter_kernel, c.T, kScatterThreads, 0, s,
-                              static_cast<const int4*>(x), n16, c.k, c.S, nb,
-                              inline_uniq, row_of, ws.block_ucnt, ws.urank,
-                              uniq_offsets, static_cast<int4*>(x_sorted),
-                              expand_idx, uniq_tokens)) != cudaSuccess)
-      return e;
-  }
   return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scatter(const moe_config_t& c, const void* x,
+                                   const int32_t* row_of,
+                                   int32_t* uniq_offsets, void* x_sorted,
+                                   int32_t* uniq_tokens, int32_t* expand_idx,
+                                   const PermuteScratch& ws, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int nb = (c.T + TB - 1) / TB;
+  const int n16 = c.H * elem_bytes(c.dtype) / 16;
+  return launch_dependent(scatter_kernel, c.T, kScatterThreads, 0, s,
+                          static_cast<const int4*>(x), n16, c.k, c.S, nb,
+                          inline_uniq(nb, c.S) ? 1 : 0, row_of,
+                          ws.block_ucnt, ws.urank, uniq_offsets,
+                          static_cast<int4*>(x_sorted), expand_idx,
+                          uniq_tokens);
+}
+
+cudaError_t launch_permute(const moe_config_t& c, const void* x,
+                           const int32_t* topk_idx, int64_t cap,
+                           void* x_sorted, int32_t* row_of,
+                           int32_t* sorted_token, int32_t* group_offsets,
+                           int32_t* uniq_offsets, int32_t* uniq_tokens,
+                           int32_t* expand_idx, int32_t* n_dropped,
+                           const PermuteScratch& ws, int32_t* status,
+                           cudaStream_t s, const PermutePlan& plan) {
+  const cudaError_t e =
+      launch_permute_tables(c, topk_idx, cap, row_of, sorted_token,
+                            group_offsets, uniq_offsets, n_dropped, ws,
+                            status, s, plan);
+  if (e != cudaSuccess) return e;
+  return launch_permute_scatter(c, x, row_of, uniq_offsets, x_sorted,
+                                uniq_tokens, expand_idx, ws, s);
 }
 
 }  // namespace moe

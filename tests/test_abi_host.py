@@ -91,6 +91,20 @@ def test_bad_arguments_are_rejected_before_any_launch(m):
     st = m.lib().moe_permute(ctypes.byref(c), p, p, 1, p, p, p, p, p, p, p, p,
                              p, 16, None)
     assert st == m.MOE_ERR_WORKSPACE
+    # the two halves of the permute: a plan needs both of its arrays, and
+    # each half needs the permute workspace
+    st = m.lib().moe_permute_tables(ctypes.byref(c), p, 1, p, None, p, p, p,
+                                    p, p, p, 1 << 20, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    st = m.lib().moe_permute_tables(ctypes.byref(c), p, 1, None, None, p, p,
+                                    p, p, p, p, 16, None)
+    assert st == m.MOE_ERR_WORKSPACE
+    st = m.lib().moe_permute_scatter(ctypes.byref(c), p, p, p, p, p, p, None,
+                                     0, None)
+    assert st == m.MOE_ERR_WORKSPACE
+    st = m.lib().moe_permute_scatter(ctypes.byref(c), ctypes.c_void_p(fake + 8),
+                                     p, p, p, p, p, p, 1 << 20, None)
+    assert st == m.MOE_ERR_INVALID_ARG
     # bf16 GEMM shape outside the tensor-core kernels
     c2 = cfg_of(m, H=72, F=128)
     st = m.lib().moe_gmm_swiglu(ctypes.byref(c2), p, p, p, p, p, p, p, None,

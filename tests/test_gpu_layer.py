@@ -160,3 +160,24 @@ def test_layer_edge_cases():
         want = ref.layer_dropless(oracle_cfg(wl), f64(x), Lg,
                                   ref.dense_weights(*(f64(w) for w in W)))
         assert ref.normwise_error(f64(y), want.y) <= 2e-2
+
+
+@pytest.mark.parametrize("n_chunks,slots", [(5, 0), (2, 0), (0, 2)])
+def test_pipelined_stepwise_passes_equal_moe_layer(n_chunks, slots):
+    """bench.py's stepwise step -- each pass's permute tables on a side
+    stream during the previous pass's FFN, two table sets in turn -- gives
+    the bits of moe_layer (5 chunks reuse each table set twice)."""
+    import bench
+    from synth import WORKLOADS
+    wl = WORKLOADS["small"].with_(T=3000, n_chunks=n_chunks,
+                                  redundant_slots=slots)
+    layer = bench.Layer(wl, "cuda")
+    passes = layer.step()
+    torch.cuda.synchronize()
+    y_api = torch.empty_like(layer.b["y"])
+    info = layer.api_layer(layer.x, layer.logits, y_api)
+    torch.cuda.synchronize()
+    assert int(layer.b["status"].item()) == 0
+    if n_chunks:
+        assert info["overflow"] and len(passes) == n_chunks
+    assert torch.equal(y_api, layer.b["y"])

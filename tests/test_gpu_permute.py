@@ -88,3 +88,44 @@ def test_dedup_counts_adversarial():
     uo = np_(bufs["uniq_offsets"])
     assert uo[1] == wl.T and uo[-1] == wl.T
     assert np.array_equal(np_(bufs["uniq_tokens"])[:wl.T], np.arange(wl.T))
+
+
+SPLIT_CASES = [WORKLOADS["small"], WORKLOADS["dsv3"],
+               [c for c in CASES if c.name == "s64"][0],
+               [c for c in CASES if c.name == "t20000"][0]]
+
+
+@pytest.mark.parametrize("wl", SPLIT_CASES, ids=lambda w: w.name)
+def test_permute_split_equals_whole(wl):
+    """moe_permute_tables then moe_permute_scatter (on another stream, after
+    an event) write exactly the bits of moe_permute."""
+    import mixture_experts_token_gb300 as moe
+    cfg = cfg_from(wl)
+    x, L = inputs(wl)
+    idx, _ = gpu_route(cfg, L)
+    side = torch.cuda.Stream()
+    for capped in (True, False):
+        whole = gpu_permute(cfg, x, idx, capped)
+        b = moe.alloc_step_buffers(cfg)
+        b["x_sorted"].zero_()
+        for k in ("sorted_token", "uniq_tokens", "expand_idx"):
+            b[k].fill_(-1)
+        moe.moe_permute_tables(cfg, idx, capped, b["row_of"],
+                               b["sorted_token"], b["group_offsets"],
+                               b["uniq_offsets"], b["n_dropped"],
+                               b["permute_ws"])
+        ev = torch.cuda.Event()
+        ev.record()
+        side.wait_event(ev)
+        moe.moe_permute_scatter(cfg, x, b["row_of"], b["uniq_offsets"],
+                                b["x_sorted"], b["uniq_tokens"],
+                                b["expand_idx"], b["permute_ws"], stream=side)
+        torch.cuda.synchronize()
+        R = int(np_(whole["group_offsets"])[-1])
+        U = int(np_(whole["uniq_offsets"])[-1])
+        for k in ("row_of", "group_offsets", "uniq_offsets", "n_dropped"):
+            assert torch.equal(b[k], whole[k]), k
+        for k, n in (("sorted_token", R), ("expand_idx", R),
+                     ("uniq_tokens", U)):
+            assert torch.equal(b[k][:n], whole[k][:n]), k
+        assert torch.equal(b["x_sorted"][:R], whole["x_sorted"][:R])

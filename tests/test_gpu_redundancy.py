@@ -86,6 +86,18 @@ def test_plan_and_permute_parity(wl, B):
         torch.cuda.synchronize()
         want = ref.permute_indices(vidx, G, wl.S, C if capped else None)
         compare_permutation(bufs, want, x.cpu() if wl.T <= 8192 else None)
+        # the same plan through the two halves of the permute
+        b2 = moe.alloc_step_buffers(cfg)
+        moe.moe_permute_tables(cfg, idx, capped, b2["row_of"],
+                               b2["sorted_token"], b2["group_offsets"],
+                               b2["uniq_offsets"], b2["n_dropped"],
+                               b2["permute_ws"], divert=d["divert"],
+                               slot_of=d["slot_of"])
+        moe.moe_permute_scatter(cfg, x, b2["row_of"], b2["uniq_offsets"],
+                                b2["x_sorted"], b2["uniq_tokens"],
+                                b2["expand_idx"], b2["permute_ws"])
+        torch.cuda.synchronize()
+        compare_permutation(b2, want, x.cpu() if wl.T <= 8192 else None)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
