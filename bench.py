@@ -608,6 +608,18 @@ def main():
 
     step_ms = [sum(d for _, d in st.durations()) for st in timers]
     mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
+    median_ms = float(np.median(step_ms))
+
+    # Warm L2: the same steps back to back, no flush in between (outside the
+    # timed region; the headline value is the flushed, cold one).
+    warm_ms = []
+    for _ in range(args.steps):
+        st = StageTimer()
+        layer.step(st)
+        warm_ms.append(st)
+    torch.cuda.synchronize()
+    warm_ms = [sum(d for _, d in st.durations()) for st in warm_ms]
+    warm_mean = max_over_ranks(sum(warm_ms) / len(warm_ms), device)
 
     # The same steps with the GPU held until the host has queued the first
     # pass: the stage times of the kernels alone, without the host's launch
@@ -730,6 +742,11 @@ def main():
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "wall_s_timed_loop": round(wall, 3),
+        "ms_per_step_median": round(median_ms, 4),
+        "warm_l2": {"value": round(whole_job_tokens_per_s(
+            world, layer.wl.T, warm_mean), 1), "unit": UNIT,
+            "ms_per_step": round(warm_mean, 4),
+            "note": "no L2 flush between steps (outside the timed region)"},
         "gpu_launches": launches_per_step(
             passes, args.mode, layer.dispatch_only,
             int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"))

@@ -405,6 +405,9 @@ moe_status_t moe_layer(const moe_config_t *cfg, const void *x,
  * (an extension).  The branch of [PR5920 How] is a conditional IF node:
  * the check kernel's flag selects, on the device, either the chunked
  * dropless passes or the capped pass, so a launch never waits on the host.
+ * In the chunked branch each chunk's permute tables (moe_permute_tables)
+ * run on a second branch of the graph during the previous chunk's expert
+ * FFN; the results are those of moe_layer, bit for bit.
  *   create: validates like moe_layer (T >= 1), captures the graph on the
  *     current device and instantiates it; the graph stays bound to x,
  *     logits, the weights, y, status_word and workspace (refresh x and the
