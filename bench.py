@@ -1335,7 +1335,8 @@ def backward_main(layer, args, world, rank, device):
     if clock_rec:
         out["clocks"] = clock_rec
     if not args.no_e2e:
-        out["e2e"] = backward_e2e(bw, args, world, device)
+        out["e2e"] = backward_e2e_pipelined(bw, args, world, device)
+        out["e2e"]["serial"] = backward_e2e(bw, args, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = BWD_CPU_SAMPLE.get(w.name, 8)
         sec, n = oracle_backward_sample(w, layer.x, layer.logits_np, layer.W,
@@ -1395,6 +1396,75 @@ def backward_e2e(bw, args, world, device):
             "unit": UNIT, "ms_per_step": round(mean, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "api": "moe_layer_backward (C ABI), pinned host buffers"}
+
+
+def backward_e2e_pipelined(bw, args, world, device):
+    """moe_layer_backward end to end with two sets of device inputs and
+    outputs: step i+1's x, logits and dy go in on one copy stream while step
+    i runs, step i's dx and dlogits come out on another while step i+1 runs.
+    One workspace and one compute stream: the backward steps themselves run
+    one after another."""
+    lay = bw.layer
+    x_h = lay.x.cpu().pin_memory()
+    L_h = lay.logits.cpu().pin_memory()
+    dy_h = bw.dy.cpu().pin_memory()
+    outs_h = [(torch.empty(bw.dx.shape, dtype=bw.dx.dtype, pin_memory=True),
+               torch.empty(bw.dl.shape, dtype=bw.dl.dtype, pin_memory=True))
+              for _ in range(2)]
+    sets = [tuple(torch.empty_like(t) for t in
+                  (lay.x, lay.logits, bw.dy, bw.dx, bw.dl)) for _ in range(2)]
+    bw.dw_api = bw.dw
+    comp = torch.cuda.current_stream()
+    up = torch.cuda.Stream(device=device)     # host -> device
+    down = torch.cuda.Stream(device=device)   # device -> host
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    free = [ev(), ev()]
+    for e in free:
+        e.record(down)
+
+    def steps(n):
+        for i in range(n):
+            b = i % 2
+            x_d, L_d, dy_d, dx_d, dl_d = sets[b]
+            with torch.cuda.stream(up):
+                up.wait_event(free[b])       # set b's last outputs are out
+                x_d.copy_(x_h, non_blocking=True)
+                L_d.copy_(L_h, non_blocking=True)
+                dy_d.copy_(dy_h, non_blocking=True)
+                h2d = ev()
+                h2d.record(up)
+            comp.wait_event(h2d)
+            bw.api(x_d, L_d, dy_d, dx_d, dl_d)
+            done = ev()
+            done.record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done)
+                outs_h[b][0].copy_(dx_d, non_blocking=True)
+                outs_h[b][1].copy_(dl_d, non_blocking=True)
+                free[b].record(down)
+
+    steps(max(1, args.warmup))
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    up.wait_event(a)
+    down.wait_event(a)
+    steps(args.steps)
+    comp.wait_stream(up)
+    comp.wait_stream(down)
+    z.record(comp)
+    z.synchronize()
+    mean = max_over_ranks(a.elapsed_time(z) / args.steps, device)
+    if not torch.equal(outs_h[(args.steps - 1) % 2][0], bw.dx.cpu()):
+        raise SystemExit("pipelined end-to-end backward output differs")
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, L_h, dy_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
+    return {"value": round(whole_job_tokens_per_s(world, lay.wl.T, mean), 1),
+            "unit": UNIT, "ms_per_step": round(mean, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "api": "moe_layer_backward (C ABI), pinned host buffers, copies "
+                   "on two copy streams overlapping neighbouring steps"}
 
 
 def reference_arm(args, wl, device):
