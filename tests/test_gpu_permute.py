@@ -76,6 +76,20 @@ def test_permute_t0():
     assert np.all(np_(bufs["group_offsets"]) == 0)
     assert np.all(np_(bufs["uniq_offsets"]) == 0)
     assert int(np_(bufs["n_dropped"])[0]) == 0
+    # the two halves with no tokens: the same zeros, nothing else written
+    import mixture_experts_token_gb300 as moe
+    b = moe.alloc_step_buffers(cfg)
+    for k in ("group_offsets", "uniq_offsets", "n_dropped"):
+        b[k].fill_(7)
+    moe.moe_permute_tables(cfg, idx, True, b["row_of"], b["sorted_token"],
+                           b["group_offsets"], b["uniq_offsets"],
+                           b["n_dropped"], b["permute_ws"])
+    moe.moe_permute_scatter(cfg, x, b["row_of"], b["uniq_offsets"],
+                            b["x_sorted"], b["uniq_tokens"], b["expand_idx"],
+                            b["permute_ws"])
+    torch.cuda.synchronize()
+    for k in ("group_offsets", "uniq_offsets", "n_dropped"):
+        assert np.all(np_(b[k]) == 0), k
 
 
 def test_dedup_counts_adversarial():
