@@ -125,13 +125,13 @@ cudaError_t launch_combine(const moe_config_t& c, const void* y_sorted,
                            const int32_t* row_of, const float* topk_w,
                            void* y, cudaStream_t s);
 
-// Buffers of one layer pass over up to `T` tokens, carved from a workspace.
 // A pass's permute tables (one set per pass in flight).
 struct PassTables {
   int32_t *sorted_token, *group_offsets, *uniq_offsets, *uniq_tokens,
       *expand_idx, *n_dropped;
   PermuteScratch pws;
 };
+// Buffers of one layer pass over up to `T` tokens, carved from a workspace.
 struct LayerBufs {
   int32_t *topk_idx, *counts, *offsets, *shard, *flag, *cap;
   float *topk_w, *req;
