@@ -249,6 +249,7 @@ class Layer:
                      {k: torch.empty_like(self.b[k]) for k in keys}]
         self.side = torch.cuda.Stream(device=device)
         self.pass_events = []   # (tables ready, pass done) per pass, reused
+        self.spec_ready = torch.cuda.Event()
 
     def sub(self, t0, t1, capped):
         """Pass over tokens [t0, t1): the config the library uses."""
@@ -281,6 +282,14 @@ class Layer:
             moe.moe_plan_duplication(c, b["expert_counts"], b["divert"],
                                      b["slot_of"], b["group_expert"],
                                      b["shard_after"], b["flag_after"])
+        # The first fallback chunk's tables do not depend on the flag: they
+        # run on the side stream while the host reads it, and are dropped
+        # if the layer takes the capped pass.
+        spec = (0, min(c.T, self.chunk), False) if c.T > 0 else None
+        if spec is not None:
+            self.side.wait_stream(torch.cuda.current_stream())
+            self._tables(spec, 0, self.side, self.spec_ready,
+                         getattr(mark, "side", None))
         mark("flag")
         flag = int((b["flag_after"] if planned else b["overflow_flag"]).item())
         if not flag:
@@ -288,14 +297,44 @@ class Layer:
         else:
             passes = [(t0, min(c.T, t0 + self.chunk), False)
                       for t0 in range(0, c.T, self.chunk)]
-        return self._passes(passes, mark, hold_cycles)
+        return self._passes(passes, mark, hold_cycles, spec)
 
-    def _passes(self, passes, mark, hold_cycles=0):
+    def _tables(self, pas, i, stream, ready, side_times=None, after=None):
+        """Permute tables of pass i over tokens pas = (t0, t1, capped) into
+        table set i % 2, on `stream` (after event `after`, if given);
+        records `ready`.  Side-stream work is timed into side_times."""
+        moe, b = self.moe, self.b
+        t0, t1, capped = pas
+        sc = self.sub(t0, t1, capped)
+        tb = self.tabs[i % 2]
+        plan = {}
+        if capped and sc.redundant_slots > 0:
+            plan = dict(divert=b["divert"], slot_of=b["slot_of"])
+        timed = side_times is not None and stream is self.side
+        with torch.cuda.stream(stream):
+            if after is not None:
+                stream.wait_event(after)
+            if timed:
+                ev0 = torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+            moe.moe_permute_tables(
+                sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
+                tb["sorted_token"], tb["group_offsets"], tb["uniq_offsets"],
+                tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
+            ready.record(stream)
+            if timed:
+                ev1 = torch.cuda.Event(enable_timing=True)
+                ev1.record(stream)
+                side_times.append((ev0, ev1))
+
+    def _passes(self, passes, mark, hold_cycles=0, spec=None):
         """The passes, each: permute tables -> row scatter -> GEMM1 ->
-        GEMM2 -> combine.  The first pass's tables run on the main stream;
-        those of pass i+1 are queued on the side stream after pass i's
-        work, so they run during pass i's FFN.  They reuse the table set of
-        pass i-1 and wait for that pass's combine."""
+        GEMM2 -> combine.  The first pass's tables run on the main stream,
+        unless spec (the first fallback chunk, whose tables the side stream
+        computed during the flag read) is that pass; those of pass i+1 are
+        queued on the side stream after pass i's work, so they run during
+        pass i's FFN.  They reuse the table set of pass i-1 and wait for
+        that pass's combine."""
         moe, b, W = self.moe, self.b, self.W
         if hold_cycles:
             mark("hold")
@@ -309,29 +348,8 @@ class Layer:
         side_times = getattr(mark, "side", None)
 
         def tables(i, stream):
-            t0, t1, capped = passes[i]
-            sc = self.sub(t0, t1, capped)
-            tb = self.tabs[i % 2]
-            plan = {}
-            if capped and sc.redundant_slots > 0:
-                plan = dict(divert=b["divert"], slot_of=b["slot_of"])
-            timed = side_times is not None and stream is side
-            with torch.cuda.stream(stream):
-                if i >= 2:
-                    stream.wait_event(done[i - 2])
-                if timed:
-                    ev0 = torch.cuda.Event(enable_timing=True)
-                    ev0.record(stream)
-                moe.moe_permute_tables(
-                    sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
-                    tb["sorted_token"], tb["group_offsets"],
-                    tb["uniq_offsets"], tb["n_dropped"], tb["permute_ws"],
-                    stream=stream, **plan)
-                ready[i].record(stream)
-                if timed:
-                    ev1 = torch.cuda.Event(enable_timing=True)
-                    ev1.record(stream)
-                    side_times.append((ev0, ev1))
+            self._tables(passes[i], i, stream, ready[i], side_times,
+                         done[i - 2] if i >= 2 else None)
 
         for i, (t0, t1, capped) in enumerate(passes):
             sc = self.sub(t0, t1, capped)
@@ -342,7 +360,11 @@ class Layer:
                 groups = dict(n_groups=sc.E + sc.S * sc.redundant_slots,
                               group_expert=b["group_expert"])
             mark("permute")
-            if i == 0:
+            if i == 0 and spec is not None and passes[0] == spec:
+                main.wait_event(self.spec_ready)   # computed during the flag
+            elif i == 0:
+                if spec is not None:
+                    main.wait_event(self.spec_ready)  # set 0 is free again
                 tables(0, main)
             else:
                 main.wait_event(ready[i])
@@ -667,9 +689,10 @@ def main():
                            "until the host has queued it; HBM fraction of "
                            "the measured copy peak. permute = the row "
                            "scatter (plus the first pass's tables); "
-                           "permute_tables = the counting-sort kernels of "
-                           "passes 2.. on the side stream, each overlapping "
-                           "the previous pass's expert FFN",
+                           "permute_tables = the counting-sort kernels on "
+                           "the side stream: the first fallback chunk's "
+                           "during the overflow-flag read, each later "
+                           "chunk's during the previous chunk's expert FFN",
                    "permute_tables": {"ms_per_step":
                                       round(side_ms / args.steps, 4),
                                       "stream": "side"}}
