@@ -30,6 +30,10 @@
 // its predecessor has started, does the work that needs none of its
 // predecessor's output (assign: the lane masks from the routing indices;
 // scatter: the read of x[t]), and then waits for its predecessor to finish.
+// launch_permute_tables runs kernels 1 to 4, launch_permute_scatter kernel 5
+// (a caller may run the two on different streams, ordered by an event, so
+// that one chunk's tables overlap the previous chunk's expert FFN);
+// launch_permute runs both on one stream.
 // With a duplication plan ("Moe dynamic redundancy" (MaxText pull request
 // 4760), review of plan_expert_duplication) the groups are virtual: shard s
 // owns its E/S experts and then its B duplicate slots, and the last
