@@ -1021,6 +1021,34 @@ class Backward:
                 torch.empty((rr, F), dtype=dt, device=dev) for _ in range(3))
             self.off2 = torch.empty(G + 1, dtype=torch.int32, device=dev)
         self.ws = moe.layer_workspace(c, moe.MOE_WS_LAYER_BACKWARD, dev)
+        # every pass keeps its own rows, row_of rows and group offsets; the
+        # dedup outputs and the permute scratch come in two sets, so that a
+        # pass's permute tables can run on the side stream ahead of it
+        b = layer.b
+        keys = ("uniq_offsets", "uniq_tokens", "n_dropped", "permute_ws")
+        self.tabs = [{k: b[k] for k in keys},
+                     {k: torch.empty_like(b[k]) for k in keys}]
+        self.spec_ready = torch.cuda.Event()
+        self.pass_events = []   # (tables ready, scatter done) per pass
+
+    def tables(self, pas, i, stream, ready, after=None, on_plan=False):
+        """Permute tables of backward pass i (tokens pas = (t0, t1, capped))
+        into its own row ranges and dedup set i % 2, on `stream`."""
+        lay = self.layer
+        moe, b, k = lay.moe, lay.b, lay.cfg.k
+        t0, t1, capped = pas
+        sc = lay.sub(t0, t1, capped)
+        tb = self.tabs[i % 2]
+        plan = dict(divert=b["divert"], slot_of=b["slot_of"]) if on_plan \
+            else {}
+        with torch.cuda.stream(stream):
+            if after is not None:
+                stream.wait_event(after)
+            moe.moe_permute_tables(
+                sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
+                b["sorted_token"][t0 * k:], self.goff[i], tb["uniq_offsets"],
+                tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
+            ready.record(stream)
 
     def step(self, ev=None):
         L = self
@@ -1043,9 +1071,16 @@ class Backward:
             moe.moe_plan_duplication(c, b["expert_counts"], b["divert"],
                                      b["slot_of"], b["group_expert"],
                                      b["shard_after"], b["flag_after"])
+        main, side = torch.cuda.current_stream(), lay.side
+        spec = None
         if lay.mode != "fallback":
             passes = [(0, c.T, lay.mode == "capped")]
         else:
+            # the first fallback chunk's tables during the flag read
+            if c.T > 0:
+                spec = (0, min(c.T, lay.chunk), False)
+                side.wait_stream(main)
+                L.tables(spec, 0, side, L.spec_ready)
             mark("flag")
             flag = b["flag_after"] if planned else b["overflow_flag"]
             if int(flag.item()):
@@ -1058,27 +1093,39 @@ class Backward:
         grp = dict(n_groups=L.G, group_expert=b["group_expert"]) \
             if on_plan else {}
         xs, h, ys = b["x_sorted"], b["h"], b["y_sorted"]
+        side.wait_stream(main)
+        while len(L.pass_events) < len(passes):
+            L.pass_events.append((torch.cuda.Event(), torch.cuda.Event()))
+        ready = [e[0] for e in L.pass_events]
+        scattered = [e[1] for e in L.pass_events]
         for i, (t0, t1, capped) in enumerate(passes):
             sc = lay.sub(t0, t1, capped)
             r0 = t0 * k
             go = L.goff[i]
+            tb = L.tabs[i % 2]
             mark("permute")
-            if on_plan:
-                moe.moe_permute_planned(
-                    sc, lay.x[t0:t1], b["topk_idx"][t0:t1], capped,
-                    b["divert"], b["slot_of"], xs[r0:], b["row_of"][t0:t1],
-                    b["sorted_token"][r0:], go, b["uniq_offsets"],
-                    b["uniq_tokens"], b["expand_idx"][r0:], b["n_dropped"],
-                    b["permute_ws"])
+            if i == 0 and spec is not None and passes[0] == spec:
+                main.wait_event(L.spec_ready)
+            elif i == 0:
+                if spec is not None:
+                    main.wait_event(L.spec_ready)   # set 0 is free again
+                L.tables(passes[0], 0, main, ready[0], on_plan=on_plan)
             else:
-                moe.moe_permute(sc, lay.x[t0:t1], b["topk_idx"][t0:t1],
-                                capped, xs[r0:], b["row_of"][t0:t1],
-                                b["sorted_token"][r0:], go, b["uniq_offsets"],
-                                b["uniq_tokens"], b["expand_idx"][r0:],
-                                b["n_dropped"], b["permute_ws"])
+                main.wait_event(ready[i])
+            moe.moe_permute_scatter(sc, lay.x[t0:t1], b["row_of"][t0:t1],
+                                    tb["uniq_offsets"], xs[r0:],
+                                    tb["uniq_tokens"], b["expand_idx"][r0:],
+                                    tb["permute_ws"])
+            scattered[i].record(main)
             mark("gmm_gate_up_saved")
             moe.moe_gmm_gate_up_saved(sc, xs[r0:], go, W[0], W[1], L.g[r0:],
                                       L.u[r0:], h[r0:], b["status"], **grp)
+            if i + 1 < len(passes):
+                # queued once the GPU has this pass's GEMM to run; the next
+                # pass's tables reuse the dedup set of pass i-1, which only
+                # that pass's scatter reads
+                L.tables(passes[i + 1], i + 1, side, ready[i + 1],
+                         scattered[i - 1] if i >= 1 else None)
             mark("gmm_down")
             moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"],
                              **grp)
