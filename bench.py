@@ -16,10 +16,18 @@ target is stated.
 The timed loop calls the C ABI entry points in the order moe_layer runs them
 (the check that both give identical bits is part of the run), with CUDA
 events on the launch stream around every launch group, so the per-kernel
-durations of the roofline come from the same timed region.  L2 is flushed
-(a 256 MiB write) between steps, outside the events.  ``e2e`` is the same
-metric through moe_layer with pinned host buffers, the host->device copies
-of x and the logits and the device->host copy of y inside the timed region.
+durations of the roofline come from the same timed region.  Each pass's
+permute tables (moe_permute_tables) run on a side stream one pass ahead --
+the first fallback chunk's during the overflow-flag read -- and the row
+scatter (moe_permute_scatter) on the launch stream.  L2 is flushed (a 256 MiB
+write) between steps, outside the events.  Outside the timed region the same
+steps run twice more with the GPU held (a sleep) until the host has queued
+the passes: with the flush (``stages_host_held``: the kernels' stage times
+without host launch latency) and without it (``warm_l2``).  ``e2e`` is the
+same metric through moe_layer_graph with pinned host buffers, the
+host->device copies of x and the logits and the device->host copy of y
+inside the timed region, overlapping the neighbouring steps on two copy
+streams (``e2e.serial``: through moe_layer, copies in line).
 ``cpu_baseline`` is the float64 oracle timed on a bounded token sample of the
 same workload on the host cores.
 
@@ -27,9 +35,11 @@ same workload on the host cores.
 route -> check -> per pass: permute, GEMM1 keeping g and u, GEMM2, combine
 backward, down-projection dgrad with the SwiGLU backward, gate/up dgrad,
 permute backward -> route backward -> the two weight-gradient GEMMs over
-the rows of every pass (one launch each).  Its ``e2e`` goes through
-moe_layer_backward with x, logits and dy copied in and dx and dlogits
-copied out every step; the weight gradients stay in HBM.  With torchrun (N > 1) every rank runs an
+the rows of every pass (one launch each), the permute tables again a pass
+ahead on the side stream.  Its ``e2e`` goes through moe_layer_backward with
+x, logits and dy copied in and dx and dlogits copied out every step, the
+copies overlapping the neighbouring steps (``e2e.serial``: in line); the
+weight gradients stay in HBM.  With torchrun (N > 1) every rank runs an
 independent replica on its own tokens (weak scaling, no collective on the
 data path); the reported time is the max over ranks.
 """
