@@ -1186,20 +1186,18 @@ class Backward:
                                       mode, self.ws, self.layer.b["status"])
 
 
-def backward_launches(passes, mode, regroup, planned=False, on_plan=False):
+def backward_launches(passes, mode, regroup, planned=False):
     """Kernel launches of one backward step: route (+ check, + the plan with
     duplicate slots), per pass permute 4 + GEMM1-saved + GEMM2 + combine
     backward + two dgrad GEMMs + permute backward, route backward, the
     regrouping of the rows (2) or the row segments in batches of 16, and per
-    batch the two weight-gradient GEMMs (+ the two zero fills of experts
-    without rows in the first batch; over the plan's groups a memset
-    replaces them)."""
+    batch the two weight-gradient GEMMs, plus the two fills in the first
+    batch that zero the experts not written by exactly one group."""
     n = len(passes)
     batches = 1 if regroup else (n + 15) // 16
     head = 1 + (1 if (mode == "fallback" or planned) else 0) + \
         (1 if planned else 0)
-    return head + 10 * n + 1 + (2 if regroup else 0) + 2 * batches + \
-        (0 if on_plan else 2)
+    return head + 10 * n + 1 + (2 if regroup else 0) + 2 * batches + 2
 
 
 def backward_work(w, accs):
@@ -1406,8 +1404,8 @@ def backward_main(layer, args, world, rank, device):
         },
         "wall_s_timed_loop": round(wall, 3),
         "gpu_launches": backward_launches(
-            passes, layer.mode, bw.regroup and len(passes) <= 64, planned,
-            on_plan) * args.steps,
+            passes, layer.mode, bw.regroup and len(passes) <= 64,
+            planned) * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }
