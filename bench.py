@@ -16,10 +16,10 @@ target is stated.
 The timed loop calls the C ABI entry points in the order moe_layer runs them
 (the check that both give identical bits is part of the run), with CUDA
 events on the launch stream around every launch group, so the per-kernel
-durations of the roofline come from the same timed region.  Each pass's
-permute tables (moe_permute_tables) run on a side stream one pass ahead --
-the first fallback chunk's during the overflow-flag read -- and the row
-scatter (moe_permute_scatter) on the launch stream.  L2 is flushed (a 256 MiB
+durations of the roofline come from the same timed region.  From the
+second pass on, each pass's permute tables (moe_permute_tables) run on a
+side stream during the previous pass's expert FFN; the row scatter
+(moe_permute_scatter) runs on the launch stream.  L2 is flushed (a 256 MiB
 write) between steps, outside the events.  Outside the timed region the same
 steps run twice more with the GPU held (a sleep) until the host has queued
 the passes: with the flush (``stages_host_held``: the kernels' stage times
@@ -259,14 +259,19 @@ class Layer:
                      {k: torch.empty_like(self.b[k]) for k in keys}]
         self.side = torch.cuda.Stream(device=device)
         self.pass_events = []   # (tables ready, pass done) per pass, reused
-        self.spec_ready = torch.cuda.Event()
+        self.routed = torch.cuda.Event()   # the step's routing is done
+        self._subs = {}
 
     def sub(self, t0, t1, capped):
-        """Pass over tokens [t0, t1): the config the library uses."""
+        """Pass over tokens [t0, t1): the config the library uses (built
+        once per pass shape)."""
         if capped:
             return self.cfg
-        return self.cfg.with_(T=t1 - t0, ragged_buffer_factor=-1.0,
-                              n_chunks=0, redundant_slots=0)
+        key = t1 - t0
+        if key not in self._subs:
+            self._subs[key] = self.cfg.with_(T=key, ragged_buffer_factor=-1.0,
+                                             n_chunks=0, redundant_slots=0)
+        return self._subs[key]
 
     def step(self, ev=None, hold_cycles=0):
         """One layer step through the entry points; ev(name) marks stages.
@@ -278,6 +283,7 @@ class Layer:
         mark = ev or (lambda name: None)
         mark("route")
         moe.moe_route(c, self.logits, b["topk_idx"], b["topk_w"], b["status"])
+        self.routed.record()   # the side stream's tables start after it
         if self.mode != "fallback":
             passes = [(0, c.T, self.mode == "capped")]
             return self._passes(passes, mark, hold_cycles)
@@ -292,14 +298,6 @@ class Layer:
             moe.moe_plan_duplication(c, b["expert_counts"], b["divert"],
                                      b["slot_of"], b["group_expert"],
                                      b["shard_after"], b["flag_after"])
-        # The first fallback chunk's tables do not depend on the flag: they
-        # run on the side stream while the host reads it, and are dropped
-        # if the layer takes the capped pass.
-        spec = (0, min(c.T, self.chunk), False) if c.T > 0 else None
-        if spec is not None:
-            self.side.wait_stream(torch.cuda.current_stream())
-            self._tables(spec, 0, self.side, self.spec_ready,
-                         getattr(mark, "side", None))
         mark("flag")
         flag = int((b["flag_after"] if planned else b["overflow_flag"]).item())
         if not flag:
@@ -307,7 +305,7 @@ class Layer:
         else:
             passes = [(t0, min(c.T, t0 + self.chunk), False)
                       for t0 in range(0, c.T, self.chunk)]
-        return self._passes(passes, mark, hold_cycles, spec)
+        return self._passes(passes, mark, hold_cycles)
 
     def _tables(self, pas, i, stream, ready, side_times=None, after=None):
         """Permute tables of pass i over tokens pas = (t0, t1, capped) into
@@ -321,36 +319,33 @@ class Layer:
         if capped and sc.redundant_slots > 0:
             plan = dict(divert=b["divert"], slot_of=b["slot_of"])
         timed = side_times is not None and stream is self.side
-        with torch.cuda.stream(stream):
-            if after is not None:
-                stream.wait_event(after)
-            if timed:
-                ev0 = torch.cuda.Event(enable_timing=True)
-                ev0.record(stream)
-            moe.moe_permute_tables(
-                sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
-                tb["sorted_token"], tb["group_offsets"], tb["uniq_offsets"],
-                tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
+        if after is not None:
+            stream.wait_event(after)
+        if timed:
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+        moe.moe_permute_tables(
+            sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
+            tb["sorted_token"], tb["group_offsets"], tb["uniq_offsets"],
+            tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
+        if ready is not None:
             ready.record(stream)
-            if timed:
-                ev1 = torch.cuda.Event(enable_timing=True)
-                ev1.record(stream)
-                side_times.append((ev0, ev1))
+        if timed:
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev1.record(stream)
+            side_times.append((ev0, ev1))
 
-    def _passes(self, passes, mark, hold_cycles=0, spec=None):
+    def _passes(self, passes, mark, hold_cycles=0):
         """The passes, each: permute tables -> row scatter -> GEMM1 ->
-        GEMM2 -> combine.  The first pass's tables run on the main stream,
-        unless spec (the first fallback chunk, whose tables the side stream
-        computed during the flag read) is that pass; those of pass i+1 are
-        queued on the side stream after pass i's work, so they run during
-        pass i's FFN.  They reuse the table set of pass i-1 and wait for
-        that pass's combine."""
+        GEMM2 -> combine.  The first pass's tables run on the main stream;
+        those of pass i+1 are queued on the side stream after pass i's
+        work, so they run during pass i's FFN.  They reuse the table set of
+        pass i-1 and wait for that pass's combine."""
         moe, b, W = self.moe, self.b, self.W
         if hold_cycles:
             mark("hold")
             torch.cuda._sleep(hold_cycles)
         main, side = torch.cuda.current_stream(), self.side
-        side.wait_stream(main)   # the routing (and the hold) first
         while len(self.pass_events) < len(passes):
             self.pass_events.append((torch.cuda.Event(), torch.cuda.Event()))
         ready = [e[0] for e in self.pass_events]
@@ -358,8 +353,13 @@ class Layer:
         side_times = getattr(mark, "side", None)
 
         def tables(i, stream):
-            self._tables(passes[i], i, stream, ready[i], side_times,
-                         done[i - 2] if i >= 2 else None)
+            # the side stream's first table work waits for the routing;
+            # a reused table set, for the combine of the pass that read it
+            after = self.routed if i == 1 else \
+                (done[i - 2] if i >= 2 else None)
+            self._tables(passes[i], i, stream,
+                         ready[i] if stream is side else None, side_times,
+                         after)
 
         for i, (t0, t1, capped) in enumerate(passes):
             sc = self.sub(t0, t1, capped)
@@ -370,11 +370,7 @@ class Layer:
                 groups = dict(n_groups=sc.E + sc.S * sc.redundant_slots,
                               group_expert=b["group_expert"])
             mark("permute")
-            if i == 0 and spec is not None and passes[0] == spec:
-                main.wait_event(self.spec_ready)   # computed during the flag
-            elif i == 0:
-                if spec is not None:
-                    main.wait_event(self.spec_ready)  # set 0 is free again
+            if i == 0:
                 tables(0, main)
             else:
                 main.wait_event(ready[i])
@@ -443,14 +439,25 @@ class StageTimer:
 HOLD_CYCLES = 1_000_000   # about 0.5 ms at 2 GHz
 
 
-def launches_per_step(passes, mode, dispatch_only=False, planned=0):
-    """Kernel launches of one step: route 1 (+ check 1 with the fallback),
-    then per pass permute 4 (block counts, expert scan, assign with the
-    dedup scan, row scatter), GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the
-    sweep)."""
-    per = 5 if dispatch_only else 7
+def table_launches(tokens, shards):
+    """Permute-table kernels of one pass over `tokens` tokens: block counts,
+    expert scan, assign, and the dedup scan when the block x shard table
+    holds more than 1024 counts (with shards = 0, never)."""
+    if tokens <= 0:
+        return 1
+    nb = (tokens + 127) // 128
+    return 3 + (1 if shards and nb * shards > 1024 else 0)
+
+
+def launches_per_step(passes, mode, dispatch_only=False, planned=0,
+                      shards=0):
+    """Kernel launches of one step: route 1 (+ check 1 with the fallback,
+    + the plan), then per pass the permute tables (table_launches) and the
+    row scatter, GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the sweep)."""
+    per = 2 if dispatch_only else 4
     return (2 if mode == "fallback" else 1) + planned + \
-        sum(per for (t0, t1, _) in passes if t1 > t0)
+        sum(table_launches(t1 - t0, shards) + per
+            for (t0, t1, _) in passes if t1 > t0)
 
 
 def pass_accounting(layer, passes):
@@ -699,10 +706,9 @@ def main():
                            "until the host has queued it; HBM fraction of "
                            "the measured copy peak. permute = the row "
                            "scatter (plus the first pass's tables); "
-                           "permute_tables = the counting-sort kernels on "
-                           "the side stream: the first fallback chunk's "
-                           "during the overflow-flag read, each later "
-                           "chunk's during the previous chunk's expert FFN",
+                           "permute_tables = the counting-sort kernels of "
+                           "passes 2.. on the side stream, each overlapping "
+                           "the previous pass's expert FFN",
                    "permute_tables": {"ms_per_step":
                                       round(side_ms / args.steps, 4),
                                       "stream": "side"}}
@@ -787,8 +793,8 @@ def main():
                     "flush between steps"},
         "gpu_launches": launches_per_step(
             passes, args.mode, layer.dispatch_only,
-            int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"))
-        * args.steps,
+            int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"),
+            layer.wl.S) * args.steps,
         "kernels": kernels,
         "stages_host_held": stages_held,
         "roofline": roof,
@@ -1038,7 +1044,6 @@ class Backward:
         keys = ("uniq_offsets", "uniq_tokens", "n_dropped", "permute_ws")
         self.tabs = [{k: b[k] for k in keys},
                      {k: torch.empty_like(b[k]) for k in keys}]
-        self.spec_ready = torch.cuda.Event()
         self.pass_events = []   # (tables ready, scatter done) per pass
 
     def tables(self, pas, i, stream, ready, after=None, on_plan=False):
@@ -1051,14 +1056,13 @@ class Backward:
         tb = self.tabs[i % 2]
         plan = dict(divert=b["divert"], slot_of=b["slot_of"]) if on_plan \
             else {}
-        with torch.cuda.stream(stream):
-            if after is not None:
-                stream.wait_event(after)
-            moe.moe_permute_tables(
-                sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
-                b["sorted_token"][t0 * k:], self.goff[i], tb["uniq_offsets"],
-                tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
-            ready.record(stream)
+        if after is not None:
+            stream.wait_event(after)
+        moe.moe_permute_tables(
+            sc, b["topk_idx"][t0:t1], capped, b["row_of"][t0:t1],
+            b["sorted_token"][t0 * k:], self.goff[i], tb["uniq_offsets"],
+            tb["n_dropped"], tb["permute_ws"], stream=stream, **plan)
+        ready.record(stream)
 
     def step(self, ev=None):
         L = self
@@ -1068,6 +1072,7 @@ class Backward:
         mark = ev or (lambda name: None)
         mark("route")
         moe.moe_route(c, lay.logits, b["topk_idx"], b["topk_w"], b["status"])
+        lay.routed.record()   # the side stream's tables start after it
         # duplicate-expert slots: check and plan first (as moe_layer_backward)
         planned = c.redundant_slots > 0 and lay.mode != "dropless"
         if planned or lay.mode == "fallback":
@@ -1082,15 +1087,9 @@ class Backward:
                                      b["slot_of"], b["group_expert"],
                                      b["shard_after"], b["flag_after"])
         main, side = torch.cuda.current_stream(), lay.side
-        spec = None
         if lay.mode != "fallback":
             passes = [(0, c.T, lay.mode == "capped")]
         else:
-            # the first fallback chunk's tables during the flag read
-            if c.T > 0:
-                spec = (0, min(c.T, lay.chunk), False)
-                side.wait_stream(main)
-                L.tables(spec, 0, side, L.spec_ready)
             mark("flag")
             flag = b["flag_after"] if planned else b["overflow_flag"]
             if int(flag.item()):
@@ -1103,7 +1102,6 @@ class Backward:
         grp = dict(n_groups=L.G, group_expert=b["group_expert"]) \
             if on_plan else {}
         xs, h, ys = b["x_sorted"], b["h"], b["y_sorted"]
-        side.wait_stream(main)
         while len(L.pass_events) < len(passes):
             L.pass_events.append((torch.cuda.Event(), torch.cuda.Event()))
         ready = [e[0] for e in L.pass_events]
@@ -1114,11 +1112,7 @@ class Backward:
             go = L.goff[i]
             tb = L.tabs[i % 2]
             mark("permute")
-            if i == 0 and spec is not None and passes[0] == spec:
-                main.wait_event(L.spec_ready)
-            elif i == 0:
-                if spec is not None:
-                    main.wait_event(L.spec_ready)   # set 0 is free again
+            if i == 0:
                 L.tables(passes[0], 0, main, ready[0], on_plan=on_plan)
             else:
                 main.wait_event(ready[i])
@@ -1135,7 +1129,7 @@ class Backward:
                 # pass's tables reuse the dedup set of pass i-1, which only
                 # that pass's scatter reads
                 L.tables(passes[i + 1], i + 1, side, ready[i + 1],
-                         scattered[i - 1] if i >= 1 else None)
+                         scattered[i - 1] if i >= 1 else lay.routed)
             mark("gmm_down")
             moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"],
                              **grp)
@@ -1186,18 +1180,21 @@ class Backward:
                                       mode, self.ws, self.layer.b["status"])
 
 
-def backward_launches(passes, mode, regroup, planned=False):
+def backward_launches(passes, mode, regroup, planned=False, shards=0):
     """Kernel launches of one backward step: route (+ check, + the plan with
-    duplicate slots), per pass permute 4 + GEMM1-saved + GEMM2 + combine
-    backward + two dgrad GEMMs + permute backward, route backward, the
-    regrouping of the rows (2) or the row segments in batches of 16, and per
-    batch the two weight-gradient GEMMs, plus the two fills in the first
-    batch that zero the experts not written by exactly one group."""
+    duplicate slots), per pass the permute tables (table_launches) + scatter
+    + GEMM1-saved + GEMM2 + combine backward + two dgrad GEMMs + permute
+    backward, route backward, the regrouping of the rows (2) or the row
+    segments in batches of 16, and per batch the two weight-gradient GEMMs,
+    plus the two fills in the first batch that zero the experts not written
+    by exactly one group."""
     n = len(passes)
     batches = 1 if regroup else (n + 15) // 16
     head = 1 + (1 if (mode == "fallback" or planned) else 0) + \
         (1 if planned else 0)
-    return head + 10 * n + 1 + (2 if regroup else 0) + 2 * batches + 2
+    return head + sum(table_launches(t1 - t0, shards) + 7
+                      for (t0, t1, _) in passes) + 1 + \
+        (2 if regroup else 0) + 2 * batches + 2
 
 
 def backward_work(w, accs):
@@ -1405,7 +1402,7 @@ def backward_main(layer, args, world, rank, device):
         "wall_s_timed_loop": round(wall, 3),
         "gpu_launches": backward_launches(
             passes, layer.mode, bw.regroup and len(passes) <= 64,
-            planned) * args.steps,
+            planned, layer.wl.S) * args.steps,
         "kernels": kernels,
         "roofline": roof,
     }

@@ -1,7 +1,8 @@
 """bench.py's host-side bookkeeping, without a GPU: the kernel-launch counts
 it reports as gpu_launches, pinned to the launch lists ncu recorded for the
 same steps (30 kernels per forward step and 49 per backward step of the
-DeepSeek-V3-shaped layer, whose Zipf routing overflows into 4 chunks)."""
+DeepSeek-V3-shaped layer, whose Zipf routing overflows into 4 chunks of 2048
+tokens; 8 shards)."""
 import bench
 
 
@@ -10,31 +11,48 @@ def chunks(n, T=8192):
     return [(i * c, (i + 1) * c, False) for i in range(n)]
 
 
+def test_table_launches():
+    # block counts, expert scan, assign; the dedup scan only above 1024
+    # block x shard counts
+    assert bench.table_launches(2048, 8) == 3      # 16 blocks x 8 shards
+    assert bench.table_launches(8192, 16) == 3     # 64 x 16 = 1024
+    assert bench.table_launches(8193, 16) == 4
+    assert bench.table_launches(65536, 8) == 4     # 512 x 8
+    assert bench.table_launches(0, 8) == 1         # the expert scan alone
+
+
 def test_forward_launches():
-    # route + check, then per chunk: block counts, expert scan, assign,
-    # scatter, GEMM1, GEMM2, combine
-    assert bench.launches_per_step(chunks(4), "fallback") == 30
-    assert bench.launches_per_step([(0, 8192, True)], "fallback") == 9
-    assert bench.launches_per_step([(0, 8192, False)], "dropless") == 8
-    # the routing/permute sweep: no expert FFN
-    assert bench.launches_per_step(chunks(8), "fallback",
-                                   dispatch_only=True) == 2 + 8 * 5
-    # the duplication plan adds one launch
+    # route + check, then per chunk: 3 table kernels, scatter, GEMM1,
+    # GEMM2, combine
+    assert bench.launches_per_step(chunks(4), "fallback", shards=8) == 30
+    # no overflow: the capped pass (Llama4-Maverick: 16 shards, 64 blocks)
     assert bench.launches_per_step([(0, 8192, True)], "fallback",
-                                   planned=1) == 10
-    # an empty pass launches nothing
-    assert bench.launches_per_step([(0, 0, False)], "fallback") == 2
+                                   shards=16) == 2 + 7
+    assert bench.launches_per_step([(0, 8192, False)], "dropless",
+                                   shards=8) == 8
+    # the routing/permute sweep: no expert FFN; 64K tokens in one capped
+    # pass take the dedup scan kernel
+    assert bench.launches_per_step(chunks(8, 65536), "fallback",
+                                   dispatch_only=True, shards=8) == 2 + 8 * 5
+    assert bench.launches_per_step([(0, 65536, True)], "capped",
+                                   dispatch_only=True, shards=8) == 1 + 6
+    # the duplication plan adds one launch
+    assert bench.launches_per_step([(0, 8192, True)], "fallback", planned=1,
+                                   shards=8) == 3 + 7
 
 
 def test_backward_launches():
-    # route + check; per chunk 4 permute kernels, GEMM1 keeping g/u, GEMM2,
-    # combine backward, two dgrad GEMMs, permute backward; route backward;
-    # regrouping (2); the two weight-gradient GEMMs; two zero fills
-    assert bench.backward_launches(chunks(4), "fallback", True) == 49
+    # route + check; per chunk 3 table kernels, scatter, GEMM1 keeping g/u,
+    # GEMM2, combine backward, two dgrad GEMMs, permute backward; route
+    # backward; regrouping (2); two weight-gradient GEMMs; two zero fills
+    assert bench.backward_launches(chunks(4), "fallback", True,
+                                   shards=8) == 49
     # without regrouping the segments go in batches of 16 passes
-    assert bench.backward_launches(chunks(20), "fallback", False) == \
+    assert bench.backward_launches(chunks(20, 20480), "fallback", False,
+                                   shards=8) == \
         2 + 20 * 10 + 1 + 2 * 2 + 2
-    # with duplicate slots (one capped pass over the plan's groups): the
-    # plan adds a launch; the zero fills stay (ncu saw two per step there)
+    # duplicate slots, one capped pass over the plan's groups: the plan
+    # adds a launch; the zero fills stay (ncu saw two per step there)
     assert bench.backward_launches([(0, 8192, True)], "fallback", True,
-                                   planned=True) == 3 + 10 + 1 + 2 + 2 + 2
+                                   planned=True, shards=8) == \
+        3 + 10 + 1 + 2 + 2 + 2
