@@ -190,7 +190,10 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x,
  *     8 MiB returns MOE_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address with
  *     that device current and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  The cached address belongs to the device's context
+ *     at that time: after cudaDeviceReset (or any reset of the primary
+ *     context) it is stale, so a process that resets a device must not
+ *     call moe_permute_noalloc on it again.
  *   - Every call on a device uses the same array, which keeps the previous
  *     call's contents (nothing in it needs to start at zero: each call
  *     writes every entry before reading it).  Calls whose work overlaps on
@@ -625,6 +628,17 @@ int64_t moe_capacity_rows(const moe_config_t *cfg);
 /* Token count of each fallback chunk and the number of chunks. */
 int32_t moe_chunk_tokens(const moe_config_t *cfg);
 int32_t moe_num_chunks(const moe_config_t *cfg);
+
+/* Which bf16 grouped GEMMs take the two-SM (CTA pair,
+ * tcgen05.mma.cta_group::2) kernel rather than the one-CTA kernel, for
+ * n_groups row groups (0: the E experts' own) holding at most rows_bound
+ * rows (<= 0: T*k).  The pair kernel runs when the groups average at least
+ * 1024 rows; both kernels give the same bits for a row.  moe_gmm_* calls use
+ * rows_bound = T*k; moe_layer's capped pass uses min(T*k, S*C).  Returns
+ * bit 0 (GEMM1 + SwiGLU), bit 1 (GEMM2, only when H % 256 == 0), 0 for the
+ * one-CTA kernels or an fp32 layer, -1 for an invalid cfg or n_groups. */
+int32_t moe_gmm_uses_pair(const moe_config_t *cfg, int32_t n_groups,
+                          int64_t rows_bound);
 
 /* Static text for a status code. */
 const char *moe_status_string(moe_status_t status);

@@ -154,6 +154,8 @@ def _declare(h):
     h.moe_chunk_tokens.restype = c_int32
     h.moe_num_chunks.argtypes = [cfg]
     h.moe_num_chunks.restype = c_int32
+    h.moe_gmm_uses_pair.argtypes = [cfg, c_int32, c_int64]
+    h.moe_gmm_uses_pair.restype = c_int32
     h.moe_test_stall_gemm_producer.argtypes = [c_int64]
     h.moe_test_stall_gemm_producer.restype = None
     h.moe_status_string.argtypes = [c_int]
@@ -217,6 +219,11 @@ def moe_chunk_tokens(cfg) -> int:
 
 def moe_num_chunks(cfg) -> int:
     return lib().moe_num_chunks(ctypes.byref(cfg))
+
+
+def moe_gmm_uses_pair(cfg, n_groups=0, rows_bound=0) -> int:
+    return int(lib().moe_gmm_uses_pair(ctypes.byref(cfg), n_groups,
+                                       rows_bound))
 
 
 def moe_test_stall_gemm_producer(fills: int):

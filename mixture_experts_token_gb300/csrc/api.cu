@@ -198,6 +198,9 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
     plan.B = c.redundant_slots;
     groups = {num_groups(c), b.group_expert};
   }
+  if (cap >= 0)  // a capped pass keeps at most S*C rows
+    groups.max_rows = std::min<int64_t>(static_cast<int64_t>(c.T) * c.k,
+                                        static_cast<int64_t>(c.S) * cap);
   cudaError_t e = launch_permute(c, x, topk_idx, cap, b.x_sorted, b.row_of,
                                  b.sorted_token, b.group_offsets,
                                  b.uniq_offsets, b.uniq_tokens, b.expand_idx,
@@ -327,6 +330,16 @@ int32_t moe_num_chunks(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
   const int ct = chunk_tokens(*cfg);
   return ct > 0 ? (cfg->T + ct - 1) / ct : 0;
+}
+
+int32_t moe_gmm_uses_pair(const moe_config_t* cfg, int32_t n_groups,
+                          int64_t rows_bound) {
+  if (validate(cfg) != MOE_OK || n_groups < 0 || n_groups > kMaxExperts)
+    return -1;
+  Groups g = identity_groups(*cfg);
+  if (n_groups > 0) g.n = n_groups;
+  if (rows_bound > 0) g.max_rows = rows_bound;
+  return gmm_pair_kinds(*cfg, g);
 }
 
 size_t moe_workspace_bytes(const moe_config_t* cfg, moe_ws_kind_t which) {

@@ -765,12 +765,21 @@ size_t smem_bytes(int E) {
 // rows, and for smaller groups the peer SM stages rows it then masks (more
 // L2 traffic and tensor work per weight tile, measured 15-25% slower on
 // weight-streaming layers).  With >= 1024 routed rows per group on average
-// it was measured 2% (GEMM1) and 9% (GEMM2) faster.
+// it was measured 2% (GEMM1) and 9% (GEMM2) faster.  The row count is the
+// host's bound on the rows the groups hold: T*k, or fewer when the caller
+// knows them to be capped (a capped pass keeps at most S*C rows), so that a
+// capped pass with many dropped rows does not take the pair kernel for
+// groups that are small in fact.
 constexpr long long kPairMinRowsPerGroup = 1024;
+
+long long group_rows_bound(const moe_config_t& c, const Groups& g) {
+  const long long all = static_cast<long long>(c.T) * c.k;
+  return g.max_rows >= 0 ? std::min<long long>(g.max_rows, all) : all;
+}
 
 bool use_pair(const moe_config_t& c, const Groups& g) {
   return g_stall_after_fills.load() < 0 &&
-         static_cast<long long>(c.T) * c.k >= kPairMinRowsPerGroup * g.n;
+         group_rows_bound(c, g) >= kPairMinRowsPerGroup * g.n;
 }
 
 size_t smem_bytes_pair(int E) {
@@ -817,6 +826,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
 }
 
 }  // namespace tc
+
+int gmm_pair_kinds(const moe_config_t& c, const Groups& g) {
+  if (!gmm_tc_supported(c) || !tc::use_pair(c, g)) return 0;
+  return 1 | (c.H % 256 == 0 ? 2 : 0);
+}
 
 void set_gemm_stall_for_tests(long long fills) {
   tc::g_stall_after_fills.store(fills);

@@ -105,8 +105,15 @@ cudaError_t launch_plan(const moe_config_t& c, const int32_t* counts,
 struct Groups {
   int n;
   const int32_t* map;
+  // Upper bound on the rows the groups hold, known on the host (a capped
+  // pass keeps at most S*C rows); -1: the allocation, T*k rows.
+  int64_t max_rows = -1;
 };
 inline Groups identity_groups(const moe_config_t& c) { return {c.E, nullptr}; }
+
+// Which bf16 GEMMs take the two-SM (CTA pair) kernel for these groups:
+// bit 0 GEMM1 + SwiGLU, bit 1 GEMM2.
+int gmm_pair_kinds(const moe_config_t& c, const Groups& g);
 
 // GEMM1 + SwiGLU (h) and GEMM2 (y_sorted), each one kernel launch.
 cudaError_t launch_gmm1(const moe_config_t& c, const Groups& g,

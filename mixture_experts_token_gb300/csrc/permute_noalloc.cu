@@ -15,7 +15,10 @@
 //  * In host code the name g_permute_scratch is a host-side stand-in, not a
 //    device address.  The device address is looked up once per device with
 //    that device current (cudaGetSymbolAddress) on the first call and
-//    cached; that first call should come before any stream capture.
+//    cached; that first call should come before any stream capture.  The
+//    cached address is that of the device's context at the time: after a
+//    cudaDeviceReset it is stale, and the entry point must not be called
+//    on that device again in the same process.
 //  * All calls on a device share the array and it keeps the last call's
 //    contents.  Nothing in it has to start at zero: each call writes every
 //    table entry before reading it.  Calls whose work overlaps on the GPU

@@ -501,6 +501,25 @@ def normwise_error(got: np.ndarray, ref: np.ndarray) -> float:
     return num / den
 
 
+def elementwise_error(got: np.ndarray, ref: np.ndarray,
+                      floor: float = 1e-3) -> float:
+    """max_i |g_i - r_i| / max(|r_i|, floor * max_j |r_j|): the largest
+    relative error of any single element, with a small absolute floor so
+    that elements near zero (whose relative error is meaningless) are
+    measured against floor * the tensor's largest magnitude.  Reported
+    beside the normwise measure; 0 when both are all zero."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    peak = float(np.max(np.abs(ref)))
+    diff = np.abs(got - ref)
+    if peak == 0.0:
+        return float(np.max(diff))
+    den = np.maximum(np.abs(ref), floor * peak)
+    return float(np.max(diff / den))
+
+
 # ---------------------------------------------------------------------------
 # Dynamic redundant experts.  "Moe dynamic redundancy" (MaxText pull request
 # 4760), review comments: plan_expert_duplication duplicates the hottest

@@ -701,4 +701,27 @@ def pin_redundant_backward_equals_dropless():
     assert diverted >= 4   # the virtual-group pass really ran
 
 
+def pin_error_measures():
+    """The two tolerance measures on hand-computed arrays: normwise is the
+    largest absolute error over the largest reference magnitude; the
+    elementwise figure divides each error by its own reference magnitude,
+    floored at 1e-3 of the largest."""
+    r = np.array([4.0, -2.0, 1.0, 0.0])
+    g = np.array([4.1, -2.0, 0.9, 0.002])
+    # errors 0.1, 0, 0.1, 0.002; max |r| = 4
+    assert math.isclose(ref.normwise_error(g, r), 0.1 / 4.0)
+    # relative: 0.1/4, 0, 0.1/1, 0.002/max(0, 0.004) = 0.5
+    assert math.isclose(ref.elementwise_error(g, r), 0.5)
+    assert math.isclose(ref.elementwise_error(g[:3], r[:3]), 0.1)
+    assert ref.elementwise_error(r, r) == 0.0
+    assert ref.normwise_error(np.zeros(3), np.zeros(3)) == 0.0
+    assert ref.elementwise_error(np.zeros(0), np.zeros(0)) == 0.0
+    # the elementwise figure is never below the normwise one
+    rng = _rng(3)
+    for _ in range(20):
+        a = rng.standard_normal(50)
+        b = a + 1e-3 * rng.standard_normal(50)
+        assert ref.elementwise_error(b, a) >= ref.normwise_error(b, a)
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -14,6 +14,7 @@ from oracle import moe_ref as ref
 from synth import WORKLOADS, make_logits, make_weights, make_x
 from synth.workloads import make_dy
 from tests.gpu_util import TOL, cfg_from, f64, np_
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -87,8 +88,7 @@ def compare(out, g, tol):
     for name, want in pairs:
         got = f64(out[name])
         assert np.isfinite(got).all(), f"{name}: unwritten or non-finite"
-        err = ref.normwise_error(got, want)
-        assert err <= tol, f"{name}: normwise error {err:.3g} > {tol}"
+        assert_close(got, want, tol, name)
 
 
 MODES = [(moe.MOE_MODE_DROPLESS, 2.0), (moe.MOE_MODE_CAPPED, 1.0),
@@ -201,7 +201,7 @@ def test_backward_entry_points_stepwise(wl):
     want = ref.layer_backward_dropless(oracle_cfg(wl), f64(x), L,
                                        *[f64(w) for w in W], f64(dy))
     tol = TOL[wl.dtype]
-    assert ref.normwise_error(f64(dtw), want.dtopk_w) <= tol
+    assert_close(f64(dtw), want.dtopk_w, tol, 'dtw')
     compare({"dx": dx, "dlogits": dl, "dwg": dw[0], "dwu": dw[1],
              "dwd": dw[2]}, want, tol)
     # saved g, u against the oracle's x_sorted W products (g = x Wg)
@@ -211,7 +211,7 @@ def test_backward_entry_points_stepwise(wl):
     gs = np.zeros((R, F))
     for e in range(E):
         gs[off[e]:off[e + 1]] = xs[off[e]:off[e + 1]] @ wg[e]
-    assert ref.normwise_error(f64(g), gs) <= tol
+    assert_close(f64(g), gs, tol, 'g')
     # accumulate: a second backward adds the same gradient again.  bf16
     # adds the finished tile to dW (a + a: exact); fp32 continues its
     # accumulation from the old value (rounding differs in the last bits).

@@ -26,6 +26,7 @@ from oracle import moe_ref as ref
 from synth import WORKLOADS, make_logits, make_weights, make_x
 from synth.workloads import make_dy
 from tests.gpu_util import TOL, cfg_from, expert_accessor, f64
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -94,7 +95,7 @@ def test_fullsize_backward_sampled(name):
         g, _ = ref.pass_backward_touched(one, xt, L[t:t + 1], get,
                                          f64(dy[t:t + 1]), None)
         got_dx = f64(dx[t:t + 1])
-        assert ref.normwise_error(got_dx, g.dx) <= tol, f"dx of token {t}"
+        assert_close(got_dx, g.dx, tol, f"dx of token {t}")
         dyt = f64(dy[t])
         A = np.array([np.linalg.norm(dyt * ref.expert_ffn(xt, *get(int(e)))[1][0])
                       for e in idx[t]])
@@ -125,5 +126,4 @@ def test_fullsize_backward_sampled(name):
             if not rows:
                 assert not got.any(), f"{name_}[{e}] not zero"
                 continue
-            err = ref.normwise_error(got, want[i])
-            assert err <= tol, f"{name_}[{e}] ({len(rows)} rows): {err:.3g}"
+            assert_close(got, want[i], tol, f"{name_}[{e}] ({len(rows)} rows)")

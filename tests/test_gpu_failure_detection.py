@@ -16,6 +16,7 @@ import torch
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
 from tests.gpu_util import f64
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -61,4 +62,4 @@ def test_gemm_wait_times_out_and_context_survives():
     want_h, want_y = ref.grouped_ffn(
         f64(xs), off.cpu().numpy(),
         ref.dense_weights(*(f64(w) for w in W)))
-    assert ref.normwise_error(f64(ys), want_y) <= 2e-2
+    assert_close(f64(ys), want_y, 2e-2, 'ys')

@@ -10,7 +10,8 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from tests.gpu_util import TOL, f64, np_
+from tests.gpu_util import TOL, expert_accessor, f64, np_
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -51,36 +52,84 @@ def run_gmm(sizes, H, F, dtype, T=None, k=1, seed=0):
 
 
 GMM_CASES = [
-    # (group sizes, H, F): empty groups, single rows, tile edges, many tiles
-    ([0, 1, 127, 128, 129, 300], 256, 256),
-    ([5, 0, 0, 700, 3], 384, 128),          # H % 256 != 0: 128-wide GEMM2
-    ([128] * 4, 128, 128),
-    ([1000], 512, 384),
-    ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512),
-    # >= 1024 rows per group on average: the two-SM (CTA pair) kernel
-    ([2100, 900, 1300, 4, 1], 512, 256),
-    ([4096, 3000], 256, 384),
+    # (group sizes, H, F, pair kinds): empty groups, single rows, tile
+    # edges, many tiles.  Pair kinds is moe_gmm_uses_pair's answer for bf16:
+    # bit 0 GEMM1 on the two-SM (CTA pair) kernel, bit 1 GEMM2 too; the
+    # pair kernel runs when the groups average >= 1024 rows.
+    ([0, 1, 127, 128, 129, 300], 256, 256, 0),
+    ([5, 0, 0, 700, 3], 384, 128, 0),       # H % 256 != 0: 128-wide GEMM2
+    ([128] * 4, 128, 128, 0),
+    ([1000], 512, 384, 0),
+    ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512, 0),
+    # 5201 rows in 5 groups (>= 1024 each on average): both pair kernels,
+    # with a small and a one-row group among the large ones
+    ([2100, 1500, 1300, 300, 1], 512, 256, 3),
+    ([4096, 3000], 256, 384, 3),
+    # H % 256 != 0: GEMM1 on the pair kernel, GEMM2 on the 128-wide one-CTA
+    ([1200, 1100, 0], 384, 256, 1),
 ]
+
+
+def test_gmm_pair_choice_query():
+    """moe_gmm_uses_pair follows the average rows per group, the row bound
+    given, the layer dtype and H % 256 for GEMM2."""
+    c = moe.make_config(2048, 512, 2, 1, 256, 1, 2.0, 0, "bf16")
+    assert moe.moe_gmm_uses_pair(c) == 3
+    assert moe.moe_gmm_uses_pair(c, rows_bound=2047) == 0
+    assert moe.moe_gmm_uses_pair(c, n_groups=3) == 0
+    assert moe.moe_gmm_uses_pair(c.with_(H=384)) == 1
+    assert moe.moe_gmm_uses_pair(c.with_(dtype=moe.MOE_F32)) == 0
+    assert moe.moe_gmm_uses_pair(c, n_groups=-1) == -1
+    # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk and the
+    # 8192-token uncapped pass both stay on the one-CTA kernel (256 groups)
+    d = moe.make_config(8192, 7168, 256, 8, 2048, 8, 2.0, 0, "bf16")
+    assert moe.moe_gmm_uses_pair(d) == 0
+    assert moe.moe_gmm_uses_pair(d.with_(T=2048)) == 0
 
 
 @pytest.mark.parametrize("case", GMM_CASES, ids=lambda c: f"{len(c[0])}x{c[1]}x{c[2]}")
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_gmm_parity(case, dtype):
-    sizes, H, F = case
+    sizes, H, F, kinds = case
+    if dtype == "bf16":
+        R0 = int(sum(sizes))
+        cq = moe.make_config(R0, H, len(sizes), 1, F, 1, 2.0, 0, dtype)
+        assert moe.moe_gmm_uses_pair(cq) == kinds
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, dtype)
     want_h, want_y = ref.grouped_ffn(f64(xs[:R]), off,
                                      ref.dense_weights(f64(wg), f64(wu),
                                                        f64(wd)))
     tol = TOL[dtype]
-    assert ref.normwise_error(f64(h[:R]), want_h) <= tol
-    assert ref.normwise_error(f64(ys[:R]), want_y) <= tol
+    assert_close(f64(h[:R]), want_h, tol, 'h[:R]')
+    assert_close(f64(ys[:R]), want_y, tol, 'ys[:R]')
     # no row outside the groups was written
     assert torch.all(h[R:] == 0) and torch.all(ys[R:] == 0)
     # each group on its own scale
     for e in range(len(sizes)):
         a, b = int(off[e]), int(off[e + 1])
         if b > a:
-            assert ref.normwise_error(f64(ys[a:b]), want_y[a:b]) <= tol
+            assert_close(f64(ys[a:b]), want_y[a:b], tol, 'ys[a:b]')
+
+
+def test_gmm_pair_kernel_full_dims():
+    """The two-SM kernels at the DeepSeek-V3 layer's dims (H=7168,
+    F=2048): 4157 rows in 4 ragged groups, one of them a 256-row tile plus
+    one row.  Every row of every group against the oracle."""
+    sizes = [1500, 1100, 1300, 257]
+    H, F = 7168, 2048
+    R0 = int(sum(sizes))
+    assert moe.moe_gmm_uses_pair(
+        moe.make_config(R0, H, 4, 1, F, 1, 2.0, 0, "bf16")) == 3
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=11)
+    W = expert_accessor(wg, wu, wd)
+    xh = f64(xs[:R])
+    hh, yh = f64(h[:R]), f64(ys[:R])
+    for e in range(len(sizes)):
+        a, b = int(off[e]), int(off[e + 1])
+        want_h, want_y = ref.expert_ffn(xh[a:b], *W(e))
+        assert_close(hh[a:b], want_h, 2e-2, f"h group {e} ({b - a} rows)")
+        assert_close(yh[a:b], want_y, 2e-2, f"y_sorted group {e} ({b - a} rows)")
+    assert torch.all(h[R:] == 0) and torch.all(ys[R:] == 0)
 
 
 def test_gmm_small_layer_shape():
@@ -92,8 +141,8 @@ def test_gmm_small_layer_shape():
     want_h, want_y = ref.grouped_ffn(f64(xs[:R]), off,
                                      ref.dense_weights(f64(wg), f64(wu),
                                                        f64(wd)))
-    assert ref.normwise_error(f64(h[:R]), want_h) <= 2e-2
-    assert ref.normwise_error(f64(ys[:R]), want_y) <= 2e-2
+    assert_close(f64(h[:R]), want_h, 2e-2, 'h[:R]')
+    assert_close(f64(ys[:R]), want_y, 2e-2, 'ys[:R]')
 
 
 def test_gmm_pair_kernel_row_independence():
@@ -186,7 +235,7 @@ def test_combine_parity(dtype, k):
     moe.moe_combine(cfg, ys, row_of, w, y)
     torch.cuda.synchronize()
     want = ref.combine(f64(ys[:R]), p.row_of, ow.astype(np.float32), H)
-    assert ref.normwise_error(f64(y), want) <= TOL[dtype]
+    assert_close(f64(y), want, TOL[dtype], 'y')
     gone = np.all(p.row_of < 0, axis=1)
     if k <= 2:   # with few slots some tokens lose every row
         assert gone.any()

@@ -13,6 +13,7 @@ import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
 from synth import WORKLOADS, make_logits, make_weights, make_x
 from tests.gpu_util import TOL, cfg_from, expert_accessor, f64, np_
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -67,18 +68,18 @@ def test_layer_modes_full_compare(wl):
         if want.overflow:
             assert info["n_chunks"] == len(ref.chunk_plan(wl.T, wl.k, wl.E,
                                                           wl.S, C))
-        assert ref.normwise_error(f64(y), want.y) <= tol
-        assert ref.normwise_error(f64(y), drop.y) <= tol
+        assert_close(f64(y), want.y, tol, 'y')
+        assert_close(f64(y), drop.y, tol, 'y vs dropless')
     # capped-only at factor 0.1 drops rows and diverges from dropless
     y_cap, _ = run_layer(wl, moe.MOE_MODE_CAPPED, x, Ld, W, factor=0.1)
     want_cap = ref.layer_capped(oracle_cfg(wl, ragged_buffer_factor=0.1), xh,
                                 L, weights)
     assert want_cap.perm.n_dropped > 0
-    assert ref.normwise_error(f64(y_cap), want_cap.y) <= tol
+    assert_close(f64(y_cap), want_cap.y, tol, 'y_cap')
     assert ref.normwise_error(f64(y_cap), drop.y) > 10 * tol
     # one uncapped pass
     y_drop, _ = run_layer(wl, moe.MOE_MODE_DROPLESS, x, Ld, W)
-    assert ref.normwise_error(f64(y_drop), drop.y) <= tol
+    assert_close(f64(y_drop), drop.y, tol, 'y_drop')
 
 
 @pytest.mark.parametrize("wl", SMALL[:2], ids=lambda w: w.name)
@@ -117,7 +118,7 @@ def test_full_size_layer_sampled(name):
     want = ref.token_outputs(f64(x[torch.from_numpy(toks).cuda()]), oi[toks],
                              ow[toks], expert_accessor(*W))
     got = f64(y[torch.from_numpy(toks).cuda()])
-    assert ref.normwise_error(got, want) <= 2e-2
+    assert_close(got, want, 2e-2, 'got')
     # capped-only pass: dropped slots are skipped
     y_cap, _ = run_layer(wl, moe.MOE_MODE_CAPPED, x, Ld, W)
     p = ref.permute_indices(oi, wl.E, wl.S, C)
@@ -126,7 +127,7 @@ def test_full_size_layer_sampled(name):
                                  oi[toks], ow[toks], expert_accessor(*W),
                                  keep=keep)
     got_cap = f64(y_cap[torch.from_numpy(toks).cuda()])
-    assert ref.normwise_error(got_cap, want_cap) <= 2e-2
+    assert_close(got_cap, want_cap, 2e-2, 'got_cap')
     if over:
         # tokens whose every slot was dropped are exactly zero
         gone = np.where(np.all(p.row_of < 0, axis=1))[0]
@@ -159,7 +160,7 @@ def test_layer_edge_cases():
         y, info = run_layer(wl, moe.MOE_MODE_DROPLESS, x, Ld, W)
         want = ref.layer_dropless(oracle_cfg(wl), f64(x), Lg,
                                   ref.dense_weights(*(f64(w) for w in W)))
-        assert ref.normwise_error(f64(y), want.y) <= 2e-2
+        assert_close(f64(y), want.y, 2e-2, 'y')
 
 
 @pytest.mark.parametrize("n_chunks,slots", [(5, 0), (2, 0), (0, 2)])

@@ -143,3 +143,48 @@ def test_permute_split_equals_whole(wl):
                      ("uniq_tokens", U)):
             assert torch.equal(b[k][:n], whole[k][:n]), k
         assert torch.equal(b["x_sorted"][:R], whole["x_sorted"][:R])
+
+
+def compare_x_sorted_on_device(x, x_sorted, sorted_token, rows_per_step=32768):
+    """Every kept row of x_sorted equals x[sorted_token[r]] (the oracle's
+    sorted_token), compared on the device in slices so no 7.5 GB host copy
+    is needed."""
+    st = torch.from_numpy(sorted_token.astype(np.int64)).cuda()
+    for a in range(0, len(sorted_token), rows_per_step):
+        z = min(len(sorted_token), a + rows_per_step)
+        assert torch.equal(x_sorted[a:z], x.index_select(0, st[a:z])), \
+            f"x_sorted rows {a}..{z}"
+
+
+@pytest.mark.parametrize("routing", ["zipf", "adversarial", "uniform"])
+def test_permute_parity_sweep_64k(routing):
+    """The sweep's largest size: 65,536 tokens at H=7168 (524,288 routed
+    rows, x_sorted 7.5 GB), bit-exact on every index output, every kept
+    x_sorted row checked: the whole batch capped (factor 2) and uncapped,
+    and one of the 8 fallback chunks as the fallback runs it."""
+    import mixture_experts_token_gb300 as moe
+    wl = sweep_workload(65536, routing)
+    cfg = cfg_from(wl)
+    x, L = inputs(wl)
+    idx, _ = gpu_route(cfg, L)
+    oi, _, _ = ref.route(L, wl.k)
+    assert np.array_equal(np_(idx), oi)
+    C = ref.capacity(wl.T, wl.k, wl.S, wl.factor)
+    for capped in (True, False):
+        bufs = gpu_permute(cfg, x, idx, capped)
+        p = ref.permute_indices(oi, wl.E, wl.S, C if capped else None)
+        compare_permutation(bufs, p)
+        compare_x_sorted_on_device(x, bufs["x_sorted"], p.sorted_token)
+        del bufs
+    # chunk 3 of the 8-chunk fallback (uncapped, its own tokens)
+    ct = moe.moe_chunk_tokens(cfg)
+    assert ct == 8192 and moe.moe_num_chunks(cfg) == 8
+    t0 = 3 * ct
+    sc = cfg_from(wl, T=ct, factor=-1.0, n_chunks=0)
+    bufs = gpu_permute(sc, x[t0:t0 + ct], idx[t0:t0 + ct].contiguous(), False)
+    p = ref.permute_indices(oi[t0:t0 + ct], wl.E, wl.S, None)
+    compare_permutation(bufs, p)
+    compare_x_sorted_on_device(x[t0:t0 + ct], bufs["x_sorted"],
+                               p.sorted_token)
+    del bufs, x
+    torch.cuda.empty_cache()

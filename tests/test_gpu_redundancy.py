@@ -16,6 +16,7 @@ from oracle import moe_ref as ref
 from synth import WORKLOADS, make_logits, make_weights, make_x, sweep_workload
 from tests.gpu_util import (TOL, cfg_from, compare_permutation, f64,
                             expert_accessor, gpu_route, np_)
+from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -123,8 +124,8 @@ def test_gmm_mapped_parity(dtype):
     weights = ref.mapped_weights(ref.dense_weights(*(f64(w) for w in W)),
                                  np.array(gexp))
     want_h, want_y = ref.grouped_ffn(f64(xs), off, weights)
-    assert ref.normwise_error(f64(h), want_h) <= TOL[dtype]
-    assert ref.normwise_error(f64(ys), want_y) <= TOL[dtype]
+    assert_close(f64(h), want_h, TOL[dtype], 'h')
+    assert_close(f64(ys), want_y, TOL[dtype], 'ys')
 
 
 def run_layer(cfg, wl, x, Ld, W, mode):
@@ -166,7 +167,7 @@ def test_layer_with_slots(wl, B):
     tt = torch.from_numpy(toks).cuda()
     want = ref.token_outputs(f64(x[tt]), oi[toks], ow[toks],
                              expert_accessor(*W))
-    assert ref.normwise_error(f64(y[tt]), want) <= 2e-2
+    assert_close(f64(y[tt]), want, 2e-2, 'y[tt]')
     # the graph gives the same bits
     yg = torch.zeros_like(y)
     ws = moe.layer_workspace(cfg)
@@ -189,4 +190,4 @@ def test_small_layer_with_slots_full_compare():
     want = ref.layer_redundant(mc, f64(x), L,
                                ref.dense_weights(*(f64(w) for w in W)), 2)
     assert info["overflow"] == int(want.overflow)
-    assert ref.normwise_error(f64(y), want.y) <= 2e-2
+    assert_close(f64(y), want.y, 2e-2, 'y')

@@ -60,3 +60,43 @@ def test_noalloc_refuses_oversize():
     with pytest.raises(moe.MoeError) as err:
         moe.moe_permute_noalloc(cfg, *([None] * 11))
     assert err.value.status == moe.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_allocates_nothing_and_runs_on_a_side_stream():
+    """After a first call (which looks up the array's address), a call
+    changes neither the device's free memory nor torch's allocation; the
+    same call enqueued on another stream gives the same outputs."""
+    cfg, x, idx = _case(sweep_workload(4096, "zipf"), 2.0)
+    want = _permute(cfg, x, idx, True, noalloc=False)
+    b = moe.alloc_step_buffers(cfg)
+    args = [cfg, x, idx, True] + [b[n] for n in OUTS]
+    moe.moe_permute_noalloc(*args)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    used0 = torch.cuda.memory_allocated()
+    moe.moe_permute_noalloc(*args)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == used0
+    for n in OUTS:
+        b[n].fill_(-7) if b[n].dtype == torch.int32 else b[n].zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    moe.moe_permute_noalloc(*args, stream=side)
+    side.synchronize()
+    for n in OUTS:
+        assert torch.equal(b[n], want[n]), n
+
+
+def test_noalloc_no_tokens():
+    """T = 0: the offsets come back zero and nothing is dropped."""
+    cfg = moe.make_config(0, 128, 8, 2, 128, 2)
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    b = moe.alloc_step_buffers(cfg)
+    for n in ("group_offsets", "uniq_offsets", "n_dropped"):
+        b[n].fill_(7)
+    moe.moe_permute_noalloc(cfg, x, idx, True, *[b[n] for n in OUTS])
+    torch.cuda.synchronize()
+    for n in ("group_offsets", "uniq_offsets", "n_dropped"):
+        assert torch.all(b[n] == 0), n
