@@ -65,7 +65,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from synth import WORKLOADS, make_logits, make_weights, make_x  # noqa: E402
+from synth import (WORKLOADS, make_logit_offset, make_router_weight,  # noqa: E402
+                   make_weights, make_x)
 from synth.workloads import make_dy  # noqa: E402
 
 METRIC = "MoE layer tokens/sec at 1 GB300; permute GB/s and GMM TFLOP/s vs roofline"
@@ -241,9 +242,16 @@ class Layer:
                                    w.n_chunks, w.dtype, w.renorm,
                                    w.redundant_slots)
         self.x = make_x(w, device)
-        L = make_logits(w, self.x if w.routing == "router" else None)
-        self.logits_np = L
-        self.logits = torch.from_numpy(L).to(device)
+        # router: logits = x @ Wr + offset, computed by the library in each
+        # step (here once more so that the logits exist before any step)
+        self.wr = make_router_weight(w, device)
+        self.offset_np = make_logit_offset(w)
+        self.offset = None if self.offset_np is None else \
+            torch.from_numpy(self.offset_np).to(device)
+        self.logits = torch.empty((w.T, w.E), dtype=torch.float32,
+                                  device=device)
+        moe.moe_router_logits(self.cfg, self.x, self.wr, self.offset,
+                              self.logits)
         self.dispatch_only = w.F == 0   # the routing/permute sweep
         self.W = make_weights(w, device) if not self.dispatch_only else None
         self.b = moe.alloc_step_buffers(self.cfg, device)
@@ -281,6 +289,9 @@ class Layer:
         passes (t0, t1, capped)."""
         moe, b, c, W = self.moe, self.b, self.cfg, self.W
         mark = ev or (lambda name: None)
+        mark("router")
+        moe.moe_router_logits(c, self.x, self.wr, self.offset, self.logits,
+                              b["status"])
         mark("route")
         moe.moe_route(c, self.logits, b["topk_idx"], b["topk_w"], b["status"])
         self.routed.record()   # the side stream's tables start after it
@@ -451,11 +462,12 @@ def table_launches(tokens, shards):
 
 def launches_per_step(passes, mode, dispatch_only=False, planned=0,
                       shards=0):
-    """Kernel launches of one step: route 1 (+ check 1 with the fallback,
-    + the plan), then per pass the permute tables (table_launches) and the
-    row scatter, GEMM1 1, GEMM2 1, combine 1 (no GEMMs in the sweep)."""
+    """Kernel launches of one step: router 1, route 1 (+ check 1 with the
+    fallback, + the plan), then per pass the permute tables
+    (table_launches) and the row scatter, GEMM1 1, GEMM2 1, combine 1 (no
+    GEMMs in the sweep)."""
     per = 2 if dispatch_only else 4
-    return (2 if mode == "fallback" else 1) + planned + \
+    return 1 + (2 if mode == "fallback" else 1) + planned + \
         sum(table_launches(t1 - t0, shards) + per
             for (t0, t1, _) in passes if t1 > t0)
 
@@ -509,14 +521,26 @@ def stage_work(w, acc):
     }
 
 
+def router_work(w, with_offset):
+    """Algorithmic bytes and flops of the router GEMM over the batch."""
+    b = 2 if w.dtype == "bf16" else 4
+    return {"bytes": w.T * w.H * b + w.H * w.E * b +
+            w.T * w.E * 4 * (2 if with_offset else 1),
+            "flops": 2 * w.T * w.H * w.E}
+
+
 # ------------------------------------------------------------ the oracle --
-def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0, mode="fallback"):
+def oracle_sample_run(wl, x_dev, wr, offset, W, n_tok, t0=0,
+                      mode="fallback"):
     """Runs the oracle layer on tokens [t0, t0+n_tok) as a batch of its own
-    (same shape parameters and factor); returns (seconds, tokens)."""
+    (same shape parameters and factor), from the router logits on; returns
+    (seconds, tokens)."""
     from oracle import moe_ref as ref
     n_tok = min(n_tok, wl.T - t0)
     xs = x_dev[t0:t0 + n_tok].to("cpu", torch.float64).numpy()
-    Ls = L[t0:t0 + n_tok]
+    wr64 = wr.to("cpu", torch.float64).numpy()
+    off = None if offset is None else offset[t0:t0 + n_tok]
+    Ls = ref.router_logits(xs, wr64, off)
     oi, _, _ = ref.route(Ls, wl.k, wl.renorm)
     touched = sorted(set(int(e) for e in oi.reshape(-1)))
     host = {e: (W[0][e].cpu(), W[1][e].cpu(), W[2][e].cpu()) for e in touched}
@@ -530,7 +554,7 @@ def oracle_sample_run(wl, x_dev, L, W, n_tok, t0=0, mode="fallback"):
     run = {"fallback": ref.layer, "capped": ref.layer_capped,
            "dropless": ref.layer_dropless}[mode]
     t = time.perf_counter()
-    run(cfg, xs, Ls, weights)
+    run(cfg, xs, ref.router_logits(xs, wr64, off), weights)
     return time.perf_counter() - t, n_tok
 
 
@@ -680,7 +704,7 @@ def main():
             s["ms"] += d
             s["n"] += 1
     acc = pass_accounting(layer, passes)
-    work = {}
+    work = {"router": router_work(layer.wl, layer.offset is not None)}
     for a in acc:
         for name, wv in stage_work(layer.wl, a).items():
             t = work.setdefault(name, {"bytes": 0, "flops": 0})
@@ -760,8 +784,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(mean_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": layer.wl.dtype,
-        "data": "synthetic (seeded; Zipf/uniform expert popularity via "
-                "Gumbel-max router logits; random N(0,0.02) expert weights)",
+        "data": "synthetic (seeded; router logits x @ Wr + offset, the "
+                "offset a Zipf/uniform expert popularity by Gumbel-max; "
+                "random N(0,0.02) router and expert weights)",
         "config": {
             "workload": layer.wl.name, "T": layer.wl.T, "H": layer.wl.H,
             "E": layer.wl.E, "k": layer.wl.k, "F": layer.wl.F,
@@ -833,21 +858,25 @@ def graph_run(layer, args, device):
     y_d = torch.empty_like(layer.b["y"])
     ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
     g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws)
-    g.launch()
+
+    def run():   # router logits, then the layer graph
+        moe.moe_router_logits(layer.cfg, x_d, layer.wr, layer.offset, L_d)
+        g.launch()
+    run()
     torch.cuda.synchronize()
     if not torch.equal(y_d, layer.b["y"]):
         raise SystemExit("graph path and stepwise path disagree")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     for _ in range(args.warmup):
         flush.zero_()
-        g.launch()
+        run()
     ms = []
     for _ in range(args.steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), \
             torch.cuda.Event(enable_timing=True)
         a.record()
-        g.launch()
+        run()
         b.record()
         b.synchronize()
         ms.append(a.elapsed_time(b))
@@ -865,17 +894,18 @@ def e2e_pipelined(layer, args, world, device):
     themselves run one after another."""
     moe = layer.moe
     x_h = layer.x.cpu().pin_memory()
-    L_h = layer.logits.cpu().pin_memory()
+    O_h = None if layer.offset is None else layer.offset.cpu().pin_memory()
     y_h = [torch.empty(layer.b["y"].shape, dtype=layer.b["y"].dtype,
                        pin_memory=True) for _ in range(2)]
     ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
+    L_d = torch.empty_like(layer.logits)   # one compute stream: one copy
     sets = []
     for _ in range(2):
         x_d = torch.empty_like(layer.x)
-        L_d = torch.empty_like(layer.logits)
+        O_d = None if O_h is None else torch.empty_like(layer.offset)
         y_d = torch.empty_like(layer.b["y"])
         g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws)
-        sets.append((x_d, L_d, y_d, g))
+        sets.append((x_d, O_d, y_d, g))
     comp = torch.cuda.current_stream()
     up = torch.cuda.Stream(device=device)     # host -> device
     down = torch.cuda.Stream(device=device)   # device -> host
@@ -887,14 +917,17 @@ def e2e_pipelined(layer, args, world, device):
     def steps(n):
         for i in range(n):
             b = i % 2
-            x_d, L_d, y_d, g = sets[b]
+            x_d, O_d, y_d, g = sets[b]
             with torch.cuda.stream(up):
                 up.wait_event(free[b])       # buffer b's last output is out
                 x_d.copy_(x_h, non_blocking=True)
-                L_d.copy_(L_h, non_blocking=True)
+                if O_d is not None:
+                    O_d.copy_(O_h, non_blocking=True)
                 h2d = ev()
                 h2d.record(up)
             comp.wait_event(h2d)
+            moe.moe_router_logits(layer.cfg, x_d, layer.wr, O_d, L_d,
+                                  stream=comp)
             g.launch(comp)
             done = ev()
             done.record(comp)
@@ -921,27 +954,32 @@ def e2e_pipelined(layer, args, world, device):
         raise SystemExit("pipelined end-to-end output differs")
     for s_ in sets:
         s_[3].close()
-    h2d = x_h.numel() * x_h.element_size() + L_h.numel() * L_h.element_size()
+    h2d = x_h.numel() * x_h.element_size() + \
+        (0 if O_h is None else O_h.numel() * O_h.element_size())
     d2h = y_h[0].numel() * y_h[0].element_size()
     return {"value": round(whole_job_tokens_per_s(world, layer.wl.T, mean), 1),
             "unit": UNIT, "ms_per_step": round(mean, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "moe_layer_graph_launch (C ABI), pinned host buffers, "
+            "api": "moe_router_logits + moe_layer_graph_launch (C ABI), "
+                   "pinned host buffers (x and the logit offset in, y out), "
                    "copies on two copy streams overlapping neighbouring "
                    "steps"}
 
 
 def e2e_run(layer, args, world, device, graph=None):
-    """Same metric end to end: pinned host x and logits copied in, the layer,
-    y copied out, every step.  Through moe_layer_graph when available (one
-    launch per layer), else moe_layer."""
+    """Same metric end to end: pinned host x and logit offset copied in, the
+    router and the layer, y copied out, every step.  Through moe_layer_graph
+    when available (one launch per layer), else moe_layer."""
+    moe = layer.moe
     x_h = layer.x.cpu().pin_memory()
-    L_h = layer.logits.cpu().pin_memory()
+    O_h = None if layer.offset is None else layer.offset.cpu().pin_memory()
     y_h = torch.empty(layer.b["y"].shape, dtype=layer.b["y"].dtype,
                       pin_memory=True)
+    O_d = None if O_h is None else torch.empty_like(layer.offset)
     if graph is not None:
         x_d, L_d, y_d = graph["x"], graph["logits"], graph["y"]
-        api = "moe_layer_graph_launch (C ABI), pinned host buffers"
+        api = "moe_router_logits + moe_layer_graph_launch (C ABI), pinned " \
+            "host buffers"
 
         def run_layer():
             graph["graph"].launch()
@@ -949,7 +987,7 @@ def e2e_run(layer, args, world, device, graph=None):
         x_d = torch.empty_like(layer.x)
         L_d = torch.empty_like(layer.logits)
         y_d = torch.empty_like(layer.b["y"])
-        api = "moe_layer (C ABI), pinned host buffers"
+        api = "moe_router_logits + moe_layer (C ABI), pinned host buffers"
 
         def run_layer():
             layer.api_layer(x_d, L_d, y_d)
@@ -957,7 +995,9 @@ def e2e_run(layer, args, world, device, graph=None):
 
     def one():
         x_d.copy_(x_h, non_blocking=True)
-        L_d.copy_(L_h, non_blocking=True)
+        if O_d is not None:
+            O_d.copy_(O_h, non_blocking=True)
+        moe.moe_router_logits(layer.cfg, x_d, layer.wr, O_d, L_d)
         run_layer()
         y_h.copy_(y_d, non_blocking=True)
 
@@ -976,7 +1016,8 @@ def e2e_run(layer, args, world, device, graph=None):
         b.synchronize()
         ms.append(a.elapsed_time(b))
     mean = max_over_ranks(sum(ms) / len(ms), device)
-    h2d = x_h.numel() * x_h.element_size() + L_h.numel() * L_h.element_size()
+    h2d = x_h.numel() * x_h.element_size() + \
+        (0 if O_h is None else O_h.numel() * O_h.element_size())
     d2h = y_h.numel() * y_h.element_size()
     return {"value": round(whole_job_tokens_per_s(world, layer.wl.T, mean), 1),
             "unit": UNIT, "ms_per_step": round(mean, 4),
@@ -987,13 +1028,14 @@ def e2e_run(layer, args, world, device, graph=None):
 def cpu_baseline(layer):
     wl = layer.wl
     n = CPU_SAMPLE.get(wl.name, 32)
-    sec, n = oracle_sample_run(wl, layer.x, layer.logits_np, layer.W, n,
-                               mode=layer.mode)
+    sec, n = oracle_sample_run(wl, layer.x, layer.wr, layer.offset_np,
+                               layer.W, n, mode=layer.mode)
     return {"value": round(n / sec, 4), "unit": UNIT, "cores": _CORES,
             "kind": "oracle",
             "sample": f"first {n} tokens of the {wl.name} batch run as a "
                       f"layer of their own (same H, E, k, F, S, factor; "
-                      f"float64 numpy oracle incl. routing, check, fallback, "
+                      f"float64 numpy oracle incl. router logits, routing, "
+                      f"check, fallback, "
                       f"FFN and combine); {sec:.1f} s"}
 
 
@@ -1234,15 +1276,17 @@ def backward_work(w, accs):
     return out
 
 
-def oracle_backward_sample(wl, x_dev, L, W, dy_dev, n_tok, mode):
+def oracle_backward_sample(wl, x_dev, wr, offset, W, dy_dev, n_tok, mode):
     """The oracle's backward of the mode on tokens [0, n_tok) as a layer of
-    their own: routing, check, the capped pass or the chunked passes, each
-    pass's full backward (weight gradients of the experts it touched)."""
+    their own: routing (on the oracle's own router logits), check, the
+    capped pass or the chunked passes, each pass's full backward (weight
+    gradients of the experts it touched)."""
     from oracle import moe_ref as ref
     n = min(n_tok, wl.T)
     xs = x_dev[:n].to("cpu", torch.float64).numpy()
     dys = dy_dev[:n].to("cpu", torch.float64).numpy()
-    Ls = L[:n]
+    Ls = ref.router_logits(xs, wr.to("cpu", torch.float64).numpy(),
+                           None if offset is None else offset[:n])
     idx, _, _ = ref.route(Ls, wl.k, wl.renorm)
     touched = sorted(set(int(e) for e in idx.reshape(-1)))
     host = {e: (W[0][e].cpu(), W[1][e].cpu(), W[2][e].cpu()) for e in touched}
@@ -1414,7 +1458,8 @@ def backward_main(layer, args, world, rank, device):
         out["e2e"]["serial"] = backward_e2e(bw, args, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = BWD_CPU_SAMPLE.get(w.name, 8)
-        sec, n = oracle_backward_sample(w, layer.x, layer.logits_np, layer.W,
+        sec, n = oracle_backward_sample(w, layer.x, layer.wr, layer.offset_np,
+                                         layer.W,
                                         bw.dy, n, layer.mode)
         out["cpu_baseline"] = {
             "value": round(n / sec, 4), "unit": UNIT, "cores": _CORES,
@@ -1545,16 +1590,18 @@ def backward_e2e_pipelined(bw, args, world, device):
 def reference_arm(args, wl, device):
     """The float64 oracle as the reference implementation, on host cores."""
     x = make_x(wl, device)
-    L = make_logits(wl, x if wl.routing == "router" else None)
+    wr = make_router_weight(wl, device)
+    off = make_logit_offset(wl)
     W = make_weights(wl, device)
     n = REF_SAMPLE.get(wl.name, 8)
     for i in range(args.warmup):
-        oracle_sample_run(wl, x, L, W, n, t0=(i * n) % max(1, wl.T - n))
+        oracle_sample_run(wl, x, wr, off, W, n,
+                          t0=(i * n) % max(1, wl.T - n))
     secs = []
     toks = 0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        s, m = oracle_sample_run(wl, x, L, W, n,
+        s, m = oracle_sample_run(wl, x, wr, off, W, n,
                                  t0=((args.warmup + i) * n) % max(1, wl.T - n))
         secs.append(s)
         toks += m

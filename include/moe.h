@@ -108,6 +108,28 @@ typedef struct {
 } moe_config_t;
 
 /* ----------------------------------------------------------------------
+ * moe_router_logits -- the router's scores of every token for every expert
+ * [PR5920 How: the overflow check is computed from the router's top-k,
+ * i.e. from these scores]:
+ *     logits[t, e] = sum_h x[t, h] w_router[h, e]  (+ logit_offset[t, e])
+ * accumulated in float32.  bf16 layers with H % 64 == 0 and E % 128 == 0
+ * (and 16-byte aligned logits and offset) run on the tensor cores (tcgen05,
+ * 128-column float32 tiles of one token group); other shapes and fp32
+ * layers on CUDA cores.
+ *   x            in  [T, H] dtype, 16-byte aligned
+ *   w_router     in  [H, E] dtype (E contiguous), 16-byte aligned
+ *   logit_offset in  [T, E] float32 or NULL: added after the product (an
+ *                    expert bias broadcast over tokens, routing noise, ...)
+ *   logits       out [T, E] float32 (the input of moe_route)
+ *   status_word  in/out, device int32 or NULL: MOE_DEV_TIMEOUT if a
+ *                pipeline wait of the tensor-core form gave up.
+ * ---------------------------------------------------------------------- */
+moe_status_t moe_router_logits(const moe_config_t *cfg, const void *x,
+                               const void *w_router,
+                               const float *logit_offset, float *logits,
+                               int32_t *status_word, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
  * moe_route -- router top-k and combine weights [PR5920 How: the check is
  * computed from the router's top-k].  One warp per token.
  *   logits   in  [T, E] float32 (device)

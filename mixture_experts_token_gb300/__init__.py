@@ -84,6 +84,7 @@ def _declare(h):
     P = c_void_p
     cfg = ctypes.POINTER(MoeConfig)
     sig = {
+        "moe_router_logits": [cfg, P, P, P, P, P, P],
         "moe_route": [cfg, P, P, P, P, P],
         "moe_check_overflow": [cfg, P, P, P, P, P, P, P, P],
         "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
@@ -233,6 +234,14 @@ def moe_test_stall_gemm_producer(fills: int):
 
 def moe_workspace_bytes(cfg, which) -> int:
     return lib().moe_workspace_bytes(ctypes.byref(cfg), which)
+
+
+def moe_router_logits(cfg, x, w_router, logit_offset, logits,
+                      status_word=None, stream=None):
+    _check(lib().moe_router_logits(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_offset),
+        _ptr(logits), _ptr(status_word), _stream(stream)),
+        "moe_router_logits")
 
 
 def moe_route(cfg, logits, topk_idx, topk_w, status_word=None, stream=None):

@@ -76,6 +76,12 @@ struct Params {
   const __nv_bfloat16* aux_g = nullptr; // MODE 2: g
   const __nv_bfloat16* aux_u = nullptr; // MODE 2: u
   int k_split = 0;                      // MODE 3: k-blocks from the 1st pair
+  // MODE 5 (router logits): float32 output [rows, out_ld], an optional
+  // float32 offset of the same shape added to it, and the row count of the
+  // single group (group_offsets is then null).
+  float* out_f32 = nullptr;
+  const float* offset = nullptr;
+  int rows1 = 0;
   // Tests of the timeout path only: the producer stops after this many
   // stage fills (-1: never), so the MMA warp's next wait runs out.
   long long stall_after_fills = -1;
@@ -117,16 +123,22 @@ __device__ __forceinline__ void decode_tile(const TileTable& tt, int tile,
 }
 
 // All threads: goff[0..G], hpre[0..G], lpre[0..G] for tiles of
-// rows_per_tile rows.
+// rows_per_tile rows.  off == null: one group of rows1 rows (G = 1).
+__device__ __forceinline__ int group_start(const int32_t* __restrict__ off,
+                                           int g, int rows1) {
+  return off ? __ldg(off + g) : (g == 0 ? 0 : rows1);
+}
+
 __device__ void build_tile_table(const int32_t* __restrict__ off, int G,
                                  int* goff, int* hpre, int* lpre, int* wsum,
-                                 int rows_per_tile) {
+                                 int rows_per_tile, int rows1 = 0) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int per = (G + kThreads - 1) / kThreads;
   const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
   int lh = 0, ll = 0;
   for (int g = g0; g < g1; ++g) {
-    const int a = __ldg(off + g), b = __ldg(off + g + 1);
+    const int a = group_start(off, g, rows1);
+    const int b = group_start(off, g + 1, rows1);
     const int mt = b > a ? (b - a + rows_per_tile - 1) / rows_per_tile : 0;
     goff[g] = a;
     hpre[g] = mt >= 2 ? mt : 0;
@@ -134,7 +146,7 @@ __device__ void build_tile_table(const int32_t* __restrict__ off, int G,
     lh += hpre[g];
     ll += lpre[g];
   }
-  if (tid == 0) goff[G] = __ldg(off + G);
+  if (tid == 0) goff[G] = group_start(off, G, rows1);
   int ih = lh, il = ll;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -186,6 +198,8 @@ __device__ void build_tile_table(const int32_t* __restrict__ off, int G,
 //         epilogue turns dh into dg (out) and du (out2) with g, u (aux_*)
 // MODE 3: dx_sorted = [dg | du] [Wg^T ; Wu^T]: K = 2F, the first k_split
 //         k-blocks from (tmA, tmB0), the rest from (tmA1, tmB1), K-major B
+// MODE 5: router logits = x Wr (+ offset) in float32: one group of rows1
+//         token rows, Wr [H, E] read MN-major like Wd, BN = 128
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -193,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmB1,
                   const __grid_constant__ CUtensorMap tmA1, Params p) {
   using L = Tile<BN>;
-  static_assert(MODE == 1 || MODE == 2 || MODE == 3 || BN == 256,
+  static_assert(MODE == 1 || MODE == 2 || MODE == 3 || MODE == 5 ||
+                    BN == 256,
                 "gate + up tiles are 128 + 128 columns");
   constexpr bool kGateUp = MODE == 0 || MODE == 4;   // MN-major gate/up B
   constexpr bool kBKMajor = MODE == 2 || MODE == 3;  // K-major B
@@ -240,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  build_tile_table(p.group_offsets, p.E, goff, hpre, lpre, wsum, BM);
+  build_tile_table(p.group_offsets, p.E, goff, hpre, lpre, wsum, BM, p.rows1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sb + 8192, &tmB0, fb, n * 128 + 64, b_row + kb * BK);
             tma_load_2d(sb + 16384, &tmB1, fb, n * 128, b_row + kb * BK);
             tma_load_2d(sb + 24576, &tmB1, fb, n * 128 + 64, b_row + kb * BK);
-          } else if (MODE == 1) {
+          } else if (MODE == 1 || MODE == 5) {
             tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -475,6 +490,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pg[4 * v + 3]);
             duo[v] = make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2],
                                 pu[4 * v + 3]);
+          }
+        }
+      } else if (MODE == 5) {
+        // float32 logits (+ the offset), one row per thread
+        const long long base =
+            static_cast<long long>(grow) * p.out_ld + n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          if (!valid) continue;
+          float4* dst = reinterpret_cast<float4*>(p.out_f32 + base + c);
+          const float4* add =
+              p.offset ? reinterpret_cast<const float4*>(p.offset + base + c)
+                       : nullptr;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 o = make_float4(__uint_as_float(r[4 * v]),
+                                   __uint_as_float(r[4 * v + 1]),
+                                   __uint_as_float(r[4 * v + 2]),
+                                   __uint_as_float(r[4 * v + 3]));
+            if (add) {
+              const float4 b = __ldg(add + v);
+              o.x += b.x;
+              o.y += b.y;
+              o.z += b.z;
+              o.w += b.w;
+            }
+            dst[v] = o;
           }
         }
       } else {
@@ -926,6 +970,29 @@ cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
   p.aux_u = static_cast<const __nv_bfloat16*>(ubuf);
   return bn == 256 ? tc::launch_one<2, 256>(ad, bd, bd, ad, p, s)
                    : tc::launch_one<2, 128>(ad, bd, bd, ad, p, s);
+}
+
+// Router logits [T, E] float32 = x [T, H] Wr [H, E] (+ offset [T, E]), on
+// the tensor cores: needs bf16, H % 64 == 0 and E % 128 == 0
+// (router_tc_supported).
+bool router_tc_supported(const moe_config_t& c) {
+  return c.dtype == MOE_BF16 && c.H % 64 == 0 && c.E % 128 == 0;
+}
+
+cudaError_t launch_router_bf16(const moe_config_t& c, const void* x,
+                               const void* w_router, const float* offset,
+                               float* logits, int32_t* status,
+                               cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  CUtensorMap a, b;
+  if (!tc::make_map(&a, x, c.H, static_cast<uint64_t>(c.T), 64, tc::BM) ||
+      !tc::make_map(&b, w_router, c.E, c.H, 64, 64))
+    return cudaErrorInvalidValue;
+  tc::Params p{nullptr, nullptr, 1, c.H, c.E / 128, nullptr, c.E, status};
+  p.out_f32 = logits;
+  p.offset = offset;
+  p.rows1 = c.T;
+  return tc::launch_one<5, 128>(a, b, b, a, p, s);
 }
 
 // dx_sorted = dg Wg^T + du Wu^T as one GEMM with K = 2F.

@@ -294,6 +294,14 @@ void set_gemm_stall_for_tests(long long fills);
 // Shape support of the bf16 tensor-core GEMM.
 bool gmm_tc_supported(const moe_config_t& c);
 
+// Router logits [T, E] float32 = x Wr (+ offset): the tensor-core form
+// (bf16, H % 64 == 0, E % 128 == 0) and the CUDA-core form (any shape).
+bool router_tc_supported(const moe_config_t& c);
+cudaError_t launch_router_bf16(const moe_config_t& c, const void* x,
+                               const void* w_router, const float* offset,
+                               float* logits, int32_t* status,
+                               cudaStream_t s);
+
 // Host-side formulas shared by validation and drivers.
 int64_t capacity_rows(const moe_config_t& c);
 int32_t chunk_tokens(const moe_config_t& c);

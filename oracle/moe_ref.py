@@ -37,6 +37,26 @@ INT = np.int64
 
 
 # ---------------------------------------------------------------------------
+# Step 0: router logits.  [PR5920 How]: the check works "from the router's
+# top-k", i.e. on the router's scores of each token for each expert.  The
+# pages do not spell the router out; READING: the scores are a dense
+# projection of the token onto the experts, logits = x Wr with Wr [H, E],
+# plus an optional per-(token, expert) offset (an expert bias and/or
+# routing noise; the synthetic workloads put their popularity law there).
+# ---------------------------------------------------------------------------
+def router_logits(x: np.ndarray, w_router: np.ndarray,
+                  offset: Optional[np.ndarray] = None) -> np.ndarray:
+    """logits [T, E] = x [T, H] @ w_router [H, E] (+ offset [T, E]), in
+    float64."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_router, dtype=np.float64)
+    out = np.matmul(x, w)
+    if offset is not None:
+        out = out + np.asarray(offset, dtype=np.float64)
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Step 1: router top-k and combine weights.
 # [PR5920 How]: the overflow check is computed "from the router's top-k";
 # route() is the function that produces it.  The pages never say how the

@@ -5,5 +5,5 @@ arithmetic.  Both the CUDA path and the float64 oracle receive exactly the
 arrays made here.
 """
 from .workloads import (WORKLOADS, SWEEP_TOKENS, SWEEP_ROUTINGS, Workload,  # noqa: F401
-                        sweep_workload, make_logits, make_x, make_weights,
-                        seeds_for)
+                        sweep_workload, make_logit_offset, make_router_weight,
+                        make_x, make_weights, seeds_for)

@@ -8,18 +8,24 @@ moe_dropless_fallback=layer on the ragged all-to-all MoE path" (MaxText pull
 request 5920), section "End-to-end").  Both pages run on synthetic data;
 these generators stand in for it.
 
-Routing recipes (router logits are an input of the layer):
+Routing recipes.  The router logits are x @ Wr + offset (the router's
+product is the first step of the layer; the oracle and the library compute
+it, this module only draws x, Wr and the offset):
 
-* ``router``: logits = x @ Wr with x, Wr ~ N(0, 1)/sqrt(H) (the tiny layer).
-* ``zipf``: logits_te = -s*ln(e+1) + G_te with G iid Gumbel(0, 1).  By the
-  Gumbel-max property the top-1 expert is Zipf(s)-distributed over experts
-  and the top-k is Zipf-weighted sampling without replacement.  (The page on
-  dynamic redundancy adds Zipf-distributed synthetic data; here the Zipf law
-  is put on expert popularity, the quantity the overflow check sees.)
-  Hot experts have low indices, so they share shard 0.
-* ``uniform``: logits = G (uniform random routing, like use_random_routing).
-* ``adversarial``: logits = 30*[e < E/S] + G: every top-k pick lands in
-  shard 0's experts.
+* ``router``: x, Wr ~ N(0, 1)/sqrt(H) and no offset (the tiny layer).
+* ``zipf``: Wr ~ N(0, 0.02) and offset_te = -s*ln(e+1) + G_te with G iid
+  Gumbel(0, 1).  Without the x @ Wr term the Gumbel-max property would make
+  the top-1 expert exactly Zipf(s)-distributed and the top-k Zipf-weighted
+  sampling without replacement; the x @ Wr term (an independent Gaussian
+  per token and expert, std 0.02*sqrt(H)) adds noise that flattens the law
+  somewhat.  (The page on dynamic redundancy adds Zipf-distributed
+  synthetic data; here the Zipf law is put on expert popularity, the
+  quantity the overflow check sees.)  Hot experts have low indices, so they
+  share shard 0.
+* ``uniform``: Wr ~ N(0, 0.02), offset = G (uniform random routing, like
+  use_random_routing).
+* ``adversarial``: Wr ~ N(0, 0.02), offset = 30*[e < E/S] + G: every top-k
+  pick lands in shard 0's experts.
 
 Seeds: one child seed per tensor from ``numpy.random.SeedSequence(seed)``,
 local generators only (no global random state).
@@ -114,19 +120,23 @@ def make_x(wl: Workload, device="cpu", T: Optional[int] = None) -> torch.Tensor:
     return x.to(wl.torch_dtype)
 
 
-def make_logits(wl: Workload, x: Optional[torch.Tensor] = None) -> np.ndarray:
-    """Router logits [T, E] as float32 numpy (made on the host so routing is
-    the same on every machine)."""
-    seeds = seeds_for(wl.seed)
-    T, E = wl.T, wl.E
+def make_router_weight(wl: Workload, device="cpu") -> torch.Tensor:
+    """Router weight Wr [H, E] in the workload dtype, drawn on the host
+    (numpy PCG64) so that routing is the same on every machine."""
+    rng = np.random.default_rng(seeds_for(wl.seed)[1])
+    w = rng.standard_normal((wl.H, wl.E))
+    w *= (1.0 / np.sqrt(wl.H)) if wl.routing == "router" else wl.w_std
+    return torch.from_numpy(w.astype(np.float32)).to(wl.torch_dtype).to(device)
+
+
+def make_logit_offset(wl: Workload, T: Optional[int] = None):
+    """Per-(token, expert) offset [T, E] float32 added to x @ Wr, or None
+    (``router`` routing)."""
+    T = wl.T if T is None else T
+    E = wl.E
     if wl.routing == "router":
-        if x is None:
-            raise ValueError("router routing needs x")
-        rng = np.random.default_rng(seeds[1])
-        wr = rng.standard_normal((wl.H, E)) / np.sqrt(wl.H)
-        xf = x.detach().to("cpu", torch.float64).numpy()
-        return (xf @ wr).astype(np.float32)
-    rng = np.random.default_rng(seeds[2])
+        return None
+    rng = np.random.default_rng(seeds_for(wl.seed)[2])
     g = rng.gumbel(size=(T, E))
     if wl.routing == "zipf":
         bias = -wl.zipf_s * np.log(np.arange(E, dtype=np.float64) + 1.0)

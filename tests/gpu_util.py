@@ -37,6 +37,24 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
+def host_logits(wl, x, T=None):
+    """The workload's router logits [T, E] as float32, computed by the
+    oracle in float64 from x (device or host), the router weight and the
+    logit offset that synth draws (x @ Wr + offset), a few thousand rows at
+    a time.  Both sides of a routing parity test take these as input."""
+    from synth import make_logit_offset, make_router_weight
+    T = x.shape[0] if T is None else T
+    wr = f64(make_router_weight(wl))
+    off = make_logit_offset(wl, T=T)
+    out = np.empty((T, wl.E), dtype=np.float32)
+    for a in range(0, T, 4096):
+        z = min(T, a + 4096)
+        out[a:z] = ref.router_logits(
+            f64(x[a:z]), wr, None if off is None else off[a:z]).astype(
+                np.float32)
+    return out
+
+
 def gpu_route(cfg, logits_np, status=None):
     T, E = logits_np.shape
     d = torch.from_numpy(np.ascontiguousarray(logits_np)).cuda()

@@ -724,4 +724,27 @@ def pin_error_measures():
         assert ref.elementwise_error(b, a) >= ref.normwise_error(b, a)
 
 
+def pin_router_logits():
+    """x Wr (+ offset): a one-hot token row reads out one row of Wr (so a
+    transposed Wr or swapped operands fail); brute-force triple loop on a
+    small case; the offset adds elementwise; no offset equals a zero one."""
+    rng = _rng(21)
+    H, E = 5, 3
+    w = rng.standard_normal((H, E))
+    x = np.eye(H)
+    assert np.array_equal(ref.router_logits(x, w), w)
+    x = rng.standard_normal((4, H))
+    want = np.zeros((4, E))
+    for t in range(4):
+        for e in range(E):
+            for h in range(H):
+                want[t, e] += x[t, h] * w[h, e]
+    assert np.allclose(ref.router_logits(x, w), want, rtol=1e-13, atol=1e-13)
+    off = rng.standard_normal((4, E))
+    assert np.allclose(ref.router_logits(x, w, off), want + off,
+                       rtol=1e-13, atol=1e-13)
+    assert np.array_equal(ref.router_logits(x, w, np.zeros((4, E))),
+                          ref.router_logits(x, w))
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -1,8 +1,8 @@
 """bench.py's host-side bookkeeping, without a GPU: the kernel-launch counts
 it reports as gpu_launches, pinned to the launch lists ncu recorded for the
-same steps (30 kernels per forward step and 49 per backward step of the
-DeepSeek-V3-shaped layer, whose Zipf routing overflows into 4 chunks of 2048
-tokens; 8 shards)."""
+same steps (31 kernels per forward step -- the router GEMM and 30 -- and
+49 per backward step of the DeepSeek-V3-shaped layer, whose Zipf routing
+overflows into 4 chunks of 2048 tokens; 8 shards)."""
 import bench
 
 
@@ -22,23 +22,23 @@ def test_table_launches():
 
 
 def test_forward_launches():
-    # route + check, then per chunk: 3 table kernels, scatter, GEMM1,
-    # GEMM2, combine
-    assert bench.launches_per_step(chunks(4), "fallback", shards=8) == 30
+    # router + route + check, then per chunk: 3 table kernels, scatter,
+    # GEMM1, GEMM2, combine
+    assert bench.launches_per_step(chunks(4), "fallback", shards=8) == 31
     # no overflow: the capped pass (Llama4-Maverick: 16 shards, 64 blocks)
     assert bench.launches_per_step([(0, 8192, True)], "fallback",
-                                   shards=16) == 2 + 7
+                                   shards=16) == 3 + 7
     assert bench.launches_per_step([(0, 8192, False)], "dropless",
-                                   shards=8) == 8
+                                   shards=8) == 9
     # the routing/permute sweep: no expert FFN; 64K tokens in one capped
     # pass take the dedup scan kernel
     assert bench.launches_per_step(chunks(8, 65536), "fallback",
-                                   dispatch_only=True, shards=8) == 2 + 8 * 5
+                                   dispatch_only=True, shards=8) == 3 + 8 * 5
     assert bench.launches_per_step([(0, 65536, True)], "capped",
-                                   dispatch_only=True, shards=8) == 1 + 6
+                                   dispatch_only=True, shards=8) == 2 + 6
     # the duplication plan adds one launch
     assert bench.launches_per_step([(0, 8192, True)], "fallback", planned=1,
-                                   shards=8) == 3 + 7
+                                   shards=8) == 4 + 7
 
 
 def test_backward_launches():

@@ -11,9 +11,9 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_weights, make_x
+from synth import WORKLOADS, make_weights, make_x
 from synth.workloads import make_dy
-from tests.gpu_util import TOL, cfg_from, f64, np_
+from tests.gpu_util import TOL, cfg_from, f64, host_logits, np_
 from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -54,7 +54,7 @@ def oracle_backward(mc, mode, x, L, W, dy):
 
 def setup(wl):
     x = make_x(wl, "cuda")
-    L = make_logits(wl, x if wl.routing == "router" else None)
+    L = host_logits(wl, x)
     W = make_weights(wl, "cuda")
     dy = make_dy(wl, "cuda")
     return x, L, W, dy

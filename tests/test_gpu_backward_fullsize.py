@@ -23,9 +23,9 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_weights, make_x
+from synth import WORKLOADS, make_weights, make_x
 from synth.workloads import make_dy
-from tests.gpu_util import TOL, cfg_from, expert_accessor, f64
+from tests.gpu_util import TOL, cfg_from, expert_accessor, f64, host_logits
 from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def dlogit_bound(logits_t, idx_t, A, renorm, tol):
 def test_fullsize_backward_sampled(name):
     wl = WORKLOADS[name]
     x = make_x(wl, "cuda")
-    L = make_logits(wl)
+    L = host_logits(wl, x)
     W = make_weights(wl, "cuda")
     dy = make_dy(wl, "cuda")
     cfg = cfg_from(wl)

@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import mixture_experts_token_gb300 as moe
-from synth import WORKLOADS, make_logits, make_weights, make_x
-from tests.gpu_util import cfg_from
+from synth import WORKLOADS, make_weights, make_x
+from tests.gpu_util import cfg_from, host_logits
 
 pytestmark = pytest.mark.gpu
 
@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 def batch(wl, seed):
     w = wl.with_(seed=seed)
     x = make_x(w, "cuda")
-    L = torch.from_numpy(make_logits(w, x if w.routing == "router" else None))
+    L = torch.from_numpy(host_logits(w, x))
     return x, L.cuda()
 
 

@@ -11,8 +11,8 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_weights, make_x
-from tests.gpu_util import TOL, cfg_from, expert_accessor, f64, np_
+from synth import WORKLOADS, make_weights, make_x
+from tests.gpu_util import TOL, cfg_from, expert_accessor, f64, host_logits, np_
 from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 def setup(wl):
     x = make_x(wl, "cuda")
-    L = make_logits(wl, x if wl.routing == "router" else None)
+    L = host_logits(wl, x)
     wg, wu, wd = make_weights(wl, "cuda")
     return x, L, torch.from_numpy(L).cuda(), (wg, wu, wd)
 

@@ -9,9 +9,9 @@ import pytest
 import torch
 
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_x, sweep_workload
+from synth import WORKLOADS, make_x, sweep_workload
 from tests.gpu_util import (cfg_from, compare_permutation, gpu_permute,
-                            gpu_route, np_)
+                            gpu_route, host_logits, np_)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ CASES = [
 
 def inputs(wl):
     x = make_x(wl, "cuda")
-    L = make_logits(wl, x if wl.routing == "router" else None)
+    L = host_logits(wl, x)
     return x, L
 
 

@@ -13,9 +13,9 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_weights, make_x, sweep_workload
+from synth import WORKLOADS, make_weights, make_x, sweep_workload
 from tests.gpu_util import (TOL, cfg_from, compare_permutation, f64,
-                            expert_accessor, gpu_route, np_)
+                            expert_accessor, gpu_route, host_logits, np_)
 from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -67,7 +67,7 @@ def test_plan_and_permute_parity(wl, B):
     wl = wl.with_(redundant_slots=B)
     cfg = cfg_from(wl)
     x = make_x(wl, "cuda")
-    L = make_logits(wl)
+    L = host_logits(wl, x)
     idx, _ = gpu_route(cfg, L)
     oi, _, _ = ref.route(L, wl.k)
     assert np.array_equal(np_(idx), oi)
@@ -149,7 +149,7 @@ def test_layer_with_slots(wl, B):
     wl = wl.with_(redundant_slots=B)
     cfg = cfg_from(wl)
     x = make_x(wl, "cuda")
-    L = make_logits(wl)
+    L = host_logits(wl, x)
     Ld = torch.from_numpy(L).cuda()
     W = make_weights(wl, "cuda")
     oi, ow, _ = ref.route(L, wl.k)
@@ -182,7 +182,7 @@ def test_small_layer_with_slots_full_compare():
     wl = WORKLOADS["small"].with_(redundant_slots=2)
     cfg = cfg_from(wl)
     x = make_x(wl, "cuda")
-    L = make_logits(wl)
+    L = host_logits(wl, x)
     W = make_weights(wl, "cuda")
     y, info = run_layer(cfg, wl, x, torch.from_numpy(L).cuda(), W,
                         moe.MOE_MODE_FALLBACK_LAYER)

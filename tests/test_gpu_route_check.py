@@ -10,8 +10,8 @@ import torch
 
 import mixture_experts_token_gb300 as moe
 from oracle import moe_ref as ref
-from synth import WORKLOADS, make_logits, make_x, sweep_workload
-from tests.gpu_util import cfg_from, gpu_check, gpu_route, np_
+from synth import WORKLOADS, make_x, sweep_workload
+from tests.gpu_util import cfg_from, gpu_check, gpu_route, host_logits, np_
 from tests.parity_log import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -24,8 +24,7 @@ ROUTE_CASES = [
 
 
 def logits_for(wl):
-    x = make_x(wl, "cpu") if wl.routing == "router" else None
-    return make_logits(wl, x)
+    return host_logits(wl, make_x(wl, "cuda"))
 
 
 def oracle_sample(T, n=3000, seed=0):

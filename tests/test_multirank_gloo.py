@@ -22,11 +22,11 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         import bench
-        from synth import WORKLOADS, make_logits
+        from synth import WORKLOADS, make_logit_offset
         # each rank's "step time": rank 1 is the slow one
         t = bench.max_over_ranks(10.0 + 5.0 * rank, "cpu")
         wl = bench.replica_workload(WORKLOADS["small"].with_(T=64), rank)
-        logits = make_logits(wl)
+        logits = make_logit_offset(wl)
         gathered = [torch.zeros(64, 16) for _ in range(world)]
         dist.all_gather(gathered, torch.from_numpy(logits))
         same_seed = bool(torch.equal(gathered[0], gathered[1]))

@@ -13,8 +13,8 @@ import pytest
 import torch
 
 import mixture_experts_token_gb300 as moe
-from synth import WORKLOADS, make_logits, make_x, sweep_workload
-from tests.gpu_util import cfg_from, gpu_route
+from synth import WORKLOADS, make_x, sweep_workload
+from tests.gpu_util import cfg_from, gpu_route, host_logits
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def _permute(cfg, x, idx, capped, noalloc):
 def _case(wl, factor):
     cfg = cfg_from(wl, factor=factor)
     x = make_x(wl, "cuda")
-    idx, _ = gpu_route(cfg, make_logits(wl))
+    idx, _ = gpu_route(cfg, host_logits(wl, x))
     return cfg, x, idx
 
 
