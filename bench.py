@@ -5,31 +5,34 @@
                     [--workload dsv3|l4mav|small|tiny|profile]
 
 One step = one pass of the whole layer over one batch of T tokens whose
-inputs (x, router logits, expert weights) are already in HBM:
-route -> counts + overflow check -> flag read -> capped path, or the chunked
-dropless fallback when a shard overflows -> (per pass) permute + dedup ->
-GEMM1 + SwiGLU -> GEMM2 -> combine.  The default workload is the
-DeepSeek-V3-shaped layer (T=8192, H=7168, E=256, k=8, F=2048, 8 shards,
-Zipf s=1.2 routing, ragged_buffer_factor 2.0), on which the grouped GEMM
-target is stated.
+inputs (x, the router weight and logit offset, the expert weights) are
+already in HBM: router logits (x @ Wr + offset) -> route -> counts +
+overflow check -> capped path, or the chunked dropless fallback when a shard
+overflows -> (per pass) permute + dedup -> GEMM1 + SwiGLU -> GEMM2 ->
+combine.  The default workload is the DeepSeek-V3-shaped layer (T=8192,
+H=7168, E=256, k=8, F=2048, 8 shards, Zipf s=1.2 routing,
+ragged_buffer_factor 2.0), on which the grouped GEMM target is stated.
 
-The timed loop calls the C ABI entry points in the order moe_layer runs them
-(the check that both give identical bits is part of the run), with CUDA
-events on the launch stream around every launch group, so the per-kernel
-durations of the roofline come from the same timed region.  From the
-second pass on, each pass's permute tables (moe_permute_tables) run on a
-side stream during the previous pass's expert FFN; the row scatter
-(moe_permute_scatter) runs on the launch stream.  L2 is flushed (a 256 MiB
-write) between steps, outside the events.  Outside the timed region the same
-steps run twice more with the GPU held (a sleep) until the host has queued
-the passes: with the flush (``stages_host_held``: the kernels' stage times
-without host launch latency) and without it (``warm_l2``).  ``e2e`` is the
-same metric through moe_layer_graph with pinned host buffers, the
-host->device copies of x and the logits and the device->host copy of y
-inside the timed region, overlapping the neighbouring steps on two copy
-streams (``e2e.serial``: through moe_layer, copies in line).
-``cpu_baseline`` is the float64 oracle timed on a bounded token sample of the
-same workload on the host cores.
+The timed step is moe_router_logits followed by one launch of the traced
+layer graph (moe_layer_graph_create_traced): the branch is a conditional
+node on the device, so no step waits on the host.  CUDA events on the launch
+stream bracket every step (and the router); the graph writes a device
+timestamp at every stage boundary, from which the per-stage times of the
+roofline come, in the same timed launches.  L2 is flushed (a 256 MiB write)
+between steps, outside the events.  The same layer through the stepwise
+entry points (host flag read, CUDA events between stages) is checked bit
+for bit against moe_layer and the graph, and reported under ``stepwise``;
+``untraced_graph`` is the graph without the stamps; ``warm_l2`` the traced
+launches without the flush.  ``e2e`` is the same metric through the C ABI
+with pinned host buffers: x and the logit offset copied in, the router and
+the layer graph, y copied out, every step, the copies overlapping the
+neighbouring steps on two copy streams (``e2e.serial``: through moe_layer,
+copies in line).  ``cpu_baseline`` is the float64 oracle timed on a bounded
+token sample of the same workload on the host cores.  The default run then
+times every other workload of the benchmark briefly (``configs``: tiny,
+small, the DeepSeek-V3 layer as one uncapped pass under uniform and Zipf
+routing, Llama4-Maverick, and the routing/permute/dedup sweep at 1K-64K
+tokens under three routings), each with its own clock record.
 
 ``--backward`` times the layer's backward pass instead (its own JSON line):
 route -> check -> per pass: permute, GEMM1 keeping g and u, GEMM2, combine
@@ -47,6 +50,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -585,6 +589,9 @@ def main():
                     help="override the workload's routing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' short runs (the default "
+                         "DeepSeek-V3 run adds them under \"configs\")")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward pass (own JSON line)")
     args = ap.parse_args()
@@ -626,83 +633,97 @@ def main():
             dist.destroy_process_group()
         return
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-
-    # identical bits: stepwise entry points vs the moe_layer call
-    passes = layer.step()
-    torch.cuda.synchronize()
-    if layer.dispatch_only:
-        info = {"overflow": int(layer.b["overflow_flag"].item())
-                if args.mode == "fallback" else -1,
-                "capacity": layer.moe.moe_capacity_rows(layer.cfg)}
-    else:
-        y_api = torch.empty_like(layer.b["y"])
-        info = layer.api_layer(layer.x, layer.logits, y_api)
-        torch.cuda.synchronize()
-        if not torch.equal(y_api, layer.b["y"]):
-            raise SystemExit("stepwise path and moe_layer disagree")
-    if int(layer.b["status"].item()) != 0:
-        raise SystemExit(f"device status {int(layer.b['status'].item())}")
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        layer.step()
-    torch.cuda.synchronize()
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     clocks = ClockSampler(device)
-    timers = []
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        flush.zero_()
-        st = StageTimer()
-        passes = layer.step(st)
-        timers.append(st)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    barrier()
-    clock_rec = clocks.stop()
+    res = measure_layer(layer, args.steps, args.warmup, device, flush,
+                        world=world, clocks=clocks, graph_too=True)
+    w = layer.wl
+    out = {
+        "metric": METRIC, "value": res["value"], "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; router logits x @ Wr + offset, the "
+                "offset a Zipf/uniform expert popularity by Gumbel-max; "
+                "random N(0,0.02) router and expert weights)",
+        "config": config_of(layer, args.mode, res, world),
+    }
+    for key in ("timed_step", "ms_per_step_median", "wall_s_timed_loop",
+                "warm_l2", "gpu_launches", "kernels", "roofline",
+                "check_us", "permute_frac", "combine_frac", "untraced_graph",
+                "stepwise", "clocks"):
+        if res.get(key) is not None:
+            out[key] = res[key]
+    if not args.no_e2e and not layer.dispatch_only:
+        if args.mode == "fallback":
+            e2e = e2e_pipelined(layer, args, world, device)
+            e2e["serial"] = e2e_run(layer, args, world, device, None)
+        else:
+            e2e = e2e_run(layer, args, world, device, None)
+        out["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and \
+            not layer.dispatch_only:
+        out["cpu_baseline"] = cpu_baseline(layer)
+    if world == 1 and args.workload == "dsv3" and args.mode == "fallback" \
+            and args.tokens == 0 and args.redundant_slots == 0 \
+            and args.routing is None and not args.no_configs:
+        # every other workload of the benchmark, a short timed run each
+        del layer
+        torch.cuda.empty_cache()
+        out["configs"] = config_runs(args, device, flush, res)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
-    step_ms = [sum(d for _, d in st.durations()) for st in timers]
-    mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
-    median_ms = float(np.median(step_ms))
 
-    # The same steps with the GPU held until the host has queued the first
-    # pass: the stage times of the kernels alone, without the host's launch
-    # latency after the overflow-flag read (outside the timed region).
-    held = {}
-    side_ms = 0.0
-    for _ in range(args.steps):
-        flush.zero_()
-        st = StageTimer()
-        layer.step(st, hold_cycles=HOLD_CYCLES)
-        torch.cuda.synchronize()
-        for name, d in st.durations():
-            held[name] = held.get(name, 0.0) + d
-        side_ms += sum(a.elapsed_time(z) for a, z in st.side)
-    held_ms = sum(d for n, d in held.items() if n != "hold") / args.steps
-    # ... and the same held steps without the L2 flush (warm L2)
-    warm_ms = 0.0
-    for _ in range(args.steps):
-        st = StageTimer()
-        layer.step(st, hold_cycles=HOLD_CYCLES)
-        torch.cuda.synchronize()
-        warm_ms += sum(d for n, d in st.durations() if n != "hold")
-    warm_ms /= args.steps
+def config_of(layer, mode, res, world):
+    w = layer.wl
+    return {
+        "workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k,
+        "F": w.F, "S": w.S, "ragged_buffer_factor": w.factor,
+        "routing": w.routing + (f" s={w.zipf_s}" if w.routing == "zipf"
+                                else ""),
+        "redundant_slots": w.redundant_slots,
+        "mode": {"fallback": "moe_dropless_fallback=layer",
+                 "capped": "capped path only",
+                 "dropless": "one uncapped pass"}[mode],
+        "overflow": res["overflow"], "passes": res["passes"],
+        "capacity": res["capacity"],
+        "l2": "flushed between steps (256 MiB write, outside the events)",
+        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+    }
 
-    # per-stage durations
-    stage = {}
-    for st in timers:
-        for name, d in st.durations():
-            s = stage.setdefault(name, {"ms": 0.0, "n": 0})
-            s["ms"] += d
-            s["n"] += 1
+
+# ------------------------------------------------ timed layer steps ------
+STAGES = ("permute", "gmm_gate_up", "gmm_down", "combine")
+
+
+def trace_stage_ms(stamps, n_pass):
+    """Stage durations (ms) of one traced graph launch from its stamps
+    (slot layout of moe_layer_graph_create_traced)."""
+    d = {"route": (stamps[1] - stamps[0]) / 1e6,
+         "check": (stamps[2] - stamps[1]) / 1e6}
+    for p in range(n_pass):
+        b = 3 + 5 * p
+        for j, name in enumerate(STAGES):
+            d[name] = d.get(name, 0.0) + (stamps[b + j + 1] -
+                                          stamps[b + j]) / 1e6
+    return d
+
+
+def graph_launches(passes, shards, planned):
+    """Kernels of one traced graph step: the router, route, check, (plan),
+    the branch select, the stamps (3 + 5 per pass), and per pass its permute
+    tables (table_launches), scatter, GEMM1, GEMM2 and combine."""
+    return 1 + 3 + planned + 3 + 5 * len(passes) + \
+        sum(table_launches(t1 - t0, shards) + 4 for (t0, t1, _) in passes
+            if t1 > t0)
+
+
+def stage_table(layer, passes, stage_ms, mean_ms, steps):
+    """kernels dict (per-stage time, share, GB/s, TFLOP/s) and the
+    algorithmic work per stage."""
     acc = pass_accounting(layer, passes)
     work = {"router": router_work(layer.wl, layer.offset is not None)}
     for a in acc:
@@ -710,47 +731,32 @@ def main():
             t = work.setdefault(name, {"bytes": 0, "flops": 0})
             t["bytes"] += wv["bytes"]
             t["flops"] += wv["flops"]
-    peaks, peak_src = load_peaks()
     kernels = {}
-    for name, s in stage.items():
-        per_step = s["ms"] / args.steps
+    for name, ms in stage_ms.items():
+        per_step = ms / steps
         ent = {"ms_per_step": round(per_step, 4),
-               "launch_groups_per_step": s["n"] // args.steps,
                "share": round(per_step / mean_ms, 4)}
-        if name in work:
+        if name in work and per_step > 0:
             wv = work[name]
-            sec = per_step / 1e3
-            ent["GBps"] = round(wv["bytes"] / sec / 1e9, 1)
+            ent["GBps"] = round(wv["bytes"] / (per_step / 1e3) / 1e9, 1)
             if wv["flops"]:
-                ent["TFLOPs"] = round(wv["flops"] / sec / 1e12, 1)
+                ent["TFLOPs"] = round(wv["flops"] / (per_step / 1e3) / 1e12,
+                                      1)
         kernels[name] = ent
+    return kernels, work
 
-    stages_held = {"note": "CUDA events per stage in separate steps whose "
-                           "GPU work waits (a sleep before the first pass) "
-                           "until the host has queued it; HBM fraction of "
-                           "the measured copy peak. permute = the row "
-                           "scatter (plus the first pass's tables); "
-                           "permute_tables = the counting-sort kernels of "
-                           "passes 2.. on the side stream, each overlapping "
-                           "the previous pass's expert FFN",
-                   "permute_tables": {"ms_per_step":
-                                      round(side_ms / args.steps, 4),
-                                      "stream": "side"}}
-    for name in ("permute", "combine"):
-        if name in held and name in work:
-            per_step = held[name] / args.steps
-            gbps = work[name]["bytes"] / (per_step / 1e3) / 1e9
-            stages_held[name] = {"ms_per_step": round(per_step, 4),
-                                 "GBps": round(gbps, 1),
-                                 "frac": round(gbps / peaks["hbm_gbs"], 4)}
 
-    dom = max((n for n in work if n in stage), key=lambda n: stage[n]["ms"])
+def roofline_of(layer, passes, stage_ms, work, steps):
+    peaks, peak_src = load_peaks()
+    cand = [n for n in work if n in stage_ms and n != "router"]
+    dom = max(cand, key=lambda n: stage_ms[n])
     wv = work[dom]
-    n_launch = len(passes)
-    dur = stage[dom]["ms"] / args.steps / n_launch / 1e3     # per launch
+    n_launch = max(1, len(passes))
+    dur = stage_ms[dom] / steps / n_launch / 1e3     # per launch
     bytes_l, flops_l = wv["bytes"] / n_launch, wv["flops"] / n_launch
     t_mem = bytes_l / (peaks["hbm_gbs"] * 1e9)
-    t_flop = flops_l / (peaks["bf16_tflops_sustained"] * 1e12) if flops_l else 0
+    t_flop = flops_l / (peaks["bf16_tflops_sustained"] * 1e12) \
+        if flops_l else 0
     if t_mem >= t_flop:
         achieved = bytes_l / dur / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1),
@@ -765,88 +771,294 @@ def main():
     roof["algorithmic_bytes_per_launch"] = int(bytes_l)
     roof["algorithmic_flops_per_launch"] = int(flops_l)
     roof["launch_ms"] = round(dur * 1e3, 4)
+    if flops_l:
+        roof["tensor_TFLOPs"] = round(flops_l / dur / 1e12, 1)
+        roof["tensor_frac_of_burst"] = round(
+            flops_l / dur / 1e12 / peaks["bf16_tflops"], 4)
     roof["peak_source"] = f"{peak_src} MEASURED_PEAKS.json" \
         if peak_src == "measured" else "fallback"
+    return roof
 
-    # the layer as one CUDA graph launch; e2e with host buffers
-    graph = None if layer.dispatch_only else graph_run(layer, args, device)
-    e2e = None
-    if not args.no_e2e and not layer.dispatch_only:
-        if graph is not None:
-            graph["graph"].close()
-            e2e = e2e_pipelined(layer, args, world, device)
-            e2e["serial"] = e2e_run(layer, args, world, device, None)
-        else:
-            e2e = e2e_run(layer, args, world, device, None)
 
-    out = {
-        "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(mean_ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": layer.wl.dtype,
-        "data": "synthetic (seeded; router logits x @ Wr + offset, the "
-                "offset a Zipf/uniform expert popularity by Gumbel-max; "
-                "random N(0,0.02) router and expert weights)",
-        "config": {
-            "workload": layer.wl.name, "T": layer.wl.T, "H": layer.wl.H,
-            "E": layer.wl.E, "k": layer.wl.k, "F": layer.wl.F,
-            "S": layer.wl.S, "ragged_buffer_factor": layer.wl.factor,
-            "routing": layer.wl.routing + (f" s={layer.wl.zipf_s}"
-                                           if layer.wl.routing == "zipf"
-                                           else ""),
-            "redundant_slots": layer.wl.redundant_slots,
-            "mode": {"fallback": "moe_dropless_fallback=layer",
-                     "capped": "capped path only",
-                     "dropless": "one uncapped pass"}[args.mode],
-            "overflow": info["overflow"], "passes": len(passes),
-            "capacity": info["capacity"],
-            "l2": "flushed between steps (256 MiB write, outside the events)",
-            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-        },
-        "wall_s_timed_loop": round(wall, 3),
-        "ms_per_step_median": round(median_ms, 4),
-        "warm_l2": {
-            "value": round(whole_job_tokens_per_s(world, layer.wl.T,
-                                                  warm_ms), 1),
-            "cold_value": round(whole_job_tokens_per_s(world, layer.wl.T,
-                                                       held_ms), 1),
-            "unit": UNIT, "ms_per_step": round(warm_ms, 4),
-            "cold_ms_per_step": round(held_ms, 4),
-            "note": "outside the timed region, both with the GPU held until "
-                    "the host has queued the passes (the hold not "
-                    "counted): value without, cold_value with the L2 "
-                    "flush between steps"},
-        "gpu_launches": launches_per_step(
-            passes, args.mode, layer.dispatch_only,
-            int(layer.cfg.redundant_slots > 0 and args.mode == "fallback"),
-            layer.wl.S) * args.steps,
+def hbm_frac(kernels, name):
+    peaks, _ = load_peaks()
+    k = kernels.get(name)
+    if not k or "GBps" not in k:
+        return None
+    return round(k["GBps"] / peaks["hbm_gbs"], 4)
+
+
+def steps_for(step_ms, steps, min_s=0.4, cap=400):
+    """Timed steps: at least `steps`, and enough for about min_s seconds so
+    that the clock sampler sees the loop."""
+    return int(max(steps, min(cap, math.ceil(min_s * 1e3 / max(step_ms,
+                                                                1e-3)))))
+
+
+def measure_layer(layer, steps, warmup, device, flush, world=1, clocks=None,
+                  graph_too=False, exact=True):
+    """One workload: the stepwise entry points checked against moe_layer,
+    then the timed steps -- the traced layer graph (router + one graph
+    launch per step) for fallback=layer, else the stepwise entry points
+    with CUDA events between stages.  exact: time exactly `steps` steps;
+    else at least ~0.4 s of steps (for the clock sampler).  Returns the
+    bench fields."""
+    moe = layer.moe
+    passes = layer.step()
+    torch.cuda.synchronize()
+    b = layer.b
+    if layer.dispatch_only:
+        overflow = int(b["overflow_flag"].item()) \
+            if layer.mode == "fallback" else -1
+    else:
+        y_api = torch.empty_like(b["y"])
+        info = layer.api_layer(layer.x, layer.logits, y_api)
+        torch.cuda.synchronize()
+        if not torch.equal(y_api, b["y"]):
+            raise SystemExit("stepwise path and moe_layer disagree")
+        overflow = info["overflow"]
+        del y_api
+    if int(b["status"].item()) != 0:
+        raise SystemExit(f"device status {int(b['status'].item())}")
+    res = {"overflow": overflow, "passes": len(passes),
+           "capacity": moe.moe_capacity_rows(layer.cfg)}
+    planned = int(layer.cfg.redundant_slots > 0 and layer.mode == "fallback")
+    use_graph = layer.mode == "fallback" and not layer.dispatch_only
+
+    # the stepwise entry points, CUDA events between stages
+    for _ in range(warmup):
+        flush.zero_()
+        layer.step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = StageTimer()
+    layer.step(st)
+    torch.cuda.synchronize()
+    one_ms = sum(d for _, d in st.durations())
+    n_sw = steps if (use_graph or exact) else steps_for(one_ms, steps)
+    timers = []
+    if not use_graph and clocks is not None:
+        clocks.start()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for _ in range(n_sw):
+        flush.zero_()
+        st = StageTimer()
+        layer.step(st)
+        timers.append(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clock_rec = clocks.stop() if (not use_graph and clocks) else None
+    sw_ms = [sum(d for _, d in t.durations()) for t in timers]
+    sw_mean = max_over_ranks(sum(sw_ms) / len(sw_ms), device)
+    sw_stage = {}
+    for t in timers:
+        for name, d in t.durations():
+            sw_stage[name] = sw_stage.get(name, 0.0) + d
+    sw_kernels, work = stage_table(layer, passes, sw_stage, sw_mean, n_sw)
+    T = layer.wl.T
+    if not use_graph:
+        res.update({
+            "timed_step": "stepwise entry points (moe_router_logits, "
+                          "moe_route, moe_check_overflow, host flag read, "
+                          "per pass moe_permute_tables/scatter, "
+                          "moe_gmm_gate_up, moe_gmm_down, moe_combine), CUDA "
+                          "events on the launch stream between stages",
+            "value": round(whole_job_tokens_per_s(world, T, sw_mean), 1),
+            "ms_per_step": round(sw_mean, 4),
+            "ms_per_step_median": round(float(np.median(sw_ms)), 4),
+            "wall_s_timed_loop": round(wall, 3), "steps_timed": n_sw,
+            "kernels": sw_kernels,
+            "roofline": roofline_of(layer, passes, sw_stage, work, n_sw),
+            "gpu_launches": launches_per_step(
+                passes, layer.mode, layer.dispatch_only, planned,
+                layer.wl.S) * n_sw,
+            "clocks": clock_rec})
+        res["permute_frac"] = hbm_frac(sw_kernels, "permute")
+        res["combine_frac"] = hbm_frac(sw_kernels, "combine")
+        if "check" in sw_kernels:
+            res["check_us"] = round(sw_kernels["check"]["ms_per_step"] * 1e3,
+                                    2)
+        return res
+
+    # the traced graph: router + one graph launch per step
+    n_slots = moe.moe_layer_graph_trace_slots(layer.cfg)
+    trace = torch.zeros(n_slots, dtype=torch.int64, device=device)
+    x_d = layer.x.clone()
+    L_d = torch.empty_like(layer.logits)
+    y_d = torch.empty_like(b["y"])
+    ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws, status,
+                          trace=trace)
+
+    def run():
+        moe.moe_router_logits(layer.cfg, x_d, layer.wr, layer.offset, L_d,
+                              status)
+        g.launch()
+    run()
+    torch.cuda.synchronize()
+    if not torch.equal(y_d, b["y"]):
+        raise SystemExit("traced graph and stepwise path disagree")
+    for _ in range(warmup):
+        flush.zero_()
+        run()
+    torch.cuda.synchronize()
+    n = steps if exact else steps_for(sw_mean, steps)
+    hist = torch.empty((n, n_slots), dtype=torch.int64, device=device)
+    evs = []
+    if clocks is not None:
+        clocks.start()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.zero_()
+        a, r, z = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record()
+        moe.moe_router_logits(layer.cfg, x_d, layer.wr, layer.offset, L_d,
+                              status)
+        r.record()
+        g.launch()
+        z.record()
+        hist[i].copy_(trace, non_blocking=True)
+        evs.append((a, r, z))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clock_rec = clocks.stop() if clocks is not None else None
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())}")
+    ms = [a.elapsed_time(z) for a, _, z in evs]
+    mean_ms = max_over_ranks(sum(ms) / len(ms), device)
+    stamps = hist.cpu().numpy()
+    stage_ms = {"router": sum(a.elapsed_time(r) for a, r, _ in evs)}
+    for i in range(n):
+        for name, d in trace_stage_ms(stamps[i], len(passes)).items():
+            stage_ms[name] = stage_ms.get(name, 0.0) + d
+    kernels, work = stage_table(layer, passes, stage_ms, mean_ms, n)
+    staged = sum(stage_ms.values()) / n
+    kernels["graph_gaps"] = {
+        "ms_per_step": round(mean_ms - staged, 4),
+        "share": round((mean_ms - staged) / mean_ms, 4),
+        "note": "step time not inside a stage: graph launch, the branch "
+                "select kernel and the stamp kernels between stages"}
+    # warm L2: the same launches without the flush
+    wz = []
+    for _ in range(min(n, 20)):
+        a, z = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        a.record()
+        run()
+        z.record()
+        wz.append((a, z))
+    torch.cuda.synchronize()
+    warm = sum(a.elapsed_time(z) for a, z in wz) / len(wz)
+    res.update({
+        "timed_step": "moe_router_logits + moe_layer_graph_launch of the "
+                      "traced layer graph (route, check, conditional node: "
+                      "capped pass | chunked fallback); CUDA events around "
+                      "each step on the launch stream, stage times from the "
+                      "graph's device timestamps at every stage boundary",
+        "value": round(whole_job_tokens_per_s(world, T, mean_ms), 1),
+        "ms_per_step": round(mean_ms, 4),
+        "ms_per_step_median": round(float(np.median(ms)), 4),
+        "wall_s_timed_loop": round(wall, 3), "steps_timed": n,
         "kernels": kernels,
-        "stages_host_held": stages_held,
-        "roofline": roof,
-    }
-    out["value"] = round(whole_job_tokens_per_s(world, layer.wl.T, mean_ms), 1)
-    if graph is not None:
-        out["graph_layer"] = {
-            "value": round(whole_job_tokens_per_s(world, layer.wl.T,
-                                                  graph["ms_per_step"]), 1),
-            "unit": UNIT, "ms_per_step": round(graph["ms_per_step"], 4),
-            "api": "moe_layer_graph_launch: route, check, conditional node "
-                   "(capped pass | chunked fallback), one launch"}
-    if clock_rec:
-        out["clocks"] = clock_rec
-    if e2e:
-        out["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and \
-            not layer.dispatch_only:
-        out["cpu_baseline"] = cpu_baseline(layer)
-    if rank == 0:
-        print(json.dumps(out))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        "roofline": roofline_of(layer, passes, stage_ms, work, n),
+        "check_us": round(kernels["check"]["ms_per_step"] * 1e3, 2),
+        "gpu_launches": graph_launches(passes, layer.wl.S, planned) * n,
+        "warm_l2": {"value": round(whole_job_tokens_per_s(world, T, warm),
+                                   1),
+                    "unit": UNIT, "ms_per_step": round(warm, 4),
+                    "note": "the timed launches without the L2 flush"},
+        "stepwise": {"value": round(whole_job_tokens_per_s(world, T,
+                                                           sw_mean), 1),
+                     "ms_per_step": round(sw_mean, 4),
+                     "note": "the same layer through the stepwise entry "
+                             "points with the host reading the overflow "
+                             "flag, CUDA events between stages",
+                     "permute_frac": hbm_frac(sw_kernels, "permute"),
+                     "combine_frac": hbm_frac(sw_kernels, "combine")},
+        "clocks": clock_rec})
+    res["permute_frac"] = hbm_frac(kernels, "permute")
+    res["combine_frac"] = hbm_frac(kernels, "combine")
+    g.close()
+    if graph_too:
+        gr = graph_run(layer, steps, warmup, device)
+        if gr is not None:
+            gr["graph"].close()
+            res["untraced_graph"] = {
+                "value": round(whole_job_tokens_per_s(world, T,
+                                                      gr["ms_per_step"]), 1),
+                "ms_per_step": round(gr["ms_per_step"], 4),
+                "note": "moe_router_logits + moe_layer_graph_launch without "
+                        "the stage stamps"}
+    del hist, trace, ws, x_d, L_d, y_d
+    return res
 
 
-def graph_run(layer, args, device):
+CONFIG_STEPS = 10
+
+
+def config_runs(args, device, flush, head):
+    """Every other workload of the benchmark at 1 GPU, each a short timed
+    run of its own (few steps; at least ~0.4 s of timed work for the clock
+    sampler): the tiny and small layers, the DeepSeek-V3 layer as one
+    uncapped pass under uniform and Zipf routing (where the GEMM's tensor
+    fraction is judged), the Llama4-Maverick layer, and the
+    routing/permute/dedup sweep.  Returns a list of compact records."""
+    from synth import SWEEP_ROUTINGS, SWEEP_TOKENS, sweep_workload
+    runs = [("dsv3", WORKLOADS["dsv3"], "fallback")]
+    runs += [(n, WORKLOADS[n], "fallback") for n in ("tiny", "small")]
+    runs += [("dsv3_uncapped_uniform",
+              WORKLOADS["dsv3"].with_(routing="uniform", zipf_s=0.0,
+                                      name="dsv3_uniform"), "dropless"),
+             ("dsv3_uncapped_zipf", WORKLOADS["dsv3"], "dropless"),
+             ("l4mav", WORKLOADS["l4mav"], "fallback")]
+    runs += [(f"sweep_T{T}_{r}", sweep_workload(T, r), "fallback")
+             for T in SWEEP_TOKENS for r in SWEEP_ROUTINGS]
+    out = []
+    for label, wl, mode in runs:
+        if label == "dsv3":
+            res = head
+        else:
+            layer = Layer(wl, device, mode=mode)
+            res = measure_layer(layer, CONFIG_STEPS, 3, device, flush,
+                                clocks=ClockSampler(device), exact=False)
+            del layer
+            torch.cuda.empty_cache()
+        rec = {"config": label, "T": wl.T, "mode": mode,
+               "routing": wl.routing, "dtype": wl.dtype,
+               "value": res["value"], "unit": UNIT,
+               "ms_per_step": res["ms_per_step"],
+               "overflow": res["overflow"], "passes": res["passes"],
+               "timed": "traced graph" if res["timed_step"].startswith(
+                   "moe_router_logits + moe_layer_graph") else "stepwise",
+               "steps_timed": res.get("steps_timed")}
+        roof = res["roofline"]
+        rec["dominant"] = {k: roof[k] for k in (
+            "kernel", "bound", "achieved", "unit", "peak", "frac")}
+        if "tensor_TFLOPs" in roof:
+            rec["dominant"]["tensor_TFLOPs"] = roof["tensor_TFLOPs"]
+            rec["dominant"]["tensor_frac_of_burst"] = \
+                roof["tensor_frac_of_burst"]
+        gm = [res["kernels"][n] for n in ("gmm_gate_up", "gmm_down")
+              if n in res["kernels"]]
+        if len(gm) == 2 and all("TFLOPs" in g_ for g_ in gm):
+            ms = gm[0]["ms_per_step"] + gm[1]["ms_per_step"]
+            fl = sum(g_["TFLOPs"] * g_["ms_per_step"] for g_ in gm) / ms
+            peaks, _ = load_peaks()
+            rec["gmm_TFLOPs"] = round(fl, 1)
+            rec["gmm_tensor_frac_of_burst"] = round(
+                fl / peaks["bf16_tflops"], 4)
+        rec["permute_frac"] = res.get("permute_frac")
+        rec["combine_frac"] = res.get("combine_frac")
+        if "check_us" in res:
+            rec["check_us"] = res["check_us"]
+        rec["clocks"] = res.get("clocks")
+        out.append(rec)
+    return out
+
+
+def graph_run(layer, steps, warmup, device):
     """The same layer as one CUDA graph launch per step (moe_layer_graph):
     device-resident throughput, and the bits checked against the stepwise
     result."""
@@ -867,11 +1079,11 @@ def graph_run(layer, args, device):
     if not torch.equal(y_d, layer.b["y"]):
         raise SystemExit("graph path and stepwise path disagree")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         run()
     ms = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), \
             torch.cuda.Event(enable_timing=True)

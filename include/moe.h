@@ -451,6 +451,28 @@ moe_status_t moe_layer_graph_create(const moe_config_t *cfg, const void *x,
                                     void *y, int32_t *status_word,
                                     void *workspace, size_t workspace_bytes,
                                     moe_layer_graph_t **graph_out);
+/* moe_layer_graph_create_traced -- the same graph with a device timestamp
+ * (int64 nanoseconds of %globaltimer, written by a one-thread kernel) at
+ * every stage boundary, for timing the stages of the graph a caller runs
+ * (a conditional node's bodies cannot hold CUDA event nodes).  trace: device
+ * int64 [moe_layer_graph_trace_slots(cfg)], 8-byte aligned; each launch
+ * writes, in order on the device:
+ *   0 layer start, 1 routing done, 2 check (and plan) and branch select
+ *   done; then for pass p (the capped pass is p = 0; the fallback's chunks
+ *   p = 0 .. n-1): 3 + 5p start (permute tables and row scatter),
+ *   4 + 5p GEMM1 start, 5 + 5p GEMM2 start, 6 + 5p combine start,
+ *   7 + 5p pass end.
+ * Slots of passes the launch did not run keep their old values.  The
+ * stamps add one small kernel per boundary (about 1 us each); the layer's
+ * results are those of the untraced graph, bit for bit. */
+moe_status_t moe_layer_graph_create_traced(
+    const moe_config_t *cfg, const void *x, const float *logits,
+    const void *w_gate, const void *w_up, const void *w_down, void *y,
+    int32_t *status_word, void *workspace, size_t workspace_bytes,
+    int64_t *trace, moe_layer_graph_t **graph_out);
+/* Trace slots of the traced graph: 3 + 5 * max(1, fallback chunks); 0 for
+ * an invalid cfg. */
+int32_t moe_layer_graph_trace_slots(const moe_config_t *cfg);
 moe_status_t moe_layer_graph_launch(moe_layer_graph_t *graph,
                                     moe_stream_t stream);
 const int32_t *moe_layer_graph_overflow_flag(const moe_layer_graph_t *graph);

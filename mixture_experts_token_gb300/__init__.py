@@ -137,6 +137,12 @@ def _declare(h):
     h.moe_layer_graph_create.argtypes = [cfg, P, P, P, P, P, P, P, P,
                                          c_size_t, ctypes.POINTER(P)]
     h.moe_layer_graph_create.restype = c_int
+    h.moe_layer_graph_create_traced.argtypes = [cfg, P, P, P, P, P, P, P,
+                                                P, c_size_t, P,
+                                                ctypes.POINTER(P)]
+    h.moe_layer_graph_create_traced.restype = c_int
+    h.moe_layer_graph_trace_slots.argtypes = [cfg]
+    h.moe_layer_graph_trace_slots.restype = c_int32
     h.moe_layer_graph_launch.argtypes = [P, P]
     h.moe_layer_graph_launch.restype = c_int
     h.moe_layer_graph_overflow_flag.argtypes = [P]
@@ -225,6 +231,10 @@ def moe_num_chunks(cfg) -> int:
 def moe_gmm_uses_pair(cfg, n_groups=0, rows_bound=0) -> int:
     return int(lib().moe_gmm_uses_pair(ctypes.byref(cfg), n_groups,
                                        rows_bound))
+
+
+def moe_layer_graph_trace_slots(cfg) -> int:
+    return int(lib().moe_layer_graph_trace_slots(ctypes.byref(cfg)))
 
 
 def moe_test_stall_gemm_producer(fills: int):
@@ -514,15 +524,22 @@ class MoeLayerGraph:
     to the tensors given here (they must outlive the graph)."""
 
     def __init__(self, cfg, x, logits, w_gate, w_up, w_down, y, workspace,
-                 status_word=None):
+                 status_word=None, trace=None):
         self._h = c_void_p()
         self._keep = (x, logits, w_gate, w_up, w_down, y, workspace,
-                      status_word)
-        _check(lib().moe_layer_graph_create(
-            ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate),
-            _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(status_word),
-            _ptr(workspace), _nbytes(workspace), ctypes.byref(self._h)),
-            "moe_layer_graph_create")
+                      status_word, trace)
+        if trace is None:
+            _check(lib().moe_layer_graph_create(
+                ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate),
+                _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(status_word),
+                _ptr(workspace), _nbytes(workspace), ctypes.byref(self._h)),
+                "moe_layer_graph_create")
+        else:
+            _check(lib().moe_layer_graph_create_traced(
+                ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(w_gate),
+                _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(status_word),
+                _ptr(workspace), _nbytes(workspace), _ptr(trace),
+                ctypes.byref(self._h)), "moe_layer_graph_create_traced")
 
     def launch(self, stream=None):
         _check(lib().moe_layer_graph_launch(self._h, _stream(stream)),

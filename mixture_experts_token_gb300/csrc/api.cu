@@ -186,10 +186,25 @@ moe_config_t sub_config(const moe_config_t& c, int T) {
 
 // One pass on tokens whose routing is already in `topk_idx/topk_w`:
 // permute (cap or uncapped) -> grouped FFN -> combine into y.
+namespace {
+__global__ void stamp_kernel(int64_t* slot) {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  *slot = static_cast<int64_t>(t);
+}
+}  // namespace
+
+cudaError_t stamp(int64_t* trace, int slot, cudaStream_t s) {
+  if (trace == nullptr) return cudaSuccess;
+  stamp_kernel<<<1, 1, 0, s>>>(trace + slot);
+  return cudaGetLastError();
+}
+
 cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const float* topk_w, int64_t cap, const void* wg,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
-                 int32_t* status, cudaStream_t s, bool planned) {
+                 int32_t* status, cudaStream_t s, bool planned,
+                 int pass_index) {
   PermutePlan plan;
   Groups groups = identity_groups(c);
   if (planned && c.redundant_slots > 0) {
@@ -201,15 +216,29 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
   if (cap >= 0)  // a capped pass keeps at most S*C rows
     groups.max_rows = std::min<int64_t>(static_cast<int64_t>(c.T) * c.k,
                                         static_cast<int64_t>(c.S) * cap);
-  cudaError_t e = launch_permute(c, x, topk_idx, cap, b.x_sorted, b.row_of,
-                                 b.sorted_token, b.group_offsets,
-                                 b.uniq_offsets, b.uniq_tokens, b.expand_idx,
-                                 b.n_dropped, b.pws, status, s, plan);
+  int64_t* tr = b.trace;
+  cudaError_t e = stamp(tr, trace_slot(pass_index, 0), s);
   if (e != cudaSuccess) return e;
-  e = launch_gmm(c, groups, b.x_sorted, b.group_offsets, wg, wu, wd, b.h,
-                 b.y_sorted, status, s);
+  e = launch_permute(c, x, topk_idx, cap, b.x_sorted, b.row_of,
+                     b.sorted_token, b.group_offsets, b.uniq_offsets,
+                     b.uniq_tokens, b.expand_idx, b.n_dropped, b.pws, status,
+                     s, plan);
   if (e != cudaSuccess) return e;
-  return launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
+  if (tr == nullptr) {
+    e = launch_gmm(c, groups, b.x_sorted, b.group_offsets, wg, wu, wd, b.h,
+                   b.y_sorted, status, s);
+  } else if ((e = stamp(tr, trace_slot(pass_index, 1), s)) == cudaSuccess &&
+             (e = launch_gmm1(c, groups, b.x_sorted, b.group_offsets, wg, wu,
+                              b.h, status, s)) == cudaSuccess &&
+             (e = stamp(tr, trace_slot(pass_index, 2), s)) == cudaSuccess) {
+    e = launch_gmm2(c, groups, b.h, b.group_offsets, wd, b.y_sorted, status,
+                    s);
+  }
+  if (e != cudaSuccess) return e;
+  if ((e = stamp(tr, trace_slot(pass_index, 3), s)) != cudaSuccess) return e;
+  e = launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
+  if (e != cudaSuccess) return e;
+  return stamp(tr, trace_slot(pass_index, 4), s);
 }
 
 // The chunked fallback with each chunk's permute tables computed one chunk
@@ -248,19 +277,27 @@ cudaError_t pipelined_passes(const moe_config_t& c, const void* x,
     const moe_config_t sc = sub_config(c, tc);
     const PassTables tb = b.tables(i);
     const size_t o = static_cast<size_t>(t0);
+    int64_t* tr = b.trace;
+    if ((e = stamp(tr, trace_slot(i, 0), s)) != cudaSuccess) return e;
     e = i == 0 ? tables(0, s) : cudaStreamWaitEvent(s, pp.ready[i & 1], 0);
     if (e != cudaSuccess) return e;
     if ((e = launch_permute_scatter(
              sc, static_cast<const char*>(x) + o * row_bytes,
              b.row_of + o * c.k, tb.uniq_offsets, b.x_sorted, tb.uniq_tokens,
              tb.expand_idx, tb.pws, s)) != cudaSuccess ||
-        (e = launch_gmm(sc, identity_groups(sc), b.x_sorted, tb.group_offsets,
-                        wg, wu, wd, b.h, b.y_sorted, status, s)) !=
+        (e = stamp(tr, trace_slot(i, 1), s)) != cudaSuccess ||
+        (e = launch_gmm1(sc, identity_groups(sc), b.x_sorted,
+                         tb.group_offsets, wg, wu, b.h, status, s)) !=
             cudaSuccess ||
+        (e = stamp(tr, trace_slot(i, 2), s)) != cudaSuccess ||
+        (e = launch_gmm2(sc, identity_groups(sc), b.h, tb.group_offsets, wd,
+                         b.y_sorted, status, s)) != cudaSuccess ||
+        (e = stamp(tr, trace_slot(i, 3), s)) != cudaSuccess ||
         (e = launch_combine(sc, b.y_sorted, b.row_of + o * c.k,
                             topk_w + o * c.k,
                             static_cast<char*>(y) + o * row_bytes, s)) !=
             cudaSuccess ||
+        (e = stamp(tr, trace_slot(i, 4), s)) != cudaSuccess ||
         (e = cudaEventRecord(pp.done[i & 1], s)) != cudaSuccess)
       return e;
     if (i + 1 < n && (e = tables(i + 1, pp.side)) != cudaSuccess) return e;
@@ -290,7 +327,8 @@ cudaError_t chunked_passes(const moe_config_t& c, const void* x,
     const size_t o = static_cast<size_t>(t0);
     cudaError_t e = pass(sc, static_cast<const char*>(x) + o * row_bytes,
                          topk_idx + o * c.k, topk_w + o * c.k, -1, wg, wu, wd,
-                         static_cast<char*>(y) + o * row_bytes, b, status, s);
+                         static_cast<char*>(y) + o * row_bytes, b, status, s,
+                         false, n);
     if (e != cudaSuccess) return e;
   }
   if (n_run) *n_run = n;

@@ -149,6 +149,9 @@ struct LayerBufs {
   PermuteScratch pws;
   void *x_sorted, *h, *y_sorted;
   PassTables alt;  // a second table set, for pipelined chunked passes
+  // Stage timestamps of a traced layer graph (device int64, slots of
+  // trace_slot below), or null: no stamps.
+  int64_t* trace = nullptr;
   PassTables tables(int i) const {  // set i % 2
     if (i & 1) return alt;
     return {sorted_token, group_offsets, uniq_offsets, uniq_tokens,
@@ -165,12 +168,26 @@ LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
                       size_t* bytes);
 size_t layer_bytes(const moe_config_t& c, int T);
 moe_config_t sub_config(const moe_config_t& c, int T);
+// Trace slots of a layer graph (moe.h, moe_layer_graph_create_traced):
+// 0 layer start, 1 routing done, 2 check (and plan) done; pass p's stage
+// boundaries at 3 + 5p + {0 start, 1 GEMM1, 2 GEMM2, 3 combine, 4 end}.
+constexpr int kTraceHead = 3;
+constexpr int kTracePerPass = 5;
+inline int trace_slot(int pass, int stage) {
+  return kTraceHead + kTracePerPass * pass + stage;
+}
+// One %globaltimer stamp (ns) into trace[slot] on s; nothing if trace is
+// null.
+cudaError_t stamp(int64_t* trace, int slot, cudaStream_t s);
+
 // permute (cap, or uncapped when cap < 0) -> GEMM1 -> GEMM2 -> combine;
 // with planned = true, over the virtual groups of the plan in b.
+// pass_index: the trace slots of the pass (b.trace).
 cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const float* topk_w, int64_t cap, const void* wg,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
-                 int32_t* status, cudaStream_t s, bool planned = false);
+                 int32_t* status, cudaStream_t s, bool planned = false,
+                 int pass_index = 0);
 // the chunked dropless fallback over routing already in topk_idx/topk_w.
 // With pp (b carved for all T tokens), the permute tables of chunk i+1 run
 // on pp->side during chunk i's expert FFN, in two table sets.

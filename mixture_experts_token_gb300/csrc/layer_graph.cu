@@ -11,7 +11,10 @@
 //
 // The graph is bound to the buffers given at creation (inputs, weights,
 // output, workspace); callers refresh x and the logits in place and launch
-// again.
+// again.  The traced form adds one-thread kernels that write %globaltimer
+// at every stage boundary into a caller buffer, so that a caller can time
+// the stages of the graph it runs (conditional bodies cannot hold event
+// nodes).
 #include "internal.h"
 
 struct moe_layer_graph {
@@ -81,8 +84,10 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
                                     cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
   const bool planned = c.redundant_slots > 0;
-  if ((e = launch_route(c, logits, b.topk_idx, b.topk_w, status,
+  if ((e = stamp(b.trace, 0, main_s.s)) != cudaSuccess ||
+      (e = launch_route(c, logits, b.topk_idx, b.topk_w, status,
                         main_s.s)) != cudaSuccess ||
+      (e = stamp(b.trace, 1, main_s.s)) != cudaSuccess ||
       (e = launch_check(c, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
                         b.req, b.cap, main_s.s)) != cudaSuccess)
     return e;
@@ -93,6 +98,7 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   set_branch_kernel<<<1, 1, 0, main_s.s>>>(handle,
                                            planned ? b.flag_after : b.flag);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = stamp(b.trace, 2, main_s.s)) != cudaSuccess) return e;
 
   cudaStreamCaptureStatus cst;
   const cudaGraphNode_t* deps = nullptr;
@@ -154,19 +160,12 @@ void release(moe_layer_graph* g) {
   delete g;
 }
 
-}  // namespace
-}  // namespace moe
-
-using namespace moe;
-
-extern "C" {
-
-moe_status_t moe_layer_graph_create(const moe_config_t* cfg, const void* x,
-                                    const float* logits, const void* w_gate,
-                                    const void* w_up, const void* w_down,
-                                    void* y, int32_t* status_word,
-                                    void* workspace, size_t workspace_bytes,
-                                    moe_layer_graph_t** graph_out) {
+moe_status_t create_graph(const moe_config_t* cfg, const void* x,
+                          const float* logits, const void* w_gate,
+                          const void* w_up, const void* w_down, void* y,
+                          int32_t* status_word, void* workspace,
+                          size_t workspace_bytes, int64_t* trace,
+                          moe_layer_graph_t** graph_out) {
   if (graph_out == nullptr) return MOE_ERR_INVALID_ARG;
   *graph_out = nullptr;
   moe_status_t st = validate(cfg);
@@ -179,7 +178,8 @@ moe_status_t moe_layer_graph_create(const moe_config_t* cfg, const void* x,
   if (workspace == nullptr || !ok_ptr(workspace, true) ||
       workspace_bytes < layer_bytes(*cfg, cfg->T))
     return MOE_ERR_WORKSPACE;
-  const LayerBufs b = carve_layer(workspace, *cfg, cfg->T, nullptr);
+  LayerBufs b = carve_layer(workspace, *cfg, cfg->T, nullptr);
+  b.trace = trace;
   moe_layer_graph* g = new moe_layer_graph();
   const cudaError_t e = build(*cfg, x, logits, w_gate, w_up, w_down, y,
                               status_word, b, g);
@@ -190,6 +190,43 @@ moe_status_t moe_layer_graph_create(const moe_config_t* cfg, const void* x,
   }
   *graph_out = g;
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_layer_graph_trace_slots(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  const int ct = chunk_tokens(*cfg);
+  const int n = ct > 0 ? (cfg->T + ct - 1) / ct : 0;
+  return trace_slot(std::max(n, 1), 0);
+}
+
+moe_status_t moe_layer_graph_create_traced(
+    const moe_config_t* cfg, const void* x, const float* logits,
+    const void* w_gate, const void* w_up, const void* w_down, void* y,
+    int32_t* status_word, void* workspace, size_t workspace_bytes,
+    int64_t* trace, moe_layer_graph_t** graph_out) {
+  if (graph_out == nullptr) return MOE_ERR_INVALID_ARG;
+  *graph_out = nullptr;
+  if (trace == nullptr || (reinterpret_cast<uintptr_t>(trace) & 7u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  return create_graph(cfg, x, logits, w_gate, w_up, w_down, y, status_word,
+                      workspace, workspace_bytes, trace, graph_out);
+}
+
+moe_status_t moe_layer_graph_create(const moe_config_t* cfg, const void* x,
+                                    const float* logits, const void* w_gate,
+                                    const void* w_up, const void* w_down,
+                                    void* y, int32_t* status_word,
+                                    void* workspace, size_t workspace_bytes,
+                                    moe_layer_graph_t** graph_out) {
+  return create_graph(cfg, x, logits, w_gate, w_up, w_down, y, status_word,
+                      workspace, workspace_bytes, nullptr, graph_out);
 }
 
 moe_status_t moe_layer_graph_launch(moe_layer_graph_t* graph,

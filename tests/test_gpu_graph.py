@@ -86,3 +86,37 @@ def test_graph_both_branches_on_one_graph():
         assert flags[-1] == info["overflow"]
     assert flags == [1, 0, 1]
     g.close()
+
+
+@pytest.mark.parametrize("wl", [WORKLOADS["small"], WORKLOADS["tiny"]],
+                         ids=["small", "tiny"])
+def test_traced_graph_bits_and_stamps(wl):
+    """The traced graph writes the bits of the untraced one, and its stamps
+    of the branch it took increase along the stages: layer start, routing,
+    check, then each pass's start, GEMM1, GEMM2, combine and end."""
+    for factor in (0.3, 50.0):          # the fallback, then the capped pass
+        cfg = cfg_from(wl, factor=factor)
+        W = make_weights(wl, "cuda")
+        x, L = batch(wl, 0)
+        slots = moe.moe_layer_graph_trace_slots(cfg)
+        n_chunks = moe.moe_num_chunks(cfg)
+        assert slots == 3 + 5 * max(1, n_chunks)
+        trace = torch.zeros(slots, dtype=torch.int64, device="cuda")
+        y = torch.zeros((wl.T, wl.H), dtype=x.dtype, device="cuda")
+        y0 = torch.zeros_like(y)
+        ws, ws0 = moe.layer_workspace(cfg), moe.layer_workspace(cfg)
+        g = moe.MoeLayerGraph(cfg, x, L, *W, y, ws, trace=trace)
+        g0 = moe.MoeLayerGraph(cfg, x, L, *W, y0, ws0)
+        g.launch()
+        g0.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y0)
+        flag = device_flag(g, ws)
+        passes = g.fallback_chunks() if flag else 1
+        st = trace.cpu().tolist()
+        used = st[:3 + 5 * passes]
+        assert all(a <= b for a, b in zip(used, used[1:])), used
+        assert used[0] > 0 and used[-1] - used[0] > 0
+        assert bool(flag) == (factor < 1.0)
+        g.close()
+        g0.close()

@@ -18,6 +18,12 @@ ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(
     os.path.abspath(__file__))), "oracle", "moe_ref.py")
 
 MUTANTS = {
+    "router_offset_dropped": (
+        "        out = out + np.asarray(offset, dtype=np.float64)",
+        "        out = out + 0.0"),
+    "router_weight_layout_misread": (
+        "    out = np.matmul(x, w)\n",
+        "    out = np.matmul(x, w.reshape(w.shape[1], w.shape[0]).T)\n"),
     "tie_to_higher_index": (
         "keyed = [(-clean_logit(float(row[e])), e) for e in range(E)]",
         "keyed = [(-clean_logit(float(row[e])), -e) for e in range(E)]"),
