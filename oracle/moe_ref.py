@@ -893,3 +893,165 @@ def layer_redundant_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
                                       dy)
     return layer_pass_backward(cfg, x, logits, w_gate, w_up, w_down, dy, C,
                                groups=(vidx, G, plan.group_expert))
+
+
+# ---------------------------------------------------------------------------
+# Expert parallelism across ranks.  [PR5920 Why, How]: on the ragged
+# all-to-all path every device sends its tokens' rows to the devices that own
+# their experts, each token once per destination, and the receiver expands a
+# token to its expert rows ([PR4760 review of ra2a_dedup_and_route]:
+# expand_indices, never truncated).  [PR5920 Tests]: the overflow flag is
+# global, so every rank takes the same branch.  READINGS:
+#  * N ranks = N shards; rank d owns experts [d*E/N, (d+1)*E/N);
+#  * the check sums each shard's receive count over the source ranks and
+#    takes C from the global token count (the single-device formula on the
+#    ranks' batches together);
+#  * the fallback's chunk count comes from that global configuration; each
+#    rank splits its own tokens into n contiguous chunks of ceil(T_r/n) and
+#    pass i is every rank's chunk i;
+#  * with fallback=layer the capped pass runs only when no shard overflows,
+#    so it drops nothing (the EP layer has no capped-only mode);
+#  * the receiver groups the received rows by its local expert in
+#    (expert, source rank, token) order, runs the expert FFN, and returns for
+#    each received token the weighted sum of its rows' outputs (the combine,
+#    split across ranks); the source adds the returns of all destinations.
+# ---------------------------------------------------------------------------
+@dataclass
+class EPDispatch:
+    """One source rank's send for one pass (dest-major)."""
+    uniq_offsets: np.ndarray  # [N+1]: rows bound for each destination
+    uniq_tokens: np.ndarray   # [U]: local token of each row, ascending per dest
+    send_idx: np.ndarray      # [U, k]: local expert of each pick bound for
+                              #         the row's destination, else -1
+    send_w: np.ndarray        # [U, k]: its combine weight, else 0
+
+
+def ep_dispatch(topk_idx: np.ndarray, topk_w: np.ndarray, E: int,
+                N: int) -> EPDispatch:
+    """The dedup'd send of one rank: for each destination d, the tokens
+    with at least one pick among d's experts, each once, with the local
+    expert index of each of its picks that d owns."""
+    topk_idx = np.asarray(topk_idx)
+    T, k = topk_idx.shape if topk_idx.size else (0, topk_idx.shape[-1])
+    Ed = E // N
+    toks, idx, w, offs = [], [], [], [0]
+    for d in range(N):
+        for t in range(T):
+            picks = [int(e) for e in topk_idx[t]]
+            if any(e // Ed == d for e in picks):
+                toks.append(t)
+                idx.append([e - d * Ed if e // Ed == d else -1
+                            for e in picks])
+                w.append([float(topk_w[t, j]) if picks[j] // Ed == d else 0.0
+                          for j in range(k)])
+        offs.append(len(toks))
+    return EPDispatch(np.array(offs, dtype=INT), np.array(toks, dtype=INT),
+                      np.array(idx, dtype=INT).reshape(-1, k),
+                      np.array(w, dtype=np.float64).reshape(-1, k))
+
+
+def ep_expert_pass(recv_x: np.ndarray, recv_idx: np.ndarray,
+                   recv_w: np.ndarray, local_weights: ExpertWeights):
+    """A receiving rank: every (row, pick) with a local expert goes through
+    that expert's FFN; each received row gets the weighted sum of its
+    picks' outputs."""
+    recv_x = np.asarray(recv_x, dtype=np.float64)
+    n = recv_x.shape[0]
+    out = np.zeros_like(recv_x)
+    by_expert = {}
+    for i in range(n):
+        for j in range(recv_idx.shape[1]):
+            e = int(recv_idx[i, j])
+            if e >= 0:
+                by_expert.setdefault(e, []).append((i, j))
+    for e in sorted(by_expert):
+        rows = by_expert[e]
+        _, y = expert_ffn(recv_x[[i for i, _ in rows]], *local_weights(e))
+        for q, (i, j) in enumerate(rows):
+            out[i] += float(recv_w[i, j]) * y[q]
+    return out
+
+
+def ep_chunk_bounds(T_r: int, n: int, c: int):
+    """Tokens [t0, t1) of rank-local chunk c of n."""
+    size = -(-T_r // n) if n > 0 else 0
+    t0 = min(T_r, c * size)
+    return t0, min(T_r, t0 + size)
+
+
+def ep_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
+             weights: ExpertWeights):
+    """The layer with fallback=layer over N ranks (cfg.T = all ranks'
+    tokens, cfg.S = N).  Returns (per-rank outputs, overflow, passes)."""
+    E, k, H = cfg.E, cfg.k, cfg.H
+    Ed = E // N
+    Ts = [np.asarray(x).shape[0] for x in xs]
+    if sum(Ts) != cfg.T or cfg.S != N:
+        raise ValueError("cfg.T must be the ranks' tokens and cfg.S = N")
+    routes = [route(L, k, cfg.renorm)[:2] for L in logits]
+    shard = np.zeros(N, dtype=INT)
+    for idx, _ in routes:
+        shard += shard_counts(expert_counts(idx, E), N)
+    C = capacity(cfg.T, k, N, cfg.ragged_buffer_factor)
+    over = overflow_flag(shard, C)
+    n = len(chunk_plan(cfg.T, k, E, N, C, cfg.n_chunks)) if over else 1
+    ys = [np.zeros((T_r, H)) for T_r in Ts]
+    xs = [np.asarray(x, dtype=np.float64) for x in xs]
+    for c in range(n):
+        bounds = [ep_chunk_bounds(Ts[r], n, c) for r in range(N)]
+        sends = [ep_dispatch(routes[r][0][t0:t1], routes[r][1][t0:t1], E, N)
+                 for r, (t0, t1) in enumerate(bounds)]
+        for d in range(N):
+            parts = []
+            for q in range(N):
+                a, z = int(sends[q].uniq_offsets[d]), \
+                    int(sends[q].uniq_offsets[d + 1])
+                parts.append((q, sends[q].uniq_tokens[a:z],
+                              sends[q].send_idx[a:z], sends[q].send_w[a:z]))
+            recv_x = np.concatenate(
+                [xs[q][bounds[q][0] + tok] for q, tok, _, _ in parts]
+                + [np.zeros((0, H))])
+            recv_idx = np.concatenate([i for _, _, i, _ in parts]
+                                      + [np.zeros((0, k), dtype=INT)])
+            recv_w = np.concatenate([w for _, _, _, w in parts]
+                                    + [np.zeros((0, k))])
+            back = ep_expert_pass(recv_x, recv_idx, recv_w,
+                                  lambda e, d=d: weights(d * Ed + e))
+            pos = 0
+            for q, tok, _, _ in parts:
+                for u, t in enumerate(tok):
+                    ys[q][bounds[q][0] + int(t)] += back[pos + u]
+                pos += len(tok)
+    return ys, over, n
+
+
+# ---------------------------------------------------------------------------
+# Ring of experts.  [PR4969 What]: tokens are all-gathered around the EP
+# ring, every rank computes its local experts for all tokens, and the
+# combine is reduce-scattered back to the tokens' owners.  No rank has a
+# receive buffer to overflow, so the pass is dropless.  READING: the
+# reduce-scatter sums each rank's weighted partial outputs; rank d owns
+# experts [d*E/N, (d+1)*E/N) as above.
+# ---------------------------------------------------------------------------
+def ring_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
+               weights: ExpertWeights):
+    """Returns the per-rank outputs of the ring-of-experts layer."""
+    E, k, H = cfg.E, cfg.k, cfg.H
+    Ed = E // N
+    Ts = [np.asarray(x).shape[0] for x in xs]
+    x_all = np.concatenate([np.asarray(x, dtype=np.float64) for x in xs]
+                           + [np.zeros((0, H))])
+    routes = [route(L, k, cfg.renorm)[:2] for L in logits]
+    idx_all = np.concatenate([r[0] for r in routes]
+                             + [np.zeros((0, k), dtype=INT)])
+    w_all = np.concatenate([r[1] for r in routes] + [np.zeros((0, k))])
+    total = np.zeros_like(x_all)
+    for d in range(N):
+        local = np.where(idx_all // Ed == d, idx_all - d * Ed, -1)
+        total += ep_expert_pass(x_all, local, np.where(local >= 0, w_all, 0.0),
+                                lambda e, d=d: weights(d * Ed + e))
+    out, t0 = [], 0
+    for T_r in Ts:
+        out.append(total[t0:t0 + T_r])
+        t0 += T_r
+    return out

@@ -747,4 +747,103 @@ def pin_router_logits():
                           ref.router_logits(x, w))
 
 
+def _ep_case(rng, N, Ts, E, k, H=3, F=4, shift=1.5):
+    xs = [rng.standard_normal((T_r, H)) for T_r in Ts]
+    Ls = [rng.standard_normal((T_r, E)) - shift * np.log(np.arange(E) + 1.0)
+          for T_r in Ts]
+    w = (rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F)),
+         rng.standard_normal((E, F, H)))
+    return xs, Ls, w
+
+
+def pin_ep_dispatch_plan():
+    """Each source's send: every pick (t, j) appears once, in the row of
+    token t bound for the rank that owns its expert, with that expert's
+    local index and weight; the rows bound for a rank are the set of tokens
+    with a pick there (brute force), ascending, each once."""
+    rng = _rng(31)
+    for _ in range(40):
+        N = int(rng.choice([1, 2, 4]))
+        E = N * int(rng.integers(1, 4))
+        k = int(rng.integers(1, E + 1))
+        T = int(rng.integers(0, 20))
+        L = rng.standard_normal((T, E))
+        idx, w, _ = ref.route(L, k) if T else (np.zeros((0, k), int),
+                                              np.zeros((0, k)), False)
+        p = ref.ep_dispatch(idx, w, E, N)
+        Ed = E // N
+        seen = set()
+        for d in range(N):
+            a, z = int(p.uniq_offsets[d]), int(p.uniq_offsets[d + 1])
+            toks = [int(t) for t in p.uniq_tokens[a:z]]
+            want = sorted({t for t in range(T)
+                           for e in idx[t] if int(e) // Ed == d})
+            assert toks == want
+            for u, t in enumerate(toks):
+                for j in range(k):
+                    e = int(idx[t, j])
+                    if e // Ed == d:
+                        assert p.send_idx[a + u, j] == e - d * Ed
+                        assert p.send_w[a + u, j] == w[t, j]
+                        seen.add((t, j))
+                    else:
+                        assert p.send_idx[a + u, j] == -1
+                        assert p.send_w[a + u, j] == 0.0
+        assert seen == {(t, j) for t in range(T) for j in range(k)}
+        assert p.uniq_offsets[N] == sum(
+            len({int(e) // Ed for e in idx[t]}) for t in range(T))
+
+
+def pin_ep_layer_equals_single_device():
+    """fallback=layer over N ranks gives the single-device layer on the
+    ranks' batches together ([PR5920 Tests]: outputs match the dropless
+    model), with the same global overflow flag and the same pass count;
+    cases that overflow and cases that do not, ranks with no tokens."""
+    rng = _rng(32)
+    over_seen = set()
+    for _ in range(30):
+        N = int(rng.choice([2, 4]))
+        E = N * int(rng.choice([1, 2, 3]))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        Ts = [int(rng.integers(0, 14)) for _ in range(N)]
+        if sum(Ts) == 0:
+            Ts[0] = 3
+        factor = float(rng.choice([0.5, 1.0, 2.0, 4.0]))
+        xs, Ls, w = _ep_case(rng, N, Ts, E, k)
+        cfg = ref.MoEConfig(sum(Ts), 3, E, k, 4, N, factor)
+        ys, over, n = ref.ep_layer(cfg, N, xs, Ls, ref.dense_weights(*w))
+        single = ref.layer(cfg, np.concatenate(xs), np.concatenate(Ls),
+                           ref.dense_weights(*w))
+        assert over == single.overflow
+        if over:
+            C = ref.capacity(cfg.T, k, N, factor)
+            assert n == len(ref.chunk_plan(cfg.T, k, E, N, C))
+        assert np.allclose(np.concatenate(ys), single.y, rtol=1e-10,
+                           atol=1e-10)
+        over_seen.add(over)
+    assert over_seen == {True, False}
+
+
+def pin_ring_layer_equals_dropless():
+    """The ring of experts (all-gather, local experts, reduce-scatter of the
+    combine) gives the dropless layer on the ranks' batches together."""
+    rng = _rng(33)
+    for _ in range(20):
+        N = int(rng.choice([2, 4]))
+        E = N * int(rng.choice([1, 2]))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        Ts = [int(rng.integers(0, 10)) for _ in range(N)]
+        xs, Ls, w = _ep_case(rng, N, Ts, E, k)
+        cfg = ref.MoEConfig(sum(Ts), 3, E, k, 4, N, 2.0)
+        ys = ref.ring_layer(cfg, N, xs, Ls, ref.dense_weights(*w))
+        for r in range(N):
+            assert ys[r].shape == (Ts[r], 3)
+        if sum(Ts):
+            drop = ref.layer_dropless(cfg, np.concatenate(xs),
+                                      np.concatenate(Ls),
+                                      ref.dense_weights(*w))
+            assert np.allclose(np.concatenate(ys), drop.y, rtol=1e-10,
+                               atol=1e-10)
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

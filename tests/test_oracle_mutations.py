@@ -18,6 +18,17 @@ ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(
     os.path.abspath(__file__))), "oracle", "moe_ref.py")
 
 MUTANTS = {
+    "ep_dest_by_modulo": (
+        "            if any(e // Ed == d for e in picks):",
+        "            if any(e % N == d for e in picks):"),
+    "ep_return_unweighted": (
+        "            out[i] += float(recv_w[i, j]) * y[q]",
+        "            out[i] += y[q]"),
+    "ep_flag_from_rank0_only": (
+        "    for idx, _ in routes:\n        shard += shard_counts(",
+        "    for idx, _ in routes[:1]:\n        shard += shard_counts("),
+    "ring_partials_not_summed": (
+        "        total += ep_expert_pass(", "        total = ep_expert_pass("),
     "router_offset_dropped": (
         "        out = out + np.asarray(offset, dtype=np.float64)",
         "        out = out + 0.0"),
