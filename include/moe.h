@@ -372,6 +372,9 @@ moe_status_t moe_permute_tables(const moe_config_t *cfg,
                                 int32_t *uniq_offsets, int32_t *n_dropped,
                                 void *workspace, size_t workspace_bytes,
                                 moe_stream_t stream);
+/* (moe_permute_scatter with x_sorted = NULL writes the index outputs --
+ * uniq_tokens, expand_idx, the rest of uniq_offsets -- and copies no row;
+ * x is then not read and may be NULL.) */
 moe_status_t moe_permute_scatter(const moe_config_t *cfg, const void *x,
                                  const int32_t *row_of,
                                  int32_t *uniq_offsets, void *x_sorted,
@@ -648,6 +651,80 @@ moe_status_t moe_layer_backward(const moe_config_t *cfg, const void *x,
                                 moe_mode_t mode, moe_layer_info_t *info,
                                 int32_t *status_word, void *workspace,
                                 size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * Expert parallelism across ranks: the rank-local steps around the two
+ * exchanges of the ragged all-to-all path ("Support
+ * moe_dropless_fallback=layer on the ragged all-to-all MoE path", MaxText
+ * pull request 5920, sections Why, How, Tests; "Moe dynamic redundancy",
+ * pull request 4760, review of ra2a_dedup_and_route: each token is sent to
+ * a destination once and expanded there; "MoE ring-of-experts ...", pull
+ * request 4969, section What: the ring variant).  The exchanges themselves
+ * are the caller's (NCCL, torch.distributed, or copies between logical
+ * ranks of one GPU).  Ranks are the shards: with cfg->S = ranks, rank d
+ * owns experts [d*E/S, (d+1)*E/S).  A pass on a source rank:
+ *   moe_permute_tables + moe_permute_scatter (x_sorted NULL), cfg->S =
+ *   ranks: the dest-major dedup sets uniq_offsets [S+1], uniq_tokens;
+ *   moe_ep_dispatch_pack: the send rows and their slots;
+ *   exchange 1 (rows uniq_offsets[d+1]-uniq_offsets[d] to rank d);
+ * on the receiving rank, with cfg->E = E/S (its experts), cfg->k =
+ * min(k, E/S) and T = rows received:
+ *   moe_permute (uncapped) on recv_idx, moe_gmm_*, moe_combine with
+ *   recv_w: one partial output row per received row;
+ *   exchange 2 (the partial rows back to their sources);
+ * and on the source: moe_ep_return_map + moe_permute_backward (cfg->k = S
+ * ranks) add the returned rows into y.
+ *
+ * moe_ep_check -- the global overflow check from shard_counts [S] (device),
+ * each shard's receive count summed over the source ranks (an all-reduce of
+ * moe_check_overflow's shard_counts); cfg->T = the tokens of all ranks, so
+ * C is the single-device capacity of the ranks' batches together.  Outputs
+ * as moe_check_overflow. */
+moe_status_t moe_ep_check(const moe_config_t *cfg, const int32_t *shard_counts,
+                          int32_t *overflow_flag, float *required_factor,
+                          int32_t *capacity, moe_stream_t stream);
+
+/* moe_ep_dispatch_pack -- a source rank's send (cfg->T = its tokens of the
+ * pass, cfg->S = ranks).  For every dedup row i < uniq_offsets[S] (row i of
+ * destination d, token t = uniq_tokens[i]):
+ *   x_send   out [T*min(k,S), H] dtype: row i = x[t]
+ *   send_idx out [T*min(k,S), kk] int32, kk = min(k, E/S): the picks of t
+ *            that rank d owns, in pick order, as topk_idx[t,j] - d*E/S,
+ *            then -1 in the remaining slots
+ *   send_w   out [T*min(k,S), kk] float32: their combine weights, then 0
+ * Rows past uniq_offsets[S] are not written.  The receiver runs its pass
+ * with cfg->k = kk and cfg->E = E/S. */
+moe_status_t moe_ep_dispatch_pack(const moe_config_t *cfg, const void *x,
+                                  const int32_t *topk_idx,
+                                  const float *topk_w,
+                                  const int32_t *uniq_offsets,
+                                  const int32_t *uniq_tokens, void *x_send,
+                                  int32_t *send_idx, float *send_w,
+                                  moe_stream_t stream);
+
+/* moe_ep_return_map -- row_of_ret [T, S] int32: the send row of token t
+ * bound for rank d, or -1; with it moe_permute_backward (cfg->k = S, unit
+ * weights) adds the rows the destinations return into y [T, H]. */
+moe_status_t moe_ep_return_map(const moe_config_t *cfg,
+                               const int32_t *uniq_offsets,
+                               const int32_t *uniq_tokens,
+                               int32_t *row_of_ret, moe_stream_t stream);
+
+/* moe_ep_localize -- the ring variant: local_idx [T, kk] (kk = min(k,
+ * n_local)) = the picks of token t in [first_expert, first_expert +
+ * n_local), in pick order, as topk_idx - first_expert, then -1; local_w
+ * [T, kk] their weights, then 0. */
+moe_status_t moe_ep_localize(const moe_config_t *cfg, const int32_t *topk_idx,
+                             const float *topk_w, int32_t first_expert,
+                             int32_t n_local, int32_t *local_idx,
+                             float *local_w, moe_stream_t stream);
+
+/* moe_ep_sum_partials -- the ring variant's reduce: y [T, H] = sum over
+ * q < n_parts of parts[q] ([n_parts, T, H], layer dtype), accumulated in
+ * float32 in part order and rounded once. */
+moe_status_t moe_ep_sum_partials(const moe_config_t *cfg, int32_t n_parts,
+                                 const void *parts, void *y,
+                                 moe_stream_t stream);
 
 /* ----------------------------------------------------------------------
  * Host-side queries (no GPU work).

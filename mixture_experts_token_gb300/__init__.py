@@ -85,6 +85,11 @@ def _declare(h):
     cfg = ctypes.POINTER(MoeConfig)
     sig = {
         "moe_router_logits": [cfg, P, P, P, P, P, P],
+        "moe_ep_check": [cfg, P, P, P, P, P],
+        "moe_ep_dispatch_pack": [cfg, P, P, P, P, P, P, P, P, P],
+        "moe_ep_return_map": [cfg, P, P, P, P],
+        "moe_ep_localize": [cfg, P, P, c_int32, c_int32, P, P, P],
+        "moe_ep_sum_partials": [cfg, c_int32, P, P, P],
         "moe_route": [cfg, P, P, P, P, P],
         "moe_check_overflow": [cfg, P, P, P, P, P, P, P, P],
         "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
@@ -252,6 +257,43 @@ def moe_router_logits(cfg, x, w_router, logit_offset, logits,
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_offset),
         _ptr(logits), _ptr(status_word), _stream(stream)),
         "moe_router_logits")
+
+
+def moe_ep_check(cfg, shard_counts, overflow_flag, required_factor,
+                 capacity, stream=None):
+    _check(lib().moe_ep_check(ctypes.byref(cfg), _ptr(shard_counts),
+                              _ptr(overflow_flag), _ptr(required_factor),
+                              _ptr(capacity), _stream(stream)),
+           "moe_ep_check")
+
+
+def moe_ep_dispatch_pack(cfg, x, topk_idx, topk_w, uniq_offsets, uniq_tokens,
+                         x_send, send_idx, send_w, stream=None):
+    _check(lib().moe_ep_dispatch_pack(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(uniq_offsets), _ptr(uniq_tokens), _ptr(x_send), _ptr(send_idx),
+        _ptr(send_w), _stream(stream)), "moe_ep_dispatch_pack")
+
+
+def moe_ep_return_map(cfg, uniq_offsets, uniq_tokens, row_of_ret,
+                      stream=None):
+    _check(lib().moe_ep_return_map(ctypes.byref(cfg), _ptr(uniq_offsets),
+                                   _ptr(uniq_tokens), _ptr(row_of_ret),
+                                   _stream(stream)), "moe_ep_return_map")
+
+
+def moe_ep_localize(cfg, topk_idx, topk_w, first_expert, n_local, local_idx,
+                    local_w, stream=None):
+    _check(lib().moe_ep_localize(ctypes.byref(cfg), _ptr(topk_idx),
+                                 _ptr(topk_w), first_expert, n_local,
+                                 _ptr(local_idx), _ptr(local_w),
+                                 _stream(stream)), "moe_ep_localize")
+
+
+def moe_ep_sum_partials(cfg, n_parts, parts, y, stream=None):
+    _check(lib().moe_ep_sum_partials(ctypes.byref(cfg), n_parts, _ptr(parts),
+                                     _ptr(y), _stream(stream)),
+           "moe_ep_sum_partials")
 
 
 def moe_route(cfg, logits, topk_idx, topk_w, status_word=None, stream=None):

@@ -663,9 +663,11 @@ moe_status_t moe_permute_scatter(const moe_config_t* cfg, const void* x,
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   if (!ok_ptr(uniq_offsets, false)) return MOE_ERR_INVALID_ARG;
-  if (cfg->T > 0 && (!ok_ptr(x, true) || !ok_ptr(row_of, false) ||
-                     !ok_ptr(x_sorted, true) || !ok_ptr(uniq_tokens, false) ||
-                     !ok_ptr(expand_idx, false)))
+  // x_sorted == NULL: the index outputs only (x is then not read)
+  if (cfg->T > 0 &&
+      ((x_sorted != nullptr && (!ok_ptr(x, true) || !ok_ptr(x_sorted, true))) ||
+       !ok_ptr(row_of, false) || !ok_ptr(uniq_tokens, false) ||
+       !ok_ptr(expand_idx, false)))
     return MOE_ERR_INVALID_ARG;
   const size_t need = permute_scratch_bytes(cfg->T, cfg->E, cfg->k, cfg->S);
   if (workspace == nullptr || workspace_bytes < need ||

@@ -384,12 +384,14 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
   const int t = blockIdx.x, tid = threadIdx.x;
   const int bt = t / TB;
   const long long tk = static_cast<long long>(t) * k;
-  const int4* src = x + static_cast<long long>(t) * n16;
+  // x_sorted == null: the index outputs only (no row is read or written)
+  const int n16r = x_sorted != nullptr ? n16 : 0;
+  const int4* src = x + static_cast<long long>(t) * n16r;
   int4 v[kScatterUnroll];
 #pragma unroll
   for (int u = 0; u < kScatterUnroll; ++u) {
     const int c = tid + u * kScatterThreads;
-    if (c < n16) v[u] = __ldg(src + c);
+    if (c < n16r) v[u] = __ldg(src + c);
   }
   for (int q = tid; q < S; q += kScatterThreads) {
     tot[q] = 0;
@@ -442,12 +444,12 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     uniq_offsets[tid] = o;
   }
   __syncthreads();
-  for (int c0 = tid; c0 < n16; c0 += kScatterThreads * kScatterUnroll) {
+  for (int c0 = tid; c0 < n16r; c0 += kScatterThreads * kScatterUnroll) {
     if (c0 != tid) {
 #pragma unroll
       for (int u = 0; u < kScatterUnroll; ++u) {
         const int c = c0 + u * kScatterThreads;
-        if (c < n16) v[u] = __ldg(src + c);
+        if (c < n16r) v[u] = __ldg(src + c);
       }
     }
     for (int j = 0; j < k; ++j) {
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 #pragma unroll
       for (int u = 0; u < kScatterUnroll; ++u) {
         const int c = c0 + u * kScatterThreads;
-        if (c < n16) dst[c] = v[u];
+        if (c < n16r) dst[c] = v[u];
       }
     }
   }

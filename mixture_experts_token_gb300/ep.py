@@ -1,0 +1,326 @@
+"""Expert parallelism across ranks: the layer's passes with the two
+exchanges of the ragged all-to-all path, and the ring-of-experts variant.
+
+"Support moe_dropless_fallback=layer on the ragged all-to-all MoE path"
+(MaxText pull request 5920), sections Why, How and Tests: every rank sends
+its tokens' rows to the ranks that own their experts; the overflow check is
+global, so every rank takes the same branch (the capped pass, or the
+chunked dropless fallback).  "Moe dynamic redundancy" (pull request 4760),
+review of ra2a_dedup_and_route: a token is sent to a destination once and
+expanded there.  "MoE ring-of-experts ..." (pull request 4969), section
+What: all-gather the tokens, compute the local experts, reduce-scatter the
+combine.
+
+Every step on the data runs in the library's kernels (include/moe.h); this
+module sequences them and moves buffers between ranks through a transport:
+
+* ``DistTransport``: one rank of a torch.distributed process group (NCCL on
+  GPUs, gloo on CPU): an all-reduce of the shard counts and all-to-all-v
+  exchanges of rows.
+* ``LoopbackTransport``: N logical ranks held by one process on one device;
+  an exchange hands each receiver the senders' buffers (device copies).  No
+  kernel of one rank waits on another's: the ranks run phase by phase.
+
+Ranks are the shards (cfg.S = ranks): rank d owns experts [d*E/S,
+(d+1)*E/S) and holds their weights.  ``EPLayer`` follows the pages'
+fallback=layer; since the capped pass runs only when no shard overflows, no
+pass drops a row, and the result equals the single-device layer on the
+ranks' batches together.  ``RingLayer`` is dropless.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (alloc_step_buffers, make_config, moe_check_overflow,
+               moe_combine, moe_ep_check, moe_ep_dispatch_pack,
+               moe_ep_localize, moe_ep_return_map, moe_ep_sum_partials,
+               moe_gmm_down, moe_gmm_gate_up, moe_num_chunks, moe_permute,
+               moe_permute_backward, moe_permute_scatter, moe_permute_tables,
+               moe_route, moe_workspace_bytes, MOE_WS_PERMUTE)
+
+
+# ------------------------------------------------------------ transports --
+class LoopbackTransport:
+    """All ranks in this process: the lists below hold one entry per rank,
+    in rank order."""
+
+    def __init__(self, n_ranks: int):
+        self.n = n_ranks
+        self.ranks = list(range(n_ranks))
+
+    def all_reduce_sum(self, tensors):
+        total = tensors[0].clone()
+        for t in tensors[1:]:
+            total += t
+        return [total.clone() for _ in tensors]
+
+    def all_to_all(self, sends):
+        """sends[r][d]: rank r's rows for rank d -> recv[d][r]."""
+        return [[sends[r][d] for r in range(self.n)] for d in range(self.n)]
+
+
+class DistTransport:
+    """This process is one rank of the default torch.distributed group."""
+
+    def __init__(self, group=None):
+        import torch.distributed as dist
+        self.dist = dist
+        self.group = group
+        self.n = dist.get_world_size(group)
+        self.ranks = [dist.get_rank(group)]
+
+    def all_reduce_sum(self, tensors):
+        (t,) = tensors
+        out = t.clone()
+        self.dist.all_reduce(out, group=self.group)
+        return [out]
+
+    def all_to_all(self, sends):
+        """all-to-all-v of row blocks: first the row counts, then the rows
+        (one all_to_all_single over the concatenated blocks)."""
+        (blocks,) = sends
+        dev = blocks[0].device
+        rows = torch.tensor([b.shape[0] for b in blocks], dtype=torch.int64,
+                            device=dev)
+        got = torch.empty_like(rows)
+        self.dist.all_to_all_single(got, rows, group=self.group)
+        in_splits = rows.tolist()
+        out_splits = got.tolist()
+        tail = tuple(blocks[0].shape[1:])
+        send = torch.cat([b.contiguous() for b in blocks])
+        recv = torch.empty((sum(out_splits),) + tail, dtype=send.dtype,
+                           device=dev)
+        self.dist.all_to_all_single(recv, send, out_splits, in_splits,
+                                    group=self.group)
+        return [list(torch.split(recv, out_splits))]
+
+
+# ------------------------------------------------------------- helpers ----
+def _cfg(base, **kw):
+    return base.with_(**kw)
+
+
+def chunk_bounds(T_r: int, n: int, c: int):
+    """Tokens [t0, t1) of rank-local chunk c of n (chunks of ceil(T_r/n))."""
+    size = -(-T_r // n) if n > 0 else 0
+    t0 = min(T_r, c * size)
+    return t0, min(T_r, t0 + size)
+
+
+class _Rank:
+    """One rank's inputs, routing and output."""
+
+    def __init__(self, rank, x, logits, cfg, dev):
+        self.rank = rank
+        self.x = x
+        self.T = x.shape[0]
+        self.cfg = _cfg(cfg, T=self.T)
+        k, E, S = cfg.k, cfg.E, cfg.S
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.idx = torch.empty((self.T, k), **i32)
+        self.w = torch.empty((self.T, k), dtype=torch.float32, device=dev)
+        if self.T:
+            moe_route(self.cfg, logits, self.idx, self.w)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.shard = torch.zeros(S, **i32)
+        self.flag = torch.zeros(1, **i32)
+        self.req = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.cap = torch.zeros(1, **i32)
+        self.y = torch.zeros((self.T, cfg.H), dtype=x.dtype, device=dev)
+
+
+class EPLayer:
+    """The layer with moe_dropless_fallback=layer over expert-parallel ranks.
+
+    cfg: the layer's configuration with T = the tokens of all ranks together
+    and S = the number of ranks.  weights(rank) -> (w_gate, w_up, w_down) of
+    the rank's E/S experts ([E/S, H, F], [E/S, H, F], [E/S, F, H])."""
+
+    def __init__(self, cfg, transport, weights):
+        if cfg.E % cfg.S:
+            raise ValueError("E must be a multiple of the ranks")
+        if transport.n != cfg.S:
+            raise ValueError("cfg.S must equal the number of ranks")
+        self.cfg = cfg
+        self.tr = transport
+        self.weights = weights
+        self.info = {}
+
+    def forward(self, xs, logits):
+        """xs[i], logits[i]: the inputs of the transport's i-th local rank;
+        returns their outputs."""
+        cfg, tr = self.cfg, self.tr
+        dev = xs[0].device
+        ranks = [_Rank(r, x, L, cfg, dev)
+                 for r, x, L in zip(tr.ranks, xs, logits)]
+        for rk in ranks:
+            if rk.T:
+                moe_check_overflow(rk.cfg, rk.idx, rk.counts, rk.offsets,
+                                   rk.shard, rk.flag, rk.req, rk.cap)
+        sums = tr.all_reduce_sum([rk.shard for rk in ranks])
+        for rk, s in zip(ranks, sums):
+            moe_ep_check(cfg, s, rk.flag, rk.req, rk.cap)
+        over = int(ranks[0].flag.item())
+        n = moe_num_chunks(cfg) if over else 1
+        for c in range(n):
+            self._pass(ranks, c, n)
+        self.info = {"overflow": over, "n_chunks": n,
+                     "required_factor": float(ranks[0].req.item())}
+        return [rk.y for rk in ranks]
+
+    def _pass(self, ranks, c, n):
+        cfg, tr = self.cfg, self.tr
+        E, S, k, H = cfg.E, cfg.S, cfg.k, cfg.H
+        El = E // S
+        kk = min(k, El)
+        dev = ranks[0].x.device
+        # source side: dedup sets per destination, then the send rows
+        sends_x, sends_i, sends_w, state = [], [], [], []
+        for rk in ranks:
+            t0, t1 = chunk_bounds(rk.T, n, c)
+            Tc = t1 - t0
+            sc = _cfg(cfg, T=Tc, ragged_buffer_factor=-1.0, n_chunks=0,
+                      redundant_slots=0)
+            b = alloc_step_buffers(sc, dev)
+            rows = Tc * min(k, S)
+            x_send = torch.empty((rows, H), dtype=rk.x.dtype, device=dev)
+            s_idx = torch.empty((rows, kk), dtype=torch.int32, device=dev)
+            s_w = torch.empty((rows, kk), dtype=torch.float32, device=dev)
+            if Tc:
+                moe_permute_tables(sc, rk.idx[t0:t1], False, b["row_of"],
+                                   b["sorted_token"], b["group_offsets"],
+                                   b["uniq_offsets"], b["n_dropped"],
+                                   b["permute_ws"])
+                moe_permute_scatter(sc, None, b["row_of"], b["uniq_offsets"],
+                                    None, b["uniq_tokens"], b["expand_idx"],
+                                    b["permute_ws"])
+                moe_ep_dispatch_pack(sc, rk.x[t0:t1], rk.idx[t0:t1],
+                                     rk.w[t0:t1], b["uniq_offsets"],
+                                     b["uniq_tokens"], x_send, s_idx, s_w)
+                uo = b["uniq_offsets"].cpu().tolist()
+            else:
+                uo = [0] * (S + 1)
+            sends_x.append([x_send[uo[d]:uo[d + 1]] for d in range(S)])
+            sends_i.append([s_idx[uo[d]:uo[d + 1]] for d in range(S)])
+            sends_w.append([s_w[uo[d]:uo[d + 1]] for d in range(S)])
+            state.append((t0, t1, sc, b))
+        recv_x = tr.all_to_all(sends_x)
+        recv_i = tr.all_to_all(sends_i)
+        recv_w = tr.all_to_all(sends_w)
+        # receiving side: the local experts over the received rows
+        backs = []
+        for j, rk in enumerate(ranks):
+            sizes = [blk.shape[0] for blk in recv_x[j]]
+            n_recv = sum(sizes)
+            rc = _cfg(cfg, T=n_recv, E=El, k=kk, S=1,
+                      ragged_buffer_factor=-1.0, n_chunks=0,
+                      redundant_slots=0)
+            part = torch.empty((n_recv, H), dtype=rk.x.dtype, device=dev)
+            if n_recv:
+                rx = torch.cat(recv_x[j])
+                ri = torch.cat(recv_i[j])
+                rw = torch.cat(recv_w[j])
+                rb = alloc_step_buffers(rc, dev)
+                moe_permute(rc, rx, ri, False, rb["x_sorted"], rb["row_of"],
+                            rb["sorted_token"], rb["group_offsets"],
+                            rb["uniq_offsets"], rb["uniq_tokens"],
+                            rb["expand_idx"], rb["n_dropped"],
+                            rb["permute_ws"])
+                wg, wu, wd = self.weights(rk.rank)
+                moe_gmm_gate_up(rc, rb["x_sorted"], rb["group_offsets"], wg,
+                                wu, rb["h"], rb["status"])
+                moe_gmm_down(rc, rb["h"], rb["group_offsets"], wd,
+                             rb["y_sorted"], rb["status"])
+                moe_combine(rc, rb["y_sorted"], rb["row_of"], rw, part)
+            backs.append(list(torch.split(part, sizes)))
+        ret = tr.all_to_all(backs)
+        # source side: add the rows the destinations returned
+        for rk, blocks, (t0, t1, sc, b) in zip(ranks, ret, state):
+            if t1 == t0:
+                continue
+            rows = torch.cat(blocks)
+            row_of_ret = torch.empty((t1 - t0, S), dtype=torch.int32,
+                                     device=dev)
+            moe_ep_return_map(sc, b["uniq_offsets"], b["uniq_tokens"],
+                              row_of_ret)
+            moe_permute_backward(_cfg(sc, k=S), rows, row_of_ret,
+                                 rk.y[t0:t1])
+
+
+class RingLayer:
+    """The ring-of-experts variant (dropless): every rank sees all tokens,
+    computes its own experts' weighted outputs, and each token's owner adds
+    the ranks' partial outputs."""
+
+    def __init__(self, cfg, transport, weights):
+        if cfg.E % cfg.S or transport.n != cfg.S:
+            raise ValueError("cfg.S must equal the ranks and divide E")
+        self.cfg = cfg
+        self.tr = transport
+        self.weights = weights
+
+    def forward(self, xs, logits):
+        cfg, tr = self.cfg, self.tr
+        E, S, k, H = cfg.E, cfg.S, cfg.k, cfg.H
+        El = E // S
+        kk = min(k, El)
+        dev = xs[0].device
+        ranks = [_Rank(r, x, L, cfg, dev)
+                 for r, x, L in zip(tr.ranks, xs, logits)]
+        # all-gather of the tokens and their routing
+        gx = tr.all_to_all([[rk.x] * S for rk in ranks])
+        gi = tr.all_to_all([[rk.idx] * S for rk in ranks])
+        gw = tr.all_to_all([[rk.w] * S for rk in ranks])
+        backs = []
+        for j, rk in enumerate(ranks):
+            sizes = [blk.shape[0] for blk in gx[j]]
+            T_all = sum(sizes)
+            part = torch.empty((T_all, H), dtype=rk.x.dtype, device=dev)
+            if T_all:
+                xa, ia, wa = torch.cat(gx[j]), torch.cat(gi[j]), \
+                    torch.cat(gw[j])
+                ac = _cfg(cfg, T=T_all)
+                li = torch.empty((T_all, kk), dtype=torch.int32, device=dev)
+                lw = torch.empty((T_all, kk), dtype=torch.float32, device=dev)
+                moe_ep_localize(ac, ia, wa, rk.rank * El, El, li, lw)
+                rc = _cfg(cfg, T=T_all, E=El, k=kk, S=1,
+                          ragged_buffer_factor=-1.0, n_chunks=0,
+                          redundant_slots=0)
+                rb = alloc_step_buffers(rc, dev)
+                moe_permute(rc, xa, li, False, rb["x_sorted"], rb["row_of"],
+                            rb["sorted_token"], rb["group_offsets"],
+                            rb["uniq_offsets"], rb["uniq_tokens"],
+                            rb["expand_idx"], rb["n_dropped"],
+                            rb["permute_ws"])
+                wg, wu, wd = self.weights(rk.rank)
+                moe_gmm_gate_up(rc, rb["x_sorted"], rb["group_offsets"], wg,
+                                wu, rb["h"], rb["status"])
+                moe_gmm_down(rc, rb["h"], rb["group_offsets"], wd,
+                             rb["y_sorted"], rb["status"])
+                moe_combine(rc, rb["y_sorted"], rb["row_of"], lw, part)
+            backs.append(list(torch.split(part, sizes)))
+        # reduce-scatter: each owner receives the ranks' partial rows of its
+        # tokens and adds them in rank order
+        ret = tr.all_to_all(backs)
+        for rk, blocks in zip(ranks, ret):
+            if rk.T:
+                moe_ep_sum_partials(rk.cfg, S, torch.cat(blocks), rk.y)
+        return [rk.y for rk in ranks]
+
+
+def local_weights(w_gate, w_up, w_down, n_ranks):
+    """weights(rank) over global [E, ...] weight tensors: the rank's
+    contiguous slice of E/n_ranks experts (views, nothing copied)."""
+    E = w_gate.shape[0]
+    El = E // n_ranks
+
+    def get(rank):
+        a, z = rank * El, (rank + 1) * El
+        return w_gate[a:z], w_up[a:z], w_down[a:z]
+    return get
+
+
+__all__ = ["LoopbackTransport", "DistTransport", "EPLayer", "RingLayer",
+           "local_weights", "chunk_bounds", "make_config",
+           "moe_workspace_bytes", "MOE_WS_PERMUTE"]

@@ -921,33 +921,37 @@ class EPDispatch:
     """One source rank's send for one pass (dest-major)."""
     uniq_offsets: np.ndarray  # [N+1]: rows bound for each destination
     uniq_tokens: np.ndarray   # [U]: local token of each row, ascending per dest
-    send_idx: np.ndarray      # [U, k]: local expert of each pick bound for
-                              #         the row's destination, else -1
-    send_w: np.ndarray        # [U, k]: its combine weight, else 0
+    send_idx: np.ndarray      # [U, kk]: local experts of the row's picks
+                              #          its destination owns, in pick
+                              #          order, then -1; kk = min(k, E/N)
+    send_w: np.ndarray        # [U, kk]: their combine weights, then 0
 
 
 def ep_dispatch(topk_idx: np.ndarray, topk_w: np.ndarray, E: int,
                 N: int) -> EPDispatch:
     """The dedup'd send of one rank: for each destination d, the tokens
     with at least one pick among d's experts, each once, with the local
-    expert index of each of its picks that d owns."""
+    expert index and weight of each of its picks that d owns (a token has
+    at most min(k, E/N) of them)."""
     topk_idx = np.asarray(topk_idx)
     T, k = topk_idx.shape if topk_idx.size else (0, topk_idx.shape[-1])
     Ed = E // N
+    kk = min(k, Ed)
     toks, idx, w, offs = [], [], [], [0]
     for d in range(N):
         for t in range(T):
             picks = [int(e) for e in topk_idx[t]]
             if any(e // Ed == d for e in picks):
                 toks.append(t)
-                idx.append([e - d * Ed if e // Ed == d else -1
-                            for e in picks])
-                w.append([float(topk_w[t, j]) if picks[j] // Ed == d else 0.0
-                          for j in range(k)])
+                own = [j for j in range(k) if picks[j] // Ed == d]
+                idx.append([picks[j] - d * Ed for j in own]
+                           + [-1] * (kk - len(own)))
+                w.append([float(topk_w[t, j]) for j in own]
+                         + [0.0] * (kk - len(own)))
         offs.append(len(toks))
     return EPDispatch(np.array(offs, dtype=INT), np.array(toks, dtype=INT),
-                      np.array(idx, dtype=INT).reshape(-1, k),
-                      np.array(w, dtype=np.float64).reshape(-1, k))
+                      np.array(idx, dtype=INT).reshape(-1, kk),
+                      np.array(w, dtype=np.float64).reshape(-1, kk))
 
 
 def ep_expert_pass(recv_x: np.ndarray, recv_idx: np.ndarray,
@@ -1011,10 +1015,11 @@ def ep_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
             recv_x = np.concatenate(
                 [xs[q][bounds[q][0] + tok] for q, tok, _, _ in parts]
                 + [np.zeros((0, H))])
+            kk = min(k, Ed)
             recv_idx = np.concatenate([i for _, _, i, _ in parts]
-                                      + [np.zeros((0, k), dtype=INT)])
+                                      + [np.zeros((0, kk), dtype=INT)])
             recv_w = np.concatenate([w for _, _, _, w in parts]
-                                    + [np.zeros((0, k))])
+                                    + [np.zeros((0, kk))])
             back = ep_expert_pass(recv_x, recv_idx, recv_w,
                                   lambda e, d=d: weights(d * Ed + e))
             pos = 0

@@ -772,6 +772,8 @@ def pin_ep_dispatch_plan():
                                               np.zeros((0, k)), False)
         p = ref.ep_dispatch(idx, w, E, N)
         Ed = E // N
+        kk = min(k, Ed)
+        assert p.send_idx.shape == (int(p.uniq_offsets[N]), kk)
         seen = set()
         for d in range(N):
             a, z = int(p.uniq_offsets[d]), int(p.uniq_offsets[d + 1])
@@ -780,15 +782,16 @@ def pin_ep_dispatch_plan():
                            for e in idx[t] if int(e) // Ed == d})
             assert toks == want
             for u, t in enumerate(toks):
-                for j in range(k):
+                q = 0
+                for j in range(k):      # the owned picks, in pick order
                     e = int(idx[t, j])
                     if e // Ed == d:
-                        assert p.send_idx[a + u, j] == e - d * Ed
-                        assert p.send_w[a + u, j] == w[t, j]
+                        assert p.send_idx[a + u, q] == e - d * Ed
+                        assert p.send_w[a + u, q] == w[t, j]
                         seen.add((t, j))
-                    else:
-                        assert p.send_idx[a + u, j] == -1
-                        assert p.send_w[a + u, j] == 0.0
+                        q += 1
+                assert np.all(p.send_idx[a + u, q:] == -1)
+                assert np.all(p.send_w[a + u, q:] == 0.0)
         assert seen == {(t, j) for t in range(T) for j in range(k)}
         assert p.uniq_offsets[N] == sum(
             len({int(e) // Ed for e in idx[t]}) for t in range(T))

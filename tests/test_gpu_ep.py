@@ -1,0 +1,206 @@
+"""GPU parity of expert parallelism across ranks, with the ranks as logical
+ranks of one GPU (LoopbackTransport: the exchanges are device copies, no
+kernel waits on another rank's).
+
+* The dispatch of every source rank -- the dedup sets per destination
+  (uniq_offsets, uniq_tokens), the send rows and their expert slots -- must
+  equal the oracle's ep_dispatch bit for bit (weights within 1e-4), and
+  every send row must be a byte copy of its token's row.
+* The EP layer (fallback=layer) must match the oracle's ep_layer per rank
+  within the layer tolerance, with the same global flag and pass count, in
+  both branches; the ring of experts must match ring_layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_token_gb300 as moe
+from mixture_experts_token_gb300 import ep
+from oracle import moe_ref as ref
+from synth import WORKLOADS, make_weights, make_x
+from tests.gpu_util import TOL, f64, host_logits, np_
+from tests.parity_log import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def rank_inputs(wl, Ts, seed=0):
+    xs, Ls = [], []
+    for r, T_r in enumerate(Ts):
+        w = wl.with_(T=T_r, seed=seed + 101 * r)
+        x = make_x(w, "cuda")
+        xs.append(x)
+        Ls.append(host_logits(w, x) if T_r else
+                  np.zeros((0, wl.E), dtype=np.float32))
+    return xs, Ls
+
+
+def gcfg(wl, Ts, N, factor):
+    return moe.make_config(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                           wl.dtype, wl.renorm)
+
+
+CASES = [
+    # (workload, ranks, tokens per rank, factor)
+    (WORKLOADS["small"].with_(name="n4", H=256, F=256, E=16, k=4, S=4), 4,
+     [300, 0, 517, 128], 2.0),
+    (WORKLOADS["small"].with_(name="n4_ovf", H=256, F=256, E=16, k=4, S=4,
+                              zipf_s=1.5), 4, [400, 250, 333, 90], 1.0),
+    (WORKLOADS["small"].with_(name="n2_k1", H=384, F=128, E=8, k=1, S=2),
+     2, [700, 1], 2.0),
+    (WORKLOADS["tiny"].with_(name="tiny_n2", S=2), 2, [128, 128], 2.0),
+    (WORKLOADS["small"].with_(name="n8_e256", H=512, F=256, E=256, k=8,
+                              S=8, zipf_s=1.2), 8,
+     [256, 200, 300, 100, 64, 256, 1, 180], 2.0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
+def test_ep_dispatch_matches_oracle(case):
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    kk = min(wl.k, wl.E // N)
+    for r in range(N):
+        T_r = Ts[r]
+        if T_r == 0:
+            continue
+        sc = cfg.with_(T=T_r, ragged_buffer_factor=-1.0)
+        b = moe.alloc_step_buffers(sc)
+        moe.moe_route(sc, torch.from_numpy(Ls[r]).cuda(), b["topk_idx"],
+                      b["topk_w"])
+        moe.moe_permute_tables(sc, b["topk_idx"], False, b["row_of"],
+                               b["sorted_token"], b["group_offsets"],
+                               b["uniq_offsets"], b["n_dropped"],
+                               b["permute_ws"])
+        moe.moe_permute_scatter(sc, None, b["row_of"], b["uniq_offsets"],
+                                None, b["uniq_tokens"], b["expand_idx"],
+                                b["permute_ws"])
+        rows = T_r * min(wl.k, N)
+        xsend = torch.zeros((rows, wl.H), dtype=xs[r].dtype, device="cuda")
+        sidx = torch.full((rows, kk), -7, dtype=torch.int32, device="cuda")
+        sw = torch.full((rows, kk), -7.0, dtype=torch.float32, device="cuda")
+        moe.moe_ep_dispatch_pack(sc, xs[r], b["topk_idx"], b["topk_w"],
+                                 b["uniq_offsets"], b["uniq_tokens"], xsend,
+                                 sidx, sw)
+        torch.cuda.synchronize()
+        oi, ow, _ = ref.route(Ls[r], wl.k)
+        assert np.array_equal(np_(b["topk_idx"]), oi)
+        p = ref.ep_dispatch(oi, ow, wl.E, N)
+        U = int(p.uniq_offsets[N])
+        assert np.array_equal(np_(b["uniq_offsets"]), p.uniq_offsets)
+        assert np.array_equal(np_(b["uniq_tokens"])[:U], p.uniq_tokens)
+        assert np.array_equal(np_(sidx)[:U], p.send_idx)
+        assert_close(np_(sw)[:U], p.send_w, 1e-4, f"send_w rank {r}")
+        tok = torch.from_numpy(p.uniq_tokens.astype(np.int64)).cuda()
+        assert torch.equal(xsend[:U], xs[r][tok])
+        assert torch.all(sidx[U:] == -7)       # rows past U untouched
+        # the return map: row_of_ret[t, d] = the send row of (t, d)
+        rr = torch.empty((T_r, N), dtype=torch.int32, device="cuda")
+        moe.moe_ep_return_map(sc, b["uniq_offsets"], b["uniq_tokens"], rr)
+        want = -np.ones((T_r, N), dtype=np.int64)
+        for d in range(N):
+            for i in range(int(p.uniq_offsets[d]), int(p.uniq_offsets[d + 1])):
+                want[int(p.uniq_tokens[i]), d] = i
+        assert np.array_equal(np_(rr), want)
+
+
+def weights_of(wl, N):
+    W = make_weights(wl, "cuda")
+    return W, ep.local_weights(*W, N)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
+def test_ep_layer_matches_oracle(case):
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    layer = ep.EPLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    ys = layer.forward(xs, [torch.from_numpy(L).cuda() for L in Ls])
+    torch.cuda.synchronize()
+    mc = ref.MoEConfig(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                       wl.renorm)
+    want, over, n = ref.ep_layer(mc, N, [f64(x) for x in xs], Ls,
+                                 ref.dense_weights(*(f64(w) for w in W)))
+    assert layer.info["overflow"] == int(over)
+    assert layer.info["n_chunks"] == n
+    tol = TOL[wl.dtype]
+    got = np.concatenate([f64(y) for y in ys])
+    assert_close(got, np.concatenate(want), tol,
+                 f"EP y (N={N}, overflow={int(over)}, passes={n})")
+    for r in range(N):
+        if Ts[r]:
+            assert_close(f64(ys[r]), want[r], tol, f"EP y rank {r}")
+
+
+@pytest.mark.parametrize("case", CASES[:3] + CASES[4:],
+                         ids=lambda c: c[0].name)
+def test_ep_layer_matches_single_gpu_layer(case):
+    """The EP layer over N logical ranks and moe_layer on the ranks'
+    batches together agree within the tolerance (the EP combine rounds each
+    destination's partial row to the layer dtype before the source adds
+    them, so the bits may differ)."""
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    ys = ep.EPLayer(cfg, ep.LoopbackTransport(N), per_rank).forward(
+        xs, [torch.from_numpy(L).cuda() for L in Ls])
+    x_all = torch.cat(xs)
+    L_all = torch.from_numpy(np.concatenate(Ls)).cuda()
+    y1 = torch.empty_like(x_all)
+    moe.moe_layer(cfg, x_all, L_all, *W, y1, moe.MOE_MODE_FALLBACK_LAYER,
+                  moe.layer_workspace(cfg))
+    torch.cuda.synchronize()
+    assert_close(f64(torch.cat(ys)), f64(y1), TOL[wl.dtype],
+                 "EP y vs single-GPU moe_layer")
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
+def test_ring_layer_matches_oracle(case):
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    ys = ep.RingLayer(cfg, ep.LoopbackTransport(N), per_rank).forward(
+        xs, [torch.from_numpy(L).cuda() for L in Ls])
+    torch.cuda.synchronize()
+    mc = ref.MoEConfig(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                       wl.renorm)
+    want = ref.ring_layer(mc, N, [f64(x) for x in xs], Ls,
+                          ref.dense_weights(*(f64(w) for w in W)))
+    assert_close(np.concatenate([f64(y) for y in ys]),
+                 np.concatenate(want), TOL[wl.dtype], f"ring y (N={N})")
+
+
+def test_ep_check_global_flag():
+    """moe_ep_check on summed shard counts: strict > C with C from the
+    global token count; required factor max_s r_s * S / (T k)."""
+    cfg = moe.make_config(1000, 128, 8, 2, 128, 4, 1.5, 0, "bf16")
+    C = moe.moe_capacity_rows(cfg)           # floor(1.5 * 2000 / 4) = 750
+    assert C == 750
+    for loads, flag in (([750, 500, 500, 250], 0), ([751, 500, 500, 249], 1),
+                        ([0, 0, 0, 0], 0)):
+        s = torch.tensor(loads, dtype=torch.int32, device="cuda")
+        f = torch.full((1,), 9, dtype=torch.int32, device="cuda")
+        q = torch.zeros(1, dtype=torch.float32, device="cuda")
+        c = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.moe_ep_check(cfg, s, f, q, c)
+        torch.cuda.synchronize()
+        assert int(f.item()) == flag and int(c.item()) == C
+        assert abs(float(q.item()) - max(loads) * 4 / 2000) < 1e-6
+
+
+def test_ep_sum_partials():
+    for dt in (torch.bfloat16, torch.float32):
+        g = torch.Generator(device="cuda").manual_seed(3)
+        parts = torch.randn(3, 77, 256, generator=g, device="cuda").to(dt)
+        cfg = moe.make_config(77, 256, 4, 2, 128, 2, 2.0, 0,
+                              "bf16" if dt == torch.bfloat16 else "f32")
+        y = torch.empty((77, 256), dtype=dt, device="cuda")
+        moe.moe_ep_sum_partials(cfg, 3, parts, y)
+        torch.cuda.synchronize()
+        want = f64(parts).sum(0)
+        assert_close(f64(y), want, TOL["bf16" if dt == torch.bfloat16
+                                        else "f32"], f"sum of parts {dt}")
