@@ -166,8 +166,8 @@ def _declare(h):
     h.moe_chunk_tokens.restype = c_int32
     h.moe_num_chunks.argtypes = [cfg]
     h.moe_num_chunks.restype = c_int32
-    h.moe_gmm_uses_pair.argtypes = [cfg, c_int32, c_int64]
-    h.moe_gmm_uses_pair.restype = c_int32
+    h.moe_gmm_kernel_choice.argtypes = [cfg, c_int32, c_int64]
+    h.moe_gmm_kernel_choice.restype = c_int32
     h.moe_test_stall_gemm_producer.argtypes = [c_int64]
     h.moe_test_stall_gemm_producer.restype = None
     h.moe_status_string.argtypes = [c_int]
@@ -233,9 +233,10 @@ def moe_num_chunks(cfg) -> int:
     return lib().moe_num_chunks(ctypes.byref(cfg))
 
 
-def moe_gmm_uses_pair(cfg, n_groups=0, rows_bound=0) -> int:
-    return int(lib().moe_gmm_uses_pair(ctypes.byref(cfg), n_groups,
-                                       rows_bound))
+def moe_gmm_kernel_choice(cfg, n_groups=0, rows_bound=0) -> int:
+    """Bits: 1 GEMM1 pair, 2 GEMM2 pair, 4 GEMM1 dual m-tile, 8 GEMM2 dual."""
+    return int(lib().moe_gmm_kernel_choice(ctypes.byref(cfg), n_groups,
+                                           rows_bound))
 
 
 def moe_layer_graph_trace_slots(cfg) -> int:

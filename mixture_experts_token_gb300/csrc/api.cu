@@ -370,8 +370,8 @@ int32_t moe_num_chunks(const moe_config_t* cfg) {
   return ct > 0 ? (cfg->T + ct - 1) / ct : 0;
 }
 
-int32_t moe_gmm_uses_pair(const moe_config_t* cfg, int32_t n_groups,
-                          int64_t rows_bound) {
+int32_t moe_gmm_kernel_choice(const moe_config_t* cfg, int32_t n_groups,
+                              int64_t rows_bound) {
   if (validate(cfg) != MOE_OK || n_groups < 0 || n_groups > kMaxExperts)
     return -1;
   Groups g = identity_groups(*cfg);

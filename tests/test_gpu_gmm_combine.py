@@ -52,14 +52,19 @@ def run_gmm(sizes, H, F, dtype, T=None, k=1, seed=0):
 
 
 GMM_CASES = [
-    # (group sizes, H, F, pair kinds): empty groups, single rows, tile
-    # edges, many tiles.  Pair kinds is moe_gmm_uses_pair's answer for bf16:
-    # bit 0 GEMM1 on the two-SM (CTA pair) kernel, bit 1 GEMM2 too; the
-    # pair kernel runs when the groups average >= 1024 rows.
+    # (group sizes, H, F, kernel kinds): empty groups, single rows, tile
+    # edges, many tiles.  Kernel kinds is moe_gmm_kernel_choice's answer for
+    # bf16: bit 0 GEMM1 on the two-SM (CTA pair) kernel, bit 1 GEMM2 too
+    # (groups averaging >= 1024 rows); bit 2 GEMM1 on the dual m-tile kernel,
+    # bit 3 GEMM2 too (>= 192 rows); 0: the one-CTA kernel.
     ([0, 1, 127, 128, 129, 300], 256, 256, 0),
     ([5, 0, 0, 700, 3], 384, 128, 0),       # H % 256 != 0: 128-wide GEMM2
     ([128] * 4, 128, 128, 0),
-    ([1000], 512, 384, 0),
+    ([1000], 512, 384, 12),                 # dual: 4 units of 2, 1 of 1
+    # dual units with one m-tile (128, 1 row, 129's second tile of 1 row,
+    # 257 and 600's last unit), empty groups
+    ([300, 250, 257, 129, 128, 1, 0, 600], 512, 256, 12),
+    ([300, 500], 384, 256, 4),              # dual GEMM1, 128-wide GEMM2
     ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512, 0),
     # 5201 rows in 5 groups (>= 1024 each on average): both pair kernels,
     # with a small and a one-row group among the large ones
@@ -70,21 +75,25 @@ GMM_CASES = [
 ]
 
 
-def test_gmm_pair_choice_query():
-    """moe_gmm_uses_pair follows the average rows per group, the row bound
-    given, the layer dtype and H % 256 for GEMM2."""
+def test_gmm_kernel_choice_query():
+    """moe_gmm_kernel_choice follows the average rows per group, the row
+    bound given, the layer dtype and H % 256 for GEMM2."""
     c = moe.make_config(2048, 512, 2, 1, 256, 1, 2.0, 0, "bf16")
-    assert moe.moe_gmm_uses_pair(c) == 3
-    assert moe.moe_gmm_uses_pair(c, rows_bound=2047) == 0
-    assert moe.moe_gmm_uses_pair(c, n_groups=3) == 0
-    assert moe.moe_gmm_uses_pair(c.with_(H=384)) == 1
-    assert moe.moe_gmm_uses_pair(c.with_(dtype=moe.MOE_F32)) == 0
-    assert moe.moe_gmm_uses_pair(c, n_groups=-1) == -1
-    # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk and the
-    # 8192-token uncapped pass both stay on the one-CTA kernel (256 groups)
+    assert moe.moe_gmm_kernel_choice(c) == 3
+    assert moe.moe_gmm_kernel_choice(c, rows_bound=2047) == 12
+    assert moe.moe_gmm_kernel_choice(c, rows_bound=383) == 0
+    assert moe.moe_gmm_kernel_choice(c, n_groups=3) == 12
+    assert moe.moe_gmm_kernel_choice(c, n_groups=11) == 0
+    assert moe.moe_gmm_kernel_choice(c.with_(H=384)) == 1
+    assert moe.moe_gmm_kernel_choice(c.with_(H=384), rows_bound=1000) == 4
+    assert moe.moe_gmm_kernel_choice(c.with_(dtype=moe.MOE_F32)) == 0
+    assert moe.moe_gmm_kernel_choice(c, n_groups=-1) == -1
+    # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk (64 rows
+    # per expert) stays on the one-CTA kernel; the 8192-token uncapped pass
+    # (256 per expert) takes the dual m-tile kernel
     d = moe.make_config(8192, 7168, 256, 8, 2048, 8, 2.0, 0, "bf16")
-    assert moe.moe_gmm_uses_pair(d) == 0
-    assert moe.moe_gmm_uses_pair(d.with_(T=2048)) == 0
+    assert moe.moe_gmm_kernel_choice(d) == 12
+    assert moe.moe_gmm_kernel_choice(d.with_(T=2048)) == 0
 
 
 @pytest.mark.parametrize("case", GMM_CASES, ids=lambda c: f"{len(c[0])}x{c[1]}x{c[2]}")
@@ -94,7 +103,7 @@ def test_gmm_parity(case, dtype):
     if dtype == "bf16":
         R0 = int(sum(sizes))
         cq = moe.make_config(R0, H, len(sizes), 1, F, 1, 2.0, 0, dtype)
-        assert moe.moe_gmm_uses_pair(cq) == kinds
+        assert moe.moe_gmm_kernel_choice(cq) == kinds
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, dtype)
     want_h, want_y = ref.grouped_ffn(f64(xs[:R]), off,
                                      ref.dense_weights(f64(wg), f64(wu),
@@ -125,7 +134,7 @@ def test_gmm_pair_kernel_full_dims():
     sizes = [1500, 1100, 1300, 257]
     H, F = 7168, 2048
     R0 = int(sum(sizes))
-    assert moe.moe_gmm_uses_pair(
+    assert moe.moe_gmm_kernel_choice(
         moe.make_config(R0, H, 4, 1, F, 1, 2.0, 0, "bf16")) == 3
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=11)
     W = expert_accessor(wg, wu, wd)
@@ -178,6 +187,27 @@ def test_gmm_pair_kernel_row_independence():
     assert torch.equal(ys2[shift:], ys[:R])
 
 
+def test_gmm_dual_and_single_cta_kernels_agree_bitwise():
+    """The same rows and weights through the dual m-tile kernel (2 groups
+    averaging 350 rows) and the one-CTA kernel (the same groups among empty
+    ones, 87 rows per group on average): identical bits."""
+    H, F = 512, 256
+    sizes = [400, 300]
+    cq = moe.make_config(700, H, 2, 1, F, 1, 2.0, 0, "bf16")
+    assert moe.moe_gmm_kernel_choice(cq) == 12
+    assert moe.moe_gmm_kernel_choice(cq, n_groups=8) == 0
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=13)
+    gexp = torch.tensor([0, 1] + [0] * 6, dtype=torch.int32, device="cuda")
+    off8 = torch.tensor([0, 400] + [R] * 7, dtype=torch.int32, device="cuda")
+    cfg = moe.make_config(R, H, 2, 1, F, 1, 2.0, 0, "bf16")
+    h2 = torch.empty_like(h)
+    ys2 = torch.empty_like(ys)
+    moe.moe_gmm_swiglu_mapped(cfg, 8, gexp, xs, off8, wg, wu, wd, h2, ys2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2[:R], h[:R])
+    assert torch.equal(ys2[:R], ys[:R])
+
+
 def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
     """The same rows and weights through the CTA-pair kernel (2 groups of
     ~1100 rows) and the one-CTA kernel (the same groups padded with empty
@@ -186,12 +216,14 @@ def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
     H, F = 512, 256
     sizes = [1500, 700]
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=9)
-    n_groups = 8                                  # 275 rows per group
+    n_groups = 16                                 # 137 rows per group
     gexp = torch.tensor([0, 1] + [0] * (n_groups - 2), dtype=torch.int32,
                         device="cuda")
     off8 = torch.tensor([0, 1500] + [R] * (n_groups - 1), dtype=torch.int32,
                         device="cuda")
     cfg = moe.make_config(R, H, 2, 1, F, 1, 2.0, 0, "bf16")
+    assert moe.moe_gmm_kernel_choice(cfg) == 3
+    assert moe.moe_gmm_kernel_choice(cfg, n_groups=n_groups) == 0
     h2 = torch.empty_like(h)
     ys2 = torch.empty_like(ys)
     moe.moe_gmm_swiglu_mapped(cfg, n_groups, gexp, xs, off8, wg, wu, wd, h2,
