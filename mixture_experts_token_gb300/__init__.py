@@ -234,7 +234,7 @@ def moe_num_chunks(cfg) -> int:
 
 
 def moe_gmm_kernel_choice(cfg, n_groups=0, rows_bound=0) -> int:
-    """Bits: 1 GEMM1 pair, 2 GEMM2 pair, 4 GEMM1 dual m-tile, 8 GEMM2 dual."""
+    """Bits: 1 GEMM1 on the CTA-pair kernel, 2 GEMM2 on it; 0: one-CTA."""
     return int(lib().moe_gmm_kernel_choice(ctypes.byref(cfg), n_groups,
                                            rows_bound))
 

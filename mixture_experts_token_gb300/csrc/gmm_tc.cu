@@ -556,274 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ------------------------------------------------- dual m-tile kernel ----
-// One CTA computes a unit of up to two m-tiles (256 rows) of one group and
-// one n-tile: each stage holds both A tiles and ONE B tile, and the MMA
-// warp issues the two M=128 MMAs of a K=16 step back to back on that B, so
-// the weights cross L2 -> shared memory once per two m-tiles (64 KB per
-// stage for 8.4 MFLOP instead of 48 KB for 4.2).  Unlike the CTA pair's
-// M=256 tiles, a unit whose second m-tile would be empty issues only the
-// first MMA, so no tensor work is spent on rows a group does not have
-// beyond the one-CTA kernel's 128-row granularity.  The two accumulators
-// take all 512 TMEM columns, so the MMA warp starts the next unit once the
-// epilogue has read them; eight epilogue warps (two per TMEM lane quadrant)
-// drain the two in parallel.  Rows give the same bits as in the other
-// kernels (same K order per row).
-constexpr int STAGES_D = 3;
-constexpr int kDualThreads = 320;           // 2 + 8 warps
-constexpr int kDualEpiThreads = 256;
-constexpr int kDualStage = 2 * BM * BK * 2 + BK * 256 * 2;   // 64 KB
-
-template <int MODE>
-__global__ void __launch_bounds__(kDualThreads, 1)
-    gmm_tc_dual_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB0,
-                       const __grid_constant__ CUtensorMap tmB1, Params p) {
-  static_assert(MODE == 0 || MODE == 1, "forward GEMMs only");
-  constexpr int kA = BM * BK * 2;   // one A tile, 16 KB
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES_D * kDualStage);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES_D;
-  uint64_t* tfull = bars + 2 * STAGES_D;    // [2]: one per accumulator
-  uint64_t* tempty = tfull + 2;             // [1]: both read
-  uint64_t* done = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [64]
-  int* goff = wsum + 64;                               // [E+1]
-  int* hpre = goff + (p.E + 1);                        // [E+1]
-  int* lpre = hpre + (p.E + 1);                        // [E+1]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t smem_base = smem_u32(smem);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES_D; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 1);
-    }
-    mbar_init(smem_u32(tfull), 1);
-    mbar_init(smem_u32(tfull + 1), 1);
-    mbar_init(smem_u32(tempty), kDualEpiThreads);
-    mbar_init(smem_u32(done), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    fence_proxy_async_smem();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB0);
-    if (MODE == 0) prefetch_tmap(&tmB1);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  build_tile_table(p.group_offsets, p.E, goff, hpre, lpre, wsum, 2 * BM);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  TileTable tt;
-  tt.goff = goff;
-  tt.hpre = hpre;
-  tt.lpre = lpre;
-  tt.G = p.E;
-  tt.n_tiles = p.n_tiles;
-  tt.heavy = static_cast<long long>(hpre[p.E]) * p.n_tiles;
-  tt.total = tt.heavy + static_cast<long long>(lpre[p.E]) * p.n_tiles;
-  const int total_tiles = static_cast<int>(tt.total);
-  const int kblocks = p.K / BK;
-  // m-tiles of unit (e, m): 2 unless the group ends within its first 128
-  auto subs = [&](int e, int m) {
-    return goff[e + 1] - (goff[e] + m * 2 * BM) > BM ? 2 : 1;
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer -----
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      long long fills = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles;
-           tile += gridDim.x) {
-        int e, m, n;
-        decode_tile(tt, tile, e, m, n);
-        const int ns = subs(e, m);
-        const int a_row = goff[e] + m * 2 * BM;
-        const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
-        const int b_row = we * p.K;
-        const uint32_t tx = static_cast<uint32_t>(ns * kA + BK * 256 * 2);
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
-                         p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(full + stage);
-          mbar_expect_tx(fb, tx);
-          const uint32_t sa = smem_base + stage * kDualStage;
-          const uint32_t sb = sa + 2 * kA;
-          tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
-          if (ns == 2) tma_load_2d(sa + kA, &tmA, fb, kb * BK, a_row + BM);
-          if (MODE == 0) {
-            tma_load_2d(sb, &tmB0, fb, n * 128, b_row + kb * BK);
-            tma_load_2d(sb + 8192, &tmB0, fb, n * 128 + 64, b_row + kb * BK);
-            tma_load_2d(sb + 16384, &tmB1, fb, n * 128, b_row + kb * BK);
-            tma_load_2d(sb + 24576, &tmB1, fb, n * 128 + 64,
-                        b_row + kb * BK);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(sb + c * 8192, &tmB0, fb, n * 256 + c * 64,
-                          b_row + kb * BK);
-          }
-          ++fills;
-          if (++stage == STAGES_D) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      const long long first = fills > STAGES_D ? fills - STAGES_D : 0;
-      for (long long f = first; f < fills; ++f)
-        mbar_wait(smem_u32(full + (f % STAGES_D)),
-                  static_cast<uint32_t>((f / STAGES_D) & 1), nullptr,
-                  p.status);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer -------
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, 256, true);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles;
-           tile += gridDim.x) {
-        int e, m, n;
-        decode_tile(tt, tile, e, m, n);
-        const int ns = subs(e, m);
-        if (!mbar_wait(smem_u32(tempty), acc_phase ^ 1u, abort_flag,
-                       p.status))
-          break;
-        tc_fence_after();
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag,
-                         p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_base + stage * kDualStage;
-          const uint32_t sb = sa + 2 * kA;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
-            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            umma_bf16(tmem_base, smem_desc(sa + kk * 32, 16, 1024), bd,
-                      idesc, acc);
-            if (ns == 2)
-              umma_bf16(tmem_base + kAccCols,
-                        smem_desc(sa + kA + kk * 32, 16, 1024), bd, idesc,
-                        acc);
-          }
-          umma_commit(smem_u32(empty + stage));
-          if (++stage == STAGES_D) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(smem_u32(tfull));
-        umma_commit(smem_u32(tfull + 1));
-        acc_phase ^= 1u;
-      }
-      umma_commit(smem_u32(done));
-      mbar_wait(smem_u32(done), 0, nullptr, p.status);
-    }
-  } else {
-    // ------------------------------------------------ epilogue ---------
-    // warps 2-5 read accumulator 0, warps 6-9 accumulator 1
-    const int sub = (warp - 2) >> 2;
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;
-    uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      int e, m, n;
-      decode_tile(tt, tile, e, m, n);
-      const int ns = subs(e, m);
-      bool ok = mbar_wait(smem_u32(tfull + sub), acc_phase, abort_flag,
-                          p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const int grow = goff[e] + m * 2 * BM + sub * BM + row;
-      const bool valid = sub < ns && grow < goff[e + 1];
-      const uint32_t taddr = tmem_base +
-                             (static_cast<uint32_t>(q * 32) << 16) +
-                             sub * kAccCols;
-      if (sub < ns) {
-        if (MODE == 0) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              p.out + static_cast<long long>(grow) * p.out_ld + n * 128);
-#pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
-            uint32_t g[32], u[32];
-            tmem_ld32x2(taddr + c, taddr + 128 + c, g, u);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]);
-              const float g1 = __uint_as_float(g[2 * i + 1]);
-              const float h0 = g0 / (1.0f + __expf(-g0)) *
-                               __uint_as_float(u[2 * i]);
-              const float h1 = g1 / (1.0f + __expf(-g1)) *
-                               __uint_as_float(u[2 * i + 1]);
-              pk[i] = pack_bf16x2(h0, h1);
-            }
-            if (valid) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
-                                            pk[4 * v + 2], pk[4 * v + 3]);
-            }
-          }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(
-              p.out + static_cast<long long>(grow) * p.out_ld + n * 256);
-#pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
-            uint32_t r[32];
-            tmem_ld32(taddr + c, r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
-                                  __uint_as_float(r[2 * i + 1]));
-            if (valid) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
-                                            pk[4 * v + 2], pk[4 * v + 3]);
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(tempty));
-      acc_phase ^= 1u;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
 // ------------------------------------------------------ pair kernel ------
 constexpr int STAGES2 = 6;
 constexpr int BMP = 2 * BM;                     // rows of a pair tile
@@ -1095,40 +827,6 @@ bool use_pair(const moe_config_t& c, const Groups& g) {
          group_rows_bound(c, g) >= kPairMinRowsPerGroup * g.n;
 }
 
-// The dual m-tile kernel: for groups of at least ~1.5 m-tiles on average
-// (most units then hold two m-tiles sharing a B tile) and below the pair
-// kernel's threshold.  Smaller groups stay on the one-CTA kernel, whose
-// four 48 KB stages keep more weight bytes in flight per SM.
-constexpr long long kDualMinRowsPerGroup = 192;
-
-bool use_dual(const moe_config_t& c, const Groups& g) {
-  return g_stall_after_fills.load() < 0 &&
-         group_rows_bound(c, g) >= kDualMinRowsPerGroup * g.n;
-}
-
-size_t smem_bytes_dual(int E) {
-  return 1024 + STAGES_D * kDualStage + 8 * (2 * STAGES_D + 4) + 16 +
-         4 * (64 + 3 * (E + 1)) + 64;
-}
-
-template <int MODE>
-cudaError_t launch_dual(const CUtensorMap& a, const CUtensorMap& b0,
-                        const CUtensorMap& b1, const Params& p,
-                        cudaStream_t s) {
-  const size_t smem = smem_bytes_dual(p.E);
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(gmm_tc_dual_kernel<MODE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  gmm_tc_dual_kernel<MODE><<<sms, kDualThreads, smem, s>>>(a, b0, b1, p);
-  return cudaGetLastError();
-}
-
 size_t smem_bytes_pair(int E) {
   return 1024 + STAGES2 * kStage2 + 8 * (2 * STAGES2 + 5) + 16 +
          4 * (64 + 3 * (E + 1)) + 64;
@@ -1175,11 +873,8 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
 }  // namespace tc
 
 int gmm_pair_kinds(const moe_config_t& c, const Groups& g) {
-  if (!gmm_tc_supported(c)) return 0;
-  const bool wide = c.H % 256 == 0;   // GEMM2's 256-column tiles
-  if (tc::use_pair(c, g)) return 1 | (wide ? 2 : 0);
-  if (tc::use_dual(c, g)) return 4 | (wide ? 8 : 0);
-  return 0;
+  if (!gmm_tc_supported(c) || !tc::use_pair(c, g)) return 0;
+  return 1 | (c.H % 256 == 0 ? 2 : 0);   // GEMM2's 256-column tiles
 }
 
 void set_gemm_stall_for_tests(long long fills) {
@@ -1207,7 +902,6 @@ cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
   tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
   if (tc::use_pair(c, g)) return tc::launch_pair<0>(a1, bg, bu, p1, s);
-  if (tc::use_dual(c, g)) return tc::launch_dual<0>(a1, bg, bu, p1, s);
   return tc::launch_one<0, 256>(a1, bg, bu, a1, p1, s);
 }
 
@@ -1226,7 +920,6 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
     tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
     if (tc::use_pair(c, g)) return tc::launch_pair<1>(a2, bd, bd, p2, s);
-    if (tc::use_dual(c, g)) return tc::launch_dual<1>(a2, bd, bd, p2, s);
     return tc::launch_one<1, 256>(a2, bd, bd, a2, p2, s);
   }
   tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 128,

@@ -55,16 +55,11 @@ GMM_CASES = [
     # (group sizes, H, F, kernel kinds): empty groups, single rows, tile
     # edges, many tiles.  Kernel kinds is moe_gmm_kernel_choice's answer for
     # bf16: bit 0 GEMM1 on the two-SM (CTA pair) kernel, bit 1 GEMM2 too
-    # (groups averaging >= 1024 rows); bit 2 GEMM1 on the dual m-tile kernel,
-    # bit 3 GEMM2 too (>= 192 rows); 0: the one-CTA kernel.
+    # (groups averaging >= 1024 rows); 0: the one-CTA kernel.
     ([0, 1, 127, 128, 129, 300], 256, 256, 0),
     ([5, 0, 0, 700, 3], 384, 128, 0),       # H % 256 != 0: 128-wide GEMM2
     ([128] * 4, 128, 128, 0),
-    ([1000], 512, 384, 12),                 # dual: 4 units of 2, 1 of 1
-    # dual units with one m-tile (128, 1 row, 129's second tile of 1 row,
-    # 257 and 600's last unit), empty groups
-    ([300, 250, 257, 129, 128, 1, 0, 600], 512, 256, 12),
-    ([300, 500], 384, 256, 4),              # dual GEMM1, 128-wide GEMM2
+    ([1000], 512, 384, 0),
     ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512, 0),
     # 5201 rows in 5 groups (>= 1024 each on average): both pair kernels,
     # with a small and a one-row group among the large ones
@@ -80,19 +75,15 @@ def test_gmm_kernel_choice_query():
     bound given, the layer dtype and H % 256 for GEMM2."""
     c = moe.make_config(2048, 512, 2, 1, 256, 1, 2.0, 0, "bf16")
     assert moe.moe_gmm_kernel_choice(c) == 3
-    assert moe.moe_gmm_kernel_choice(c, rows_bound=2047) == 12
-    assert moe.moe_gmm_kernel_choice(c, rows_bound=383) == 0
-    assert moe.moe_gmm_kernel_choice(c, n_groups=3) == 12
-    assert moe.moe_gmm_kernel_choice(c, n_groups=11) == 0
+    assert moe.moe_gmm_kernel_choice(c, rows_bound=2047) == 0
+    assert moe.moe_gmm_kernel_choice(c, n_groups=3) == 0
     assert moe.moe_gmm_kernel_choice(c.with_(H=384)) == 1
-    assert moe.moe_gmm_kernel_choice(c.with_(H=384), rows_bound=1000) == 4
     assert moe.moe_gmm_kernel_choice(c.with_(dtype=moe.MOE_F32)) == 0
     assert moe.moe_gmm_kernel_choice(c, n_groups=-1) == -1
-    # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk (64 rows
-    # per expert) stays on the one-CTA kernel; the 8192-token uncapped pass
-    # (256 per expert) takes the dual m-tile kernel
+    # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk and the
+    # 8192-token uncapped pass both stay on the one-CTA kernel (256 groups)
     d = moe.make_config(8192, 7168, 256, 8, 2048, 8, 2.0, 0, "bf16")
-    assert moe.moe_gmm_kernel_choice(d) == 12
+    assert moe.moe_gmm_kernel_choice(d) == 0
     assert moe.moe_gmm_kernel_choice(d.with_(T=2048)) == 0
 
 
@@ -185,27 +176,6 @@ def test_gmm_pair_kernel_row_independence():
     torch.cuda.synchronize()
     assert torch.equal(h2[shift:], h[:R])
     assert torch.equal(ys2[shift:], ys[:R])
-
-
-def test_gmm_dual_and_single_cta_kernels_agree_bitwise():
-    """The same rows and weights through the dual m-tile kernel (2 groups
-    averaging 350 rows) and the one-CTA kernel (the same groups among empty
-    ones, 87 rows per group on average): identical bits."""
-    H, F = 512, 256
-    sizes = [400, 300]
-    cq = moe.make_config(700, H, 2, 1, F, 1, 2.0, 0, "bf16")
-    assert moe.moe_gmm_kernel_choice(cq) == 12
-    assert moe.moe_gmm_kernel_choice(cq, n_groups=8) == 0
-    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=13)
-    gexp = torch.tensor([0, 1] + [0] * 6, dtype=torch.int32, device="cuda")
-    off8 = torch.tensor([0, 400] + [R] * 7, dtype=torch.int32, device="cuda")
-    cfg = moe.make_config(R, H, 2, 1, F, 1, 2.0, 0, "bf16")
-    h2 = torch.empty_like(h)
-    ys2 = torch.empty_like(ys)
-    moe.moe_gmm_swiglu_mapped(cfg, 8, gexp, xs, off8, wg, wu, wd, h2, ys2)
-    torch.cuda.synchronize()
-    assert torch.equal(h2[:R], h[:R])
-    assert torch.equal(ys2[:R], ys[:R])
 
 
 def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
