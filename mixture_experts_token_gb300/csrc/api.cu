@@ -165,6 +165,7 @@ LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
   b.alt.expand_idx = cv.take<int32_t>(tk);
   b.alt.n_dropped = cv.take<int32_t>(1);
   b.alt.pws = carve_permute_scratch(cv, T, c.E, c.k, c.S);
+  b.row_of_alt = cv.take<int32_t>(tk);
   if (bytes) *bytes = align_up(cv.off, 256);
   return b;
 }
@@ -279,7 +280,8 @@ cudaError_t pipelined_passes(const moe_config_t& c, const void* x,
     const size_t o = static_cast<size_t>(t0);
     int64_t* tr = b.trace;
     if ((e = stamp(tr, trace_slot(i, 0), s)) != cudaSuccess) return e;
-    e = i == 0 ? tables(0, s) : cudaStreamWaitEvent(s, pp.ready[i & 1], 0);
+    e = i == 0 ? (pp.first_ready ? cudaSuccess : tables(0, s))
+               : cudaStreamWaitEvent(s, pp.ready[i & 1], 0);
     if (e != cudaSuccess) return e;
     if ((e = launch_permute_scatter(
              sc, static_cast<const char*>(x) + o * row_bytes,
@@ -303,6 +305,36 @@ cudaError_t pipelined_passes(const moe_config_t& c, const void* x,
     if (i + 1 < n && (e = tables(i + 1, pp.side)) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t capped_pass_tabled(const moe_config_t& c, const void* x,
+                               const float* topk_w, const void* wg,
+                               const void* wu, const void* wd, void* y,
+                               const LayerBufs& b, const int32_t* row_of,
+                               const PassTables& tb, int32_t* status,
+                               cudaStream_t s) {
+  int64_t* tr = b.trace;
+  Groups groups = identity_groups(c);
+  groups.max_rows = std::min<int64_t>(static_cast<int64_t>(c.T) * c.k,
+                                      static_cast<int64_t>(c.S) *
+                                          std::max<int64_t>(capacity_rows(c),
+                                                            0));
+  cudaError_t e;
+  if ((e = stamp(tr, trace_slot(0, 0), s)) != cudaSuccess ||
+      (e = launch_permute_scatter(c, x, row_of, tb.uniq_offsets, b.x_sorted,
+                                  tb.uniq_tokens, tb.expand_idx, tb.pws, s)) !=
+          cudaSuccess ||
+      (e = stamp(tr, trace_slot(0, 1), s)) != cudaSuccess ||
+      (e = launch_gmm1(c, groups, b.x_sorted, tb.group_offsets, wg, wu, b.h,
+                       status, s)) != cudaSuccess ||
+      (e = stamp(tr, trace_slot(0, 2), s)) != cudaSuccess ||
+      (e = launch_gmm2(c, groups, b.h, tb.group_offsets, wd, b.y_sorted,
+                       status, s)) != cudaSuccess ||
+      (e = stamp(tr, trace_slot(0, 3), s)) != cudaSuccess ||
+      (e = launch_combine(c, b.y_sorted, row_of, topk_w, y, s)) !=
+          cudaSuccess)
+    return e;
+  return stamp(tr, trace_slot(0, 4), s);
 }
 
 // The chunked dropless fallback over precomputed routing.

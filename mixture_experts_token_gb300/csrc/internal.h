@@ -149,6 +149,8 @@ struct LayerBufs {
   PermuteScratch pws;
   void *x_sorted, *h, *y_sorted;
   PassTables alt;  // a second table set, for pipelined chunked passes
+  int32_t* row_of_alt;  // [T*k] row_of of the capped pass whose tables a
+                        // layer graph computes before its branch
   // Stage timestamps of a traced layer graph (device int64, slots of
   // trace_slot below), or null: no stamps.
   int64_t* trace = nullptr;
@@ -163,6 +165,7 @@ struct LayerBufs {
 struct PassPipeline {
   cudaStream_t side;
   cudaEvent_t fork, ready[2], done[2];
+  bool first_ready = false;  // chunk 0's tables (set 0) already computed
 };
 LayerBufs carve_layer(void* base, const moe_config_t& c, int T,
                       size_t* bytes);
@@ -188,6 +191,14 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                  const void* wu, const void* wd, void* y, const LayerBufs& b,
                  int32_t* status, cudaStream_t s, bool planned = false,
                  int pass_index = 0);
+// The capped pass over tables already computed (moe_permute_tables with cap
+// into row_of and table set `tb`): row scatter, GEMM1, GEMM2, combine.
+cudaError_t capped_pass_tabled(const moe_config_t& c, const void* x,
+                               const float* topk_w, const void* wg,
+                               const void* wu, const void* wd, void* y,
+                               const LayerBufs& b, const int32_t* row_of,
+                               const PassTables& tb, int32_t* status,
+                               cudaStream_t s);
 // the chunked dropless fallback over routing already in topk_idx/topk_w.
 // With pp (b carved for all T tokens), the permute tables of chunk i+1 run
 // on pp->side during chunk i's expert FFN, in two table sets.

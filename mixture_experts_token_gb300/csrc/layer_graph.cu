@@ -1,4 +1,6 @@
 // The whole layer with moe_dropless_fallback=layer as one CUDA graph.
+// (While the check runs, two side branches already compute the first
+// permute tables of either outcome; see build().)
 //
 // "Support moe_dropless_fallback=layer on the ragged all-to-all MoE path"
 // (MaxText pull request 5920), section How: a lax.cond picks the capped path
@@ -48,7 +50,7 @@ struct CaptureGuard {  // ends a capture left open by an early return
 
 // Events of one capture, destroyed with it (the graph keeps the edges).
 struct PipelineEvents {
-  cudaEvent_t ev[5] = {};
+  cudaEvent_t ev[8] = {};
   cudaError_t create() {
     for (auto& e : ev) {
       const cudaError_t r =
@@ -87,8 +89,45 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   if ((e = stamp(b.trace, 0, main_s.s)) != cudaSuccess ||
       (e = launch_route(c, logits, b.topk_idx, b.topk_w, status,
                         main_s.s)) != cudaSuccess ||
-      (e = stamp(b.trace, 1, main_s.s)) != cudaSuccess ||
-      (e = launch_check(c, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
+      (e = stamp(b.trace, 1, main_s.s)) != cudaSuccess)
+    return e;
+
+  // While the check runs, two side branches compute the permute tables each
+  // branch needs first: the capped pass's (into row_of_alt and table set
+  // 1; not with a duplication plan, whose tables need the plan) and the
+  // first fallback chunk's (into row_of and set 0).  Both depend only on the
+  // routing; the branch not taken leaves its tables unused.
+  CaptureGuard spec_a, spec_b;
+  PipelineEvents se;
+  const int ct = chunk_tokens(c);
+  const int n_all = ct > 0 ? (c.T + ct - 1) / ct : 0;
+  const bool spec_capped = !planned;
+  const bool spec_chunk = n_all >= 2;
+  if ((e = se.create()) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&spec_a.s, cudaStreamNonBlocking)) !=
+          cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&spec_b.s, cudaStreamNonBlocking)) !=
+          cudaSuccess ||
+      (e = cudaEventRecord(se.ev[0], main_s.s)) != cudaSuccess)
+    return e;
+  if (spec_capped &&
+      ((e = cudaStreamWaitEvent(spec_a.s, se.ev[0], 0)) != cudaSuccess ||
+       (e = launch_permute_tables(c, b.topk_idx, capacity_rows(c),
+                                  b.row_of_alt, b.alt.sorted_token,
+                                  b.alt.group_offsets, b.alt.uniq_offsets,
+                                  b.alt.n_dropped, b.alt.pws, status,
+                                  spec_a.s)) != cudaSuccess ||
+       (e = cudaEventRecord(se.ev[1], spec_a.s)) != cudaSuccess))
+    return e;
+  if (spec_chunk &&
+      ((e = cudaStreamWaitEvent(spec_b.s, se.ev[0], 0)) != cudaSuccess ||
+       (e = launch_permute_tables(sub_config(c, ct), b.topk_idx, -1,
+                                  b.row_of, b.sorted_token, b.group_offsets,
+                                  b.uniq_offsets, b.n_dropped, b.pws, status,
+                                  spec_b.s)) != cudaSuccess ||
+       (e = cudaEventRecord(se.ev[2], spec_b.s)) != cudaSuccess))
+    return e;
+  if ((e = launch_check(c, b.topk_idx, b.counts, b.offsets, b.shard, b.flag,
                         b.req, b.cap, main_s.s)) != cudaSuccess)
     return e;
   if (planned &&
@@ -98,6 +137,11 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   set_branch_kernel<<<1, 1, 0, main_s.s>>>(handle,
                                            planned ? b.flag_after : b.flag);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((spec_capped &&
+       (e = cudaStreamWaitEvent(main_s.s, se.ev[1], 0)) != cudaSuccess) ||
+      (spec_chunk &&
+       (e = cudaStreamWaitEvent(main_s.s, se.ev[2], 0)) != cudaSuccess))
+    return e;
   if ((e = stamp(b.trace, 2, main_s.s)) != cudaSuccess) return e;
 
   cudaStreamCaptureStatus cst;
@@ -128,6 +172,7 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
     return e;
   PassPipeline pp{side_s.s, pe.ev[0], {pe.ev[1], pe.ev[2]},
                   {pe.ev[3], pe.ev[4]}};
+  pp.first_ready = spec_chunk;
   e = cudaStreamBeginCaptureToGraph(body_s.s, body_overflow, nullptr, nullptr,
                                     0, cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
@@ -140,8 +185,11 @@ cudaError_t build(const moe_config_t& c, const void* x, const float* logits,
   e = cudaStreamBeginCaptureToGraph(body_s.s, body_capped, nullptr, nullptr,
                                     0, cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return e;
-  e = pass(c, x, b.topk_idx, b.topk_w, capacity_rows(c), wg, wu, wd, y, b,
-           status, body_s.s, planned);
+  e = spec_capped
+          ? capped_pass_tabled(c, x, b.topk_w, wg, wu, wd, y, b,
+                               b.row_of_alt, b.alt, status, body_s.s)
+          : pass(c, x, b.topk_idx, b.topk_w, capacity_rows(c), wg, wu, wd, y,
+                 b, status, body_s.s, planned);
   if (e != cudaSuccess) return e;
   if ((e = cudaStreamEndCapture(body_s.s, &tmp)) != cudaSuccess) return e;
 
