@@ -712,13 +712,29 @@ def trace_stage_ms(stamps, n_pass):
     return d
 
 
-def graph_launches(passes, shards, planned):
+def graph_launches(passes, T, shards, planned, chunk_tokens, n_chunks):
     """Kernels of one traced graph step: the router, route, check, (plan),
-    the branch select, the stamps (3 + 5 per pass), and per pass its permute
-    tables (table_launches), scatter, GEMM1, GEMM2 and combine."""
-    return 1 + 3 + planned + 3 + 5 * len(passes) + \
-        sum(table_launches(t1 - t0, shards) + 4 for (t0, t1, _) in passes
-            if t1 > t0)
+    the branch select, the stamps (3 + 5 per pass); before the branch, on
+    side branches, the capped pass's permute tables (not with a plan) and the
+    first fallback chunk's (when the fallback has two chunks or more); then
+    per pass the scatter, GEMM1, GEMM2 and combine, and the permute tables
+    the side branches did not compute (the later chunks', or the capped
+    pass's with a plan)."""
+    n = 1 + 3 + planned + 3 + 5 * len(passes)
+    if not planned:
+        n += table_launches(T, shards)
+    if n_chunks >= 2:
+        n += table_launches(chunk_tokens, shards)
+    overflow = bool(passes) and not passes[0][2]
+    for i, (t0, t1, _) in enumerate(passes):
+        if t1 <= t0:
+            continue
+        n += 4
+        if overflow and (i >= 1 or n_chunks < 2):
+            n += table_launches(t1 - t0, shards)
+        if not overflow and planned:
+            n += table_launches(t1 - t0, shards)
+    return n
 
 
 def stage_table(layer, passes, stage_ms, mean_ms, steps):
@@ -964,7 +980,9 @@ def measure_layer(layer, steps, warmup, device, flush, world=1, clocks=None,
         "kernels": kernels,
         "roofline": roofline_of(layer, passes, stage_ms, work, n),
         "check_us": round(kernels["check"]["ms_per_step"] * 1e3, 2),
-        "gpu_launches": graph_launches(passes, layer.wl.S, planned) * n,
+        "gpu_launches": graph_launches(
+            passes, layer.wl.T, layer.wl.S, planned, layer.chunk,
+            moe.moe_num_chunks(layer.cfg)) * n,
         "warm_l2": {"value": round(whole_job_tokens_per_s(world, T, warm),
                                    1),
                     "unit": UNIT, "ms_per_step": round(warm, 4),

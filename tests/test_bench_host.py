@@ -56,3 +56,19 @@ def test_backward_launches():
     assert bench.backward_launches([(0, 8192, True)], "fallback", True,
                                    planned=True, shards=8) == \
         3 + 10 + 1 + 2 + 2 + 2
+
+
+def test_traced_graph_launches():
+    # DeepSeek-V3 layer, 4 chunks of 2048 tokens: router, route, check,
+    # branch select, 23 stamps; side branches: the capped pass's tables (64
+    # blocks x 8 shards: 3 kernels) and chunk 0's (3); per chunk scatter,
+    # GEMM1, GEMM2, combine; chunks 1-3 their tables (3 each)
+    assert bench.graph_launches(chunks(4), 8192, 8, 0, 2048, 4) == \
+        1 + 3 + 23 + 3 + 3 + 16 + 9
+    # Llama4-Maverick, no overflow: the capped pass only (its tables and
+    # chunk 0's of the 8-chunk fallback ran before the branch)
+    assert bench.graph_launches([(0, 8192, True)], 8192, 16, 0, 1024, 8) == \
+        1 + 3 + 8 + 3 + 3 + 4
+    # with a duplication plan the capped pass computes its own tables
+    assert bench.graph_launches([(0, 8192, True)], 8192, 8, 1, 2048, 4) == \
+        1 + 3 + 1 + 8 + 3 + 4 + 3
