@@ -421,7 +421,8 @@ class Layer:
         mode = {"fallback": self.moe.MOE_MODE_FALLBACK_LAYER,
                 "capped": self.moe.MOE_MODE_CAPPED,
                 "dropless": self.moe.MOE_MODE_DROPLESS}[self.mode]
-        return self.moe.moe_layer(self.cfg, x, logits, *self.W, y, mode,
+        W = self.W if self.W is not None else (None, None, None)
+        return self.moe.moe_layer(self.cfg, x, logits, *W, y, mode,
                                   self.ws, self.b["status"])
 
 
@@ -823,23 +824,19 @@ def measure_layer(layer, steps, warmup, device, flush, world=1, clocks=None,
     passes = layer.step()
     torch.cuda.synchronize()
     b = layer.b
-    if layer.dispatch_only:
-        overflow = int(b["overflow_flag"].item()) \
-            if layer.mode == "fallback" else -1
-    else:
-        y_api = torch.empty_like(b["y"])
-        info = layer.api_layer(layer.x, layer.logits, y_api)
-        torch.cuda.synchronize()
-        if not torch.equal(y_api, b["y"]):
-            raise SystemExit("stepwise path and moe_layer disagree")
-        overflow = info["overflow"]
-        del y_api
+    y_api = torch.empty_like(b["y"])
+    info = layer.api_layer(layer.x, layer.logits, y_api)
+    torch.cuda.synchronize()
+    if not torch.equal(y_api, b["y"]):
+        raise SystemExit("stepwise path and moe_layer disagree")
+    overflow = info["overflow"]
+    del y_api
     if int(b["status"].item()) != 0:
         raise SystemExit(f"device status {int(b['status'].item())}")
     res = {"overflow": overflow, "passes": len(passes),
            "capacity": moe.moe_capacity_rows(layer.cfg)}
     planned = int(layer.cfg.redundant_slots > 0 and layer.mode == "fallback")
-    use_graph = layer.mode == "fallback" and not layer.dispatch_only
+    use_graph = layer.mode == "fallback"
 
     # the stepwise entry points, CUDA events between stages
     for _ in range(warmup):
@@ -905,7 +902,8 @@ def measure_layer(layer, steps, warmup, device, flush, world=1, clocks=None,
     y_d = torch.empty_like(b["y"])
     ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws, status,
+    W = layer.W if layer.W is not None else (None, None, None)
+    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *W, y_d, ws, status,
                           trace=trace)
 
     def run():
@@ -949,6 +947,8 @@ def measure_layer(layer, steps, warmup, device, flush, world=1, clocks=None,
     stage_ms = {"router": sum(a.elapsed_time(r) for a, r, _ in evs)}
     for i in range(n):
         for name, d in trace_stage_ms(stamps[i], len(passes)).items():
+            if layer.dispatch_only and name.startswith("gmm"):
+                continue    # no expert FFN: two adjacent stamps
             stage_ms[name] = stage_ms.get(name, 0.0) + d
     kernels, work = stage_table(layer, passes, stage_ms, mean_ms, n)
     staged = sum(stage_ms.values()) / n
@@ -1087,7 +1087,8 @@ def graph_run(layer, steps, warmup, device):
     L_d = layer.logits.clone()
     y_d = torch.empty_like(layer.b["y"])
     ws = moe.layer_workspace(layer.cfg, moe.MOE_WS_LAYER, device)
-    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *layer.W, y_d, ws)
+    W = layer.W if layer.W is not None else (None, None, None)
+    g = moe.MoeLayerGraph(layer.cfg, x_d, L_d, *W, y_d, ws)
 
     def run():   # router logits, then the layer graph
         moe.moe_router_logits(layer.cfg, x_d, layer.wr, layer.offset, L_d)

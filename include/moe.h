@@ -397,6 +397,9 @@ moe_status_t moe_gmm_swiglu_mapped(const moe_config_t *cfg, int32_t n_groups,
 
 /* ----------------------------------------------------------------------
  * moe_layer -- the whole layer (an extension composing the calls above).
+ *   cfg->F = 0 gives the dispatch-only layer of the routing/permute/dedup
+ *   sweep: no expert FFN, the combine reads the permuted rows back
+ *   (y[t] = sum_j w[t,j] x[t] over its kept rows); the weights may be NULL.
  *   MOE_MODE_FALLBACK_LAYER: route, check, read the flag; no overflow -> the
  *     capped path; overflow -> the chunked dropless fallback, reusing the
  *     routing [PR5920 How, moe_dropless_fallback=layer].  With
@@ -430,7 +433,7 @@ moe_status_t moe_layer(const moe_config_t *cfg, const void *x,
 
 /* ----------------------------------------------------------------------
  * moe_layer_graph_* -- the MOE_MODE_FALLBACK_LAYER layer as one CUDA graph
- * (an extension).  The branch of [PR5920 How] is a conditional IF node:
+ * (an extension; cfg->F = 0: the dispatch-only layer, as moe_layer).  The branch of [PR5920 How] is a conditional IF node:
  * the check kernel's flag selects, on the device, either the chunked
  * dropless passes or the capped pass, so a launch never waits on the host.
  * In the chunked branch each chunk's permute tables (moe_permute_tables)

@@ -225,19 +225,24 @@ cudaError_t pass(const moe_config_t& c, const void* x, const int32_t* topk_idx,
                      b.uniq_tokens, b.expand_idx, b.n_dropped, b.pws, status,
                      s, plan);
   if (e != cudaSuccess) return e;
+  const bool ffn = c.F > 0;  // F = 0: dispatch only, combine of x_sorted
   if (tr == nullptr) {
-    e = launch_gmm(c, groups, b.x_sorted, b.group_offsets, wg, wu, wd, b.h,
-                   b.y_sorted, status, s);
+    if (ffn)
+      e = launch_gmm(c, groups, b.x_sorted, b.group_offsets, wg, wu, wd, b.h,
+                     b.y_sorted, status, s);
   } else if ((e = stamp(tr, trace_slot(pass_index, 1), s)) == cudaSuccess &&
-             (e = launch_gmm1(c, groups, b.x_sorted, b.group_offsets, wg, wu,
-                              b.h, status, s)) == cudaSuccess &&
+             (!ffn || (e = launch_gmm1(c, groups, b.x_sorted,
+                                       b.group_offsets, wg, wu, b.h, status,
+                                       s)) == cudaSuccess) &&
              (e = stamp(tr, trace_slot(pass_index, 2), s)) == cudaSuccess) {
-    e = launch_gmm2(c, groups, b.h, b.group_offsets, wd, b.y_sorted, status,
-                    s);
+    if (ffn)
+      e = launch_gmm2(c, groups, b.h, b.group_offsets, wd, b.y_sorted,
+                      status, s);
   }
   if (e != cudaSuccess) return e;
   if ((e = stamp(tr, trace_slot(pass_index, 3), s)) != cudaSuccess) return e;
-  e = launch_combine(c, b.y_sorted, b.row_of, topk_w, y, s);
+  e = launch_combine(c, ffn ? b.y_sorted : b.x_sorted, b.row_of, topk_w, y,
+                     s);
   if (e != cudaSuccess) return e;
   return stamp(tr, trace_slot(pass_index, 4), s);
 }
@@ -288,14 +293,17 @@ cudaError_t pipelined_passes(const moe_config_t& c, const void* x,
              b.row_of + o * c.k, tb.uniq_offsets, b.x_sorted, tb.uniq_tokens,
              tb.expand_idx, tb.pws, s)) != cudaSuccess ||
         (e = stamp(tr, trace_slot(i, 1), s)) != cudaSuccess ||
-        (e = launch_gmm1(sc, identity_groups(sc), b.x_sorted,
-                         tb.group_offsets, wg, wu, b.h, status, s)) !=
-            cudaSuccess ||
+        (c.F > 0 &&
+         (e = launch_gmm1(sc, identity_groups(sc), b.x_sorted,
+                          tb.group_offsets, wg, wu, b.h, status, s)) !=
+             cudaSuccess) ||
         (e = stamp(tr, trace_slot(i, 2), s)) != cudaSuccess ||
-        (e = launch_gmm2(sc, identity_groups(sc), b.h, tb.group_offsets, wd,
-                         b.y_sorted, status, s)) != cudaSuccess ||
+        (c.F > 0 &&
+         (e = launch_gmm2(sc, identity_groups(sc), b.h, tb.group_offsets, wd,
+                          b.y_sorted, status, s)) != cudaSuccess) ||
         (e = stamp(tr, trace_slot(i, 3), s)) != cudaSuccess ||
-        (e = launch_combine(sc, b.y_sorted, b.row_of + o * c.k,
+        (e = launch_combine(sc, c.F > 0 ? b.y_sorted : b.x_sorted,
+                            b.row_of + o * c.k,
                             topk_w + o * c.k,
                             static_cast<char*>(y) + o * row_bytes, s)) !=
             cudaSuccess ||
@@ -325,14 +333,16 @@ cudaError_t capped_pass_tabled(const moe_config_t& c, const void* x,
                                   tb.uniq_tokens, tb.expand_idx, tb.pws, s)) !=
           cudaSuccess ||
       (e = stamp(tr, trace_slot(0, 1), s)) != cudaSuccess ||
-      (e = launch_gmm1(c, groups, b.x_sorted, tb.group_offsets, wg, wu, b.h,
-                       status, s)) != cudaSuccess ||
+      (c.F > 0 &&
+       (e = launch_gmm1(c, groups, b.x_sorted, tb.group_offsets, wg, wu, b.h,
+                        status, s)) != cudaSuccess) ||
       (e = stamp(tr, trace_slot(0, 2), s)) != cudaSuccess ||
-      (e = launch_gmm2(c, groups, b.h, tb.group_offsets, wd, b.y_sorted,
-                       status, s)) != cudaSuccess ||
+      (c.F > 0 &&
+       (e = launch_gmm2(c, groups, b.h, tb.group_offsets, wd, b.y_sorted,
+                        status, s)) != cudaSuccess) ||
       (e = stamp(tr, trace_slot(0, 3), s)) != cudaSuccess ||
-      (e = launch_combine(c, b.y_sorted, row_of, topk_w, y, s)) !=
-          cudaSuccess)
+      (e = launch_combine(c, c.F > 0 ? b.y_sorted : b.x_sorted, row_of,
+                          topk_w, y, s)) != cudaSuccess)
     return e;
   return stamp(tr, trace_slot(0, 4), s);
 }
@@ -795,8 +805,9 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x,
   if (mode != MOE_MODE_FALLBACK_LAYER && mode != MOE_MODE_CAPPED &&
       mode != MOE_MODE_DROPLESS)
     return MOE_ERR_INVALID_ARG;
-  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
-  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  // F = 0: the dispatch-only layer (no expert FFN; the combine reads the
+  // permuted rows back), the routing/permute/dedup round trip
+  if (cfg->F > 0 && !gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   const int64_t cap = capacity_rows(*cfg);
   if (info) {
     info->overflow = -1;
@@ -805,7 +816,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x,
   }
   if (cfg->T == 0) return MOE_OK;
   if (!ok_ptr(x, true) || !ok_ptr(logits, false) ||
-      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(y, true))
+      (cfg->F > 0 && !weights_ok(w_gate, w_up, w_down)) || !ok_ptr(y, true))
     return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !ok_ptr(workspace, true) ||
       workspace_bytes < layer_bytes(*cfg, cfg->T))

@@ -218,10 +218,10 @@ moe_status_t create_graph(const moe_config_t* cfg, const void* x,
   *graph_out = nullptr;
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
-  if (cfg->F < 1 || cfg->T < 1) return MOE_ERR_INVALID_ARG;
-  if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T < 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->F > 0 && !gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
   if (!ok_ptr(x, true) || !ok_ptr(logits, false) ||
-      !weights_ok(w_gate, w_up, w_down) || !ok_ptr(y, true))
+      (cfg->F > 0 && !weights_ok(w_gate, w_up, w_down)) || !ok_ptr(y, true))
     return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !ok_ptr(workspace, true) ||
       workspace_bytes < layer_bytes(*cfg, cfg->T))

@@ -120,3 +120,43 @@ def test_traced_graph_bits_and_stamps(wl):
         assert bool(flag) == (factor < 1.0)
         g.close()
         g0.close()
+
+
+@pytest.mark.parametrize("T,routing,factor", [(4096, "uniform", 2.0),
+                                              (4096, "zipf", 2.0),
+                                              (1024, "adversarial", 2.0)])
+def test_dispatch_only_layer(T, routing, factor):
+    """F = 0, the routing/permute/dedup sweep's layer: moe_layer and the
+    graph give y[t] = sum_j w[t,j] x[t] over the token's kept rows (the
+    combine of the permuted rows), bit for bit between the two, and within
+    the bf16 tolerance of that sum from the oracle's routing (no pass
+    drops a row, so it is (sum_j w[t,j]) x[t])."""
+    from oracle import moe_ref as ref
+    from synth import sweep_workload
+    from tests.gpu_util import f64
+    from tests.parity_log import assert_close
+    wl = sweep_workload(T, routing)
+    cfg = cfg_from(wl, factor=factor)
+    x, L = batch(wl, 0)
+    y = torch.zeros((wl.T, wl.H), dtype=x.dtype, device="cuda")
+    ws = moe.layer_workspace(cfg)
+    info = moe.moe_layer(cfg, x, L, None, None, None, y,
+                         moe.MOE_MODE_FALLBACK_LAYER, ws)
+    y_g = torch.zeros_like(y)
+    ws_g = moe.layer_workspace(cfg)
+    g = moe.MoeLayerGraph(cfg, x, L, None, None, None, y_g, ws_g)
+    g.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_g)
+    assert device_flag(g, ws_g) == info["overflow"]
+    Ln = L.cpu().numpy()
+    idx, w, _ = ref.route(Ln, wl.k)
+    C = ref.capacity(wl.T, wl.k, wl.S, factor)
+    over = ref.overflow_flag(ref.shard_counts(ref.expert_counts(idx, wl.E),
+                                              wl.S), C)
+    assert info["overflow"] == int(over)
+    # dispatch-only: every pass keeps its rows (the capped pass runs only
+    # when nothing overflows), so y[t] = (sum_j w[t,j]) x[t]
+    want = w.sum(axis=1, keepdims=True) * f64(x)
+    assert_close(f64(y), want, 2e-2, f"dispatch-only y ({routing})")
+    g.close()
