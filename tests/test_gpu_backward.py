@@ -374,11 +374,8 @@ def test_wgrad_pair_kernel_matches_one_cta_bitwise(dup):
     """The weight-gradient GEMMs over regrouped rows (16-row-aligned groups,
     zero pads): with MOE_WGRAD_ROWS_ALIGNED16 they run on the two-SM kernel
     (256-row tiles of dW), without it on the one-CTA kernel; both write the
-    same bits in overwrite mode (two groups of one expert add onto its zeroed
-    slice, 0 + a + b in either order) and in accumulate mode without shared
-    experts.  Accumulating two groups' tiles onto a gradient that is already
-    there depends on which tile lands first, so there the two agree within
-    float32 rounding."""
+    same bits, in overwrite and in accumulate mode, also when several groups
+    share an expert (their tiles add onto it)."""
     E, H, F, k, T = 6, 512, 256, 2, 700
     G = 8 if dup else E
     cfg = cfg_from(BWD[1], T=T, H=H, E=E, k=k, F=F, S=2)
@@ -397,7 +394,7 @@ def test_wgrad_pair_kernel_matches_one_cta_bitwise(dup):
            for n, w in (("xs", H), ("dg", F), ("du", F), ("h", F),
                         ("dys", H))}
     segs = [(off, 0)]
-    outs, firsts = [], []
+    outs = []
     for flags in (0, moe.MOE_WGRAD_ROWS_ALIGNED16):
         dw = [torch.full((E, H, F), 0.25, device="cuda"),
               torch.full((E, H, F), 0.25, device="cuda"),
@@ -408,18 +405,10 @@ def test_wgrad_pair_kernel_matches_one_cta_bitwise(dup):
                                       **kw)
             moe.moe_gmm_down_wgrad(cfg, segs, R, src["h"], src["dys"], dw[2],
                                    flags | acc, **kw)
-            if acc == 0:
-                torch.cuda.synchronize()
-                firsts.append([t.clone() for t in dw])
         torch.cuda.synchronize()
         outs.append(dw)
-    for a, b in zip(*firsts):
-        assert torch.equal(a, b)
     for a, b in zip(*outs):
-        if dup:
-            assert_close(f64(a), f64(b), 1e-6, "accumulated dW, pair vs one-CTA")
-        else:
-            assert torch.equal(a, b)
+        assert torch.equal(a, b)
     # and against x^T dg summed over each expert's groups, twice (accumulate)
     ge = [0, 1, 2, 3, 4, 5, 1, 4] if dup else list(range(E))
     xs, dg = f64(src["xs"]), f64(src["dg"])
