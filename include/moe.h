@@ -575,25 +575,14 @@ typedef struct {
   int32_t first_row;
 } moe_row_segment_t;
 
-/* Bits of the weight-gradient calls' `accumulate` argument. */
-#define MOE_WGRAD_ACCUMULATE 1     /* add into dW (else overwrite)          */
-#define MOE_WGRAD_ROWS_ALIGNED16 2 /* every group of every segment has a
-                                      multiple of 16 rows, the pad rows zero
-                                      (moe_regroup_rows's output): lets the
-                                      two-SM (CTA pair) kernel run            */
-
 /* Weight gradients summed over n_segments row ranges (a host array; e.g.
  * one per chunk of the fallback, so that an expert's gradient over all
  * chunks is accumulated on chip and written once), over the rows of
  * expert e:
  *   gate_up: dWg[e] (+)= x^T dg,  dWu[e] (+)= x^T du   ([E,H,F] float32)
  *   down:    dWd[e] (+)= h^T dy_sorted                 ([E,F,H] float32)
- * The row buffers have rows_total rows.  accumulate: MOE_WGRAD_ACCUMULATE
- * clear overwrites every expert's gradient (zeros for experts without
- * rows), set adds into it; with MOE_WGRAD_ROWS_ALIGNED16 (and H, F
- * multiples of 256) the launch takes the two-SM kernel, whose tiles of dW
- * are 256 rows (each CTA of the pair stages its 128 rows of one operand and
- * half of the other: a third fewer operand bytes per dW byte). */
+ * The row buffers have rows_total rows.  accumulate = 0 overwrites every
+ * expert's gradient (zeros for experts without rows), 1 adds into it. */
 moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t *cfg,
                                    int32_t n_groups,
                                    const int32_t *group_expert,

@@ -24,7 +24,6 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_MODE_FALLBACK_LAYER, MOE_MODE_CAPPED, MOE_MODE_DROPLESS = 0, 1, 2
 MOE_WS_PERMUTE, MOE_WS_CHUNKED, MOE_WS_LAYER = 0, 1, 2
 MOE_WS_GMM_BACKWARD, MOE_WS_LAYER_BACKWARD = 3, 4
-MOE_WGRAD_ACCUMULATE, MOE_WGRAD_ROWS_ALIGNED16 = 1, 2
 
 
 class MoeConfig(ctypes.Structure):

@@ -268,16 +268,13 @@ cudaError_t launch_gate_up_dgrad_bf16(const moe_config_t& c, const Groups& g,
                                       const void* dg, const void* du,
                                       void* dx_sorted, int32_t* status,
                                       cudaStream_t s);
-// rows_aligned16: every group of every segment has a multiple of 16 rows
-// (moe_regroup_rows's layout), which lets the two-SM kernel run.
 cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               const WgradSegment* seg, int n_seg,
                               int64_t rows_total, const void* x_sorted,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
                               float* dw_up, float* dw_down, int accumulate,
-                              int parts, int32_t* status, cudaStream_t s,
-                              bool rows_aligned16 = false);
+                              int parts, int32_t* status, cudaStream_t s);
 // Dispatch on the layer dtype (bf16: tensor cores, fp32: CUDA cores).
 cudaError_t launch_gate_up_saved(const moe_config_t& c, const Groups& g,
                                  const void* xs, const int32_t* off,
@@ -299,8 +296,7 @@ cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
                          int64_t rows_total, const void* xs, const void* dg,
                          const void* du, const void* h, const void* dys,
                          float* dwg, float* dwu, float* dwd, int accumulate,
-                         int parts, int32_t* status, cudaStream_t s,
-                         bool rows_aligned16 = false);
+                         int parts, int32_t* status, cudaStream_t s);
 // Rows of up to kMaxRegroupSegments ranges copied into one expert-major
 // layout with 16-row-aligned groups and zero pad rows (see regroup.cu);
 // destination buffers of regroup_rows(c) rows.

@@ -170,12 +170,10 @@ cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
                          int64_t rows_total, const void* xs, const void* dg,
                          const void* du, const void* h, const void* dys,
                          float* dwg, float* dwu, float* dwd, int accumulate,
-                         int parts, int32_t* status, cudaStream_t s,
-                         bool rows_aligned16) {
+                         int parts, int32_t* status, cudaStream_t s) {
   if (c.dtype == MOE_BF16)
     return launch_wgrad_bf16(c, g, seg, n_seg, rows_total, xs, dg, du, h, dys,
-                             dwg, dwu, dwd, accumulate, parts, status, s,
-                             rows_aligned16);
+                             dwg, dwu, dwd, accumulate, parts, status, s);
   return launch_wgrad_f32(c, g, seg, n_seg, xs, dg, du, h, dys, dwg, dwu, dwd,
                           accumulate, parts, s);
 }
@@ -408,7 +406,7 @@ moe_status_t check_segments(const moe_config_t* cfg,
   if (st != MOE_OK) return st;
   if (cfg->F < 1 || n_segments < 0 || rows_total < 0 ||
       rows_total > std::numeric_limits<int32_t>::max() ||
-      (accumulate & ~(MOE_WGRAD_ACCUMULATE | MOE_WGRAD_ROWS_ALIGNED16)) != 0 ||
+      (accumulate != 0 && accumulate != 1) ||
       (n_segments > 0 && segments == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
@@ -440,9 +438,7 @@ moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t* cfg, int32_t n_groups,
   return cuda_st(launch_wgrad(*cfg, grp, segments,
                               n_segments, rows_total, x_sorted, dg, du,
                               nullptr, nullptr, dw_gate, dw_up, nullptr,
-                              accumulate & MOE_WGRAD_ACCUMULATE, kWgradGateUp,
-                              status_word, stream,
-                              (accumulate & MOE_WGRAD_ROWS_ALIGNED16) != 0));
+                              accumulate, kWgradGateUp, status_word, stream));
 }
 
 moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg, int32_t n_groups,
@@ -463,9 +459,8 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t* cfg, int32_t n_groups,
   return cuda_st(launch_wgrad(*cfg, grp, segments,
                               n_segments, rows_total, nullptr, nullptr,
                               nullptr, h, dy_sorted, nullptr, nullptr,
-                              dw_down, accumulate & MOE_WGRAD_ACCUMULATE,
-                              kWgradDown, status_word, stream,
-                              (accumulate & MOE_WGRAD_ROWS_ALIGNED16) != 0));
+                              dw_down, accumulate, kWgradDown, status_word,
+                              stream));
 }
 
 moe_status_t moe_regroup_rows(const moe_config_t* cfg, int32_t n_groups,
@@ -619,7 +614,7 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
     return cuda_st(launch_wgrad(*cfg, wgroups, &one, 1, rr,
                                 b.xs2, b.dg2, b.du2, b.h2, b.dys2, dw_gate,
                                 dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
-                                status_word, stream, true));
+                                status_word, stream));
   }
   return cuda_st(launch_wgrad(
       *cfg, wgroups, segs.data(), static_cast<int>(segs.size()),

@@ -427,266 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------- two-SM weight gradients --
-// The same reduction with a CTA pair (cluster of 2, tcgen05.mma.cta_group::2)
-// sharing each M=256 x N=256 tile of dW: each CTA stages its 128 rows of the
-// tile's P columns and HALF of its Q columns (WMODE 0: the leader the dg
-// columns, the peer the du columns; WMODE 1: the first and the last 128 of
-// the 256 dW columns), so a stage carries 32 KB per CTA instead of 48 KB
-// and the operand bytes the SMs pull per dW byte they write fall from 1.5 to
-// 1.0.  The leader issues the MMAs and multicasts its commits to both CTAs;
-// both CTAs write their own 128 rows of the tile.  Only for rows that
-// moe_regroup_rows laid out (every group a multiple of 16 rows, zero pads),
-// so that no K=16 step holds rows of two groups and nothing is cleared.
-constexpr int W2STAGES = 4;
-constexpr int kW2A = BM * BK * 2;                 // this CTA's 128 P columns
-constexpr int kW2B = BK * 128 * 2;                // this CTA's half of Q
-constexpr int kW2Stage = kW2A + kW2B;             // 32 KB
-constexpr uint32_t kW2Tx = 2 * kW2Stage;          // both CTAs, one stage
-
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst,
-                                                      const CUtensorMap* m,
-                                                      uint32_t bar_cluster,
-                                                      int c0, int c1,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
-      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], "
-      "[%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0),
-      "r"(c1), "l"(policy)
-      : "memory");
-}
-
-template <int WMODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tmP,
-                     const __grid_constant__ CUtensorMap tmQ0,
-                     const __grid_constant__ CUtensorMap tmQ1,
-                     const __grid_constant__ CUtensorMap tmO0,
-                     const __grid_constant__ CUtensorMap tmO1, WParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stagebuf = smem + W2STAGES * kW2Stage;  // [4][kStageBufs][4 KB]
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(stagebuf + 4 * kStageBufs * kStageBuf);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + W2STAGES;
-  uint64_t* tfull = bars + 2 * W2STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
-  int* tpre = wsum + 16;                               // [G+1]
-  int* ecnt = tpre + (p.G + 1);                        // [E]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();  // 0: leader, 1: peer
-  const uint32_t smem_base = smem_u32(smem);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < W2STAGES; ++s) {
-      mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_u32(tfull + a), 1);
-      mbar_init(smem_u32(tempty + a), 2 * kEpilogueThreads);
-    }
-    mbar_init(smem_u32(done), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    fence_proxy_async_smem();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmP);
-    prefetch_tmap(&tmQ0);
-    if (WMODE == 0) prefetch_tmap(&tmQ1);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish_pair();
-  }
-  build_wgrad_table(p, tpre, wsum);
-  for (int e = threadIdx.x; e < p.E; e += blockDim.x) ecnt[e] = 0;
-  __syncthreads();
-  if (p.group_expert != nullptr)
-    for (int g = threadIdx.x; g < p.G; g += blockDim.x)
-      if (tpre[g + 1] > tpre[g]) atomicAdd(&ecnt[__ldg(p.group_expert + g)], 1);
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // both CTAs' barriers exist before either signals them
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = tpre[p.G];
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-
-  if (warp == 0) {
-    // ---------------------------------------- TMA producer (both CTAs) ---
-    if (lane == 0) {
-      const uint64_t keep = policy_evict_last();
-      const CUtensorMap* mq = (WMODE == 0 && rank == 1) ? &tmQ1 : &tmQ0;
-      int stage = 0;
-      uint32_t phase = 0;
-      long long fills = 0;
-      bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
-        const int g = group_of(tpre, p.G, tile);
-        const int local = tile - tpre[g];
-        const int n = local % p.n_tiles, m = local / p.n_tiles;
-        const int pcol = m * 2 * BM + static_cast<int>(rank) * BM;
-        const int qcol = WMODE == 0 ? n * 128 : n * 256 + rank * 128;
-        for (int sg = 0; ok && sg < p.n_seg; ++sg) {
-          const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
-          for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
-               r += BK) {
-            if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
-                           p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb = map_to_rank(smem_u32(full + stage), 0);
-            if (rank == 0) mbar_expect_tx(smem_u32(full + stage), kW2Tx);
-            const uint32_t sa = smem_base + stage * kW2Stage;
-            const uint32_t sb = sa + kW2A;
-            tma_load_2d_pair_hint(sa, &tmP, fb, pcol, r, keep);
-            tma_load_2d_pair_hint(sa + 8192, &tmP, fb, pcol + 64, r, keep);
-            tma_load_2d_pair_hint(sb, mq, fb, qcol, r, keep);
-            tma_load_2d_pair_hint(sb + 8192, mq, fb, qcol + 64, r, keep);
-            ++fills;
-            if (++stage == W2STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-      }
-      if (rank == 0) {  // the leader's full barriers count both CTAs' bytes
-        const long long first = fills > W2STAGES ? fills - W2STAGES : 0;
-        for (long long f = first; f < fills; ++f)
-          mbar_wait(smem_u32(full + (f % W2STAGES)),
-                    static_cast<uint32_t>((f / W2STAGES) & 1), nullptr,
-                    p.status);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------- MMA issuer (leader) ------
-    if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = make_idesc(2 * BM, 256, true, true);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
-        const int g = group_of(tpre, p.G, tile);
-        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag,
-                       p.status))
-          break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + acc * kAccCols;
-        bool first = true;
-        for (int sg = 0; ok && sg < p.n_seg; ++sg) {
-          const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
-          for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
-               r += BK) {
-            if (!mbar_wait(smem_u32(full + stage), phase, abort_flag,
-                           p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_base + stage * kW2Stage;
-            const uint32_t sb = sa + kW2A;
-            // whole K=16 steps only: the groups are 16-row aligned
-            const int steps = min(BK, r1 - r) >> 4;
-            for (int kk = 0; kk < steps; ++kk) {
-              const uint64_t ad = smem_desc(sa + kk * 2048, 8192, 1024);
-              const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
-              umma_bf16_pair(d, ad, bd, idesc,
-                             (!first || kk != 0) ? 1u : 0u);
-            }
-            umma_commit_pair_mc(smem_u32(empty + stage));
-            first = false;
-            if (++stage == W2STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        if (!ok) break;
-        umma_commit_pair_mc(smem_u32(tfull + acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      umma_commit_pair(smem_u32(done));
-      mbar_wait(smem_u32(done), 0, nullptr, p.status);
-    }
-  } else {
-    // ---------------------------------------- epilogue (both CTAs) -----
-    const int q = warp & 3;
-    uint8_t* mybuf = stagebuf + q * kStageBufs * kStageBuf;
-    const uint64_t stream = policy_evict_first();
-    int acc = 0, nsub = 0;
-    uint32_t acc_phase = 0;
-    for (int tile = pair; tile < total_tiles; tile += npairs) {
-      const int g = group_of(tpre, p.G, tile);
-      const int local = tile - tpre[g];
-      const int n = local % p.n_tiles, m = local / p.n_tiles;
-      const int we = p.group_expert ? __ldg(p.group_expert + g) : g;
-      bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
-                          p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      const int orow = we * p.m_tiles * 2 * BM + m * 2 * BM +
-                       static_cast<int>(rank) * BM + q * 32;
-      const bool add = p.reduce || (p.group_expert != nullptr && ecnt[we] > 1);
-#pragma unroll 1
-      for (int sub = 0; sub < 8; ++sub, ++nsub) {
-        uint32_t r[32];
-        tmem_ld32(taddr + sub * 32, r);
-        uint8_t* buf = mybuf + (nsub % kStageBufs) * kStageBuf;
-        if (lane == 0) bulk_wait_read_free();
-        __syncwarp();
-        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          row[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1],
-                                           r[4 * j + 2], r[4 * j + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const CUtensorMap* om = &tmO0;
-          int col = n * 256 + sub * 32;
-          if (WMODE == 0) {
-            om = sub < 4 ? &tmO0 : &tmO1;
-            col = n * 128 + (sub & 3) * 32;
-          }
-          if (add)
-            tma_reduce_add_2d(om, smem_u32(buf), col, orow, stream);
-          else
-            tma_store_2d(om, smem_u32(buf), col, orow, stream);
-          bulk_commit();
-        }
-      }
-      tc_fence_before();
-      mbar_arrive_cluster(map_to_rank(smem_u32(tempty + acc), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // neither CTA leaves while its peer may still use it
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
-  }
-}
-
 // Store mode: zeroes dW[e] of every expert that does not have exactly one
 // group with rows -- none (no tile writes it) or several (its tiles add onto
 // it).  Grid (E, blocks), 16-byte stores.
@@ -716,31 +456,6 @@ size_t smem_bytes_wgrad(int G, int E) {
   return 1024 + WSTAGES * kWStage + 4 * kStageBufs * kStageBuf +
          8 * (2 * WSTAGES + 5) +
          16 + 4 * (16 + G + 1 + E) + 64;
-}
-
-size_t smem_bytes_wgrad_pair(int G, int E) {
-  return 1024 + W2STAGES * kW2Stage + 4 * kStageBufs * kStageBuf +
-         8 * (2 * W2STAGES + 5) + 16 + 4 * (16 + G + 1 + E) + 64;
-}
-
-template <int WMODE>
-cudaError_t launch_wgrad_pair(const CUtensorMap& pm, const CUtensorMap& q0,
-                              const CUtensorMap& q1, const CUtensorMap& o0,
-                              const CUtensorMap& o1, const WParams& p,
-                              cudaStream_t s) {
-  const size_t smem = smem_bytes_wgrad_pair(p.G, p.E);
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(wgrad_tc2_kernel<WMODE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  wgrad_tc2_kernel<WMODE><<<sms & ~1, kThreads, smem, s>>>(pm, q0, q1, o0,
-                                                            o1, p);
-  return cudaGetLastError();
 }
 
 template <int WMODE, int BN>
@@ -774,8 +489,7 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
                               float* dw_up, float* dw_down, int accumulate,
-                              int parts, int32_t* status, cudaStream_t s,
-                              bool rows_aligned16) {
+                              int parts, int32_t* status, cudaStream_t s) {
   const bool gu = (parts & kWgradGateUp) != 0;
   const bool dn = (parts & kWgradDown) != 0;
   const uint64_t E = static_cast<uint64_t>(c.E);
@@ -819,22 +533,17 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (p.n_seg == 0) break;
-    // the two-SM kernel: 256-row tiles of dW, 16-row-aligned groups
-    const bool pair_gu = rows_aligned16 && c.H % 256 == 0;
-    const bool pair_dn = rows_aligned16 && c.F % 256 == 0 && c.H % 256 == 0;
     if (gu) {
-      p.m_tiles = c.H / (pair_gu ? 2 * tc::BM : tc::BM);
+      p.m_tiles = c.H / tc::BM;
       p.n_tiles = c.F / 128;
-      e = pair_gu ? tc::launch_wgrad_pair<0>(px, qg, qu, og, ou, p, s)
-                  : tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
+      e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
       if (e != cudaSuccess) return e;
     }
     if (dn) {
-      p.m_tiles = c.F / (pair_dn ? 2 * tc::BM : tc::BM);
+      p.m_tiles = c.F / tc::BM;
       p.n_tiles = c.H / bnd;
-      e = pair_dn ? tc::launch_wgrad_pair<1>(ph, qd, qd, od, od, p, s)
-          : bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
-                       : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
+      e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
+                     : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
       if (e != cudaSuccess) return e;
     }
   }

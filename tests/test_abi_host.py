@@ -198,16 +198,13 @@ def test_backward_arguments_are_rejected_before_any_launch(m):
     # a group map without its group count
     assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, p, seg, 1, rows, p, p,
                                   p, 0, None, None) == m.MOE_ERR_INVALID_ARG
-    # weight gradients: a negative range start, accumulate with a bit other
-    # than MOE_WGRAD_ACCUMULATE | MOE_WGRAD_ROWS_ALIGNED16
+    # weight gradients: a negative range start, accumulate not 0/1
     seg[0].first_row = -1
     assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 0,
                                   None, None) == m.MOE_ERR_INVALID_ARG
     seg[0].first_row = 0
-    for bad in (4, 5, -1):
-        assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p,
-                                      p, p, bad, None,
-                                      None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 2,
+                                  None, None) == m.MOE_ERR_INVALID_ARG
     # layer backward: no workspace
     info = m.MoeLayerInfo()
     assert lib.moe_layer_backward(ctypes.byref(c), p, p, p, p, p, p, p, p, p,

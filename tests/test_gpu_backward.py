@@ -367,56 +367,3 @@ def test_layer_backward_redundant_capped(wl):
     g = ref.layer_pass_backward(mc, f64(x), L, *[f64(w) for w in W], f64(dy),
                                 C, groups=(vidx, G, plan.group_expert))
     compare(out, g, TOL[wl.dtype])
-
-
-@pytest.mark.parametrize("dup", [False, True], ids=["experts", "dup_slots"])
-def test_wgrad_pair_kernel_matches_one_cta_bitwise(dup):
-    """The weight-gradient GEMMs over regrouped rows (16-row-aligned groups,
-    zero pads): with MOE_WGRAD_ROWS_ALIGNED16 they run on the two-SM kernel
-    (256-row tiles of dW), without it on the one-CTA kernel; both write the
-    same bits, in overwrite and in accumulate mode, also when several groups
-    share an expert (their tiles add onto it)."""
-    E, H, F, k, T = 6, 512, 256, 2, 700
-    G = 8 if dup else E
-    cfg = cfg_from(BWD[1], T=T, H=H, E=E, k=k, F=F, S=2)
-    rng = np.random.default_rng(11)
-    cnt = rng.integers(1, 14, size=G) * 16
-    cnt[2] = 0
-    off = torch.from_numpy(np.concatenate([[0], np.cumsum(cnt)]).astype(
-        np.int32)).cuda()
-    R = int(cnt.sum())
-    assert R <= T * k
-    kw = {}
-    if dup:
-        kw = dict(n_groups=G, group_expert=torch.tensor(
-            [0, 1, 2, 3, 4, 5, 1, 4], dtype=torch.int32, device="cuda"))
-    src = {n: (torch.randn((R, w), device="cuda") * 0.5).to(torch.bfloat16)
-           for n, w in (("xs", H), ("dg", F), ("du", F), ("h", F),
-                        ("dys", H))}
-    segs = [(off, 0)]
-    outs = []
-    for flags in (0, moe.MOE_WGRAD_ROWS_ALIGNED16):
-        dw = [torch.full((E, H, F), 0.25, device="cuda"),
-              torch.full((E, H, F), 0.25, device="cuda"),
-              torch.full((E, F, H), 0.25, device="cuda")]
-        for acc in (0, moe.MOE_WGRAD_ACCUMULATE):
-            moe.moe_gmm_gate_up_wgrad(cfg, segs, R, src["xs"], src["dg"],
-                                      src["du"], dw[0], dw[1], flags | acc,
-                                      **kw)
-            moe.moe_gmm_down_wgrad(cfg, segs, R, src["h"], src["dys"], dw[2],
-                                   flags | acc, **kw)
-        torch.cuda.synchronize()
-        outs.append(dw)
-    for a, b in zip(*outs):
-        assert torch.equal(a, b)
-    # and against x^T dg summed over each expert's groups, twice (accumulate)
-    ge = [0, 1, 2, 3, 4, 5, 1, 4] if dup else list(range(E))
-    xs, dg = f64(src["xs"]), f64(src["dg"])
-    o = np_(off)
-    for e in range(E):
-        want = np.zeros((H, F))
-        for g in range(G):
-            if ge[g] == e:
-                want += xs[o[g]:o[g + 1]].T @ dg[o[g]:o[g + 1]]
-        assert_close(f64(outs[1][0][e]), 2 * want, 1e-4,
-                     f"dWg expert {e} (two launches)")
