@@ -204,3 +204,38 @@ def test_ep_sum_partials():
         want = f64(parts).sum(0)
         assert_close(f64(y), want, TOL["bf16" if dt == torch.bfloat16
                                         else "f32"], f"sum of parts {dt}")
+
+
+def test_ep_dsv3_full_size_8_ranks():
+    """The DeepSeek-V3-shaped layer's 8192-token batch split over 8 logical
+    EP ranks of 1024 tokens (32 experts each): the global check overflows
+    (4 chunks per rank), and the outputs match moe_layer on the whole batch
+    within the tolerance, and the oracle on sampled tokens."""
+    wl = WORKLOADS["dsv3"]
+    N, T_r = 8, 1024
+    x_all = make_x(wl, "cuda")
+    L_all = host_logits(wl, x_all)
+    xs = [x_all[r * T_r:(r + 1) * T_r] for r in range(N)]
+    Ls = [np.ascontiguousarray(L_all[r * T_r:(r + 1) * T_r])
+          for r in range(N)]
+    W = make_weights(wl, "cuda")
+    cfg = moe.make_config(wl.T, wl.H, wl.E, wl.k, wl.F, N, wl.factor, 0,
+                          wl.dtype)
+    layer = ep.EPLayer(cfg, ep.LoopbackTransport(N), ep.local_weights(*W, N))
+    ys = layer.forward(xs, [torch.from_numpy(L).cuda() for L in Ls])
+    y1 = torch.empty_like(x_all)
+    info = moe.moe_layer(cfg, x_all, torch.from_numpy(L_all).cuda(), *W, y1,
+                         moe.MOE_MODE_FALLBACK_LAYER, moe.layer_workspace(cfg))
+    torch.cuda.synchronize()
+    assert layer.info["overflow"] == info["overflow"] == 1
+    assert layer.info["n_chunks"] == info["n_chunks"] == 4
+    y_ep = torch.cat(ys)
+    assert_close(f64(y_ep), f64(y1), 2e-2, "EP (8 ranks) vs moe_layer, dsv3")
+    toks = np.sort(np.random.default_rng(4).choice(wl.T, 8, replace=False))
+    oi, ow, _ = ref.route(L_all[toks], wl.k)
+    ti = torch.from_numpy(toks).cuda()
+    from tests.gpu_util import expert_accessor
+    want = ref.token_outputs(f64(x_all[ti]), oi, ow, expert_accessor(*W))
+    assert_close(f64(y_ep[ti]), want, 2e-2, "EP dsv3 sampled tokens")
+    del W, x_all
+    torch.cuda.empty_cache()
