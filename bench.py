@@ -1067,6 +1067,8 @@ def config_runs(args, device, flush, head):
             rec["gmm_TFLOPs"] = round(fl, 1)
             rec["gmm_tensor_frac_of_burst"] = round(
                 fl / peaks["bf16_tflops"], 4)
+            rec["gmm_tensor_frac_of_sustained"] = round(
+                fl / peaks["bf16_tflops_sustained"], 4)
         rec["permute_frac"] = res.get("permute_frac")
         rec["combine_frac"] = res.get("combine_frac")
         if "check_us" in res:
