@@ -1060,3 +1060,67 @@ def ring_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
         out.append(total[t0:t0 + T_r])
         t0 += T_r
     return out
+
+
+# ---------------------------------------------------------------------------
+# Ring of experts, backward.  [PR4969 What]: the combine's reduce-scatter has
+# the all-gather of the output cotangent as its transpose (the pages run it
+# as a ring all-gather kernel, numerically a plain all-gather), and the
+# forward's all-gather of the tokens has a reduce-scatter of the token
+# gradients as its transpose.  READING: rank d differentiates its own
+# experts' pass over all tokens with the gathered cotangent; each token's
+# owner adds the ranks' partial dx, takes the gradient of each pick's
+# combine weight from the rank that owns the pick, and runs the router's
+# backward on its own logits.  Weight gradients stay with the experts'
+# rank.
+# ---------------------------------------------------------------------------
+def ring_layer_backward(cfg: MoEConfig, N: int, xs: list, logits: list,
+                        weights: ExpertWeights, dys: list):
+    """Returns (dxs, dlogits) per rank and (dWg, dWu, dWd) [E, ...] (zero
+    for experts without rows)."""
+    E, k, H = cfg.E, cfg.k, cfg.H
+    Ed = E // N
+    Ts = [np.asarray(x).shape[0] for x in xs]
+    x_all = np.concatenate([np.asarray(x, dtype=np.float64) for x in xs]
+                           + [np.zeros((0, H))])
+    dy_all = np.concatenate([np.asarray(d, dtype=np.float64) for d in dys]
+                            + [np.zeros((0, H))])   # cotangent all-gather
+    routes = [route(L, k, cfg.renorm)[:2] for L in logits]
+    idx_all = np.concatenate([r[0] for r in routes]
+                             + [np.zeros((0, k), dtype=INT)])
+    w_all = np.concatenate([r[1] for r in routes] + [np.zeros((0, k))])
+    T_all = x_all.shape[0]
+    wg0, wu0, wd0 = weights(0)
+    F = np.shape(wg0)[1]
+    dwg, dwu, dwd = np.zeros((E, H, F)), np.zeros((E, H, F)), \
+        np.zeros((E, F, H))
+    dx_all = np.zeros((T_all, H))
+    dtw_all = np.zeros((T_all, k))
+    for d in range(N):
+        part = np.zeros((T_all, H))       # rank d's dx for every token
+        for el in range(Ed):
+            e = d * Ed + el
+            picks = [(t, j) for t in range(T_all) for j in range(k)
+                     if int(idx_all[t, j]) == e]
+            if not picks:
+                continue
+            rows = [t for t, _ in picks]
+            _, y = expert_ffn(x_all[rows], *weights(e))
+            dy_rows = np.zeros((len(picks), H))
+            for q, (t, j) in enumerate(picks):
+                dtw_all[t, j] = float(dy_all[t] @ y[q])
+                dy_rows[q] = w_all[t, j] * dy_all[t]
+            dx_rows, (a, b, c) = expert_ffn_backward(x_all[rows], dy_rows,
+                                                     *weights(e))
+            dwg[e], dwu[e], dwd[e] = a, b, c
+            for q, t in enumerate(rows):
+                part[t] += dx_rows[q]
+        dx_all += part                    # reduce-scatter: summed over d
+    dxs, dls, t0 = [], [], 0
+    for r, T_r in enumerate(Ts):
+        dxs.append(dx_all[t0:t0 + T_r])
+        dls.append(route_backward(logits[r], routes[r][0],
+                                  dtw_all[t0:t0 + T_r], cfg.renorm)
+                   if T_r else np.zeros((0, E)))
+        t0 += T_r
+    return dxs, dls, (dwg, dwu, dwd)

@@ -849,4 +849,36 @@ def pin_ring_layer_equals_dropless():
                                atol=1e-10)
 
 
+def pin_ring_backward_equals_dropless_backward():
+    """The ring's backward (cotangent all-gather, each rank's experts
+    differentiated over all tokens, partial dx summed at the owners, pick
+    gradients taken from the experts' ranks) gives the dropless layer's
+    gradients on the ranks' batches together -- whose backward is pinned by
+    finite differences -- with both routings (softmax over all experts or
+    renormalised over the k picks)."""
+    rng = _rng(35)
+    for i in range(16):
+        N = int(rng.choice([2, 4]))
+        E = N * int(rng.choice([1, 2]))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        Ts = [int(rng.integers(0, 8)) for _ in range(N)]
+        xs, Ls, w = _ep_case(rng, N, Ts, E, k)
+        dys = [rng.standard_normal((T_r, 3)) for T_r in Ts]
+        cfg = ref.MoEConfig(sum(Ts), 3, E, k, 4, N, 2.0, renorm=bool(i % 2))
+        dxs, dls, dW = ref.ring_layer_backward(cfg, N, xs, Ls,
+                                               ref.dense_weights(*w), dys)
+        for r in range(N):
+            assert dxs[r].shape == (Ts[r], 3) and dls[r].shape == (Ts[r], E)
+        if not sum(Ts):
+            assert all(not np.any(a) for a in dW)
+            continue
+        g = ref.layer_backward_dropless(cfg, np.concatenate(xs),
+                                        np.concatenate(Ls), *w,
+                                        np.concatenate(dys))
+        for got, want in ((np.concatenate(dxs), g.dx),
+                          (np.concatenate(dls), g.dlogits),
+                          (dW[0], g.dwg), (dW[1], g.dwu), (dW[2], g.dwd)):
+            assert np.allclose(got, want, rtol=1e-10, atol=1e-10)
+
+
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]

@@ -118,6 +118,12 @@ MUTANTS = {
     "duplicate_dw_not_summed": (
         "        dW[e] = dWe if e not in dW else tuple(",
         "        dW[e] = dWe if True else tuple("),
+    "ring_bwd_partials_not_summed": (
+        "        dx_all += part ",
+        "        dx_all = part "),
+    "ring_bwd_cotangent_unweighted": (
+        "                dy_rows[q] = w_all[t, j] * dy_all[t]",
+        "                dy_rows[q] = dy_all[t]"),
     "slot_uses_group_weights": (
         "        wg, wu, wd = weights(grp if gexp is None else int(gexp[grp]))",
         "        wg, wu, wd = weights(grp % cfg.E)"),
