@@ -722,6 +722,21 @@ moe_status_t moe_ep_localize(const moe_config_t *cfg, const int32_t *topk_idx,
                              int32_t n_local, int32_t *local_idx,
                              float *local_w, moe_stream_t stream);
 
+/* moe_ep_delocalize -- the ring variant's backward ("MoE ring-of-experts
+ * ...", pull request 4969, section What: the backward of the combine's
+ * reduce-scatter and of the tokens' all-gather): the transpose of
+ * moe_ep_localize.  For each token t, the q-th pick of t in [first_expert,
+ * first_expert + n_local) (pick order) gets v[t, j] = local_v[t, q]
+ * (local_v [T, kk] float32, kk = min(k, n_local)); v [T, k] float32 keeps
+ * its value at every other pick, so the N ranks' calls together fill every
+ * pick once.  Used for the gradient of the combine weights, which each pick
+ * receives from the rank that owns its expert.  Errors: expert range
+ * outside [0, E), pointers not 4-byte aligned. */
+moe_status_t moe_ep_delocalize(const moe_config_t *cfg,
+                               const int32_t *topk_idx, int32_t first_expert,
+                               int32_t n_local, const float *local_v,
+                               float *v, moe_stream_t stream);
+
 /* moe_ep_sum_partials -- the ring variant's reduce: y [T, H] = sum over
  * q < n_parts of parts[q] ([n_parts, T, H], layer dtype), accumulated in
  * float32 in part order and rounded once. */

@@ -28,7 +28,9 @@
 //   ep_localize    (ring) the picks a rank owns, as local expert indices,
 //                  in min(k, experts of the rank) slots;
 //   ep_sum_parts   (ring) y[t] = sum over ranks of their partial outputs,
-//                  accumulated in fp32 in rank order.
+//                  accumulated in fp32 in rank order;
+//   ep_delocalize  (ring backward) the transpose of ep_localize: a rank's
+//                  per-slot values written back at the picks it owns.
 // A receiving rank runs the ordinary permute / GEMMs / combine on the rows
 // it received, with cfg.E = its local experts and cfg.k = min(k, E/S) slots
 // per row in which -1 marks an empty slot.
@@ -130,6 +132,23 @@ __global__ void ep_localize_kernel(const int32_t* __restrict__ topk_idx,
   for (; q < kk; ++q) {
     li[q] = -1;
     lw[q] = 0.0f;
+  }
+}
+
+// One thread per token: the q-th pick of t in [e0, e0 + n_local) (pick
+// order) receives slot q of local_v; the other picks are left as they are.
+__global__ void ep_delocalize_kernel(const int32_t* __restrict__ topk_idx,
+                                     const float* __restrict__ local_v, int T,
+                                     int k, int kk, int e0, int n_local,
+                                     float* __restrict__ v) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const long long o = static_cast<long long>(t) * k;
+  const float* lv = local_v + static_cast<long long>(t) * kk;
+  int q = 0;
+  for (int j = 0; j < k && q < kk; ++j) {
+    const int e = __ldg(topk_idx + o + j);
+    if (e >= e0 && e < e0 + n_local) v[o + j] = __ldg(lv + q++);
   }
 }
 
@@ -265,6 +284,22 @@ moe_status_t moe_ep_localize(const moe_config_t* cfg,
   ep_localize_kernel<<<(cfg->T + 255) / 256, 256, 0, stream>>>(
       topk_idx, topk_w, cfg->T, cfg->k, std::min(cfg->k, n_local),
       first_expert, n_local, local_idx, local_w);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_ep_delocalize(const moe_config_t* cfg,
+                               const int32_t* topk_idx, int32_t first_expert,
+                               int32_t n_local, const float* local_v,
+                               float* v, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (first_expert < 0 || n_local < 1 || first_expert + n_local > cfg->E)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (!al4(topk_idx) || !al4(local_v) || !al4(v)) return MOE_ERR_INVALID_ARG;
+  ep_delocalize_kernel<<<(cfg->T + 255) / 256, 256, 0, stream>>>(
+      topk_idx, local_v, cfg->T, cfg->k, std::min(cfg->k, n_local),
+      first_expert, n_local, v);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -32,11 +32,14 @@ from __future__ import annotations
 import torch
 
 from . import (alloc_step_buffers, make_config, moe_check_overflow,
-               moe_combine, moe_ep_check, moe_ep_dispatch_pack,
-               moe_ep_localize, moe_ep_return_map, moe_ep_sum_partials,
-               moe_gmm_down, moe_gmm_gate_up, moe_num_chunks, moe_permute,
-               moe_permute_backward, moe_permute_scatter, moe_permute_tables,
-               moe_route, moe_workspace_bytes, MOE_WS_PERMUTE)
+               moe_combine, moe_combine_backward, moe_ep_check,
+               moe_ep_delocalize, moe_ep_dispatch_pack, moe_ep_localize,
+               moe_ep_return_map, moe_ep_sum_partials, moe_gmm_down,
+               moe_gmm_gate_up, moe_gmm_swiglu_backward, moe_gmm_swiglu_saved,
+               moe_num_chunks, moe_permute, moe_permute_backward,
+               moe_permute_scatter, moe_permute_tables, moe_route,
+               moe_route_backward, moe_workspace_bytes, MOE_WS_GMM_BACKWARD,
+               MOE_WS_PERMUTE)
 
 
 # ------------------------------------------------------------ transports --
@@ -251,62 +254,159 @@ class EPLayer:
 class RingLayer:
     """The ring-of-experts variant (dropless): every rank sees all tokens,
     computes its own experts' weighted outputs, and each token's owner adds
-    the ranks' partial outputs."""
+    the ranks' partial outputs.
 
-    def __init__(self, cfg, transport, weights):
+    backward() differentiates it ("MoE ring-of-experts ...", pull request
+    4969, section What): the output cotangents are all-gathered (the
+    transpose of the combine's reduce-scatter), each rank runs the backward
+    of its experts' pass over all tokens, and the owners add the ranks'
+    partial token gradients (the transpose of the tokens' all-gather) and
+    collect each pick's combine-weight gradient from the rank that owns its
+    expert.  With save_x_sorted (the pages' moe_x_sorted=device) the forward
+    keeps each rank's gathered, expert-sorted rows and routing, and the
+    backward reuses them instead of gathering and sorting again."""
+
+    def __init__(self, cfg, transport, weights, save_x_sorted=False):
         if cfg.E % cfg.S or transport.n != cfg.S:
             raise ValueError("cfg.S must equal the ranks and divide E")
         self.cfg = cfg
         self.tr = transport
         self.weights = weights
+        self.save_x_sorted = save_x_sorted
+        self.saved = None
 
-    def forward(self, xs, logits):
+    def _gather(self, ranks):
+        """All-gather of the tokens and their routing; each rank then keeps
+        its own picks and sorts the rows by its experts."""
         cfg, tr = self.cfg, self.tr
-        E, S, k, H = cfg.E, cfg.S, cfg.k, cfg.H
-        El = E // S
-        kk = min(k, El)
-        dev = xs[0].device
-        ranks = [_Rank(r, x, L, cfg, dev)
-                 for r, x, L in zip(tr.ranks, xs, logits)]
-        # all-gather of the tokens and their routing
+        S, El = cfg.S, cfg.E // cfg.S
+        kk = min(cfg.k, El)
         gx = tr.all_to_all([[rk.x] * S for rk in ranks])
         gi = tr.all_to_all([[rk.idx] * S for rk in ranks])
         gw = tr.all_to_all([[rk.w] * S for rk in ranks])
-        backs = []
+        states = []
         for j, rk in enumerate(ranks):
+            dev = rk.x.device
             sizes = [blk.shape[0] for blk in gx[j]]
-            T_all = sum(sizes)
-            part = torch.empty((T_all, H), dtype=rk.x.dtype, device=dev)
-            if T_all:
-                xa, ia, wa = torch.cat(gx[j]), torch.cat(gi[j]), \
-                    torch.cat(gw[j])
-                ac = _cfg(cfg, T=T_all)
-                li = torch.empty((T_all, kk), dtype=torch.int32, device=dev)
-                lw = torch.empty((T_all, kk), dtype=torch.float32, device=dev)
-                moe_ep_localize(ac, ia, wa, rk.rank * El, El, li, lw)
-                rc = _cfg(cfg, T=T_all, E=El, k=kk, S=1,
-                          ragged_buffer_factor=-1.0, n_chunks=0,
-                          redundant_slots=0)
-                rb = alloc_step_buffers(rc, dev)
-                moe_permute(rc, xa, li, False, rb["x_sorted"], rb["row_of"],
-                            rb["sorted_token"], rb["group_offsets"],
-                            rb["uniq_offsets"], rb["uniq_tokens"],
-                            rb["expand_idx"], rb["n_dropped"],
-                            rb["permute_ws"])
+            st = {"sizes": sizes, "T_all": sum(sizes)}
+            states.append(st)
+            if not st["T_all"]:
+                continue
+            T_all = st["T_all"]
+            xa, ia, wa = torch.cat(gx[j]), torch.cat(gi[j]), torch.cat(gw[j])
+            li = torch.empty((T_all, kk), dtype=torch.int32, device=dev)
+            lw = torch.empty((T_all, kk), dtype=torch.float32, device=dev)
+            moe_ep_localize(_cfg(cfg, T=T_all), ia, wa, rk.rank * El, El, li,
+                            lw)
+            rc = _cfg(cfg, T=T_all, E=El, k=kk, S=1,
+                      ragged_buffer_factor=-1.0, n_chunks=0,
+                      redundant_slots=0)
+            rb = alloc_step_buffers(rc, dev)
+            moe_permute(rc, xa, li, False, rb["x_sorted"], rb["row_of"],
+                        rb["sorted_token"], rb["group_offsets"],
+                        rb["uniq_offsets"], rb["uniq_tokens"],
+                        rb["expand_idx"], rb["n_dropped"], rb["permute_ws"])
+            st.update(li=li, lw=lw, rc=rc, rb=rb)
+        return states
+
+    def forward(self, xs, logits):
+        cfg, tr = self.cfg, self.tr
+        S, H = cfg.S, cfg.H
+        dev = xs[0].device
+        ranks = [_Rank(r, x, L, cfg, dev)
+                 for r, x, L in zip(tr.ranks, xs, logits)]
+        states = self._gather(ranks)
+        backs = []
+        for rk, st in zip(ranks, states):
+            part = torch.empty((st["T_all"], H), dtype=rk.x.dtype, device=dev)
+            if st["T_all"]:
+                rc, rb = st["rc"], st["rb"]
                 wg, wu, wd = self.weights(rk.rank)
                 moe_gmm_gate_up(rc, rb["x_sorted"], rb["group_offsets"], wg,
                                 wu, rb["h"], rb["status"])
                 moe_gmm_down(rc, rb["h"], rb["group_offsets"], wd,
                              rb["y_sorted"], rb["status"])
-                moe_combine(rc, rb["y_sorted"], rb["row_of"], lw, part)
-            backs.append(list(torch.split(part, sizes)))
+                moe_combine(rc, rb["y_sorted"], rb["row_of"], st["lw"], part)
+            backs.append(list(torch.split(part, st["sizes"])))
         # reduce-scatter: each owner receives the ranks' partial rows of its
         # tokens and adds them in rank order
         ret = tr.all_to_all(backs)
         for rk, blocks in zip(ranks, ret):
             if rk.T:
                 moe_ep_sum_partials(rk.cfg, S, torch.cat(blocks), rk.y)
+        self.saved = (ranks, states) if self.save_x_sorted else None
         return [rk.y for rk in ranks]
+
+    def backward(self, xs, logits, dys):
+        """Gradients of sum_r <dys[r], forward(xs, logits)[r]>: per rank
+        (dx [T_r, H] layer dtype, dlogits [T_r, E] float32, (dWg, dWu, dWd)
+        float32 of its own experts)."""
+        cfg, tr = self.cfg, self.tr
+        S, H, E, F = cfg.S, cfg.H, cfg.E, cfg.F
+        El = E // S
+        dev = xs[0].device
+        if self.saved is not None:
+            ranks, states = self.saved
+            self.saved = None
+        else:                       # remat: gather and sort again
+            ranks = [_Rank(r, x, L, cfg, dev)
+                     for r, x, L in zip(tr.ranks, xs, logits)]
+            states = self._gather(ranks)
+        f32 = dict(dtype=torch.float32, device=dev)
+        # the cotangent all-gather
+        gdy = tr.all_to_all([[dy] * S for dy in dys])
+        dx_back, dw_back, dWs = [], [], []
+        for j, (rk, st) in enumerate(zip(ranks, states)):
+            T_all = st["T_all"]
+            dwg = torch.zeros((El, H, F), **f32)
+            dwu = torch.zeros((El, H, F), **f32)
+            dwd = torch.zeros((El, F, H), **f32)
+            dWs.append((dwg, dwu, dwd))
+            part = torch.empty((T_all, H), dtype=rk.x.dtype, device=dev)
+            kk = min(cfg.k, El)
+            dlw = torch.zeros((T_all, kk), **f32)
+            if T_all:
+                rc, rb = st["rc"], st["rb"]
+                R = rc.T * rc.k
+                wg, wu, wd = self.weights(rk.rank)
+                g = torch.empty((R, F), dtype=rk.x.dtype, device=dev)
+                u = torch.empty_like(g)
+                moe_gmm_swiglu_saved(rc, rb["x_sorted"], rb["group_offsets"],
+                                     wg, wu, wd, g, u, rb["h"],
+                                     rb["y_sorted"], rb["status"])
+                dY = torch.cat(gdy[j])
+                dys_ = torch.empty((R, H), dtype=rk.x.dtype, device=dev)
+                moe_combine_backward(rc, dY, rb["y_sorted"], rb["row_of"],
+                                     st["lw"], dys_, dlw)
+                dxs_ = torch.empty((R, H), dtype=rk.x.dtype, device=dev)
+                ws = torch.empty(max(moe_workspace_bytes(
+                    rc, MOE_WS_GMM_BACKWARD), 256), dtype=torch.uint8,
+                    device=dev)
+                moe_gmm_swiglu_backward(rc, rb["x_sorted"],
+                                        rb["group_offsets"], wg, wu, wd, g, u,
+                                        rb["h"], dys_, dxs_, dwg, dwu, dwd, 0,
+                                        ws, rb["status"])
+                moe_permute_backward(rc, dxs_, rb["row_of"], part)
+            dx_back.append(list(torch.split(part, st["sizes"])))
+            dw_back.append(list(torch.split(dlw, st["sizes"])))
+        # the owners: partial dx summed (the tokens' all-gather transposed),
+        # each pick's weight gradient from its expert's rank, then the router
+        rdx = tr.all_to_all(dx_back)
+        rdw = tr.all_to_all(dw_back)
+        dxs, dls = [], []
+        for rk, blocks, wblocks, L in zip(ranks, rdx, rdw, logits):
+            dx = torch.zeros((rk.T, H), dtype=rk.x.dtype, device=dev)
+            dl = torch.zeros((rk.T, E), **f32)
+            if rk.T:
+                moe_ep_sum_partials(rk.cfg, S, torch.cat(blocks), dx)
+                dtw = torch.zeros((rk.T, cfg.k), **f32)
+                for d, blk in enumerate(wblocks):
+                    moe_ep_delocalize(rk.cfg, rk.idx, d * El, El,
+                                      blk.contiguous(), dtw)
+                moe_route_backward(rk.cfg, L, rk.idx, dtw, dl)
+            dxs.append(dx)
+            dls.append(dl)
+        return dxs, dls, dWs
 
 
 def local_weights(w_gate, w_up, w_down, n_ranks):

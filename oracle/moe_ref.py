@@ -1074,12 +1074,43 @@ def ring_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
 # backward on its own logits.  Weight gradients stay with the experts'
 # rank.
 # ---------------------------------------------------------------------------
+def ring_rank_backward(cfg: MoEConfig, N: int, d: int, x_all, idx_all,
+                       w_all, dy_all, weights: ExpertWeights):
+    """Rank d's share of the ring backward, over the gathered tokens x_all,
+    their routing (idx_all, w_all) and the gathered cotangent dy_all.
+    Returns (dx_part [T_all, H]: its experts' contribution to every token's
+    dx; dtw_part [T_all, k]: the combine-weight gradient of the picks it
+    owns, zero elsewhere; {e: (dWg, dWu, dWd)} of its experts with rows)."""
+    k, H = cfg.k, cfg.H
+    Ed = cfg.E // N
+    T_all = x_all.shape[0]
+    part = np.zeros((T_all, H))
+    dtw = np.zeros((T_all, k))
+    dW = {}
+    for el in range(Ed):
+        e = d * Ed + el
+        picks = [(t, j) for t in range(T_all) for j in range(k)
+                 if int(idx_all[t, j]) == e]
+        if not picks:
+            continue
+        rows = [t for t, _ in picks]
+        _, y = expert_ffn(x_all[rows], *weights(e))
+        dy_rows = np.zeros((len(picks), H))
+        for q, (t, j) in enumerate(picks):
+            dtw[t, j] = float(dy_all[t] @ y[q])
+            dy_rows[q] = w_all[t, j] * dy_all[t]
+        dx_rows, dW[e] = expert_ffn_backward(x_all[rows], dy_rows,
+                                             *weights(e))
+        for q, t in enumerate(rows):
+            part[t] += dx_rows[q]
+    return part, dtw, dW
+
+
 def ring_layer_backward(cfg: MoEConfig, N: int, xs: list, logits: list,
                         weights: ExpertWeights, dys: list):
     """Returns (dxs, dlogits) per rank and (dWg, dWu, dWd) [E, ...] (zero
     for experts without rows)."""
     E, k, H = cfg.E, cfg.k, cfg.H
-    Ed = E // N
     Ts = [np.asarray(x).shape[0] for x in xs]
     x_all = np.concatenate([np.asarray(x, dtype=np.float64) for x in xs]
                            + [np.zeros((0, H))])
@@ -1090,32 +1121,19 @@ def ring_layer_backward(cfg: MoEConfig, N: int, xs: list, logits: list,
                              + [np.zeros((0, k), dtype=INT)])
     w_all = np.concatenate([r[1] for r in routes] + [np.zeros((0, k))])
     T_all = x_all.shape[0]
-    wg0, wu0, wd0 = weights(0)
+    wg0 = weights(0)[0]
     F = np.shape(wg0)[1]
     dwg, dwu, dwd = np.zeros((E, H, F)), np.zeros((E, H, F)), \
         np.zeros((E, F, H))
     dx_all = np.zeros((T_all, H))
     dtw_all = np.zeros((T_all, k))
     for d in range(N):
-        part = np.zeros((T_all, H))       # rank d's dx for every token
-        for el in range(Ed):
-            e = d * Ed + el
-            picks = [(t, j) for t in range(T_all) for j in range(k)
-                     if int(idx_all[t, j]) == e]
-            if not picks:
-                continue
-            rows = [t for t, _ in picks]
-            _, y = expert_ffn(x_all[rows], *weights(e))
-            dy_rows = np.zeros((len(picks), H))
-            for q, (t, j) in enumerate(picks):
-                dtw_all[t, j] = float(dy_all[t] @ y[q])
-                dy_rows[q] = w_all[t, j] * dy_all[t]
-            dx_rows, (a, b, c) = expert_ffn_backward(x_all[rows], dy_rows,
-                                                     *weights(e))
-            dwg[e], dwu[e], dwd[e] = a, b, c
-            for q, t in enumerate(rows):
-                part[t] += dx_rows[q]
+        part, dtw, dW = ring_rank_backward(cfg, N, d, x_all, idx_all, w_all,
+                                           dy_all, weights)
         dx_all += part                    # reduce-scatter: summed over d
+        dtw_all += dtw                    # each pick has one owner rank
+        for e, (a, b, c) in dW.items():
+            dwg[e], dwu[e], dwd[e] = a, b, c
     dxs, dls, t0 = [], [], 0
     for r, T_r in enumerate(Ts):
         dxs.append(dx_all[t0:t0 + T_r])

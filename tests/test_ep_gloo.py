@@ -5,7 +5,10 @@ made by the oracle, since the kernels need a GPU -- to the right ranks, and
 the returned partial rows add up to the oracle's EP layer output.
 
 Every rank can compute every rank's inputs (seeded), so each checks what it
-received against the sender's plan, block by block."""
+received against the sender's plan, block by block.  The ring of experts
+runs its all-gathers and reduce-scatters (forward and backward) through the
+same transport, each rank's share of the work from the oracle, against the
+oracle's ring layer and its backward."""
 import os
 import socket
 
@@ -112,3 +115,82 @@ def test_ep_exchange_over_gloo(Ts):
     mp.spawn(_worker, args=(world, port, Ts, out), nprocs=world, join=True)
     for r in range(world):
         assert out[r] < 1e-5, (r, out[r])
+
+
+def _ring_worker(rank, world, port, Ts, out):
+    """The ring of experts over gloo: the all-gathers (tokens, routing, and
+    in the backward the output cotangent) and the reduce-scatters (partial
+    outputs, partial dx, the picks' weight gradients) through
+    DistTransport, each rank's local share from the oracle."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from mixture_experts_token_gb300.ep import DistTransport
+        from oracle import moe_ref as ref
+        tr = DistTransport()
+        N, Ed = world, E // world
+        weights = ref.dense_weights(*_weights())
+        ins = [_inputs(r, Ts[r]) for r in range(N)]
+        dys = [np.random.default_rng(500 + r).standard_normal((Ts[r], H))
+               for r in range(N)]
+        x, L = ins[rank]
+        idx, w = ref.route(L, K)[:2]
+        f64 = torch.float64
+
+        def gather(a, dtype):
+            (got,) = tr.all_to_all([[torch.tensor(a, dtype=dtype)] * N])
+            return torch.cat(got).numpy()
+
+        x_all = gather(x, f64)
+        idx_all = gather(idx, torch.int32)
+        w_all = gather(w, f64)
+        assert np.array_equal(x_all, np.concatenate([a for a, _ in ins]))
+        sizes = list(Ts)
+        local = np.where(idx_all // Ed == rank, idx_all - rank * Ed, -1)
+        part = ref.ep_expert_pass(x_all, local,
+                                  np.where(local >= 0, w_all, 0.0),
+                                  lambda e: weights(rank * Ed + e))
+        (ret,) = tr.all_to_all([list(torch.split(torch.tensor(part),
+                                                 sizes))])
+        y = sum(b.numpy() for b in ret) if Ts[rank] else np.zeros((0, H))
+        cfg = ref.MoEConfig(sum(Ts), H, E, K, F, N, -1.0)
+        ys = ref.ring_layer(cfg, N, [a for a, _ in ins],
+                            [b for _, b in ins], weights)
+        err = float(np.max(np.abs(y - ys[rank]))) if Ts[rank] else 0.0
+        # backward: cotangent all-gather, this rank's share, reduce-scatters
+        dy_all = gather(dys[rank], f64)
+        dpart, dtw, dW = ref.ring_rank_backward(cfg, N, rank, x_all, idx_all,
+                                                w_all, dy_all, weights)
+        (rdx,) = tr.all_to_all([list(torch.split(torch.tensor(dpart),
+                                                 sizes))])
+        (rdw,) = tr.all_to_all([list(torch.split(torch.tensor(dtw),
+                                                 sizes))])
+        wdx, wdl, wdW = ref.ring_layer_backward(
+            cfg, N, [a for a, _ in ins], [b for _, b in ins], weights, dys)
+        if Ts[rank]:
+            dx = sum(b.numpy() for b in rdx)
+            dl = ref.route_backward(L, idx, sum(b.numpy() for b in rdw),
+                                    False)
+            err = max(err, float(np.max(np.abs(dx - wdx[rank]))),
+                      float(np.max(np.abs(dl - wdl[rank]))))
+        for e in range(rank * Ed, (rank + 1) * Ed):
+            got = dW.get(e, (np.zeros((H, F)), np.zeros((H, F)),
+                             np.zeros((F, H))))
+            err = max([err] + [float(np.max(np.abs(g - wdW[i][e])))
+                               for i, g in enumerate(got)])
+        out[rank] = err
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("Ts", [[29, 17], [11, 0, 20]],
+                         ids=["world2", "world3_empty_rank"])
+def test_ring_exchange_over_gloo(Ts):
+    world = len(Ts)
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_ring_worker, args=(world, port, Ts, out), nprocs=world,
+             join=True)
+    for r in range(world):
+        assert out[r] < 1e-6, (r, out[r])

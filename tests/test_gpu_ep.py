@@ -174,6 +174,77 @@ def test_ring_layer_matches_oracle(case):
                  np.concatenate(want), TOL[wl.dtype], f"ring y (N={N})")
 
 
+@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0].name)
+def test_ring_backward_matches_oracle(case):
+    """The ring's backward over logical ranks (cotangent all-gather, each
+    rank's expert pass differentiated over all tokens, partial dx summed at
+    the owners, pick gradients from the experts' ranks, the router backward
+    on the owners) against the oracle's ring backward: dx and dlogits per
+    rank, each rank's weight gradients.  Saving the sorted rows in the
+    forward (moe_x_sorted=device) gives the same bits as gathering and
+    sorting again in the backward."""
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    dys = [torch.randn((T_r, wl.H), generator=g, device="cuda").to(x.dtype)
+           for T_r, x in zip(Ts, xs)]
+    Lt = [torch.from_numpy(L).cuda() for L in Ls]
+    remat = ep.RingLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    dxs, dls, dWs = remat.backward(xs, Lt, dys)
+    saved = ep.RingLayer(cfg, ep.LoopbackTransport(N), per_rank,
+                         save_x_sorted=True)
+    saved.forward(xs, Lt)
+    dxs2, dls2, dWs2 = saved.backward(xs, Lt, dys)
+    torch.cuda.synchronize()
+    for a, b in zip(dxs + dls + [w for t in dWs for w in t],
+                    dxs2 + dls2 + [w for t in dWs2 for w in t]):
+        assert torch.equal(a, b)
+    mc = ref.MoEConfig(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                       wl.renorm)
+    wdx, wdl, wdW = ref.ring_layer_backward(
+        mc, N, [f64(x) for x in xs], Ls,
+        ref.dense_weights(*(f64(w) for w in W)), [f64(d) for d in dys])
+    tol = TOL[wl.dtype]
+    assert_close(np.concatenate([f64(d) for d in dxs]), np.concatenate(wdx),
+                 tol, f"ring dx (N={N})")
+    assert_close(np.concatenate([f64(d) for d in dls]), np.concatenate(wdl),
+                 tol, f"ring dlogits (N={N})")
+    for i, name in enumerate(("dwg", "dwu", "dwd")):
+        got = np.concatenate([f64(t[i]) for t in dWs])
+        assert np.isfinite(got).all()
+        assert_close(got, wdW[i], tol, f"ring {name} (N={N})")
+
+
+def test_ep_delocalize_is_localize_transposed():
+    """moe_ep_delocalize writes slot q of a rank's values at the q-th pick
+    it owns and leaves every other pick alone, so the ranks' calls together
+    rebuild a [T, k] array from its localized pieces exactly."""
+    T, E, k, N = 300, 12, 3, 4
+    El = E // N
+    gen = np.random.default_rng(5)
+    idx = np.stack([gen.permutation(E)[:k] for _ in range(T)]).astype(
+        np.int32)
+    v = gen.standard_normal((T, k)).astype(np.float32)
+    cfg = moe.make_config(T, 128, E, k, 128, N, 2.0, 0, "bf16")
+    it = torch.from_numpy(idx).cuda()
+    vt = torch.from_numpy(v).cuda()
+    out = torch.full((T, k), 7.0, dtype=torch.float32, device="cuda")
+    kk = min(k, El)
+    for d in range(N):
+        li = torch.empty((T, kk), dtype=torch.int32, device="cuda")
+        lv = torch.empty((T, kk), dtype=torch.float32, device="cuda")
+        moe.moe_ep_localize(cfg, it, vt, d * El, El, li, lv)
+        before = out.clone()
+        moe.moe_ep_delocalize(cfg, it, d * El, El, lv, out)
+        torch.cuda.synchronize()
+        mine = (idx // El) == d
+        assert np.array_equal(np_(out)[mine], v[mine])
+        assert np.array_equal(np_(out)[~mine], np_(before)[~mine])
+    assert np.array_equal(np_(out), v)
+
+
 def test_ep_check_global_flag():
     """moe_ep_check on summed shard counts: strict > C with C from the
     global token count; required factor max_s r_s * S / (T k)."""

@@ -122,8 +122,8 @@ MUTANTS = {
         "        dx_all += part ",
         "        dx_all = part "),
     "ring_bwd_cotangent_unweighted": (
-        "                dy_rows[q] = w_all[t, j] * dy_all[t]",
-        "                dy_rows[q] = dy_all[t]"),
+        "            dy_rows[q] = w_all[t, j] * dy_all[t]",
+        "            dy_rows[q] = dy_all[t]"),
     "slot_uses_group_weights": (
         "        wg, wu, wd = weights(grp if gexp is None else int(gexp[grp]))",
         "        wg, wu, wd = weights(grp % cfg.E)"),
