@@ -983,6 +983,20 @@ def ep_chunk_bounds(T_r: int, n: int, c: int):
     return t0, min(T_r, t0 + size)
 
 
+def ep_global_check(cfg: MoEConfig, N: int, routes: list):
+    """The check over all ranks: each shard's receive count summed over the
+    ranks' routings, against the capacity of the ranks' tokens together.
+    Returns (overflow, passes)."""
+    E, k = cfg.E, cfg.k
+    shard = np.zeros(N, dtype=INT)
+    for idx, _ in routes:
+        shard += shard_counts(expert_counts(idx, E), N)
+    C = capacity(cfg.T, k, N, cfg.ragged_buffer_factor)
+    over = overflow_flag(shard, C)
+    n = len(chunk_plan(cfg.T, k, E, N, C, cfg.n_chunks)) if over else 1
+    return over, n
+
+
 def ep_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
              weights: ExpertWeights):
     """The layer with fallback=layer over N ranks (cfg.T = all ranks'
@@ -993,12 +1007,7 @@ def ep_layer(cfg: MoEConfig, N: int, xs: list, logits: list,
     if sum(Ts) != cfg.T or cfg.S != N:
         raise ValueError("cfg.T must be the ranks' tokens and cfg.S = N")
     routes = [route(L, k, cfg.renorm)[:2] for L in logits]
-    shard = np.zeros(N, dtype=INT)
-    for idx, _ in routes:
-        shard += shard_counts(expert_counts(idx, E), N)
-    C = capacity(cfg.T, k, N, cfg.ragged_buffer_factor)
-    over = overflow_flag(shard, C)
-    n = len(chunk_plan(cfg.T, k, E, N, C, cfg.n_chunks)) if over else 1
+    over, n = ep_global_check(cfg, N, routes)
     ys = [np.zeros((T_r, H)) for T_r in Ts]
     xs = [np.asarray(x, dtype=np.float64) for x in xs]
     for c in range(n):
@@ -1141,4 +1150,115 @@ def ring_layer_backward(cfg: MoEConfig, N: int, xs: list, logits: list,
                                   dtw_all[t0:t0 + T_r], cfg.renorm)
                    if T_r else np.zeros((0, E)))
         t0 += T_r
+    return dxs, dls, (dwg, dwu, dwd)
+
+
+# ---------------------------------------------------------------------------
+# Expert parallelism, backward.  [PR5920 Tests]: the fallback's gradients
+# equal the dropless model's; [PR5920 How]: the backward differentiates
+# each pass (each chunk of the fallback) and sums the weight gradients.
+# READING: each exchange of the forward has its transpose: the rows the
+# destinations returned become the output cotangent sent again to the same
+# destinations (one row per dedup'd token), and the rows the source sent
+# become token gradients the destinations return and the source adds.  Each
+# pick's combine-weight gradient comes back in the slot that carried its
+# weight.  Weight gradients stay on the experts' rank, summed over passes.
+# ---------------------------------------------------------------------------
+def ep_expert_pass_backward(recv_x, recv_idx, recv_w, recv_dy,
+                            local_weights: ExpertWeights):
+    """The receiving rank's backward of ep_expert_pass, given the cotangent
+    recv_dy of its returned rows.  Returns (dx_recv [n, H], dw_recv [n, kk]
+    the gradient of each slot's weight, {e: (dWg, dWu, dWd)} of its local
+    experts with rows)."""
+    recv_x = np.asarray(recv_x, dtype=np.float64)
+    recv_dy = np.asarray(recv_dy, dtype=np.float64)
+    n = recv_x.shape[0]
+    kk = recv_idx.shape[1] if recv_idx.ndim == 2 else 0
+    dx = np.zeros_like(recv_x)
+    dw = np.zeros((n, kk))
+    dW = {}
+    by_expert = {}
+    for i in range(n):
+        for j in range(kk):
+            e = int(recv_idx[i, j])
+            if e >= 0:
+                by_expert.setdefault(e, []).append((i, j))
+    for e in sorted(by_expert):
+        picks = by_expert[e]
+        rows = [i for i, _ in picks]
+        _, y = expert_ffn(recv_x[rows], *local_weights(e))
+        dy_rows = np.zeros((len(picks), recv_x.shape[1]))
+        for q, (i, j) in enumerate(picks):
+            dw[i, j] = float(recv_dy[i] @ y[q])
+            dy_rows[q] = float(recv_w[i, j]) * recv_dy[i]
+        dx_rows, dW[e] = expert_ffn_backward(recv_x[rows], dy_rows,
+                                             *local_weights(e))
+        for q, i in enumerate(rows):
+            dx[i] += dx_rows[q]
+    return dx, dw, dW
+
+
+def ep_layer_backward(cfg: MoEConfig, N: int, xs: list, logits: list,
+                      weights: ExpertWeights, dys: list):
+    """Backward of ep_layer: per rank (dx, dlogits), and (dWg, dWu, dWd)
+    [E, ...] summed over the passes (zero for experts without rows)."""
+    E, k, H = cfg.E, cfg.k, cfg.H
+    Ed = E // N
+    Ts = [np.asarray(x).shape[0] for x in xs]
+    if sum(Ts) != cfg.T or cfg.S != N:
+        raise ValueError("cfg.T must be the ranks' tokens and cfg.S = N")
+    routes = [route(L, k, cfg.renorm)[:2] for L in logits]
+    over, n = ep_global_check(cfg, N, routes)
+    xs = [np.asarray(x, dtype=np.float64) for x in xs]
+    dys = [np.asarray(d, dtype=np.float64) for d in dys]
+    wg0 = weights(0)[0]
+    F = np.shape(wg0)[1]
+    dwg, dwu, dwd = np.zeros((E, H, F)), np.zeros((E, H, F)), \
+        np.zeros((E, F, H))
+    dxs = [np.zeros((T_r, H)) for T_r in Ts]
+    dtws = [np.zeros((T_r, k)) for T_r in Ts]
+    kk = min(k, Ed)
+    for c in range(n):
+        bounds = [ep_chunk_bounds(Ts[r], n, c) for r in range(N)]
+        sends = [ep_dispatch(routes[r][0][t0:t1], routes[r][1][t0:t1], E, N)
+                 for r, (t0, t1) in enumerate(bounds)]
+        for d in range(N):
+            parts = []
+            for q in range(N):
+                a, z = int(sends[q].uniq_offsets[d]), \
+                    int(sends[q].uniq_offsets[d + 1])
+                parts.append((q, sends[q].uniq_tokens[a:z],
+                              sends[q].send_idx[a:z], sends[q].send_w[a:z]))
+            t0s = [bounds[q][0] for q, _, _, _ in parts]
+            recv_x = np.concatenate(
+                [xs[q][t0 + tok] for (q, tok, _, _), t0 in zip(parts, t0s)]
+                + [np.zeros((0, H))])
+            recv_dy = np.concatenate(
+                [dys[q][t0 + tok] for (q, tok, _, _), t0 in zip(parts, t0s)]
+                + [np.zeros((0, H))])
+            recv_idx = np.concatenate([i for _, _, i, _ in parts]
+                                      + [np.zeros((0, kk), dtype=INT)])
+            recv_w = np.concatenate([w for _, _, _, w in parts]
+                                    + [np.zeros((0, kk))])
+            dx_r, dw_r, dW = ep_expert_pass_backward(
+                recv_x, recv_idx, recv_w, recv_dy,
+                lambda e, d=d: weights(d * Ed + e))
+            for el, (a, b, cc) in dW.items():
+                e = d * Ed + el
+                dwg[e] += a
+                dwu[e] += b
+                dwd[e] += cc
+            pos = 0
+            for (q, tok, _, _), t0 in zip(parts, t0s):
+                for u, t in enumerate(tok):
+                    t = t0 + int(t)
+                    dxs[q][t] += dx_r[pos + u]
+                    # slot s of this row = the s-th pick of t that d owns
+                    own = [j for j in range(k)
+                           if int(routes[q][0][t, j]) // Ed == d]
+                    for s, j in enumerate(own):
+                        dtws[q][t, j] = dw_r[pos + u, s]
+                pos += len(tok)
+    dls = [route_backward(logits[r], routes[r][0], dtws[r], cfg.renorm)
+           if Ts[r] else np.zeros((0, E)) for r in range(N)]
     return dxs, dls, (dwg, dwu, dwd)

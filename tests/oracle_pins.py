@@ -827,6 +827,40 @@ def pin_ep_layer_equals_single_device():
     assert over_seen == {True, False}
 
 
+def pin_ep_backward_equals_dropless_backward():
+    """The EP layer's backward (fallback=layer over N ranks; the cotangent
+    sent along the dispatch's dedup'd rows, token gradients returned and
+    added, slot weight gradients returned, weight gradients summed over the
+    fallback's passes) equals the dropless layer's backward on the ranks'
+    batches together ([PR5920 Tests]), whether or not a shard overflows."""
+    rng = _rng(36)
+    over_seen = set()
+    for i in range(24):
+        N = int(rng.choice([2, 4]))
+        E = N * int(rng.choice([1, 2, 3]))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        Ts = [int(rng.integers(0, 10)) for _ in range(N)]
+        if sum(Ts) == 0:
+            Ts[0] = 3
+        factor = float(rng.choice([0.5, 1.0, 2.0]))
+        xs, Ls, w = _ep_case(rng, N, Ts, E, k)
+        dys = [rng.standard_normal((T_r, 3)) for T_r in Ts]
+        cfg = ref.MoEConfig(sum(Ts), 3, E, k, 4, N, factor,
+                            renorm=bool(i % 3 == 0))
+        _, over, n = ref.ep_layer(cfg, N, xs, Ls, ref.dense_weights(*w))
+        over_seen.add(over)
+        dxs, dls, dW = ref.ep_layer_backward(cfg, N, xs, Ls,
+                                             ref.dense_weights(*w), dys)
+        g = ref.layer_backward_dropless(cfg, np.concatenate(xs),
+                                        np.concatenate(Ls), *w,
+                                        np.concatenate(dys))
+        for got, want in ((np.concatenate(dxs), g.dx),
+                          (np.concatenate(dls), g.dlogits),
+                          (dW[0], g.dwg), (dW[1], g.dwu), (dW[2], g.dwd)):
+            assert np.allclose(got, want, rtol=1e-10, atol=1e-10)
+    assert over_seen == {True, False}
+
+
 def pin_ring_layer_equals_dropless():
     """The ring of experts (all-gather, local experts, reduce-scatter of the
     combine) gives the dropless layer on the ranks' batches together."""

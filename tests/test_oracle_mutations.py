@@ -118,6 +118,12 @@ MUTANTS = {
     "duplicate_dw_not_summed": (
         "        dW[e] = dWe if e not in dW else tuple(",
         "        dW[e] = dWe if True else tuple("),
+    "ep_bwd_dw_not_summed_over_passes": (
+        "                dwg[e] += a\n",
+        "                dwg[e] = a\n"),
+    "ep_bwd_slot_gradient_to_first_pick": (
+        "                        dtws[q][t, j] = dw_r[pos + u, s]",
+        "                        dtws[q][t, own[0]] += dw_r[pos + u, s]"),
     "ring_bwd_partials_not_summed": (
         "        dx_all += part ",
         "        dx_all = part "),
