@@ -722,19 +722,27 @@ moe_status_t moe_ep_localize(const moe_config_t *cfg, const int32_t *topk_idx,
                              int32_t n_local, int32_t *local_idx,
                              float *local_w, moe_stream_t stream);
 
-/* moe_ep_delocalize -- the ring variant's backward ("MoE ring-of-experts
- * ...", pull request 4969, section What: the backward of the combine's
- * reduce-scatter and of the tokens' all-gather): the transpose of
- * moe_ep_localize.  For each token t, the q-th pick of t in [first_expert,
- * first_expert + n_local) (pick order) gets v[t, j] = local_v[t, q]
- * (local_v [T, kk] float32, kk = min(k, n_local)); v [T, k] float32 keeps
- * its value at every other pick, so the N ranks' calls together fill every
- * pick once.  Used for the gradient of the combine weights, which each pick
- * receives from the rank that owns its expert.  Errors: expert range
- * outside [0, E), pointers not 4-byte aligned. */
+/* moe_ep_delocalize -- the backward of the ring variant ("MoE
+ * ring-of-experts ...", pull request 4969, section What: the backward of
+ * the combine's reduce-scatter and of the tokens' all-gather) and of the EP
+ * layer ("Support moe_dropless_fallback=layer on the ragged all-to-all MoE
+ * path", pull request 5920, section Tests: gradients as the dropless
+ * model's): the transpose of moe_ep_localize and of the slots of
+ * moe_ep_dispatch_pack.  For each token t with local row r (r =
+ * row_of[t * row_stride] when row_of is given, device int32, e.g. one
+ * destination's column of moe_ep_return_map's [T, S] map with row_stride =
+ * S; else r = t; r < 0 skips t), the q-th pick of t in [first_expert,
+ * first_expert + n_local) (pick order) gets v[t, j] = local_v[r, q]
+ * (local_v [rows, kk] float32, kk = min(k, n_local)); v [T, k] float32
+ * keeps its value at every other pick, so the calls for all ranks together
+ * fill every pick once.  Used for the gradient of the combine weights,
+ * which each pick receives from the rank that owns its expert.  Errors:
+ * expert range outside [0, E), row_stride < 1 with a map, pointers not
+ * 4-byte aligned. */
 moe_status_t moe_ep_delocalize(const moe_config_t *cfg,
                                const int32_t *topk_idx, int32_t first_expert,
-                               int32_t n_local, const float *local_v,
+                               int32_t n_local, const int32_t *row_of,
+                               int32_t row_stride, const float *local_v,
                                float *v, moe_stream_t stream);
 
 /* moe_ep_sum_partials -- the ring variant's reduce: y [T, H] = sum over

@@ -90,7 +90,8 @@ def _declare(h):
         "moe_ep_return_map": [cfg, P, P, P, P],
         "moe_ep_localize": [cfg, P, P, c_int32, c_int32, P, P, P],
         "moe_ep_sum_partials": [cfg, c_int32, P, P, P],
-        "moe_ep_delocalize": [cfg, P, c_int32, c_int32, P, P, P],
+        "moe_ep_delocalize": [cfg, P, c_int32, c_int32, P, c_int32, P, P,
+                              P],
         "moe_route": [cfg, P, P, P, P, P],
         "moe_check_overflow": [cfg, P, P, P, P, P, P, P, P],
         "moe_permute": [cfg, P, P, c_int32, P, P, P, P, P, P, P, P, P,
@@ -293,11 +294,11 @@ def moe_ep_localize(cfg, topk_idx, topk_w, first_expert, n_local, local_idx,
 
 
 def moe_ep_delocalize(cfg, topk_idx, first_expert, n_local, local_v, v,
-                      stream=None):
+                      row_of=None, row_stride=1, stream=None):
     _check(lib().moe_ep_delocalize(ctypes.byref(cfg), _ptr(topk_idx),
-                                   first_expert, n_local, _ptr(local_v),
-                                   _ptr(v), _stream(stream)),
-           "moe_ep_delocalize")
+                                   first_expert, n_local, _ptr(row_of),
+                                   row_stride, _ptr(local_v), _ptr(v),
+                                   _stream(stream)), "moe_ep_delocalize")
 
 
 def moe_ep_sum_partials(cfg, n_parts, parts, y, stream=None):

@@ -136,15 +136,22 @@ __global__ void ep_localize_kernel(const int32_t* __restrict__ topk_idx,
 }
 
 // One thread per token: the q-th pick of t in [e0, e0 + n_local) (pick
-// order) receives slot q of local_v; the other picks are left as they are.
+// order) receives slot q of row r of local_v (r = row_of[t * row_stride],
+// or t without a map; a negative r skips the token); the other picks are
+// left as they are.
 __global__ void ep_delocalize_kernel(const int32_t* __restrict__ topk_idx,
+                                     const int32_t* __restrict__ row_of,
+                                     int row_stride,
                                      const float* __restrict__ local_v, int T,
                                      int k, int kk, int e0, int n_local,
                                      float* __restrict__ v) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
+  const long long r =
+      row_of ? __ldg(row_of + static_cast<long long>(t) * row_stride) : t;
+  if (r < 0) return;
   const long long o = static_cast<long long>(t) * k;
-  const float* lv = local_v + static_cast<long long>(t) * kk;
+  const float* lv = local_v + r * kk;
   int q = 0;
   for (int j = 0; j < k && q < kk; ++j) {
     const int e = __ldg(topk_idx + o + j);
@@ -289,17 +296,21 @@ moe_status_t moe_ep_localize(const moe_config_t* cfg,
 
 moe_status_t moe_ep_delocalize(const moe_config_t* cfg,
                                const int32_t* topk_idx, int32_t first_expert,
-                               int32_t n_local, const float* local_v,
+                               int32_t n_local, const int32_t* row_of,
+                               int32_t row_stride, const float* local_v,
                                float* v, moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   if (first_expert < 0 || n_local < 1 || first_expert + n_local > cfg->E)
     return MOE_ERR_INVALID_ARG;
+  if (row_of != nullptr && row_stride < 1) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
-  if (!al4(topk_idx) || !al4(local_v) || !al4(v)) return MOE_ERR_INVALID_ARG;
+  if (!al4(topk_idx) || !al4(local_v) || !al4(v) ||
+      (row_of != nullptr && !al4(row_of)))
+    return MOE_ERR_INVALID_ARG;
   ep_delocalize_kernel<<<(cfg->T + 255) / 256, 256, 0, stream>>>(
-      topk_idx, local_v, cfg->T, cfg->k, std::min(cfg->k, n_local),
-      first_expert, n_local, v);
+      topk_idx, row_of, row_stride, local_v, cfg->T, cfg->k,
+      std::min(cfg->k, n_local), first_expert, n_local, v);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -157,6 +157,14 @@ class EPLayer:
         dev = xs[0].device
         ranks = [_Rank(r, x, L, cfg, dev)
                  for r, x, L in zip(tr.ranks, xs, logits)]
+        n = self._check(ranks)
+        for c in range(n):
+            self._pass(ranks, c, n)
+        return [rk.y for rk in ranks]
+
+    def _check(self, ranks):
+        """The global check; returns the pass count."""
+        cfg, tr = self.cfg, self.tr
         for rk in ranks:
             if rk.T:
                 moe_check_overflow(rk.cfg, rk.idx, rk.counts, rk.offsets,
@@ -165,22 +173,21 @@ class EPLayer:
         for rk, s in zip(ranks, sums):
             moe_ep_check(cfg, s, rk.flag, rk.req, rk.cap)
         over = int(ranks[0].flag.item())
-        n = moe_num_chunks(cfg) if over else 1
-        for c in range(n):
-            self._pass(ranks, c, n)
-        self.info = {"overflow": over, "n_chunks": n,
+        self.info = {"overflow": over,
+                     "n_chunks": moe_num_chunks(cfg) if over else 1,
                      "required_factor": float(ranks[0].req.item())}
-        return [rk.y for rk in ranks]
+        return self.info["n_chunks"]
 
-    def _pass(self, ranks, c, n):
-        cfg, tr = self.cfg, self.tr
-        E, S, k, H = cfg.E, cfg.S, cfg.k, cfg.H
-        El = E // S
-        kk = min(k, El)
+    def _send(self, ranks, c, n, dys=None):
+        """Source side of pass c of n: dedup sets per destination and the
+        send rows (x, and with dys the output cotangent along the same
+        rows), split by destination."""
+        cfg = self.cfg
+        S, k, H = cfg.S, cfg.k, cfg.H
+        kk = min(k, cfg.E // S)
         dev = ranks[0].x.device
-        # source side: dedup sets per destination, then the send rows
-        sends_x, sends_i, sends_w, state = [], [], [], []
-        for rk in ranks:
+        out = {"x": [], "i": [], "w": [], "dy": [], "state": []}
+        for j, rk in enumerate(ranks):
             t0, t1 = chunk_bounds(rk.T, n, c)
             Tc = t1 - t0
             sc = _cfg(cfg, T=Tc, ragged_buffer_factor=-1.0, n_chunks=0,
@@ -190,6 +197,8 @@ class EPLayer:
             x_send = torch.empty((rows, H), dtype=rk.x.dtype, device=dev)
             s_idx = torch.empty((rows, kk), dtype=torch.int32, device=dev)
             s_w = torch.empty((rows, kk), dtype=torch.float32, device=dev)
+            dy_send = (torch.empty_like(x_send) if dys is not None
+                       else None)
             if Tc:
                 moe_permute_tables(sc, rk.idx[t0:t1], False, b["row_of"],
                                    b["sorted_token"], b["group_offsets"],
@@ -201,54 +210,167 @@ class EPLayer:
                 moe_ep_dispatch_pack(sc, rk.x[t0:t1], rk.idx[t0:t1],
                                      rk.w[t0:t1], b["uniq_offsets"],
                                      b["uniq_tokens"], x_send, s_idx, s_w)
+                if dys is not None:
+                    # the same rows and slots, carrying dy instead of x
+                    i2 = torch.empty_like(s_idx)
+                    w2 = torch.empty_like(s_w)
+                    moe_ep_dispatch_pack(sc, dys[j][t0:t1], rk.idx[t0:t1],
+                                         rk.w[t0:t1], b["uniq_offsets"],
+                                         b["uniq_tokens"], dy_send, i2, w2)
                 uo = b["uniq_offsets"].cpu().tolist()
             else:
                 uo = [0] * (S + 1)
-            sends_x.append([x_send[uo[d]:uo[d + 1]] for d in range(S)])
-            sends_i.append([s_idx[uo[d]:uo[d + 1]] for d in range(S)])
-            sends_w.append([s_w[uo[d]:uo[d + 1]] for d in range(S)])
-            state.append((t0, t1, sc, b))
-        recv_x = tr.all_to_all(sends_x)
-        recv_i = tr.all_to_all(sends_i)
-        recv_w = tr.all_to_all(sends_w)
+            out["x"].append([x_send[uo[d]:uo[d + 1]] for d in range(S)])
+            out["i"].append([s_idx[uo[d]:uo[d + 1]] for d in range(S)])
+            out["w"].append([s_w[uo[d]:uo[d + 1]] for d in range(S)])
+            if dys is not None:
+                out["dy"].append([dy_send[uo[d]:uo[d + 1]]
+                                  for d in range(S)])
+            out["state"].append((t0, t1, sc, b))
+        return out
+
+    def _recv_sorted(self, rk, rx, ri):
+        """Receiving side: the received rows sorted by local expert."""
+        cfg = self.cfg
+        El = cfg.E // cfg.S
+        n_recv = rx.shape[0]
+        rc = _cfg(cfg, T=n_recv, E=El, k=min(cfg.k, El), S=1,
+                  ragged_buffer_factor=-1.0, n_chunks=0, redundant_slots=0)
+        rb = alloc_step_buffers(rc, rx.device)
+        moe_permute(rc, rx, ri, False, rb["x_sorted"], rb["row_of"],
+                    rb["sorted_token"], rb["group_offsets"],
+                    rb["uniq_offsets"], rb["uniq_tokens"], rb["expand_idx"],
+                    rb["n_dropped"], rb["permute_ws"])
+        return rc, rb
+
+    @staticmethod
+    def _return_map(sc, b, T):
+        row_of_ret = torch.empty((T, sc.S), dtype=torch.int32,
+                                 device=b["uniq_offsets"].device)
+        moe_ep_return_map(sc, b["uniq_offsets"], b["uniq_tokens"],
+                          row_of_ret)
+        return row_of_ret
+
+    def _pass(self, ranks, c, n):
+        cfg, tr = self.cfg, self.tr
+        S, H = cfg.S, cfg.H
+        dev = ranks[0].x.device
+        snd = self._send(ranks, c, n)
+        recv_x = tr.all_to_all(snd["x"])
+        recv_i = tr.all_to_all(snd["i"])
+        recv_w = tr.all_to_all(snd["w"])
         # receiving side: the local experts over the received rows
         backs = []
         for j, rk in enumerate(ranks):
             sizes = [blk.shape[0] for blk in recv_x[j]]
             n_recv = sum(sizes)
-            rc = _cfg(cfg, T=n_recv, E=El, k=kk, S=1,
-                      ragged_buffer_factor=-1.0, n_chunks=0,
-                      redundant_slots=0)
             part = torch.empty((n_recv, H), dtype=rk.x.dtype, device=dev)
             if n_recv:
-                rx = torch.cat(recv_x[j])
-                ri = torch.cat(recv_i[j])
-                rw = torch.cat(recv_w[j])
-                rb = alloc_step_buffers(rc, dev)
-                moe_permute(rc, rx, ri, False, rb["x_sorted"], rb["row_of"],
-                            rb["sorted_token"], rb["group_offsets"],
-                            rb["uniq_offsets"], rb["uniq_tokens"],
-                            rb["expand_idx"], rb["n_dropped"],
-                            rb["permute_ws"])
+                rc, rb = self._recv_sorted(rk, torch.cat(recv_x[j]),
+                                           torch.cat(recv_i[j]))
                 wg, wu, wd = self.weights(rk.rank)
                 moe_gmm_gate_up(rc, rb["x_sorted"], rb["group_offsets"], wg,
                                 wu, rb["h"], rb["status"])
                 moe_gmm_down(rc, rb["h"], rb["group_offsets"], wd,
                              rb["y_sorted"], rb["status"])
-                moe_combine(rc, rb["y_sorted"], rb["row_of"], rw, part)
+                moe_combine(rc, rb["y_sorted"], rb["row_of"],
+                            torch.cat(recv_w[j]), part)
             backs.append(list(torch.split(part, sizes)))
         ret = tr.all_to_all(backs)
         # source side: add the rows the destinations returned
-        for rk, blocks, (t0, t1, sc, b) in zip(ranks, ret, state):
+        for rk, blocks, (t0, t1, sc, b) in zip(ranks, ret, snd["state"]):
             if t1 == t0:
                 continue
-            rows = torch.cat(blocks)
-            row_of_ret = torch.empty((t1 - t0, S), dtype=torch.int32,
-                                     device=dev)
-            moe_ep_return_map(sc, b["uniq_offsets"], b["uniq_tokens"],
-                              row_of_ret)
-            moe_permute_backward(_cfg(sc, k=S), rows, row_of_ret,
+            moe_permute_backward(_cfg(sc, k=S), torch.cat(blocks),
+                                 self._return_map(sc, b, t1 - t0),
                                  rk.y[t0:t1])
+
+    def backward(self, xs, logits, dys):
+        """Gradients of sum_r <dys[r], forward(xs, logits)[r]> (the forward
+        recomputed pass by pass): per rank (dx [T_r, H] layer dtype,
+        dlogits [T_r, E] float32, (dWg, dWu, dWd) float32 of its own
+        experts, summed over the passes).  Each exchange of the forward runs
+        transposed: the cotangent goes out along the dispatch's dedup'd rows,
+        the token gradients and the slots' weight gradients come back."""
+        cfg, tr = self.cfg, self.tr
+        S, H, E, F, k = cfg.S, cfg.H, cfg.E, cfg.F, cfg.k
+        El = E // S
+        kk = min(k, El)
+        dev = xs[0].device
+        f32 = dict(dtype=torch.float32, device=dev)
+        ranks = [_Rank(r, x, L, cfg, dev)
+                 for r, x, L in zip(tr.ranks, xs, logits)]
+        n = self._check(ranks)
+        dWs = [(torch.zeros((El, H, F), **f32), torch.zeros((El, H, F), **f32),
+                torch.zeros((El, F, H), **f32)) for _ in ranks]
+        dxs = [torch.zeros((rk.T, H), dtype=rk.x.dtype, device=dev)
+               for rk in ranks]
+        dtws = [torch.zeros((rk.T, k), **f32) for rk in ranks]
+        for c in range(n):
+            snd = self._send(ranks, c, n, dys)
+            recv_x = tr.all_to_all(snd["x"])
+            recv_i = tr.all_to_all(snd["i"])
+            recv_w = tr.all_to_all(snd["w"])
+            recv_dy = tr.all_to_all(snd["dy"])
+            dx_back, dw_back = [], []
+            for j, rk in enumerate(ranks):
+                sizes = [blk.shape[0] for blk in recv_x[j]]
+                n_recv = sum(sizes)
+                dxr = torch.empty((n_recv, H), dtype=rk.x.dtype, device=dev)
+                dwr = torch.zeros((n_recv, kk), **f32)
+                if n_recv:
+                    rc, rb = self._recv_sorted(rk, torch.cat(recv_x[j]),
+                                               torch.cat(recv_i[j]))
+                    R = rc.T * rc.k
+                    wg, wu, wd = self.weights(rk.rank)
+                    g = torch.empty((R, F), dtype=rk.x.dtype, device=dev)
+                    u = torch.empty_like(g)
+                    moe_gmm_swiglu_saved(rc, rb["x_sorted"],
+                                         rb["group_offsets"], wg, wu, wd, g,
+                                         u, rb["h"], rb["y_sorted"],
+                                         rb["status"])
+                    dy_sorted = torch.empty((R, H), dtype=rk.x.dtype,
+                                            device=dev)
+                    moe_combine_backward(rc, torch.cat(recv_dy[j]),
+                                         rb["y_sorted"], rb["row_of"],
+                                         torch.cat(recv_w[j]), dy_sorted, dwr)
+                    dx_sorted = torch.empty_like(dy_sorted)
+                    ws = torch.empty(max(moe_workspace_bytes(
+                        rc, MOE_WS_GMM_BACKWARD), 256), dtype=torch.uint8,
+                        device=dev)
+                    dwg, dwu, dwd = dWs[j]
+                    moe_gmm_swiglu_backward(rc, rb["x_sorted"],
+                                            rb["group_offsets"], wg, wu, wd,
+                                            g, u, rb["h"], dy_sorted,
+                                            dx_sorted, dwg, dwu, dwd, 1, ws,
+                                            rb["status"])
+                    moe_permute_backward(rc, dx_sorted, rb["row_of"], dxr)
+                dx_back.append(list(torch.split(dxr, sizes)))
+                dw_back.append(list(torch.split(dwr, sizes)))
+            rdx = tr.all_to_all(dx_back)
+            rdw = tr.all_to_all(dw_back)
+            # source side: the token gradients added over the destinations,
+            # each slot's weight gradient back at its pick
+            for j, (rk, (t0, t1, sc, b)) in enumerate(zip(ranks,
+                                                          snd["state"])):
+                if t1 == t0:
+                    continue
+                row_of_ret = self._return_map(sc, b, t1 - t0)
+                moe_permute_backward(_cfg(sc, k=S), torch.cat(rdx[j]),
+                                     row_of_ret, dxs[j][t0:t1])
+                dw_rows = torch.cat(rdw[j])
+                for d in range(S):
+                    moe_ep_delocalize(sc, rk.idx[t0:t1], d * El, El, dw_rows,
+                                      dtws[j][t0:t1],
+                                      row_of=row_of_ret.data_ptr() + 4 * d,
+                                      row_stride=S)
+        dls = []
+        for rk, L, dtw in zip(ranks, logits, dtws):
+            dl = torch.zeros((rk.T, E), **f32)
+            if rk.T:
+                moe_route_backward(rk.cfg, L, rk.idx, dtw, dl)
+            dls.append(dl)
+        return dxs, dls, dWs
 
 
 class RingLayer:

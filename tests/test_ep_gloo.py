@@ -194,3 +194,99 @@ def test_ring_exchange_over_gloo(Ts):
              join=True)
     for r in range(world):
         assert out[r] < 1e-6, (r, out[r])
+
+
+def _ep_bwd_worker(rank, world, port, Ts, factor, out):
+    """The EP layer's backward over gloo: the global check, then per pass
+    the dispatch's rows out with the cotangent along them, the token
+    gradients and slot weight gradients back; each rank's receiving share
+    from the oracle; against the oracle's EP backward."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from mixture_experts_token_gb300.ep import DistTransport
+        from oracle import moe_ref as ref
+        tr = DistTransport()
+        N, Ed = world, E // world
+        kk = min(K, Ed)
+        weights = ref.dense_weights(*_weights())
+        ins = [_inputs(r, Ts[r]) for r in range(N)]
+        dys = [np.random.default_rng(600 + r).standard_normal((Ts[r], H))
+               for r in range(N)]
+        x, L = ins[rank]
+        idx, w = ref.route(L, K)[:2]
+        cfg = ref.MoEConfig(sum(Ts), H, E, K, F, N, factor)
+        local = ref.shard_counts(ref.expert_counts(idx, E), N)
+        (tot,) = tr.all_reduce_sum([torch.tensor(local, dtype=torch.int32)])
+        C = ref.capacity(cfg.T, K, N, factor)
+        over = ref.overflow_flag(tot.numpy(), C)
+        n = len(ref.chunk_plan(cfg.T, K, E, N, C)) if over else 1
+        dx = np.zeros((Ts[rank], H))
+        dtw = np.zeros((Ts[rank], K))
+        dW = {}
+        for c in range(n):
+            t0, t1 = ref.ep_chunk_bounds(Ts[rank], n, c)
+            p = ref.ep_dispatch(idx[t0:t1], w[t0:t1], E, N)
+            uo = [int(v) for v in p.uniq_offsets]
+
+            def blocks(a, dtype):
+                return [torch.tensor(a[uo[d]:uo[d + 1]], dtype=dtype)
+                        for d in range(N)]
+            tok = t0 + p.uniq_tokens
+            (rx,) = tr.all_to_all([blocks(x[tok], torch.float64)])
+            (rdy,) = tr.all_to_all([blocks(dys[rank][tok], torch.float64)])
+            (ri,) = tr.all_to_all([blocks(p.send_idx, torch.int32)])
+            (rw,) = tr.all_to_all([blocks(p.send_w, torch.float64)])
+            cat = lambda bl, shp: (torch.cat(bl).numpy() if bl else
+                                   np.zeros(shp))
+            dx_r, dw_r, dWl = ref.ep_expert_pass_backward(
+                cat(rx, (0, H)), cat(ri, (0, kk)).reshape(-1, kk),
+                cat(rw, (0, kk)).reshape(-1, kk), cat(rdy, (0, H)),
+                lambda e: weights(rank * Ed + e))
+            for e, gs in dWl.items():
+                dW[e] = gs if e not in dW else tuple(
+                    a + b for a, b in zip(dW[e], gs))
+            sizes = [t.shape[0] for t in rx]
+            (bdx,) = tr.all_to_all([list(torch.split(torch.tensor(dx_r),
+                                                     sizes))])
+            (bdw,) = tr.all_to_all([list(torch.split(torch.tensor(dw_r),
+                                                     sizes))])
+            for d in range(N):
+                for u, t in enumerate(p.uniq_tokens[uo[d]:uo[d + 1]]):
+                    t = t0 + int(t)
+                    dx[t] += bdx[d][u].numpy()
+                    own = [j for j in range(K) if int(idx[t, j]) // Ed == d]
+                    for s, j in enumerate(own):
+                        dtw[t, j] = float(bdw[d][u, s])
+        wdx, wdl, wdW = ref.ep_layer_backward(
+            cfg, N, [a for a, _ in ins], [b for _, b in ins], weights, dys)
+        err = 0.0
+        if Ts[rank]:
+            dl = ref.route_backward(L, idx, dtw, False)
+            err = max(float(np.max(np.abs(dx - wdx[rank]))),
+                      float(np.max(np.abs(dl - wdl[rank]))))
+        for e in range(Ed):
+            got = dW.get(e, (np.zeros((H, F)), np.zeros((H, F)),
+                             np.zeros((F, H))))
+            err = max([err] + [float(np.max(np.abs(g - wdW[i][rank * Ed + e])))
+                               for i, g in enumerate(got)])
+        out[rank] = (err, int(over), n)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("Ts,factor", [([37, 21], 2.0), ([16, 0, 25], 2.0),
+                                       ([40, 33], 0.6)],
+                         ids=["world2", "world3_empty_rank",
+                              "world2_fallback"])
+def test_ep_backward_exchange_over_gloo(Ts, factor):
+    world = len(Ts)
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_ep_bwd_worker, args=(world, port, Ts, factor, out),
+             nprocs=world, join=True)
+    for r in range(world):
+        assert out[r][0] < 1e-6, (r, out[r])
+    if factor < 1.0:
+        assert out[0][1] == 1 and out[0][2] > 1   # the fallback ran

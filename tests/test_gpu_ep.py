@@ -175,6 +175,66 @@ def test_ring_layer_matches_oracle(case):
 
 
 @pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0].name)
+def test_ep_backward_matches_oracle(case):
+    """The EP layer's backward over logical ranks (the forward recomputed
+    pass by pass; the cotangent sent along the dispatch's dedup'd rows,
+    token gradients returned and added, each slot's weight gradient back at
+    its pick, weight gradients summed over the passes, the router backward
+    on each rank) against the oracle's EP backward -- in the fallback too
+    (n4_ovf overflows) -- and, for the token and router gradients, against
+    moe_layer_backward on the ranks' batches together."""
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    g = torch.Generator(device="cuda").manual_seed(78)
+    dys = [torch.randn((T_r, wl.H), generator=g, device="cuda").to(x.dtype)
+           for T_r, x in zip(Ts, xs)]
+    Lt = [torch.from_numpy(L).cuda() for L in Ls]
+    layer = ep.EPLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    dxs, dls, dWs = layer.backward(xs, Lt, dys)
+    torch.cuda.synchronize()
+    mc = ref.MoEConfig(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                       wl.renorm)
+    _, over, n = ref.ep_layer(mc, N, [f64(x) for x in xs], Ls,
+                              ref.dense_weights(*(f64(w) for w in W)))
+    assert layer.info["overflow"] == int(over)
+    assert layer.info["n_chunks"] == n
+    wdx, wdl, wdW = ref.ep_layer_backward(
+        mc, N, [f64(x) for x in xs], Ls,
+        ref.dense_weights(*(f64(w) for w in W)), [f64(d) for d in dys])
+    tol = TOL[wl.dtype]
+    assert_close(np.concatenate([f64(d) for d in dxs]), np.concatenate(wdx),
+                 tol, f"EP dx (N={N}, passes={n})")
+    assert_close(np.concatenate([f64(d) for d in dls]), np.concatenate(wdl),
+                 tol, f"EP dlogits (N={N}, passes={n})")
+    for i, name in enumerate(("dwg", "dwu", "dwd")):
+        got = np.concatenate([f64(t[i]) for t in dWs])
+        assert np.isfinite(got).all()
+        assert_close(got, wdW[i], tol, f"EP {name} (N={N}, passes={n})")
+    # the single-device layer's backward on all tokens at once
+    T = sum(Ts)
+    dev = "cuda"
+    xa, dya = torch.cat(xs), torch.cat(dys)
+    La = torch.cat(Lt)
+    dx1 = torch.empty_like(xa)
+    dl1 = torch.empty((T, wl.E), dtype=torch.float32, device=dev)
+    dw1 = [torch.empty(tuple(w.shape), dtype=torch.float32, device=dev)
+           for w in W]
+    ws = moe.layer_workspace(cfg, moe.MOE_WS_LAYER_BACKWARD)
+    moe.moe_layer_backward(cfg, xa, La, *W, dya, dx1, dl1, *dw1,
+                           moe.MOE_MODE_FALLBACK_LAYER, ws)
+    torch.cuda.synchronize()
+    assert_close(np.concatenate([f64(d) for d in dxs]), f64(dx1), tol,
+                 f"EP dx vs moe_layer_backward (N={N})")
+    assert_close(np.concatenate([f64(d) for d in dls]), f64(dl1), tol,
+                 f"EP dlogits vs moe_layer_backward (N={N})")
+    for i, name in enumerate(("dwg", "dwu", "dwd")):
+        assert_close(np.concatenate([f64(t[i]) for t in dWs]), f64(dw1[i]),
+                     tol, f"EP {name} vs moe_layer_backward (N={N})")
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0].name)
 def test_ring_backward_matches_oracle(case):
     """The ring's backward over logical ranks (cotangent all-gather, each
     rank's expert pass differentiated over all tokens, partial dx summed at
