@@ -53,6 +53,42 @@ def assert_close(got, want, tol: float, what: str = "", scale=None,
     return nw, ew
 
 
+def assert_close_device(pairs, tol: float, what: str = "") -> tuple:
+    """assert_close for device tensors too large to copy to the host: the
+    same two measures over the (got, want) tensor pairs taken together
+    (pieces of one output), computed on the device in float64, a slice of
+    rows at a time."""
+    import torch
+    pairs = [(g, w) for g, w in pairs if g.numel()]
+    dmax, rmax = 0.0, 0.0
+    for got, want in pairs:
+        g2, r2 = got.reshape(got.shape[0], -1), want.reshape(want.shape[0], -1)
+        step = max(1, (1 << 26) // max(1, g2.shape[1]))
+        for a in range(0, g2.shape[0], step):
+            g = g2[a:a + step].to(torch.float64)
+            r = r2[a:a + step].to(torch.float64)
+            if g.numel():
+                dmax = max(dmax, float((g - r).abs().max()))
+                rmax = max(rmax, float(r.abs().max()))
+    nw = dmax / rmax if rmax > 0 else dmax
+    floor = 1e-3 * rmax
+    ew = dmax if floor == 0 else 0.0
+    for got, want in (pairs if floor > 0 else []):
+        g2, r2 = got.reshape(got.shape[0], -1), want.reshape(want.shape[0], -1)
+        step = max(1, (1 << 26) // max(1, g2.shape[1]))
+        for a in range(0, g2.shape[0], step):
+            g = g2[a:a + step].to(torch.float64)
+            r = r2[a:a + step].to(torch.float64)
+            if g.numel():
+                den = torch.clamp(r.abs(), min=floor)
+                ew = max(ew, float(((g - r).abs() / den).max()))
+    RECORDS.append(dict(test=_test_id(), what=what, nw=nw, ew=ew, tol=tol,
+                        cw=None, cw_bound=None))
+    assert nw <= tol, (f"{what}: normwise error {nw:.3g} > {tol} "
+                       f"(max elementwise relative error {ew:.3g})")
+    return nw, ew
+
+
 def summary_lines():
     if not RECORDS:
         return []

@@ -19,7 +19,7 @@ from mixture_experts_token_gb300 import ep
 from oracle import moe_ref as ref
 from synth import WORKLOADS, make_weights, make_x
 from tests.gpu_util import TOL, f64, host_logits, np_
-from tests.parity_log import assert_close
+from tests.parity_log import assert_close, assert_close_device
 
 pytestmark = pytest.mark.gpu
 
@@ -369,4 +369,61 @@ def test_ep_dsv3_full_size_8_ranks():
     want = ref.token_outputs(f64(x_all[ti]), oi, ow, expert_accessor(*W))
     assert_close(f64(y_ep[ti]), want, 2e-2, "EP dsv3 sampled tokens")
     del W, x_all
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", ["ep", "ring"])
+def test_backward_dsv3_full_size_8_ranks(variant):
+    """The DeepSeek-V3-shaped layer's backward over 8 logical ranks of 1024
+    tokens: the EP layer (its global check overflows: 4 passes per rank) and
+    the ring of experts (dropless).  dx, dlogits and the weight gradients
+    match moe_layer_backward on the whole batch (fallback=layer, which
+    equals the dropless gradients) within the tolerance."""
+    wl = WORKLOADS["dsv3"]
+    N, T_r = 8, 1024
+    x_all = make_x(wl, "cuda")
+    L_all = host_logits(wl, x_all)
+    Lt_all = torch.from_numpy(L_all).cuda()
+    xs = [x_all[r * T_r:(r + 1) * T_r] for r in range(N)]
+    Lt = [Lt_all[r * T_r:(r + 1) * T_r] for r in range(N)]
+    g = torch.Generator(device="cuda").manual_seed(79)
+    dy_all = torch.randn(x_all.shape, generator=g, device="cuda").to(
+        x_all.dtype)
+    dys = [dy_all[r * T_r:(r + 1) * T_r] for r in range(N)]
+    W = make_weights(wl, "cuda")
+    cfg = moe.make_config(wl.T, wl.H, wl.E, wl.k, wl.F, N, wl.factor, 0,
+                          wl.dtype)
+    per_rank = ep.local_weights(*W, N)
+    if variant == "ep":
+        layer = ep.EPLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    else:
+        layer = ep.RingLayer(cfg, ep.LoopbackTransport(N), per_rank,
+                             save_x_sorted=True)
+        layer.forward(xs, Lt)
+    dxs, dls, dWs = layer.backward(xs, Lt, dys)
+    torch.cuda.synchronize()
+    if variant == "ep":
+        assert layer.info["overflow"] == 1 and layer.info["n_chunks"] == 4
+    del layer
+    torch.cuda.empty_cache()
+    dx1 = torch.empty_like(x_all)
+    dl1 = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    dw1 = [torch.empty(tuple(w.shape), dtype=torch.float32, device="cuda")
+           for w in W]
+    info = moe.moe_layer_backward(cfg, x_all, Lt_all, *W, dy_all, dx1, dl1,
+                                  *dw1, moe.MOE_MODE_FALLBACK_LAYER,
+                                  moe.layer_workspace(
+                                      cfg, moe.MOE_WS_LAYER_BACKWARD))
+    torch.cuda.synchronize()
+    assert info["overflow"] == 1
+    what = f"{variant} (8 ranks) vs moe_layer_backward, dsv3"
+    El = wl.E // N
+    assert_close_device([(dxs[r], dx1[r * T_r:(r + 1) * T_r])
+                         for r in range(N)], 2e-2, f"{what}: dx")
+    assert_close_device([(dls[r], dl1[r * T_r:(r + 1) * T_r])
+                         for r in range(N)], 2e-2, f"{what}: dlogits")
+    for i, name in enumerate(("dwg", "dwu", "dwd")):
+        assert_close_device([(dWs[r][i], dw1[i][r * El:(r + 1) * El])
+                             for r in range(N)], 2e-2, f"{what}: {name}")
+    del W, x_all, dw1, dWs
     torch.cuda.empty_cache()
