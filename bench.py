@@ -1290,6 +1290,12 @@ class Backward:
         self.dys = torch.empty((R, H), dtype=dt, device=dev)
         self.dxs = torch.empty((R, H), dtype=dt, device=dev)
         self.dtw = torch.empty((T, k), dtype=torch.float32, device=dev)
+        # the split combine backward (bf16 with regrouped weight gradients):
+        # each row's combine weight and the down dgrad's row dots
+        self.parts = max(1, moe.moe_row_dot_parts(c))
+        self.wrow = torch.empty(R, dtype=torch.float32, device=dev)
+        self.rdot = torch.empty(R * self.parts, dtype=torch.float32,
+                                device=dev)
         self.dx = torch.empty((T, H), dtype=dt, device=dev)
         self.dl = torch.empty((T, E), dtype=torch.float32, device=dev)
         self.dw = [torch.empty((E, H, F), dtype=torch.float32, device=dev),
@@ -1377,6 +1383,9 @@ class Backward:
         grp = dict(n_groups=L.G, group_expert=b["group_expert"]) \
             if on_plan else {}
         xs, h, ys = b["x_sorted"], b["h"], b["y_sorted"]
+        # as moe_layer_backward: with bf16 and regrouped weight gradients the
+        # combine weights' gradient comes from the down dgrad (no GEMM2)
+        split = L.regroup and len(passes) <= 64
         while len(L.pass_events) < len(passes):
             L.pass_events.append((torch.cuda.Event(), torch.cuda.Event()))
         ready = [e[0] for e in L.pass_events]
@@ -1405,17 +1414,33 @@ class Backward:
                 # that pass's scatter reads
                 L.tables(passes[i + 1], i + 1, side, ready[i + 1],
                          scattered[i - 1] if i >= 1 else lay.routed)
-            mark("gmm_down")
-            moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"],
-                             **grp)
-            mark("combine_bwd")
-            moe.moe_combine_backward(sc, L.dy[t0:t1], ys[r0:],
-                                     b["row_of"][t0:t1], b["topk_w"][t0:t1],
-                                     L.dys[r0:], L.dtw[t0:t1])
-            mark("gmm_down_dgrad")
-            moe.moe_gmm_down_dgrad(sc, go, W[2], L.g[r0:], L.u[r0:],
-                                   L.dys[r0:], L.dg[r0:], L.du[r0:],
-                                   b["status"], **grp)
+            if split:
+                mark("combine_bwd")
+                moe.moe_combine_backward_rows(
+                    sc, L.dy[t0:t1], b["row_of"][t0:t1], b["topk_w"][t0:t1],
+                    L.dys[r0:], L.wrow[r0:])
+                mark("gmm_down_dgrad")
+                rd = L.rdot[r0 * L.parts:]
+                moe.moe_gmm_down_dgrad_rows(sc, go, W[2], L.g[r0:], L.u[r0:],
+                                            h[r0:], L.dys[r0:], L.wrow[r0:],
+                                            L.dg[r0:], L.du[r0:], rd,
+                                            b["status"], **grp)
+                mark("combine_wgrad")
+                moe.moe_combine_weight_grad(sc, b["row_of"][t0:t1], rd,
+                                            L.dtw[t0:t1])
+            else:
+                mark("gmm_down")
+                moe.moe_gmm_down(sc, h[r0:], go, W[2], ys[r0:], b["status"],
+                                 **grp)
+                mark("combine_bwd")
+                moe.moe_combine_backward(sc, L.dy[t0:t1], ys[r0:],
+                                         b["row_of"][t0:t1],
+                                         b["topk_w"][t0:t1], L.dys[r0:],
+                                         L.dtw[t0:t1])
+                mark("gmm_down_dgrad")
+                moe.moe_gmm_down_dgrad(sc, go, W[2], L.g[r0:], L.u[r0:],
+                                       L.dys[r0:], L.dg[r0:], L.du[r0:],
+                                       b["status"], **grp)
             mark("gmm_gate_up_dgrad")
             moe.moe_gmm_gate_up_dgrad(sc, go, W[0], W[1], L.dg[r0:],
                                       L.du[r0:], L.dxs[r0:], b["status"],
@@ -1430,7 +1455,8 @@ class Backward:
             mark("regroup")
             moe.moe_regroup_rows(c, segs, L.rr, xs, L.dg, L.du, h, L.dys,
                                  L.xs2, L.dg2, L.du2, L.h2, L.dys2, L.off2,
-                                 n_groups=L.G if on_plan else 0)
+                                 n_groups=L.G if on_plan else 0,
+                                 w_row=L.wrow)
             segs, rows = [(L.off2, 0)], L.rr
             wx, wdg, wdu, wh, wdy = L.xs2, L.dg2, L.du2, L.h2, L.dys2
         else:
@@ -1458,11 +1484,13 @@ class Backward:
 def backward_launches(passes, mode, regroup, planned=False, shards=0):
     """Kernel launches of one backward step: route (+ check, + the plan with
     duplicate slots), per pass the permute tables (table_launches) + scatter
-    + GEMM1-saved + GEMM2 + combine backward + two dgrad GEMMs + permute
-    backward, route backward, the regrouping of the rows (2) or the row
-    segments in batches of 16, and per batch the two weight-gradient GEMMs,
-    plus the two fills in the first batch that zero the experts not written
-    by exactly one group."""
+    + GEMM1-saved + the combine backward's dy rows + the down dgrad + the
+    combine weights' gradient + the gate/up dgrad + permute backward (with
+    the row segments in batches: GEMM2 + combine backward + the two dgrads +
+    permute backward), route backward, the regrouping of the rows (2) or the
+    row segments in batches of 16, and per batch the two weight-gradient
+    GEMMs, plus the two fills in the first batch that zero the experts not
+    written by exactly one group."""
     n = len(passes)
     batches = 1 if regroup else (n + 15) // 16
     head = 1 + (1 if (mode == "fallback" or planned) else 0) + \
@@ -1476,6 +1504,8 @@ def backward_work(w, accs):
     """Algorithmic bytes and flops of each backward stage over the step."""
     b = 2 if w.dtype == "bf16" else 4
     H, F, k, E = w.H, w.F, w.k, w.E
+    split = w.dtype == "bf16" and len(accs) <= 64
+    parts = F // 256 if F % 256 == 0 else F // 128
     out = {}
 
     def add(name, by, fl):
@@ -1492,16 +1522,26 @@ def backward_work(w, accs):
         add("permute", T * H * b + R * H * b + 16 * R, 0)
         add("gmm_gate_up_saved", 2 * Ea * H * F * b + R * H * b + 3 * R * F * b,
             4 * R * H * F)
-        add("gmm_down", Ea * F * H * b + R * F * b + R * H * b, 2 * R * F * H)
-        add("combine_bwd", T * H * b + 2 * R * H * b + 12 * T * k, 0)
-        add("gmm_down_dgrad", Ea * F * H * b + R * H * b + 4 * R * F * b,
-            2 * R * H * F)
+        if split:
+            # dy rows unscaled + each row's weight; the dgrad also reads h
+            # and writes the row dots; the weights' gradient sums them
+            add("combine_bwd", T * H * b + R * H * b + 12 * T * k + 4 * R, 0)
+            add("gmm_down_dgrad", Ea * F * H * b + R * H * b + 5 * R * F * b
+                + 4 * R + 4 * R * parts, 2 * R * H * F)
+            add("combine_wgrad", 4 * R * parts + 8 * T * k, 0)
+        else:
+            add("gmm_down", Ea * F * H * b + R * F * b + R * H * b,
+                2 * R * F * H)
+            add("combine_bwd", T * H * b + 2 * R * H * b + 12 * T * k, 0)
+            add("gmm_down_dgrad", Ea * F * H * b + R * H * b + 4 * R * F * b,
+                2 * R * H * F)
         add("gmm_gate_up_dgrad", 2 * Ea * H * F * b + 2 * R * F * b + R * H * b,
             4 * R * H * F)
         add("permute_bwd", R * H * b + T * H * b + 4 * T * k, 0)
     add("route_bwd", 8 * T_tot * E + 8 * T_tot * k, 0)
     # the five row buffers read once and written once (pad rows not counted)
-    add("regroup", 2 * R_tot * (2 * H + 3 * F) * b, 0)
+    add("regroup", 2 * R_tot * (2 * H + 3 * F) * b + (4 * R_tot if split
+                                                       else 0), 0)
     add("gmm_gate_up_wgrad", R_tot * H * b + 2 * R_tot * F * b + 2 * E * H * F * 4,
         4 * R_tot * H * F)
     add("gmm_down_wgrad", R_tot * F * b + R_tot * H * b + E * F * H * 4,

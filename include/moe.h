@@ -612,7 +612,10 @@ moe_status_t moe_gmm_down_wgrad(const moe_config_t *cfg, int32_t n_groups,
  * 1 <= n_segments <= 64.  The source ranges must lie inside the source
  * buffers; a row of the output that no range fills is zero.  n_groups: the
  * groups of the ranges' offsets (0: E; else the virtual groups of
- * moe_plan_duplication, E + S*redundant_slots). */
+ * moe_plan_duplication, E + S*redundant_slots).  w_row (optional, device
+ * float32, indexed by source row; bf16 only): dy_sorted holds unscaled rows
+ * (moe_combine_backward_rows) and each is written times its row's weight,
+ * rounded to bf16 -- the rows moe_combine_backward would have produced. */
 moe_status_t moe_regroup_rows(const moe_config_t *cfg, int32_t n_groups,
                               const moe_row_segment_t *segments,
                               int32_t n_segments, int64_t rows_out,
@@ -621,7 +624,46 @@ moe_status_t moe_regroup_rows(const moe_config_t *cfg, int32_t n_groups,
                               const void *dy_sorted, void *x_out,
                               void *dg_out, void *du_out, void *h_out,
                               void *dy_out, int32_t *out_offsets,
-                              moe_stream_t stream);
+                              const float *w_row, moe_stream_t stream);
+
+/* The split form of the combine backward that moe_layer_backward uses (bf16;
+ * "Support moe_dropless_fallback=layer on the ragged all-to-all MoE path",
+ * pull request 5920, section How: the backward recomputes each pass's
+ * forward).  A combine weight's gradient is dy[t] . y_e(x_t) = dy[t] .
+ * (h Wd) = (dy[t] Wd^T) . h, and dy[t] Wd^T is what the down-projection
+ * dgrad computes, so the pass needs no recomputed y_sorted:
+ *   moe_combine_backward_rows: dy_rows [T*k, H] (layer dtype) row r = dy[t]
+ *     unscaled, w_row [T*k] float32 row r = topk_w[t, j], for every kept
+ *     row r = row_of[t, j] (other rows untouched);
+ *   moe_gmm_down_dgrad_rows: as moe_gmm_down_dgrad on the unscaled rows,
+ *     with dh = w_row[r] * (dy_rows Wd^T)[r] in the SwiGLU backward, and
+ *     row_dot [T*k, moe_row_dot_parts(cfg)] float32: entry (r, q) = the
+ *     dot of (dy_rows Wd^T)[r] with h[r] over the q-th column tile of F
+ *     (h [T*k, F] from the forward);
+ *   moe_combine_weight_grad: dtopk_w [T, k] float32 = the sum over q, in
+ *     order, of row_dot[row_of[t, j], q] (0 for a dropped pick);
+ *   moe_regroup_rows with w_row scales the rows for dWd.
+ * Errors as moe_combine_backward and moe_gmm_down_dgrad; float32 layers:
+ * MOE_ERR_UNSUPPORTED for moe_gmm_down_dgrad_rows. */
+int32_t moe_row_dot_parts(const moe_config_t *cfg);
+moe_status_t moe_combine_backward_rows(const moe_config_t *cfg,
+                                       const void *dy, const int32_t *row_of,
+                                       const float *topk_w, void *dy_rows,
+                                       float *w_row, moe_stream_t stream);
+moe_status_t moe_gmm_down_dgrad_rows(const moe_config_t *cfg,
+                                     int32_t n_groups,
+                                     const int32_t *group_expert,
+                                     const int32_t *group_offsets,
+                                     const void *w_down, const void *g,
+                                     const void *u, const void *h,
+                                     const void *dy_rows, const float *w_row,
+                                     void *dg, void *du, float *row_dot,
+                                     int32_t *status_word,
+                                     moe_stream_t stream);
+moe_status_t moe_combine_weight_grad(const moe_config_t *cfg,
+                                     const int32_t *row_of,
+                                     const float *row_dot, float *dtopk_w,
+                                     moe_stream_t stream);
 
 /* Backward of the grouped SwiGLU FFN (down dgrad, gate/up dgrad, then
  * both weight gradients over one row range).  accumulate != 0 adds the

@@ -132,7 +132,11 @@ def _declare(h):
                                c_int64, P, P, P, c_int32, P, P],
         "moe_regroup_rows": [cfg, c_int32, ctypes.POINTER(MoeRowSegment),
                              c_int32, c_int64, P, P, P, P, P, P, P, P, P, P,
-                             P, P],
+                             P, P, P],
+        "moe_combine_backward_rows": [cfg, P, P, P, P, P, P],
+        "moe_gmm_down_dgrad_rows": [cfg, c_int32, P, P, P, P, P, P, P, P, P,
+                                    P, P, P, P],
+        "moe_combine_weight_grad": [cfg, P, P, P, P],
         "moe_layer_backward": [cfg, P, P, P, P, P, P, P, P, P, P, P, c_int,
                                ctypes.POINTER(MoeLayerInfo), P, P, c_size_t,
                                P],
@@ -162,6 +166,8 @@ def _declare(h):
     h.moe_workspace_bytes.restype = c_size_t
     h.moe_validate_config.argtypes = [cfg]
     h.moe_validate_config.restype = c_int
+    h.moe_row_dot_parts.argtypes = [cfg]
+    h.moe_row_dot_parts.restype = c_int32
     h.moe_capacity_rows.argtypes = [cfg]
     h.moe_capacity_rows.restype = c_int64
     h.moe_chunk_tokens.argtypes = [cfg]
@@ -550,12 +556,40 @@ def moe_gmm_down_wgrad(cfg, segments, rows_total, h, dy_sorted, dw_down,
 
 def moe_regroup_rows(cfg, segments, rows_out, x_sorted, dg, du, h,
                      dy_sorted, x_out, dg_out, du_out, h_out, dy_out,
-                     out_offsets, stream=None, n_groups=0):
+                     out_offsets, stream=None, n_groups=0, w_row=None):
     _check(lib().moe_regroup_rows(
         ctypes.byref(cfg), n_groups, _segments(segments), len(segments), int(rows_out),
         _ptr(x_sorted), _ptr(dg), _ptr(du), _ptr(h), _ptr(dy_sorted),
         _ptr(x_out), _ptr(dg_out), _ptr(du_out), _ptr(h_out), _ptr(dy_out),
-        _ptr(out_offsets), _stream(stream)), "moe_regroup_rows")
+        _ptr(out_offsets), _ptr(w_row), _stream(stream)), "moe_regroup_rows")
+
+
+def moe_row_dot_parts(cfg) -> int:
+    return int(lib().moe_row_dot_parts(ctypes.byref(cfg)))
+
+
+def moe_combine_backward_rows(cfg, dy, row_of, topk_w, dy_rows, w_row,
+                              stream=None):
+    _check(lib().moe_combine_backward_rows(
+        ctypes.byref(cfg), _ptr(dy), _ptr(row_of), _ptr(topk_w),
+        _ptr(dy_rows), _ptr(w_row), _stream(stream)),
+        "moe_combine_backward_rows")
+
+
+def moe_gmm_down_dgrad_rows(cfg, group_offsets, w_down, g, u, h, dy_rows,
+                            w_row, dg, du, row_dot, status_word=None,
+                            stream=None, n_groups=0, group_expert=None):
+    _check(lib().moe_gmm_down_dgrad_rows(
+        ctypes.byref(cfg), n_groups, _ptr(group_expert), _ptr(group_offsets),
+        _ptr(w_down), _ptr(g), _ptr(u), _ptr(h), _ptr(dy_rows), _ptr(w_row),
+        _ptr(dg), _ptr(du), _ptr(row_dot), _ptr(status_word),
+        _stream(stream)), "moe_gmm_down_dgrad_rows")
+
+
+def moe_combine_weight_grad(cfg, row_of, row_dot, dtopk_w, stream=None):
+    _check(lib().moe_combine_weight_grad(
+        ctypes.byref(cfg), _ptr(row_of), _ptr(row_dot), _ptr(dtopk_w),
+        _stream(stream)), "moe_combine_weight_grad")
 
 
 def moe_layer_backward(cfg, x, logits, w_gate, w_up, w_down, dy, dx,

@@ -327,7 +327,68 @@ unsigned blocks_for(long long n, int t) {
   return static_cast<unsigned>((n + t - 1) / t);
 }
 
+// The layer backward's form of the combine backward: each kept row gets its
+// token's output gradient unscaled, dy_rows[r] = dy[t], and its combine
+// weight w_row[r] = topk_w[t, j]; the weight is applied later (to dh in the
+// down-projection dgrad, to the rows of dWd in the regroup), so that the
+// dgrad GEMM yields dh_u = dy[t] Wd^T, whose dot with h is the weight's
+// gradient dy[t] . (h Wd) without recomputing y_sorted.  One CTA per token.
+__global__ void __launch_bounds__(kThreads) gather_dy_rows_kernel(
+    const int4* __restrict__ dy, const int32_t* __restrict__ row_of,
+    const float* __restrict__ topk_w, int k, int n16,
+    int4* __restrict__ dy_rows, float* __restrict__ w_row) {
+  const long long t = blockIdx.x;
+  const int4* src = dy + t * n16;
+  for (int j = 0; j < k; ++j) {
+    const int r = __ldg(row_of + t * k + j);
+    if (r < 0) continue;
+    if (threadIdx.x == 0) w_row[r] = __ldg(topk_w + t * k + j);
+    int4* dst = dy_rows + static_cast<long long>(r) * n16;
+    for (int c = threadIdx.x; c < n16; c += kThreads) dst[c] = __ldg(src + c);
+  }
+}
+
+// dtopk_w[t, j] = sum over the dgrad's column tiles q (in order) of
+// row_dot[r * n_parts + q] for the kept row r of pick (t, j); 0 if dropped.
+__global__ void dtopk_from_row_dots_kernel(const int32_t* __restrict__ row_of,
+                                           const float* __restrict__ row_dot,
+                                           int n_parts, long long n,
+                                           float* __restrict__ dtopk_w) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x +
+                      threadIdx.x;
+  if (i >= n) return;
+  const int r = __ldg(row_of + i);
+  float v = 0.0f;
+  if (r >= 0) {
+    const float* d = row_dot + static_cast<long long>(r) * n_parts;
+    for (int q = 0; q < n_parts; ++q) v += __ldg(d + q);
+  }
+  dtopk_w[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_gather_dy_rows(const moe_config_t& c, const void* dy,
+                                  const int32_t* row_of, const float* topk_w,
+                                  void* dy_rows, float* w_row,
+                                  cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  gather_dy_rows_kernel<<<c.T, kThreads, 0, s>>>(
+      static_cast<const int4*>(dy), row_of, topk_w, c.k,
+      c.H * elem_bytes(c.dtype) / 16, static_cast<int4*>(dy_rows), w_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dtopk_from_row_dots(const moe_config_t& c,
+                                       const int32_t* row_of,
+                                       const float* row_dot, int n_parts,
+                                       float* dtopk_w, cudaStream_t s) {
+  const long long n = static_cast<long long>(c.T) * c.k;
+  if (n == 0) return cudaSuccess;
+  dtopk_from_row_dots_kernel<<<blocks_for(n, 256), 256, 0, s>>>(
+      row_of, row_dot, n_parts, n, dtopk_w);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy,
                                     const void* y_sorted,

@@ -75,6 +75,11 @@ struct Params {
   __nv_bfloat16* out3 = nullptr;        // MODE 4: g
   const __nv_bfloat16* aux_g = nullptr; // MODE 2: g
   const __nv_bfloat16* aux_u = nullptr; // MODE 2: u
+  // MODE 2 with unscaled dy rows: dh = row_w[r] * acc, and row_dot[r *
+  // n_tiles + n] = acc . h over the tile's columns (h = aux_h)
+  const float* row_w = nullptr;
+  const __nv_bfloat16* aux_h = nullptr;
+  float* row_dot = nullptr;
   int k_split = 0;                      // MODE 3: k-blocks from the 1st pair
   // MODE 5 (router logits): float32 output [rows, out_ld], an optional
   // float32 offset of the same shape added to it, and the row count of the
@@ -447,13 +452,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (MODE == 2) {
-        // dh (TMEM) -> dg = dh * u * silu'(g), du = dh * silu(g)
+        // dh (TMEM) -> dg = dh * u * silu'(g), du = dh * silu(g); with
+        // unscaled dy rows dh = w_r * acc and the row's dot acc . h is kept
         const long long base = static_cast<long long>(grow) * p.out_ld + n * BN;
+        const bool unscaled = p.row_w != nullptr;
+        const float wr = unscaled && valid ? __ldg(p.row_w + grow) : 1.0f;
+        float rdot = 0.0f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c, r);
           if (!valid) continue;
+          if (unscaled) {
+            const uint4* hs =
+                reinterpret_cast<const uint4*>(p.aux_h + base + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 hq = hs[v];
+              const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int e0 = 8 * v + 2 * i;
+                const float a0 = __uint_as_float(r[e0]);
+                const float a1 = __uint_as_float(r[e0 + 1]);
+                rdot = fmaf(a0, __uint_as_float(hw[i] << 16), rdot);
+                rdot = fmaf(a1, __uint_as_float(hw[i] & 0xffff0000u), rdot);
+                r[e0] = __float_as_uint(wr * a0);
+                r[e0 + 1] = __float_as_uint(wr * a1);
+              }
+            }
+          }
           uint32_t gk[16], uk[16];
           const uint4* gs = reinterpret_cast<const uint4*>(p.aux_g + base + c);
           const uint4* us = reinterpret_cast<const uint4*>(p.aux_u + base + c);
@@ -493,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pu[4 * v + 3]);
           }
         }
+        if (unscaled && valid)
+          p.row_dot[static_cast<long long>(grow) * p.n_tiles + n] = rdot;
       } else if (MODE == 5) {
         // float32 logits (+ the offset), one row per thread
         const long long base =
@@ -955,7 +985,8 @@ cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
                                    const void* w_down, const void* gbuf,
                                    const void* ubuf, const void* dy_sorted,
                                    void* dg, void* du, int32_t* status,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, const float* w_row,
+                                   const void* h, float* row_dot) {
   const uint64_t rows = static_cast<uint64_t>(c.T) * c.k;
   if (rows == 0) return cudaSuccess;
   const uint64_t E = static_cast<uint64_t>(c.E);
@@ -969,6 +1000,12 @@ cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
   p.out2 = static_cast<__nv_bfloat16*>(du);
   p.aux_g = static_cast<const __nv_bfloat16*>(gbuf);
   p.aux_u = static_cast<const __nv_bfloat16*>(ubuf);
+  if (w_row != nullptr) {
+    if (h == nullptr || row_dot == nullptr) return cudaErrorInvalidValue;
+    p.row_w = w_row;
+    p.aux_h = static_cast<const __nv_bfloat16*>(h);
+    p.row_dot = row_dot;
+  }
   return bn == 256 ? tc::launch_one<2, 256>(ad, bd, bd, ad, p, s)
                    : tc::launch_one<2, 128>(ad, bd, bd, ad, p, s);
 }

@@ -224,6 +224,17 @@ cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy,
                                     const int32_t* row_of,
                                     const float* topk_w, void* dy_sorted,
                                     float* dtopk_w, cudaStream_t s);
+// The layer backward's split form of the combine backward (bf16): unscaled
+// dy rows and per-row weights now, the weights' gradient from the
+// down-projection dgrad's per-tile row dots afterwards.
+cudaError_t launch_gather_dy_rows(const moe_config_t& c, const void* dy,
+                                  const int32_t* row_of, const float* topk_w,
+                                  void* dy_rows, float* w_row,
+                                  cudaStream_t s);
+cudaError_t launch_dtopk_from_row_dots(const moe_config_t& c,
+                                       const int32_t* row_of,
+                                       const float* row_dot, int n_parts,
+                                       float* dtopk_w, cudaStream_t s);
 cudaError_t launch_route_backward(const moe_config_t& c, const float* logits,
                                   const int32_t* topk_idx,
                                   const float* dtopk_w, float* dlogits,
@@ -256,12 +267,21 @@ cudaError_t launch_gate_up_saved_bf16(const moe_config_t& c, const Groups& g,
                                       const void* w_gate, const void* w_up,
                                       void* gbuf, void* ubuf, void* h,
                                       int32_t* status, cudaStream_t s);
+// With w_row: dy_sorted holds unscaled rows; the epilogue scales dh by
+// w_row[r], and writes row_dot[r * (F / bn) + q] = dh_u . h over the
+// column tile q (bn = 256 if F % 256 == 0, else 128), h [rows, F] bf16.
 cudaError_t launch_down_dgrad_bf16(const moe_config_t& c, const Groups& g,
                                    const int32_t* group_offsets,
                                    const void* w_down, const void* gbuf,
                                    const void* ubuf, const void* dy_sorted,
                                    void* dg, void* du, int32_t* status,
-                                   cudaStream_t s);
+                                   cudaStream_t s,
+                                   const float* w_row = nullptr,
+                                   const void* h = nullptr,
+                                   float* row_dot = nullptr);
+inline int down_dgrad_col_tiles(const moe_config_t& c) {
+  return c.F % 256 == 0 ? c.F / 256 : c.F / 128;
+}
 cudaError_t launch_gate_up_dgrad_bf16(const moe_config_t& c, const Groups& g,
                                       const int32_t* group_offsets,
                                       const void* w_gate, const void* w_up,
@@ -305,13 +325,15 @@ inline int64_t regroup_rows(const moe_config_t& c) {
   return static_cast<int64_t>(c.T) * c.k +
          16 * static_cast<int64_t>(num_groups(c));
 }
+// w_row (optional): dys holds unscaled rows; dys2 gets them times w_row
+// of their source row, rounded to bf16.
 cudaError_t launch_regroup(const moe_config_t& c, int G,
                            const WgradSegment* seg,
                            int n_seg, int64_t rows_out, const void* xs,
                            const void* dg, const void* du, const void* h,
                            const void* dys, void* xs2, void* dg2, void* du2,
                            void* h2, void* dys2, int32_t* out_off,
-                           cudaStream_t s);
+                           cudaStream_t s, const float* w_row = nullptr);
 size_t gmm_backward_bytes(const moe_config_t& c);
 size_t layer_backward_bytes(const moe_config_t& c);
 

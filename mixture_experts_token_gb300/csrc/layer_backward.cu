@@ -32,6 +32,10 @@ struct BwdBufs {
   void *g, *u, *dg, *du;  // [T*k, F]
   void *dys, *dxs;        // [T*k, H]
   float* dtw;             // [T, k]
+  // bf16 with regrouped weight gradients: dys holds unscaled dy rows, wrow
+  // their combine weights, rdot the down dgrad's per-column-tile row dots
+  float* wrow;            // [T*k]
+  float* rdot;            // [T*k, F / 128]
   int32_t* seg_off;       // [n_seg, G + 1] group offsets of every pass
   // the passes' rows regrouped for the weight gradients (regroup.cu)
   void *xs2, *dg2, *du2, *h2, *dys2;  // [T*k + 16*E, H or F]
@@ -59,6 +63,8 @@ BwdBufs carve_bwd(void* base, const moe_config_t& c, int n_seg,
   b.dys = cv.take<char>(rows * c.H * eb);
   b.dxs = cv.take<char>(rows * c.H * eb);
   b.dtw = cv.take<float>(rows);
+  b.wrow = cv.take<float>(rows);
+  b.rdot = cv.take<float>(rows * static_cast<size_t>(c.F / 128));
   b.seg_off =
       cv.take<int32_t>(static_cast<size_t>(n_seg) * (num_groups(c) + 1));
   const size_t rr = static_cast<size_t>(regroup_rows(c));
@@ -81,10 +87,15 @@ void* rows_at(const void* p, size_t row, size_t row_bytes) {
 // [t0*k, (t0+tc)*k) of the row buffers and its group offsets row `seg` of
 // the segment table.  planned: over the virtual groups of the duplication
 // plan in b (each computing with its expert's weights).
+// unscaled (bf16, regrouped weight gradients): the combine weights' gradient
+// comes from the down dgrad -- dy[t] . (h Wd) = (dy[t] Wd^T) . h -- so the
+// pass does not recompute y_sorted = h Wd; dys keeps the unscaled dy rows
+// and the regroup applies the weights for dWd.
 cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
                      bool planned, int seg, const void* x, const void* wg,
                      const void* wu, const void* wd, const void* dy, void* dx,
-                     const BwdBufs& b, int32_t* status, cudaStream_t s) {
+                     const BwdBufs& b, bool unscaled, int32_t* status,
+                     cudaStream_t s) {
   moe_config_t sc = c;
   sc.T = tc;
   const size_t eb = elem_bytes(c.dtype);
@@ -117,6 +128,23 @@ cudaError_t bwd_pass(const moe_config_t& c, int t0, int tc, int64_t cap,
       b.f.uniq_offsets, b.f.uniq_tokens, b.f.expand_idx + base, b.f.n_dropped,
       b.f.pws, status, s, plan);
   if (e != cudaSuccess) return e;
+  if (unscaled) {
+    const int nt = down_dgrad_col_tiles(c);
+    float* rd = b.rdot + base * nt;
+    if ((e = launch_gate_up_saved(sc, ids, xs, goff, wg, wu, gg, uu, h,
+                                  status, s)) != cudaSuccess ||
+        (e = launch_gather_dy_rows(sc, rows_at(dy, t0, hb), row_of, w, dys,
+                                   b.wrow + base, s)) != cudaSuccess ||
+        (e = launch_down_dgrad_bf16(sc, ids, goff, wd, gg, uu, dys, dg, du,
+                                    status, s, b.wrow + base, h, rd)) !=
+            cudaSuccess ||
+        (e = launch_dtopk_from_row_dots(sc, row_of, rd, nt, b.dtw + base,
+                                        s)) != cudaSuccess ||
+        (e = launch_gate_up_dgrad(sc, ids, goff, wg, wu, dg, du, dxs, status,
+                                  s)) != cudaSuccess)
+      return e;
+    return launch_combine(sc, dxs, row_of, nullptr, rows_at(dx, t0, hb), s);
+  }
   if ((e = launch_gate_up_saved(sc, ids, xs, goff, wg, wu, gg, uu, h, status,
                                 s)) != cudaSuccess ||
       (e = launch_gmm2(sc, ids, h, goff, wd, ys, status, s)) != cudaSuccess ||
@@ -471,7 +499,7 @@ moe_status_t moe_regroup_rows(const moe_config_t* cfg, int32_t n_groups,
                               const void* dy_sorted, void* x_out,
                               void* dg_out, void* du_out, void* h_out,
                               void* dy_out, int32_t* out_offsets,
-                              moe_stream_t stream) {
+                              const float* w_row, moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   const int G = n_groups == 0 ? cfg->E : n_groups;
@@ -487,11 +515,78 @@ moe_status_t moe_regroup_rows(const moe_config_t* cfg, int32_t n_groups,
   if (!ok_ptr(x_sorted, true) || !ok_ptr(dg, true) || !ok_ptr(du, true) ||
       !ok_ptr(h, true) || !ok_ptr(dy_sorted, true) || !ok_ptr(x_out, true) ||
       !ok_ptr(dg_out, true) || !ok_ptr(du_out, true) || !ok_ptr(h_out, true) ||
-      !ok_ptr(dy_out, true) || !ok_ptr(out_offsets, false))
+      !ok_ptr(dy_out, true) || !ok_ptr(out_offsets, false) ||
+      (w_row != nullptr && !ok_ptr(w_row, false)))
     return MOE_ERR_INVALID_ARG;
+  if (w_row != nullptr && cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return cuda_st(launch_regroup(*cfg, G, segments, n_segments, rows_out,
                                 x_sorted, dg, du, h, dy_sorted, x_out, dg_out,
-                                du_out, h_out, dy_out, out_offsets, stream));
+                                du_out, h_out, dy_out, out_offsets, stream,
+                                w_row));
+}
+
+int32_t moe_row_dot_parts(const moe_config_t* cfg) {
+  if (cfg == nullptr || validate(cfg) != MOE_OK || cfg->F < 1) return -1;
+  return down_dgrad_col_tiles(*cfg);
+}
+
+moe_status_t moe_combine_backward_rows(const moe_config_t* cfg,
+                                       const void* dy, const int32_t* row_of,
+                                       const float* topk_w, void* dy_rows,
+                                       float* w_row, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(dy, true) || !ok_ptr(row_of, false) ||
+      !ok_ptr(topk_w, false) || !ok_ptr(dy_rows, true) ||
+      !ok_ptr(w_row, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_gather_dy_rows(*cfg, dy, row_of, topk_w, dy_rows,
+                                       w_row, stream));
+}
+
+moe_status_t moe_gmm_down_dgrad_rows(const moe_config_t* cfg,
+                                     int32_t n_groups,
+                                     const int32_t* group_expert,
+                                     const int32_t* group_offsets,
+                                     const void* w_down, const void* g,
+                                     const void* u, const void* h,
+                                     const void* dy_rows, const float* w_row,
+                                     void* dg, void* du, float* row_dot,
+                                     int32_t* status_word,
+                                     moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype != MOE_BF16 || !gmm_shape_ok(*cfg))
+    return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  Groups grp;
+  if (!bwd_groups(*cfg, n_groups, group_expert, &grp) ||
+      !ok_ptr(group_offsets, false) || !ok_ptr(w_down, true) ||
+      !ok_ptr(g, true) || !ok_ptr(u, true) || !ok_ptr(h, true) ||
+      !ok_ptr(dy_rows, true) || !ok_ptr(w_row, false) || !ok_ptr(dg, true) ||
+      !ok_ptr(du, true) || !ok_ptr(row_dot, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_down_dgrad_bf16(*cfg, grp, group_offsets, w_down, g,
+                                        u, dy_rows, dg, du, status_word,
+                                        stream, w_row, h, row_dot));
+}
+
+moe_status_t moe_combine_weight_grad(const moe_config_t* cfg,
+                                     const int32_t* row_of,
+                                     const float* row_dot, float* dtopk_w,
+                                     moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->F < 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(row_of, false) || !ok_ptr(row_dot, false) ||
+      !ok_ptr(dtopk_w, false))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_st(launch_dtopk_from_row_dots(*cfg, row_of, row_dot,
+                                            down_dgrad_col_tiles(*cfg),
+                                            dtopk_w, stream));
 }
 
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
@@ -586,10 +681,16 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
   }
   std::vector<WgradSegment> segs;
   const size_t G1 = static_cast<size_t>(num_groups(*cfg)) + 1;
+  // the tensor-core path with regrouped rows takes the weights' gradient
+  // from the down dgrad (bwd_pass) and scales dWd's rows in the regroup
+  const bool regrouped =
+      cfg->dtype == MOE_BF16 &&
+      passes.size() <= static_cast<size_t>(kMaxRegroupSegments);
   for (size_t i = 0; i < passes.size(); ++i) {
     const Pass& p = passes[i];
     e = bwd_pass(*cfg, p.t0, p.tc, p.cap, p.planned, static_cast<int>(i), x,
-                 w_gate, w_up, w_down, dy, dx, b, status_word, stream);
+                 w_gate, w_up, w_down, dy, dx, b, regrouped, status_word,
+                 stream);
     if (e != cudaSuccess) return cuda_st(e);
     segs.push_back({b.seg_off + i * G1, p.t0 * cfg->k});
   }
@@ -601,14 +702,14 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
   e = launch_route_backward(*cfg, logits, b.f.topk_idx, b.dtw, dlogits,
                             stream);
   if (e != cudaSuccess) return cuda_st(e);
-  if (cfg->dtype == MOE_BF16 &&
-      segs.size() <= static_cast<size_t>(kMaxRegroupSegments)) {
-    // one 16-row-aligned row range per expert for the tensor-core GEMMs
+  if (regrouped) {
+    // one 16-row-aligned row range per expert for the tensor-core GEMMs;
+    // the dy rows get their combine weights on the way
     const int64_t rr = regroup_rows(*cfg);
     e = launch_regroup(*cfg, wgroups.n, segs.data(),
                        static_cast<int>(segs.size()), rr, b.f.x_sorted, b.dg,
                        b.du, b.f.h, b.dys, b.xs2, b.dg2, b.du2, b.h2, b.dys2,
-                       b.off2, stream);
+                       b.off2, stream, b.wrow);
     if (e != cudaSuccess) return cuda_st(e);
     const WgradSegment one{b.off2, 0};
     return cuda_st(launch_wgrad(*cfg, wgroups, &one, 1, rr,

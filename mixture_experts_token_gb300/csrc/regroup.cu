@@ -13,8 +13,12 @@
 // Kernel 1 (one CTA): out_off[g] = exclusive scan of roundup16(rows of g).
 // Kernel 2: one warp per destination row: find its group (binary search) and
 // its source range, copy the five rows with 16-byte loads and stores, or
-// write zeros for a pad row.  Algorithmic traffic: the rows of the five
+// write zeros for a pad row.  Given per-row combine weights, the output
+// gradient rows are scaled by their weight on the way (the layer backward
+// keeps them unscaled until here).  Algorithmic traffic: the rows of the five
 // buffers read once and written once.
+#include <cuda_bf16.h>
+
 #include "internal.h"
 
 namespace moe {
@@ -71,11 +75,31 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ src,
   for (int c = lane; c < n16; c += 32) dst[c] = zero ? z : __ldg(src + c);
 }
 
+// dst = bf16(w * src) for one bf16 row (the combine backward's scaling of
+// an output-gradient row by its combine weight).
+__device__ __forceinline__ void scale_row_bf16(const uint4* __restrict__ src,
+                                               uint4* __restrict__ dst,
+                                               int n16, int lane, float w) {
+  for (int c = lane; c < n16; c += 32) {
+    const uint4 q = __ldg(src + c);
+    const uint32_t in[4] = {q.x, q.y, q.z, q.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 pr = __floats2bfloat162_rn(
+          w * __uint_as_float(in[i] << 16),
+          w * __uint_as_float(in[i] & 0xffff0000u));
+      out[i] = *reinterpret_cast<uint32_t*>(&pr);
+    }
+    dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 __global__ void __launch_bounds__(256) regroup_rows_kernel(
     RegroupParams p, const int32_t* __restrict__ out_off, const uint4* xs,
     const uint4* dg, const uint4* du, const uint4* h, const uint4* dys,
     uint4* xs2, uint4* dg2, uint4* du2, uint4* h2, uint4* dys2, int h16,
-    int f16) {
+    int f16, const float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
   const long long warp =
       (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -106,7 +130,11 @@ __global__ void __launch_bounds__(256) regroup_rows_kernel(
     const bool zero = src < 0;  // a pad row
     const long long sr = zero ? 0 : src;
     copy_row(xs + sr * h16, xs2 + d * h16, h16, lane, zero);
-    copy_row(dys + sr * h16, dys2 + d * h16, h16, lane, zero);
+    if (w_row != nullptr && !zero)
+      scale_row_bf16(dys + sr * h16, dys2 + d * h16, h16, lane,
+                     __ldg(w_row + sr));
+    else
+      copy_row(dys + sr * h16, dys2 + d * h16, h16, lane, zero);
     copy_row(dg + sr * f16, dg2 + d * f16, f16, lane, zero);
     copy_row(du + sr * f16, du2 + d * f16, f16, lane, zero);
     copy_row(h + sr * f16, h2 + d * f16, f16, lane, zero);
@@ -121,9 +149,9 @@ cudaError_t launch_regroup(const moe_config_t& c, int G,
                            const void* dg, const void* du, const void* h,
                            const void* dys, void* xs2, void* dg2, void* du2,
                            void* h2, void* dys2, int32_t* out_off,
-                           cudaStream_t s) {
+                           cudaStream_t s, const float* w_row) {
   if (n_seg < 1 || n_seg > kMaxRegroupSegments || G < 1 ||
-      G > kRegroupThreads)
+      G > kRegroupThreads || (w_row != nullptr && c.dtype != MOE_BF16))
     return cudaErrorInvalidValue;
   RegroupParams p{};
   for (int i = 0; i < n_seg; ++i) {
@@ -150,7 +178,7 @@ cudaError_t launch_regroup(const moe_config_t& c, int G,
       static_cast<const uint4*>(dys), static_cast<uint4*>(xs2),
       static_cast<uint4*>(dg2), static_cast<uint4*>(du2),
       static_cast<uint4*>(h2), static_cast<uint4*>(dys2), c.H * eb / 16,
-      c.F * eb / 16);
+      c.F * eb / 16, w_row);
   return cudaGetLastError();
 }
 

@@ -187,14 +187,32 @@ def test_backward_arguments_are_rejected_before_any_launch(m):
     args = (p, p, p, p, p, p, p, p, p, p, p)
     rows = c.T * c.k + 16 * c.E
     assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 0, rows, *args,
-                                None) == m.MOE_ERR_INVALID_ARG
+                                None, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 65, rows, *args,
-                                None) == m.MOE_ERR_INVALID_ARG
+                                None, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_regroup_rows(ctypes.byref(c), 0, seg, 1, rows - 1, *args,
-                                None) == m.MOE_ERR_INVALID_ARG
+                                None, None) == m.MOE_ERR_INVALID_ARG
     # a group count beyond the configuration's groups
     assert lib.moe_regroup_rows(ctypes.byref(c), c.E + 1, seg, 1, rows,
-                                *args, None) == m.MOE_ERR_INVALID_ARG
+                                *args, None, None) == m.MOE_ERR_INVALID_ARG
+    # per-row weights are a bf16 path
+    c32 = cfg_of(m, H=128, dtype="f32")
+    assert lib.moe_regroup_rows(ctypes.byref(c32), 0, seg, 1, rows, *args,
+                                p, None) == m.MOE_ERR_UNSUPPORTED
+    # the split combine backward: parts per row, f32 rejected, bad pointers
+    assert m.moe_row_dot_parts(c) == c.F // 128           # F = 128
+    assert m.moe_row_dot_parts(cfg_of(m, F=512)) == 2      # 256-wide tiles
+    assert m.moe_row_dot_parts(cfg_of(m, F=384)) == 3
+    assert lib.moe_gmm_down_dgrad_rows(
+        ctypes.byref(c32), 0, None, p, p, p, p, p, p, p, p, p, p, None,
+        None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_gmm_down_dgrad_rows(
+        ctypes.byref(c), 0, None, p, p, p, p, None, p, p, p, p, p, None,
+        None) == m.MOE_ERR_INVALID_ARG                      # h missing
+    assert lib.moe_combine_backward_rows(ctypes.byref(c), p, p, p, p, None,
+                                         None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_weight_grad(ctypes.byref(c), p, None, p,
+                                       None) == m.MOE_ERR_INVALID_ARG
     # a group map without its group count
     assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, p, seg, 1, rows, p, p,
                                   p, 0, None, None) == m.MOE_ERR_INVALID_ARG

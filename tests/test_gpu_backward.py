@@ -265,6 +265,95 @@ def test_combine_backward_exact_small():
                                                      np.abs(ysh[r]) + 1e-30)
 
 
+@pytest.mark.parametrize("F", [512, 384], ids=["F512_256wide", "F384_128wide"])
+def test_split_combine_backward(F):
+    """The split combine backward moe_layer_backward uses: dy rows unscaled
+    and each row's weight (exact copies); the down dgrad on them scales dh
+    by the row's weight and writes per-column-tile dots of dy Wd^T with h;
+    their ordered sum is each pick's weight gradient dy[t] . (h Wd), within
+    the bf16-product bound of the float64 value; dg and du match the float64
+    SwiGLU backward; and the regroup with the row weights writes exactly the
+    weighted rows moe_combine_backward produces (dropped rows included)."""
+    wl = BWD[1].with_(name="split", T=96, F=F)
+    x, L, W, dy = setup(wl)
+    cfg = cfg_from(wl, factor=0.5)
+    b = moe.alloc_step_buffers(cfg)
+    Ld = torch.from_numpy(L).cuda()
+    moe.moe_route(cfg, Ld, b["topk_idx"], b["topk_w"], b["status"])
+    moe.moe_permute(cfg, x, b["topk_idx"], 1, b["x_sorted"], b["row_of"],
+                    b["sorted_token"], b["group_offsets"], b["uniq_offsets"],
+                    b["uniq_tokens"], b["expand_idx"], b["n_dropped"],
+                    b["permute_ws"])
+    R, H = wl.T * wl.k, wl.H
+    g = torch.empty((R, F), dtype=x.dtype, device="cuda")
+    u, h = torch.empty_like(g), torch.empty_like(g)
+    ys = torch.empty((R, H), dtype=x.dtype, device="cuda")
+    moe.moe_gmm_swiglu_saved(cfg, b["x_sorted"], b["group_offsets"], *W, g,
+                             u, h, ys, b["status"])
+    parts = moe.moe_row_dot_parts(cfg)
+    assert parts == (F // 256 if F % 256 == 0 else F // 128)
+    dyr = torch.zeros((R, H), dtype=x.dtype, device="cuda")
+    wrow = torch.full((R,), float("nan"), device="cuda")
+    moe.moe_combine_backward_rows(cfg, dy, b["row_of"], b["topk_w"], dyr,
+                                  wrow)
+    dg = torch.empty_like(g)
+    du = torch.empty_like(g)
+    rdot = torch.full((R * parts,), float("nan"), device="cuda")
+    moe.moe_gmm_down_dgrad_rows(cfg, b["group_offsets"], W[2], g, u, h, dyr,
+                                wrow, dg, du, rdot, b["status"])
+    dtw = torch.full((wl.T, wl.k), float("nan"), device="cuda")
+    moe.moe_combine_weight_grad(cfg, b["row_of"], rdot, dtw)
+    # the weighted rows the other form writes, and the regroup's scaling
+    dys_w = torch.zeros_like(dyr)
+    dtw_w = torch.empty_like(dtw)
+    moe.moe_combine_backward(cfg, dy, ys, b["row_of"], b["topk_w"], dys_w,
+                             dtw_w)
+    off = b["group_offsets"]
+    rr = R + 16 * wl.E
+    bufs = [torch.zeros((rr, n), dtype=x.dtype, device="cuda")
+            for n in (H, F, F, F, H)]
+    off2 = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    moe.moe_regroup_rows(cfg, [(off, 0)], rr, b["x_sorted"], dg, du, h, dyr,
+                         *bufs, off2, w_row=wrow)
+    bufs_w = [torch.zeros_like(t) for t in bufs]
+    moe.moe_regroup_rows(cfg, [(off, 0)], rr, b["x_sorted"], dg, du, h,
+                         dys_w, *bufs_w, off2)
+    torch.cuda.synchronize()
+    assert int(b["status"].item()) == 0
+    assert torch.equal(bufs[4], bufs_w[4])
+    row_of = np_(b["row_of"]).astype(np.int64)
+    w = np_(b["topk_w"]).astype(np.float64)
+    assert (row_of < 0).any()
+    dyh, dyrh, hh = f64(dy), f64(dyr), f64(h)
+    wd = f64(W[2])
+    goff = np_(off)
+    expert = np.searchsorted(goff, np.arange(R), side="right") - 1
+    dtwh = f64(dtw)
+    for t in range(wl.T):
+        for j in range(wl.k):
+            r = row_of[t, j]
+            if r < 0:
+                assert dtwh[t, j] == 0.0
+                continue
+            assert np.array_equal(dyrh[r], dyh[t])
+            assert float(np_(wrow)[r]) == np.float32(w[t, j])
+            e = expert[r]
+            dh_u = wd[e] @ dyh[t]                    # dy Wd^T, float64
+            want = float(dh_u @ hh[r])
+            bound = 2.0 ** -8 * float(np.abs(wd[e]) @ np.abs(dyh[t]) @
+                                      np.abs(hh[r])) + 1e-30
+            assert abs(dtwh[t, j] - want) <= bound, (t, j)
+    kept = [r for r in range(R) if r < goff[-1]]
+    gh, uh = f64(g)[kept], f64(u)[kept]
+    dh = np.stack([float(np_(wrow)[r]) * (wd[expert[r]] @ dyrh[r])
+                   for r in kept])
+    s_ = 1.0 / (1.0 + np.exp(-gh))
+    assert_close(f64(dg)[kept], dh * uh * s_ * (1.0 + gh * (1.0 - s_)),
+                 2e-2, "split dg")
+    assert_close(f64(du)[kept], dh * gh * s_, 2e-2, "split du")
+    assert_close(f64(dtw), f64(dtw_w), 2e-2, "split dtopk_w vs dy . y_sorted")
+
+
 def test_regroup_rows_layout():
     """moe_regroup_rows: group e of the output holds e's rows of every range
     in range order (byte copies), starts at the exclusive scan of the
