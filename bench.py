@@ -121,15 +121,21 @@ def load_peaks():
 
 
 def kernel_source_digest(kernel):
-    """First 16 hex digits of the sha256 of the sources a GEMM kernel is
-    built from (the shared tensor-core header + its own file)."""
+    """First 16 hex digits of the sha256 of the code a GEMM kernel is built
+    from (the shared tensor-core header + its own file), comments and blank
+    lines left out, so that an edit of a comment keeps a profile valid."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "mixture_experts_token_gb300", "csrc")
     own = "wgrad_tc.cu" if kernel.endswith("_wgrad") else "gmm_tc.cu"
     h = hashlib.sha256()
     for name in ("tc_common.cuh", own):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        lines = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in
+                 src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -201,7 +201,9 @@ __device__ void build_tile_table(const int32_t* __restrict__ off, int G,
 // MODE 1: out = y_sorted = A Wd, BN = 256 or 128
 // MODE 4: MODE 0 that also stores g (out3) and u (out2) for the backward
 // MODE 2: dh = dy_sorted Wd^T with Wd read K-major (one 64 x 256 box); the
-//         epilogue turns dh into dg (out) and du (out2) with g, u (aux_*)
+//         epilogue turns dh into dg (out) and du (out2) with g, u (aux_*);
+//         on unscaled dy rows (row_w set) dh = row_w[r] * acc and the row's
+//         dot acc . h (aux_h) over the tile goes to row_dot
 // MODE 3: dx_sorted = [dg | du] [Wg^T ; Wu^T]: K = 2F, the first k_split
 //         k-blocks from (tmA, tmB0), the rest from (tmA1, tmB1), K-major B
 // MODE 5: router logits = x Wr (+ offset) in float32: one group of rows1

@@ -114,15 +114,19 @@ def test_layer_backward_matches_oracle(wl, mode, factor):
     compare(out, g, TOL[wl.dtype])
 
 
-def test_fallback_backward_many_chunks():
-    """More chunks than one weight-gradient launch takes (segments are
-    handled 16 at a time, the later batches adding into dW)."""
-    wl = BWD[1].with_(name="bwd_chunks", T=700, n_chunks=20)
+@pytest.mark.parametrize("n_chunks", [20, 70], ids=["regrouped", "segments"])
+def test_fallback_backward_many_chunks(n_chunks):
+    """Many fallback chunks: 20 are regrouped into one row range per expert
+    (the combine weights' gradient from the down dgrad); 70 are more than
+    the regroup takes, so the combine backward reads a recomputed y_sorted
+    and the weight gradients sum the row segments 16 at a time, the later
+    batches adding into dW."""
+    wl = BWD[1].with_(name="bwd_chunks", T=700, n_chunks=n_chunks)
     x, L, W, dy = setup(wl)
     cfg = cfg_from(wl, factor=1.0)
     out, info = gpu_layer_backward(cfg, x, L, W, dy,
                                    moe.MOE_MODE_FALLBACK_LAYER)
-    assert info["overflow"] == 1 and info["n_chunks"] == 20
+    assert info["overflow"] == 1 and info["n_chunks"] == n_chunks
     mc = oracle_cfg(wl, ragged_buffer_factor=1.0)
     g = ref.layer_backward_dropless(mc, f64(x), L, *[f64(w) for w in W],
                                     f64(dy))
