@@ -49,6 +49,10 @@ CASES = [
     (WORKLOADS["small"].with_(name="n2_k1", H=384, F=128, E=8, k=1, S=2),
      2, [700, 1], 2.0),
     (WORKLOADS["tiny"].with_(name="tiny_n2", S=2), 2, [128, 128], 2.0),
+    # fewer experts per rank than picks (E/S = 2 < k = 4): two slots per
+    # send row, a token's picks split over several ranks or two on one
+    (WORKLOADS["small"].with_(name="n4_k4_e2", H=256, F=256, E=8, k=4, S=4,
+                              zipf_s=1.2), 4, [200, 150, 0, 333], 1.5),
     (WORKLOADS["small"].with_(name="n8_e256", H=512, F=256, E=256, k=8,
                               S=8, zipf_s=1.2), 8,
      [256, 200, 300, 100, 64, 256, 1, 180], 2.0),
@@ -174,7 +178,7 @@ def test_ring_layer_matches_oracle(case):
                  np.concatenate(want), TOL[wl.dtype], f"ring y (N={N})")
 
 
-@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0].name)
+@pytest.mark.parametrize("case", CASES[:5], ids=lambda c: c[0].name)
 def test_ep_backward_matches_oracle(case):
     """The EP layer's backward over logical ranks (the forward recomputed
     pass by pass; the cotangent sent along the dispatch's dedup'd rows,
@@ -234,7 +238,7 @@ def test_ep_backward_matches_oracle(case):
                      tol, f"EP {name} vs moe_layer_backward (N={N})")
 
 
-@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0].name)
+@pytest.mark.parametrize("case", CASES[:5], ids=lambda c: c[0].name)
 def test_ring_backward_matches_oracle(case):
     """The ring's backward over logical ranks (cotangent all-gather, each
     rank's expert pass differentiated over all tokens, partial dx summed at
