@@ -1026,8 +1026,8 @@ def config_runs(args, device, flush, head):
     """Every other workload of the benchmark at 1 GPU, each a short timed
     run of its own (few steps; at least ~0.4 s of timed work for the clock
     sampler): the tiny and small layers, the DeepSeek-V3 layer as one
-    uncapped pass under uniform and Zipf routing (where the GEMM's tensor
-    fraction is judged), the Llama4-Maverick layer, and the
+    uncapped pass under uniform and Zipf routing (the regime in which the
+    GEMMs lean on the tensor cores), the Llama4-Maverick layer, and the
     routing/permute/dedup sweep.  Returns a list of compact records."""
     from synth import SWEEP_ROUTINGS, SWEEP_TOKENS, sweep_workload
     runs = [("dsv3", WORKLOADS["dsv3"], "fallback")]
