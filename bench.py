@@ -1046,7 +1046,8 @@ def config_runs(args, device, flush, head):
         else:
             layer = Layer(wl, device, mode=mode)
             res = measure_layer(layer, CONFIG_STEPS, 3, device, flush,
-                                clocks=ClockSampler(device), exact=False)
+                                clocks=ClockSampler(device), exact=False,
+                                graph_too=mode == "fallback")
             del layer
             torch.cuda.empty_cache()
         rec = {"config": label, "T": wl.T, "mode": mode,
@@ -1077,6 +1078,12 @@ def config_runs(args, device, flush, head):
                 fl / peaks["bf16_tflops_sustained"], 4)
         rec["permute_frac"] = res.get("permute_frac")
         rec["combine_frac"] = res.get("combine_frac")
+        if "untraced_graph" in res:
+            # the same graph without the stage stamps (1 µs a stage, which
+            # matters in steps of a few tens of µs)
+            rec["untraced_value"] = res["untraced_graph"]["value"]
+            rec["untraced_ms_per_step"] = \
+                res["untraced_graph"]["ms_per_step"]
         if "check_us" in res:
             rec["check_us"] = res["check_us"]
         rec["clocks"] = res.get("clocks")

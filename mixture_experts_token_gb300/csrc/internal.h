@@ -351,6 +351,12 @@ cudaError_t launch_router_bf16(const moe_config_t& c, const void* x,
                                const void* w_router, const float* offset,
                                float* logits, int32_t* status,
                                cudaStream_t s);
+// The router's tensor-core launch (router_tc.cu): the one-group GEMM
+// above, or for batches whose tiles leave SMs idle the reduction split over
+// clusters of 2, 4 or 8 CTAs, whichever takes fewer k-block steps per SM.
+cudaError_t launch_router_tc(const moe_config_t& c, const void* x,
+                             const void* w_router, const float* offset,
+                             float* logits, int32_t* status, cudaStream_t s);
 
 // Host-side formulas shared by validation and drivers.
 int64_t capacity_rows(const moe_config_t& c);

@@ -10,6 +10,8 @@
 //  * bf16 layers with H % 64 == 0 and E % 128 == 0: the grouped tcgen05
 //    GEMM (gmm_tc.cu, one group of T rows, 128-column float32 tiles),
 //    because at the DeepSeek-V3 layer's size it is a 30 GFLOP contraction;
+//    batches whose 128 x 128 tiles leave SMs idle split the reduction over
+//    a cluster instead when that is faster (router_tc.cu);
 //  * everything else (the fp32 tiny layer, E = 16 of the small layer):
 //    this CUDA-core kernel.  A CTA of 256 threads takes 16 tokens and 256
 //    experts; x is staged in shared memory 64 columns at a time, each
@@ -79,7 +81,7 @@ cudaError_t launch_router(const moe_config_t& c, const void* x,
   if (c.T == 0) return cudaSuccess;
   if (router_tc_supported(c) && aligned16(logits) &&
       (offset == nullptr || aligned16(offset)))
-    return launch_router_bf16(c, x, w_router, offset, logits, status, s);
+    return launch_router_tc(c, x, w_router, offset, logits, status, s);
   const dim3 grid((c.T + kTok - 1) / kTok, (c.E + kCols - 1) / kCols);
   if (c.dtype == MOE_F32)
     router_simt_kernel<float><<<grid, kCols, 0, s>>>(

@@ -6,7 +6,8 @@ within 2^-10 of its dot-product scale (|x| |Wr|)_i + |r_i| (float32
 accumulation over H terms, whatever the cancellation in the sum).  Shapes
 cover the tensor-core form (bf16, H % 64 == 0, E % 128 == 0: the
 DeepSeek-V3 and Llama4-Maverick layers at full size, several column tiles,
-ragged row tiles, one token) and the CUDA-core form (the fp32 tiny layer,
+ragged row tiles, one token; small batches with the reduction split over a
+cluster, including CTAs with an empty k-slice) and the CUDA-core form (the fp32 tiny layer,
 E = 16 of the small layer, odd H and E).
 """
 import numpy as np
@@ -31,6 +32,13 @@ CASES = [
     WORKLOADS["small"].with_(name="h104_e24", T=333, H=104, E=24, S=4),
     WORKLOADS["tiny"].with_(name="f32_e40", T=77, H=48, E=40, S=4,
                             routing="zipf", zipf_s=1.0),
+    # batches whose tiles leave most SMs idle: the reduction split over a
+    # cluster (8 CTAs at up to 1024 tokens of H = 7168, 2 at 4096 tokens)
+    WORKLOADS["dsv3"].with_(name="split8_t1", T=1),
+    WORKLOADS["dsv3"].with_(name="split8_t1024", T=1024),
+    WORKLOADS["dsv3"].with_(name="split2_t4096", T=4096),
+    # 10 k-blocks over 8 CTAs: three CTAs get no k-block and add zeros
+    WORKLOADS["dsv3"].with_(name="split_empty_slices", T=200, H=640),
 ]
 
 
@@ -58,6 +66,18 @@ def test_router_logits_parity(wl, with_offset):
     scale = np.abs(xh) @ np.abs(wh) + np.abs(want)
     assert_close(got, want, 1e-4, f"logits ({'offset' if with_offset else 'x Wr'})",
                  scale=scale, cw_bound=2.0 ** -10)
+
+
+def test_split_router_is_deterministic():
+    """The split form sums the cluster's partial tiles in rank order, so two
+    launches give the same bits."""
+    wl = WORKLOADS["dsv3"].with_(T=700)
+    x = make_x(wl, "cuda")
+    wr = make_router_weight(wl, "cuda")
+    off = make_logit_offset(wl)
+    a = gpu_logits(wl, x, wr, off)
+    b = gpu_logits(wl, x, wr, off)
+    assert torch.equal(a, b)
 
 
 def test_router_logits_feed_the_same_routing():
