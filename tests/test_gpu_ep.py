@@ -431,3 +431,75 @@ def test_backward_dsv3_full_size_8_ranks(variant):
                              for r in range(N)], 2e-2, f"{what}: {name}")
     del W, x_all, dw1, dWs
     torch.cuda.empty_cache()
+
+
+def draw_ep(i):
+    """A seeded random expert-parallel layer: ranks, experts per rank, k,
+    dims, per-rank token counts (some ranks empty), factor, dtype."""
+    rng = np.random.default_rng(7000 + i)
+    N = int(rng.choice([2, 4, 8]))
+    E = N * int(rng.choice([1, 2, 4]))
+    k = int(rng.integers(1, min(E, 6) + 1))
+    bf = i % 3 != 2
+    H = int(rng.choice([128, 256, 384])) if bf else int(rng.choice([32, 64]))
+    F = int(rng.choice([128, 256])) if bf else 64
+    Ts = [int(rng.integers(0, 300)) if rng.random() > 0.15 else 0
+          for _ in range(N)]
+    if sum(Ts) == 0:
+        Ts[0] = 17
+    wl = WORKLOADS["small"].with_(
+        name=f"ep_rand{i}", T=sum(Ts), H=H, E=E, k=k, F=F, S=N,
+        dtype="bf16" if bf else "f32",
+        routing=str(rng.choice(["uniform", "zipf"])), zipf_s=1.2, seed=i,
+        renorm=bool(rng.integers(0, 2)), x_scale=1.0 if bf else 0.25)
+    return wl, N, Ts, float(rng.choice([0.5, 1.0, 2.0]))
+
+
+EP_RANDOM = [draw_ep(i) for i in range(12)]
+
+
+@pytest.mark.parametrize("case", EP_RANDOM, ids=lambda c: (
+    f"{c[0].name}-{c[0].dtype}-N{c[1]}-E{c[0].E}-k{c[0].k}-f{c[3]}"))
+def test_random_ep_and_ring_layers(case):
+    """Seeded random EP layers over logical ranks: the EP layer (fallback=
+    layer, global check) and the ring of experts, forward and backward,
+    against the oracle's ep_layer, ring_layer and their backward."""
+    wl, N, Ts, factor = case
+    xs, Ls = rank_inputs(wl, Ts)
+    cfg = gcfg(wl, Ts, N, factor)
+    W, per_rank = weights_of(wl, N)
+    g = torch.Generator(device="cuda").manual_seed(80 + N)
+    dys = [torch.randn((T_r, wl.H), generator=g, device="cuda").to(x.dtype)
+           for T_r, x in zip(Ts, xs)]
+    Lt = [torch.from_numpy(L).cuda() for L in Ls]
+    tol = TOL[wl.dtype]
+    mc = ref.MoEConfig(sum(Ts), wl.H, wl.E, wl.k, wl.F, N, factor, 0,
+                       wl.renorm)
+    xh = [f64(x) for x in xs]
+    dense = ref.dense_weights(*(f64(w) for w in W))
+    layer = ep.EPLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    ys = layer.forward(xs, Lt)
+    want, over, n = ref.ep_layer(mc, N, xh, Ls, dense)
+    torch.cuda.synchronize()
+    assert layer.info["overflow"] == int(over) and layer.info["n_chunks"] == n
+    assert_close(np.concatenate([f64(y) for y in ys]), np.concatenate(want),
+                 tol, "EP y")
+    ring = ep.RingLayer(cfg, ep.LoopbackTransport(N), per_rank)
+    yr = ring.forward(xs, Lt)
+    torch.cuda.synchronize()
+    assert_close(np.concatenate([f64(y) for y in yr]),
+                 np.concatenate(ref.ring_layer(mc, N, xh, Ls, dense)), tol,
+                 "ring y")
+    dyh = [f64(d) for d in dys]
+    for name, lay, oracle in (("EP", layer, ref.ep_layer_backward),
+                              ("ring", ring, ref.ring_layer_backward)):
+        dxs, dls, dWs = lay.backward(xs, Lt, dys)
+        torch.cuda.synchronize()
+        wdx, wdl, wdW = oracle(mc, N, xh, Ls, dense, dyh)
+        assert_close(np.concatenate([f64(d) for d in dxs]),
+                     np.concatenate(wdx), tol, f"{name} dx")
+        assert_close(np.concatenate([f64(d) for d in dls]),
+                     np.concatenate(wdl), tol, f"{name} dlogits")
+        for i, wname in enumerate(("dwg", "dwu", "dwd")):
+            assert_close(np.concatenate([f64(t[i]) for t in dWs]), wdW[i],
+                         tol, f"{name} {wname}")
