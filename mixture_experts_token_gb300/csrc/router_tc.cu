@@ -34,6 +34,11 @@
 
 namespace moe {
 namespace tc {
+
+// The GEMMs' test hook (gmm_tc.cu): stop the producer after this many stage
+// fills (-1: never), so that the next wait runs out.
+extern std::atomic<long long> g_stall_after_fills;
+
 namespace {
 
 constexpr int kRBN = 128;                              // experts per tile
@@ -47,6 +52,7 @@ struct RouterParams {
   const float* offset;  // [T, E] or null
   float* logits;        // [T, E]
   int32_t* status;
+  long long stall_after_fills;  // tests of the timeout path only (-1: off)
 };
 
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
@@ -114,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long long fills = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
+        if (p.stall_after_fills >= 0 && fills >= p.stall_after_fills)
+          break;  // test hook: leave the MMA warp waiting
         if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
                        p.status))
           break;
@@ -161,8 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // all MMAs issued by this thread are complete (a CTA with an empty
-      // k-slice issues none and the epilogue does not wait for them)
-      if (kb1 > kb0) umma_commit(smem_u32(done));
+      // k-slice issues none and the epilogue does not wait for them); the
+      // drain waits for them itself, bounded by time alone, so that the
+      // tensor memory is not freed under an MMA after a timeout
+      if (kb1 > kb0) {
+        umma_commit(smem_u32(done));
+        mbar_wait(smem_u32(done), 0, nullptr, p.status);
+      }
     }
   } else {
     // ------------------- epilogue: the partial tile to shared memory ---
@@ -334,7 +347,7 @@ cudaError_t launch_router_tc(const moe_config_t& c, const void* x,
       !make_map(&b, w_router, c.E, c.H, 64, 64))
     return cudaErrorInvalidValue;
   RouterParams p{c.T, c.E, kblocks, splits, c.E / kRBN, offset, logits,
-                 status};
+                 status, g_stall_after_fills.load()};
   const size_t smem = router_splitk_smem();
   if ((err = set_smem_attribute(dev)) != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];

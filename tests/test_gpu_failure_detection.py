@@ -1,4 +1,5 @@
-"""Failure detection on the GPU without a fault: the GEMM's bounded waits.
+"""Failure detection on the GPU without a fault: the bounded waits of the
+GEMM and of the router's cluster kernel.
 
 A test hook stops the GEMM's TMA producer after a few stage fills, so the
 MMA warp waits on a barrier nothing will complete.  The wait gives up after
@@ -63,3 +64,36 @@ def test_gemm_wait_times_out_and_context_survives():
         f64(xs), off.cpu().numpy(),
         ref.dense_weights(*(f64(w) for w in W)))
     assert_close(f64(ys), want_y, 2e-2, 'ys')
+
+
+def test_split_router_wait_times_out_and_context_survives():
+    """The router's split form (a cluster of CTAs per tile, two cluster
+    barriers): with the producers stopped, every CTA's MMA wait runs out,
+    the status word reports MOE_DEV_TIMEOUT, every CTA still passes both
+    cluster barriers and the launch returns; the next launch is correct."""
+    from synth import WORKLOADS, make_logit_offset, make_router_weight, \
+        make_x
+    wl = WORKLOADS["dsv3"].with_(T=1024)
+    cfg = moe.make_config(wl.T, wl.H, wl.E, wl.k, wl.F, wl.S, 2.0, 0, "bf16")
+    x = make_x(wl, "cuda")
+    wr = make_router_weight(wl, "cuda")
+    off = make_logit_offset(wl)
+    L = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    offd = torch.from_numpy(off).cuda()
+    try:
+        moe.moe_test_stall_gemm_producer(3)
+        t0 = time.time()
+        moe.moe_router_logits(cfg, x, wr, offd, L, status)
+        torch.cuda.synchronize()
+        took = time.time() - t0
+    finally:
+        moe.moe_test_stall_gemm_producer(-1)
+    assert int(status.item()) & moe.MOE_DEV_TIMEOUT
+    assert took < 30.0
+    status.zero_()
+    moe.moe_router_logits(cfg, x, wr, offd, L, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    want = ref.router_logits(f64(x), f64(wr), off)
+    assert_close(f64(L), want, 1e-4, "logits after the timeout")
