@@ -1472,14 +1472,16 @@ class Backward:
                                  w_row=L.wrow)
             segs, rows = [(L.off2, 0)], L.rr
             wx, wdg, wdu, wh, wdy = L.xs2, L.dg2, L.du2, L.h2, L.dys2
+            flags = moe.MOE_WGRAD_ROWS16     # 16-row groups, zero pad rows
         else:
             rows = c.T * k
             wx, wdg, wdu, wh, wdy = xs, L.dg, L.du, h, L.dys
+            flags = 0
         mark("gmm_gate_up_wgrad")
         moe.moe_gmm_gate_up_wgrad(c, segs, rows, wx, wdg, wdu,
-                                  L.dw[0], L.dw[1], 0, b["status"], **grp)
+                                  L.dw[0], L.dw[1], flags, b["status"], **grp)
         mark("gmm_down_wgrad")
-        moe.moe_gmm_down_wgrad(c, segs, rows, wh, wdy, L.dw[2], 0,
+        moe.moe_gmm_down_wgrad(c, segs, rows, wh, wdy, L.dw[2], flags,
                                b["status"], **grp)
         mark(None)
         return passes

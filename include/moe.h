@@ -78,6 +78,8 @@ typedef enum {
 #define MOE_DEV_NONFINITE 1 /* a NaN/inf logit was seen; it ranked as -inf */
 #define MOE_DEV_TIMEOUT 2   /* a bounded wait in the GEMM gave up          */
 #define MOE_DEV_BAD_INDEX 4 /* an expert index outside [0, E) was skipped  */
+#define MOE_DEV_UNALIGNED 8 /* MOE_WGRAD_ROWS16 given, a group's rows are
+                               not a multiple of 16: nothing was written  */
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 
@@ -581,8 +583,18 @@ typedef struct {
  * expert e:
  *   gate_up: dWg[e] (+)= x^T dg,  dWu[e] (+)= x^T du   ([E,H,F] float32)
  *   down:    dWd[e] (+)= h^T dy_sorted                 ([E,F,H] float32)
- * The row buffers have rows_total rows.  accumulate = 0 overwrites every
- * expert's gradient (zeros for experts without rows), 1 adds into it. */
+ * The row buffers have rows_total rows.  accumulate: a set of flags.
+ * Without MOE_WGRAD_ACCUMULATE every expert's gradient is overwritten
+ * (zeros for experts without rows); with it the gradients are added into.
+ * MOE_WGRAD_ROWS16 states that every group holds a multiple of 16 rows in
+ * every segment (as in the layout moe_regroup_rows writes, whose pad rows
+ * are zero): bf16 layers whose gradient has a multiple of 256 rows (H for
+ * gate_up, F for down, with H % 256 == 0) then take a two-SM tensor-core
+ * kernel.  If the statement is false, that kernel raises MOE_DEV_UNALIGNED
+ * in status_word and leaves the gradients it would have written as they
+ * were (those of experts without rows still zeroed). */
+#define MOE_WGRAD_ACCUMULATE 1
+#define MOE_WGRAD_ROWS16 2
 moe_status_t moe_gmm_gate_up_wgrad(const moe_config_t *cfg,
                                    int32_t n_groups,
                                    const int32_t *group_expert,

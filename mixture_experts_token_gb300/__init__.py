@@ -20,6 +20,8 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, \
     MOE_ERR_CUDA = range(5)
 MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 1, 2, 4
+MOE_DEV_UNALIGNED = 8
+MOE_WGRAD_ACCUMULATE, MOE_WGRAD_ROWS16 = 1, 2
 MOE_F32, MOE_BF16 = 0, 1
 MOE_MODE_FALLBACK_LAYER, MOE_MODE_CAPPED, MOE_MODE_DROPLESS = 0, 1, 2
 MOE_WS_PERMUTE, MOE_WS_CHUNKED, MOE_WS_LAYER = 0, 1, 2

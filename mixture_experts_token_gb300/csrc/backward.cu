@@ -491,8 +491,9 @@ cudaError_t launch_wgrad_f32(const moe_config_t& c, const Groups& g,
                              const WgradSegment* seg, int n_seg,
                              const void* xs, const void* dg, const void* du,
                              const void* h, const void* dys, float* dwg,
-                             float* dwu, float* dwd, int accumulate,
+                             float* dwu, float* dwd, int flags,
                              int parts, cudaStream_t s) {
+  const bool accumulate = (flags & kWgradAccumulate) != 0;
   const long long nw = static_cast<long long>(c.E) * c.H * c.F;
   const bool gu = (parts & kWgradGateUp) != 0;
   const bool dn = (parts & kWgradDown) != 0;

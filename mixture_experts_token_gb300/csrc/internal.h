@@ -219,6 +219,10 @@ bool weights_ok(const void* wg, const void* wu, const void* wd);
 using WgradSegment = moe_row_segment_t;
 constexpr int kWgradGateUp = 1;  // dWg and dWu
 constexpr int kWgradDown = 2;    // dWd
+// flags of launch_wgrad (the values of MOE_WGRAD_ACCUMULATE and
+// MOE_WGRAD_ROWS16)
+constexpr int kWgradAccumulate = 1;  // add into dW instead of overwriting
+constexpr int kWgradRows16 = 2;      // groups hold multiples of 16 rows
 cudaError_t launch_combine_backward(const moe_config_t& c, const void* dy,
                                     const void* y_sorted,
                                     const int32_t* row_of,
@@ -258,7 +262,7 @@ cudaError_t launch_wgrad_f32(const moe_config_t& c, const Groups& g,
                              const WgradSegment* seg, int n_seg,
                              const void* xs, const void* dg, const void* du,
                              const void* h, const void* dys, float* dwg,
-                             float* dwu, float* dwd, int accumulate,
+                             float* dwu, float* dwd, int flags,
                              int parts, cudaStream_t s);
 // bf16 (tensor cores)
 cudaError_t launch_gate_up_saved_bf16(const moe_config_t& c, const Groups& g,
@@ -293,7 +297,7 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               int64_t rows_total, const void* x_sorted,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
-                              float* dw_up, float* dw_down, int accumulate,
+                              float* dw_up, float* dw_down, int flags,
                               int parts, int32_t* status, cudaStream_t s);
 // Dispatch on the layer dtype (bf16: tensor cores, fp32: CUDA cores).
 cudaError_t launch_gate_up_saved(const moe_config_t& c, const Groups& g,
@@ -311,11 +315,12 @@ cudaError_t launch_gate_up_dgrad(const moe_config_t& c, const Groups& g,
                                  const void* wu, const void* dg,
                                  const void* du, void* dxs, int32_t* status,
                                  cudaStream_t s);
+// flags: kWgradAccumulate | kWgradRows16 (see wgrad_tc.cu)
 cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
                          const WgradSegment* seg, int n_seg,
                          int64_t rows_total, const void* xs, const void* dg,
                          const void* du, const void* h, const void* dys,
-                         float* dwg, float* dwu, float* dwd, int accumulate,
+                         float* dwg, float* dwu, float* dwd, int flags,
                          int parts, int32_t* status, cudaStream_t s);
 // Rows of up to kMaxRegroupSegments ranges copied into one expert-major
 // layout with 16-row-aligned groups and zero pad rows (see regroup.cu);

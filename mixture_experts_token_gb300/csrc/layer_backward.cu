@@ -197,13 +197,13 @@ cudaError_t launch_wgrad(const moe_config_t& c, const Groups& g,
                          const WgradSegment* seg, int n_seg,
                          int64_t rows_total, const void* xs, const void* dg,
                          const void* du, const void* h, const void* dys,
-                         float* dwg, float* dwu, float* dwd, int accumulate,
+                         float* dwg, float* dwu, float* dwd, int flags,
                          int parts, int32_t* status, cudaStream_t s) {
   if (c.dtype == MOE_BF16)
     return launch_wgrad_bf16(c, g, seg, n_seg, rows_total, xs, dg, du, h, dys,
-                             dwg, dwu, dwd, accumulate, parts, status, s);
+                             dwg, dwu, dwd, flags, parts, status, s);
   return launch_wgrad_f32(c, g, seg, n_seg, xs, dg, du, h, dys, dwg, dwu, dwd,
-                          accumulate, parts, s);
+                          flags, parts, s);
 }
 
 size_t gmm_backward_bytes(const moe_config_t& c) {
@@ -337,7 +337,8 @@ moe_status_t moe_gmm_swiglu_backward(
   const WgradSegment seg{group_offsets, 0};
   return cuda_st(launch_wgrad(*cfg, ids, &seg, cfg->T > 0 ? 1 : 0,
                               static_cast<int64_t>(rows), x_sorted, dg, du, h,
-                              dy_sorted, dw_gate, dw_up, dw_down, accumulate,
+                              dy_sorted, dw_gate, dw_up, dw_down,
+                              accumulate != 0 ? kWgradAccumulate : 0,
                               kWgradGateUp | kWgradDown, status_word,
                               stream));
 }
@@ -434,7 +435,7 @@ moe_status_t check_segments(const moe_config_t* cfg,
   if (st != MOE_OK) return st;
   if (cfg->F < 1 || n_segments < 0 || rows_total < 0 ||
       rows_total > std::numeric_limits<int32_t>::max() ||
-      (accumulate != 0 && accumulate != 1) ||
+      (accumulate & ~(kWgradAccumulate | kWgradRows16)) != 0 ||
       (n_segments > 0 && segments == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (!gmm_shape_ok(*cfg)) return MOE_ERR_UNSUPPORTED;
@@ -714,7 +715,8 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* x,
     const WgradSegment one{b.off2, 0};
     return cuda_st(launch_wgrad(*cfg, wgroups, &one, 1, rr,
                                 b.xs2, b.dg2, b.du2, b.h2, b.dys2, dw_gate,
-                                dw_up, dw_down, 0, kWgradGateUp | kWgradDown,
+                                dw_up, dw_down, kWgradRows16,
+                                kWgradGateUp | kWgradDown,
                                 status_word, stream));
   }
   return cuda_st(launch_wgrad(

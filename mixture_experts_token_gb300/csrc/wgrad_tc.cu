@@ -33,10 +33,16 @@ namespace tc {
 // in tensor memory before its single write.  The epilogue moves each
 // 32 x 32 fp32 sub-tile through a 128-byte-swizzled staging buffer to a
 // TMA store (overwrite) or a TMA reduce-add (accumulate in L2).
-constexpr int WSTAGES = 3;
+#ifndef MOE_WGRAD_STAGES
+#define MOE_WGRAD_STAGES 3
+#endif
+#ifndef MOE_WGRAD_STAGE_BUFS
+#define MOE_WGRAD_STAGE_BUFS 4
+#endif
+constexpr int WSTAGES = MOE_WGRAD_STAGES;
 constexpr int kWStage = BM * BK * 2 + BK * 256 * 2;  // 48 KB
 constexpr int kStageBuf = 32 * 32 * 4;               // 4 KB
-constexpr int kStageBufs = 4;  // staging buffers per epilogue warp
+constexpr int kStageBufs = MOE_WGRAD_STAGE_BUFS;  // staging buffers per epilogue warp
 constexpr int kMaxSeg = 16;
 
 struct WParams {
@@ -112,8 +118,8 @@ __device__ __forceinline__ void bulk_commit() {
 // At most kStageBufs - 1 bulk groups of this thread still reading shared
 // memory: the oldest staging buffer is free again.
 __device__ __forceinline__ void bulk_wait_read_free() {
-  static_assert(kStageBufs == 4, "the wait depth below is kStageBufs - 1");
-  asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kStageBufs - 1)
+               : "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() {
@@ -427,6 +433,302 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------- two-SM weight gradients ----
+// A cluster of two CTAs (tcgen05.mma.cta_group::2) computes a 256 x 256
+// tile of dW[e]: each CTA stages its own 128 columns of P (its 128 rows of
+// the tile) and one half of the tile's 256 columns of Q (WMODE 0: the
+// leader dg, the peer du, over the same 128 columns of F; WMODE 1: the
+// leader the first 128, the peer the last 128 columns of H).  A CTA then
+// loads 256 operand columns per routed row for its 128 x 256 outputs
+// instead of 384, and a stage is 32 KB instead of 48, so more of them fit.
+// The TMEM of either CTA holds its 128 rows x 256 columns laid out as in
+// the one-CTA kernel (WMODE 0: gate in columns 0-127, up in 128-255), and
+// both CTAs run the same epilogue.  The leader issues the MMAs and
+// multicasts its commits to both CTAs; the peer's loads complete on the
+// leader's barrier.  There is no ragged K=16 step: every group holds a
+// multiple of 16 rows in every segment (the regrouped layout, zero pad
+// rows included), which the kernel checks before it starts; otherwise it
+// raises MOE_DEV_UNALIGNED and writes nothing.
+#ifndef MOE_WGRAD2_STAGES
+#define MOE_WGRAD2_STAGES 4
+#endif
+constexpr int W2STAGES = MOE_WGRAD2_STAGES;
+constexpr int kW2Stage = 4 * 8192;  // 2 boxes of P + 2 of Q, 64 rows each
+constexpr uint32_t kW2Tx = 2 * kW2Stage;  // both CTAs' bytes
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst,
+                                                      const CUtensorMap* m,
+                                                      uint32_t bar_cluster,
+                                                      int c0, int c1,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
+      "mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], "
+      "[%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1),
+      "l"(policy)
+      : "memory");
+}
+
+template <int WMODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tmP,
+                     const __grid_constant__ CUtensorMap tmQ0,
+                     const __grid_constant__ CUtensorMap tmQ1,
+                     const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmO1, WParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stagebuf = smem + W2STAGES * kW2Stage;  // [4][kStageBufs][4 KB]
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(stagebuf + 4 * kStageBufs * kStageBuf);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + W2STAGES;
+  uint64_t* tfull = bars + 2 * W2STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* unaligned = reinterpret_cast<int*>(tmem_slot + 2);
+  int* wsum = reinterpret_cast<int*>(tmem_slot + 4);  // [16]
+  int* tpre = wsum + 16;                               // [G+1]
+  int* ecnt = tpre + (p.G + 1);                        // [E]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: leader, 1: peer
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < W2STAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(tfull + a), 1);
+      // the leader's four epilogue warps and the peer's relay
+      mbar_init(smem_u32(tempty + a), rank == 0 ? kEpilogueThreads / 32 + 1
+                                                : kEpilogueThreads / 32);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    *unaligned = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmP);
+    prefetch_tmap(&tmQ0);
+    if (WMODE == 0) prefetch_tmap(&tmQ1);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  build_wgrad_table(p, tpre, wsum);
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) ecnt[e] = 0;
+  // every group's rows in every segment: a multiple of 16
+  for (int g = threadIdx.x; g < p.G; g += blockDim.x)
+    for (int sg = 0; sg < p.n_seg; ++sg)
+      if (((__ldg(p.seg_off[sg] + g + 1) - __ldg(p.seg_off[sg] + g)) & 15) !=
+          0)
+        *unaligned = 1;
+  __syncthreads();
+  if (p.group_expert != nullptr)
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x)
+      if (tpre[g + 1] > tpre[g]) atomicAdd(&ecnt[__ldg(p.group_expert + g)], 1);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool bad = *unaligned != 0;
+  if (bad && rank == 0 && threadIdx.x == 0 && p.status)
+    atomicOr(p.status, MOE_DEV_UNALIGNED);
+  const int total_tiles = bad ? 0 : tpre[p.G];
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------------------------------- TMA producer (both CTAs) ---
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const CUtensorMap* mq = (WMODE == 0 && rank == 1) ? &tmQ1 : &tmQ0;
+      int stage = 0;
+      uint32_t phase = 0;
+      long long fills = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const int g = group_of(tpre, p.G, tile);
+        const int local = tile - tpre[g];
+        const int n = local % p.n_tiles, m = local / p.n_tiles;
+        const int pcol = m * 2 * BM + static_cast<int>(rank) * BM;
+        const int qcol = WMODE == 0 ? n * 128 : n * 256 + rank * 128;
+        for (int sg = 0; ok && sg < p.n_seg; ++sg) {
+          const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
+          for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
+               r += BK) {
+            if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
+                           p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = map_to_rank(smem_u32(full + stage), 0);
+            if (rank == 0) mbar_expect_tx(smem_u32(full + stage), kW2Tx);
+            const uint32_t sa = smem_base + stage * kW2Stage;
+            tma_load_2d_pair_hint(sa, &tmP, fb, pcol, r, keep);
+            tma_load_2d_pair_hint(sa + 8192, &tmP, fb, pcol + 64, r, keep);
+            tma_load_2d_pair_hint(sa + 16384, mq, fb, qcol, r, keep);
+            tma_load_2d_pair_hint(sa + 24576, mq, fb, qcol + 64, r, keep);
+            ++fills;
+            if (++stage == W2STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Drain: the leader's full barriers count both CTAs' bytes.
+      if (rank == 0) {
+        const long long first = fills > W2STAGES ? fills - W2STAGES : 0;
+        for (long long f = first; f < fills; ++f)
+          mbar_wait(smem_u32(full + (f % W2STAGES)),
+                    static_cast<uint32_t>((f / W2STAGES) & 1), nullptr,
+                    p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------- MMA issuer (leader) ------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = make_idesc(2 * BM, 256, true, true);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const int g = group_of(tpre, p.G, tile);
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag,
+                       p.status))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccCols;
+        bool first = true;
+        for (int sg = 0; ok && sg < p.n_seg; ++sg) {
+          const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
+          for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
+               r += BK) {
+            if (!mbar_wait(smem_u32(full + stage), phase, abort_flag,
+                           p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_base + stage * kW2Stage;
+            const uint32_t sb = sa + 16384;
+            const int steps = min(BK, r1 - r) >> 4;  // whole K=16 steps
+            for (int kk = 0; kk < steps; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 2048, 8192, 1024);
+              const uint64_t bd = smem_desc(sb + kk * 2048, 8192, 1024);
+              umma_bf16_pair(d, ad, bd, idesc, (!first || kk != 0) ? 1u : 0u);
+            }
+            umma_commit_pair_mc(smem_u32(empty + stage));
+            first = false;
+            if (++stage == W2STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(smem_u32(tfull + acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit_pair(smem_u32(done));
+      mbar_wait(smem_u32(done), 0, nullptr, p.status);
+    } else if (lane == 0) {
+      // ------------------------------ TMEM-empty relay (peer) -----------
+      // the peer's epilogue warps arrive on its own barrier; this thread
+      // forwards each completed phase to the leader with one cluster-scope
+      // arrival, so that no epilogue warp waits on a cluster-wide fence
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = pair; tile < total_tiles; tile += npairs) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase, abort_flag,
+                       p.status))
+          break;
+        mbar_arrive_cluster(map_to_rank(smem_u32(tempty + acc), 0));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  } else {
+    // ---------------------------------------- epilogue (both CTAs) -----
+    const int q = warp & 3;
+    uint8_t* mybuf = stagebuf + q * kStageBufs * kStageBuf;
+    const uint64_t stream = policy_evict_first();
+    int acc = 0, nsub = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < total_tiles; tile += npairs) {
+      const int g = group_of(tpre, p.G, tile);
+      const int local = tile - tpre[g];
+      const int n = local % p.n_tiles, m = local / p.n_tiles;
+      const int we = p.group_expert ? __ldg(p.group_expert + g) : g;
+      bool ok = mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag,
+                          p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      const int orow = (we * p.m_tiles + m) * 2 * BM +
+                       static_cast<int>(rank) * BM + q * 32;
+      const bool add = p.reduce || (p.group_expert != nullptr && ecnt[we] > 1);
+#pragma unroll 1
+      for (int sub = 0; sub < 8; ++sub, ++nsub) {
+        uint32_t r[32];
+        tmem_ld32(taddr + sub * 32, r);
+        uint8_t* buf = mybuf + (nsub % kStageBufs) * kStageBuf;
+        if (lane == 0) bulk_wait_read_free();
+        __syncwarp();
+        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          row[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1],
+                                           r[4 * j + 2], r[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const CUtensorMap* om = &tmO0;
+          int col = n * 256 + sub * 32;
+          if (WMODE == 0) {
+            om = sub < 4 ? &tmO0 : &tmO1;
+            col = n * 128 + (sub & 3) * 32;
+          }
+          if (add)
+            tma_reduce_add_2d(om, smem_u32(buf), col, orow, stream);
+          else
+            tma_store_2d(om, smem_u32(buf), col, orow, stream);
+          bulk_commit();
+        }
+      }
+      // one arrival per warp, on its own CTA's barrier, once its lanes'
+      // TMEM loads are done (the peer's relay forwards it to the leader)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still use it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // Store mode: zeroes dW[e] of every expert that does not have exactly one
 // group with rows -- none (no tile writes it) or several (its tiles add onto
 // it).  Grid (E, blocks), 16-byte stores.
@@ -458,6 +760,31 @@ size_t smem_bytes_wgrad(int G, int E) {
          16 + 4 * (16 + G + 1 + E) + 64;
 }
 
+size_t smem_bytes_wgrad2(int G, int E) {
+  return 1024 + W2STAGES * kW2Stage + 4 * kStageBufs * kStageBuf +
+         8 * (2 * W2STAGES + 5) + 16 + 4 * (16 + G + 1 + E) + 64;
+}
+
+template <int WMODE>
+cudaError_t launch_wgrad2(const CUtensorMap& pm, const CUtensorMap& q0,
+                          const CUtensorMap& q1, const CUtensorMap& o0,
+                          const CUtensorMap& o1, const WParams& p,
+                          cudaStream_t s) {
+  const size_t smem = smem_bytes_wgrad2(p.G, p.E);
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(wgrad_tc2_kernel<WMODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int grid = sms & ~1;  // whole CTA pairs
+  wgrad_tc2_kernel<WMODE><<<grid, kThreads, smem, s>>>(pm, q0, q1, o0, o1, p);
+  return cudaGetLastError();
+}
+
 template <int WMODE, int BN>
 cudaError_t launch_wgrad(const CUtensorMap& pm, const CUtensorMap& q0,
                          const CUtensorMap& q1, const CUtensorMap& o0,
@@ -481,15 +808,20 @@ cudaError_t launch_wgrad(const CUtensorMap& pm, const CUtensorMap& q0,
 }  // namespace tc
 
 // Weight gradients over row segments (each {group offsets, first row}),
-// all inside buffers of `rows_total` rows.  accumulate = 0 overwrites every
-// expert's dW (experts without rows get zeros); 1 adds into dW.
+// all inside buffers of `rows_total` rows.  flags: kWgradAccumulate adds
+// into dW, otherwise every expert's dW is overwritten (experts without rows
+// get zeros); kWgradRows16 (every group holds a multiple of 16 rows in
+// every segment) takes the two-SM kernel where the gradient's row count is
+// a multiple of 256.
 cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
                               const WgradSegment* seg, int n_seg,
                               int64_t rows_total, const void* x_sorted,
                               const void* dg, const void* du, const void* h,
                               const void* dy_sorted, float* dw_gate,
-                              float* dw_up, float* dw_down, int accumulate,
+                              float* dw_up, float* dw_down, int flags,
                               int parts, int32_t* status, cudaStream_t s) {
+  const bool accumulate = (flags & kWgradAccumulate) != 0;
+  const bool rows16 = (flags & kWgradRows16) != 0;
   const bool gu = (parts & kWgradGateUp) != 0;
   const bool dn = (parts & kWgradDown) != 0;
   const uint64_t E = static_cast<uint64_t>(c.E);
@@ -534,16 +866,26 @@ cudaError_t launch_wgrad_bf16(const moe_config_t& c, const Groups& g,
     }
     if (p.n_seg == 0) break;
     if (gu) {
-      p.m_tiles = c.H / tc::BM;
       p.n_tiles = c.F / 128;
-      e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
+      if (rows16 && c.H % 256 == 0) {
+        p.m_tiles = c.H / 256;
+        e = tc::launch_wgrad2<0>(px, qg, qu, og, ou, p, s);
+      } else {
+        p.m_tiles = c.H / tc::BM;
+        e = tc::launch_wgrad<0, 256>(px, qg, qu, og, ou, p, s);
+      }
       if (e != cudaSuccess) return e;
     }
     if (dn) {
-      p.m_tiles = c.F / tc::BM;
       p.n_tiles = c.H / bnd;
-      e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
-                     : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
+      if (rows16 && c.F % 256 == 0 && bnd == 256) {
+        p.m_tiles = c.F / 256;
+        e = tc::launch_wgrad2<1>(ph, qd, qd, od, od, p, s);
+      } else {
+        p.m_tiles = c.F / tc::BM;
+        e = bnd == 256 ? tc::launch_wgrad<1, 256>(ph, qd, qd, od, od, p, s)
+                       : tc::launch_wgrad<1, 128>(ph, qd, qd, od, od, p, s);
+      }
       if (e != cudaSuccess) return e;
     }
   }

@@ -838,6 +838,33 @@ def layer_pass_backward(cfg: MoEConfig, x, logits, w_gate, w_up, w_down,
     return g
 
 
+def segmented_weight_grads(P, Q, segments, n_groups: int, E: int,
+                           group_expert=None) -> np.ndarray:
+    """Weight gradient of one expert projection row -> P row -> Q row, summed
+    over row ranges: dW[e] = sum over the segments s and the groups g of
+    expert e of P[rows of g in s]^T Q[rows of g in s], shape [E, cols of P,
+    cols of Q].  (x, dg) gives dWg, (x, du) dWu and (h, dy_sorted) dWd.
+
+    [PR5920 How]: the fallback's backward takes one chunk at a time and
+    accumulates the expert-weight gradients over the chunks: one segment
+    per chunk, given as (group_offsets [n_groups + 1], first_row), the rows
+    of group g being first_row + group_offsets[g] .. first_row +
+    group_offsets[g + 1].  group_expert (None: group g is expert g) maps
+    the groups of a duplication plan to their experts: a duplicate's rows
+    add into its expert's gradient ([PR4760 review on the dynamic weight
+    manager]: the copies' gradients are summed)."""
+    P = np.asarray(P, dtype=np.float64)
+    Q = np.asarray(Q, dtype=np.float64)
+    dW = np.zeros((E, P.shape[1], Q.shape[1]))
+    for off, base in segments:
+        off = np.asarray(off, dtype=INT)
+        for g in range(n_groups):
+            e = g if group_expert is None else int(group_expert[g])
+            r0, r1 = base + int(off[g]), base + int(off[g + 1])
+            dW[e] += P[r0:r1].T @ Q[r0:r1]
+    return dW
+
+
 def layer_backward_dropless(cfg, x, logits, w_gate, w_up, w_down, dy):
     return layer_pass_backward(cfg, x, logits, w_gate, w_up, w_down, dy, None)
 

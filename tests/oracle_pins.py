@@ -643,6 +643,43 @@ def pin_backward_chunked_equals_dropless():
         assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
 
 
+def pin_segmented_weight_grads():
+    """dW from segmented_weight_grads against finite differences (and torch
+    autograd) of the loss sum_r Q[r] . (P[r] W[expert of r]) over the rows
+    the segments name: two segments with foreign rows around and between
+    them, a group with no rows in one segment, and a duplicate group whose
+    rows add into its expert."""
+    rng = _rng(21)
+    rows, cp, cq, E = 40, 3, 2, 3
+    P = rng.standard_normal((rows, cp))
+    Q = rng.standard_normal((rows, cq))
+    gexp = [0, 1, 2, 1]                       # group 3 duplicates expert 1
+    segs = [(np.array([0, 3, 3, 7, 9]), 2),   # group 1 empty here
+            (np.array([0, 4, 6, 11, 12]), 20)]
+    W = rng.standard_normal((E, cp, cq))
+    got = ref.segmented_weight_grads(P, Q, segs, 4, E, gexp)
+    assert got.shape == (E, cp, cq)
+
+    def loss():
+        tot = 0.0
+        for off, base in segs:
+            for g in range(4):
+                for r in range(base + off[g], base + off[g + 1]):
+                    tot += float(Q[r] @ (P[r] @ W[gexp[g]]))
+        return tot
+    _fd_check(loss, W, got)
+    # identity group map, one segment: torch autograd of the same loss
+    off = np.array([0, 5, 5, 17])
+    Wt = torch.tensor(W, requires_grad=True)
+    Pt, Qt = torch.from_numpy(P), torch.from_numpy(Q)
+    lt = sum((Qt[off[e]:off[e + 1]] * (Pt[off[e]:off[e + 1]] @ Wt[e])).sum()
+             for e in range(E))
+    lt.backward()
+    g1 = ref.segmented_weight_grads(P, Q, [(off, 0)], 3, E)
+    assert np.allclose(g1, Wt.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.all(g1[1] == 0)                 # expert 1 has no rows
+
+
 def pin_backward_dense_reduction():
     rng = _rng(16)
     T, H, F = 7, 5, 6

@@ -216,12 +216,12 @@ def test_backward_arguments_are_rejected_before_any_launch(m):
     # a group map without its group count
     assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, p, seg, 1, rows, p, p,
                                   p, 0, None, None) == m.MOE_ERR_INVALID_ARG
-    # weight gradients: a negative range start, accumulate not 0/1
+    # weight gradients: a negative range start, an unknown flag bit
     seg[0].first_row = -1
     assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 0,
                                   None, None) == m.MOE_ERR_INVALID_ARG
     seg[0].first_row = 0
-    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 2,
+    assert lib.moe_gmm_down_wgrad(ctypes.byref(c), 0, None, seg, 1, rows, p, p, p, 4,
                                   None, None) == m.MOE_ERR_INVALID_ARG
     # layer backward: no workspace
     info = m.MoeLayerInfo()

@@ -136,6 +136,15 @@ MUTANTS = {
     "chunked_dw_not_summed": (
         "        out.dwg += g.dwg",
         "        out.dwg = g.dwg"),
+    "wgrad_segment_base_dropped": (
+        "            r0, r1 = base + int(off[g]), base + int(off[g + 1])",
+        "            r0, r1 = int(off[g]), int(off[g + 1])"),
+    "wgrad_duplicate_to_own_slot": (
+        "            e = g if group_expert is None else int(group_expert[g])",
+        "            e = g if group_expert is None else min(g, E - 1)"),
+    "wgrad_operands_swapped": (
+        "            dW[e] += P[r0:r1].T @ Q[r0:r1]",
+        "            dW[e] += (Q[r0:r1].T @ P[r0:r1]).T[::-1, ::-1]"),
     "chunk_one_too_big": (
         "c = max(1, C // worst_per_token)",
         "c = max(1, C // worst_per_token + 1)"),
