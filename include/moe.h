@@ -833,13 +833,14 @@ int32_t moe_num_chunks(const moe_config_t *cfg);
 /* Which bf16 grouped-GEMM kernel a launch takes for n_groups row groups (0:
  * the E experts' own) holding at most rows_bound rows (<= 0: T*k): the
  * one-CTA kernel (128-row tiles, two accumulators so that a tile's epilogue
- * overlaps the next tile's MMAs) or, when the groups average at least 1024
- * rows, the two-SM CTA-pair kernel (tcgen05.mma.cta_group::2, 256-row
- * tiles).  Both give the same bits for a row.  moe_gmm_* calls use
- * rows_bound = T*k; moe_layer's capped pass uses min(T*k, S*C).  Returns
- * bit 0 (GEMM1 + SwiGLU on the pair kernel), bit 1 (GEMM2 on the pair
- * kernel, only when H % 256 == 0); 0 for the one-CTA kernels or an fp32
- * layer, -1 for an invalid cfg or n_groups. */
+ * overlaps the next tile's MMAs) or, for GEMM2 when H % 256 == 0 and the
+ * groups average at least 512 rows, the two-SM CTA-pair kernel
+ * (tcgen05.mma.cta_group::2, 256-row tiles).  Both give the same bits for a
+ * row.  moe_gmm_* calls use rows_bound = T*k; moe_layer's capped pass uses
+ * min(T*k, S*C).  Returns bit 1 (GEMM2 on the pair kernel); bit 0 (once
+ * GEMM1 on a pair kernel) is never set: GEMM1 + SwiGLU always runs on the
+ * one-CTA kernel.  0 for the one-CTA kernels or an fp32 layer, -1 for an
+ * invalid cfg or n_groups. */
 int32_t moe_gmm_kernel_choice(const moe_config_t *cfg, int32_t n_groups,
                               int64_t rows_bound);
 

@@ -244,7 +244,8 @@ def moe_num_chunks(cfg) -> int:
 
 
 def moe_gmm_kernel_choice(cfg, n_groups=0, rows_bound=0) -> int:
-    """Bits: 1 GEMM1 on the CTA-pair kernel, 2 GEMM2 on it; 0: one-CTA."""
+    """Bit 1 (value 2): GEMM2 on the CTA-pair kernel; 0: the one-CTA
+    kernels (GEMM1 always; bit 0 is never set)."""
     return int(lib().moe_gmm_kernel_choice(ctypes.byref(cfg), n_groups,
                                            rows_bound))
 

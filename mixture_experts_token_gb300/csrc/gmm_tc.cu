@@ -32,14 +32,15 @@
 //   GEMM1 issues one N=256 MMA whose columns 0-127 are the gate projection
 //     and 128-255 the up projection of the same 128 output columns.
 //
-// Two-SM form (gmm_tc2_kernel, used when the output tile is 256 wide): a
-// cluster of two CTAs on one TPC shares each M=256 x N=256 tile through
-// tcgen05.mma.cta_group::2.  Each CTA stages its own 128 rows of A and half
-// of B (for GEMM1: the leader the gate columns, the peer the up columns) in
-// 6 stages of 32 KB, so a stage of compute needs a third less shared memory
-// and more loads are in flight.  The leader issues the MMAs and multicasts
-// its commits to both CTAs; the peer's TMA loads complete on the leader's
-// barrier; both CTAs run an epilogue on their own 128 rows of TMEM.
+// Two-SM form of GEMM2 (gmm_tc2_kernel, used when its output tile is 256
+// wide and groups are large): a cluster of two CTAs on one TPC shares each
+// M=256 x N=256 tile through tcgen05.mma.cta_group::2.  Each CTA stages its
+// own 128 rows of A and half of B in 6 stages of 32 KB, so a stage of
+// compute needs a third less shared memory and more loads are in flight.
+// The leader issues the MMAs and multicasts its commits to both CTAs; the
+// peer's TMA loads complete on the leader's barrier; both CTAs run an
+// epilogue on their own 128 rows of TMEM, and the peer's idle MMA lane
+// relays its warps' release of the accumulator to the leader.
 //
 // Every wait is bounded (2 s of %globaltimer); on expiry the kernel raises
 // MOE_DEV_TIMEOUT in the status word, tells the other roles to stop, drains
@@ -595,18 +596,14 @@ constexpr int kA2Bytes = BM * BK * 2;           // this CTA's 128 rows
 constexpr int kB2Bytes = BK * 128 * 2;          // this CTA's half of N=256
 constexpr int kStage2 = kA2Bytes + kB2Bytes;    // 32 KB
 constexpr uint32_t kTxPair = 2 * kStage2;       // bytes per stage, both CTAs
-constexpr int kPairArrivals = 2 * kEpilogueThreads;
 
-// MODE 0: h = silu(A Wg) * (A Wu): the leader stages the gate columns, the
-// peer the up columns of the same 128 outputs; TMEM columns 0-127 of either
-// CTA hold gate, 128-255 up, for its own 128 rows.
-// MODE 1: y_sorted = A Wd, 256 output columns: the leader stages the first
-// 128, the peer the last 128.
-template <int MODE>
+// y_sorted = A Wd, 256 output columns: the leader stages the first 128, the
+// peer the last 128 of Wd's tile.  (GEMM1 + SwiGLU stays on the one-CTA
+// kernel: at H = 7168, F = 2048 it measured 3-12 % faster than a pair form
+// at 256 to 2048 rows per group.)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gmm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, Params p) {
+                   const __grid_constant__ CUtensorMap tmB, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -634,7 +631,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(tfull + a), 1);
-      mbar_init(smem_u32(tempty + a), kPairArrivals);
+      // one arrival per epilogue warp of this CTA; the leader's also
+      // counts the peer's relay
+      mbar_init(smem_u32(tempty + a), rank == 0 ? kEpilogueThreads / 32 + 1
+                                                : kEpilogueThreads / 32);
     }
     mbar_init(smem_u32(done), 1);
     *abort_flag = 0;
@@ -643,8 +643,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB0);
-    if (MODE == 0) prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmB);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
@@ -671,7 +670,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------- TMA producer (both CTAs) ---
     if (lane == 0) {
-      const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
       int stage = 0;
       uint32_t phase = 0;
       long long fills = 0;
@@ -682,7 +680,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int a_row = goff[e] + m * BMP + static_cast<int>(rank) * BM;
         const int we = p.group_expert ? __ldg(p.group_expert + e) : e;
         const int b_row = we * p.K;
-        const int b_col = MODE == 0 ? n * 128 : n * 256 + rank * 128;
+        const int b_col = n * 256 + rank * 128;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
                          p.status)) {
@@ -694,8 +692,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_base + stage * kStage2;
           const uint32_t sb = sa + kA2Bytes;
           tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
-          tma_load_2d_pair(sb, mb, fb, b_col, b_row + kb * BK);
-          tma_load_2d_pair(sb + 8192, mb, fb, b_col + 64, b_row + kb * BK);
+          tma_load_2d_pair(sb, &tmB, fb, b_col, b_row + kb * BK);
+          tma_load_2d_pair(sb + 8192, &tmB, fb, b_col + 64, b_row + kb * BK);
           ++fills;
           if (++stage == STAGES2) {
             stage = 0;
@@ -753,6 +751,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       umma_commit_pair(smem_u32(done));
       mbar_wait(smem_u32(done), 0, nullptr, p.status);
+    } else if (lane == 0) {
+      // ---------------------------------- TMEM-empty relay (peer) -------
+      // the peer's epilogue warps arrive on its own barrier; this thread
+      // forwards each completed phase to the leader with one cluster-scope
+      // arrival, so that no epilogue warp waits on a cluster-wide fence
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = pair; tile < total_tiles; tile += npairs) {
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase, abort_flag,
+                       p.status))
+          break;
+        mbar_arrive_cluster(map_to_rank(smem_u32(tempty + acc), 0));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
     }
   } else {
     // ---------------------------------------- epilogue (both CTAs) -----
@@ -771,53 +784,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool valid = grow < goff[e + 1];
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      if (MODE == 0) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + static_cast<long long>(grow) * p.out_ld + n * 128);
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.out + static_cast<long long>(grow) * p.out_ld + n * 256);
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32x2(taddr + c, taddr + 128 + c, g, u);
-          uint32_t pk[16];
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c, r);
+        uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(g[2 * i]);
-            const float g1 = __uint_as_float(g[2 * i + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) *
-                             __uint_as_float(u[2 * i]);
-            const float h1 = g1 / (1.0f + __expf(-g1)) *
-                             __uint_as_float(u[2 * i + 1]);
-            pk[i] = pack_bf16x2(h0, h1);
-          }
-          if (valid) {
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
+                              __uint_as_float(r[2 * i + 1]));
+        if (valid) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
-                                          pk[4 * v + 2], pk[4 * v + 3]);
-          }
-        }
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + static_cast<long long>(grow) * p.out_ld + n * 256);
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c, r);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
-                                __uint_as_float(r[2 * i + 1]));
-          if (valid) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
-                                          pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            dst[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1],
+                                        pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       tc_fence_before();
-      mbar_arrive_cluster(map_to_rank(smem_u32(tempty + acc), 0));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -838,16 +825,18 @@ size_t smem_bytes(int E) {
          4 * (64 + 3 * (E + 1)) + 64;
 }
 
-// The pair form pays off only when groups are large: a pair tile covers 256
-// rows, and for smaller groups the peer SM stages rows it then masks (more
-// L2 traffic and tensor work per weight tile, measured 15-25% slower on
-// weight-streaming layers).  With >= 1024 routed rows per group on average
-// it was measured 2% (GEMM1) and 9% (GEMM2) faster.  The row count is the
-// host's bound on the rows the groups hold: T*k, or fewer when the caller
-// knows them to be capped (a capped pass keeps at most S*C rows), so that a
-// capped pass with many dropped rows does not take the pair kernel for
-// groups that are small in fact.
-constexpr long long kPairMinRowsPerGroup = 1024;
+// The pair form of GEMM2 pays off only when groups are large: a pair tile
+// covers 256 rows, and for smaller groups the peer SM stages rows it then
+// masks.  At H = 7168, F = 2048, E = 256 it measured 1-11 % slower with 256
+// routed rows per group and 7-10 % faster with 512 to 2048.  The row count
+// is the host's bound on the rows the groups hold: T*k, or fewer when the
+// caller knows them to be capped (a capped pass keeps at most S*C rows), so
+// that a capped pass with many dropped rows does not take the pair kernel
+// for groups that are small in fact.
+#ifndef MOE_PAIR_MIN_ROWS
+#define MOE_PAIR_MIN_ROWS 512
+#endif
+constexpr long long kPairMinRowsPerGroup = MOE_PAIR_MIN_ROWS;
 
 long long group_rows_bound(const moe_config_t& c, const Groups& g) {
   const long long all = static_cast<long long>(c.T) * c.k;
@@ -864,22 +853,20 @@ size_t smem_bytes_pair(int E) {
          4 * (64 + 3 * (E + 1)) + 64;
 }
 
-template <int MODE>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0,
-                        const CUtensorMap& b1, const Params& p,
-                        cudaStream_t s) {
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b,
+                        const Params& p, cudaStream_t s) {
   const size_t smem = smem_bytes_pair(p.E);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(gmm_tc2_kernel<MODE>,
+  err = cudaFuncSetAttribute(gmm_tc2_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = sms & ~1;  // whole CTA pairs
-  gmm_tc2_kernel<MODE><<<grid, kThreads, smem, s>>>(a, b0, b1, p);
+  gmm_tc2_kernel<<<grid, kThreads, smem, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -906,7 +893,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0,
 
 int gmm_pair_kinds(const moe_config_t& c, const Groups& g) {
   if (!gmm_tc_supported(c) || !tc::use_pair(c, g)) return 0;
-  return 1 | (c.H % 256 == 0 ? 2 : 0);   // GEMM2's 256-column tiles
+  return c.H % 256 == 0 ? 2 : 0;   // GEMM2's 256-column tiles
 }
 
 void set_gemm_stall_for_tests(long long fills) {
@@ -933,7 +920,6 @@ cudaError_t launch_gmm1_bf16(const moe_config_t& c, const Groups& g,
     return cudaErrorInvalidValue;
   tc::Params p1{group_offsets, g.map, g.n, c.H, c.F / 128,
                 static_cast<__nv_bfloat16*>(h), c.F, status};
-  if (tc::use_pair(c, g)) return tc::launch_pair<0>(a1, bg, bu, p1, s);
   return tc::launch_one<0, 256>(a1, bg, bu, a1, p1, s);
 }
 
@@ -951,7 +937,7 @@ cudaError_t launch_gmm2_bf16(const moe_config_t& c, const Groups& g,
   if (c.H % 256 == 0) {
     tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 256,
                   static_cast<__nv_bfloat16*>(y_sorted), c.H, status};
-    if (tc::use_pair(c, g)) return tc::launch_pair<1>(a2, bd, bd, p2, s);
+    if (tc::use_pair(c, g)) return tc::launch_pair(a2, bd, p2, s);
     return tc::launch_one<1, 256>(a2, bd, bd, a2, p2, s);
   }
   tc::Params p2{group_offsets, g.map, g.n, c.F, c.H / 128,

@@ -54,19 +54,20 @@ def run_gmm(sizes, H, F, dtype, T=None, k=1, seed=0):
 GMM_CASES = [
     # (group sizes, H, F, kernel kinds): empty groups, single rows, tile
     # edges, many tiles.  Kernel kinds is moe_gmm_kernel_choice's answer for
-    # bf16: bit 0 GEMM1 on the two-SM (CTA pair) kernel, bit 1 GEMM2 too
-    # (groups averaging >= 1024 rows); 0: the one-CTA kernel.
+    # bf16: bit 1 GEMM2 on the two-SM (CTA pair) kernel (H % 256 == 0 and
+    # groups averaging >= 512 rows); 0: the one-CTA kernels.
     ([0, 1, 127, 128, 129, 300], 256, 256, 0),
     ([5, 0, 0, 700, 3], 384, 128, 0),       # H % 256 != 0: 128-wide GEMM2
     ([128] * 4, 128, 128, 0),
-    ([1000], 512, 384, 0),
+    ([1000], 512, 384, 2),                  # one group of 1000 rows
     ([37, 250, 1, 0, 90, 64, 513, 2], 1024, 512, 0),
-    # 5201 rows in 5 groups (>= 1024 each on average): both pair kernels,
-    # with a small and a one-row group among the large ones
-    ([2100, 1500, 1300, 300, 1], 512, 256, 3),
-    ([4096, 3000], 256, 384, 3),
-    # H % 256 != 0: GEMM1 on the pair kernel, GEMM2 on the 128-wide one-CTA
-    ([1200, 1100], 384, 256, 1),
+    # 5201 rows in 5 groups (>= 512 each on average): the pair GEMM2, with a
+    # small and a one-row group among the large ones
+    ([2100, 1500, 1300, 300, 1], 512, 256, 2),
+    ([4096, 3000], 256, 384, 2),
+    ([600, 520, 0, 1000], 512, 128, 2),     # 530 rows per group
+    # H % 256 != 0: GEMM2 on the 128-wide one-CTA kernel
+    ([1200, 1100], 384, 256, 0),
 ]
 
 
@@ -74,17 +75,21 @@ def test_gmm_kernel_choice_query():
     """moe_gmm_kernel_choice follows the average rows per group, the row
     bound given, the layer dtype and H % 256 for GEMM2."""
     c = moe.make_config(2048, 512, 2, 1, 256, 1, 2.0, 0, "bf16")
-    assert moe.moe_gmm_kernel_choice(c) == 3
-    assert moe.moe_gmm_kernel_choice(c, rows_bound=2047) == 0
-    assert moe.moe_gmm_kernel_choice(c, n_groups=3) == 0
-    assert moe.moe_gmm_kernel_choice(c.with_(H=384)) == 1
+    assert moe.moe_gmm_kernel_choice(c) == 2
+    assert moe.moe_gmm_kernel_choice(c, rows_bound=1024) == 2
+    assert moe.moe_gmm_kernel_choice(c, rows_bound=1023) == 0
+    assert moe.moe_gmm_kernel_choice(c, n_groups=4) == 2
+    assert moe.moe_gmm_kernel_choice(c, n_groups=5) == 0
+    assert moe.moe_gmm_kernel_choice(c.with_(H=384)) == 0
     assert moe.moe_gmm_kernel_choice(c.with_(dtype=moe.MOE_F32)) == 0
     assert moe.moe_gmm_kernel_choice(c, n_groups=-1) == -1
     # the DeepSeek-V3-shaped layer: a 2048-token fallback chunk and the
-    # 8192-token uncapped pass both stay on the one-CTA kernel (256 groups)
+    # 8192-token uncapped pass stay on the one-CTA kernel (256 rows per
+    # group at most); the 16384-token uncapped pass takes the pair GEMM2
     d = moe.make_config(8192, 7168, 256, 8, 2048, 8, 2.0, 0, "bf16")
     assert moe.moe_gmm_kernel_choice(d) == 0
     assert moe.moe_gmm_kernel_choice(d.with_(T=2048)) == 0
+    assert moe.moe_gmm_kernel_choice(d.with_(T=16384)) == 2
 
 
 @pytest.mark.parametrize("case", GMM_CASES, ids=lambda c: f"{len(c[0])}x{c[1]}x{c[2]}")
@@ -119,14 +124,14 @@ def test_gmm_parity(case, dtype):
 
 
 def test_gmm_pair_kernel_full_dims():
-    """The two-SM kernels at the DeepSeek-V3 layer's dims (H=7168,
-    F=2048): 4157 rows in 4 ragged groups, one of them a 256-row tile plus
-    one row.  Every row of every group against the oracle."""
+    """The two-SM GEMM2 at the DeepSeek-V3 layer's dims (H=7168, F=2048):
+    4157 rows in 4 ragged groups, one of them a 256-row tile plus one row.
+    Every row of every group against the oracle."""
     sizes = [1500, 1100, 1300, 257]
     H, F = 7168, 2048
     R0 = int(sum(sizes))
     assert moe.moe_gmm_kernel_choice(
-        moe.make_config(R0, H, 4, 1, F, 1, 2.0, 0, "bf16")) == 3
+        moe.make_config(R0, H, 4, 1, F, 1, 2.0, 0, "bf16")) == 2
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=11)
     W = expert_accessor(wg, wu, wd)
     xh = f64(xs[:R])
@@ -155,10 +160,8 @@ def test_gmm_small_layer_shape():
 
 
 def test_gmm_pair_kernel_row_independence():
-    """Large groups take the CTA-pair kernel (256-row tiles): a row computed
-    at another offset inside its pair tile gives the same bits, and the
-    same bits as the one-CTA kernel computes for it in a small-group
-    launch."""
+    """Large groups take the CTA-pair GEMM2 (256-row tiles): a row computed
+    at another offset inside its pair tile gives the same bits."""
     H, F = 256, 256
     sizes = [1500, 700]                      # 1100 rows per group: pair
     xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=7)
@@ -179,7 +182,7 @@ def test_gmm_pair_kernel_row_independence():
 
 
 def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
-    """The same rows and weights through the CTA-pair kernel (2 groups of
+    """The same rows and weights through the CTA-pair GEMM2 (2 groups of
     ~1100 rows) and the one-CTA kernel (the same groups padded with empty
     ones, so fewer rows per group): identical bits.  This keeps chunked and
     dropless passes bit-identical when they pick different kernels."""
@@ -192,7 +195,7 @@ def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
     off8 = torch.tensor([0, 1500] + [R] * (n_groups - 1), dtype=torch.int32,
                         device="cuda")
     cfg = moe.make_config(R, H, 2, 1, F, 1, 2.0, 0, "bf16")
-    assert moe.moe_gmm_kernel_choice(cfg) == 3
+    assert moe.moe_gmm_kernel_choice(cfg) == 2
     assert moe.moe_gmm_kernel_choice(cfg, n_groups=n_groups) == 0
     h2 = torch.empty_like(h)
     ys2 = torch.empty_like(ys)
