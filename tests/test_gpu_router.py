@@ -7,8 +7,9 @@ accumulation over H terms, whatever the cancellation in the sum).  Shapes
 cover the tensor-core form (bf16, H % 64 == 0, E % 128 == 0: the
 DeepSeek-V3 and Llama4-Maverick layers at full size, several column tiles,
 ragged row tiles, one token; small batches with the reduction split over a
-cluster, including CTAs with an empty k-slice) and the CUDA-core form (the fp32 tiny layer,
-E = 16 of the small layer, odd H and E).
+cluster, including CTAs with an empty k-slice) and the CUDA-core forms (the fp32 tiny layer,
+E = 16 of the small layer, odd H and E, E = 1 and 64 with Wr staged in several
+chunks; E = 96, above 64 and no multiple of 128, on the thread-per-expert kernel).
 """
 import numpy as np
 import pytest
@@ -32,6 +33,12 @@ CASES = [
     WORKLOADS["small"].with_(name="h104_e24", T=333, H=104, E=24, S=4),
     WORKLOADS["tiny"].with_(name="f32_e40", T=77, H=48, E=40, S=4,
                             routing="zipf", zipf_s=1.0),
+    # the warp kernel (E <= 64): Wr staged in two chunks of rows (160 rows
+    # a chunk at E = 64), a last CTA with fewer tokens than its warps take;
+    # one expert
+    WORKLOADS["small"].with_(name="e64_h200", T=777, H=200, E=64, S=4),
+    WORKLOADS["small"].with_(name="e1", T=50, H=64, E=1, k=1, S=1),
+    WORKLOADS["small"].with_(name="e96", T=300, H=128, E=96, S=4),
     # batches whose tiles leave most SMs idle: the reduction split over a
     # cluster (8 CTAs at up to 1024 tokens of H = 7168, 2 at 4096 tokens)
     WORKLOADS["dsv3"].with_(name="split8_t1", T=1),
