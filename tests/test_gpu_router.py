@@ -33,10 +33,10 @@ CASES = [
     WORKLOADS["small"].with_(name="h104_e24", T=333, H=104, E=24, S=4),
     WORKLOADS["tiny"].with_(name="f32_e40", T=77, H=48, E=40, S=4,
                             routing="zipf", zipf_s=1.0),
-    # the warp kernel (E <= 64): Wr staged in two chunks of rows (160 rows
-    # a chunk at E = 64), a last CTA with fewer tokens than its warps take;
-    # one expert
-    WORKLOADS["small"].with_(name="e64_h200", T=777, H=200, E=64, S=4),
+    # the warp kernel (E <= 64): Wr staged in three chunks of rows (256
+    # rows a chunk at E = 64, the last one 8 rows), a last CTA with fewer
+    # tokens than its warps take; one expert
+    WORKLOADS["small"].with_(name="e64_h520", T=777, H=520, E=64, S=4),
     WORKLOADS["small"].with_(name="e1", T=50, H=64, E=1, k=1, S=1),
     WORKLOADS["small"].with_(name="e96", T=300, H=128, E=96, S=4),
     # batches whose tiles leave most SMs idle: the reduction split over a
