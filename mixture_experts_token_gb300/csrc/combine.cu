@@ -6,7 +6,11 @@
 // psum_scatter across shards in the ring variant; a gather here, where all
 // shards share one GPU).  Dropped rows (row_of = -1) contribute nothing.
 //
-// One CTA per token.  Each thread owns a few 16-byte column chunks, issues
+// One CTA per token, or per (token, column slice) when there are too few
+// tokens to keep every SM busy (a fallback chunk of 128 tokens, say): the
+// row's 16-byte chunks are then split into `splits` contiguous slices, one
+// CTA each, so that the k row loads of a token are spread over several SMs.
+// Each thread owns a few 16-byte column chunks, issues
 // the k row loads of a chunk back to back (the slot loop is unrolled to a
 // compile-time bound so the loads overlap), accumulates in fp32 in slot
 // order j = 0..k-1 (deterministic: no atomics), and stores once.
@@ -14,6 +18,8 @@
 // With null weights every kept row counts once: the permute's transpose,
 // dx[t] = sum_j dx_sorted[row_of[t,j]], in the backward pass.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "internal.h"
 
@@ -68,7 +74,8 @@ struct Vec<__nv_bfloat16> {
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const int4* __restrict__ ys, const int32_t* __restrict__ row_of,
-    const float* __restrict__ topk_w, int k, int n16, int4* __restrict__ y) {
+    const float* __restrict__ topk_w, int k, int n16, int per_split,
+    int4* __restrict__ y) {
   using V = Vec<T>;
   __shared__ int rows[KMAX];
   __shared__ float wts[KMAX];
@@ -81,7 +88,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
                             : 1.0f;
   }
   __syncthreads();
-  for (int c0 = tid; c0 < n16; c0 += kThreads * kUnroll) {
+  const int begin = blockIdx.y * per_split;
+  const int end = min(n16, begin + per_split);
+  for (int c0 = begin + tid; c0 < end; c0 += kThreads * kUnroll) {
     float acc[kUnroll][V::N];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * kThreads;
-        if (c < n16) {
+        if (c < end) {
           float f[V::N];
           V::load(__ldg(src + c), f);
 #pragma unroll
@@ -108,9 +117,23 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int c = c0 + u * kThreads;
-      if (c < n16) dst[c] = V::store(acc[u]);
+      if (c < end) dst[c] = V::store(acc[u]);
     }
   }
+}
+
+// CTAs per token: enough that the grid holds about kCtasPerSm CTAs per SM,
+// but no slice narrower than one pass of the CTA's threads.
+constexpr int kCtasPerSm = 4;
+
+int combine_splits(int T, int n16) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess)
+    return 1;
+  const int want = (kCtasPerSm * sms + T - 1) / T;
+  return std::max(1, std::min(want, n16 / kThreads));
 }
 
 template <typename T>
@@ -118,13 +141,16 @@ cudaError_t launch_typed(const moe_config_t& c, const void* ys,
                          const int32_t* row_of, const float* w, void* y,
                          cudaStream_t s) {
   const int n16 = c.H * static_cast<int>(sizeof(T)) / 16;
+  const int splits = combine_splits(c.T, n16);
+  const int per = (n16 + splits - 1) / splits;
+  const dim3 grid(static_cast<unsigned>(c.T), static_cast<unsigned>(splits));
   const int4* src = static_cast<const int4*>(ys);
   int4* dst = static_cast<int4*>(y);
-#define MOE_COMBINE_CASE(KM)                                          \
-  if (c.k <= KM) {                                                    \
-    combine_kernel<T, KM><<<c.T, kThreads, 0, s>>>(src, row_of, w, c.k, \
-                                                   n16, dst);         \
-    return cudaGetLastError();                                        \
+#define MOE_COMBINE_CASE(KM)                                            \
+  if (c.k <= KM) {                                                      \
+    combine_kernel<T, KM><<<grid, kThreads, 0, s>>>(src, row_of, w, c.k, \
+                                                    n16, per, dst);     \
+    return cudaGetLastError();                                          \
   }
   MOE_COMBINE_CASE(1)
   MOE_COMBINE_CASE(2)

@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(64) scan_uniq_kernel(
 
 constexpr int kScatterThreads = 128;
 constexpr int kScatterUnroll = 8;
+constexpr int kScatterCtasPerSm = 4;
 
 // Block-shard tables up to this many counts are summed by every scatter CTA
 // (no scan kernel between assign and the scatter).
@@ -365,8 +366,11 @@ inline bool inline_uniq(int nb, int S) {
   return static_cast<long long>(nb) * S <= kInlineUniqCounts;
 }
 
-// One CTA per token.  The first slice of x[t] (all of it up to 16 KB) is
-// read before the wait for the tables.  Dedup position of (t, j) in shard
+// One CTA per token, or per (token, column slice) when there are too few
+// tokens to keep every SM busy: the row's 16-byte chunks are split into
+// contiguous slices, one CTA each, and only the slice-0 CTA of a token
+// writes its index outputs.  The first part of the CTA's slice (all of it
+// up to 16 KB) is read before the wait for the tables.  Dedup position of (t, j) in shard
 // s: the members of shards before s, plus those of s in the token blocks
 // before t's, plus t's rank among its block's members.  With inline_uniq
 // the first two come from the block_ucnt counts as assign left them, and
@@ -376,7 +380,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     int inline_uniq, const int32_t* __restrict__ row_of,
     const int32_t* __restrict__ block_ucnt, const int32_t* __restrict__ urank,
     int32_t* __restrict__ uniq_offsets, int4* __restrict__ x_sorted,
-    int32_t* __restrict__ expand_idx, int32_t* __restrict__ uniq_tokens) {
+    int32_t* __restrict__ expand_idx, int32_t* __restrict__ uniq_tokens,
+    int per_split) {
   __shared__ int rows[kMaxTopK];
   __shared__ int codes[kMaxTopK];
   __shared__ int tot[kMaxShards];     // members of shard s, all blocks
@@ -386,12 +391,15 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
   const long long tk = static_cast<long long>(t) * k;
   // x_sorted == null: the index outputs only (no row is read or written)
   const int n16r = x_sorted != nullptr ? n16 : 0;
+  const bool index_cta = blockIdx.y == 0;  // writes the index outputs
+  const int begin = blockIdx.y * per_split;
+  const int end = min(n16r, begin + per_split);
   const int4* src = x + static_cast<long long>(t) * n16r;
   int4 v[kScatterUnroll];
 #pragma unroll
   for (int u = 0; u < kScatterUnroll; ++u) {
-    const int c = tid + u * kScatterThreads;
-    if (c < n16r) v[u] = __ldg(src + c);
+    const int c = begin + tid + u * kScatterThreads;
+    if (c < end) v[u] = __ldg(src + c);
   }
   for (int q = tid; q < S; q += kScatterThreads) {
     tot[q] = 0;
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     rows[tid] = row_of[tk + tid];
     codes[tid] = urank[tk + tid];
   }
-  if (inline_uniq) {
+  if (inline_uniq && index_cta) {
     constexpr int kPer = kInlineUniqCounts / kScatterThreads;
     int c[kPer];
 #pragma unroll
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     }
   }
   __syncthreads();
-  if (tid < k && rows[tid] >= 0) {
+  if (index_cta && tid < k && rows[tid] >= 0) {
     const int code = codes[tid];
     const int q = code & 63;
     int base;
@@ -438,18 +446,19 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
       if (rows[p] >= 0 && (codes[p] & 63) == q) first = false;
     if (first) uniq_tokens[upos] = t;
   }
-  if (inline_uniq && t == 0 && tid <= S) {
+  if (inline_uniq && index_cta && t == 0 && tid <= S) {
     int o = 0;
     for (int p = 0; p < tid; ++p) o += tot[p];
     uniq_offsets[tid] = o;
   }
   __syncthreads();
-  for (int c0 = tid; c0 < n16r; c0 += kScatterThreads * kScatterUnroll) {
-    if (c0 != tid) {
+  for (int c0 = begin + tid; c0 < end;
+       c0 += kScatterThreads * kScatterUnroll) {
+    if (c0 != begin + tid) {
 #pragma unroll
       for (int u = 0; u < kScatterUnroll; ++u) {
         const int c = c0 + u * kScatterThreads;
-        if (c < n16r) v[u] = __ldg(src + c);
+        if (c < end) v[u] = __ldg(src + c);
       }
     }
     for (int j = 0; j < k; ++j) {
@@ -459,7 +468,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 #pragma unroll
       for (int u = 0; u < kScatterUnroll; ++u) {
         const int c = c0 + u * kScatterThreads;
-        if (c < n16r) dst[c] = v[u];
+        if (c < end) dst[c] = v[u];
       }
     }
   }
@@ -473,11 +482,11 @@ size_t assign_smem_bytes(int E, int S) {
 // finished (that kernel calls allow_dependents(), this one
 // wait_for_producer() before reading its output).
 template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid,
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid,
                              unsigned block, size_t smem, cudaStream_t s,
                              Args... args) {
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(grid);
+  lc.gridDim = grid;
   lc.blockDim = dim3(block);
   lc.dynamicSmemBytes = smem;
   lc.stream = s;
@@ -555,12 +564,26 @@ cudaError_t launch_permute_scatter(const moe_config_t& c, const void* x,
   if (c.T == 0) return cudaSuccess;
   const int nb = (c.T + TB - 1) / TB;
   const int n16 = c.H * elem_bytes(c.dtype) / 16;
-  return launch_dependent(scatter_kernel, c.T, kScatterThreads, 0, s,
+  // CTAs per token: about kScatterCtasPerSm CTAs per SM over the grid, but
+  // no slice narrower than one pass of the CTA's threads
+  int splits = 1;
+  int dev = 0, sms = 0;
+  if (x_sorted != nullptr && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+          cudaSuccess) {
+    const int want = (kScatterCtasPerSm * sms + c.T - 1) / c.T;
+    splits = std::max(1, std::min(want, n16 / kScatterThreads));
+  }
+  const int per = (n16 + splits - 1) / splits;
+  return launch_dependent(scatter_kernel,
+                          dim3(static_cast<unsigned>(c.T),
+                               static_cast<unsigned>(splits)),
+                          kScatterThreads, 0, s,
                           static_cast<const int4*>(x), n16, c.k, c.S, nb,
                           inline_uniq(nb, c.S) ? 1 : 0, row_of,
                           ws.block_ucnt, ws.urank, uniq_offsets,
                           static_cast<int4*>(x_sorted), expand_idx,
-                          uniq_tokens);
+                          uniq_tokens, per);
 }
 
 cudaError_t launch_permute(const moe_config_t& c, const void* x,

@@ -228,6 +228,32 @@ def test_gmm_row_result_independent_of_tile_position():
     assert torch.equal(ys2[shift:], ys[:R])
 
 
+@pytest.mark.parametrize("T,H,dtype", [(37, 7168, "bf16"), (300, 7168, "bf16"),
+                                         (90, 3072, "f32")])
+def test_combine_split_rows(T, H, dtype):
+    """Few tokens with wide rows: each token's combine is split over several
+    CTAs (column slices of 128-chunk passes, the last slice ragged at
+    T = 300), against the oracle and with no column left unwritten."""
+    rng = np.random.default_rng(T)
+    E, S, k = 64, 8, 8
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    oi, ow, _ = ref.route(L, k)
+    p = ref.permute_indices(oi, E, S, None)
+    R = int(p.group_offsets[-1])
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    ys = torch.randn(T * k, H, device="cuda").to(dt)
+    cfg = moe.make_config(T, H, E, k, 128, S, 2.0, 0, dtype)
+    row_of = torch.from_numpy(p.row_of.astype(np.int32)).cuda()
+    w = torch.from_numpy(ow.astype(np.float32)).cuda()
+    y = torch.full((T, H), float("nan"), dtype=dt, device="cuda")
+    moe.moe_combine(cfg, ys, row_of, w, y)
+    torch.cuda.synchronize()
+    want = ref.combine(f64(ys[:R]), p.row_of, ow.astype(np.float32), H)
+    got = f64(y)
+    assert np.isfinite(got).all()
+    assert_close(got, want, TOL[dtype], 'y')
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("k", [1, 2, 8, 13])
 def test_combine_parity(dtype, k):

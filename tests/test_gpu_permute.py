@@ -42,6 +42,11 @@ CASES = [
     # 157 token blocks x 8 shards: the dedup scan kernel with 8 shards
     WORKLOADS["small"].with_(name="t20000", T=20000, H=64, E=256, k=8, S=8,
                              zipf_s=1.2),
+    # few tokens with wide rows: each row's copy split over several CTAs
+    # (7 slices of 128 chunks at H = 7168; 5 at H = 5120; 2 at H = 2048)
+    WORKLOADS["dsv3"].with_(name="split_t100_h7168", T=100),
+    WORKLOADS["l4mav"].with_(name="split_t50_h5120", T=50),
+    WORKLOADS["small"].with_(name="split_t333_h2048", T=333, H=2048),
 ]
 
 
