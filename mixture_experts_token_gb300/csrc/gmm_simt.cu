@@ -7,10 +7,13 @@
 // (MaxText pull request 4760), review of get_gmm_for_local_experts: a
 // grouped matmul over ragged group_sizes).
 //
-// Tiles of 32 output columns x 32 rows: the weight tile of a k-slab is
-// shared by the rows of one expert through shared memory, and each thread
-// accumulates 4 rows of one column.  A tile that straddles two experts is
-// split per row (each row reads its own expert's weights from L2).
+// Tiles of 32 output columns x 32 rows; each thread accumulates 4 rows of
+// one column, over k in ascending order.  For each k-slab, the slab of the
+// input rows is staged in shared memory, then, for each group with rows in
+// the tile (the rows are sorted, so those groups are consecutive; usually
+// one or two), that group's expert's weight slab, with coalesced loads, and
+// the rows of that group accumulate it.  A row's sum runs over k in the
+// same order wherever its tile starts, so it gets the same bits.
 #include "internal.h"
 
 namespace moe {
@@ -43,20 +46,25 @@ __global__ void __launch_bounds__(256) gmm_f32_kernel(
     const float* __restrict__ w0, const float* __restrict__ w1,
     float* __restrict__ out, int rows_alloc) {
   __shared__ float sa[BR][KS + 1];
+  constexpr int kW1 = MODE == 0 ? 1 : 0;  // slot of the up weights
+  __shared__ float sw[kW1 + 1][KS][BN];
   const int R = __ldg(off + E);
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int n = blockIdx.x * BN + tx;
   for (int r0 = blockIdx.y * BR; r0 < R && r0 < rows_alloc;
        r0 += gridDim.y * BR) {
     float g[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
-    int rr[4], ee[4];
+    int rr[4], gg[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       rr[q] = r0 + ty + 8 * q;
-      const int g = rr[q] < R ? expert_of_row(off, E, rr[q]) : 0;
-      ee[q] = group_expert ? max(__ldg(group_expert + g), 0) : g;
+      gg[q] = rr[q] < R ? expert_of_row(off, E, rr[q]) : -1;
     }
+    // the groups of the tile's rows: consecutive, as the rows are sorted
+    const int gfirst = expert_of_row(off, E, r0);
+    const int glast = expert_of_row(off, E, min(r0 + BR, R) - 1);
     for (int k0 = 0; k0 < K; k0 += KS) {
+      const int kend = min(KS, K - k0);
       __syncthreads();
       for (int i = ty * BN + tx; i < BR * KS; i += 256) {
         const int rl = i / KS, kl = i % KS;
@@ -65,17 +73,31 @@ __global__ void __launch_bounds__(256) gmm_f32_kernel(
                          ? __ldg(a + static_cast<long long>(r) * K + kk)
                          : 0.0f;
       }
-      __syncthreads();
-      if (n < N) {
-        const int kend = min(KS, K - k0);
-        for (int kl = 0; kl < kend; ++kl) {
+      for (int grp = gfirst; grp <= glast; ++grp) {
+        if (__ldg(off + grp + 1) == __ldg(off + grp)) continue;  // empty
+        const int ex = group_expert ? max(__ldg(group_expert + grp), 0) : grp;
+        if (grp != gfirst) __syncthreads();  // the previous group's readers
+        for (int i = ty * BN + tx; i < KS * BN; i += 256) {
+          const int kl = i / BN, nl = i % BN;
+          const int kk = k0 + kl, nn = blockIdx.x * BN + nl;
+          const bool in = kk < K && nn < N;
+          const long long widx = (static_cast<long long>(ex) * K + kk) * N + nn;
+          sw[0][kl][nl] = in ? __ldg(w0 + widx) : 0.0f;
+          if (MODE == 0) sw[kW1][kl][nl] = in ? __ldg(w1 + widx) : 0.0f;
+        }
+        __syncthreads();
+        if (n < N) {
+#pragma unroll 8
+          for (int kl = 0; kl < kend; ++kl) {
+            const float w0v = sw[0][kl][tx];
+            const float w1v = MODE == 0 ? sw[kW1][kl][tx] : 0.0f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const long long widx =
-                (static_cast<long long>(ee[q]) * K + k0 + kl) * N + n;
-            const float av = sa[ty + 8 * q][kl];
-            g[q] = fmaf(av, __ldg(w0 + widx), g[q]);
-            if (MODE == 0) u[q] = fmaf(av, __ldg(w1 + widx), u[q]);
+            for (int q = 0; q < 4; ++q) {
+              if (gg[q] != grp) continue;
+              const float av = sa[ty + 8 * q][kl];
+              g[q] = fmaf(av, w0v, g[q]);
+              if (MODE == 0) u[q] = fmaf(av, w1v, u[q]);
+            }
           }
         }
       }
