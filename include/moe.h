@@ -847,8 +847,9 @@ int32_t moe_gmm_kernel_choice(const moe_config_t *cfg, int32_t n_groups,
 /* Static text for a status code. */
 const char *moe_status_string(moe_status_t status);
 
-/* For tests of failure detection only: with fills >= 0 the bf16 GEMM's TMA
- * producer stops after that many pipeline-stage fills, so the MMA warp's
+/* For tests of failure detection only: with fills >= 0 the TMA producers of
+ * the bf16 GEMM, of the router's cluster form and of the two-SM weight
+ * gradient stop after that many pipeline-stage fills, so the MMA warp's
  * bounded wait runs out (about 2 s): the kernel then sets MOE_DEV_TIMEOUT in
  * the status word, stops its other roles, drains its copies and MMAs, frees
  * its tensor memory and returns, and the CUDA context stays usable.  -1

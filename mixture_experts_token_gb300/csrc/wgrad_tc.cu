@@ -6,6 +6,8 @@
 // accumulates the expert-weight gradients over the chunks; "Moe dynamic
 // redundancy" (MaxText pull request 4760), review comments: the expert FFN
 // is a grouped matmul over experts with ragged group sizes.
+#include <atomic>
+
 #include "tc_common.cuh"
 
 namespace moe {
@@ -58,7 +60,13 @@ struct WParams {
                  // tiles add onto a slice zeroed beforehand
   int E;         // experts (dW slices)
   int32_t* status;
+  // Tests of the timeout path only (the two-SM kernel): both CTAs' producers
+  // stop after this many stage fills (-1: never), so the MMA's wait runs out.
+  long long stall_after_fills = -1;
 };
+
+// The GEMMs' test hook (gmm_tc.cu), shared by the two-SM weight gradient.
+extern std::atomic<long long> g_stall_after_fills;
 
 // L2 policies: the weight gradients stream through L2 once (evict first);
 // the activation rows feed every tile of their expert (evict last).
@@ -567,6 +575,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int r1 = p.seg_base[sg] + __ldg(p.seg_off[sg] + g + 1);
           for (int r = p.seg_base[sg] + __ldg(p.seg_off[sg] + g); r < r1;
                r += BK) {
+            if (p.stall_after_fills >= 0 && fills >= p.stall_after_fills) {
+              ok = false;  // test hook: leave the MMA waiting
+              break;
+            }
             if (!mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag,
                            p.status)) {
               ok = false;
@@ -768,8 +780,9 @@ size_t smem_bytes_wgrad2(int G, int E) {
 template <int WMODE>
 cudaError_t launch_wgrad2(const CUtensorMap& pm, const CUtensorMap& q0,
                           const CUtensorMap& q1, const CUtensorMap& o0,
-                          const CUtensorMap& o1, const WParams& p,
+                          const CUtensorMap& o1, WParams p,
                           cudaStream_t s) {
+  p.stall_after_fills = g_stall_after_fills.load();
   const size_t smem = smem_bytes_wgrad2(p.G, p.E);
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);

@@ -1,5 +1,5 @@
 """Failure detection on the GPU without a fault: the bounded waits of the
-GEMM and of the router's cluster kernel.
+GEMM, of the router's cluster kernel and of the two-SM weight gradient.
 
 A test hook stops the GEMM's TMA producer after a few stage fills, so the
 MMA warp waits on a barrier nothing will complete.  The wait gives up after
@@ -97,3 +97,37 @@ def test_split_router_wait_times_out_and_context_survives():
     assert int(status.item()) == 0
     want = ref.router_logits(f64(x), f64(wr), off)
     assert_close(f64(L), want, 1e-4, "logits after the timeout")
+
+
+def test_pair_wgrad_wait_times_out_and_context_survives():
+    """The two-SM weight gradient (a CTA pair per tile of dW): with both
+    CTAs' producers stopped after 3 stage fills, the leader's MMA wait runs
+    out, the status word reports MOE_DEV_TIMEOUT, both CTAs' epilogues and
+    the peer's TMEM relay give up on their own bounded waits, both CTAs pass
+    the final cluster barrier and the launch returns; the next launch is
+    correct."""
+    from tests.test_gpu_wgrad_pair import case_cfg, run
+    H, F, G = 512, 256, 4
+    off = np.array([0, 400, 416, 416, 688], dtype=np.int32)  # 7 and 5 blocks
+    segs = [(off, 3)]
+    rows = 3 + int(off[-1]) + 5
+    gen = torch.Generator().manual_seed(11)
+    t = {n: (torch.randn((rows, w), generator=gen) * 0.5).to(torch.bfloat16)
+         for n, w in (("x", H), ("dg", F), ("du", F), ("h", F), ("dy", H))}
+    cfg = case_cfg(H, F, G)
+    try:
+        moe.moe_test_stall_gemm_producer(3)
+        t0 = time.time()
+        _, st = run(cfg, segs, rows, t, moe.MOE_WGRAD_ROWS16, G, None)
+        took = time.time() - t0
+    finally:
+        moe.moe_test_stall_gemm_producer(-1)
+    assert st & moe.MOE_DEV_TIMEOUT
+    assert took < 60.0
+    dw, st = run(cfg, segs, rows, t, moe.MOE_WGRAD_ROWS16, G, None)
+    assert st == 0
+    ops = {n: f64(v) for n, v in t.items()}
+    for got, p_, q_ in ((dw[0], "x", "dg"), (dw[1], "x", "du"),
+                        (dw[2], "h", "dy")):
+        want = ref.segmented_weight_grads(ops[p_], ops[q_], segs, G, G)
+        assert_close(f64(got), want, 1e-3, f"d{q_} after the timeout")
