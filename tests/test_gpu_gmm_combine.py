@@ -206,20 +206,23 @@ def test_gmm_pair_and_single_cta_kernels_agree_bitwise():
     assert torch.equal(ys2[:R], ys[:R])
 
 
-def test_gmm_row_result_independent_of_tile_position():
-    """The same row computed at a different offset inside its 128-row tile
-    gives the same bits (this makes chunked and dropless passes agree
-    exactly)."""
-    H, F = 256, 256
-    sizes = [200, 77, 300]
-    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, "bf16", seed=5)
+@pytest.mark.parametrize("dtype,H,F,sizes", [
+    ("bf16", 256, 256, [200, 77, 300]),
+    # fp32 (CUDA cores, 32-row tiles): groups that straddle tiles in both
+    # runs, a group inside one tile, one-row groups
+    ("f32", 96, 64, [45, 7, 1, 70, 33, 1, 64]),
+])
+def test_gmm_row_result_independent_of_tile_position(dtype, H, F, sizes):
+    """The same row computed at a different offset inside its tile gives
+    the same bits (this makes chunked and dropless passes agree exactly)."""
+    xs, off, (wg, wu, wd), h, ys, R = run_gmm(sizes, H, F, dtype, seed=5)
     shift = 37
     xs2 = torch.cat([torch.randn(shift, H, device="cuda").to(xs.dtype),
                      xs[:R]])
     off2 = torch.from_numpy(np.concatenate(
         [[0], np.cumsum([sizes[0] + shift] + sizes[1:])]).astype(np.int32)
     ).cuda()
-    cfg = moe.make_config(R + shift, H, 3, 1, F, 1, 2.0, 0, "bf16")
+    cfg = moe.make_config(R + shift, H, len(sizes), 1, F, 1, 2.0, 0, dtype)
     h2 = torch.empty((R + shift, F), dtype=xs.dtype, device="cuda")
     ys2 = torch.empty((R + shift, H), dtype=xs.dtype, device="cuda")
     moe.moe_gmm_swiglu(cfg, xs2, off2, wg, wu, wd, h2, ys2)
