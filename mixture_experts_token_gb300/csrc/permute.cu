@@ -370,11 +370,12 @@ inline bool inline_uniq(int nb, int S) {
 // tokens to keep every SM busy: the row's 16-byte chunks are split into
 // contiguous slices, one CTA each, and only the slice-0 CTA of a token
 // writes its index outputs.  The first part of the CTA's slice (all of it
-// up to 16 KB) is read before the wait for the tables.  Dedup position of (t, j) in shard
-// s: the members of shards before s, plus those of s in the token blocks
-// before t's, plus t's rank among its block's members.  With inline_uniq
-// the first two come from the block_ucnt counts as assign left them, and
-// CTA 0 writes uniq_offsets; otherwise scan_uniq has scanned them.
+// up to 16 KB) is read before the wait for the tables.  Dedup position of
+// (t, j) in shard s: the members of shards before s, plus those of s in
+// the token blocks before t's, plus t's rank among its block's members.
+// With inline_uniq the first two come from the block_ucnt counts as assign
+// left them, and CTA 0 writes uniq_offsets; otherwise scan_uniq has
+// scanned them.
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     const int4* __restrict__ x, int n16, int k, int S, int nb,
     int inline_uniq, const int32_t* __restrict__ row_of,
