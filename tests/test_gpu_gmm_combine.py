@@ -231,8 +231,16 @@ def test_gmm_row_result_independent_of_tile_position(dtype, H, F, sizes):
     assert torch.equal(ys2[shift:], ys[:R])
 
 
+def _draw_combine(i):
+    rng = np.random.default_rng(4000 + i)
+    dtype = "f32" if i % 3 == 2 else "bf16"
+    H = 64 * int(rng.integers(16, 113 if dtype == "bf16" else 65))
+    return int(rng.integers(1, 600)), H, dtype
+
+
 @pytest.mark.parametrize("T,H,dtype", [(37, 7168, "bf16"), (300, 7168, "bf16"),
-                                         (90, 3072, "f32")])
+                                         (90, 3072, "f32")] +
+                         [_draw_combine(i) for i in range(6)])
 def test_combine_split_rows(T, H, dtype):
     """Few tokens with wide rows: each token's combine is split over several
     CTAs (column slices of 128-chunk passes, the last slice ragged at

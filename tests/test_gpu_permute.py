@@ -193,3 +193,39 @@ def test_permute_parity_sweep_64k(routing):
                                p.sorted_token)
     del bufs, x
     torch.cuda.empty_cache()
+
+
+def draw_split(i):
+    """Seeded random pass with few tokens and wide rows (the scatter splits
+    each row over several CTAs): T 1..600, H a multiple of 64 up to 8192,
+    E, k and S drawn, bf16 or fp32, Zipf or uniform routing."""
+    rng = np.random.default_rng(5000 + i)
+    S = int(rng.choice([1, 2, 4, 8]))
+    E = S * int(rng.integers(1, 33))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    dtype = "f32" if i % 4 == 3 else "bf16"
+    H = 64 * int(rng.integers(8, 129))
+    if dtype == "f32":
+        H = min(H, 4096)
+    T = int(rng.integers(1, 601))
+    routing = str(rng.choice(["uniform", "zipf"]))
+    return WORKLOADS["small"].with_(
+        name=f"split_rnd{i}", T=T, H=H, E=E, k=k, S=S, dtype=dtype,
+        routing=routing, zipf_s=1.2 if routing == "zipf" else 0.0,
+        seed=200 + i)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_permute_split_random(i):
+    """Bit-exact against the oracle, capped (factor 0.5) and dropless."""
+    wl = draw_split(i)
+    cfg = cfg_from(wl, factor=0.5)
+    x, L = inputs(wl)
+    idx, _ = gpu_route(cfg, L)
+    oi, _, _ = ref.route(L, wl.k)
+    assert np.array_equal(np_(idx), oi)
+    C = ref.capacity(wl.T, wl.k, wl.S, 0.5)
+    for capped in (True, False):
+        bufs = gpu_permute(cfg, x, idx, capped)
+        p = ref.permute_indices(oi, wl.E, wl.S, C if capped else None)
+        compare_permutation(bufs, p, x.cpu())

@@ -134,3 +134,34 @@ def test_router_rejects_bad_arguments():
         moe.moe_router_logits(cfg, x.view(torch.uint8)[:, 2:], wr, None, out)
     # T = 0 does nothing
     moe.moe_router_logits(cfg_from(wl, T=0), x, wr, None, out)
+
+
+def draw_small_e(i):
+    """Seeded random router case for the CUDA-core kernels: E in 1..64
+    (the warp kernel) or 65..200 not a multiple of 128 (thread-per-expert),
+    H a whole number of 16-byte words, ragged T, bf16 or fp32."""
+    rng = np.random.default_rng(6000 + i)
+    dtype = "f32" if i % 3 == 2 else "bf16"
+    E = int(rng.integers(1, 65)) if i % 4 else int(rng.integers(65, 200))
+    if E % 128 == 0:
+        E += 1
+    step = 4 if dtype == "f32" else 8
+    H = step * int(rng.integers(1, 400))
+    T = int(rng.integers(1, 3000))
+    base = WORKLOADS["tiny"] if dtype == "f32" else WORKLOADS["small"]
+    return base.with_(name=f"rnd{i}", T=T, H=H, E=E, k=1, S=1,
+                      routing="uniform", seed=100 + i)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_router_logits_random_small_e(i):
+    wl = draw_small_e(i)
+    x = make_x(wl, "cuda")
+    wr = make_router_weight(wl, "cuda")
+    off = make_logit_offset(wl) if i % 2 else None
+    got = f64(gpu_logits(wl, x, wr, off))
+    xh, wh = f64(x), f64(wr)
+    want = ref.router_logits(xh, wh, off)
+    scale = np.abs(xh) @ np.abs(wh) + np.abs(want)
+    assert_close(got, want, 1e-4, f"logits {wl.name} T{wl.T} H{wl.H} E{wl.E}",
+                 scale=scale, cw_bound=2.0 ** -10)

@@ -157,3 +157,55 @@ def test_rows16_statement_checked():
     ops = {n: f64(v) for n, v in t.items()}
     want = ref.segmented_weight_grads(ops["x"], ops["dg"], segs, G, E)
     assert_close(f64(one[0]), want, 1e-3, "dwg one-CTA")
+
+
+def draw_case(i):
+    """Seeded random case: H, F multiples of 128 (some of 256, some not),
+    1-4 segments, 16-row groups of 0-520 rows, sometimes a duplicate map."""
+    rng = np.random.default_rng(7000 + i)
+    H = int(rng.choice([256, 384, 512, 768]))
+    F = int(rng.choice([128, 256, 384, 512]))
+    E = int(rng.integers(1, 7))
+    dup = bool(rng.integers(0, 2)) and E > 1
+    G = E + (int(rng.integers(1, 3)) if dup else 0)
+    gexp = None
+    if dup:
+        gexp = list(range(E)) + [int(rng.integers(0, E)) for _ in range(G - E)]
+    n_seg = int(rng.integers(1, 5))
+    segs, base = [], int(rng.integers(0, 20))
+    for _ in range(n_seg):
+        cnt = rng.integers(0, 33, size=G) * 16
+        off = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        segs.append((off, base))
+        base += int(off[-1]) + int(rng.integers(0, 30))
+    rows = base + 3
+    gen = torch.Generator().manual_seed(8000 + i)
+    t = {n: (torch.randn((rows, w), generator=gen) * 0.5).to(torch.bfloat16)
+         for n, w in (("x", H), ("dg", F), ("du", F), ("h", F), ("dy", H))}
+    acc = bool(rng.integers(0, 2))
+    return H, F, E, G, gexp, segs, rows, t, acc
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_rows16_random_cases(i):
+    """Ten seeded random layouts through the ROWS16 entries (the two-SM
+    kernel where the gradient's rows are a multiple of 256, else the
+    one-CTA kernel), with and without ACCUMULATE onto a known dW, against
+    the oracle's segmented weight gradient."""
+    H, F, E, G, gexp, segs, rows, t, acc = draw_case(i)
+    cfg = case_cfg(H, F, E)
+    flags = moe.MOE_WGRAD_ROWS16 | (moe.MOE_WGRAD_ACCUMULATE if acc else 0)
+    init = [torch.full(s, 0.25, device="cuda")
+            for s in ((E, H, F), (E, H, F), (E, F, H))]
+    dw, st = run(cfg, segs, rows, t, flags, G, gexp,
+                 [x.clone() for x in init])
+    assert st == 0
+    ops = {n: f64(v) for n, v in t.items()}
+    for k, (got, p_, q_) in enumerate(((dw[0], "x", "dg"), (dw[1], "x", "du"),
+                                       (dw[2], "h", "dy"))):
+        want = ref.segmented_weight_grads(ops[p_], ops[q_], segs, G, E, gexp)
+        if acc:
+            want = want + 0.25
+        got = f64(got)
+        assert np.isfinite(got).all()
+        assert_close(got, want, 1e-3, f"d{q_} case {i}")
